@@ -1,0 +1,22 @@
+"""The chunk algebra used by the tensor-core build reaches the token-by-token
+definition (fp64, several chunks with a ragged tail, every variant)."""
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins as pins
+from chunkform import build_chunked
+
+
+@pytest.mark.parametrize("variant", pins.ALL)
+@pytest.mark.parametrize("chunk", [4, 7, 64])
+def test_chunk_form_equals_token_form(variant, chunk):
+    N, h_k, h_v, d_k, d_v = 37, 2, 4, 6, 5
+    k, v, q, g, beta = pins.tiny_inputs(variant, N, h_k, h_v, d_k, d_v, 900)
+    off = [0, 3, 30, N]
+    T, S = oracle.build_pairs(variant, off, 0, h_k, h_v, d_k, d_v, k, v, g, beta)
+    for i in range(3):
+        for h in range(h_v):
+            Tc, Sc = build_chunked(variant, k, v, g, beta, off[i], off[i + 1], h, h_k, h_v, chunk=chunk)
+            assert np.abs(Tc.numpy() - T[i, h]).max() < 1e-12
+            assert np.abs(Sc.numpy() - S[i, h]).max() < 1e-12 * max(1.0, np.abs(S[i, h]).max())
