@@ -1,0 +1,396 @@
+"""Benchmark of the HYPIC state-algebra hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  plan + segment build of one Qwen3.5-35B-A3B-shaped GDN layer
+    (64 segments x 1024 tokens, 16 key / 32 value heads, d = 128, bf16,
+     one batched launch, fp32 pairs into the cache pool), then
+  compose of a warm RAG prompt
+    (30 GDN layers x 32 value heads, d = 128, 100 cached segments with
+     lognormal lengths, 8 seam tokens per segment, ~12.6 GB of fp32 pairs
+     resident in HBM).
+`value` is the build throughput in tokens/s (tokens of the layer per second of
+build time); the compose's GB/s against the HBM roofline is reported beside
+it.  Inputs are seeded and synthetic and larger than L2, so no flush is
+needed between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same per-GPU work (weak scaling); times
+are the max over ranks.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "(T_C,S) build tokens/s (tensor %peak); compose GB/s vs HBM peak, GDN H=32 d=128"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------- algorithmic work
+C = 64
+
+
+def build_flops(lengths, h_v, d_k=128, d_v=128, g=2):
+    """Algorithmic FLOPs of the chunkwise build: per chunk of c tokens and
+    value head, Gram 2c^2 d_k / g + W,U solves 2c^2 (d_k + d_v) + K^T Y
+    2c d_k (d_k + d_v) + W X (skipped on the first chunk) 2c d_k (d_k + d_v)."""
+    tot = 0.0
+    for L in lengths:
+        n_full, tail = divmod(int(L), C)
+        chunks = [C] * n_full + ([tail] if tail else [])
+        for j, c in enumerate(chunks):
+            f = 2 * c * c * d_k / g + 2 * c * c * (d_k + d_v) + 2 * c * d_k * (d_k + d_v)
+            if j > 0:
+                f += 2 * c * d_k * (d_k + d_v)
+            tot += f
+    return tot * h_v
+
+
+def build_bytes(n_tokens, n_pairs, h_k, h_v, d_k=128, d_v=128, in_bytes=2):
+    """Inputs read once per key-head group (k) / value head (v, g, beta),
+    fp32 pairs written once."""
+    return (n_tokens * h_k * d_k * in_bytes + n_tokens * h_v * d_v * in_bytes + n_tokens * h_v * 8
+            + n_pairs * h_v * (d_k * d_k + d_k * d_v) * 4)
+
+
+def compose_bytes(n_layers, n_seg, w, h_k, h_v, d_k=128, d_v=128, in_bytes=2, with_init=False):
+    pairs = n_layers * n_seg * h_v * (d_k * d_k + d_k * d_v) * 4
+    seam_in = n_layers * n_seg * w * (2 * h_k * d_k * in_bytes + h_v * d_v * in_bytes + 2 * h_v * 4)
+    seam_out = n_layers * n_seg * w * h_v * d_v * 4
+    states = n_layers * h_v * d_k * d_v * 4 * (2 if with_init else 1)
+    slots = n_layers * n_seg * 4
+    return pairs + seam_in + seam_out + states + slots
+
+
+def compose_flops(n_layers, n_seg, w, h_v, d_k=128, d_v=128):
+    ts = 2.0 * d_k * d_k * d_v
+    seam = w * (6.0 * d_k * d_v)
+    return n_layers * n_seg * h_v * (ts + seam)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def setup_build(dev, seed=0):
+    import synth_inputs as si
+    W = si.workload(3, seed=seed, device=dev)
+    return W
+
+
+def setup_compose(dev, hy, seed=0, n_layers=30):
+    """Cache pool of the warm RAG prompt: pairs of 30 GDN layers built on the
+    GPU from seeded token inputs (untimed set-up), plus the seam tokens."""
+    import torch
+    import synth_inputs as si
+    W = si.workload(4, seed=seed, device=dev, n_layers=1)
+    n_seg = W.n_seg
+    n_slots = n_layers * n_seg
+    T_pool = torch.empty((n_slots, W.h_v, W.d_k, W.d_k), device=dev)
+    S_pool = torch.empty((n_slots, W.h_v, W.d_k, W.d_v), device=dev)
+    seams = []
+    for l in range(n_layers):
+        lay = W.layers[0] if l == 0 else si.make_layer(seed=seed, cfg=4, layer=l, n_tokens=W.n_tokens, h_k=W.h_k,
+                                                        h_v=W.h_v, d_k=W.d_k, d_v=W.d_v, variant="gdn",
+                                                        dtype=torch.bfloat16, device=dev)
+        slots = np.arange(n_seg, dtype=np.int32) + l * n_seg
+        hy.segment_build(lay.k, lay.v, lay.g, lay.beta, W.seg_offsets, variant="gdn", seam_w=W.seam_w,
+                         T_pool=T_pool, S_pool=S_pool, slot_of_seg=slots)
+        W.layers = [lay]
+        seams.append(si.seam_gather(W, lay))
+        del lay
+    torch.cuda.synchronize()
+    sa = {k: torch.stack([s[k] for s in seams]).contiguous() for k in ("k", "v", "q", "g", "beta")}
+    slot = torch.arange(n_slots, dtype=torch.int32, device=dev).reshape(n_layers, n_seg)
+    S_out = torch.empty((n_layers, W.h_v, W.d_k, W.d_v), device=dev)
+    seam_out = torch.empty((n_layers, n_seg, W.seam_w, W.h_v, W.d_v), device=dev)
+    return dict(W=W, n_layers=n_layers, T_pool=T_pool, S_pool=S_pool, sa=sa, slot=slot, S_out=S_out,
+                seam_out=seam_out)
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_build_sample(W, n_seg_sample, threads):
+    import oracle
+    L = W.layers[0]
+    off = W.seg_offsets
+    end = int(off[n_seg_sample])
+    sub = np.asarray(off[:n_seg_sample + 1])
+    k, v, g, b = (x[:end].cpu() for x in (L.k, L.v, L.g, L.beta))
+    t0 = time.perf_counter()
+    oracle.build_pairs("gdn", sub, W.seam_w, W.h_k, W.h_v, W.d_k, W.d_v, k, v, g, b, n_threads=threads)
+    return time.perf_counter() - t0, end
+
+
+def cpu_baseline(W3, threads, budget_s=15.0):
+    """Oracle build throughput on a bounded sample of the same layer: the
+    first few segments, all 32 value heads."""
+    n = 1
+    dt, tok = oracle_build_sample(W3, n, threads)
+    if dt < budget_s / 4:
+        n = max(1, min(W3.n_seg, int(budget_s / 2 / max(dt, 1e-3))))
+        dt, tok = oracle_build_sample(W3, n, threads)
+    return {"value": tok / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 token-by-token build of the first {n} of 64 segments (x1024 tokens, all 32 value "
+                      f"heads) of the GDN layer; {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import torch  # noqa: F401  (inputs are drawn with torch's CPU generator)
+    W3 = setup_build("cpu")
+    threads = os.cpu_count() or 1
+    n_seg = 1
+    for _ in range(args.warmup):
+        oracle_build_sample(W3, n_seg, threads)
+    times = []
+    for _ in range(args.steps):
+        dt, tok = oracle_build_sample(W3, n_seg, threads)
+        times.append(dt)
+    tot = sum(times)
+    value = args.steps * tok / tot
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "GDN layer build, Qwen3.5-35B-A3B shape (h_k=16, h_v=32, d=128), "
+                                   "sample: 1 of 64 segments x 1024 tokens per step",
+                       "global_batch": 1024, "seq_len": 1024, "parallelism": "cpu-oracle"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": "1 segment x 1024 tokens, 32 value heads per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU leg
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    import hybrid_linear_attention_chunkwise_gb300 as hy
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    hy.load()
+    peaks = _peaks()
+
+    # ---- set-up (untimed): inputs resident in HBM
+    W3 = setup_build(dev)
+    L3 = W3.layers[0]
+    T3 = torch.empty((W3.n_seg, W3.h_v, W3.d_k, W3.d_k), device=dev)
+    S3 = torch.empty((W3.n_seg, W3.h_v, W3.d_k, W3.d_v), device=dev)
+    ws3 = hy.alloc_workspace(hy.build_workspace_bytes(W3.n_seg, W3.h_k, W3.h_v, W3.d_k, W3.d_v), dev)
+    comp = setup_compose(dev, hy)
+    W4 = comp["W"]
+    stream = torch.cuda.current_stream()
+
+    def do_build():
+        hy.segment_build(L3.k, L3.v, L3.g, L3.beta, W3.seg_offsets, variant="gdn", seam_w=W3.seam_w,
+                         T_pool=T3, S_pool=S3, workspace=ws3)
+
+    def do_compose():
+        sa = comp["sa"]
+        hy.compose(comp["slot"], comp["T_pool"], comp["S_pool"], sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"],
+                   variant="gdn", S_out=comp["S_out"], seam_out=comp["seam_out"])
+
+    for _ in range(args.warmup):
+        do_build()
+        do_compose()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            do_build()
+            ev[i][1].record(stream)
+            do_compose()
+            ev[i][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    b_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
+    c_ms = float(np.mean([b.elapsed_time(c) for _, b, c in ev]))
+    if ws > 1:
+        t = torch.tensor([total_ms, b_ms, c_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, b_ms, c_ms = (float(x) for x in t.tolist())
+
+    lens3 = np.diff(W3.seg_offsets) - W3.seam_w
+    bflops = build_flops(lens3, W3.h_v)
+    bbytes = build_bytes(W3.n_tokens, W3.n_seg, W3.h_k, W3.h_v)
+    cbytes = compose_bytes(comp["n_layers"], W4.n_seg, W4.seam_w, W4.h_k, W4.h_v)
+    cflops = compose_flops(comp["n_layers"], W4.n_seg, W4.seam_w, W4.h_v)
+    tokens_per_s = ws * W3.n_tokens / (b_ms * 1e-3)
+    b_tflops = bflops / (b_ms * 1e-3) / 1e12
+    c_gbs = cbytes / (c_ms * 1e-3) / 1e9
+    roof_build = {"bound": "tensor", "achieved": b_tflops, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                  "frac": b_tflops / peaks["bf16"], "traffic": None,
+                  "kernel": "segment build", "peak_source": peaks["src"] + " bf16 dense (burst)"}
+    roof_comp = {"bound": "hbm", "achieved": c_gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                 "frac": c_gbs / peaks["hbm"], "traffic": None, "kernel": "compose",
+                 "peak_source": peaks["src"] + " HBM copy"}
+    dominant = roof_comp if c_ms >= b_ms else roof_build
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if rank == 0 or ws > 1:
+        pin = {n: getattr(L3, n).cpu().pin_memory() for n in ("k", "v", "g", "beta")}
+        dk = {n: torch.empty_like(getattr(L3, n)) for n in ("k", "v", "g", "beta")}
+        hT = torch.empty(T3.shape, dtype=torch.float32).pin_memory()
+        hS = torch.empty(S3.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in pin.values())
+        d2h = hT.numel() * 4 + hS.numel() * 4
+
+        def e2e_step():
+            for n in pin:
+                dk[n].copy_(pin[n], non_blocking=True)
+            hy.segment_build(dk["k"], dk["v"], dk["g"], dk["beta"], W3.seg_offsets, variant="gdn",
+                             seam_w=W3.seam_w, T_pool=T3, S_pool=S3, workspace=ws3)
+            hT.copy_(T3, non_blocking=True)
+            hS.copy_(S3, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / args.steps
+        e2e = {"value": ws * W3.n_tokens / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "what": "H2D of the layer's k/v/g/beta from pinned memory + build + D2H of all pairs"}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(W3, os.cpu_count() or 1)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "build: GDN layer 64x1024 tokens, h_k=16 h_v=32 d=128 bf16 (one launch); "
+                                   "compose: 30 GDN layers x 32 heads, 100 lognormal segments, w=8, "
+                                   "12.6 GB fp32 pairs in HBM",
+                       "global_batch": int(W3.n_tokens) * ws, "seq_len": 1024, "parallelism": f"dp{ws}",
+                       "l2": "inputs larger than L2 (no flush)"},
+            "build_ms": b_ms, "build_tflops": b_tflops,
+            "compose_ms": c_ms, "compose_gbs": c_gbs, "compose_tflops": cflops / (c_ms * 1e-3) / 1e12,
+            "roofline": dominant, "roofline_build": roof_build, "roofline_compose": roof_comp,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,265 @@
+"""Python binding of libhypic: the linear-attention state algebra behind
+HYPIC's position-independent caching, on GB300 (sm_103a).
+
+Argument marshalling only -- every step of the path runs in the CUDA kernels
+of ``libhypic.so`` behind the C ABI of ``include/hypic.h``.  PyTorch supplies
+device memory and streams.  There is no CPU fallback: if the library is not
+built, every call raises.
+
+Entry points (same names as the C ABI):
+  segment_build(...)   -> cache (T_C, S(C|0)) of every (segment, value head)
+  compose(...)         -> running state + seam outputs from cached pairs
+  plan_lpt(...)        -> longest-processing-time-first packing (host)
+  build_workspace_bytes(...), alloc_workspace(...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libhypic.so")
+_lock = threading.Lock()
+_lib = None
+
+GDN, DELTANET, CHANNEL_DELTA, SCALAR_DECAY, UNGATED, DIAG_GATE = range(6)
+VARIANT = {"gdn": GDN, "deltanet": DELTANET, "channel": CHANNEL_DELTA, "scalar": SCALAR_DECAY,
+           "ungated": UNGATED, "diag": DIAG_GATE}
+IN_BF16, IN_F32 = 0, 1
+FLAG_CHECK_FINITE = 1
+STATUS_TIMEOUT, STATUS_NONFINITE, STATUS_BAD_SLOT = 1, 2, 4
+OK = 0
+
+P = ctypes.c_void_p
+
+
+class BuildDesc(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_int32), ("n_seg", ctypes.c_int32),
+                ("h_k", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("seam_w", ctypes.c_int32), ("variant", ctypes.c_int32),
+                ("in_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("k", P), ("v", P), ("g", P), ("beta", P),
+                ("seg_offsets", P), ("slot_of_seg", P), ("n_slots", ctypes.c_int64),
+                ("T_pool", P), ("S_pool", P), ("workspace", P), ("workspace_bytes", ctypes.c_size_t),
+                ("status", P)]
+
+
+class ComposeDesc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_seg", ctypes.c_int32),
+                ("h_k", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("seam_w", ctypes.c_int32), ("variant", ctypes.c_int32),
+                ("in_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("slot", P), ("n_slots", ctypes.c_int64), ("T_pool", P), ("S_pool", P),
+                ("seam_k", P), ("seam_v", P), ("seam_q", P), ("seam_g", P), ("seam_beta", P),
+                ("S_init", P), ("S_out", P), ("seam_out", P),
+                ("workspace", P), ("workspace_bytes", ctypes.c_size_t), ("status", P)]
+
+
+SYMBOLS = ("hypic_segment_build", "hypic_build_workspace_bytes", "hypic_compose",
+           "hypic_compose_workspace_bytes", "hypic_plan_lpt", "hypic_status_from_word",
+           "hypic_status_string", "hypic_version")
+
+
+class HypicError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libhypic.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"libhypic.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.hypic_segment_build.argtypes = [ctypes.POINTER(BuildDesc), P]
+            lib.hypic_segment_build.restype = ctypes.c_int
+            lib.hypic_build_workspace_bytes.argtypes = [ctypes.POINTER(BuildDesc)]
+            lib.hypic_build_workspace_bytes.restype = ctypes.c_size_t
+            lib.hypic_compose.argtypes = [ctypes.POINTER(ComposeDesc), P]
+            lib.hypic_compose.restype = ctypes.c_int
+            lib.hypic_compose_workspace_bytes.argtypes = [ctypes.POINTER(ComposeDesc)]
+            lib.hypic_compose_workspace_bytes.restype = ctypes.c_size_t
+            lib.hypic_plan_lpt.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P]
+            lib.hypic_plan_lpt.restype = ctypes.c_int
+            lib.hypic_status_from_word.argtypes = [ctypes.c_uint32]
+            lib.hypic_status_from_word.restype = ctypes.c_int
+            lib.hypic_status_string.argtypes = [ctypes.c_int]
+            lib.hypic_status_string.restype = ctypes.c_char_p
+            lib.hypic_version.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().hypic_status_string(int(code)).decode()
+
+
+def status_from_word(word: int) -> int:
+    return load().hypic_status_from_word(int(word) & 0xFFFFFFFF)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _in_dtype(t):
+    if t.dtype == torch.bfloat16:
+        return IN_BF16
+    if t.dtype == torch.float32:
+        return IN_F32
+    raise ValueError(f"unsupported input dtype {t.dtype}")
+
+
+def pool_T_shape(variant: str, n_slots: int, h_v: int, d_k: int):
+    v = VARIANT[variant]
+    if v in (GDN, DELTANET, CHANNEL_DELTA):
+        return (n_slots, h_v, d_k, d_k)
+    if v == DIAG_GATE:
+        return (n_slots, h_v, d_k)
+    return (n_slots, h_v)
+
+
+def _check(t, name, dtype=None, ndim=None):
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def _build_desc(k, v, g, beta, seg_offsets, variant, seam_w, T_pool, S_pool, slot_of_seg, workspace,
+                status, flags):
+    _check(k, "k", ndim=3)
+    _check(v, "v", dtype=k.dtype, ndim=3)
+    _check(g, "g", dtype=torch.float32)
+    _check(beta, "beta", dtype=torch.float32)
+    _check(T_pool, "T_pool", dtype=torch.float32)
+    _check(S_pool, "S_pool", dtype=torch.float32, ndim=4)
+    off = np.ascontiguousarray(np.asarray(seg_offsets, dtype=np.int64))
+    slots = None if slot_of_seg is None else np.ascontiguousarray(np.asarray(slot_of_seg, dtype=np.int32))
+    d = BuildDesc()
+    d.n_tokens, d.h_k, d.d_k = k.shape[0], k.shape[1], k.shape[2]
+    d.h_v, d.d_v = v.shape[1], v.shape[2]
+    d.n_seg = len(off) - 1
+    d.seam_w = int(seam_w)
+    d.variant = VARIANT[variant]
+    d.in_dtype = _in_dtype(k)
+    d.flags = int(flags)
+    d.k, d.v, d.g, d.beta = _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
+    d.seg_offsets = off.ctypes.data_as(P)
+    d.slot_of_seg = None if slots is None else slots.ctypes.data_as(P)
+    d.n_slots = S_pool.shape[0]
+    d.T_pool, d.S_pool = _ptr(T_pool), _ptr(S_pool)
+    d.workspace = _ptr(workspace)
+    d.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    d.status = _ptr(status)
+    return d, (off, slots)
+
+
+def build_workspace_bytes(n_seg: int, h_k: int, h_v: int, d_k: int, d_v: int, variant: str = "gdn",
+                          dtype=torch.bfloat16, seam_w: int = 0) -> int:
+    d = BuildDesc()
+    d.n_seg, d.h_k, d.h_v, d.d_k, d.d_v = n_seg, h_k, h_v, d_k, d_v
+    d.variant = VARIANT[variant]
+    d.in_dtype = IN_BF16 if dtype == torch.bfloat16 else IN_F32
+    d.seam_w = seam_w
+    return int(load().hypic_build_workspace_bytes(ctypes.byref(d)))
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A 256-byte aligned device buffer of at least `nbytes` bytes."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def segment_build(k, v, g, beta, seg_offsets, *, variant: str, seam_w: int, T_pool, S_pool,
+                  slot_of_seg=None, workspace=None, status=None, flags: int = 0, stream=None):
+    """hypic_segment_build on torch tensors.  k [N,h_k,d_k], v [N,h_v,d_v]
+    (bf16 or fp32), g / beta fp32 as in hypic.h, seg_offsets host int64
+    [n_seg+1].  Writes T_pool / S_pool slots in place."""
+    lib = load()
+    d, keep = _build_desc(k, v, g, beta, seg_offsets, variant, seam_w, T_pool, S_pool, slot_of_seg,
+                          workspace, status, flags)
+    if workspace is None:
+        nb = int(lib.hypic_build_workspace_bytes(ctypes.byref(d)))
+        workspace = alloc_workspace(nb, k.device)
+        d.workspace = _ptr(workspace)
+        d.workspace_bytes = workspace.numel()
+    rc = lib.hypic_segment_build(ctypes.byref(d), _stream(stream))
+    del keep
+    if rc != OK:
+        raise HypicError(rc, "hypic_segment_build")
+    return workspace
+
+
+def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str,
+            S_out, seam_out=None, S_init=None, h_k=None, d_k=None, d_v=None, status=None,
+            flags: int = 0, stream=None):
+    """hypic_compose on torch tensors.  slot int32 [L, n_seg] (device);
+    seam arrays [L, n_seg, w, heads, d]; S_out [L, h_v, d_k, d_v]."""
+    lib = load()
+    _check(slot, "slot", dtype=torch.int32, ndim=2)
+    _check(S_out, "S_out", dtype=torch.float32, ndim=4)
+    for name, t in (("seam_k", seam_k), ("seam_v", seam_v), ("seam_q", seam_q)):
+        _check(t, name, ndim=5)
+    d = ComposeDesc()
+    d.n_layers, d.n_seg = slot.shape
+    _, d.h_v, d.d_k, d.d_v = S_out.shape
+    w = 0 if seam_k is None else seam_k.shape[2]
+    d.seam_w = w
+    d.h_k = seam_k.shape[3] if seam_k is not None else (h_k if h_k is not None else d.h_v)
+    d.variant = VARIANT[variant]
+    ref = seam_k if seam_k is not None else None
+    d.in_dtype = _in_dtype(ref) if ref is not None else IN_BF16
+    d.flags = int(flags)
+    d.slot = _ptr(slot)
+    d.n_slots = S_pool.shape[0]
+    d.T_pool, d.S_pool = _ptr(T_pool), _ptr(S_pool)
+    d.seam_k, d.seam_v, d.seam_q = _ptr(seam_k), _ptr(seam_v), _ptr(seam_q)
+    d.seam_g, d.seam_beta = _ptr(seam_g), _ptr(seam_beta)
+    d.S_init, d.S_out, d.seam_out = _ptr(S_init), _ptr(S_out), _ptr(seam_out)
+    nb = int(lib.hypic_compose_workspace_bytes(ctypes.byref(d)))
+    ws = alloc_workspace(nb, S_out.device) if nb else None
+    d.workspace = _ptr(ws)
+    d.workspace_bytes = 0 if ws is None else ws.numel()
+    d.status = _ptr(status)
+    rc = lib.hypic_compose(ctypes.byref(d), _stream(stream))
+    if rc != OK:
+        raise HypicError(rc, "hypic_compose")
+
+
+def plan_lpt(costs, n_workers: int):
+    """Host LPT packing: returns (order, worker_of_item, makespan)."""
+    lib = load()
+    c = np.ascontiguousarray(np.asarray(costs, dtype=np.int64))
+    n = len(c)
+    order = np.zeros(n, dtype=np.int32)
+    worker = np.zeros(n, dtype=np.int32)
+    mk = ctypes.c_int64(0)
+    rc = lib.hypic_plan_lpt(c.ctypes.data_as(P), n, int(n_workers), order.ctypes.data_as(P),
+                            worker.ctypes.data_as(P), ctypes.byref(mk))
+    if rc != OK:
+        raise HypicError(rc, "hypic_plan_lpt")
+    return order, worker, int(mk.value)

@@ -1,0 +1,251 @@
+// api.cpp -- host side of libhypic: descriptor validation, the LPT work plan,
+// workspace sizing and kernel launches behind the C ABI of hypic.h.
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+#include <queue>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+using namespace hypic;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int in_size(int dt) { return dt == HYPIC_IN_BF16 ? 2 : 4; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+int check_common_shapes(int h_k, int h_v, int d_k, int d_v, int seam_w, int variant, int in_dtype) {
+  if (h_k < 1 || h_v < 1 || d_k < 1 || d_v < 1 || seam_w < 0) return HYPIC_ERR_INVALID_ARG;
+  if (h_v % h_k != 0) return HYPIC_ERR_INVALID_ARG;
+  if (variant < HYPIC_GDN || variant > HYPIC_DIAG_GATE) return HYPIC_ERR_INVALID_ARG;
+  if (in_dtype != HYPIC_IN_BF16 && in_dtype != HYPIC_IN_F32) return HYPIC_ERR_INVALID_ARG;
+  if (d_k > 128 || d_v > 128) return HYPIC_ERR_UNSUPPORTED;
+  return HYPIC_OK;
+}
+
+int64_t n_build_items(const hypic_build_desc *d) { return (int64_t)d->n_seg * d->h_v; }
+
+size_t plan_bytes(int64_t n_items) { return round_up(sizeof(PlanHeader) + n_items * sizeof(BuildItem), kAlign); }
+
+}  // namespace
+
+extern "C" {
+
+int hypic_version(void) { return 100; }
+
+const char *hypic_status_string(int s) {
+  switch (s) {
+    case HYPIC_OK: return "ok";
+    case HYPIC_ERR_INVALID_ARG: return "invalid argument";
+    case HYPIC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case HYPIC_ERR_WORKSPACE: return "workspace missing or too small";
+    case HYPIC_ERR_CUDA: return "CUDA error";
+    case HYPIC_ERR_TIMEOUT: return "device wait timed out";
+    case HYPIC_ERR_NONFINITE: return "non-finite output";
+    case HYPIC_ERR_BAD_SLOT: return "pool slot index out of range";
+    default: return "unknown status";
+  }
+}
+
+int hypic_status_from_word(uint32_t w) {
+  if (w & HYPIC_STATUS_TIMEOUT) return HYPIC_ERR_TIMEOUT;
+  if (w & HYPIC_STATUS_BAD_SLOT) return HYPIC_ERR_BAD_SLOT;
+  if (w & HYPIC_STATUS_NONFINITE) return HYPIC_ERR_NONFINITE;
+  return HYPIC_OK;
+}
+
+int hypic_plan_lpt(const int64_t *costs, int32_t n_items, int32_t n_workers, int32_t *order_out,
+                   int32_t *worker_out, int64_t *makespan_out) {
+  if (n_items < 0 || n_workers < 1 || (n_items > 0 && (!costs || !order_out))) return HYPIC_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n_items; i++)
+    if (costs[i] < 0) return HYPIC_ERR_INVALID_ARG;
+  std::vector<int32_t> order(n_items);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return costs[a] > costs[b]; });
+  // least-loaded worker first; ties to the lower worker index
+  using W = std::pair<int64_t, int32_t>;
+  std::priority_queue<W, std::vector<W>, std::greater<W>> heap;
+  for (int32_t w = 0; w < n_workers; w++) heap.push({0, w});
+  int64_t makespan = 0;
+  for (int32_t r = 0; r < n_items; r++) {
+    const int32_t it = order[r];
+    W top = heap.top();
+    heap.pop();
+    top.first += costs[it];
+    makespan = std::max(makespan, top.first);
+    if (worker_out) worker_out[it] = top.second;
+    heap.push(top);
+    order_out[r] = it;
+  }
+  if (makespan_out) *makespan_out = makespan;
+  return HYPIC_OK;
+}
+
+size_t hypic_build_workspace_bytes(const hypic_build_desc *d) {
+  if (!d || d->n_seg < 0 || d->h_v < 1) return 0;
+  return plan_bytes(n_build_items(d));
+}
+
+int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  int st = check_common_shapes(d->h_k, d->h_v, d->d_k, d->d_v, d->seam_w, d->variant, d->in_dtype);
+  if (st) return st;
+  if (d->n_tokens < 0 || d->n_seg < 0 || d->n_slots < 0) return HYPIC_ERR_INVALID_ARG;
+  if (!d->seg_offsets) return HYPIC_ERR_INVALID_ARG;
+  if (d->seg_offsets[0] != 0 || d->seg_offsets[d->n_seg] != d->n_tokens) return HYPIC_ERR_INVALID_ARG;
+  for (int i = 0; i < d->n_seg; i++)
+    if (d->seg_offsets[i + 1] < d->seg_offsets[i]) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_seg == 0) return HYPIC_OK;
+  const int esz = in_size(d->in_dtype);
+  if (d->n_tokens > 0) {
+    if (!d->k || !d->v || !aligned(d->k, esz) || !aligned(d->v, esz)) return HYPIC_ERR_INVALID_ARG;
+  }
+  const bool delta = is_delta(d->variant);
+  const bool needs_g = d->variant == HYPIC_GDN || d->variant == HYPIC_CHANNEL_DELTA ||
+                       d->variant == HYPIC_DIAG_GATE || d->variant == HYPIC_SCALAR_DECAY;
+  if (needs_g && (!d->g || !aligned(d->g, 4))) return HYPIC_ERR_INVALID_ARG;
+  if (delta && d->n_tokens > 0 && (!d->beta || !aligned(d->beta, 4))) return HYPIC_ERR_INVALID_ARG;
+  if (!d->T_pool || !d->S_pool || !aligned(d->T_pool, 4) || !aligned(d->S_pool, 4)) return HYPIC_ERR_INVALID_ARG;
+  // slots: in range and distinct (two items writing one slot would race)
+  std::vector<int32_t> slots(d->n_seg);
+  for (int i = 0; i < d->n_seg; i++) slots[i] = d->slot_of_seg ? d->slot_of_seg[i] : i;
+  {
+    std::vector<int32_t> s2(slots);
+    std::sort(s2.begin(), s2.end());
+    for (int i = 0; i < d->n_seg; i++) {
+      if (s2[i] < 0 || s2[i] >= d->n_slots) return HYPIC_ERR_INVALID_ARG;
+      if (i && s2[i] == s2[i - 1]) return HYPIC_ERR_INVALID_ARG;
+    }
+  }
+  const int64_t n_items = n_build_items(d);
+  if (n_items > INT32_MAX / 2) return HYPIC_ERR_UNSUPPORTED;
+  const size_t need = plan_bytes(n_items);
+  if (!d->workspace || d->workspace_bytes < need || !aligned(d->workspace, kAlign)) return HYPIC_ERR_WORKSPACE;
+
+  // ---- LPT plan over (segment, value head) items; cost = body length ----
+  std::vector<int64_t> cost(n_items);
+  for (int64_t it = 0; it < n_items; it++) {
+    const int i = (int)(it / d->h_v);
+    const int64_t s = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
+    cost[it] = d->seg_offsets[i + 1] - s;
+  }
+  std::vector<int32_t> order(n_items);
+  st = hypic_plan_lpt(cost.data(), (int32_t)n_items, sm_count(), order.data(), nullptr, nullptr);
+  if (st) return st;
+  std::vector<unsigned char> host(need, 0);
+  PlanHeader *hdr = reinterpret_cast<PlanHeader *>(host.data());
+  hdr->ticket = 0;
+  hdr->n_items = (int32_t)n_items;
+  BuildItem *items = reinterpret_cast<BuildItem *>(hdr + 1);
+  for (int64_t r = 0; r < n_items; r++) {
+    const int64_t it = order[r];
+    const int i = (int)(it / d->h_v);
+    BuildItem b;
+    b.seg = i;
+    b.head = (int32_t)(it % d->h_v);
+    b.slot = slots[i];
+    b.part = 0;
+    b.start = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
+    b.end = d->seg_offsets[i + 1];
+    items[r] = b;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // pageable source: the call returns once the bytes are staged, so `host`
+  // may be released when it goes out of scope
+  if (cudaMemcpyAsync(d->workspace, host.data(), need, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
+
+  BuildParams p{};
+  p.h_k = d->h_k;
+  p.h_v = d->h_v;
+  p.d_k = d->d_k;
+  p.d_v = d->d_v;
+  p.variant = d->variant;
+  p.in_dtype = d->in_dtype;
+  p.flags = d->flags;
+  p.n_slots = d->n_slots;
+  p.k = d->k;
+  p.v = d->v;
+  p.g = d->g;
+  p.beta = d->beta;
+  p.T_pool = d->T_pool;
+  p.S_pool = d->S_pool;
+  p.plan = reinterpret_cast<PlanHeader *>(d->workspace);
+  p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
+  p.status = d->status;
+  if (launch_build_token(p, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
+  return HYPIC_OK;
+}
+
+size_t hypic_compose_workspace_bytes(const hypic_compose_desc *d) {
+  (void)d;
+  return 0;
+}
+
+int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  int st = check_common_shapes(d->h_k, d->h_v, d->d_k, d->d_v, d->seam_w, d->variant, d->in_dtype);
+  if (st) return st;
+  if (d->n_layers < 0 || d->n_seg < 0 || d->n_slots < 0) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_layers == 0) return HYPIC_OK;
+  if (!d->S_out || !aligned(d->S_out, 4)) return HYPIC_ERR_INVALID_ARG;
+  if (d->S_init && !aligned(d->S_init, 4)) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_seg > 0) {
+    if (!d->slot || !aligned(d->slot, 4) || !d->T_pool || !d->S_pool) return HYPIC_ERR_INVALID_ARG;
+    if (!aligned(d->T_pool, 4) || !aligned(d->S_pool, 4)) return HYPIC_ERR_INVALID_ARG;
+  }
+  const bool delta = is_delta(d->variant);
+  const int esz = in_size(d->in_dtype);
+  if (d->seam_w > 0 && d->n_seg > 0) {
+    if (!d->seam_k || !d->seam_v || !d->seam_q || !d->seam_out) return HYPIC_ERR_INVALID_ARG;
+    if (!aligned(d->seam_k, esz) || !aligned(d->seam_v, esz) || !aligned(d->seam_q, esz)) return HYPIC_ERR_INVALID_ARG;
+    if (!aligned(d->seam_out, 4)) return HYPIC_ERR_INVALID_ARG;
+    if (delta && !d->seam_beta) return HYPIC_ERR_INVALID_ARG;
+    if ((d->variant == HYPIC_GDN || is_vector_gate(d->variant)) && !d->seam_g) return HYPIC_ERR_INVALID_ARG;
+  }
+  if (d->variant == HYPIC_SCALAR_DECAY && !d->seam_g) return HYPIC_ERR_INVALID_ARG;
+
+  ComposeParams p{};
+  p.n_layers = d->n_layers;
+  p.n_seg = d->n_seg;
+  p.h_k = d->h_k;
+  p.h_v = d->h_v;
+  p.d_k = d->d_k;
+  p.d_v = d->d_v;
+  p.seam_w = d->seam_w;
+  p.variant = d->variant;
+  p.in_dtype = d->in_dtype;
+  p.flags = d->flags;
+  p.slot = d->slot;
+  p.n_slots = d->n_slots;
+  p.T_pool = d->T_pool;
+  p.S_pool = d->S_pool;
+  p.seam_k = d->seam_k;
+  p.seam_v = d->seam_v;
+  p.seam_q = d->seam_q;
+  p.seam_g = d->seam_g;
+  p.seam_beta = d->seam_beta;
+  p.S_init = d->S_init;
+  p.S_out = d->S_out;
+  p.seam_out = d->seam_out;
+  p.status = d->status;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_compose_simt(p, s) != cudaSuccess) return HYPIC_ERR_CUDA;
+  return HYPIC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,225 @@
+// build_token.cu -- fp32 token-recurrence segment build (all six variants).
+//
+// The fp32-input path of hypic_segment_build: for each (segment, value head)
+// item it applies the per-token transitions in order,
+//     T <- T_t T,   S <- T_t S + U_t,
+// which is the definition of the cached pair (T_C, S(C|0)) on the HYPIC news
+// pages (nav.aitube.vip §2.1: T_C is the product of all token transition
+// matrices of the segment; S(C|0) the final state from zero).
+//
+// Layout on chip: the augmented block X = [T | S] (d_k x (d_k + d_v)) is held
+// one column per thread, in registers (DK fp32 values per thread), so the
+// rank-1 erase  X <- a (X - b k (k^T X)) + [0 | b k v^T]  needs only a local
+// dot product per column: no cross-thread reduction.  Token inputs are staged
+// through shared memory in tiles of TB tokens (broadcast reads).  Variants
+// without an erase (scalar decay, ungated, diagonal gate) carry no T columns:
+// their T is a product of gates, formed from fp64 sums of the log-gates.
+//
+// Items are pulled from the LPT-ordered plan by an atomic ticket (dynamic
+// list scheduling in LPT order); an item's result does not depend on which
+// block computes it.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace hypic {
+
+namespace {
+
+constexpr int TB = 16;  // tokens per shared-memory tile
+
+template <int DK>
+struct TokSmem {
+  float k[TB][DK];    // k (zero beyond d_k / past the end)
+  float kd[TB][DK];   // vector gates: k * a (the erase acts after Diag(a)); else unused
+  float a[TB][DK];    // vector gates: a = exp(g); else unused
+  float lg[TB][DK];   // vector gates: g (for the log-sum of diagonal T)
+  float v[TB][128];
+  float gs[TB];       // scalar gate a_t (GDN) / 1
+  float b[TB];        // beta_t (0 on padding tokens)
+  int item;
+};
+
+template <int DK>
+__global__ void __launch_bounds__(256) build_token_kernel(BuildParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TokSmem<DK> &sm = *reinterpret_cast<TokSmem<DK> *>(smem_raw);
+  const int tid = threadIdx.x;
+  const bool delta = is_delta(p.variant);
+  const bool vec = is_vector_gate(p.variant);
+  const int d_k = p.d_k, d_v = p.d_v;
+  const int n_t_thr = delta ? DK : 0;              // threads [0, DK) own T columns
+  const bool is_T = tid < n_t_thr;
+  const int col = is_T ? tid : tid - n_t_thr;      // column within T or S
+  const bool active = is_T ? (col < d_k) : (col < d_v);
+  const int n_items = p.plan->n_items;
+
+  for (;;) {
+    if (tid == 0) sm.item = atomicAdd(&p.plan->ticket, 1);
+    __syncthreads();
+    const int idx = sm.item;
+    __syncthreads();
+    if (idx >= n_items) break;
+    const BuildItem it = p.items[idx];
+    const int h = it.head;
+    const int kh = (int)(((int64_t)h * p.h_k) / p.h_v);
+
+    float X[DK];
+#pragma unroll
+    for (int i = 0; i < DK; i++) X[i] = (is_T && i == col) ? 1.f : 0.f;
+    double logsum = 0.0;  // non-delta variants: sum of log-gates of channel `tid`
+
+    float gconst = 1.f;
+    if (p.variant == HYPIC_SCALAR_DECAY) gconst = expf(p.g[h]);
+
+    for (int64_t t0 = it.start; t0 < it.end; t0 += TB) {
+      const int nt = (int)((it.end - t0) < TB ? (it.end - t0) : TB);
+      for (int e = tid; e < TB * DK; e += blockDim.x) {
+        const int t = e / DK, i = e % DK;
+        float kv = 0.f, a = 1.f, lg = 0.f;
+        if (t < nt && i < d_k) {
+          kv = load_in(p.k, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype);
+          if (vec) {
+            lg = p.g[((t0 + t) * p.h_v + h) * (int64_t)d_k + i];
+            a = expf(lg);
+          }
+        }
+        sm.k[t][i] = kv;
+        if (vec) {
+          sm.a[t][i] = a;
+          sm.kd[t][i] = kv * a;
+          sm.lg[t][i] = lg;
+        }
+      }
+      for (int e = tid; e < TB * 128; e += blockDim.x) {
+        const int t = e / 128, j = e % 128;
+        sm.v[t][j] = (t < nt && j < d_v) ? load_in(p.v, ((t0 + t) * p.h_v + h) * (int64_t)d_v + j, p.in_dtype) : 0.f;
+      }
+      for (int t = tid; t < TB; t += blockDim.x) {
+        float gs = 1.f, b = 0.f;
+        if (t < nt) {
+          if (p.variant == HYPIC_GDN) gs = expf(p.g[(t0 + t) * p.h_v + h]);
+          else if (p.variant == HYPIC_SCALAR_DECAY) gs = gconst;
+          if (delta) b = p.beta[(t0 + t) * p.h_v + h];
+        }
+        sm.gs[t] = gs;
+        sm.b[t] = b;
+      }
+      __syncthreads();
+      if (!delta && vec && tid < d_k) {
+        for (int t = 0; t < nt; t++) logsum += (double)sm.lg[t][tid];
+      }
+      if (active) {
+        for (int t = 0; t < nt; t++) {
+          const float b = sm.b[t], gs = sm.gs[t];
+          const float vj = is_T ? 0.f : sm.v[t][col];
+          if (delta) {
+            const float *kd = vec ? sm.kd[t] : sm.k[t];
+            float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+            for (int i = 0; i < DK; i += 4) {
+              x0 = fmaf(kd[i + 0], X[i + 0], x0);
+              x1 = fmaf(kd[i + 1], X[i + 1], x1);
+              x2 = fmaf(kd[i + 2], X[i + 2], x2);
+              x3 = fmaf(kd[i + 3], X[i + 3], x3);
+            }
+            const float x = (x0 + x1) + (x2 + x3);
+            // X <- s (X - b k x) + b k v  with s = a_t (GDN), 1, or Diag(a) applied first
+            const float c = vec ? (b * vj - b * x) : (gs * (-b * x) + b * vj);
+            const float *kk = sm.k[t];
+            if (vec) {
+              const float *aa = sm.a[t];
+#pragma unroll
+              for (int i = 0; i < DK; i++) X[i] = fmaf(aa[i], X[i], kk[i] * c);
+            } else {
+#pragma unroll
+              for (int i = 0; i < DK; i++) X[i] = fmaf(gs, X[i], kk[i] * c);
+            }
+          } else {
+            const float *kk = sm.k[t];
+            if (vec) {
+              const float *aa = sm.a[t];
+#pragma unroll
+              for (int i = 0; i < DK; i++) X[i] = fmaf(aa[i], X[i], kk[i] * vj);
+            } else {
+#pragma unroll
+              for (int i = 0; i < DK; i++) X[i] = fmaf(gs, X[i], kk[i] * vj);
+            }
+          }
+        }
+      }
+      __syncthreads();
+    }
+
+    // epilogue: write the pair into the pool slot
+    const int64_t sh = (int64_t)it.slot * p.h_v + h;
+    bool bad = false;
+    if (active) {
+      if (is_T) {
+        float *T = p.T_pool + sh * d_k * d_k;
+#pragma unroll
+        for (int i = 0; i < DK; i++)
+          if (i < d_k) {
+            T[(int64_t)i * d_k + col] = X[i];
+            bad |= !finite_f(X[i]);
+          }
+      } else {
+        float *S = p.S_pool + sh * d_k * d_v;
+#pragma unroll
+        for (int i = 0; i < DK; i++)
+          if (i < d_k) {
+            S[(int64_t)i * d_v + col] = X[i];
+            bad |= !finite_f(X[i]);
+          }
+      }
+    }
+    if (!delta) {
+      const int64_t L = it.end - it.start;
+      if (p.variant == HYPIC_DIAG_GATE) {
+        if (tid < d_k) {
+          float tv = (float)exp(logsum);
+          p.T_pool[sh * d_k + tid] = tv;
+          bad |= !finite_f(tv);
+        }
+      } else if (tid == 0) {
+        float tv = (p.variant == HYPIC_SCALAR_DECAY) ? (float)exp((double)L * (double)p.g[h]) : 1.f;
+        p.T_pool[sh] = tv;
+        bad |= !finite_f(tv);
+      }
+    }
+    if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
+  }
+}
+
+template <int DK>
+cudaError_t launch_dk(const BuildParams &p, int n_items, int n_sm, cudaStream_t s) {
+  const bool delta = is_delta(p.variant);
+  const int dvp = ((p.d_v + 31) / 32) * 32;
+  int threads = (delta ? DK : 0) + dvp;
+  const int dkp = ((p.d_k + 31) / 32) * 32;
+  if (threads < dkp) threads = dkp;  // diagonal gates: one thread per channel for the log-sum
+  threads = ((threads + 31) / 32) * 32;
+  const size_t smem = sizeof(TokSmem<DK>);
+  cudaError_t e = cudaFuncSetAttribute(build_token_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_token_kernel<DK>, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  int grid = n_sm * per_sm;
+  if (grid > n_items) grid = n_items;
+  if (grid < 1) return cudaSuccess;
+  build_token_kernel<DK><<<grid, threads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_build_token(const BuildParams &p, int n_items, int n_sm, cudaStream_t s) {
+  if (p.d_k <= 16) return launch_dk<16>(p, n_items, n_sm, s);
+  if (p.d_k <= 32) return launch_dk<32>(p, n_items, n_sm, s);
+  if (p.d_k <= 64) return launch_dk<64>(p, n_items, n_sm, s);
+  return launch_dk<128>(p, n_items, n_sm, s);
+}
+
+}  // namespace hypic

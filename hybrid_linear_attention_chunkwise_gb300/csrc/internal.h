@@ -1,0 +1,67 @@
+// internal.h -- types shared by the host library and the CUDA kernels of
+// libhypic (not part of the public ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "hypic.h"
+
+namespace hypic {
+
+// One unit of build work: one (segment, value head) pair, or one half of it
+// for kernels that split the augmented block [T | S] by columns.
+struct BuildItem {
+  int32_t seg;
+  int32_t head;
+  int32_t slot;
+  int32_t part;   // kernel-specific sub-item (0 when unused)
+  int64_t start;  // first body token (after the seam window)
+  int64_t end;    // one past the last token
+};
+
+// Device-visible build plan header, followed by n_items BuildItem records in
+// LPT order.  `ticket` is the dynamic work counter (zeroed by the host copy).
+struct PlanHeader {
+  int32_t ticket;
+  int32_t n_items;
+  int32_t pad[14];  // keeps the item array 64-byte aligned
+};
+static_assert(sizeof(PlanHeader) == 64, "plan header size");
+
+struct BuildParams {
+  int32_t h_k, h_v, d_k, d_v;
+  int32_t variant, in_dtype;
+  uint32_t flags;
+  int64_t n_slots;
+  const void *k, *v;
+  const float *g, *beta;
+  float *T_pool, *S_pool;
+  PlanHeader *plan;         // device copy of the plan
+  const BuildItem *items;   // = (BuildItem*)(plan + 1)
+  uint32_t *status;
+};
+
+struct ComposeParams {
+  int32_t n_layers, n_seg, h_k, h_v, d_k, d_v, seam_w;
+  int32_t variant, in_dtype;
+  uint32_t flags;
+  const int32_t *slot;
+  int64_t n_slots;
+  const float *T_pool, *S_pool;
+  const void *seam_k, *seam_v, *seam_q;
+  const float *seam_g, *seam_beta;
+  const float *S_init;
+  float *S_out, *seam_out;
+  uint32_t *status;
+};
+
+__host__ __device__ inline bool is_delta(int v) { return v == HYPIC_GDN || v == HYPIC_DELTANET || v == HYPIC_CHANNEL_DELTA; }
+__host__ __device__ inline bool is_dense_T(int v) { return is_delta(v); }
+__host__ __device__ inline bool is_vector_gate(int v) { return v == HYPIC_CHANNEL_DELTA || v == HYPIC_DIAG_GATE; }
+
+// Launchers (each returns a cudaError_t from the launch).
+cudaError_t launch_build_token(const BuildParams &p, int n_items, int n_sm, cudaStream_t s);
+cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s);
+
+}  // namespace hypic

@@ -1,0 +1,196 @@
+/*
+ * hypic.h -- C ABI of the GB300 (sm_103a) library for the linear-attention
+ * state algebra behind HYPIC's position-independent caching.
+ *
+ * Method (HYPIC news pages: nav.aitube.vip "首 token 延迟降 3.25 倍！...HYPIC..."
+ * §2.1 linear layers and §2.2 seam window; xix.ai Spanish/Japanese pages,
+ * paragraphs on linear layers and on full-attention seams):
+ *   - for a segment C and a head, the segment-cumulative transition operator
+ *     T_C is the product of every token transition matrix in the segment, and
+ *     S(C|0) is the segment's final state from a zero initial state; the pair
+ *     depends only on the segment's own tokens, so it is cached once;
+ *   - at reuse the exact state under any prefix follows by left-multiplying
+ *     with T_C and adding: S(C1·C2) = T(C2)·S(C1) + S(C2);
+ *   - the first w tokens of each segment (the seam window, w = 8 by default)
+ *     are not cached: at reuse the linear layer advances the running state
+ *     through them token by token and emits each seam token's output.
+ *
+ * Per-token transitions (state S in R^{d_k x d_v}, S_t = T_t S_{t-1} + U_t,
+ * output o_t = S_t^T q_t with the post-update state):
+ *   HYPIC_GDN            T_t = a_t (I - b_t k_t k_t^T),          U_t = b_t k_t v_t^T
+ *   HYPIC_DELTANET       T_t = I - b_t k_t k_t^T,                U_t = b_t k_t v_t^T
+ *   HYPIC_CHANNEL_DELTA  T_t = (I - b_t k_t k_t^T) Diag(a_t),    U_t = b_t k_t v_t^T
+ *   HYPIC_SCALAR_DECAY   T_t = gamma_h I (RetNet),               U_t = k_t v_t^T
+ *   HYPIC_UNGATED        T_t = I,                                U_t = k_t v_t^T
+ *   HYPIC_DIAG_GATE      T_t = Diag(a_t) (GLA-type),             U_t = k_t v_t^T
+ * Gates are passed as fp32 log-gates g (a = exp(g), gamma = exp(g)).
+ * Value head h reads key head floor(h * h_k / h_v) (grouped heads).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked [dev] are caller-owned device memory, [host] are host
+ *     memory read during the call only.  The library allocates no device
+ *     memory and keeps no global mutable state; calls are thread-safe.
+ *   - Work is enqueued asynchronously on the caller's stream.  Host-side
+ *     validation runs first: an invalid descriptor returns an error code and
+ *     launches nothing.  A failed launch returns HYPIC_ERR_CUDA.
+ *   - Conditions found on the device (bounded wait expired, slot index out of
+ *     range, non-finite output under HYPIC_FLAG_CHECK_FINITE) set bits of the
+ *     optional device status word; read it after synchronising the stream and
+ *     decode it with hypic_status_from_word().  The library never traps.
+ *   - Results are deterministic: no atomics in any reduction; the order in
+ *     which work is scheduled never changes a result bit.
+ *   - Row-major layouts throughout; all state, transition and pair tensors
+ *     are fp32.
+ */
+#ifndef HYPIC_H_
+#define HYPIC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *hypic_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  HYPIC_OK = 0,
+  HYPIC_ERR_INVALID_ARG = 1, /* bad descriptor: null/misaligned pointer, bad size, offsets not monotone */
+  HYPIC_ERR_UNSUPPORTED = 2, /* valid but not supported (head size > 128, variant/dtype combination) */
+  HYPIC_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the *_workspace_bytes query */
+  HYPIC_ERR_CUDA = 4,        /* a CUDA call failed (launch, copy, attribute) */
+  HYPIC_ERR_TIMEOUT = 5,     /* device: a bounded wait ran out (reported through the status word) */
+  HYPIC_ERR_NONFINITE = 6,   /* device: non-finite output seen (HYPIC_FLAG_CHECK_FINITE) */
+  HYPIC_ERR_BAD_SLOT = 7     /* device: a pool slot index was out of range; that chain was skipped */
+} hypic_status;
+
+typedef enum {
+  HYPIC_GDN = 0,
+  HYPIC_DELTANET = 1,
+  HYPIC_CHANNEL_DELTA = 2,
+  HYPIC_SCALAR_DECAY = 3,
+  HYPIC_UNGATED = 4,
+  HYPIC_DIAG_GATE = 5
+} hypic_variant;
+
+typedef enum {
+  HYPIC_IN_BF16 = 0, /* k/v/q bf16: tensor-core paths, max relative error 5e-3 per head */
+  HYPIC_IN_F32 = 1   /* k/v/q fp32: fp32 paths, max relative error 1e-5 per head */
+} hypic_in_dtype;
+
+/* flags */
+#define HYPIC_FLAG_CHECK_FINITE 1u /* scan outputs for NaN/Inf and report through the status word */
+
+/* Device status word bits (OR-ed by kernels; cleared by the caller). */
+#define HYPIC_STATUS_TIMEOUT   1u
+#define HYPIC_STATUS_NONFINITE 2u
+#define HYPIC_STATUS_BAD_SLOT  4u
+
+/* Shape of the transition stored in a pool slot for each variant:
+ *   dense  (GDN, DELTANET, CHANNEL_DELTA): T_pool [n_slots, h_v, d_k, d_k]
+ *   scalar (SCALAR_DECAY, UNGATED):        T_pool [n_slots, h_v]
+ *   diag   (DIAG_GATE):                    T_pool [n_slots, h_v, d_k]
+ * and always S_pool [n_slots, h_v, d_k, d_v]. */
+
+/*
+ * hypic_segment_build -- cache the pair (T_C, S(C|0)) of every segment and
+ * value head (pages: the pair is stored at a segment's first prefill, §2.1).
+ *
+ * Segment i spans tokens [seg_offsets[i], seg_offsets[i+1]); its first seam_w
+ * tokens form the seam window and are left out of the pair (§2.2), so the
+ * pair covers the body [seg_offsets[i] + seam_w, seg_offsets[i+1]).  A body
+ * that is empty gives (I, 0).  The pair of segment i goes to pool slot
+ * slot_of_seg[i] (or slot i when slot_of_seg is NULL).
+ *
+ * Work is split into (segment, value head) items packed over the SMs
+ * longest-first (LPT), the single-GPU analogue of the pages' greedy LPT
+ * balancing of segments over workers (§2.3).
+ */
+typedef struct {
+  int32_t n_tokens, n_seg;
+  int32_t h_k, h_v, d_k, d_v; /* 1 <= d_k, d_v <= 128; h_v a multiple of h_k */
+  int32_t seam_w;             /* >= 0 */
+  int32_t variant;            /* hypic_variant */
+  int32_t in_dtype;           /* hypic_in_dtype */
+  uint32_t flags;
+  const void *k;              /* [dev] [n_tokens, h_k, d_k] bf16 or fp32 */
+  const void *v;              /* [dev] [n_tokens, h_v, d_v] bf16 or fp32 */
+  const float *g;             /* [dev] log-gates: GDN [n_tokens,h_v]; CHANNEL_DELTA/DIAG_GATE
+                                 [n_tokens,h_v,d_k]; SCALAR_DECAY [h_v]; NULL otherwise */
+  const float *beta;          /* [dev] [n_tokens, h_v] for the delta variants, NULL otherwise */
+  const int64_t *seg_offsets; /* [host] [n_seg+1], non-decreasing, from 0 to n_tokens */
+  const int32_t *slot_of_seg; /* [host] [n_seg] distinct slots in [0, n_slots), or NULL */
+  int64_t n_slots;
+  float *T_pool;              /* [dev] see the shape note above */
+  float *S_pool;              /* [dev] [n_slots, h_v, d_k, d_v] */
+  void *workspace;            /* [dev] >= hypic_build_workspace_bytes(), 256-byte aligned */
+  size_t workspace_bytes;
+  uint32_t *status;           /* [dev] optional status word (may be NULL) */
+} hypic_build_desc;
+
+/* Workspace the build needs for this descriptor (shapes only are read). */
+size_t hypic_build_workspace_bytes(const hypic_build_desc *d);
+/* Returns a hypic_status; work is enqueued on `stream`. */
+int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream);
+
+/*
+ * hypic_compose -- rebuild the running state of every (layer, value head)
+ * from cached pairs in prompt order (pages §2.1 composition rule, §2.2 seam):
+ *   S <- S_init (or 0)
+ *   for segment i = 0 .. n_seg-1:
+ *     for each seam token t of segment i:  S <- T_t S + U_t,  o_t = S^T q_t
+ *     S <- T_{C_i} S + S(C_i|0)             (pair from pool slot slot[l, i])
+ * Every segment has exactly seam_w seam tokens; a segment with fewer real
+ * tokens passes identity tokens (k = v = q = 0, g = 0, beta = 0) in the rest,
+ * whose outputs carry no meaning.
+ */
+typedef struct {
+  int32_t n_layers, n_seg;
+  int32_t h_k, h_v, d_k, d_v;
+  int32_t seam_w;
+  int32_t variant, in_dtype;
+  uint32_t flags;
+  const int32_t *slot;        /* [dev] [n_layers, n_seg] pool slot per (layer, segment) */
+  int64_t n_slots;
+  const float *T_pool;        /* [dev] as written by hypic_segment_build */
+  const float *S_pool;        /* [dev] */
+  const void *seam_k;         /* [dev] [n_layers, n_seg, seam_w, h_k, d_k] bf16 or fp32 */
+  const void *seam_v;         /* [dev] [n_layers, n_seg, seam_w, h_v, d_v] */
+  const void *seam_q;         /* [dev] [n_layers, n_seg, seam_w, h_k, d_k] */
+  const float *seam_g;        /* [dev] GDN [L,n_seg,w,h_v]; CHANNEL/DIAG [L,n_seg,w,h_v,d_k];
+                                 SCALAR_DECAY [n_layers, h_v]; NULL otherwise */
+  const float *seam_beta;     /* [dev] [L, n_seg, w, h_v] for the delta variants, else NULL */
+  const float *S_init;        /* [dev] [n_layers, h_v, d_k, d_v] or NULL (= 0) */
+  float *S_out;               /* [dev] [n_layers, h_v, d_k, d_v]; may alias S_init */
+  float *seam_out;            /* [dev] [n_layers, n_seg, seam_w, h_v, d_v] (NULL if seam_w = 0) */
+  void *workspace;            /* [dev] >= hypic_compose_workspace_bytes() */
+  size_t workspace_bytes;
+  uint32_t *status;           /* [dev] optional */
+} hypic_compose_desc;
+
+size_t hypic_compose_workspace_bytes(const hypic_compose_desc *d);
+int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream);
+
+/*
+ * hypic_plan_lpt -- greedy longest-processing-time-first packing of items
+ * over workers (pages §2.3: LPT balancing of segments over scatter workers).
+ * Items are taken in order of decreasing cost (ties: lower index first) and
+ * each goes to the currently least-loaded worker (ties: lower worker index).
+ * Host-only.  order_out [n_items] receives the item order, worker_out
+ * [n_items] (may be NULL) the worker of each item (indexed by item), and
+ * *makespan_out (may be NULL) the largest worker load.
+ */
+int hypic_plan_lpt(const int64_t *costs, int32_t n_items, int32_t n_workers, int32_t *order_out,
+                   int32_t *worker_out, int64_t *makespan_out);
+
+/* Decode a device status word into the first hypic_status it reports. */
+int hypic_status_from_word(uint32_t word);
+const char *hypic_status_string(int status);
+/* Library version: major * 10000 + minor * 100 + patch. */
+int hypic_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HYPIC_H_ */

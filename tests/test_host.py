@@ -1,0 +1,173 @@
+"""Host-side checks that need no GPU: the C ABI library loads and exports
+every entry point that include/hypic.h declares, the LPT planner is the
+greedy longest-first rule (checked against brute force and Graham's bound),
+and invalid descriptors are rejected before anything is launched."""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_chunkwise_gb300 as hy
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__ as g
+    g.build()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "hypic.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hypic_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_entry_point():
+    lib = hy.load()
+    names = _declared()
+    assert "hypic_segment_build" in names and "hypic_compose" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in hypic.h but not exported"
+    assert set(hy.SYMBOLS) <= set(names)
+
+
+def test_status_strings_and_word_decoding():
+    assert hy.status_string(0) == "ok"
+    for c in range(1, 8):
+        assert hy.status_string(c) != "unknown status"
+    assert hy.status_from_word(0) == 0
+    assert hy.status_from_word(hy.STATUS_TIMEOUT) == 5
+    assert hy.status_from_word(hy.STATUS_BAD_SLOT) == 7
+    assert hy.status_from_word(hy.STATUS_NONFINITE) == 6
+
+
+def _lpt_reference(costs, m):
+    order = sorted(range(len(costs)), key=lambda i: (-costs[i], i))
+    loads = [0] * m
+    for i in order:
+        w = min(range(m), key=lambda j: (loads[j], j))
+        loads[w] += costs[i]
+    return order, max(loads) if costs else 0
+
+
+def _optimum(costs, m):
+    best = None
+    for assign in itertools.product(range(m), repeat=len(costs)):
+        loads = [0] * m
+        for c, w in zip(costs, assign):
+            loads[w] += c
+        mk = max(loads)
+        best = mk if best is None else min(best, mk)
+    return best
+
+
+def test_lpt_matches_rule_and_graham_bound():
+    rng = np.random.default_rng(3)
+    for trial in range(60):
+        n = int(rng.integers(1, 9))
+        m = int(rng.integers(1, 4))
+        costs = [int(x) for x in rng.integers(1, 20, n)]
+        if trial % 5 == 0:
+            costs = [7] * n  # all ties: index order
+        order, worker, mk = hy.plan_lpt(costs, m)
+        ref_order, ref_mk = _lpt_reference(costs, m)
+        assert list(order) == ref_order
+        assert mk == ref_mk
+        loads = np.zeros(m, dtype=np.int64)
+        for i, w in enumerate(worker):
+            loads[w] += costs[i]
+        assert loads.max() == mk
+        opt = _optimum(costs, m)
+        assert mk <= (4.0 / 3.0 - 1.0 / (3 * m)) * opt + 1e-9
+
+
+def test_lpt_beats_round_robin_on_uneven_mix():
+    # segments of 256..8192 tokens as in the cold uneven build
+    rng = np.random.default_rng(0)
+    costs = rng.choice([256, 1024, 4096, 8192], size=256, p=[0.4, 0.3, 0.2, 0.1])
+    _, _, mk = hy.plan_lpt(costs, 8)
+    rr = max(costs[w::8].sum() for w in range(8))
+    assert mk <= rr
+    assert mk <= costs.sum() / 8 + costs.max()
+
+
+def _fake_build_desc(**over):
+    d = hy.BuildDesc()
+    d.n_tokens, d.n_seg, d.h_k, d.h_v, d.d_k, d.d_v, d.seam_w = 8, 2, 1, 2, 16, 16, 0
+    d.variant, d.in_dtype = hy.GDN, hy.IN_F32
+    fake = ctypes.c_void_p(1 << 20)
+    d.k = d.v = d.g = d.beta = d.T_pool = d.S_pool = fake
+    d.n_slots = 2
+    d.workspace = ctypes.c_void_p(1 << 24)
+    d.workspace_bytes = 1 << 20
+    for k, v in over.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("case,offs,expect", [
+    ("non-monotone offsets", [0, 6, 4, 8], 1),
+    ("offsets not ending at n_tokens", [0, 3, 7], 1),
+    ("offsets not starting at 0", [1, 3, 8], 1),
+])
+def test_build_rejects_bad_offsets(case, offs, expect):
+    off = np.asarray(offs, dtype=np.int64)
+    d = _fake_build_desc(n_seg=len(offs) - 1, seg_offsets=off.ctypes.data_as(ctypes.c_void_p), n_slots=8)
+    assert hy.load().hypic_segment_build(ctypes.byref(d), None) == expect, case
+
+
+def test_build_rejects_bad_descriptors():
+    lib = hy.load()
+    off = np.asarray([0, 3, 8], dtype=np.int64)
+    po = off.ctypes.data_as(ctypes.c_void_p)
+    cases = [
+        (dict(h_v=3, h_k=2), 1),                          # h_v not a multiple of h_k
+        (dict(d_k=129), 2),                               # head size > 128
+        (dict(d_k=0), 1),
+        (dict(variant=9), 1),
+        (dict(k=None), 1),
+        (dict(beta=None), 1),                              # delta variant needs beta
+        (dict(g=None), 1),                                 # GDN needs log-gates
+        (dict(k=ctypes.c_void_p((1 << 20) + 2)), 1),       # misaligned fp32 input
+        (dict(workspace_bytes=16), 3),
+        (dict(workspace=None), 3),
+        (dict(n_slots=1), 1),                              # slot 1 out of range
+        (dict(seam_w=-1), 1),
+    ]
+    for over, want in cases:
+        d = _fake_build_desc(seg_offsets=po, **over)
+        assert lib.hypic_segment_build(ctypes.byref(d), None) == want, over
+    dup = np.asarray([1, 1], dtype=np.int32)
+    d = _fake_build_desc(seg_offsets=po, slot_of_seg=dup.ctypes.data_as(ctypes.c_void_p))
+    assert lib.hypic_segment_build(ctypes.byref(d), None) == 1
+
+
+def test_compose_rejects_bad_descriptors():
+    lib = hy.load()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def desc(**over):
+        d = hy.ComposeDesc()
+        d.n_layers, d.n_seg, d.h_k, d.h_v, d.d_k, d.d_v, d.seam_w = 1, 2, 1, 1, 16, 16, 2
+        d.variant, d.in_dtype = hy.GDN, hy.IN_F32
+        d.slot = d.T_pool = d.S_pool = d.seam_k = d.seam_v = d.seam_q = d.seam_g = d.seam_beta = fake
+        d.S_out = d.seam_out = fake
+        d.n_slots = 2
+        for k, v in over.items():
+            setattr(d, k, v)
+        return d
+    for over, want in [(dict(S_out=None), 1), (dict(seam_beta=None), 1), (dict(seam_g=None), 1),
+                       (dict(d_v=200), 2), (dict(slot=None), 1), (dict(seam_out=None), 1),
+                       (dict(seam_k=ctypes.c_void_p((1 << 20) + 1)), 1)]:
+        assert lib.hypic_compose(ctypes.byref(desc(**over)), None) == want, over
+
+
+def test_binding_refuses_host_tensors():
+    with pytest.raises(ValueError):
+        hy._ptr(torch.zeros(4))
