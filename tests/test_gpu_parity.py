@@ -243,8 +243,9 @@ def test_status_word_bad_slot_and_nonfinite():
                S_out=S_out, seam_out=seam_out, status=status)
     torch.cuda.synchronize()
     assert hy.status_from_word(int(status.item())) == 7
-    # a NaN planted in the host-made inputs is reported, not trapped
-    W.layers[0].v[3, 1, 5] = float("nan")
+    # a NaN planted in the host-made inputs (token 10: inside the first
+    # segment's body, past its 4 seam tokens) is reported, not trapped
+    W.layers[0].v[10, 1, 5] = float("nan")
     status.zero_()
     gpu_build(W, status=status, flags=hy.FLAG_CHECK_FINITE)
     torch.cuda.synchronize()
