@@ -1,6 +1,7 @@
 // api.cpp -- host side of libhypic: descriptor validation, the LPT work plan,
 // workspace sizing and kernel launches behind the C ABI of hypic.h.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <numeric>
 #include <queue>
@@ -43,6 +44,30 @@ int64_t n_build_items(const hypic_build_desc *d) { return (int64_t)d->n_seg * d-
 size_t plan_bytes(int64_t n_items) { return round_up(sizeof(PlanHeader) + n_items * sizeof(BuildItem), kAlign); }
 
 }  // namespace
+
+namespace hypic {
+uint32_t wait_limit() {
+  // default: ~2^24 polls of try_wait (seconds); the debug override lets a
+  // test make a wait run out on purpose
+  static const uint32_t lim = [] {
+    const char *e = std::getenv("HYPIC_DEBUG_WAIT_LIMIT");
+    if (e && *e) {
+      long v = std::strtol(e, nullptr, 10);
+      if (v >= 1) return (uint32_t)v;
+    }
+    return (uint32_t)(1u << 24);
+  }();
+  return lim;
+}
+
+bool debug_stall() {
+  static const bool on = [] {
+    const char *e = std::getenv("HYPIC_DEBUG_STALL");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+}  // namespace hypic
 
 extern "C" {
 
@@ -244,7 +269,11 @@ int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream) {
   p.seam_out = d->seam_out;
   p.status = d->status;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_compose_simt(p, s) != cudaSuccess) return HYPIC_ERR_CUDA;
+  // Dense transitions with bf16 seam tokens and 128-wide heads stream the
+  // pool through the tensor cores; fp32 inputs (1e-5 bar), smaller heads and
+  // scalar/diagonal transitions run the fp32 kernel.
+  cudaError_t e = compose_tc_supported(p) ? launch_compose_tc(p, wait_limit(), s) : launch_compose_simt(p, s);
+  if (e != cudaSuccess) return HYPIC_ERR_CUDA;
   return HYPIC_OK;
 }
 

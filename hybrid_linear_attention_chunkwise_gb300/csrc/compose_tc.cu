@@ -1,0 +1,452 @@
+// compose_tc.cu -- tensor-core compose of cached pairs for the dense-transition
+// variants (GDN, DeltaNet, per-channel delta) with bf16 seam tokens and
+// d_k = d_v = 128: the bandwidth-bound left-multiply-add S <- T_C S + S(C|0)
+// of the HYPIC news pages (nav.aitube.vip §2.1), with the seam-window advance
+// and per-token outputs of §2.2.
+//
+// One CTA of 128 threads per (layer, value head) chain, two CTAs per SM.
+// Thread n owns column n of the running state S (128 fp32 registers).  Per
+// segment, in prompt order:
+//   seam  the seam tokens update S in place (local dot product k^T S[:,n],
+//         rank-1 update) and emit o_t[n] = q_t . S[:,n];
+//   MMA   S is rounded to tf32 and stored to TMEM as the A operand (lane n =
+//         S[:,n]^T); thread 0 issues D = S^T T_C^T (M = N = K = 128,
+//         kind::tf32) from TMEM A and a shared-memory B operand, so lane n of
+//         D is column n of T_C S;
+//   add   each thread adds column n of S(C|0), read from global memory.
+// Data movement, all issued by thread 0 at the moment the consumer frees the
+// space (no producer warp: four warps per CTA leave each thread the full
+// register file it needs for its 128-value column):
+//   T_C   four 16 KiB K-slabs per pair (TMA 2-D tiles, 128-byte swizzle = the
+//         K-major MMA operand layout) through a ring of NSLOT slots; the slots
+//         of a pair are refilled as soon as its MMAs complete;
+//   S(C|0) prefetched into L2 one segment ahead (bulk prefetch), then read
+//         with coalesced loads, 32 rows at a time, one chunk ahead;
+//   seam  k/q/v rows and the gate block of each group of SB tokens by bulk
+//         copies into one of two seam buffers.
+// Each pool byte crosses HBM once: 128 KiB per (segment, head) pair.
+//
+// Every wait is bounded: one that runs out sets HYPIC_STATUS_TIMEOUT; the CTA
+// then skips its remaining work (control flow stays uniform across threads),
+// waits for the copies it issued and releases its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace hypic {
+
+namespace {
+
+constexpr int NSLOT = 5;   // T_C K-slab ring (16 KiB each)
+constexpr int SLAB = 16384;
+constexpr int SB = 8;      // seam tokens per seam buffer
+constexpr int NT = 128;    // threads per CTA
+constexpr int MAX_HV = 128;
+constexpr uint32_t DRAIN_LIMIT = 1u << 22;
+
+struct SeamBuf {
+  __nv_bfloat16 k[SB][128];
+  __nv_bfloat16 q[SB][128];
+  __nv_bfloat16 v[SB][128];
+  union {
+    float gv[SB][128];       // per-channel log-gates of this head (channel variant)
+    float g[SB * MAX_HV];    // scalar log-gates of every head (GDN)
+  };
+  float b[SB * MAX_HV];      // beta of every head
+};
+
+struct __align__(1024) ComposeTcSmem {
+  unsigned char slot[NSLOT][SLAB];  // 1024-aligned: swizzled TMA tiles
+  SeamBuf seam[2];
+  uint64_t full[NSLOT];
+  uint64_t seam_full[2];
+  uint64_t mma_done;
+  uint64_t never;  // no thread ever arrives here (debug stall)
+  uint32_t tmem_base;
+  int abort;
+  int stop;
+};
+
+struct TcArgs {
+  ComposeParams p;
+  uint32_t wait_limit;
+  int debug_stall;  // wait first on a barrier nothing signals (timeout test)
+};
+
+__device__ __forceinline__ bool aborted(ComposeTcSmem &sm) { return *(volatile int *)&sm.abort != 0; }
+
+__device__ __forceinline__ void fail(ComposeTcSmem &sm, const ComposeParams &p) {
+  *(volatile int *)&sm.abort = 1;
+  report(p.status, HYPIC_STATUS_TIMEOUT);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
+// eight bf16 values (one 16-byte shared-memory load) to fp32
+__device__ __forceinline__ void unpack8(const __nv_bfloat16 *src, float (&out)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(src);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    out[2 * j] = __uint_as_float(w[j] << 16);
+    out[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
+
+struct Chain {
+  int l, h, kh, n_seg, w, groups;
+};
+
+__device__ __forceinline__ int pair_slot(const ComposeParams &p, const Chain &c, int seg) {
+  const int s = p.slot[(int64_t)c.l * p.n_seg + seg];
+  return (s < 0 || s >= p.n_slots) ? -1 : s;
+}
+
+// T_C K-slab r (pair r/4, columns 32*(r%4) .. +32) into ring slot r % NSLOT
+__device__ __forceinline__ void issue_slab(ComposeTcSmem &sm, const ComposeParams &p, const Chain &c,
+                                           const CUtensorMap *tmap, uint32_t r) {
+  if (r >= 4u * (uint32_t)c.n_seg) return;
+  const int seg = (int)(r / 4), j = (int)(r % 4);
+  int slot = pair_slot(p, c, seg);
+  if (slot < 0) slot = 0;  // keep the ring in step; the pair is skipped at use
+  const int si = r % NSLOT;
+  tc::mbar_expect_tx(&sm.full[si], SLAB);
+  tc::tma_load_2d(sm.slot[si], tmap, 32 * j, (int32_t)(((int64_t)slot * p.h_v + c.h) * 128), &sm.full[si]);
+}
+
+template <bool VEC>
+__device__ __forceinline__ void issue_seam(ComposeTcSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
+  if (gq >= c.n_seg * c.groups) return;
+  const int seg = gq / c.groups, gi = gq % c.groups;
+  const int b = gq & 1;
+  SeamBuf &s = sm.seam[b];
+  const int t0 = gi * SB;
+  const int nt = min(SB, c.w - t0);
+  const int64_t tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + t0;
+  const uint32_t gbytes = (uint32_t)(nt * p.h_v * 4);
+  uint32_t bytes = (uint32_t)nt * 3 * 256 + gbytes + (VEC ? (uint32_t)nt * 512 : gbytes);
+  tc::mbar_expect_tx(&sm.seam_full[b], bytes);
+  const __nv_bfloat16 *sk = static_cast<const __nv_bfloat16 *>(p.seam_k);
+  const __nv_bfloat16 *sqp = static_cast<const __nv_bfloat16 *>(p.seam_q);
+  const __nv_bfloat16 *sv = static_cast<const __nv_bfloat16 *>(p.seam_v);
+  for (int t = 0; t < nt; t++) {
+    tc::bulk_load(s.k[t], sk + ((tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.seam_full[b]);
+    tc::bulk_load(s.q[t], sqp + ((tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.seam_full[b]);
+    tc::bulk_load(s.v[t], sv + ((tok0 + t) * p.h_v + c.h) * 128, 256, &sm.seam_full[b]);
+    if (VEC) tc::bulk_load(s.gv[t], p.seam_g + ((tok0 + t) * p.h_v + c.h) * 128, 512, &sm.seam_full[b]);
+  }
+  tc::bulk_load(s.b, p.seam_beta + tok0 * p.h_v, gbytes, &sm.seam_full[b]);
+  if (!VEC) tc::bulk_load(s.g, p.seam_g + tok0 * p.h_v, gbytes, &sm.seam_full[b]);
+}
+
+__device__ __forceinline__ void prefetch_pair_S(const ComposeParams &p, const Chain &c, int seg) {
+  if (seg >= c.n_seg) return;
+  const int slot = pair_slot(p, c, seg);
+  if (slot < 0) return;
+  prefetch_l2(p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128, 128 * 128 * 4);
+}
+
+// VAR: HYPIC_GDN, HYPIC_DELTANET or HYPIC_CHANNEL_DELTA
+template <int VAR>
+__global__ void __launch_bounds__(NT, 2)
+    compose_tc_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tmap_T) {
+  constexpr bool VEC = VAR == HYPIC_CHANNEL_DELTA;
+  constexpr bool GDN = VAR == HYPIC_GDN;
+  extern __shared__ unsigned char smem_raw[];
+  ComposeTcSmem &sm = *reinterpret_cast<ComposeTcSmem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const ComposeParams &p = args.p;
+  const uint32_t LIM = args.wait_limit;
+  const int n = threadIdx.x;  // column of S owned by this thread
+  const int warp = n / 32;
+  Chain c;
+  c.l = blockIdx.x / p.h_v;
+  c.h = blockIdx.x % p.h_v;
+  c.kh = (int)(((int64_t)c.h * p.h_k) / p.h_v);
+  c.n_seg = p.n_seg;
+  c.w = p.seam_w;
+  c.groups = (c.w + SB - 1) / SB;
+  const int total_groups = c.n_seg * c.groups;
+  const uint32_t total_slabs = 4u * (uint32_t)c.n_seg;
+
+  if (n == 0) {
+    for (int i = 0; i < NSLOT; i++) tc::mbar_init(&sm.full[i], 1);
+    tc::mbar_init(&sm.seam_full[0], 1);
+    tc::mbar_init(&sm.seam_full[1], 1);
+    tc::mbar_init(&sm.mma_done, 1);
+    tc::mbar_init(&sm.never, 1);
+    sm.abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&sm.tmem_base, 256);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tD = sm.tmem_base, tA = sm.tmem_base + 128;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+  uint32_t issued = 0;  // T_C slabs issued (thread 0)
+  int seam_issued = 0;  // seam groups issued (thread 0)
+  if (n == 0) {
+    tc::prefetch_tmap(&tmap_T);
+    for (; issued < (uint32_t)NSLOT && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued);
+    issue_seam<VEC>(sm, p, c, 0);
+    issue_seam<VEC>(sm, p, c, 1);
+    seam_issued = min(2, total_groups);
+    prefetch_pair_S(p, c, 0);
+    prefetch_pair_S(p, c, 1);
+  }
+
+  if (args.debug_stall && !tc::mbar_wait(&sm.never, 0, LIM)) fail(sm, p);
+
+  const int64_t state = (int64_t)blockIdx.x * 128 * 128;
+  float S[128];
+#pragma unroll
+  for (int i = 0; i < 128; i++) S[i] = p.S_init ? p.S_init[state + (int64_t)i * 128 + n] : 0.f;
+  bool bad = false;
+  const uint32_t id = tc::idesc(tc::FMT_TF32, 128, 128);
+
+  for (int seg = 0; seg < c.n_seg; seg++) {
+    // uniform stop decision
+    if (n == 0) sm.stop = *(volatile int *)&sm.abort;
+    __syncthreads();
+    const bool stop = *(volatile int *)&sm.stop != 0;
+    __syncthreads();
+    if (stop) break;
+
+    // ---- seam tokens
+    for (int gi = 0; gi < c.groups; gi++) {
+      const int gq = seg * c.groups + gi;
+      const int b = gq & 1;
+      const bool ok = !aborted(sm) && tc::mbar_wait(&sm.seam_full[b], (gq >> 1) & 1, LIM);
+      if (!ok) fail(sm, p);
+      SeamBuf &s = sm.seam[b];
+      const int t0 = gi * SB;
+      const int nt = ok ? min(SB, c.w - t0) : 0;
+      const int64_t tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + t0;
+      if (VEC) {
+        // per-channel gates a = exp(g), once per buffer (thread n: channel n)
+        for (int t = 0; t < nt; t++) s.gv[t][n] = __expf(s.gv[t][n]);
+        __syncthreads();
+      }
+      for (int t = 0; t < nt; t++) {
+        const float vj = __bfloat162float(s.v[t][n]);
+        const float bt = s.b[t * p.h_v + c.h];
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 128; i += 8) {
+          float kv[8];
+          unpack8(s.k[t] + i, kv);
+          if (VEC) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) kv[j] *= s.gv[t][i + j];
+          }
+          x0 = fmaf(kv[0], S[i], x0);
+          x1 = fmaf(kv[1], S[i + 1], x1);
+          x2 = fmaf(kv[2], S[i + 2], x2);
+          x3 = fmaf(kv[3], S[i + 3], x3);
+          x0 = fmaf(kv[4], S[i + 4], x0);
+          x1 = fmaf(kv[5], S[i + 5], x1);
+          x2 = fmaf(kv[6], S[i + 6], x2);
+          x3 = fmaf(kv[7], S[i + 7], x3);
+        }
+        const float x = (x0 + x1) + (x2 + x3);
+        // S <- a (S - b k x) + b k v   (channel: Diag(a) S first, then the erase)
+        const float gs = GDN ? __expf(s.g[t * p.h_v + c.h]) : 1.f;
+        const float cc = VEC ? (bt * vj - bt * x) : (gs * (-bt * x) + bt * vj);
+#pragma unroll
+        for (int i = 0; i < 128; i++) {
+          const float a = VEC ? s.gv[t][i] : gs;
+          S[i] = fmaf(a, S[i], __bfloat162float(s.k[t][i]) * cc);
+        }
+        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 128; i += 8) {
+          float qv[8];
+          unpack8(s.q[t] + i, qv);
+          o0 = fmaf(qv[0], S[i], o0);
+          o1 = fmaf(qv[1], S[i + 1], o1);
+          o2 = fmaf(qv[2], S[i + 2], o2);
+          o3 = fmaf(qv[3], S[i + 3], o3);
+          o0 = fmaf(qv[4], S[i + 4], o0);
+          o1 = fmaf(qv[5], S[i + 5], o1);
+          o2 = fmaf(qv[6], S[i + 6], o2);
+          o3 = fmaf(qv[7], S[i + 7], o3);
+        }
+        const float o = (o0 + o1) + (o2 + o3);
+        p.seam_out[((tok0 + t) * p.h_v + c.h) * 128 + n] = o;
+        bad |= !finite_f(o);
+      }
+      __syncthreads();  // every thread is done with this seam buffer
+      if (n == 0 && !aborted(sm) && gq + 2 < total_groups) {
+        issue_seam<VEC>(sm, p, c, gq + 2);
+        seam_issued = gq + 3;
+      }
+    }
+
+    // ---- S -> TMEM (A operand, tf32 round-to-nearest)
+#pragma unroll
+    for (int ch = 0; ch < 8; ch++) {
+      uint32_t r[16];
+#pragma unroll
+      for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(S[16 * ch + j]);
+      tc::tmem_st16(tA + lane_base + 16 * ch, r);
+    }
+    tc::tmem_wait_st();
+    tc::tc_fence_before();
+    __syncthreads();
+    const uint32_t q = 4u * (uint32_t)seg;
+    if (n == 0) {
+      tc::tc_fence_after();
+      bool ok = !aborted(sm);
+      for (int sl = 0; sl < 4 && ok; sl++) {
+        const uint32_t r = q + sl;
+        const int si = r % NSLOT;
+        if (!tc::mbar_wait(&sm.full[si], (r / NSLOT) & 1, LIM)) {
+          fail(sm, p);
+          ok = false;
+          break;
+        }
+        const uint32_t base = tc::smem_u32(sm.slot[si]);
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++) {
+          const uint64_t bd = tc::smem_desc(base + 32 * kk, 16, 1024, tc::SW_128B);
+          tc::mma_ts_tf32(tD, tA + 32 * sl + 8 * kk, bd, id, (sl | kk) != 0);
+        }
+      }
+      tc::mma_commit(&sm.mma_done);  // arrives once the MMAs above are complete
+    }
+    if (!tc::mbar_wait(&sm.mma_done, seg & 1, DRAIN_LIMIT)) fail(sm, p);
+    tc::tc_fence_after();
+    if (n == 0 && !aborted(sm)) {
+      // this pair's four slots are free: refill them, and warm L2 with the
+      // S(C|0) of the segment after next
+      for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
+      prefetch_pair_S(p, c, seg + 2);
+    }
+
+    // ---- S <- T_C S + S(C|0)
+    const int slot = pair_slot(p, c, seg);
+    if (slot < 0 && n == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
+    const bool use = slot >= 0 && !aborted(sm);
+    const float *Sc = p.S_pool + ((int64_t)(slot < 0 ? 0 : slot) * p.h_v + c.h) * 128 * 128 + n;
+    float nxt[32];
+#pragma unroll
+    for (int j = 0; j < 32; j++) nxt[j] = use ? Sc[j * 128] : 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 4; ch++) {
+      float cur[32];
+#pragma unroll
+      for (int j = 0; j < 32; j++) cur[j] = nxt[j];
+      if (ch < 3) {
+#pragma unroll
+        for (int j = 0; j < 32; j++) nxt[j] = use ? Sc[(32 * (ch + 1) + j) * 128] : 0.f;
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        uint32_t r[16];
+        tc::tmem_ld16(tD + lane_base + 32 * ch + 16 * hh, r);
+        tc::tmem_wait_ld();
+        if (use) {
+#pragma unroll
+          for (int j = 0; j < 16; j++) S[32 * ch + 16 * hh + j] = __uint_as_float(r[j]) + cur[16 * hh + j];
+        }
+      }
+    }
+    tc::tc_fence_before();  // TMEM reads done before the next MMA overwrites D
+  }
+
+  __syncthreads();
+  if (!aborted(sm)) {
+#pragma unroll
+    for (int i = 0; i < 128; i++) {
+      p.S_out[state + (int64_t)i * 128 + n] = S[i];
+      bad |= !finite_f(S[i]);
+    }
+  }
+  if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
+  // drain: every copy thread 0 issued lands before the CTA releases its smem
+  if (n == 0) {
+    const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
+    for (uint32_t r = first; r < issued; r++) tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, DRAIN_LIMIT);
+    for (int r = seam_issued > 2 ? seam_issued - 2 : 0; r < seam_issued; r++)
+      tc::mbar_wait(&sm.seam_full[r & 1], (r >> 1) & 1, DRAIN_LIMIT);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(sm.tmem_base, 256);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+// 2-D fp32 view [rows, 128] with 32-column x box_rows tiles and 128-byte
+// swizzle (one K-slab of a K-major tf32 MMA operand per tile).
+bool make_tmap_f32_rows(CUtensorMap *map, const float *base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {128 * sizeof(float)};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool compose_tc_supported(const ComposeParams &p) {
+  const bool dense = p.variant == HYPIC_GDN || p.variant == HYPIC_DELTANET || p.variant == HYPIC_CHANNEL_DELTA;
+  auto a16 = [](const void *x) { return x == nullptr || (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+  return dense && p.in_dtype == HYPIC_IN_BF16 && p.d_k == 128 && p.d_v == 128 && p.h_v <= MAX_HV &&
+         (p.h_v % 4) == 0 && a16(p.T_pool) && a16(p.S_pool) && a16(p.seam_k) && a16(p.seam_q) && a16(p.seam_v) &&
+         a16(p.seam_g) && a16(p.seam_beta);
+}
+
+cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s) {
+  CUtensorMap tmap;
+  if (!make_tmap_f32_rows(&tmap, p.T_pool, (uint64_t)p.n_slots * p.h_v * 128, 128)) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(ComposeTcSmem) + 1024;
+  auto kern = p.variant == HYPIC_GDN        ? compose_tc_kernel<HYPIC_GDN>
+              : p.variant == HYPIC_DELTANET ? compose_tc_kernel<HYPIC_DELTANET>
+                                            : compose_tc_kernel<HYPIC_CHANNEL_DELTA>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = p.n_layers * p.h_v;
+  if (grid < 1) return cudaSuccess;
+  TcArgs a;
+  a.p = p;
+  a.wait_limit = wait_limit;
+  a.debug_stall = debug_stall() ? 1 : 0;
+  kern<<<grid, NT, smem, s>>>(a, tmap);
+  return cudaGetLastError();
+}
+
+}  // namespace hypic

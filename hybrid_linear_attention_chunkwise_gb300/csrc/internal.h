@@ -63,5 +63,16 @@ __host__ __device__ inline bool is_vector_gate(int v) { return v == HYPIC_CHANNE
 // Launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_build_token(const BuildParams &p, int n_items, int n_sm, cudaStream_t s);
 cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s);
+cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s);
+// The tensor-core compose covers dense transitions, bf16 seam tokens,
+// d_k = d_v = 128, h_v % 4 == 0 and 16-byte aligned tensors.
+bool compose_tc_supported(const ComposeParams &p);
+
+// Bounded-wait poll limit for the pipelined kernels (HYPIC_DEBUG_WAIT_LIMIT
+// overrides it, for the timeout test).
+uint32_t wait_limit();
+// HYPIC_DEBUG_STALL=1: pipelined kernels first wait on a barrier that is never
+// signalled, so the bounded wait runs out (the timeout test).
+bool debug_stall();
 
 }  // namespace hypic

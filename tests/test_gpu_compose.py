@@ -1,0 +1,129 @@
+"""GPU tests of the tensor-core compose path (dense transitions, bf16 seam
+tokens, d = 128): parity with the fp64 oracle composing the same fp32 pairs,
+seam widths that need one or two seam buffers per segment, out-of-range
+slots, and the bounded-wait timeout."""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+from gpu_common import gpu_build, seam_arrays
+from tolerance import TOL_BF16, per_head_rel_err
+import hybrid_linear_attention_chunkwise_gb300 as hy
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import __graft_entry__ as g
+    g.build()
+
+
+def _run(W, n_layers, S_init=None, status=None, slot=None):
+    pools = [gpu_build(W, layer=l) for l in range(n_layers)]
+    T_pool = torch.cat([p[0] for p in pools])
+    S_pool = torch.cat([p[1] for p in pools])
+    sa = seam_arrays(W, range(n_layers))
+    if slot is None:
+        slot = torch.arange(n_layers * W.n_seg, dtype=torch.int32, device=DEV).reshape(n_layers, W.n_seg)
+    S_out = torch.empty((n_layers, W.h_v, 128, 128), device=DEV)
+    seam_out = torch.zeros((n_layers, W.n_seg, W.seam_w, W.h_v, 128), device=DEV) if W.seam_w else None
+    hy.compose(slot, T_pool, S_pool, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"], variant=W.variant,
+               S_out=S_out, seam_out=seam_out, S_init=S_init, status=status)
+    torch.cuda.synchronize()
+    return T_pool, S_pool, sa, slot, S_out, seam_out
+
+
+def _oracle_compose(W, T_pool, S_pool, sa, slot, S_init, n_layers):
+    sl = slot.long().cpu()
+    Tp = T_pool.cpu()[sl]          # [L, n_seg, h_v, 128, 128]
+    Sp = S_pool.cpu()[sl]
+    outs = []
+    for l in range(n_layers):
+        g = sa["g"][l:l + 1].cpu() if sa["g"] is not None else None
+        b = sa["beta"][l:l + 1].cpu() if sa["beta"] is not None else None
+        S0 = None if S_init is None else S_init[l:l + 1].cpu()
+        outs.append(oracle.compose(W.variant, Tp[l:l + 1], Sp[l:l + 1], sa["k"][l:l + 1].cpu(),
+                                   sa["v"][l:l + 1].cpu(), sa["q"][l:l + 1].cpu(), g, b, W.h_k, W.h_v,
+                                   S_init=S0))
+    return np.concatenate([o[0] for o in outs]), np.concatenate([o[1] for o in outs])
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "channel"])
+@pytest.mark.parametrize("w", [0, 3, 8, 11])
+def test_compose_tc_parity(variant, w):
+    lens = [40, 130, 12, 64, 300, 25]
+    W = si.workload(5, device=DEV, variant=variant, lengths=lens, h_k=2, h_v=4, seam_w=w, n_layers=2)
+    S_init = si.random_state((2, W.h_v, 128, 128), seed=0, cfg=5, device=DEV)
+    T_pool, S_pool, sa, slot, S_out, seam_out = _run(W, 2, S_init=S_init)
+    So, seam = _oracle_compose(W, T_pool, S_pool, sa, slot, S_init, 2)
+    assert per_head_rel_err(S_out, So).max() <= TOL_BF16
+    if w:
+        e = per_head_rel_err(seam_out.permute(0, 3, 1, 2, 4).reshape(2, W.h_v, -1),
+                             np.transpose(seam, (0, 3, 1, 2, 4)).reshape(2, W.h_v, -1), inner=1)
+        assert e.max() <= TOL_BF16, e.max()
+
+
+def test_compose_tc_bad_slot_reported_and_skipped():
+    W = si.workload(5, device=DEV, variant="deltanet", lengths=[30, 40, 50], h_k=1, h_v=4, seam_w=8)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slot = torch.tensor([[0, 99, 2]], dtype=torch.int32, device=DEV)
+    T_pool, S_pool, sa, _, S_out, seam_out = _run(W, 1, status=status, slot=slot)
+    assert hy.status_from_word(int(status.item())) == 7   # HYPIC_ERR_BAD_SLOT
+    # the chain skipped the bad pair: same as composing with (I, 0) there
+    T2 = T_pool.clone()
+    S2 = S_pool.clone()
+    T2[1] = torch.eye(128, device=DEV)
+    S2[1] = 0
+    ok_slot = torch.tensor([[0, 1, 2]], dtype=torch.int32, device=DEV)
+    ref = torch.empty_like(S_out)
+    hy.compose(ok_slot, T2, S2, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"], variant="deltanet", S_out=ref,
+               seam_out=torch.empty_like(seam_out))
+    torch.cuda.synchronize()
+    assert per_head_rel_err(S_out, ref).max() <= TOL_BF16
+
+
+_TIMEOUT_CHILD = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + '/tests')
+import synth_inputs as si
+import hybrid_linear_attention_chunkwise_gb300 as hy
+from gpu_common import gpu_build, seam_arrays
+W = si.workload(5, device='cuda', variant='gdn', lengths=[40, 70, 33], h_k=1, h_v=4, seam_w=8)
+T, S = gpu_build(W)
+torch.cuda.synchronize()
+sa = seam_arrays(W)
+status = torch.zeros(1, dtype=torch.int32, device='cuda')
+slot = torch.arange(3, dtype=torch.int32, device='cuda')[None]
+out = torch.empty((1, 4, 128, 128), device='cuda')
+so = torch.empty((1, 3, 8, 4, 128), device='cuda')
+hy.compose(slot, T, S, sa['k'], sa['v'], sa['q'], sa['g'], sa['beta'], variant='gdn', S_out=out, seam_out=so,
+           status=status)
+torch.cuda.synchronize()
+code = hy.status_from_word(int(status.item()))
+x = torch.ones(4, device='cuda').sum().item()   # the context is still usable
+print('STATUS', code, 'CTX', x)
+"""
+
+
+def test_compose_tc_bounded_wait_reports_timeout():
+    """The debug stall makes every CTA wait on an mbarrier that nothing ever
+    signals, with a short poll limit: the wait runs out, the kernel reports
+    HYPIC_ERR_TIMEOUT through the status word, drains its copies and returns;
+    nothing spins and the context stays usable."""
+    env = dict(os.environ, HYPIC_DEBUG_WAIT_LIMIT="2000", HYPIC_DEBUG_STALL="1")
+    r = subprocess.run([sys.executable, "-c", _TIMEOUT_CHILD, ROOT], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("STATUS")][-1]
+    assert line.split()[1] == "5" and line.split()[3] == "4.0", line
