@@ -120,7 +120,9 @@ __device__ __forceinline__ void issue_slab(ComposeTcSmem &sm, const ComposeParam
   tc::tma_load_2d(sm.slot[si], tmap, 32 * j, (int32_t)(((int64_t)slot * p.h_v + c.h) * 128), &sm.full[si]);
 }
 
-template <bool VEC>
+// VEC: per-channel gate rows; GDN: scalar gate block; neither (DeltaNet): no
+// gates at all (seam_g is NULL then and must not be touched)
+template <bool VEC, bool GDN>
 __device__ __forceinline__ void issue_seam(ComposeTcSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
   if (gq >= c.n_seg * c.groups) return;
   const int seg = gq / c.groups, gi = gq % c.groups;
@@ -130,7 +132,7 @@ __device__ __forceinline__ void issue_seam(ComposeTcSmem &sm, const ComposeParam
   const int nt = min(SB, c.w - t0);
   const int64_t tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + t0;
   const uint32_t gbytes = (uint32_t)(nt * p.h_v * 4);
-  uint32_t bytes = (uint32_t)nt * 3 * 256 + gbytes + (VEC ? (uint32_t)nt * 512 : gbytes);
+  const uint32_t bytes = (uint32_t)nt * 3 * 256 + gbytes + (VEC ? (uint32_t)nt * 512 : 0) + (GDN ? gbytes : 0);
   tc::mbar_expect_tx(&sm.seam_full[b], bytes);
   const __nv_bfloat16 *sk = static_cast<const __nv_bfloat16 *>(p.seam_k);
   const __nv_bfloat16 *sqp = static_cast<const __nv_bfloat16 *>(p.seam_q);
@@ -142,7 +144,7 @@ __device__ __forceinline__ void issue_seam(ComposeTcSmem &sm, const ComposeParam
     if (VEC) tc::bulk_load(s.gv[t], p.seam_g + ((tok0 + t) * p.h_v + c.h) * 128, 512, &sm.seam_full[b]);
   }
   tc::bulk_load(s.b, p.seam_beta + tok0 * p.h_v, gbytes, &sm.seam_full[b]);
-  if (!VEC) tc::bulk_load(s.g, p.seam_g + tok0 * p.h_v, gbytes, &sm.seam_full[b]);
+  if (GDN) tc::bulk_load(s.g, p.seam_g + tok0 * p.h_v, gbytes, &sm.seam_full[b]);
 }
 
 __device__ __forceinline__ void prefetch_pair_S(const ComposeParams &p, const Chain &c, int seg) {
@@ -199,8 +201,8 @@ __global__ void __launch_bounds__(NT, 2)
   if (n == 0) {
     tc::prefetch_tmap(&tmap_T);
     for (; issued < (uint32_t)NSLOT && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued);
-    issue_seam<VEC>(sm, p, c, 0);
-    issue_seam<VEC>(sm, p, c, 1);
+    issue_seam<VEC, GDN>(sm, p, c, 0);
+    issue_seam<VEC, GDN>(sm, p, c, 1);
     seam_issued = min(2, total_groups);
     prefetch_pair_S(p, c, 0);
     prefetch_pair_S(p, c, 1);
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(NT, 2)
       }
       __syncthreads();  // every thread is done with this seam buffer
       if (n == 0 && !aborted(sm) && gq + 2 < total_groups) {
-        issue_seam<VEC>(sm, p, c, gq + 2);
+        issue_seam<VEC, GDN>(sm, p, c, gq + 2);
         seam_issued = gq + 3;
       }
     }
