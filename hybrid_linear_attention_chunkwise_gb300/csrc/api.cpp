@@ -123,7 +123,7 @@ int hypic_plan_lpt(const int64_t *costs, int32_t n_items, int32_t n_workers, int
 
 size_t hypic_build_workspace_bytes(const hypic_build_desc *d) {
   if (!d || d->n_seg < 0 || d->h_v < 1) return 0;
-  return plan_bytes(n_build_items(d));
+  return plan_bytes(2 * n_build_items(d));  // room for two items per pair (tensor-core path)
 }
 
 int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
@@ -157,43 +157,6 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
       if (i && s2[i] == s2[i - 1]) return HYPIC_ERR_INVALID_ARG;
     }
   }
-  const int64_t n_items = n_build_items(d);
-  if (n_items > INT32_MAX / 2) return HYPIC_ERR_UNSUPPORTED;
-  const size_t need = plan_bytes(n_items);
-  if (!d->workspace || d->workspace_bytes < need || !aligned(d->workspace, kAlign)) return HYPIC_ERR_WORKSPACE;
-
-  // ---- LPT plan over (segment, value head) items; cost = body length ----
-  std::vector<int64_t> cost(n_items);
-  for (int64_t it = 0; it < n_items; it++) {
-    const int i = (int)(it / d->h_v);
-    const int64_t s = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
-    cost[it] = d->seg_offsets[i + 1] - s;
-  }
-  std::vector<int32_t> order(n_items);
-  st = hypic_plan_lpt(cost.data(), (int32_t)n_items, sm_count(), order.data(), nullptr, nullptr);
-  if (st) return st;
-  std::vector<unsigned char> host(need, 0);
-  PlanHeader *hdr = reinterpret_cast<PlanHeader *>(host.data());
-  hdr->ticket = 0;
-  hdr->n_items = (int32_t)n_items;
-  BuildItem *items = reinterpret_cast<BuildItem *>(hdr + 1);
-  for (int64_t r = 0; r < n_items; r++) {
-    const int64_t it = order[r];
-    const int i = (int)(it / d->h_v);
-    BuildItem b;
-    b.seg = i;
-    b.head = (int32_t)(it % d->h_v);
-    b.slot = slots[i];
-    b.part = 0;
-    b.start = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
-    b.end = d->seg_offsets[i + 1];
-    items[r] = b;
-  }
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // pageable source: the call returns once the bytes are staged, so `host`
-  // may be released when it goes out of scope
-  if (cudaMemcpyAsync(d->workspace, host.data(), need, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
-
   BuildParams p{};
   p.h_k = d->h_k;
   p.h_v = d->h_v;
@@ -212,7 +175,53 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
   p.plan = reinterpret_cast<PlanHeader *>(d->workspace);
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
   p.status = d->status;
-  if (launch_build_token(p, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
+  // bf16 scalar-gate delta rules with 128-wide heads run chunkwise on the
+  // tensor cores, one item per half of [T | S]; every other case runs the
+  // fp32 token recurrence, one item per (segment, head)
+  const bool tc_path = build_tc_supported(p);
+  const int parts = tc_path ? 2 : 1;
+
+  const int64_t n_pairs = n_build_items(d);
+  const int64_t n_items = n_pairs * parts;
+  if (n_items > INT32_MAX / 2) return HYPIC_ERR_UNSUPPORTED;
+  const size_t need = plan_bytes(n_items);
+  if (!d->workspace || d->workspace_bytes < need || !aligned(d->workspace, kAlign)) return HYPIC_ERR_WORKSPACE;
+
+  // ---- LPT plan over the items; cost = body length ----
+  std::vector<int64_t> cost(n_items);
+  for (int64_t it = 0; it < n_items; it++) {
+    const int i = (int)((it / parts) / d->h_v);
+    const int64_t s0 = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
+    cost[it] = d->seg_offsets[i + 1] - s0;
+  }
+  std::vector<int32_t> order(n_items);
+  st = hypic_plan_lpt(cost.data(), (int32_t)n_items, sm_count(), order.data(), nullptr, nullptr);
+  if (st) return st;
+  std::vector<unsigned char> host(need, 0);
+  PlanHeader *hdr = reinterpret_cast<PlanHeader *>(host.data());
+  hdr->ticket = 0;
+  hdr->n_items = (int32_t)n_items;
+  BuildItem *items = reinterpret_cast<BuildItem *>(hdr + 1);
+  for (int64_t r = 0; r < n_items; r++) {
+    const int64_t it = order[r];
+    const int64_t pr = it / parts;
+    const int i = (int)(pr / d->h_v);
+    BuildItem b;
+    b.seg = i;
+    b.head = (int32_t)(pr % d->h_v);
+    b.slot = slots[i];
+    b.part = (int32_t)(it % parts);
+    b.start = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
+    b.end = d->seg_offsets[i + 1];
+    items[r] = b;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // pageable source: the call returns once the bytes are staged, so `host`
+  // may be released when it goes out of scope
+  if (cudaMemcpyAsync(d->workspace, host.data(), need, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
+  const cudaError_t e = tc_path ? launch_build_tc(p, d->n_tokens, (int)n_items, sm_count(), wait_limit(), s)
+                                : launch_build_token(p, (int)n_items, sm_count(), s);
+  if (e != cudaSuccess) return HYPIC_ERR_CUDA;
   return HYPIC_OK;
 }
 

@@ -62,6 +62,11 @@ __host__ __device__ inline bool is_vector_gate(int v) { return v == HYPIC_CHANNE
 
 // Launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_build_token(const BuildParams &p, int n_items, int n_sm, cudaStream_t s);
+// Tensor-core chunkwise build: GDN / DeltaNet, bf16 inputs, d_k = d_v = 128,
+// 16-byte aligned k / v.  Items are (segment, head, half of [T | S]).
+bool build_tc_supported(const BuildParams &p);
+cudaError_t launch_build_tc(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, uint32_t wait_limit,
+                            cudaStream_t s);
 cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s);
 // The tensor-core compose covers dense transitions, bf16 seam tokens,
