@@ -243,8 +243,9 @@ __global__ void __launch_bounds__(NT, 1)
     build_tc_kernel(const __grid_constant__ BuildTcArgs args, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v) {
   extern __shared__ unsigned char smem_raw[];
-  BuildTcSmem &sm = *reinterpret_cast<BuildTcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                     ~uintptr_t(1023));
+  // 1024-byte alignment by pointer arithmetic on the shared array, so the
+  // compiler keeps every access in the shared address space
+  BuildTcSmem &sm = *reinterpret_cast<BuildTcSmem *>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   const BuildParams &p = args.p;
   const uint32_t LIM = args.wait_limit;
   const int n = threadIdx.x, warp = n >> 5, lane = n & 31;

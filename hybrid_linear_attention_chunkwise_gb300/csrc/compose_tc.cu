@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(NT, 2)
   constexpr bool VEC = VAR == HYPIC_CHANNEL_DELTA;
   constexpr bool GDN = VAR == HYPIC_GDN;
   extern __shared__ unsigned char smem_raw[];
-  ComposeTcSmem &sm = *reinterpret_cast<ComposeTcSmem *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte alignment by pointer arithmetic on the shared array, so the
+  // compiler keeps every access in the shared address space
+  ComposeTcSmem &sm = *reinterpret_cast<ComposeTcSmem *>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   const ComposeParams &p = args.p;
   const uint32_t LIM = args.wait_limit;
   const int n = threadIdx.x;  // column of S owned by this thread
