@@ -18,25 +18,31 @@
 // so each CTA owns one half of one (segment, head): a 128 x 128 block of
 // X^T, kept in TMEM as the fp32 accumulator (lane j = column j of the half,
 // TMEM column d) next to a tf32-rounded copy, the A operand of chain 1.
-// The TMA-loaded bf16 K and V tiles [64 tokens x 128] serve directly as MMA
-// operands -- K-major for the Gram, MN-major (transposed view) elsewhere --
-// so no operand is ever transposed by the threads.  Per chunk:
-//   Gram     K K^T                                   kind::f16, exact inputs
-//   UT       A = (I + M)^-1                          SIMT, 16 x 16 blocks
-//   W        W^T  = K^T (A diag(bG))^T               kind::f16, factor split hi + lo
-//   U        -U^T = V^T (-A diag(b))^T   (S half)    kind::f16, factor split hi + lo
-//   chain 1  Y^T (+)= X^T W^T                        kind::tf32, A from TMEM
-//   chain 2  X^T += Ytilde^T K                       kind::f16, Ytilde split hi + lo
-// with Ytilde = -Y diag(exp(lam_C - lam)) and X scaled by G_C in TMEM before
-// chain 2.  Split operands make those products exact to ~2^-17 (K and V are
-// exact bf16); chain 1 uses tf32 operands rounded to nearest by the threads
-// (the tensor core itself truncates fp32 operands).  fp32 accumulation
-// throughout.  This keeps long products (8192 tokens) inside 5e-3 per head.
+// The TMA-loaded bf16 K and V tiles [64 tokens x 128] are MMA operands as
+// they land -- K-major for the Gram, MN-major (transposed view) elsewhere --
+// so no operand is ever transposed by the threads.
+//
+// Two warp groups run one chunk apart:
+//   P (warps 4-7) prepares chunk c+1 from its inputs alone
+//       Gram   K K^T                              kind::f16, exact inputs
+//       UT     A = (I + M)^-1                     SIMT, 16 x 16 blocks
+//       W, U   W^T = K^T (A diag(bG))^T,  U^T = V^T (A diag(b))^T
+//                                                 kind::f16, factors split hi + lo
+//       and stages W (tf32, rounded) as the B operand of chain 1;
+//   X (warps 0-3) advances the state through chunk c
+//       chain 1  Y^T = X^T W^T                    kind::tf32, A from TMEM
+//       Ytilde   = -(Y - [0 | U]) diag(exp(lam_C - lam)), split hi + lo
+//       chain 2  X^T = G_C X^T + Ytilde^T K       kind::f16 (B = K tile, MN-major)
+// handing off through mbarriers.  Split operands make W, U and chain 2 exact
+// to ~2^-17 (K and V are exact bf16); chain 1 uses tf32 operands rounded to
+// nearest by the threads (the tensor core itself truncates fp32 operands).
+// fp32 accumulation throughout.  This keeps long products (8192 tokens)
+// inside 5e-3 per head.
 //
 // Items are (segment, value head, half) in LPT order, pulled by an atomic
 // ticket.  Inputs come in by TMA (3-D maps over [token, head, channel],
-// 128-byte swizzle), two chunks ahead; the per-token gates by plain loads one
-// chunk ahead.  All waits are bounded.
+// 128-byte swizzle) through three buffers, two chunks ahead of their use.
+// All waits are bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,15 +55,19 @@ namespace hypic {
 namespace {
 
 constexpr int C = 64;      // tokens per chunk
-constexpr int NT = 256;    // threads per CTA (warps w and w+4 share TMEM lanes)
+constexpr int NT = 256;    // threads: X group = warps 0-3, P group = warps 4-7
+constexpr int NG = 128;    // threads per group
+constexpr int NBUF = 3;    // input buffers
+constexpr int BAR_X = 1, BAR_P = 2;  // named barriers of the two groups
 constexpr uint32_t DRAIN_LIMIT = 1u << 22;
 
 // TMEM columns (512 allocated, one CTA per SM)
-constexpr uint32_t TM_X = 0;     // X^T half, fp32 accumulator           [128 x 128]
-constexpr uint32_t TM_XR = 128;  // tf32-rounded copy (A of chain 1)     [128 x 128]
-constexpr uint32_t TM_Y = 256;   // Y^T half                             [128 x 64]
-constexpr uint32_t TM_W = 320;   // W^T                                  [128 x 64]
-constexpr uint32_t TM_G = 384;   // K K^T (lanes 0..63)                  [128 x 64]
+constexpr uint32_t TM_X = 0;     // X^T half, fp32 accumulator      (X group)
+constexpr uint32_t TM_XR = 128;  // tf32-rounded copy: A of chain 1 (X group)
+constexpr uint32_t TM_Y = 256;   // chain 1 output                  (X group)
+constexpr uint32_t TM_W = 320;   // W^T                             (P group)
+constexpr uint32_t TM_U = 384;   // U^T (S half)                    (P writes, X reads)
+constexpr uint32_t TM_G = 448;   // K K^T, lanes 0..63              (P group)
 
 // Byte offsets in K-major, 128-byte-swizzled tiles of R rows (the layout the
 // shared-memory descriptors describe and TMA writes): 4-byte elements sit 32
@@ -85,24 +95,35 @@ __device__ __forceinline__ uint64_t mndesc16(uint32_t base, int t) {
 }
 
 struct __align__(1024) BuildTcSmem {
-  struct In {                   // one chunk of inputs (TMA tiles, two slabs each)
-    unsigned char k[16384];     // K [64 t x 128 d] bf16
-    unsigned char v[16384];     // V [64 t x 128 j] bf16 (S half); also pads the Gram's rows 64..127
-  } in[2];
+  // inputs as TMA tiles [64 t x 128] bf16 in two 64-channel slabs: K of
+  // chunk c in kin[c % 3] (read by P's Gram and W and by X's chain 2 one
+  // chunk later), V in vin[c % 2] (read only by P's U MMA).  V follows K so
+  // the Gram's padded rows 64..127 read valid (ignored) bytes.
+  unsigned char kin[NBUF][16384];
+  unsigned char vin[2][16384];
   unsigned char wt[32768];      // W  [64 t x 128 d] tf32, K-major: B of chain 1
   unsigned char yh[16384];      // Ytilde hi [128 j x 64 t] bf16: A of chain 2
   unsigned char yl[16384];      // Ytilde lo
-  unsigned char bwh[8192];      // A diag(bG) hi [64 t x 64 t'] bf16: B of the W MMA
-  unsigned char bwl[8192];      //   lo
-  unsigned char buh[8192];      // -A diag(b) hi: B of the U MMA
+  union {
+    struct {
+      unsigned char bwh[8192];  // A diag(bG) hi [64 t x 64 t'] bf16: B of the W MMA
+      unsigned char bwl[8192];  //   lo
+    };
+    float pm[3][16][18];        // block products of the inverse (done before the factors)
+  };
+  unsigned char buh[8192];      // A diag(b) hi: B of the U MMA
   unsigned char bul[8192];      //   lo
-  float nm[64][65];             // M
-  float am[64][65];             // A = (I + M)^-1
-  float pm[3][16][17];          // block products of the inverse
-  float lam[64], bg[64], bt[64], dec[64];
-  float gC;
-  uint64_t full[2];
-  uint64_t bar_g, bar_w, bar_y, bar_x;
+  float nm[64][68];             // M (rows 16-byte aligned for vector stores)
+  float am[64][66];             // A = (I + M)^-1 (rows 8-byte aligned for pair loads)
+  float lam[64], bg[64], bt[64];
+  float ea[64], eb[64];         // b_t exp(lam_t - lam_0), exp(lam_0 - lam_i): M_ti = ea_t eb_i k_t.k_i
+  int fact;                     // the factored form is in range for this chunk
+  float dec[3][64];             // exp(lam_C - lam_t) of chunk c in [c % 3] (read by X)
+  float gc[3];                  // G_C of chunk c in [c % 3] (read by X)
+  uint64_t full[NBUF];
+  uint64_t bar_g, bar_wu;       // P's MMA completions
+  uint64_t bar_y, bar_x;        // X's MMA completions (P also waits on them)
+  uint64_t wt_ready, ys_done;   // P -> X: W staged; X -> P: U consumed
   uint64_t never;
   uint32_t tmem_base;
   int item;
@@ -120,6 +141,11 @@ __device__ __forceinline__ void fail(BuildTcSmem &sm, const BuildParams &p) {
   *(volatile int *)&sm.abort = 1;
   report(p.status, HYPIC_STATUS_TIMEOUT);
 }
+// bounded wait on phase `ph` of an mbarrier that completes once per chunk
+__device__ __forceinline__ void wait_phase(BuildTcSmem &sm, const BuildParams &p, uint64_t *bar, uint32_t ph,
+                                           uint32_t lim) {
+  if (!tc::mbar_wait(bar, ph & 1, aborted(sm) ? DRAIN_LIMIT : lim)) fail(sm, p);
+}
 
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi)
 __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
@@ -129,30 +155,22 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bflo
 __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
   return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
-
-// TMEM address of this thread's lane at column `col` (warps w and w+4 share
-// the lane quadrant w % 4)
+// TMEM address of this thread's lane (warp w covers lanes 32 (w % 4) ..)
 __device__ __forceinline__ uint32_t trow(uint32_t base, int col) {
   return base + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)col;
-}
-
-__device__ __forceinline__ void wait_mma(BuildTcSmem &sm, const BuildParams &p, uint64_t *bar, uint32_t &phase) {
-  if (!tc::mbar_wait(bar, phase & 1, DRAIN_LIMIT)) fail(sm, p);
-  phase++;
-  tc::tc_fence_after();
 }
 // ---------------------------------------------------------------- UT inverse
 // A = (I + N)^-1 for the strictly lower 64 x 64 N in sm.nm, into sm.am:
 // diagonal 16 x 16 blocks by forward substitution (one thread per column),
 // then the off-diagonal blocks level by level,
 //     A_ij = -A_ii * sum_{k=j}^{i-1} N_ik A_kj      (i > j).
-// Called by all threads; ends with a barrier.
-__device__ void ut_inverse(BuildTcSmem &sm) {
-  const int n = threadIdx.x;
-  for (int e = n; e < 64 * 64; e += NT) sm.am[e >> 6][e & 63] = 0.f;
-  __syncthreads();
-  if (n < 64) {
-    const int b = 16 * (n >> 4), l = n & 15;
+// Called by the 128 threads of the P group (q = index in the group); ends
+// with a group barrier.
+__device__ void ut_inverse(BuildTcSmem &sm, int q) {
+  for (int e = q; e < 64 * 64; e += NG) sm.am[e >> 6][e & 63] = 0.f;
+  tc::named_bar(BAR_P, NG);
+  if (q < 64) {
+    const int b = 16 * (q >> 4), l = q & 15;
     float a[16];
 #pragma unroll
     for (int r = 0; r < 16; r++) {
@@ -167,44 +185,55 @@ __device__ void ut_inverse(BuildTcSmem &sm) {
 #pragma unroll
     for (int r = 0; r < 16; r++) sm.am[b + r][b + l] = a[r];
   }
-  __syncthreads();
+  tc::named_bar(BAR_P, NG);
+  // off-diagonal levels; each thread forms 2 x 2 output tiles (64 per block)
   for (int d = 1; d < 4; d++) {
     const int nb = 4 - d;  // blocks (i, i - d), i = d .. 3
-    for (int e = n; e < nb * 256; e += NT) {
-      const int q = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      const int i = d + q, j = i - d;
-      float s0 = 0.f, s1 = 0.f;
+    for (int e = q; e < nb * 64; e += NG) {
+      const int bq = e >> 6, r = 2 * ((e >> 3) & 7), c = 2 * (e & 7);
+      const int i = d + bq, j = i - d;
+      float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
       for (int k = j; k < i; k++) {
 #pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-          s0 = fmaf(sm.nm[16 * i + r][16 * k + m], sm.am[16 * k + m][16 * j + c], s0);
-          s1 = fmaf(sm.nm[16 * i + r][16 * k + m + 1], sm.am[16 * k + m + 1][16 * j + c], s1);
+        for (int m = 0; m < 16; m++) {
+          const float n0 = sm.nm[16 * i + r][16 * k + m], n1 = sm.nm[16 * i + r + 1][16 * k + m];
+          const float2 a = *reinterpret_cast<const float2 *>(&sm.am[16 * k + m][16 * j + c]);
+          s00 = fmaf(n0, a.x, s00);
+          s01 = fmaf(n0, a.y, s01);
+          s10 = fmaf(n1, a.x, s10);
+          s11 = fmaf(n1, a.y, s11);
         }
       }
-      sm.pm[q][r][c] = s0 + s1;
+      *reinterpret_cast<float2 *>(&sm.pm[bq][r][c]) = make_float2(s00, s01);
+      *reinterpret_cast<float2 *>(&sm.pm[bq][r + 1][c]) = make_float2(s10, s11);
     }
-    __syncthreads();
-    for (int e = n; e < nb * 256; e += NT) {
-      const int q = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      const int i = d + q, j = i - d;
-      float s0 = 0.f, s1 = 0.f;
+    tc::named_bar(BAR_P, NG);
+    for (int e = q; e < nb * 64; e += NG) {
+      const int bq = e >> 6, r = 2 * ((e >> 3) & 7), c = 2 * (e & 7);
+      const int i = d + bq, j = i - d;
+      float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
 #pragma unroll
-      for (int m = 0; m < 16; m += 2) {
-        s0 = fmaf(sm.am[16 * i + r][16 * i + m], sm.pm[q][m][c], s0);
-        s1 = fmaf(sm.am[16 * i + r][16 * i + m + 1], sm.pm[q][m + 1][c], s1);
+      for (int m = 0; m < 16; m++) {
+        const float a0 = sm.am[16 * i + r][16 * i + m], a1 = sm.am[16 * i + r + 1][16 * i + m];
+        const float2 pv = *reinterpret_cast<const float2 *>(&sm.pm[bq][m][c]);
+        s00 = fmaf(a0, pv.x, s00);
+        s01 = fmaf(a0, pv.y, s01);
+        s10 = fmaf(a1, pv.x, s10);
+        s11 = fmaf(a1, pv.y, s11);
       }
-      sm.am[16 * i + r][16 * j + c] = -(s0 + s1);
+      *reinterpret_cast<float2 *>(&sm.am[16 * i + r][16 * j + c]) = make_float2(-s00, -s01);
+      *reinterpret_cast<float2 *>(&sm.am[16 * i + r + 1][16 * j + c]) = make_float2(-s10, -s11);
     }
-    __syncthreads();
+    tc::named_bar(BAR_P, NG);
   }
 }
 
-// Split factor tiles A diag(bG) and -A diag(b) (K-major bf16 [64 t x 64 t'],
-// hi and lo): thread n writes 16 consecutive t' of row n / 4.
-__device__ __forceinline__ void write_factors(BuildTcSmem &sm, bool s_half) {
-  const int n = threadIdx.x, t = n >> 2, q0 = 16 * (n & 3);
+// Split factor tiles A diag(bG) and A diag(b) (K-major bf16 [64 t x 64 t'],
+// hi and lo): thread q writes 32 consecutive t' of row q / 2.
+__device__ __forceinline__ void write_factors(BuildTcSmem &sm, int q, bool s_half) {
+  const int t = q >> 1, q0 = 32 * (q & 1);
 #pragma unroll
-  for (int h8 = 0; h8 < 2; h8++) {
+  for (int h8 = 0; h8 < 4; h8++) {
     const int c0 = q0 + 8 * h8;
     uint32_t wh[4], wl[4], uh[4], ul[4];
 #pragma unroll
@@ -215,8 +244,8 @@ __device__ __forceinline__ void write_factors(BuildTcSmem &sm, bool s_half) {
       split_bf16(a1 * sm.bg[c0 + 2 * j + 1], h1, l1);
       wh[j] = pack2(h0, h1);
       wl[j] = pack2(l0, l1);
-      split_bf16(-a0 * sm.bt[c0 + 2 * j], h0, l0);
-      split_bf16(-a1 * sm.bt[c0 + 2 * j + 1], h1, l1);
+      split_bf16(a0 * sm.bt[c0 + 2 * j], h0, l0);
+      split_bf16(a1 * sm.bt[c0 + 2 * j + 1], h1, l1);
       uh[j] = pack2(h0, h1);
       ul[j] = pack2(l0, l1);
     }
@@ -230,15 +259,292 @@ __device__ __forceinline__ void write_factors(BuildTcSmem &sm, bool s_half) {
   }
 }
 
-// K (and, for the S half, V) of chunk `ch` of item `it` into input buffer b
-__device__ __forceinline__ void issue_chunk(BuildTcSmem &sm, const BuildItem &it, int ch, int b, bool s_half,
-                                            int kh, const CUtensorMap *tk, const CUtensorMap *tv) {
+// K (and, for the S half, V) of chunk `ch` of item `it`
+__device__ __forceinline__ void issue_chunk(BuildTcSmem &sm, const BuildItem &it, int ch, bool s_half, int kh,
+                                            const CUtensorMap *tk, const CUtensorMap *tv) {
   const int32_t t0 = (int32_t)(it.start + (int64_t)C * ch);
-  tc::mbar_expect_tx(&sm.full[b], s_half ? 32768u : 16384u);
-  for (int s = 0; s < 2; s++) tc::tma_load_3d(sm.in[b].k + s * 8192, tk, 64 * s, kh, t0, &sm.full[b]);
+  const int bk = ch % NBUF, bv = ch & 1;
+  tc::mbar_expect_tx(&sm.full[bk], s_half ? 32768u : 16384u);
+  for (int s = 0; s < 2; s++) tc::tma_load_3d(sm.kin[bk] + s * 8192, tk, 64 * s, kh, t0, &sm.full[bk]);
   if (s_half)
-    for (int s = 0; s < 2; s++) tc::tma_load_3d(sm.in[b].v + s * 8192, tv, 64 * s, it.head, t0, &sm.full[b]);
+    for (int s = 0; s < 2; s++) tc::tma_load_3d(sm.vin[bv] + s * 8192, tv, 64 * s, it.head, t0, &sm.full[bk]);
 }
+struct ItemCtx {
+  BuildItem it;
+  bool s_half;
+  int kh;
+  int n_ch;
+  uint32_t gch0;  // index of the item's first chunk in this CTA's chunk sequence
+};
+
+struct MmaIds {
+  uint32_t gram, wu, c1, c2;
+};
+
+// ---------------------------------------------------------------- P group
+// Prepares chunk ch: everything that depends on the inputs alone.  q is the
+// thread's index in the group (0..127).  Once-per-chunk barriers are waited
+// on with the phase of the chunk they belong to (global chunk index).
+__device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx &x, int ch, int q,
+                           uint32_t tm, const MmaIds &id, uint32_t LIM, uint32_t (&ph_full)[NBUF], float &g_cur,
+                           float &b_cur, const CUtensorMap *tk, const CUtensorMap *tv) {
+  const BuildItem &it = x.it;
+  const bool gdn = p.variant == HYPIC_GDN;
+  const uint32_t g = x.gch0 + (uint32_t)ch;  // global chunk index
+  const int bk = ch % NBUF, bv = ch & 1, b3 = (int)(g % 3);
+  const int64_t t0 = it.start + (int64_t)C * ch;
+  const int nt = (it.end - t0) < C ? (int)(it.end - t0) : C;
+  const int wp = q >> 5, lane = q & 31;
+  // gates of the next chunk, one chunk ahead
+  float g_nxt = 0.f, b_nxt = 0.f;
+  if (q < C && t0 + C + q < it.end) {
+    if (gdn) g_nxt = p.g[(t0 + C + q) * p.h_v + it.head];
+    b_nxt = p.beta[(t0 + C + q) * p.h_v + it.head];
+  }
+  // ---- inputs landed; ragged tail -> identity tokens (k = v = 0)
+  if (!tc::mbar_wait(&sm.full[bk], ph_full[bk] & 1, aborted(sm) ? DRAIN_LIMIT : LIM)) fail(sm, p);
+  ph_full[bk]++;
+  unsigned char *kin = sm.kin[bk], *vin = sm.vin[bv];
+  if (nt < C) {
+    for (int e = q; e < (C - nt) * 16; e += NG) {
+      const int r = nt + (e >> 4), s = (e >> 3) & 1, c16 = e & 7;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(kin + s * 8192 + r * 128 + c16 * 16) = z;
+      if (x.s_half) *reinterpret_cast<uint4 *>(vin + s * 8192 + r * 128 + c16 * 16) = z;
+    }
+  }
+  if (q < C) {
+    sm.bt[q] = b_cur;
+    sm.lam[q] = g_cur;
+  }
+  tc::named_bar(BAR_P, NG);
+  if (wp == 0) {  // lam_t = sum_{j<=t} g_j (two tokens per lane)
+    float x0 = sm.lam[lane], x1 = sm.lam[lane + 32];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+      const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+      if (lane >= o) {
+        x0 += y0;
+        x1 += y1;
+      }
+    }
+    x1 += __shfl_sync(0xffffffffu, x0, 31);
+    const float lc = __shfl_sync(0xffffffffu, x1, 31);
+    sm.lam[lane] = x0;
+    sm.lam[lane + 32] = x1;
+    sm.bg[lane] = sm.bt[lane] * __expf(x0);
+    sm.bg[lane + 32] = sm.bt[lane + 32] * __expf(x1);
+    sm.dec[b3][lane] = __expf(lc - x0);
+    sm.dec[b3][lane + 32] = __expf(lc - x1);
+    // factors of exp(lam_t - lam_i) = exp(lam_t - lam_0) exp(lam_0 - lam_i);
+    // in fp32 range when the chunk's log-gates sum above -80
+    const float l0 = __shfl_sync(0xffffffffu, x0, 0);
+    sm.ea[lane] = sm.bt[lane] * __expf(x0 - l0);
+    sm.ea[lane + 32] = sm.bt[lane + 32] * __expf(x1 - l0);
+    sm.eb[lane] = __expf(l0 - x0);
+    sm.eb[lane + 32] = __expf(l0 - x1);
+    if (lane == 0) {
+      sm.gc[b3] = __expf(lc);
+      sm.fact = (l0 - lc) <= 80.f;
+    }
+  }
+  tc::fence_proxy_async_smem();  // zeroed tail rows are MMA operands
+  tc::tc_fence_before();
+  tc::named_bar(BAR_P, NG);
+  // ---- Gram K K^T (K-major view; padded rows 64..127 are ignored)
+  if (q == 0) {
+    tc::tc_fence_after();
+    const uint32_t kb = tc::smem_u32(kin);
+#pragma unroll
+    for (int ks = 0; ks < 8; ks++)
+      tc::mma_ss_f16(tm + TM_G, kdesc16(kb, 16 * ks, 64), kdesc16(kb, 16 * ks, 64), id.gram, ks > 0);
+    tc::mma_commit(&sm.bar_g);
+  }
+  wait_phase(sm, p, &sm.bar_g, g, DRAIN_LIMIT);
+  tc::tc_fence_after();
+  // ---- M_ti = b_t exp(lam_t - lam_i) k_t.k_i (i < t): warps holding lanes 0..63
+  if (wp < 2) {
+    const int t = q;
+    const bool fact = sm.fact != 0;  // uniform over the chunk
+    const float lt = sm.lam[t], btt = sm.bt[t], eat = sm.ea[t];
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t r[32];
+      float li[32];
+      tc::tmem_ld32(trow(tm + TM_G, c0), r);
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {  // into registers before any store
+        const float4 l4 = *reinterpret_cast<const float4 *>(fact ? &sm.eb[c0 + j] : &sm.lam[c0 + j]);
+        li[j] = l4.x;
+        li[j + 1] = l4.y;
+        li[j + 2] = l4.z;
+        li[j + 3] = l4.w;
+      }
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; j++)
+        li[j] = (c0 + j < t) ? (fact ? eat * li[j] : btt * __expf(lt - li[j])) * __uint_as_float(r[j]) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4 *>(&sm.nm[t][c0 + j]) = make_float4(li[j], li[j + 1], li[j + 2], li[j + 3]);
+    }
+  }
+  tc::named_bar(BAR_P, NG);
+  ut_inverse(sm, q);
+  write_factors(sm, q, x.s_half);
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  tc::named_bar(BAR_P, NG);
+  // ---- W^T = K^T (A diag(bG))^T;  S half: U^T = V^T (A diag(b))^T once X
+  // has consumed the previous chunk's U
+  if (x.s_half && g > 0) wait_phase(sm, p, &sm.ys_done, g - 1, LIM);
+  if (q == 0) {
+    tc::tc_fence_after();
+    const uint32_t kb = tc::smem_u32(kin), vb = tc::smem_u32(vin);
+    const uint32_t wh = tc::smem_u32(sm.bwh), wl = tc::smem_u32(sm.bwl);
+    const uint32_t uh = tc::smem_u32(sm.buh), ul = tc::smem_u32(sm.bul);
+#pragma unroll
+    for (int ks = 0; ks < 4; ks++) {
+      tc::mma_ss_f16(tm + TM_W, mndesc16(kb, 16 * ks), kdesc16(wh, 16 * ks, 64), id.wu, ks > 0);
+      tc::mma_ss_f16(tm + TM_W, mndesc16(kb, 16 * ks), kdesc16(wl, 16 * ks, 64), id.wu, 1u);
+      if (x.s_half) {
+        tc::mma_ss_f16(tm + TM_U, mndesc16(vb, 16 * ks), kdesc16(uh, 16 * ks, 64), id.wu, ks > 0);
+        tc::mma_ss_f16(tm + TM_U, mndesc16(vb, 16 * ks), kdesc16(ul, 16 * ks, 64), id.wu, 1u);
+      }
+    }
+    tc::mma_commit(&sm.bar_wu);
+  }
+  wait_phase(sm, p, &sm.bar_wu, g, DRAIN_LIMIT);
+  tc::tc_fence_after();
+  // ---- stage W (tf32, rounded) as chain 1's B tile once chain 1 of the
+  // previous chunk is done with it (each warp writes whole row segments)
+  if (g > 0) wait_phase(sm, p, &sm.bar_y, g - 1, LIM);
+#pragma unroll
+  for (int c0 = 0; c0 < 64; c0 += 32) {
+    uint32_t r[32];
+    tc::tmem_ld32(trow(tm + TM_W, c0), r);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; j++)
+      *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, q, 64)) = tc::to_tf32(__uint_as_float(r[j]));
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  tc::named_bar(BAR_P, NG);
+  if (q == 0) {
+    // chunk ch + 2 goes to K buffer (ch + 2) % 3 = (ch - 1) % 3, free once X's
+    // chain 2 of chunk ch - 1 is done (waited before wt_ready, so the phase
+    // waited on is the latest one), and to V buffer ch % 2, whose U MMA above
+    // is complete
+    if (ch + 2 < x.n_ch) {
+      if (ch >= 1) wait_phase(sm, p, &sm.bar_x, g - 1, LIM);
+      if (!aborted(sm)) issue_chunk(sm, it, ch + 2, x.s_half, x.kh, tk, tv);
+    }
+    tc::mbar_arrive(&sm.wt_ready);
+  }
+  g_cur = g_nxt;
+  b_cur = b_nxt;
+}
+
+// ---------------------------------------------------------------- X group
+// Advances the state half through chunk ch (n = thread = TMEM lane).
+__device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx &x, int ch, int n, uint32_t tm,
+                            const MmaIds &id, uint32_t LIM) {
+  const uint32_t g = x.gch0 + (uint32_t)ch;
+  const int bk = ch % NBUF, b3 = (int)(g % 3);
+  wait_phase(sm, p, &sm.wt_ready, g, LIM);
+  tc::tc_fence_after();
+  // ---- X *= G_C (the accumulator; chain 1 reads the rounded copy)
+  {
+    const float gC = sm.gc[b3];
+#pragma unroll
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      uint32_t r[32];
+      tc::tmem_ld32(trow(tm + TM_X, c0), r);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; j++) r[j] = __float_as_uint(gC * __uint_as_float(r[j]));
+      tc::tmem_st32(trow(tm + TM_X, c0), r);
+    }
+    tc::tmem_wait_st();
+  }
+  tc::tc_fence_before();
+  tc::named_bar(BAR_X, NG);
+  // ---- chain 1: Y^T = X^T W^T
+  if (n == 0) {
+    tc::tc_fence_after();
+    const uint32_t wb = tc::smem_u32(sm.wt);
+#pragma unroll
+    for (int ks = 0; ks < 16; ks++)
+      tc::mma_ts_tf32(tm + TM_Y, tm + TM_XR + 8 * ks, kdesc32(wb, 8 * ks, 64), id.c1, ks > 0);
+    tc::mma_commit(&sm.bar_y);
+  }
+  wait_phase(sm, p, &sm.bar_y, g, DRAIN_LIMIT);
+  tc::tc_fence_after();
+  // ---- Ytilde = -(Y - [0 | U]) diag(exp(lam_C - lam_t)), split hi + lo, as
+  // the K-major A tiles [128 j x 64 t] of chain 2
+#pragma unroll
+  for (int c0 = 0; c0 < 64; c0 += 32) {
+    uint32_t r[32], u[32];
+    tc::tmem_ld32(trow(tm + TM_Y, c0), r);
+    if (x.s_half) tc::tmem_ld32(trow(tm + TM_U, c0), u);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int q8 = 0; q8 < 4; q8++) {
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const int jj = 8 * q8 + 2 * j, t = c0 + jj;
+        float y0 = __uint_as_float(r[jj]), y1 = __uint_as_float(r[jj + 1]);
+        if (x.s_half) {
+          y0 -= __uint_as_float(u[jj]);
+          y1 -= __uint_as_float(u[jj + 1]);
+        }
+        __nv_bfloat16 h0, l0, h1, l1;
+        split_bf16(-sm.dec[b3][t] * y0, h0, l0);
+        split_bf16(-sm.dec[b3][t + 1] * y1, h1, l1);
+        hw[j] = pack2(h0, h1);
+        lw[j] = pack2(l0, l1);
+      }
+      const uint32_t off = sw16(n, c0 + 8 * q8, 128);
+      *reinterpret_cast<uint4 *>(sm.yh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4 *>(sm.yl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  tc::named_bar(BAR_X, NG);
+  // ---- chain 2: X^T += Ytilde^T K  (B = this chunk's K tile, MN-major);
+  // U of this chunk is consumed: P may overwrite it
+  if (n == 0) {
+    tc::mbar_arrive(&sm.ys_done);
+    tc::tc_fence_after();
+    const uint32_t kb = tc::smem_u32(sm.kin[bk]), yhb = tc::smem_u32(sm.yh), ylb = tc::smem_u32(sm.yl);
+#pragma unroll
+    for (int ks = 0; ks < 4; ks++) {
+      tc::mma_ss_f16(tm + TM_X, kdesc16(yhb, 16 * ks, 128), mndesc16(kb, 16 * ks), id.c2, 1u);
+      tc::mma_ss_f16(tm + TM_X, kdesc16(ylb, 16 * ks, 128), mndesc16(kb, 16 * ks), id.c2, 1u);
+    }
+    tc::mma_commit(&sm.bar_x);
+  }
+  wait_phase(sm, p, &sm.bar_x, g, DRAIN_LIMIT);
+  tc::tc_fence_after();
+  // ---- rounded copy of the new X for the next chunk's chain 1
+#pragma unroll
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    uint32_t r[32];
+    tc::tmem_ld32(trow(tm + TM_X, c0), r);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; j++) r[j] = tc::to_tf32(__uint_as_float(r[j]));
+    tc::tmem_st32(trow(tm + TM_XR, c0), r);
+  }
+  tc::tmem_wait_st();
+  tc::tc_fence_before();
+  tc::named_bar(BAR_X, NG);
+}
+
 __global__ void __launch_bounds__(NT, 1)
     build_tc_kernel(const __grid_constant__ BuildTcArgs args, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v) {
@@ -248,18 +554,18 @@ __global__ void __launch_bounds__(NT, 1)
   BuildTcSmem &sm = *reinterpret_cast<BuildTcSmem *>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   const BuildParams &p = args.p;
   const uint32_t LIM = args.wait_limit;
-  const int n = threadIdx.x, warp = n >> 5, lane = n & 31;
-  const int lj = 32 * (warp & 3) + lane;  // TMEM lane of this thread
-  const int hsel = warp >> 2;             // which half of the TMEM columns it handles
-  const bool gdn = p.variant == HYPIC_GDN;
+  const int n = threadIdx.x, warp = n >> 5;
+  const bool is_p = warp >= 4;
+  const int q = n - NG;  // index inside the P group
 
   if (n == 0) {
-    tc::mbar_init(&sm.full[0], 1);
-    tc::mbar_init(&sm.full[1], 1);
+    for (int b = 0; b < NBUF; b++) tc::mbar_init(&sm.full[b], 1);
     tc::mbar_init(&sm.bar_g, 1);
-    tc::mbar_init(&sm.bar_w, 1);
+    tc::mbar_init(&sm.bar_wu, 1);
     tc::mbar_init(&sm.bar_y, 1);
     tc::mbar_init(&sm.bar_x, 1);
+    tc::mbar_init(&sm.wt_ready, 1);
+    tc::mbar_init(&sm.ys_done, 1);
     tc::mbar_init(&sm.never, 1);
     sm.abort = 0;
     tc::fence_mbar_init();
@@ -276,11 +582,13 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t tm = sm.tmem_base;
   if (args.debug_stall && !tc::mbar_wait(&sm.never, 0, LIM)) fail(sm, p);
 
-  const uint32_t id_gram = tc::idesc(tc::FMT_BF16, 128, 64);
-  const uint32_t id_wu = tc::idesc(tc::FMT_BF16, 128, 64, false, false, /*a_mn=*/true, false);
-  const uint32_t id_c1 = tc::idesc(tc::FMT_TF32, 128, 64);
-  const uint32_t id_c2 = tc::idesc(tc::FMT_BF16, 128, 128, false, false, false, /*b_mn=*/true);
-  uint32_t ph_full[2] = {0, 0}, ph_g = 0, ph_w = 0, ph_y = 0, ph_x = 0;
+  MmaIds id;
+  id.gram = tc::idesc(tc::FMT_BF16, 128, 64);
+  id.wu = tc::idesc(tc::FMT_BF16, 128, 64, false, false, /*a_mn=*/true, false);
+  id.c1 = tc::idesc(tc::FMT_TF32, 128, 64);
+  id.c2 = tc::idesc(tc::FMT_BF16, 128, 128, false, false, false, /*b_mn=*/true);
+  uint32_t ph_full[NBUF] = {0, 0, 0};
+  uint32_t gch = 0;  // chunks processed by this CTA so far
   const int n_items = p.plan->n_items;
 
   for (;;) {
@@ -289,249 +597,56 @@ __global__ void __launch_bounds__(NT, 1)
     const int idx = sm.item;
     __syncthreads();
     if (idx >= n_items) break;
-    const BuildItem it = p.items[idx];
-    const bool s_half = it.part == 1;
-    const int h = it.head;
-    const int kh = (int)(((int64_t)h * p.h_k) / p.h_v);
-    const int64_t L = it.end - it.start;
-    const int n_ch = (int)((L + C - 1) / C);
+    ItemCtx x;
+    x.it = p.items[idx];
+    x.s_half = x.it.part == 1;
+    x.kh = (int)(((int64_t)x.it.head * p.h_k) / p.h_v);
+    x.n_ch = (int)((x.it.end - x.it.start + C - 1) / C);
+    x.gch0 = gch;
 
-    // X^T half := T half: identity, S half: zero (accumulator and rounded copy)
+    if (is_p) {
+      if (q == 0)  // chunks 0 and 1; chunk c + 2 is issued at the end of prep(c)
+        for (int ch = 0; ch < 2 && ch < x.n_ch; ch++) issue_chunk(sm, x.it, ch, x.s_half, x.kh, &tmap_k, &tmap_v);
+      float g_cur = 0.f, b_cur = 0.f;
+      if (q < C && x.it.start + q < x.it.end) {
+        if (p.variant == HYPIC_GDN) g_cur = p.g[(x.it.start + q) * p.h_v + x.it.head];
+        b_cur = p.beta[(x.it.start + q) * p.h_v + x.it.head];
+      }
+      for (int ch = 0; ch < x.n_ch; ch++)
+        prep_chunk(sm, p, x, ch, q, tm, id, LIM, ph_full, g_cur, b_cur, &tmap_k, &tmap_v);
+    } else {
+      // X^T half := T half: identity, S half: zero (accumulator and rounded copy)
 #pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 32) {
-      const int col = 64 * hsel + c0;
-      uint32_t r[32];
-#pragma unroll
-      for (int j = 0; j < 32; j++) r[j] = (!s_half && col + j == lj) ? 0x3f800000u : 0u;
-      tc::tmem_st32(trow(tm + TM_X, col), r);
-      tc::tmem_st32(trow(tm + TM_XR, col), r);
-    }
-    tc::tmem_wait_st();
-    if (n == 0)
-      for (int ch = 0; ch < 2 && ch < n_ch; ch++) issue_chunk(sm, it, ch, ch & 1, s_half, kh, &tmap_k, &tmap_v);
-    float g_cur = 0.f, b_cur = 0.f;
-    if (n < C && n < L) {
-      if (gdn) g_cur = p.g[(it.start + n) * p.h_v + h];
-      b_cur = p.beta[(it.start + n) * p.h_v + h];
-    }
-
-    for (int ch = 0; ch < n_ch; ch++) {
-      const int b = ch & 1;
-      const int64_t t0 = it.start + (int64_t)C * ch;
-      const int nt = (it.end - t0) < C ? (int)(it.end - t0) : C;
-      float g_nxt = 0.f, b_nxt = 0.f;  // gates of the next chunk, one chunk ahead
-      if (n < C && t0 + C + n < it.end) {
-        if (gdn) g_nxt = p.g[(t0 + C + n) * p.h_v + h];
-        b_nxt = p.beta[(t0 + C + n) * p.h_v + h];
-      }
-      // ---- A: inputs landed (once aborted: wait with the drain limit, the copy lands)
-      if (!tc::mbar_wait(&sm.full[b], ph_full[b] & 1, aborted(sm) ? DRAIN_LIMIT : LIM)) fail(sm, p);
-      ph_full[b]++;
-      unsigned char *kin = sm.in[b].k, *vin = sm.in[b].v;
-      if (nt < C) {  // ragged tail: identity tokens (k = v = 0; their gates and beta are 0)
-        for (int e = n; e < (C - nt) * 16; e += NT) {
-          const int r = nt + (e >> 4), q = e & 15;  // 16 x 16 B per row: 8 per slab
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4 *>(kin + (q >> 3) * 8192 + r * 128 + (q & 7) * 16) = z;
-          if (s_half) *reinterpret_cast<uint4 *>(vin + (q >> 3) * 8192 + r * 128 + (q & 7) * 16) = z;
-        }
-      }
-      if (n < C) {
-        sm.bt[n] = b_cur;
-        sm.lam[n] = g_cur;
-      }
-      __syncthreads();
-      if (warp == 0) {  // lam_t = sum_{j<=t} g_j (two tokens per lane)
-        float x0 = sm.lam[lane], x1 = sm.lam[lane + 32];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
-          const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-          if (lane >= o) {
-            x0 += y0;
-            x1 += y1;
-          }
-        }
-        x1 += __shfl_sync(0xffffffffu, x0, 31);
-        const float lc = __shfl_sync(0xffffffffu, x1, 31);
-        sm.lam[lane] = x0;
-        sm.lam[lane + 32] = x1;
-        sm.bg[lane] = sm.bt[lane] * __expf(x0);
-        sm.bg[lane + 32] = sm.bt[lane + 32] * __expf(x1);
-        sm.dec[lane] = __expf(lc - x0);
-        sm.dec[lane + 32] = __expf(lc - x1);
-        if (lane == 0) sm.gC = __expf(lc);
-      }
-      tc::fence_proxy_async_smem();  // zeroed tail rows are MMA operands
-      tc::tc_fence_before();
-      __syncthreads();
-
-      // ---- B: Gram K K^T (K-major view of the K tile; rows 64..127 of the
-      // padded M read the adjacent tiles and are ignored)
-      if (n == 0) {
-        tc::tc_fence_after();
-        const uint32_t kb = tc::smem_u32(kin);
-#pragma unroll
-        for (int ks = 0; ks < 8; ks++)
-          tc::mma_ss_f16(tm + TM_G, kdesc16(kb, 16 * ks, 64), kdesc16(kb, 16 * ks, 64), id_gram, ks > 0);
-        tc::mma_commit(&sm.bar_g);
-      }
-      wait_mma(sm, p, &sm.bar_g, ph_g);
-      // ---- C: M_ti = b_t exp(lam_t - lam_i) k_t.k_i (i < t): warps 0, 1, 4, 5
-      if ((warp & 3) < 2) {
-        const int t = lj, c0 = 32 * hsel;
+      for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t r[32];
-        tc::tmem_ld32(trow(tm + TM_G, c0), r);
-        tc::tmem_wait_ld();
-        const float lt = sm.lam[t], btt = sm.bt[t];
 #pragma unroll
-        for (int j = 0; j < 32; j++) {
-          const int i = c0 + j;
-          sm.nm[t][i] = (i < t) ? btt * __expf(lt - sm.lam[i]) * __uint_as_float(r[j]) : 0.f;
-        }
-      }
-      __syncthreads();
-      ut_inverse(sm);
-      write_factors(sm, s_half);
-      tc::fence_proxy_async_smem();
-      __syncthreads();
-
-      // ---- D: W^T = K^T (A diag(bG))^T;  S half: Y^T := V^T (-A diag(b))^T = -U^T
-      if (n == 0) {
-        tc::tc_fence_after();
-        const uint32_t kb = tc::smem_u32(kin), vb = tc::smem_u32(vin);
-        const uint32_t wh = tc::smem_u32(sm.bwh), wl = tc::smem_u32(sm.bwl);
-        const uint32_t uh = tc::smem_u32(sm.buh), ul = tc::smem_u32(sm.bul);
-#pragma unroll
-        for (int ks = 0; ks < 4; ks++) {
-          tc::mma_ss_f16(tm + TM_W, mndesc16(kb, 16 * ks), kdesc16(wh, 16 * ks, 64), id_wu, ks > 0);
-          tc::mma_ss_f16(tm + TM_W, mndesc16(kb, 16 * ks), kdesc16(wl, 16 * ks, 64), id_wu, 1u);
-          if (s_half) {
-            tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(uh, 16 * ks, 64), id_wu, ks > 0);
-            tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(ul, 16 * ks, 64), id_wu, 1u);
-          }
-        }
-        tc::mma_commit(&sm.bar_w);
-      }
-      wait_mma(sm, p, &sm.bar_w, ph_w);
-
-      // ---- E: W (tf32, rounded) as the K-major B tile [64 t x 128 d] of
-      // chain 1 (each warp writes whole 128-byte row segments); X scaled by G_C
-      {
-        const int c0 = 32 * hsel;  // tokens c0 .. c0 + 31 of column d = lj
-        uint32_t r[32];
-        tc::tmem_ld32(trow(tm + TM_W, c0), r);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; j++) *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, lj, 64)) = tc::to_tf32(__uint_as_float(r[j]));
-        const float gC = sm.gC;
-#pragma unroll
-        for (int cc = 0; cc < 64; cc += 32) {
-          const int col = 64 * hsel + cc;
-          tc::tmem_ld32(trow(tm + TM_X, col), r);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; j++) r[j] = __float_as_uint(gC * __uint_as_float(r[j]));
-          tc::tmem_st32(trow(tm + TM_X, col), r);
-        }
-        tc::tmem_wait_st();
-      }
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_before();
-      __syncthreads();
-
-      // ---- F: chain 1, Y^T (+)= X^T W^T  (the S half accumulates onto -U^T)
-      if (n == 0) {
-        tc::tc_fence_after();
-        const uint32_t wb = tc::smem_u32(sm.wt);
-#pragma unroll
-        for (int ks = 0; ks < 16; ks++)
-          tc::mma_ts_tf32(tm + TM_Y, tm + TM_XR + 8 * ks, kdesc32(wb, 8 * ks, 64), id_c1, (s_half || ks > 0) ? 1u : 0u);
-        tc::mma_commit(&sm.bar_y);
-      }
-      wait_mma(sm, p, &sm.bar_y, ph_y);
-
-      // ---- G: Ytilde = -Y diag(exp(lam_C - lam_t)), split hi + lo, as the
-      // K-major A tiles [128 j x 64 t] of chain 2
-      {
-        const int c0 = 32 * hsel;
-        uint32_t r[32];
-        tc::tmem_ld32(trow(tm + TM_Y, c0), r);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int q8 = 0; q8 < 4; q8++) {
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int j = 0; j < 4; j++) {
-            const int t = c0 + 8 * q8 + 2 * j;
-            __nv_bfloat16 h0, l0, h1, l1;
-            split_bf16(-sm.dec[t] * __uint_as_float(r[8 * q8 + 2 * j]), h0, l0);
-            split_bf16(-sm.dec[t + 1] * __uint_as_float(r[8 * q8 + 2 * j + 1]), h1, l1);
-            hw[j] = pack2(h0, h1);
-            lw[j] = pack2(l0, l1);
-          }
-          const uint32_t off = sw16(lj, c0 + 8 * q8, 128);
-          *reinterpret_cast<uint4 *>(sm.yh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4 *>(sm.yl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_before();
-      __syncthreads();
-
-      // ---- H: chain 2, X^T += Ytilde^T K  (B = K tile, MN-major view)
-      if (n == 0) {
-        tc::tc_fence_after();
-        const uint32_t kb = tc::smem_u32(kin), yhb = tc::smem_u32(sm.yh), ylb = tc::smem_u32(sm.yl);
-#pragma unroll
-        for (int ks = 0; ks < 4; ks++) {
-          tc::mma_ss_f16(tm + TM_X, kdesc16(yhb, 16 * ks, 128), mndesc16(kb, 16 * ks), id_c2, 1u);
-          tc::mma_ss_f16(tm + TM_X, kdesc16(ylb, 16 * ks, 128), mndesc16(kb, 16 * ks), id_c2, 1u);
-        }
-        tc::mma_commit(&sm.bar_x);
-      }
-      wait_mma(sm, p, &sm.bar_x, ph_x);
-
-      // ---- I: rounded copy of X for the next chunk; this input buffer is
-      // now consumed by every MMA: refill it with chunk ch + 2
-#pragma unroll
-      for (int cc = 0; cc < 64; cc += 32) {
-        const int col = 64 * hsel + cc;
-        uint32_t r[32];
-        tc::tmem_ld32(trow(tm + TM_X, col), r);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; j++) r[j] = tc::to_tf32(__uint_as_float(r[j]));
-        tc::tmem_st32(trow(tm + TM_XR, col), r);
+        for (int j = 0; j < 32; j++) r[j] = (!x.s_half && c0 + j == n) ? 0x3f800000u : 0u;
+        tc::tmem_st32(trow(tm + TM_X, c0), r);
+        tc::tmem_st32(trow(tm + TM_XR, c0), r);
       }
       tc::tmem_wait_st();
-      if (n == 0 && ch + 2 < n_ch && !aborted(sm)) issue_chunk(sm, it, ch + 2, b, s_half, kh, &tmap_k, &tmap_v);
       tc::tc_fence_before();
-      __syncthreads();
-      g_cur = g_nxt;
-      b_cur = b_nxt;
-    }
-
-    // ---- epilogue: lane lj holds column lj of its half of [T | S]
-    {
-      const int64_t sh = (int64_t)it.slot * p.h_v + h;
-      float *out = (s_half ? p.S_pool : p.T_pool) + sh * 128 * 128 + lj;
+      tc::named_bar(BAR_X, NG);
+      for (int ch = 0; ch < x.n_ch; ch++) chain_chunk(sm, p, x, ch, n, tm, id, LIM);
+      // epilogue: lane n holds column n of its half of [T | S]
+      const int64_t sh = (int64_t)x.it.slot * p.h_v + x.it.head;
+      float *out = (x.s_half ? p.S_pool : p.T_pool) + sh * 128 * 128 + n;
       bool bad = false;
 #pragma unroll
-      for (int cc = 0; cc < 64; cc += 32) {
-        const int col = 64 * hsel + cc;
+      for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t r[32];
-        tc::tmem_ld32(trow(tm + TM_X, col), r);
+        tc::tmem_ld32(trow(tm + TM_X, c0), r);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; j++) {
-          const float x = __uint_as_float(r[j]);
-          out[(int64_t)(col + j) * 128] = x;
-          bad |= !finite_f(x);
+          const float v = __uint_as_float(r[j]);
+          out[(int64_t)(c0 + j) * 128] = v;
+          bad |= !finite_f(v);
         }
       }
       if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
     }
+    gch += (uint32_t)x.n_ch;
     tc::tc_fence_before();
     __syncthreads();
   }

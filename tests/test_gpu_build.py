@@ -1,0 +1,72 @@
+"""GPU tests of the tensor-core chunkwise build (GDN / DeltaNet, bf16,
+d = 128): many items of every chunk count (exercising the hand-off between
+the two warp groups across item boundaries), bitwise determinism, and the
+bounded-wait timeout."""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as si
+from gpu_common import compare_pairs, gpu_build, oracle_pairs
+from tolerance import TOL_BF16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import __graft_entry__ as g
+    g.build()
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet"])
+def test_build_tc_many_lengths(variant):
+    lens = [1, 2, 63, 64, 65, 127, 128, 129, 200, 257, 511, 1000, 8, 9, 16, 300]
+    W = si.workload(5, device=DEV, variant=variant, lengths=lens, h_k=2, h_v=4, seam_w=8)
+    T_pool, S_pool = gpu_build(W)
+    T, S = oracle_pairs(W)
+    eT, eS = compare_pairs(W, T_pool, S_pool, T, S, range(W.n_seg))
+    assert eT <= TOL_BF16 and eS <= TOL_BF16, (eT, eS)
+
+
+def test_build_tc_bitwise_deterministic():
+    W = si.workload(3, device=DEV, n_seg=6, seg_len=700)
+    a = [x.clone() for x in gpu_build(W)]
+    b = gpu_build(W)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+_TIMEOUT_CHILD = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + '/tests')
+import synth_inputs as si
+import hybrid_linear_attention_chunkwise_gb300 as hy
+from gpu_common import gpu_build
+W = si.workload(5, device='cuda', variant='gdn', lengths=[100, 300], h_k=1, h_v=2, seam_w=0)
+status = torch.zeros(1, dtype=torch.int32, device='cuda')
+gpu_build(W, status=status)
+torch.cuda.synchronize()
+code = hy.status_from_word(int(status.item()))
+x = torch.ones(4, device='cuda').sum().item()   # the context is still usable
+print('STATUS', code, 'CTX', x)
+"""
+
+
+def test_build_tc_bounded_wait_reports_timeout():
+    """Every CTA first waits on an mbarrier that nothing signals, with a short
+    poll limit: the wait runs out, HYPIC_ERR_TIMEOUT comes back through the
+    status word, the kernel returns and the context stays usable."""
+    env = dict(os.environ, HYPIC_DEBUG_WAIT_LIMIT="2000", HYPIC_DEBUG_STALL="1")
+    r = subprocess.run([sys.executable, "-c", _TIMEOUT_CHILD, ROOT], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("STATUS")][-1]
+    assert line.split()[1] == "5" and line.split()[3] == "4.0", line
