@@ -59,7 +59,7 @@ class ComposeDesc(ctypes.Structure):
                 ("workspace", P), ("workspace_bytes", ctypes.c_size_t), ("status", P)]
 
 
-SYMBOLS = ("hypic_segment_build", "hypic_build_workspace_bytes", "hypic_compose",
+SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_workspace_bytes", "hypic_compose",
            "hypic_compose_workspace_bytes", "hypic_plan_lpt", "hypic_status_from_word",
            "hypic_status_string", "hypic_version")
 
@@ -84,6 +84,8 @@ def load():
             lib = ctypes.CDLL(_LIB_PATH)
             lib.hypic_segment_build.argtypes = [ctypes.POINTER(BuildDesc), P]
             lib.hypic_segment_build.restype = ctypes.c_int
+            lib.hypic_segment_build_noalloc.argtypes = [ctypes.POINTER(BuildDesc), P]
+            lib.hypic_segment_build_noalloc.restype = ctypes.c_int
             lib.hypic_build_workspace_bytes.argtypes = [ctypes.POINTER(BuildDesc)]
             lib.hypic_build_workspace_bytes.restype = ctypes.c_size_t
             lib.hypic_compose.argtypes = [ctypes.POINTER(ComposeDesc), P]
@@ -212,6 +214,24 @@ def segment_build(k, v, g, beta, seg_offsets, *, variant: str, seam_w: int, T_po
     if rc != OK:
         raise HypicError(rc, "hypic_segment_build")
     return workspace
+
+
+NOALLOC_MAX_PAIRS = 16383  # HYPIC_NOALLOC_MAX_PAIRS
+
+
+def segment_build_noalloc(k, v, g, beta, seg_offsets, *, variant: str, seam_w: int, T_pool, S_pool,
+                          slot_of_seg=None, status=None, flags: int = 0, stream=None):
+    """hypic_segment_build_noalloc on torch tensors: the same build with its
+    plan in the library's fixed device scratch (no workspace, no allocation).
+    At most NOALLOC_MAX_PAIRS (segment, value head) pairs; calls that overlap
+    on the GPU race on the shared scratch."""
+    lib = load()
+    d, keep = _build_desc(k, v, g, beta, seg_offsets, variant, seam_w, T_pool, S_pool, slot_of_seg,
+                          None, status, flags)
+    rc = lib.hypic_segment_build_noalloc(ctypes.byref(d), _stream(stream))
+    del keep
+    if rc != OK:
+        raise HypicError(rc, "hypic_segment_build_noalloc")
 
 
 def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str,

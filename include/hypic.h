@@ -135,6 +135,29 @@ size_t hypic_build_workspace_bytes(const hypic_build_desc *d);
 int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream);
 
 /*
+ * hypic_segment_build_noalloc -- hypic_segment_build for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is a
+ * deployment variant of the same build, with the same results bit for bit.
+ *
+ * d->workspace and d->workspace_bytes are ignored.  The work plan goes to a
+ * fixed device array of HYPIC_NOALLOC_SCRATCH_BYTES (1 MiB) inside the
+ * library; its address is looked up once per device.  The call allocates no
+ * device or heap memory (no cudaMalloc / cudaFree).
+ *
+ * Limit: n_seg * h_v <= HYPIC_NOALLOC_MAX_PAIRS; a larger problem returns
+ * HYPIC_ERR_WORKSPACE before any CUDA call and launches nothing.
+ *
+ * Every call in the process shares the one array.  Calls ordered on the GPU
+ * (one stream, or ordered by events) are safe; calls that overlap on the GPU
+ * race on the array and give undefined results.  Host calls are serialised
+ * by a lock.  The dynamic work counter is reset to zero by the plan copy that
+ * opens each call.
+ */
+#define HYPIC_NOALLOC_SCRATCH_BYTES 1048576
+#define HYPIC_NOALLOC_MAX_PAIRS 16383
+int hypic_segment_build_noalloc(const hypic_build_desc *d, hypic_stream_t stream);
+
+/*
  * hypic_compose -- rebuild the running state of every (layer, value head)
  * from cached pairs in prompt order (pages §2.1 composition rule, §2.2 seam):
  *   S <- S_init (or 0)
