@@ -29,6 +29,8 @@
 // Every wait is bounded: one that runs out sets HYPIC_STATUS_TIMEOUT; the CTA
 // then skips its remaining work (control flow stays uniform across threads),
 // waits for the copies it issued and releases its TMEM.
+#include <cstddef>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -76,9 +78,11 @@ struct TcArgs {
   int debug_stall;  // wait first on a barrier nothing signals (timeout test)
 };
 
-__device__ __forceinline__ bool aborted(ComposeTcSmem &sm) { return *(volatile int *)&sm.abort != 0; }
+template <class SM>
+__device__ __forceinline__ bool aborted(SM &sm) { return *(volatile int *)&sm.abort != 0; }
 
-__device__ __forceinline__ void fail(ComposeTcSmem &sm, const ComposeParams &p) {
+template <class SM>
+__device__ __forceinline__ void fail(SM &sm, const ComposeParams &p) {
   *(volatile int *)&sm.abort = 1;
   report(p.status, HYPIC_STATUS_TIMEOUT);
 }
@@ -109,8 +113,9 @@ __device__ __forceinline__ int pair_slot(const ComposeParams &p, const Chain &c,
 }
 
 // T_C K-slab r (pair r/4, columns 32*(r%4) .. +32) into ring slot r % NSLOT
-__device__ __forceinline__ void issue_slab(ComposeTcSmem &sm, const ComposeParams &p, const Chain &c,
-                                           const CUtensorMap *tmap, uint32_t r) {
+template <class SM>
+__device__ __forceinline__ void issue_slab(SM &sm, const ComposeParams &p, const Chain &c, const CUtensorMap *tmap,
+                                           uint32_t r) {
   if (r >= 4u * (uint32_t)c.n_seg) return;
   const int seg = (int)(r / 4), j = (int)(r % 4);
   int slot = pair_slot(p, c, seg);
@@ -152,6 +157,16 @@ __device__ __forceinline__ void prefetch_pair_S(const ComposeParams &p, const Ch
   const int slot = pair_slot(p, c, seg);
   if (slot < 0) return;
   prefetch_l2(p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128, 128 * 128 * 4);
+}
+
+// both halves of segment seg's pair (T_C and S(C|0), 64 KiB each) into L2
+__device__ __forceinline__ void prefetch_pair(const ComposeParams &p, const Chain &c, int seg) {
+  if (seg >= c.n_seg) return;
+  const int slot = pair_slot(p, c, seg);
+  if (slot < 0) return;
+  const int64_t off = ((int64_t)slot * p.h_v + c.h) * 128 * 128;
+  prefetch_l2(p.T_pool + off, 128 * 128 * 4);
+  prefetch_l2(p.S_pool + off, 128 * 128 * 4);
 }
 
 // VAR: HYPIC_GDN, HYPIC_DELTANET or HYPIC_CHANNEL_DELTA
@@ -392,6 +407,569 @@ __global__ void __launch_bounds__(NT, 2)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Scalar-gate variants (GDN, DeltaNet): the seam tokens on the tensor cores.
+//
+// For a group of nt <= 8 seam tokens entered with state S0, cumulative
+// log-gates lam_t = g_0 + ... + g_t (DeltaNet: 0) and c_t = b_t (v_t - xh_t),
+// the token updates S_t = a_t S_{t-1} + k_t c_t^T (the GDN rule
+// a (I - b k k^T) S + b k v^T written per column) unroll to
+//   S_t  = e^{lam_t} S0 + sum_{i<=t} e^{lam_t - lam_i} k_i c_i^T
+//   xh_t = a_t k_t^T S_{t-1} = e^{lam_t} k_t^T S0 + sum_{i<t} e^{lam_t-lam_i} (k_t.k_i) c_i
+//   o_t  = q_t^T S_t         = e^{lam_t} q_t^T S0 + sum_{i<=t} e^{lam_t-lam_i} (q_t.k_i) c_i
+// so one MMA gives k_t^T S0 and q_t^T S0 for the 8 tokens and all 128
+// columns (D = S0^T [K;Q]^T: M = 128, N = 16, A = S0 in TMEM), and what
+// remains per column is an 8-step scalar recurrence.  For the last group of a
+// segment the state never has to be formed: with S0 the state entering it,
+//   T_C S_n + S(C|0) = e^{lam_last} (T_C S0 + sum_i (T_C k_i) e^{-lam_i} c_i^T) + S(C|0)
+// so the same MMA round also gives T_C k_i (A = the T_C K-slabs), the T_C S0
+// product starts at once from the same TMEM operand, and the rank-8 seam term
+// is accumulated onto it by one more MMA (K = 8) from two 128 x 8 tiles.
+// Earlier groups of a long seam window, a group whose decay underflows and a
+// skipped pair update S in registers instead.  The decayed Gram terms and
+// the [K;Q] operand tile depend on the seam tokens only: the group that opens
+// segment s+1 is prepared while the T_C S product of segment s runs.
+// ---------------------------------------------------------------------------
+constexpr int GW = 8;  // seam tokens per group
+
+struct SeamRaw {
+  __nv_bfloat16 k[GW][128];
+  __nv_bfloat16 q[GW][128];
+  __nv_bfloat16 v[GW][128];
+};
+
+struct __align__(1024) SeamMmaSmem {
+  unsigned char slot[NSLOT][SLAB];  // T_C K-slab ring (swizzled TMA tiles)
+  float bt[4][16][32];              // [K;Q] operand: tf32, K-major, 128-byte swizzle, 4 K-slabs
+  float tk[128][GW];                // (T_C k_i)[r]: tf32, K-major, 32-byte swizzle
+  float cp[128][GW];                // e^{-lam_i} c_i[n]: tf32, K-major, 32-byte swizzle
+  SeamRaw raw[2];                   // seam k / q / v rows of a group (bulk copies)
+  float gk[GW][GW];                 // e^{lam_t - lam_i} (k_t.k_i), i < t
+  float gq[GW][GW];                 // e^{lam_t - lam_i} (q_t.k_i), i <= t
+  float ea[GW];                     // e^{lam_t}
+  float eb[GW];                     // e^{lam_last - lam_i}
+  float en[GW];                     // e^{-lam_i}
+  float beta[GW];
+  float glog[GW];
+  float alast;                      // e^{lam_last}
+  uint64_t full[NSLOT];
+  uint64_t raw_full[2];
+  uint64_t mma_done;
+  uint64_t never;
+  uint32_t tmem_base;
+  int abort;
+  int stop;
+};
+static_assert(offsetof(SeamMmaSmem, bt) % 1024 == 0, "B tile must sit on a swizzle atom");
+static_assert(offsetof(SeamMmaSmem, tk) % 1024 == 0 && offsetof(SeamMmaSmem, cp) % 1024 == 0,
+              "32-byte swizzled tiles must sit on a swizzle atom");
+
+// a 32-byte row (8 tf32) of a K-major tile with 32-byte swizzle: the two
+// 16-byte halves trade places in rows whose index has bit 2 set
+__device__ __forceinline__ void store_row_sw32(float (*tile)[GW], int row, const float (&v)[GW]) {
+  const int sw = (row >> 2) & 1;
+  float4 *dst = reinterpret_cast<float4 *>(&tile[row][0]);
+  dst[sw] = make_float4(__uint_as_float(tc::to_tf32(v[0])), __uint_as_float(tc::to_tf32(v[1])),
+                        __uint_as_float(tc::to_tf32(v[2])), __uint_as_float(tc::to_tf32(v[3])));
+  dst[sw ^ 1] = make_float4(__uint_as_float(tc::to_tf32(v[4])), __uint_as_float(tc::to_tf32(v[5])),
+                            __uint_as_float(tc::to_tf32(v[6])), __uint_as_float(tc::to_tf32(v[7])));
+}
+
+struct SeamGroup {
+  int64_t tok0;  // first seam token of the group in [L, n_seg, w] order
+  int nt;        // real tokens in the group
+};
+
+__device__ __forceinline__ SeamGroup seam_group(const ComposeParams &p, const Chain &c, int gq) {
+  const int seg = gq / c.groups, gi = gq % c.groups;
+  SeamGroup g;
+  g.tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + gi * GW;
+  g.nt = min(GW, c.w - gi * GW);
+  return g;
+}
+
+// bulk copies of a group's k / q / v rows; the group's beta and gate rows
+// (all heads, contiguous) are warmed in L2 for the plain loads of the prep
+template <bool GDN>
+__device__ __forceinline__ void issue_raw(SeamMmaSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
+  if (gq >= c.n_seg * c.groups) return;
+  const SeamGroup sg = seam_group(p, c, gq);
+  const int b = gq & 1;
+  SeamRaw &r = sm.raw[b];
+  tc::mbar_expect_tx(&sm.raw_full[b], (uint32_t)sg.nt * 3 * 256);
+  const __nv_bfloat16 *sk = static_cast<const __nv_bfloat16 *>(p.seam_k);
+  const __nv_bfloat16 *sqp = static_cast<const __nv_bfloat16 *>(p.seam_q);
+  const __nv_bfloat16 *sv = static_cast<const __nv_bfloat16 *>(p.seam_v);
+  for (int t = 0; t < sg.nt; t++) {
+    tc::bulk_load(r.k[t], sk + ((sg.tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.raw_full[b]);
+    tc::bulk_load(r.q[t], sqp + ((sg.tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.raw_full[b]);
+    tc::bulk_load(r.v[t], sv + ((sg.tok0 + t) * p.h_v + c.h) * 128, 256, &sm.raw_full[b]);
+  }
+  const uint32_t gbytes = (uint32_t)(sg.nt * p.h_v * 4);
+  prefetch_l2(p.seam_beta + sg.tok0 * p.h_v, gbytes);
+  if (GDN) prefetch_l2(p.seam_g + sg.tok0 * p.h_v, gbytes);
+}
+
+// register select of lam[u] for a run-time u (keeps lam[] in registers)
+__device__ __forceinline__ float pick(const float (&lam)[GW], int u) {
+  float r = 0.f;
+#pragma unroll
+  for (int j = 0; j < GW; j++) r = (j == u) ? lam[j] : r;
+  return r;
+}
+
+// State-independent preparation of group gq (all threads; its raw buffer has
+// landed).  Threads n < GW pass beta and the log-gate of the group's token n
+// (loaded one group ahead; zero past nt).  Leaves v_t[n] in vv; the raw
+// buffer is free afterwards.
+__device__ __forceinline__ void prep_group(SeamMmaSmem &sm, const ComposeParams &p, const Chain &c, int gq,
+                                           float b_n, float g_n, float (&vv)[GW]) {
+  const int n = threadIdx.x;
+  const SeamGroup sg = seam_group(p, c, gq);
+  const int nt = sg.nt;
+  const SeamRaw &r = sm.raw[gq & 1];
+  if (n < GW) {
+    sm.beta[n] = b_n;
+    sm.glog[n] = g_n;
+  }
+  __syncthreads();
+  float lam[GW];
+  float acc = 0.f;
+#pragma unroll
+  for (int t = 0; t < GW; t++) {
+    acc += sm.glog[t];  // zero past nt
+    lam[t] = acc;
+  }
+  const float lam_last = pick(lam, nt - 1);
+
+  // decayed Gram entry: thread n -> (matrix m, row t, column i)
+  {
+    const int m = n >> 6, t = (n >> 3) & 7, i = n & 7;
+    float val = 0.f;
+    if (t < nt && i < nt && (m ? i <= t : i < t)) {
+      const __nv_bfloat16 *ra = m ? r.q[t] : r.k[t];
+      const __nv_bfloat16 *rb = r.k[i];
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+      for (int it = 0; it < 16; it++) {
+        const int ch = (it + i) & 15;  // staggered: the 8 key rows hit different banks
+        float a8[8], b8[8];
+        unpack8(ra + 8 * ch, a8);
+        unpack8(rb + 8 * ch, b8);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          s0 = fmaf(a8[j], b8[j], s0);
+          s1 = fmaf(a8[j + 1], b8[j + 1], s1);
+        }
+      }
+      val = (s0 + s1) * __expf(pick(lam, t) - pick(lam, i));
+    }
+    (m ? sm.gq : sm.gk)[t][i] = val;
+  }
+  // [K;Q] operand tile: thread n -> row n/8 (k_0..k_7, q_0..q_7), 16 channels
+  {
+    const int row = n >> 3, kb = (n & 7) * 16;
+    const bool valid = (row & 7) < nt;
+    const __nv_bfloat16 *src = row < 8 ? r.k[row] : r.q[row - 8];
+    float f[16];
+    if (valid) {
+      float a8[8];
+      unpack8(src + kb, a8);
+#pragma unroll
+      for (int j = 0; j < 8; j++) f[j] = a8[j];
+      unpack8(src + kb + 8, a8);
+#pragma unroll
+      for (int j = 0; j < 8; j++) f[8 + j] = a8[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; j++) f[j] = 0.f;
+    }
+    // bf16 values are exact in tf32; 128-byte swizzle: 16-byte chunk ^ (row % 8)
+    unsigned char *slab = reinterpret_cast<unsigned char *>(&sm.bt[kb >> 5][0][0]);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; q4++) {
+      const int chunk = ((kb & 31) >> 2) + q4;
+      float4 *dst = reinterpret_cast<float4 *>(slab + row * 128 + ((chunk ^ (row & 7)) << 4));
+      *dst = make_float4(f[4 * q4], f[4 * q4 + 1], f[4 * q4 + 2], f[4 * q4 + 3]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < GW; i++) vv[i] = i < nt ? __bfloat162float(r.v[i][n]) : 0.f;
+  if (n < GW) {
+    const float li = pick(lam, n);
+    sm.ea[n] = n < nt ? __expf(li) : 0.f;
+    sm.eb[n] = n < nt ? __expf(lam_last - li) : 0.f;
+    sm.en[n] = n < nt ? __expf(fminf(-li, 80.f)) : 0.f;
+  }
+  if (n == 0) sm.alast = __expf(lam_last);
+  tc::fence_proxy_async_smem();  // the operand tile is read by the tensor cores
+  __syncthreads();
+}
+
+template <bool GDN>
+__global__ void __launch_bounds__(NT, 2)
+    compose_seam_mma_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tmap_T) {
+  extern __shared__ unsigned char smem_raw[];
+  SeamMmaSmem &sm = *reinterpret_cast<SeamMmaSmem *>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
+  const ComposeParams &p = args.p;
+  const uint32_t LIM = args.wait_limit;
+  const int n = threadIdx.x;  // column of S owned by this thread
+  const int warp = n / 32;
+  Chain c;
+  c.l = blockIdx.x / p.h_v;
+  c.h = blockIdx.x % p.h_v;
+  c.kh = (int)(((int64_t)c.h * p.h_k) / p.h_v);
+  c.n_seg = p.n_seg;
+  c.w = p.seam_w;
+  c.groups = (c.w + GW - 1) / GW;
+  const int total_groups = c.n_seg * c.groups;
+  const uint32_t total_slabs = 4u * (uint32_t)c.n_seg;
+  const bool has_seam = c.groups > 0;
+
+  if (n == 0) {
+    for (int i = 0; i < NSLOT; i++) tc::mbar_init(&sm.full[i], 1);
+    tc::mbar_init(&sm.raw_full[0], 1);
+    tc::mbar_init(&sm.raw_full[1], 1);
+    tc::mbar_init(&sm.mma_done, 1);
+    tc::mbar_init(&sm.never, 1);
+    sm.abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&sm.tmem_base, 256);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tD = sm.tmem_base, tA = sm.tmem_base + 128;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+  uint32_t issued = 0;  // T_C slabs issued (thread 0)
+  int raw_issued = 0;   // seam groups issued (thread 0)
+  if (n == 0) {
+    tc::prefetch_tmap(&tmap_T);
+    for (; issued < (uint32_t)NSLOT && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued);
+    issue_raw<GDN>(sm, p, c, 0);
+    issue_raw<GDN>(sm, p, c, 1);
+    raw_issued = min(2, total_groups);
+    for (int s = 0; s < 2; s++) prefetch_pair(p, c, s);
+  }
+
+  if (args.debug_stall && !tc::mbar_wait(&sm.never, 0, LIM)) fail(sm, p);
+
+  const int64_t state = (int64_t)blockIdx.x * 128 * 128;
+  float S[128];
+#pragma unroll
+  for (int i = 0; i < 128; i++) S[i] = p.S_init ? p.S_init[state + (int64_t)i * 128 + n] : 0.f;
+  bool bad = false;
+  const uint32_t id_T = tc::idesc(tc::FMT_TF32, 128, 128);
+  const uint32_t id_s = tc::idesc(tc::FMT_TF32, 128, 16);
+  uint32_t mcount = 0;  // commits to mma_done so far (uniform)
+  float vv[GW];
+  float pb = 0.f, pg = 0.f;  // threads n < GW: beta / log-gate of token n of the next group
+
+  auto load_bg = [&](int gq) {
+    pb = 0.f;
+    pg = 0.f;
+    if (n < GW && gq < total_groups) {
+      const SeamGroup sg = seam_group(p, c, gq);
+      if (n < sg.nt) {
+        pb = p.seam_beta[(sg.tok0 + n) * p.h_v + c.h];
+        if (GDN) pg = p.seam_g[(sg.tok0 + n) * p.h_v + c.h];
+      }
+    }
+  };
+  // raw group gq has landed: prepare it, hand its buffer back and start the
+  // loads of the next group's beta / gates
+  auto ready_group = [&](int gq) {
+    const bool ok = !aborted(sm) && tc::mbar_wait(&sm.raw_full[gq & 1], (gq >> 1) & 1, LIM);
+    if (!ok) fail(sm, p);
+    prep_group(sm, p, c, gq, pb, pg, vv);
+    if (n == 0 && !aborted(sm) && gq + 2 < total_groups) {
+      issue_raw<GDN>(sm, p, c, gq + 2);
+      raw_issued = gq + 3;
+    }
+    load_bg(gq + 1);
+  };
+  // scale * S (tf32, round to nearest) -> TMEM A operand
+  auto put_A = [&](float scale) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ch++) {
+      uint32_t r[16];
+#pragma unroll
+      for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(scale * S[16 * ch + j]);
+      tc::tmem_st16(tA + lane_base + 16 * ch, r);
+    }
+    tc::tmem_wait_st();
+  };
+  auto wait_mma = [&]() {
+    if (!tc::mbar_wait(&sm.mma_done, mcount & 1, DRAIN_LIMIT)) fail(sm, p);
+    mcount++;
+    tc::tc_fence_after();
+  };
+  // D cols 0..15 = S^T [K;Q]^T (thread 0)
+  auto issue_seam_mma = [&]() {
+    const uint32_t base = tc::smem_u32(&sm.bt[0][0][0]);
+#pragma unroll
+    for (int kk = 0; kk < 16; kk++) {
+      const uint64_t bd = tc::smem_desc(base + 2048 * (kk >> 2) + 32 * (kk & 3), 16, 1024, tc::SW_128B);
+      tc::mma_ts_tf32(tD, tA + 8 * kk, bd, id_s, kk != 0);
+    }
+  };
+  // D = S^T T_C^T from TMEM A and the four K-slabs of segment seg (thread 0)
+  auto issue_T_mma = [&](uint32_t q) {
+    for (int sl = 0; sl < 4; sl++) {
+      const uint32_t base = tc::smem_u32(sm.slot[(q + sl) % NSLOT]);
+#pragma unroll
+      for (int kk = 0; kk < 4; kk++) {
+        const uint64_t bd = tc::smem_desc(base + 32 * kk, 16, 1024, tc::SW_128B);
+        tc::mma_ts_tf32(tD, tA + 32 * sl + 8 * kk, bd, id_T, (sl | kk) != 0);
+      }
+    }
+  };
+  // thread 0: the four K-slabs of segment seg have landed
+  auto wait_slabs = [&](uint32_t q) {
+    for (int sl = 0; sl < 4; sl++) {
+      const uint32_t r = q + sl;
+      if (!tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, LIM)) {
+        fail(sm, p);
+        return false;
+      }
+    }
+    return true;
+  };
+  // c_t of every token of the group for column n, and its outputs o_t
+  auto seam_recurrence = [&](const uint32_t (&d)[16], const SeamGroup &sg, float (&cc)[GW]) {
+#pragma unroll
+    for (int t = 0; t < GW; t++) {
+      cc[t] = 0.f;
+      if (t < sg.nt) {
+        float x = sm.ea[t] * __uint_as_float(d[t]);
+#pragma unroll
+        for (int i = 0; i < t; i++) x = fmaf(sm.gk[t][i], cc[i], x);
+        cc[t] = sm.beta[t] * (vv[t] - x);
+        float o = sm.ea[t] * __uint_as_float(d[8 + t]);
+#pragma unroll
+        for (int i = 0; i <= t; i++) o = fmaf(sm.gq[t][i], cc[i], o);
+        p.seam_out[((sg.tok0 + t) * p.h_v + c.h) * 128 + n] = o;
+        bad |= !finite_f(o);
+      }
+    }
+  };
+
+  load_bg(0);
+  if (has_seam) ready_group(0);
+
+  for (int seg = 0; seg < c.n_seg; seg++) {
+    // uniform stop decision
+    if (n == 0) sm.stop = *(volatile int *)&sm.abort;
+    __syncthreads();
+    const bool stop = *(volatile int *)&sm.stop != 0;
+    __syncthreads();
+    if (stop) break;
+
+    const int slot = pair_slot(p, c, seg);  // uniform
+    const bool pair_ok = slot >= 0;
+    if (!pair_ok && n == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
+    const uint32_t q = 4u * (uint32_t)seg;
+
+    // ---- seam groups through the registers: all but the last, or all of
+    // them when the pair is skipped.  S <- e^{lam_last} S + sum_i
+    // e^{lam_last - lam_i} k_i c_i^T with k_i read from the operand tile.
+    const int reg_groups = pair_ok ? c.groups - 1 : c.groups;
+    for (int gi = 0; gi < reg_groups; gi++) {
+      const int gq = seg * c.groups + gi;
+      if (gi > 0) ready_group(gq);
+      put_A(1.f);
+      tc::tc_fence_before();
+      __syncthreads();
+      if (n == 0) {
+        tc::tc_fence_after();
+        if (!aborted(sm)) issue_seam_mma();
+        tc::mma_commit(&sm.mma_done);
+      }
+      wait_mma();
+      uint32_t d[16];
+      tc::tmem_ld16(tD + lane_base, d);
+      tc::tmem_wait_ld();
+      tc::tc_fence_before();  // D is rewritten by the next MMA
+      if (!aborted(sm)) {
+        float cc[GW];
+        seam_recurrence(d, seam_group(p, c, gq), cc);
+#pragma unroll
+        for (int i = 0; i < GW; i++) cc[i] *= sm.eb[i];
+        const float al = sm.alast;
+        const float *bt = &sm.bt[0][0][0];
+#pragma unroll
+        for (int r = 0; r < 128; r++) {
+          float x = al * S[r];
+#pragma unroll
+          for (int i = 0; i < GW; i++)
+            x = fmaf(bt[(r >> 5) * 512 + i * 32 + ((((r & 31) >> 2) ^ i) << 2) + (r & 3)], cc[i], x);
+          S[r] = x;
+        }
+      }
+    }
+
+    if (!pair_ok) {
+      // a bad slot skips the pair; its slabs (loaded from slot 0) still pass
+      // through the ring
+      if (n == 0 && !aborted(sm) && wait_slabs(q)) {
+        for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
+        prefetch_pair(p, c, seg + 2);
+      }
+      if (seg + 1 < c.n_seg && has_seam) ready_group((seg + 1) * c.groups);
+      continue;
+    }
+
+    if (has_seam) {
+      // ---- last seam group, fused with the pair
+      const int gq = seg * c.groups + c.groups - 1;
+      if (c.groups > 1) ready_group(gq);
+      put_A(1.f);
+      tc::tc_fence_before();
+      __syncthreads();
+      if (n == 0) {
+        tc::tc_fence_after();
+        if (!aborted(sm)) {
+          issue_seam_mma();
+          if (wait_slabs(q)) {
+            // D cols 16..31 = T_C [K;Q]^T: lane r holds (T_C k_i)[r]
+            const uint32_t bbase = tc::smem_u32(&sm.bt[0][0][0]);
+            for (int sl = 0; sl < 4; sl++) {
+              const uint32_t abase = tc::smem_u32(sm.slot[(q + sl) % NSLOT]);
+#pragma unroll
+              for (int kk = 0; kk < 4; kk++) {
+                const uint64_t ad = tc::smem_desc(abase + 32 * kk, 16, 1024, tc::SW_128B);
+                const uint64_t bd = tc::smem_desc(bbase + 2048 * sl + 32 * kk, 16, 1024, tc::SW_128B);
+                tc::mma_ss_tf32(tD + 16, ad, bd, id_s, (sl | kk) != 0);
+              }
+            }
+          }
+        }
+        tc::mma_commit(&sm.mma_done);
+      }
+      wait_mma();
+      uint32_t d[16];
+      {
+        uint32_t e[16];
+        tc::tmem_ld16(tD + lane_base, d);
+        tc::tmem_ld16(tD + lane_base + 16, e);
+        tc::tmem_wait_ld();
+        float tkr[GW];
+#pragma unroll
+        for (int i = 0; i < GW; i++) tkr[i] = __uint_as_float(e[i]);
+        store_row_sw32(sm.tk, n, tkr);
+      }
+      // A <- e^{lam_last} S0 for the T_C product (after the reads above)
+      tc::tc_fence_before();
+      put_A(sm.alast);
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      __syncthreads();
+      if (n == 0) {
+        tc::tc_fence_after();
+        if (!aborted(sm)) issue_T_mma(q);
+      }
+      // while it runs: the group's recurrence and outputs, then the rank-8
+      // seam term sum_i (T_C k_i) e^{lam_last - lam_i} c_i^T onto D
+      {
+        float cc[GW];
+        if (!aborted(sm)) {
+          seam_recurrence(d, seam_group(p, c, gq), cc);
+#pragma unroll
+          for (int i = 0; i < GW; i++) cc[i] *= sm.eb[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < GW; i++) cc[i] = 0.f;
+        }
+        store_row_sw32(sm.cp, n, cc);
+      }
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+      if (n == 0) {
+        if (!aborted(sm)) {
+          const uint64_t ad = tc::smem_desc(tc::smem_u32(&sm.cp[0][0]), 16, 256, tc::SW_32B);
+          const uint64_t bd = tc::smem_desc(tc::smem_u32(&sm.tk[0][0]), 16, 256, tc::SW_32B);
+          tc::mma_ss_tf32(tD, ad, bd, id_T, 1);
+        }
+        tc::mma_commit(&sm.mma_done);
+      }
+      // ... and the preparation of the group that opens the next segment
+      if (seg + 1 < c.n_seg) ready_group((seg + 1) * c.groups);
+    } else {
+      put_A(1.f);
+      tc::tc_fence_before();
+      __syncthreads();
+      if (n == 0) {
+        tc::tc_fence_after();
+        if (!aborted(sm) && wait_slabs(q)) issue_T_mma(q);
+        tc::mma_commit(&sm.mma_done);
+      }
+    }
+
+    const bool use = !aborted(sm);
+    const float *Sc = p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128 + n;
+    float nxt[32];
+#pragma unroll
+    for (int j = 0; j < 32; j++) nxt[j] = use ? Sc[j * 128] : 0.f;
+    wait_mma();
+    if (n == 0 && !aborted(sm)) {
+      // this pair's four slots are free: refill them, and warm L2 with the
+      // pair of the segment after next
+      for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
+      prefetch_pair(p, c, seg + 2);
+    }
+
+    // ---- S <- D + S(C|0)
+#pragma unroll
+    for (int ch = 0; ch < 4; ch++) {
+      float cur[32];
+#pragma unroll
+      for (int j = 0; j < 32; j++) cur[j] = nxt[j];
+      if (ch < 3) {
+#pragma unroll
+        for (int j = 0; j < 32; j++) nxt[j] = use ? Sc[(32 * (ch + 1) + j) * 128] : 0.f;
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        uint32_t r[16];
+        tc::tmem_ld16(tD + lane_base + 32 * ch + 16 * hh, r);
+        tc::tmem_wait_ld();
+        if (use) {
+#pragma unroll
+          for (int j = 0; j < 16; j++) S[32 * ch + 16 * hh + j] = __uint_as_float(r[j]) + cur[16 * hh + j];
+        }
+      }
+    }
+    tc::tc_fence_before();  // TMEM reads done before the next MMA overwrites D
+  }
+
+  __syncthreads();
+  if (!aborted(sm)) {
+#pragma unroll
+    for (int i = 0; i < 128; i++) {
+      p.S_out[state + (int64_t)i * 128 + n] = S[i];
+      bad |= !finite_f(S[i]);
+    }
+  }
+  if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
+  // drain: every copy thread 0 issued lands before the CTA releases its smem
+  if (n == 0) {
+    const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
+    for (uint32_t r = first; r < issued; r++) tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, DRAIN_LIMIT);
+    for (int r = raw_issued > 2 ? raw_issued - 2 : 0; r < raw_issued; r++)
+      tc::mbar_wait(&sm.raw_full[r & 1], (r >> 1) & 1, DRAIN_LIMIT);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(sm.tmem_base, 256);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -436,10 +1014,13 @@ bool compose_tc_supported(const ComposeParams &p) {
 cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s) {
   CUtensorMap tmap;
   if (!make_tmap_f32_rows(&tmap, p.T_pool, (uint64_t)p.n_slots * p.h_v * 128, 128)) return cudaErrorInvalidValue;
-  const size_t smem = sizeof(ComposeTcSmem) + 1024;
-  auto kern = p.variant == HYPIC_GDN        ? compose_tc_kernel<HYPIC_GDN>
-              : p.variant == HYPIC_DELTANET ? compose_tc_kernel<HYPIC_DELTANET>
-                                            : compose_tc_kernel<HYPIC_CHANNEL_DELTA>;
+  // scalar gates: seam tokens on the tensor cores; per-channel gates: the
+  // token-by-token seam
+  const bool vec = p.variant == HYPIC_CHANNEL_DELTA;
+  const size_t smem = (vec ? sizeof(ComposeTcSmem) : sizeof(SeamMmaSmem)) + 1024;
+  auto kern = vec                       ? compose_tc_kernel<HYPIC_CHANNEL_DELTA>
+              : p.variant == HYPIC_GDN ? compose_seam_mma_kernel<true>
+                                       : compose_seam_mma_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.n_layers * p.h_v;
