@@ -418,24 +418,47 @@ __global__ void __launch_bounds__(NT, 2)
 //   xh_t = a_t k_t^T S_{t-1} = e^{lam_t} k_t^T S0 + sum_{i<t} e^{lam_t-lam_i} (k_t.k_i) c_i
 //   o_t  = q_t^T S_t         = e^{lam_t} q_t^T S0 + sum_{i<=t} e^{lam_t-lam_i} (q_t.k_i) c_i
 // so one MMA gives k_t^T S0 and q_t^T S0 for the 8 tokens and all 128
-// columns (D = S0^T [K;Q]^T: M = 128, N = 16, A = S0 in TMEM), and what
-// remains per column is an 8-step scalar recurrence.  For the last group of a
-// segment the state never has to be formed: with S0 the state entering it,
+// columns (D = S0^T [K;Q]^T: M = 128, N = 16, A = S0 in TMEM), and per column
+// c = M (v - e^{lam} . k^T S0) with the 8 x 8 lower-triangular
+// M = (I + diag(b) Gk)^{-1} diag(b), Gk the decayed key Gram.  For the last
+// group of a segment the state never has to be formed: with S0 the state
+// entering it,
 //   T_C S_n + S(C|0) = e^{lam_last} (T_C S0 + sum_i (T_C k_i) e^{-lam_i} c_i^T) + S(C|0)
 // so the same MMA round also gives T_C k_i (A = the T_C K-slabs), the T_C S0
 // product starts at once from the same TMEM operand, and the rank-8 seam term
 // is accumulated onto it by one more MMA (K = 8) from two 128 x 8 tiles.
 // Earlier groups of a long seam window, a group whose decay underflows and a
-// skipped pair update S in registers instead.  The decayed Gram terms and
-// the [K;Q] operand tile depend on the seam tokens only: the group that opens
-// segment s+1 is prepared while the T_C S product of segment s runs.
+// skipped pair update the exact state (kept in S_out) instead.  Everything
+// that depends on the seam tokens only (the [K;Q] operand tile, the decayed
+// Grams, M) is prepared by warps 5..7 while warps 0..3 run the previous
+// group's recurrence; warp 4 issues the MMAs and the seam copies.
 // ---------------------------------------------------------------------------
-constexpr int GW = 8;  // seam tokens per group
+constexpr int GW = 8;             // seam tokens per group
+constexpr int NT2 = 256;          // threads per CTA: two per state column (rows 0..63, 64..127)
+constexpr int ISSUER_WARP = 4;    // lane 0 issues the MMAs; the warp issues the seam copies
+constexpr int PREP_WARP0 = 5;     // warps 5..7 prepare the next seam group
+constexpr int NPREP = 96;
+constexpr int BAR_PREP = 1;       // named barrier of the preparing warps
+constexpr int BAR_CORR = 2;       // warps 0..4: the seam term tile is written
+constexpr float AL_MIN = 1e-30f;  // smallest e^{lam_last} of a fused group
 
 struct SeamRaw {
   __nv_bfloat16 k[GW][128];
   __nv_bfloat16 q[GW][128];
   __nv_bfloat16 v[GW][128];
+};
+
+// constants of one seam group (double-buffered by group parity)
+struct GroupConst {
+  float gk[GW][GW];  // e^{lam_t - lam_i} (k_t.k_i), i < t
+  float gq[GW][GW];  // e^{lam_t - lam_i} (q_t.k_i), i <= t
+  float mm[GW][GW];  // (I + diag(beta) gk)^{-1} diag(beta)
+  float ea[GW];      // e^{lam_t}
+  float eb[GW];      // e^{lam_last - lam_i}
+  float beta[GW];
+  float glog[GW];
+  float alast;       // e^{lam_last}
+  float pad[3];
 };
 
 struct __align__(1024) SeamMmaSmem {
@@ -444,14 +467,7 @@ struct __align__(1024) SeamMmaSmem {
   float tk[128][GW];                // (T_C k_i)[r]: tf32, K-major, 32-byte swizzle
   float cp[128][GW];                // e^{-lam_i} c_i[n]: tf32, K-major, 32-byte swizzle
   SeamRaw raw[2];                   // seam k / q / v rows of a group (bulk copies)
-  float gk[GW][GW];                 // e^{lam_t - lam_i} (k_t.k_i), i < t
-  float gq[GW][GW];                 // e^{lam_t - lam_i} (q_t.k_i), i <= t
-  float ea[GW];                     // e^{lam_t}
-  float eb[GW];                     // e^{lam_last - lam_i}
-  float en[GW];                     // e^{-lam_i}
-  float beta[GW];
-  float glog[GW];
-  float alast;                      // e^{lam_last}
+  GroupConst gc[2];
   uint64_t full[NSLOT];
   uint64_t raw_full[2];
   uint64_t mma_done;
@@ -488,28 +504,6 @@ __device__ __forceinline__ SeamGroup seam_group(const ComposeParams &p, const Ch
   return g;
 }
 
-// bulk copies of a group's k / q / v rows; the group's beta and gate rows
-// (all heads, contiguous) are warmed in L2 for the plain loads of the prep
-template <bool GDN>
-__device__ __forceinline__ void issue_raw(SeamMmaSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
-  if (gq >= c.n_seg * c.groups) return;
-  const SeamGroup sg = seam_group(p, c, gq);
-  const int b = gq & 1;
-  SeamRaw &r = sm.raw[b];
-  tc::mbar_expect_tx(&sm.raw_full[b], (uint32_t)sg.nt * 3 * 256);
-  const __nv_bfloat16 *sk = static_cast<const __nv_bfloat16 *>(p.seam_k);
-  const __nv_bfloat16 *sqp = static_cast<const __nv_bfloat16 *>(p.seam_q);
-  const __nv_bfloat16 *sv = static_cast<const __nv_bfloat16 *>(p.seam_v);
-  for (int t = 0; t < sg.nt; t++) {
-    tc::bulk_load(r.k[t], sk + ((sg.tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.raw_full[b]);
-    tc::bulk_load(r.q[t], sqp + ((sg.tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.raw_full[b]);
-    tc::bulk_load(r.v[t], sv + ((sg.tok0 + t) * p.h_v + c.h) * 128, 256, &sm.raw_full[b]);
-  }
-  const uint32_t gbytes = (uint32_t)(sg.nt * p.h_v * 4);
-  prefetch_l2(p.seam_beta + sg.tok0 * p.h_v, gbytes);
-  if (GDN) prefetch_l2(p.seam_g + sg.tok0 * p.h_v, gbytes);
-}
-
 // register select of lam[u] for a run-time u (keeps lam[] in registers)
 __device__ __forceinline__ float pick(const float (&lam)[GW], int u) {
   float r = 0.f;
@@ -518,103 +512,151 @@ __device__ __forceinline__ float pick(const float (&lam)[GW], int u) {
   return r;
 }
 
-// State-independent preparation of group gq (all threads; its raw buffer has
-// landed).  Threads n < GW pass beta and the log-gate of the group's token n
-// (loaded one group ahead; zero past nt).  Leaves v_t[n] in vv; the raw
-// buffer is free afterwards.
+// Gram of the group on the legacy warp MMA (one warp, 8 x m16n8k16 bf16,
+// exact products, fp32 sums): D[m][i] = A[m] . k_i with A = [k_0..k_7;
+// q_0..q_7]; lane (g = lane/4, u = lane%4) receives D[g][2u], D[g][2u+1],
+// D[g+8][2u], D[g+8][2u+1].
+__device__ __forceinline__ void gram_mma(const SeamRaw &r, float (&dd)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, u = lane & 3;
+  dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
+  const uint32_t *kg = reinterpret_cast<const uint32_t *>(r.k[g]);
+  const uint32_t *qg = reinterpret_cast<const uint32_t *>(r.q[g]);
+#pragma unroll
+  for (int kc = 0; kc < 8; kc++) {
+    const int w0 = 8 * kc + u, w1 = 8 * kc + 4 + u;  // 32-bit words: channels 16kc+2u.., 16kc+8+2u..
+    const uint32_t a0 = kg[w0], a1 = qg[w0], a2 = kg[w1], a3 = qg[w1];
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(dd[0]), "+f"(dd[1]), "+f"(dd[2]), "+f"(dd[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a0), "r"(a2));
+  }
+}
+
+// State-independent preparation of group gq by the NPREP threads of warps
+// PREP_WARP0.. (its raw buffer has landed).  Threads ptid < GW pass beta and
+// the log-gate of the group's token ptid (loaded one group ahead; zero past
+// nt).  The raw buffer stays in use until the group's recurrence has read its
+// v rows; the results become visible to the other warps at their next
+// CTA-wide barrier.
 __device__ __forceinline__ void prep_group(SeamMmaSmem &sm, const ComposeParams &p, const Chain &c, int gq,
-                                           float b_n, float g_n, float (&vv)[GW]) {
-  const int n = threadIdx.x;
+                                           float b_n, float g_n) {
+  const int ptid = threadIdx.x - 32 * PREP_WARP0;
   const SeamGroup sg = seam_group(p, c, gq);
   const int nt = sg.nt;
   const SeamRaw &r = sm.raw[gq & 1];
-  if (n < GW) {
-    sm.beta[n] = b_n;
-    sm.glog[n] = g_n;
+  GroupConst &G = sm.gc[gq & 1];
+  if (ptid < GW) {
+    G.beta[ptid] = b_n;
+    G.glog[ptid] = g_n;
   }
-  __syncthreads();
+  tc::named_bar(BAR_PREP, NPREP);
   float lam[GW];
   float acc = 0.f;
 #pragma unroll
   for (int t = 0; t < GW; t++) {
-    acc += sm.glog[t];  // zero past nt
+    acc += G.glog[t];  // zero past nt
     lam[t] = acc;
   }
   const float lam_last = pick(lam, nt - 1);
 
-  // decayed Gram entry: thread n -> (matrix m, row t, column i)
-  {
-    const int m = n >> 6, t = (n >> 3) & 7, i = n & 7;
-    float val = 0.f;
-    if (t < nt && i < nt && (m ? i <= t : i < t)) {
-      const __nv_bfloat16 *ra = m ? r.q[t] : r.k[t];
-      const __nv_bfloat16 *rb = r.k[i];
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-      for (int it = 0; it < 16; it++) {
-        const int ch = (it + i) & 15;  // staggered: the 8 key rows hit different banks
-        float a8[8], b8[8];
-        unpack8(ra + 8 * ch, a8);
-        unpack8(rb + 8 * ch, b8);
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          s0 = fmaf(a8[j], b8[j], s0);
-          s1 = fmaf(a8[j + 1], b8[j + 1], s1);
-        }
-      }
-      val = (s0 + s1) * __expf(pick(lam, t) - pick(lam, i));
-    }
-    (m ? sm.gq : sm.gk)[t][i] = val;
-  }
-  // [K;Q] operand tile: thread n -> row n/8 (k_0..k_7, q_0..q_7), 16 channels
-  {
-    const int row = n >> 3, kb = (n & 7) * 16;
-    const bool valid = (row & 7) < nt;
-    const __nv_bfloat16 *src = row < 8 ? r.k[row] : r.q[row - 8];
-    float f[16];
-    if (valid) {
-      float a8[8];
-      unpack8(src + kb, a8);
-#pragma unroll
-      for (int j = 0; j < 8; j++) f[j] = a8[j];
-      unpack8(src + kb + 8, a8);
-#pragma unroll
-      for (int j = 0; j < 8; j++) f[8 + j] = a8[j];
+  // [K;Q] operand tile: task -> row task/16 (k_0..k_7, q_0..q_7), 8 channels
+  for (int task = ptid; task < 256; task += NPREP) {
+    const int row = task >> 4, kb = (task & 15) * 8;
+    float f[8];
+    if ((row & 7) < nt) {
+      unpack8((row < 8 ? r.k[row] : r.q[row - 8]) + kb, f);
     } else {
 #pragma unroll
-      for (int j = 0; j < 16; j++) f[j] = 0.f;
+      for (int j = 0; j < 8; j++) f[j] = 0.f;
     }
     // bf16 values are exact in tf32; 128-byte swizzle: 16-byte chunk ^ (row % 8)
     unsigned char *slab = reinterpret_cast<unsigned char *>(&sm.bt[kb >> 5][0][0]);
 #pragma unroll
-    for (int q4 = 0; q4 < 4; q4++) {
+    for (int q4 = 0; q4 < 2; q4++) {
       const int chunk = ((kb & 31) >> 2) + q4;
       float4 *dst = reinterpret_cast<float4 *>(slab + row * 128 + ((chunk ^ (row & 7)) << 4));
       *dst = make_float4(f[4 * q4], f[4 * q4 + 1], f[4 * q4 + 2], f[4 * q4 + 3]);
     }
   }
+  // decayed Grams; rows and columns past nt (stale raw rows) are masked out
+  if (ptid < 32) {
+    float dd[4];
+    gram_mma(r, dd);
+    const int t = ptid >> 2;
 #pragma unroll
-  for (int i = 0; i < GW; i++) vv[i] = i < nt ? __bfloat162float(r.v[i][n]) : 0.f;
-  if (n < GW) {
-    const float li = pick(lam, n);
-    sm.ea[n] = n < nt ? __expf(li) : 0.f;
-    sm.eb[n] = n < nt ? __expf(lam_last - li) : 0.f;
-    sm.en[n] = n < nt ? __expf(fminf(-li, 80.f)) : 0.f;
+    for (int j = 0; j < 2; j++) {
+      const int i = 2 * (ptid & 3) + j;
+      const bool in = t < nt && i < nt;
+      const float e = __expf(pick(lam, t) - pick(lam, i));
+      G.gk[t][i] = (in && i < t) ? dd[j] * e : 0.f;
+      G.gq[t][i] = (in && i <= t) ? dd[2 + j] * e : 0.f;
+    }
+  } else if (ptid < 32 + GW) {
+    const int t = ptid - 32;
+    const float li = pick(lam, t);
+    G.ea[t] = t < nt ? __expf(li) : 0.f;
+    G.eb[t] = t < nt ? __expf(lam_last - li) : 0.f;
+  } else if (ptid == 32 + GW) {
+    G.alast = __expf(lam_last);
   }
-  if (n == 0) sm.alast = __expf(lam_last);
+  tc::named_bar(BAR_PREP, NPREP);
+  // M: thread j < 8 solves column j by forward substitution
+  if (ptid < GW) {
+    const int j = ptid;
+    float m[GW];
+#pragma unroll
+    for (int t = 0; t < GW; t++) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < t; i++) s = fmaf(G.gk[t][i], (i >= j) ? m[i] : 0.f, s);
+      m[t] = t < j ? 0.f : (t == j ? G.beta[t] : -G.beta[t] * s);
+      G.mm[t][j] = m[t];
+    }
+  }
   tc::fence_proxy_async_smem();  // the operand tile is read by the tensor cores
-  __syncthreads();
+}
+
+// bulk copies of group gq's k / q / v rows, one per lane of the calling warp
+// (all 32 lanes call); its beta and gate rows (all heads, contiguous) are
+// warmed in L2 for the plain loads one group ahead
+template <bool GDN>
+__device__ __forceinline__ void issue_raw_warp(SeamMmaSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
+  const int lane = threadIdx.x & 31;
+  const SeamGroup sg = seam_group(p, c, gq);
+  const int b = gq & 1;
+  SeamRaw &r = sm.raw[b];
+  if (lane == 0) tc::mbar_expect_tx(&sm.raw_full[b], (uint32_t)sg.nt * 3 * 256);
+  __syncwarp();
+  if (lane < 3 * sg.nt) {
+    const int t = lane / 3, kind = lane % 3;
+    const int64_t tok = sg.tok0 + t;
+    const __nv_bfloat16 *src =
+        kind == 0 ? static_cast<const __nv_bfloat16 *>(p.seam_k) + (tok * p.h_k + c.kh) * 128
+        : kind == 1 ? static_cast<const __nv_bfloat16 *>(p.seam_q) + (tok * p.h_k + c.kh) * 128
+                    : static_cast<const __nv_bfloat16 *>(p.seam_v) + (tok * p.h_v + c.h) * 128;
+    __nv_bfloat16 *dst = kind == 0 ? r.k[t] : kind == 1 ? r.q[t] : r.v[t];
+    tc::bulk_load(dst, src, 256, &sm.raw_full[b]);
+  } else if (lane == 31) {
+    const uint32_t gbytes = (uint32_t)(sg.nt * p.h_v * 4);
+    prefetch_l2(p.seam_beta + sg.tok0 * p.h_v, gbytes);
+    if (GDN) prefetch_l2(p.seam_g + sg.tok0 * p.h_v, gbytes);
+  }
 }
 
 template <bool GDN>
-__global__ void __launch_bounds__(NT, 2)
+__global__ void __launch_bounds__(NT2, 2)
     compose_seam_mma_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tmap_T) {
   extern __shared__ unsigned char smem_raw[];
   SeamMmaSmem &sm = *reinterpret_cast<SeamMmaSmem *>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   const ComposeParams &p = args.p;
   const uint32_t LIM = args.wait_limit;
-  const int n = threadIdx.x;  // column of S owned by this thread
-  const int warp = n / 32;
+  const int tid = threadIdx.x;
+  const int n = tid & 127;   // column of S
+  const int hf = tid >> 7;   // rows 64*hf .. 64*hf+63 of that column
+  const int warp = tid / 32;
+  const bool preper = warp >= PREP_WARP0;
   Chain c;
   c.l = blockIdx.x / p.h_v;
   c.h = blockIdx.x % p.h_v;
@@ -626,7 +668,7 @@ __global__ void __launch_bounds__(NT, 2)
   const uint32_t total_slabs = 4u * (uint32_t)c.n_seg;
   const bool has_seam = c.groups > 0;
 
-  if (n == 0) {
+  if (tid == 0) {
     for (int i = 0; i < NSLOT; i++) tc::mbar_init(&sm.full[i], 1);
     tc::mbar_init(&sm.raw_full[0], 1);
     tc::mbar_init(&sm.raw_full[1], 1);
@@ -642,73 +684,71 @@ __global__ void __launch_bounds__(NT, 2)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  // warps w and w + 4 share the TMEM lane quadrant w % 4 (lanes = columns)
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t tD = sm.tmem_base, tA = sm.tmem_base + 128;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t tDh = tD + lane_base + 64 * hf, tAh = tA + lane_base + 64 * hf;  // this thread's rows
+  const bool issuer = tid == 32 * ISSUER_WARP;
 
   uint32_t issued = 0;  // T_C slabs issued (thread 0)
-  int raw_issued = 0;   // seam groups issued (thread 0)
-  if (n == 0) {
+  int raw_issued = min(2, total_groups);  // seam groups issued (uniform)
+  if (tid == 0) {
     tc::prefetch_tmap(&tmap_T);
     for (; issued < (uint32_t)NSLOT && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued);
-    issue_raw<GDN>(sm, p, c, 0);
-    issue_raw<GDN>(sm, p, c, 1);
-    raw_issued = min(2, total_groups);
     for (int s = 0; s < 2; s++) prefetch_pair(p, c, s);
+  }
+  if (warp == ISSUER_WARP) {
+    for (int g = 0; g < raw_issued; g++) issue_raw_warp<GDN>(sm, p, c, g);
   }
 
   if (args.debug_stall && !tc::mbar_wait(&sm.never, 0, LIM)) fail(sm, p);
 
-  const int64_t state = (int64_t)blockIdx.x * 128 * 128;
-  float S[128];
-#pragma unroll
-  for (int i = 0; i < 128; i++) S[i] = p.S_init ? p.S_init[state + (int64_t)i * 128 + n] : 0.f;
+  // The exact fp32 state lives in global memory (S_init, then S_out: this
+  // thread's 64 rows of column n) only where a register-path group or the
+  // end needs it; the MMAs read RN(S) from TMEM A.
+  const int64_t state = (int64_t)blockIdx.x * 128 * 128 + (int64_t)(64 * hf) * 128 + n;
+  const float *exact = p.S_init ? p.S_init + state : nullptr;  // NULL: zero
+  float *const out = p.S_out + state;
   bool bad = false;
   const uint32_t id_T = tc::idesc(tc::FMT_TF32, 128, 128);
   const uint32_t id_s = tc::idesc(tc::FMT_TF32, 128, 16);
   uint32_t mcount = 0;  // commits to mma_done so far (uniform)
-  float vv[GW];
-  float pb = 0.f, pg = 0.f;  // threads n < GW: beta / log-gate of token n of the next group
+  const int ptid = tid - 32 * PREP_WARP0;
+  float pb = 0.f, pg = 0.f;  // preparing threads ptid < GW: beta / log-gate of token ptid of the next group
 
   auto load_bg = [&](int gq) {
     pb = 0.f;
     pg = 0.f;
-    if (n < GW && gq < total_groups) {
+    if (ptid >= 0 && ptid < GW && gq < total_groups) {
       const SeamGroup sg = seam_group(p, c, gq);
-      if (n < sg.nt) {
-        pb = p.seam_beta[(sg.tok0 + n) * p.h_v + c.h];
-        if (GDN) pg = p.seam_g[(sg.tok0 + n) * p.h_v + c.h];
+      if (ptid < sg.nt) {
+        pb = p.seam_beta[(sg.tok0 + ptid) * p.h_v + c.h];
+        if (GDN) pg = p.seam_g[(sg.tok0 + ptid) * p.h_v + c.h];
       }
     }
   };
-  // raw group gq has landed: prepare it, hand its buffer back and start the
-  // loads of the next group's beta / gates
-  auto ready_group = [&](int gq) {
+  // preparing warps: raw group gq has landed, prepare it and start the loads
+  // of the next group's beta / gates
+  auto prepare = [&](int gq) {
     const bool ok = !aborted(sm) && tc::mbar_wait(&sm.raw_full[gq & 1], (gq >> 1) & 1, LIM);
     if (!ok) fail(sm, p);
-    prep_group(sm, p, c, gq, pb, pg, vv);
-    if (n == 0 && !aborted(sm) && gq + 2 < total_groups) {
-      issue_raw<GDN>(sm, p, c, gq + 2);
-      raw_issued = gq + 3;
-    }
+    prep_group(sm, p, c, gq, pb, pg);
     load_bg(gq + 1);
   };
-  // scale * S (tf32, round to nearest) -> TMEM A operand
-  auto put_A = [&](float scale) {
-#pragma unroll
-    for (int ch = 0; ch < 8; ch++) {
-      uint32_t r[16];
-#pragma unroll
-      for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(scale * S[16 * ch + j]);
-      tc::tmem_st16(tA + lane_base + 16 * ch, r);
+  // after a barrier that follows group gq's recurrence: its raw buffer is
+  // free, refill it with group gq + 2 (uniform call; the issuer warp copies)
+  auto release_raw = [&](int gq) {
+    if (gq + 2 < total_groups) {
+      if (warp == ISSUER_WARP && !aborted(sm)) issue_raw_warp<GDN>(sm, p, c, gq + 2);
+      raw_issued = gq + 3;
     }
-    tc::tmem_wait_st();
   };
   auto wait_mma = [&]() {
     if (!tc::mbar_wait(&sm.mma_done, mcount & 1, DRAIN_LIMIT)) fail(sm, p);
     mcount++;
     tc::tc_fence_after();
   };
-  // D cols 0..15 = S^T [K;Q]^T (thread 0)
+  // D cols 0..15 = S^T [K;Q]^T (issuer)
   auto issue_seam_mma = [&]() {
     const uint32_t base = tc::smem_u32(&sm.bt[0][0][0]);
 #pragma unroll
@@ -717,7 +757,7 @@ __global__ void __launch_bounds__(NT, 2)
       tc::mma_ts_tf32(tD, tA + 8 * kk, bd, id_s, kk != 0);
     }
   };
-  // D = S^T T_C^T from TMEM A and the four K-slabs of segment seg (thread 0)
+  // D = S^T T_C^T from TMEM A and the four K-slabs at ring position q (issuer)
   auto issue_T_mma = [&](uint32_t q) {
     for (int sl = 0; sl < 4; sl++) {
       const uint32_t base = tc::smem_u32(sm.slot[(q + sl) % NSLOT]);
@@ -728,7 +768,7 @@ __global__ void __launch_bounds__(NT, 2)
       }
     }
   };
-  // thread 0: the four K-slabs of segment seg have landed
+  // the four K-slabs at ring position q have landed (one thread)
   auto wait_slabs = [&](uint32_t q) {
     for (int sl = 0; sl < 4; sl++) {
       const uint32_t r = q + sl;
@@ -739,52 +779,85 @@ __global__ void __launch_bounds__(NT, 2)
     }
     return true;
   };
-  // c_t of every token of the group for column n, and its outputs o_t
-  auto seam_recurrence = [&](const uint32_t (&d)[16], const SeamGroup &sg, float (&cc)[GW]) {
+  // c_t of every token of group gq for column n (c = M u, u = v - e^{lam} x0),
+  // and (first half only) the outputs o_t
+  auto seam_recurrence = [&](const uint32_t (&d)[16], int gq, float (&cc)[GW]) {
+    const SeamGroup sg = seam_group(p, c, gq);
+    const SeamRaw &raw = sm.raw[gq & 1];
+    const GroupConst &G = sm.gc[gq & 1];
+    float u[GW];
+#pragma unroll
+    for (int t = 0; t < GW; t++)
+      u[t] = t < sg.nt ? __bfloat162float(raw.v[t][n]) - G.ea[t] * __uint_as_float(d[t]) : 0.f;
 #pragma unroll
     for (int t = 0; t < GW; t++) {
-      cc[t] = 0.f;
-      if (t < sg.nt) {
-        float x = sm.ea[t] * __uint_as_float(d[t]);
+      float x = 0.f;
 #pragma unroll
-        for (int i = 0; i < t; i++) x = fmaf(sm.gk[t][i], cc[i], x);
-        cc[t] = sm.beta[t] * (vv[t] - x);
-        float o = sm.ea[t] * __uint_as_float(d[8 + t]);
+      for (int i = 0; i <= t; i++) x = fmaf(G.mm[t][i], u[i], x);
+      cc[t] = x;
+    }
+    if (hf == 0) {
 #pragma unroll
-        for (int i = 0; i <= t; i++) o = fmaf(sm.gq[t][i], cc[i], o);
-        p.seam_out[((sg.tok0 + t) * p.h_v + c.h) * 128 + n] = o;
-        bad |= !finite_f(o);
+      for (int t = 0; t < GW; t++) {
+        if (t < sg.nt) {
+          float o = G.ea[t] * __uint_as_float(d[8 + t]);
+#pragma unroll
+          for (int i = 0; i <= t; i++) o = fmaf(G.gq[t][i], cc[i], o);
+          p.seam_out[((sg.tok0 + t) * p.h_v + c.h) * 128 + n] = o;
+          bad |= !finite_f(o);
+        }
       }
     }
   };
 
-  load_bg(0);
-  if (has_seam) ready_group(0);
+  if (preper) {
+    load_bg(0);
+    if (has_seam) prepare(0);
+  }
+  // RN(S_init) -> TMEM A
+#pragma unroll
+  for (int b = 0; b < 4; b++) {
+    uint32_t r[16];
+#pragma unroll
+    for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(exact ? exact[(int64_t)(16 * b + j) * 128] : 0.f);
+    tc::tmem_st16(tAh + 16 * b, r);
+  }
+  tc::tmem_wait_st();
+  tc::tc_fence_before();
+  int slot_next = c.n_seg > 0 ? pair_slot(p, c, 0) : 0;
 
+  // invariant at the top of a segment: TMEM A holds RN(S), the first seam
+  // group is prepared, and the exact S is at `exact` (NULL: zero) whenever
+  // this segment runs a register-path group
   for (int seg = 0; seg < c.n_seg; seg++) {
-    // uniform stop decision
-    if (n == 0) sm.stop = *(volatile int *)&sm.abort;
+    // uniform stop decision (sm.stop is read by all before thread 0 passes
+    // the next barrier)
+    if (tid == 0) sm.stop = *(volatile int *)&sm.abort;
     __syncthreads();
-    const bool stop = *(volatile int *)&sm.stop != 0;
-    __syncthreads();
-    if (stop) break;
+    if (*(volatile int *)&sm.stop != 0) break;
 
-    const int slot = pair_slot(p, c, seg);  // uniform
+    const int slot = slot_next;  // uniform
+    const bool last = seg + 1 == c.n_seg;
+    slot_next = last ? 0 : pair_slot(p, c, seg + 1);
     const bool pair_ok = slot >= 0;
-    if (!pair_ok && n == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
+    if (!pair_ok && tid == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
     const uint32_t q = 4u * (uint32_t)seg;
 
-    // ---- seam groups through the registers: all but the last, or all of
-    // them when the pair is skipped.  S <- e^{lam_last} S + sum_i
-    // e^{lam_last - lam_i} k_i c_i^T with k_i read from the operand tile.
-    const int reg_groups = pair_ok ? c.groups - 1 : c.groups;
-    for (int gi = 0; gi < reg_groups; gi++) {
+    // ---- seam groups on the exact state: all but a fused last group.
+    // S <- e^{lam_last} S + sum_i e^{lam_last - lam_i} k_i c_i^T (k_i from
+    // the operand tile); exact S to S_out, RN(S) to TMEM A.
+    bool fused = false;
+    for (int gi = 0; gi < c.groups; gi++) {
       const int gq = seg * c.groups + gi;
-      if (gi > 0) ready_group(gq);
-      put_A(1.f);
-      tc::tc_fence_before();
-      __syncthreads();
-      if (n == 0) {
+      if (gi > 0) {
+        if (preper) prepare(gq);
+        __syncthreads();
+      }
+      if (gi == c.groups - 1 && pair_ok && sm.gc[gq & 1].alast >= AL_MIN) {
+        fused = true;
+        break;
+      }
+      if (issuer) {
         tc::tc_fence_after();
         if (!aborted(sm)) issue_seam_mma();
         tc::mma_commit(&sm.mma_done);
@@ -793,44 +866,60 @@ __global__ void __launch_bounds__(NT, 2)
       uint32_t d[16];
       tc::tmem_ld16(tD + lane_base, d);
       tc::tmem_wait_ld();
-      tc::tc_fence_before();  // D is rewritten by the next MMA
       if (!aborted(sm)) {
         float cc[GW];
-        seam_recurrence(d, seam_group(p, c, gq), cc);
+        seam_recurrence(d, gq, cc);
+        const GroupConst &G = sm.gc[gq & 1];
 #pragma unroll
-        for (int i = 0; i < GW; i++) cc[i] *= sm.eb[i];
-        const float al = sm.alast;
-        const float *bt = &sm.bt[0][0][0];
+        for (int i = 0; i < GW; i++) cc[i] *= G.eb[i];
+        const float al = G.alast;
+        const float *bt = &sm.bt[0][0][0] + 1024 * hf;  // K-slabs 2*hf, 2*hf+1 hold this thread's rows
+#pragma unroll 1
+        for (int rr = 0; rr < 64; rr++) {
+          float x = al * (exact ? exact[(int64_t)rr * 128] : 0.f);
+          const float *row = bt + (rr >> 5) * 512 + (rr & 3);
+          const int chunk = (rr & 31) >> 2;
 #pragma unroll
-        for (int r = 0; r < 128; r++) {
-          float x = al * S[r];
+          for (int i = 0; i < GW; i++) x = fmaf(row[i * 32 + ((chunk ^ i) << 2)], cc[i], x);
+          out[(int64_t)rr * 128] = x;
+        }
+        exact = out;
+        tc::tc_fence_before();  // the D reads above precede the stores to A
 #pragma unroll
-          for (int i = 0; i < GW; i++)
-            x = fmaf(bt[(r >> 5) * 512 + i * 32 + ((((r & 31) >> 2) ^ i) << 2) + (r & 3)], cc[i], x);
-          S[r] = x;
+        for (int b = 0; b < 4; b++) {
+          uint32_t r[16];
+#pragma unroll
+          for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(out[(int64_t)(16 * b + j) * 128]);
+          tc::tmem_st16(tAh + 16 * b, r);
         }
       }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      __syncthreads();
+      release_raw(gq);
     }
+    const int gq_next = (seg + 1) * c.groups;  // the group that opens the next segment
 
     if (!pair_ok) {
       // a bad slot skips the pair; its slabs (loaded from slot 0) still pass
       // through the ring
-      if (n == 0 && !aborted(sm) && wait_slabs(q)) {
+      if (tid == 0 && !aborted(sm) && wait_slabs(q)) {
         for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
         prefetch_pair(p, c, seg + 2);
       }
-      if (seg + 1 < c.n_seg && has_seam) ready_group((seg + 1) * c.groups);
+      if (preper && !last && has_seam) prepare(gq_next);
+      tc::tc_fence_before();
       continue;
     }
 
-    if (has_seam) {
-      // ---- last seam group, fused with the pair
+    float al = 1.f;
+    if (fused) {
+      // ---- last seam group, fused with the pair.  With S0 the state entering
+      // it (RN in TMEM A), D = T_C S0 + sum_i (T_C k_i) e^{-lam_i} c_i^T and
+      // the segment ends at e^{lam_last} D + S(C|0).
       const int gq = seg * c.groups + c.groups - 1;
-      if (c.groups > 1) ready_group(gq);
-      put_A(1.f);
-      tc::tc_fence_before();
-      __syncthreads();
-      if (n == 0) {
+      al = sm.gc[gq & 1].alast;
+      if (issuer) {
         tc::tc_fence_after();
         if (!aborted(sm)) {
           issue_seam_mma();
@@ -852,111 +941,114 @@ __global__ void __launch_bounds__(NT, 2)
       }
       wait_mma();
       uint32_t d[16];
-      {
+      if (hf == 0) {
+        tc::tmem_ld16(tD + lane_base, d);  // k_t^T S0, q_t^T S0
+      } else {
         uint32_t e[16];
-        tc::tmem_ld16(tD + lane_base, d);
-        tc::tmem_ld16(tD + lane_base + 16, e);
+        tc::tmem_ld16(tD + lane_base + 16, e);  // (T_C k_i)[n]
         tc::tmem_wait_ld();
         float tkr[GW];
 #pragma unroll
         for (int i = 0; i < GW; i++) tkr[i] = __uint_as_float(e[i]);
         store_row_sw32(sm.tk, n, tkr);
+        tc::fence_proxy_async_smem();
       }
-      // A <- e^{lam_last} S0 for the T_C product (after the reads above)
-      tc::tc_fence_before();
-      put_A(sm.alast);
-      tc::fence_proxy_async_smem();
+      tc::tmem_wait_ld();
       tc::tc_fence_before();
       __syncthreads();
-      if (n == 0) {
-        tc::tc_fence_after();
-        if (!aborted(sm)) issue_T_mma(q);
-      }
-      // while it runs: the group's recurrence and outputs, then the rank-8
-      // seam term sum_i (T_C k_i) e^{lam_last - lam_i} c_i^T onto D
-      {
+      if (hf == 0) {
+        // warps 0..3, while the product runs: the group's recurrence and
+        // outputs, and the seam term tile
         float cc[GW];
         if (!aborted(sm)) {
-          seam_recurrence(d, seam_group(p, c, gq), cc);
+          seam_recurrence(d, gq, cc);
+          const GroupConst &G = sm.gc[gq & 1];
 #pragma unroll
-          for (int i = 0; i < GW; i++) cc[i] *= sm.eb[i];
+          for (int i = 0; i < GW; i++) cc[i] *= G.eb[i] / al;  // e^{-lam_i} c_i
         } else {
 #pragma unroll
           for (int i = 0; i < GW; i++) cc[i] = 0.f;
         }
         store_row_sw32(sm.cp, n, cc);
-      }
-      tc::fence_proxy_async_smem();
-      __syncthreads();
-      if (n == 0) {
-        if (!aborted(sm)) {
-          const uint64_t ad = tc::smem_desc(tc::smem_u32(&sm.cp[0][0]), 16, 256, tc::SW_32B);
-          const uint64_t bd = tc::smem_desc(tc::smem_u32(&sm.tk[0][0]), 16, 256, tc::SW_32B);
-          tc::mma_ss_tf32(tD, ad, bd, id_T, 1);
+        tc::fence_proxy_async_smem();
+        tc::named_bar(BAR_CORR, 160);
+      } else if (warp == ISSUER_WARP) {
+        if (issuer) {
+          tc::tc_fence_after();
+          if (!aborted(sm)) issue_T_mma(q);
         }
-        tc::mma_commit(&sm.mma_done);
+        tc::named_bar(BAR_CORR, 160);
+        if (issuer) {
+          if (!aborted(sm)) {
+            const uint64_t ad = tc::smem_desc(tc::smem_u32(&sm.cp[0][0]), 16, 256, tc::SW_32B);
+            const uint64_t bd = tc::smem_desc(tc::smem_u32(&sm.tk[0][0]), 16, 256, tc::SW_32B);
+            tc::mma_ss_tf32(tD, ad, bd, id_T, 1);
+          }
+          tc::mma_commit(&sm.mma_done);
+        }
+        __syncwarp();
+      } else if (!last) {
+        // warps 5..7: the group that opens the next segment
+        prepare(gq_next);
       }
-      // ... and the preparation of the group that opens the next segment
-      if (seg + 1 < c.n_seg) ready_group((seg + 1) * c.groups);
+      release_raw(gq);
     } else {
-      put_A(1.f);
-      tc::tc_fence_before();
-      __syncthreads();
-      if (n == 0) {
+      if (issuer) {
         tc::tc_fence_after();
         if (!aborted(sm) && wait_slabs(q)) issue_T_mma(q);
         tc::mma_commit(&sm.mma_done);
       }
+      if (preper && has_seam && !last) prepare(gq_next);
     }
 
+    // ---- S <- al D + S(C|0) for this thread's 64 rows (all loads issued
+    // before the wait); RN(S) back to TMEM A, the exact S to S_out where needed
     const bool use = !aborted(sm);
-    const float *Sc = p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128 + n;
-    float nxt[32];
+    const float *Sc = p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128 + (int64_t)(64 * hf) * 128 + n;
+    float sc[64];
 #pragma unroll
-    for (int j = 0; j < 32; j++) nxt[j] = use ? Sc[j * 128] : 0.f;
+    for (int j = 0; j < 64; j++) sc[j] = use ? Sc[j * 128] : 0.f;
+    // the next segment's first group is prepared (and visible) past here
+    if (has_seam) __syncthreads();
+    // the exact state is needed after this segment if it is the last one or
+    // if the next one runs a register-path group
+    const bool keep = last || slot_next < 0 || c.groups > 1 || (has_seam && sm.gc[gq_next & 1].alast < AL_MIN);
     wait_mma();
-    if (n == 0 && !aborted(sm)) {
+    if (tid == 0 && !aborted(sm)) {
       // this pair's four slots are free: refill them, and warm L2 with the
       // pair of the segment after next
       for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
       prefetch_pair(p, c, seg + 2);
     }
-
-    // ---- S <- D + S(C|0)
+    if (use) {
 #pragma unroll
-    for (int ch = 0; ch < 4; ch++) {
-      float cur[32];
-#pragma unroll
-      for (int j = 0; j < 32; j++) cur[j] = nxt[j];
-      if (ch < 3) {
-#pragma unroll
-        for (int j = 0; j < 32; j++) nxt[j] = use ? Sc[(32 * (ch + 1) + j) * 128] : 0.f;
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
+      for (int b = 0; b < 4; b++) {
         uint32_t r[16];
-        tc::tmem_ld16(tD + lane_base + 32 * ch + 16 * hh, r);
+        tc::tmem_ld16(tDh + 16 * b, r);
         tc::tmem_wait_ld();
-        if (use) {
 #pragma unroll
-          for (int j = 0; j < 16; j++) S[32 * ch + 16 * hh + j] = __uint_as_float(r[j]) + cur[16 * hh + j];
+        for (int j = 0; j < 16; j++) {
+          const float x = fmaf(al, __uint_as_float(r[j]), sc[16 * b + j]);
+          if (keep) out[(int64_t)(16 * b + j) * 128] = x;
+          if (last) bad |= !finite_f(x);
+          r[j] = tc::to_tf32(x);
         }
+        tc::tmem_st16(tAh + 16 * b, r);
       }
+      if (keep) exact = out;
     }
-    tc::tc_fence_before();  // TMEM reads done before the next MMA overwrites D
+    tc::tmem_wait_st();
+    tc::tc_fence_before();  // TMEM reads and writes done before the next MMA
   }
 
-  __syncthreads();
-  if (!aborted(sm)) {
-#pragma unroll
-    for (int i = 0; i < 128; i++) {
-      p.S_out[state + (int64_t)i * 128 + n] = S[i];
-      bad |= !finite_f(S[i]);
-    }
+  // no segment at all: the state passes through
+  if (c.n_seg == 0) {
+#pragma unroll 8
+    for (int i = 0; i < 64; i++) out[(int64_t)i * 128] = exact ? exact[(int64_t)i * 128] : 0.f;
   }
   if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
-  // drain: every copy thread 0 issued lands before the CTA releases its smem
-  if (n == 0) {
+  // drain: every copy issued lands before the CTA releases its smem
+  if (tid == 0) {
     const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
     for (uint32_t r = first; r < issued; r++) tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, DRAIN_LIMIT);
     for (int r = raw_issued > 2 ? raw_issued - 2 : 0; r < raw_issued; r++)
@@ -1029,7 +1121,7 @@ cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaS
   a.p = p;
   a.wait_limit = wait_limit;
   a.debug_stall = debug_stall() ? 1 : 0;
-  kern<<<grid, NT, smem, s>>>(a, tmap);
+  kern<<<grid, vec ? NT : NT2, smem, s>>>(a, tmap);
   return cudaGetLastError();
 }
 
