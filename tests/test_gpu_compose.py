@@ -127,3 +127,20 @@ def test_compose_tc_bounded_wait_reports_timeout():
     assert r.returncode == 0, r.stderr[-2000:]
     line = [ln for ln in r.stdout.splitlines() if ln.startswith("STATUS")][-1]
     assert line.split()[1] == "5" and line.split()[3] == "4.0", line
+
+
+@pytest.mark.parametrize("variant", ["deltanet", "gdn"])
+def test_compose_tc_long_chain(variant):
+    """100 lognormal segments (the warm-prompt length law), w = 8, random
+    S_init.  With alpha = 1 (DeltaNet) T_C stays of order one, so the
+    tensor-core rounding of T_C and of the state enters all 100 products of
+    the chain; the error must stay within the bf16 bar at the far end."""
+    W = si.workload(4, device=DEV, variant=variant, n_layers=1, h_k=1, h_v=4)
+    S_init = si.random_state((1, W.h_v, 128, 128), seed=1, cfg=4, device=DEV)
+    T_pool, S_pool, sa, slot, S_out, seam_out = _run(W, 1, S_init=S_init)
+    So, seam = _oracle_compose(W, T_pool, S_pool, sa, slot, S_init, 1)
+    e1 = per_head_rel_err(S_out, So).max()
+    e2 = per_head_rel_err(seam_out.permute(0, 3, 1, 2, 4).reshape(1, W.h_v, -1),
+                          np.transpose(seam, (0, 3, 1, 2, 4)).reshape(1, W.h_v, -1), inner=1).max()
+    print(f"{variant} 100-segment chain: state {e1:.2e}, seam outputs {e2:.2e}")
+    assert e1 <= TOL_BF16 and e2 <= TOL_BF16, (e1, e2)
