@@ -88,8 +88,47 @@ def compose_flops(n_layers, n_seg, w, h_v, d_k=128, d_v=128):
     return n_layers * n_seg * h_v * (ts + seam)
 
 
+# ---------------------------------------------------------------- ncu traffic
+KERNEL_SOURCES = {
+    "build": ("build_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
+    "compose": ("compose_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
+}
+PROFILE_FILES = {"build": "segment_build_tc__gdn_16x1024.md", "compose": "compose_seam_mma__gdn_4x32x100.md"}
+
+
+def source_hash(kind):
+    """sha256 over the kernel's source files: a captured traffic figure is
+    only reported while the kernel is unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "hybrid_linear_attention_chunkwise_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(kind, units_full):
+    """DRAM bytes per full launch from the committed ncu summary of a small
+    case (scaled by the units processed), or None when the summary is missing
+    or was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", PROFILE_FILES[kind])
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.split(":", 1)[0].strip() in ("source_sha256", "dram_bytes_per_unit"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip().split()[0]
+    if vals.get("source_sha256") != source_hash(kind) or "dram_bytes_per_unit" not in vals:
+        return None
+    return float(vals["dram_bytes_per_unit"]) * units_full
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi clock / throttle samples every 50 ms; `region()` marks the
+    timed region, and the summary uses the samples taken inside it (or the
+    nearest ones when the region is shorter than the sampling period)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -97,22 +136,33 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (time, line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.time() + 3.0
+            while not self.lines and time.time() < deadline:
+                time.sleep(0.01)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        time.sleep(0.06)  # one more sample after the region
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -123,9 +173,16 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        lines = self.lines
+        if self.t0 is not None and self.t1 is not None and lines:
+            inside = [x for x in lines if self.t0 <= x[0] <= self.t1]
+            if not inside:
+                mid = 0.5 * (self.t0 + self.t1)
+                inside = sorted(lines, key=lambda x: abs(x[0] - mid))[:2]
+            lines = inside
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for _, ln in lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -187,6 +244,39 @@ def setup_compose(dev, hy, seed=0, n_layers=30):
 
 
 # ---------------------------------------------------------------- CPU oracle leg
+def run_profile_case(kind):
+    """One small case of one kernel for an ncu capture: two warm-up launches,
+    then the launch to capture.  Inputs are larger than L2 and a few GB at
+    most.  build: GDN, 16 segments x 1024 tokens, h_k = 16, h_v = 32 (512
+    (segment, head) pairs); compose: 4 GDN layers x 32 heads x 100 segments, w = 8 (12800
+    pairs, 1.7 GB pool)."""
+    import torch
+    import hybrid_linear_attention_chunkwise_gb300 as hy
+    import synth_inputs as si
+    dev = torch.device("cuda", 0)
+    hy.load()
+    if kind == "build":
+        W = si.workload(3, seed=0, device=dev, n_seg=16)
+        L = W.layers[0]
+        T = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_k), device=dev)
+        S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
+        ws = hy.alloc_workspace(hy.build_workspace_bytes(W.n_seg, W.h_k, W.h_v, W.d_k, W.d_v), dev)
+        run = lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=W.seam_w,
+                                       T_pool=T, S_pool=S, workspace=ws)
+        units = W.n_seg * W.h_v
+    else:
+        comp = setup_compose(dev, hy, n_layers=4)
+        sa = comp["sa"]
+        run = lambda: hy.compose(comp["slot"], comp["T_pool"], comp["S_pool"], sa["k"], sa["v"], sa["q"], sa["g"],
+                                 sa["beta"], variant="gdn", S_out=comp["S_out"], seam_out=comp["seam_out"])
+        units = comp["n_layers"] * comp["W"].n_seg * comp["W"].h_v
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": kind, "units_per_launch": units, "source_sha256": source_hash(kind)}), flush=True)
+    return 0
+
+
 def oracle_build_sample(W, n_seg_sample, threads):
     import oracle
     L = W.layers[0]
@@ -246,13 +336,17 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["build", "compose"], default=None,
+                    help="run one small case of one kernel (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile_case(args.profile)
 
     import torch
     import torch.distributed as dist
@@ -267,12 +361,14 @@ def main():
     peaks = _peaks()
 
     # ---- set-up (untimed): inputs resident in HBM
-    W3 = setup_build(dev)
+    # weak scaling: each rank runs its own shard of independent units (seeded
+    # by rank); no data-path exchange between ranks
+    W3 = setup_build(dev, seed=rank)
     L3 = W3.layers[0]
     T3 = torch.empty((W3.n_seg, W3.h_v, W3.d_k, W3.d_k), device=dev)
     S3 = torch.empty((W3.n_seg, W3.h_v, W3.d_k, W3.d_v), device=dev)
     ws3 = hy.alloc_workspace(hy.build_workspace_bytes(W3.n_seg, W3.h_k, W3.h_v, W3.d_k, W3.d_v), dev)
-    comp = setup_compose(dev, hy)
+    comp = setup_compose(dev, hy, seed=rank)
     W4 = comp["W"]
     stream = torch.cuda.current_stream()
 
@@ -296,6 +392,7 @@ def main():
         if ws > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        clk.start()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -307,6 +404,7 @@ def main():
             ev[i][2].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        clk.stop()
         if ws > 1:
             dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -326,11 +424,13 @@ def main():
     b_tflops = bflops / (b_ms * 1e-3) / 1e12
     c_gbs = cbytes / (c_ms * 1e-3) / 1e9
     roof_build = {"bound": "tensor", "achieved": b_tflops, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                  "frac": b_tflops / peaks["bf16"], "traffic": None,
-                  "kernel": "segment build", "peak_source": peaks["src"] + " bf16 dense (burst)"}
+                  "frac": b_tflops / peaks["bf16"], "traffic": captured_traffic("build", W3.n_seg * W3.h_v),
+                  "kernel": "segment build", "algorithmic": bbytes,
+                  "peak_source": peaks["src"] + " bf16 dense (burst)"}
     roof_comp = {"bound": "hbm", "achieved": c_gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                 "frac": c_gbs / peaks["hbm"], "traffic": None, "kernel": "compose",
-                 "peak_source": peaks["src"] + " HBM copy"}
+                 "frac": c_gbs / peaks["hbm"],
+                 "traffic": captured_traffic("compose", comp["n_layers"] * W4.n_seg * W4.h_v),
+                 "kernel": "compose", "algorithmic": cbytes, "peak_source": peaks["src"] + " HBM copy"}
     dominant = roof_comp if c_ms >= b_ms else roof_build
 
     # ---- end to end through the public API with host buffers

@@ -283,3 +283,13 @@ def plan_lpt(costs, n_workers: int):
     if rc != OK:
         raise HypicError(rc, "hypic_plan_lpt")
     return order, worker, int(mk.value)
+
+
+def shard_lpt(costs, world_size: int):
+    """Multi-GPU partition of independent units (cold segments to build, or
+    (layer, head) chains to compose) over ranks by the same LPT rule the
+    pages use to balance segments over scatter workers (nav.aitube.vip
+    §2.3).  Returns one sorted index array per rank; every unit lands on
+    exactly one rank and the units need no exchange while they run."""
+    _, worker, _ = plan_lpt(costs, world_size)
+    return [np.sort(np.nonzero(worker == r)[0]) for r in range(int(world_size))]

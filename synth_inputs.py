@@ -22,7 +22,7 @@ Shapes and distributions follow the five workloads of the HYPIC state algebra:
 
 Draws: k ~ N(0,1) then L2-normalised (in fp64); v, q ~ N(0,1);
 beta = sigmoid(N(0,1)); gates are stored as log-gates g = log(alpha):
-config 1 g = -u, u ~ U(0.001, 0.1); configs 3-5 g ~ U(-0.1, -0.001);
+workload 1 g = -u, u ~ U(0.001, 0.1); workloads 3-5 g ~ U(-0.1, -0.001);
 per-channel g = -softplus(N(0,1)).  Every tensor is rounded once to its
 storage dtype (fp32 or bf16, round-to-nearest-even); the oracle reads the
 rounded values upcast to fp64.
