@@ -123,7 +123,7 @@ int hypic_plan_lpt(const int64_t *costs, int32_t n_items, int32_t n_workers, int
 
 size_t hypic_build_workspace_bytes(const hypic_build_desc *d) {
   if (!d || d->n_seg < 0 || d->h_v < 1) return 0;
-  return plan_bytes(2 * n_build_items(d));  // room for two items per pair (tensor-core path)
+  return plan_bytes(2 * n_build_items(d));  // room for up to two items per pair
 }
 
 int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
@@ -176,10 +176,10 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
   p.status = d->status;
   // bf16 scalar-gate delta rules with 128-wide heads run chunkwise on the
-  // tensor cores, one item per half of [T | S]; every other case runs the
-  // fp32 token recurrence, one item per (segment, head)
+  // tensor cores; every other case runs the fp32 token recurrence.  Both
+  // take one item per (segment, value head).
   const bool tc_path = build_tc_supported(p);
-  const int parts = tc_path ? 2 : 1;
+  const int parts = 1;
 
   const int64_t n_pairs = n_build_items(d);
   const int64_t n_items = n_pairs * parts;

@@ -23,7 +23,7 @@ namespace {
 constexpr size_t kScratchBytes = (size_t)HYPIC_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
-// Plan header + two items per (segment, head) pair fill the array exactly at
+// Plan header + up to two items per (segment, head) pair fit the array at
 // the stated maximum number of pairs.
 static_assert(sizeof(PlanHeader) + 2 * (size_t)HYPIC_NOALLOC_MAX_PAIRS * sizeof(BuildItem) <= kScratchBytes,
               "pair limit does not fit the fixed scratch");
@@ -137,7 +137,7 @@ int hypic_segment_build_noalloc(const hypic_build_desc *d, hypic_stream_t stream
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
   p.status = d->status;
   const bool tc_path = build_tc_supported(p);
-  const int parts = tc_path ? 2 : 1;
+  const int parts = 1;  // one item per (segment, value head) on both paths
   const int64_t n_items = (int64_t)d->n_seg * d->h_v * parts;
 
   // Plan in the static host buffer: the ticket starts at zero, items go

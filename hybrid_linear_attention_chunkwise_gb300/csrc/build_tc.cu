@@ -14,10 +14,11 @@
 // oracle).
 //
 // Layout.  The kernel works on X^T, whose rows are the 256 columns of
-// [T | S].  The T half and the S half are independent chains that share W,
-// so each CTA owns one half of one (segment, head): a 128 x 128 block of
-// X^T, kept in TMEM as the fp32 accumulator (lane j = column j of the half,
-// TMEM column d) next to a tf32-rounded copy, the A operand of chain 1.
+// [T | S].  The T half and the S half are independent chains that share the
+// chunk's preparation (W, and U for S), so one CTA owns one (segment, head):
+// both 128 x 128 halves of X^T stay in TMEM as fp32 accumulators (lane j =
+// column j of the half, TMEM column d), and one tf32-rounded copy, the A
+// operand of chain 1, is restaged for each half in turn.
 // The TMA-loaded bf16 K and V tiles [64 tokens x 128] are MMA operands as
 // they land -- K-major for the Gram, MN-major (transposed view) elsewhere --
 // so no operand is ever transposed by the threads.
@@ -28,10 +29,11 @@
 //       UT     A = (I + M)^-1                     SIMT, 16 x 16 blocks
 //       W, U   W^T = K^T (A diag(bG))^T,  U^T = V^T (A diag(b))^T
 //                                                 kind::f16, factors split hi + lo
-//       and stages W (tf32, rounded) as the B operand of chain 1;
-//   X (warps 0-3) advances the state through chunk c
-//       chain 1  Y^T = X^T W^T                    kind::tf32, A from TMEM
-//       Ytilde   = -(Y - [0 | U]) diag(exp(lam_C - lam)), split hi + lo
+//       and stages W (tf32, rounded) as the B operand of chain 1; U goes
+//       straight to the chain-1 accumulator as -U^T;
+//   X (warps 0-3) advances both halves through chunk c, S half first
+//       chain 1  Y^T = X^T W^T (- U^T)            kind::tf32, A from TMEM
+//       Ytilde   = -Y diag(exp(lam_C - lam)), split hi + lo
 //       chain 2  X^T = G_C X^T + Ytilde^T K       kind::f16 (B = K tile, MN-major)
 // handing off through mbarriers.  Split operands make W, U and chain 2 exact
 // to ~2^-17 (K and V are exact bf16); chain 1 uses tf32 operands rounded to
@@ -39,7 +41,7 @@
 // fp32 accumulation throughout.  This keeps long products (8192 tokens)
 // inside 5e-3 per head.
 //
-// Items are (segment, value head, half) in LPT order, pulled by an atomic
+// Items are (segment, value head) in LPT order, pulled by an atomic
 // ticket.  Inputs come in by TMA (3-D maps over [token, head, channel],
 // 128-byte swizzle) through three buffers, two chunks ahead of their use.
 // All waits are bounded.
@@ -62,12 +64,11 @@ constexpr int BAR_X = 1, BAR_P = 2;  // named barriers of the two groups
 constexpr uint32_t DRAIN_LIMIT = 1u << 22;
 
 // TMEM columns (512 allocated, one CTA per SM)
-constexpr uint32_t TM_X = 0;     // X^T half, fp32 accumulator      (X group)
-constexpr uint32_t TM_XR = 128;  // tf32-rounded copy: A of chain 1 (X group)
-constexpr uint32_t TM_Y = 256;   // chain 1 output                  (X group)
-constexpr uint32_t TM_W = 320;   // W^T                             (P group)
-constexpr uint32_t TM_U = 384;   // U^T (S half)                    (P writes, X reads)
-constexpr uint32_t TM_G = 448;   // K K^T, lanes 0..63              (P group)
+constexpr uint32_t TM_XT = 0;    // T half of X^T, fp32 accumulator  (X group)
+constexpr uint32_t TM_XS = 128;  // S half of X^T, fp32 accumulator  (X group)
+constexpr uint32_t TM_XR = 256;  // tf32-rounded copy of the half being chained: A of chain 1
+constexpr uint32_t TM_Y = 384;   // chain 1 output; -U^T written there by P before the S half's chain 1
+constexpr uint32_t TM_WG = 448;  // K K^T (lanes 0..63), then W^T   (P group)
 
 // Byte offsets in K-major, 128-byte-swizzled tiles of R rows (the layout the
 // shared-memory descriptors describe and TMA writes): 4-byte elements sit 32
@@ -96,7 +97,7 @@ __device__ __forceinline__ uint64_t mndesc16(uint32_t base, int t) {
 
 struct __align__(1024) BuildTcSmem {
   // inputs as TMA tiles [64 t x 128] bf16 in two 64-channel slabs: K of
-  // chunk c in kin[c % 3] (read by P's Gram and W and by X's chain 2 one
+  // chunk c in kin[c % 3] (read by P's Gram and W and by X's chains 2 one
   // chunk later), V in vin[c % 2] (read only by P's U MMA).  V follows K so
   // the Gram's padded rows 64..127 read valid (ignored) bytes.
   unsigned char kin[NBUF][16384];
@@ -122,8 +123,9 @@ struct __align__(1024) BuildTcSmem {
   float gc[3];                  // G_C of chunk c in [c % 3] (read by X)
   uint64_t full[NBUF];
   uint64_t bar_g, bar_wu;       // P's MMA completions
-  uint64_t bar_y, bar_x;        // X's MMA completions (P also waits on them)
-  uint64_t wt_ready, ys_done;   // P -> X: W staged; X -> P: U consumed
+  uint64_t bar_y1, bar_y2;      // X's chain 1 completions (S half, T half; P waits on the T half's)
+  uint64_t bar_x1, bar_x2;      // X's chain 2 completions (S half, T half; P waits on the T half's)
+  uint64_t wt_ready, ys_done;   // P -> X: W staged, -U in place; X -> P: chain-1 output consumed
   uint64_t never;
   uint32_t tmem_base;
   int item;
@@ -230,7 +232,7 @@ __device__ void ut_inverse(BuildTcSmem &sm, int q) {
 
 // Split factor tiles A diag(bG) and A diag(b) (K-major bf16 [64 t x 64 t'],
 // hi and lo): thread q writes 32 consecutive t' of row q / 2.
-__device__ __forceinline__ void write_factors(BuildTcSmem &sm, int q, bool s_half) {
+__device__ __forceinline__ void write_factors(BuildTcSmem &sm, int q) {
   const int t = q >> 1, q0 = 32 * (q & 1);
 #pragma unroll
   for (int h8 = 0; h8 < 4; h8++) {
@@ -252,33 +254,29 @@ __device__ __forceinline__ void write_factors(BuildTcSmem &sm, int q, bool s_hal
     const uint32_t off = sw16(t, c0, 64);
     *reinterpret_cast<uint4 *>(sm.bwh + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
     *reinterpret_cast<uint4 *>(sm.bwl + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-    if (s_half) {
-      *reinterpret_cast<uint4 *>(sm.buh + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
-      *reinterpret_cast<uint4 *>(sm.bul + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
-    }
+    *reinterpret_cast<uint4 *>(sm.buh + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+    *reinterpret_cast<uint4 *>(sm.bul + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
   }
 }
 
 // K (and, for the S half, V) of chunk `ch` of item `it`
-__device__ __forceinline__ void issue_chunk(BuildTcSmem &sm, const BuildItem &it, int ch, bool s_half, int kh,
+__device__ __forceinline__ void issue_chunk(BuildTcSmem &sm, const BuildItem &it, int ch, int kh,
                                             const CUtensorMap *tk, const CUtensorMap *tv) {
   const int32_t t0 = (int32_t)(it.start + (int64_t)C * ch);
   const int bk = ch % NBUF, bv = ch & 1;
-  tc::mbar_expect_tx(&sm.full[bk], s_half ? 32768u : 16384u);
+  tc::mbar_expect_tx(&sm.full[bk], 32768u);
   for (int s = 0; s < 2; s++) tc::tma_load_3d(sm.kin[bk] + s * 8192, tk, 64 * s, kh, t0, &sm.full[bk]);
-  if (s_half)
-    for (int s = 0; s < 2; s++) tc::tma_load_3d(sm.vin[bv] + s * 8192, tv, 64 * s, it.head, t0, &sm.full[bk]);
+  for (int s = 0; s < 2; s++) tc::tma_load_3d(sm.vin[bv] + s * 8192, tv, 64 * s, it.head, t0, &sm.full[bk]);
 }
 struct ItemCtx {
   BuildItem it;
-  bool s_half;
   int kh;
   int n_ch;
   uint32_t gch0;  // index of the item's first chunk in this CTA's chunk sequence
 };
 
 struct MmaIds {
-  uint32_t gram, wu, c1, c2;
+  uint32_t gram, wu, wu_neg, c1, c2;
 };
 
 // ---------------------------------------------------------------- P group
@@ -310,7 +308,7 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
       const int r = nt + (e >> 4), s = (e >> 3) & 1, c16 = e & 7;
       const uint4 z = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4 *>(kin + s * 8192 + r * 128 + c16 * 16) = z;
-      if (x.s_half) *reinterpret_cast<uint4 *>(vin + s * 8192 + r * 128 + c16 * 16) = z;
+      *reinterpret_cast<uint4 *>(vin + s * 8192 + r * 128 + c16 * 16) = z;
     }
   }
   if (q < C) {
@@ -358,7 +356,7 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
     const uint32_t kb = tc::smem_u32(kin);
 #pragma unroll
     for (int ks = 0; ks < 8; ks++)
-      tc::mma_ss_f16(tm + TM_G, kdesc16(kb, 16 * ks, 64), kdesc16(kb, 16 * ks, 64), id.gram, ks > 0);
+      tc::mma_ss_f16(tm + TM_WG, kdesc16(kb, 16 * ks, 64), kdesc16(kb, 16 * ks, 64), id.gram, ks > 0);
     tc::mma_commit(&sm.bar_g);
   }
   wait_phase(sm, p, &sm.bar_g, g, DRAIN_LIMIT);
@@ -372,7 +370,7 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
     for (int c0 = 0; c0 < 64; c0 += 32) {
       uint32_t r[32];
       float li[32];
-      tc::tmem_ld32(trow(tm + TM_G, c0), r);
+      tc::tmem_ld32(trow(tm + TM_WG, c0), r);
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {  // into registers before any store
         const float4 l4 = *reinterpret_cast<const float4 *>(fact ? &sm.eb[c0 + j] : &sm.lam[c0 + j]);
@@ -392,13 +390,14 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
   }
   tc::named_bar(BAR_P, NG);
   ut_inverse(sm, q);
-  write_factors(sm, q, x.s_half);
+  write_factors(sm, q);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   tc::named_bar(BAR_P, NG);
-  // ---- W^T = K^T (A diag(bG))^T;  S half: U^T = V^T (A diag(b))^T once X
-  // has consumed the previous chunk's U
-  if (x.s_half && g > 0) wait_phase(sm, p, &sm.ys_done, g - 1, LIM);
+  // ---- W^T = K^T (A diag(bG))^T, and -U^T = -V^T (A diag(b))^T straight
+  // into the chain-1 accumulator once X has consumed the previous chunk's
+  // chain-1 output
+  if (g > 0) wait_phase(sm, p, &sm.ys_done, g - 1, LIM);
   if (q == 0) {
     tc::tc_fence_after();
     const uint32_t kb = tc::smem_u32(kin), vb = tc::smem_u32(vin);
@@ -406,24 +405,23 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
     const uint32_t uh = tc::smem_u32(sm.buh), ul = tc::smem_u32(sm.bul);
 #pragma unroll
     for (int ks = 0; ks < 4; ks++) {
-      tc::mma_ss_f16(tm + TM_W, mndesc16(kb, 16 * ks), kdesc16(wh, 16 * ks, 64), id.wu, ks > 0);
-      tc::mma_ss_f16(tm + TM_W, mndesc16(kb, 16 * ks), kdesc16(wl, 16 * ks, 64), id.wu, 1u);
-      if (x.s_half) {
-        tc::mma_ss_f16(tm + TM_U, mndesc16(vb, 16 * ks), kdesc16(uh, 16 * ks, 64), id.wu, ks > 0);
-        tc::mma_ss_f16(tm + TM_U, mndesc16(vb, 16 * ks), kdesc16(ul, 16 * ks, 64), id.wu, 1u);
-      }
+      tc::mma_ss_f16(tm + TM_WG, mndesc16(kb, 16 * ks), kdesc16(wh, 16 * ks, 64), id.wu, ks > 0);
+      tc::mma_ss_f16(tm + TM_WG, mndesc16(kb, 16 * ks), kdesc16(wl, 16 * ks, 64), id.wu, 1u);
+      tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(uh, 16 * ks, 64), id.wu_neg, ks > 0);
+      tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(ul, 16 * ks, 64), id.wu_neg, 1u);
     }
     tc::mma_commit(&sm.bar_wu);
   }
   wait_phase(sm, p, &sm.bar_wu, g, DRAIN_LIMIT);
   tc::tc_fence_after();
-  // ---- stage W (tf32, rounded) as chain 1's B tile once chain 1 of the
-  // previous chunk is done with it (each warp writes whole row segments)
-  if (g > 0) wait_phase(sm, p, &sm.bar_y, g - 1, LIM);
+  // ---- stage W (tf32, rounded) as chain 1's B tile once the last chain 1
+  // of the previous chunk (T half) is done with it (each warp writes whole
+  // row segments)
+  if (g > 0) wait_phase(sm, p, &sm.bar_y2, g - 1, LIM);
 #pragma unroll
   for (int c0 = 0; c0 < 64; c0 += 32) {
     uint32_t r[32];
-    tc::tmem_ld32(trow(tm + TM_W, c0), r);
+    tc::tmem_ld32(trow(tm + TM_WG, c0), r);
     tc::tmem_wait_ld();
 #pragma unroll
     for (int j = 0; j < 32; j++)
@@ -434,12 +432,12 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
   tc::named_bar(BAR_P, NG);
   if (q == 0) {
     // chunk ch + 2 goes to K buffer (ch + 2) % 3 = (ch - 1) % 3, free once X's
-    // chain 2 of chunk ch - 1 is done (waited before wt_ready, so the phase
-    // waited on is the latest one), and to V buffer ch % 2, whose U MMA above
-    // is complete
+    // last chain 2 of chunk ch - 1 (T half) is done (waited before
+    // wt_ready, so the phase waited on is the latest one), and to V buffer
+    // ch % 2, whose U MMA above is complete
     if (ch + 2 < x.n_ch) {
-      if (ch >= 1) wait_phase(sm, p, &sm.bar_x, g - 1, LIM);
-      if (!aborted(sm)) issue_chunk(sm, it, ch + 2, x.s_half, x.kh, tk, tv);
+      if (ch >= 1) wait_phase(sm, p, &sm.bar_x2, g - 1, LIM);
+      if (!aborted(sm)) issue_chunk(sm, it, ch + 2, x.kh, tk, tv);
     }
     tc::mbar_arrive(&sm.wt_ready);
   }
@@ -448,47 +446,57 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
 }
 
 // ---------------------------------------------------------------- X group
-// Advances the state half through chunk ch (n = thread = TMEM lane).
-__device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx &x, int ch, int n, uint32_t tm,
-                            const MmaIds &id, uint32_t LIM) {
-  const uint32_t g = x.gch0 + (uint32_t)ch;
-  const int bk = ch % NBUF, b3 = (int)(g % 3);
-  wait_phase(sm, p, &sm.wt_ready, g, LIM);
-  tc::tc_fence_after();
-  // ---- X *= G_C (the accumulator; chain 1 reads the rounded copy)
-  {
-    const float gC = sm.gc[b3];
+// XR <- RN(X_h) (chain 1 reads the start-of-chunk state), X_h <- G_C X_h
+// (the accumulator chain 2 adds onto), in one pass over the half.
+__device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC) {
 #pragma unroll
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-      uint32_t r[32];
-      tc::tmem_ld32(trow(tm + TM_X, c0), r);
-      tc::tmem_wait_ld();
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    uint32_t r[32], xr[32];
+    tc::tmem_ld32(trow(tm + tx, c0), r);
+    tc::tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; j++) r[j] = __float_as_uint(gC * __uint_as_float(r[j]));
-      tc::tmem_st32(trow(tm + TM_X, c0), r);
+    for (int j = 0; j < 32; j++) {
+      const float v = __uint_as_float(r[j]);
+      xr[j] = tc::to_tf32(v);
+      r[j] = __float_as_uint(gC * v);
     }
-    tc::tmem_wait_st();
+    tc::tmem_st32(trow(tm + TM_XR, c0), xr);
+    tc::tmem_st32(trow(tm + tx, c0), r);
   }
-  tc::tc_fence_before();
-  tc::named_bar(BAR_X, NG);
-  // ---- chain 1: Y^T = X^T W^T
-  if (n == 0) {
-    tc::tc_fence_after();
-    const uint32_t wb = tc::smem_u32(sm.wt);
-#pragma unroll
-    for (int ks = 0; ks < 16; ks++)
-      tc::mma_ts_tf32(tm + TM_Y, tm + TM_XR + 8 * ks, kdesc32(wb, 8 * ks, 64), id.c1, ks > 0);
-    tc::mma_commit(&sm.bar_y);
-  }
-  wait_phase(sm, p, &sm.bar_y, g, DRAIN_LIMIT);
+  tc::tmem_wait_st();
+}
+
+// chain 1 into TM_Y: Y^T (+)= XR^T W^T (issued by lane 0 of the group)
+__device__ __forceinline__ void issue_chain1(BuildTcSmem &sm, uint32_t tm, const MmaIds &id, bool onto_u,
+                                             uint64_t *bar) {
   tc::tc_fence_after();
-  // ---- Ytilde = -(Y - [0 | U]) diag(exp(lam_C - lam_t)), split hi + lo, as
-  // the K-major A tiles [128 j x 64 t] of chain 2
+  const uint32_t wb = tc::smem_u32(sm.wt);
+#pragma unroll
+  for (int ks = 0; ks < 16; ks++)
+    tc::mma_ts_tf32(tm + TM_Y, tm + TM_XR + 8 * ks, kdesc32(wb, 8 * ks, 64), id.c1, (onto_u || ks > 0) ? 1u : 0u);
+  tc::mma_commit(bar);
+}
+
+// chain 2 into the half tx: X^T += Ytilde^T K (B = the chunk's K tile, MN-major)
+__device__ __forceinline__ void issue_chain2(BuildTcSmem &sm, uint32_t tm, uint32_t tx, int bk, const MmaIds &id,
+                                             uint64_t *bar) {
+  tc::tc_fence_after();
+  const uint32_t kb = tc::smem_u32(sm.kin[bk]), yhb = tc::smem_u32(sm.yh), ylb = tc::smem_u32(sm.yl);
+#pragma unroll
+  for (int ks = 0; ks < 4; ks++) {
+    tc::mma_ss_f16(tm + tx, kdesc16(yhb, 16 * ks, 128), mndesc16(kb, 16 * ks), id.c2, 1u);
+    tc::mma_ss_f16(tm + tx, kdesc16(ylb, 16 * ks, 128), mndesc16(kb, 16 * ks), id.c2, 1u);
+  }
+  tc::mma_commit(bar);
+}
+
+// Ytilde = -Y diag(exp(lam_C - lam_t)), split hi + lo, as the K-major A
+// tiles [128 j x 64 t] of chain 2 (the S half's Y already holds -U)
+__device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int b3) {
 #pragma unroll
   for (int c0 = 0; c0 < 64; c0 += 32) {
-    uint32_t r[32], u[32];
+    uint32_t r[32];
     tc::tmem_ld32(trow(tm + TM_Y, c0), r);
-    if (x.s_half) tc::tmem_ld32(trow(tm + TM_U, c0), u);
     tc::tmem_wait_ld();
 #pragma unroll
     for (int q8 = 0; q8 < 4; q8++) {
@@ -496,14 +504,9 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
 #pragma unroll
       for (int j = 0; j < 4; j++) {
         const int jj = 8 * q8 + 2 * j, t = c0 + jj;
-        float y0 = __uint_as_float(r[jj]), y1 = __uint_as_float(r[jj + 1]);
-        if (x.s_half) {
-          y0 -= __uint_as_float(u[jj]);
-          y1 -= __uint_as_float(u[jj + 1]);
-        }
         __nv_bfloat16 h0, l0, h1, l1;
-        split_bf16(-sm.dec[b3][t] * y0, h0, l0);
-        split_bf16(-sm.dec[b3][t + 1] * y1, h1, l1);
+        split_bf16(-sm.dec[b3][t] * __uint_as_float(r[jj]), h0, l0);
+        split_bf16(-sm.dec[b3][t + 1] * __uint_as_float(r[jj + 1]), h1, l1);
         hw[j] = pack2(h0, h1);
         lw[j] = pack2(l0, l1);
       }
@@ -512,37 +515,51 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
       *reinterpret_cast<uint4 *>(sm.yl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
   }
+}
+
+// Advances both halves of the state through chunk ch (n = thread = TMEM
+// lane), the S half first: its chain 1 accumulates onto the -U^T that P put
+// in TM_Y.
+__device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx &x, int ch, int n, uint32_t tm,
+                            const MmaIds &id, uint32_t LIM) {
+  const uint32_t g = x.gch0 + (uint32_t)ch;
+  const int bk = ch % NBUF, b3 = (int)(g % 3);
+  wait_phase(sm, p, &sm.wt_ready, g, LIM);
+  tc::tc_fence_after();
+  const float gC = sm.gc[b3];
+  // ---- S half (its chain 2 of the previous chunk was waited on before the
+  // T half's Ytilde)
+  stage_half(tm, TM_XS, gC);
+  tc::tc_fence_before();
+  tc::named_bar(BAR_X, NG);
+  if (n == 0) issue_chain1(sm, tm, id, true, &sm.bar_y1);
+  wait_phase(sm, p, &sm.bar_y1, g, DRAIN_LIMIT);
+  tc::tc_fence_after();
+  split_y(sm, tm, n, b3);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
-  // ---- chain 2: X^T += Ytilde^T K  (B = this chunk's K tile, MN-major);
-  // U of this chunk is consumed: P may overwrite it
-  if (n == 0) {
-    tc::mbar_arrive(&sm.ys_done);
-    tc::tc_fence_after();
-    const uint32_t kb = tc::smem_u32(sm.kin[bk]), yhb = tc::smem_u32(sm.yh), ylb = tc::smem_u32(sm.yl);
-#pragma unroll
-    for (int ks = 0; ks < 4; ks++) {
-      tc::mma_ss_f16(tm + TM_X, kdesc16(yhb, 16 * ks, 128), mndesc16(kb, 16 * ks), id.c2, 1u);
-      tc::mma_ss_f16(tm + TM_X, kdesc16(ylb, 16 * ks, 128), mndesc16(kb, 16 * ks), id.c2, 1u);
-    }
-    tc::mma_commit(&sm.bar_x);
-  }
-  wait_phase(sm, p, &sm.bar_x, g, DRAIN_LIMIT);
+  if (n == 0) issue_chain2(sm, tm, TM_XS, bk, id, &sm.bar_x1);
+  // ---- T half: XR is free (chain 1 of S is complete); the T half's chain 2
+  // of the previous chunk must be
+  if (ch > 0) wait_phase(sm, p, &sm.bar_x2, g - 1, DRAIN_LIMIT);
   tc::tc_fence_after();
-  // ---- rounded copy of the new X for the next chunk's chain 1
-#pragma unroll
-  for (int c0 = 0; c0 < 128; c0 += 32) {
-    uint32_t r[32];
-    tc::tmem_ld32(trow(tm + TM_X, c0), r);
-    tc::tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 32; j++) r[j] = tc::to_tf32(__uint_as_float(r[j]));
-    tc::tmem_st32(trow(tm + TM_XR, c0), r);
-  }
-  tc::tmem_wait_st();
+  stage_half(tm, TM_XT, gC);
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
+  if (n == 0) issue_chain1(sm, tm, id, false, &sm.bar_y2);
+  wait_phase(sm, p, &sm.bar_y2, g, DRAIN_LIMIT);
+  // the Ytilde tiles are free once the S half's chain 2 has read them
+  wait_phase(sm, p, &sm.bar_x1, g, DRAIN_LIMIT);
+  tc::tc_fence_after();
+  split_y(sm, tm, n, b3);
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  tc::named_bar(BAR_X, NG);
+  if (n == 0) {
+    tc::mbar_arrive(&sm.ys_done);  // TM_Y is free for the next chunk's -U
+    issue_chain2(sm, tm, TM_XT, bk, id, &sm.bar_x2);
+  }
 }
 
 __global__ void __launch_bounds__(NT, 1)
@@ -562,8 +579,10 @@ __global__ void __launch_bounds__(NT, 1)
     for (int b = 0; b < NBUF; b++) tc::mbar_init(&sm.full[b], 1);
     tc::mbar_init(&sm.bar_g, 1);
     tc::mbar_init(&sm.bar_wu, 1);
-    tc::mbar_init(&sm.bar_y, 1);
-    tc::mbar_init(&sm.bar_x, 1);
+    tc::mbar_init(&sm.bar_y1, 1);
+    tc::mbar_init(&sm.bar_y2, 1);
+    tc::mbar_init(&sm.bar_x1, 1);
+    tc::mbar_init(&sm.bar_x2, 1);
     tc::mbar_init(&sm.wt_ready, 1);
     tc::mbar_init(&sm.ys_done, 1);
     tc::mbar_init(&sm.never, 1);
@@ -585,6 +604,7 @@ __global__ void __launch_bounds__(NT, 1)
   MmaIds id;
   id.gram = tc::idesc(tc::FMT_BF16, 128, 64);
   id.wu = tc::idesc(tc::FMT_BF16, 128, 64, false, false, /*a_mn=*/true, false);
+  id.wu_neg = tc::idesc(tc::FMT_BF16, 128, 64, /*neg_a=*/true, false, /*a_mn=*/true, false);
   id.c1 = tc::idesc(tc::FMT_TF32, 128, 64);
   id.c2 = tc::idesc(tc::FMT_BF16, 128, 128, false, false, false, /*b_mn=*/true);
   uint32_t ph_full[NBUF] = {0, 0, 0};
@@ -599,14 +619,13 @@ __global__ void __launch_bounds__(NT, 1)
     if (idx >= n_items) break;
     ItemCtx x;
     x.it = p.items[idx];
-    x.s_half = x.it.part == 1;
     x.kh = (int)(((int64_t)x.it.head * p.h_k) / p.h_v);
     x.n_ch = (int)((x.it.end - x.it.start + C - 1) / C);
     x.gch0 = gch;
 
     if (is_p) {
       if (q == 0)  // chunks 0 and 1; chunk c + 2 is issued at the end of prep(c)
-        for (int ch = 0; ch < 2 && ch < x.n_ch; ch++) issue_chunk(sm, x.it, ch, x.s_half, x.kh, &tmap_k, &tmap_v);
+        for (int ch = 0; ch < 2 && ch < x.n_ch; ch++) issue_chunk(sm, x.it, ch, x.kh, &tmap_k, &tmap_v);
       float g_cur = 0.f, b_cur = 0.f;
       if (q < C && x.it.start + q < x.it.end) {
         if (p.variant == HYPIC_GDN) g_cur = p.g[(x.it.start + q) * p.h_v + x.it.head];
@@ -615,33 +634,43 @@ __global__ void __launch_bounds__(NT, 1)
       for (int ch = 0; ch < x.n_ch; ch++)
         prep_chunk(sm, p, x, ch, q, tm, id, LIM, ph_full, g_cur, b_cur, &tmap_k, &tmap_v);
     } else {
-      // X^T half := T half: identity, S half: zero (accumulator and rounded copy)
+      // X^T := [I | 0]
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t r[32];
+        uint32_t r[32], z[32];
 #pragma unroll
-        for (int j = 0; j < 32; j++) r[j] = (!x.s_half && c0 + j == n) ? 0x3f800000u : 0u;
-        tc::tmem_st32(trow(tm + TM_X, c0), r);
-        tc::tmem_st32(trow(tm + TM_XR, c0), r);
+        for (int j = 0; j < 32; j++) {
+          r[j] = (c0 + j == n) ? 0x3f800000u : 0u;
+          z[j] = 0u;
+        }
+        tc::tmem_st32(trow(tm + TM_XT, c0), r);
+        tc::tmem_st32(trow(tm + TM_XS, c0), z);
       }
       tc::tmem_wait_st();
       tc::tc_fence_before();
       tc::named_bar(BAR_X, NG);
       for (int ch = 0; ch < x.n_ch; ch++) chain_chunk(sm, p, x, ch, n, tm, id, LIM);
-      // epilogue: lane n holds column n of its half of [T | S]
-      const int64_t sh = (int64_t)x.it.slot * p.h_v + x.it.head;
-      float *out = (x.s_half ? p.S_pool : p.T_pool) + sh * 128 * 128 + n;
+      if (x.n_ch > 0) {
+        wait_phase(sm, p, &sm.bar_x2, gch + (uint32_t)x.n_ch - 1, DRAIN_LIMIT);
+        tc::tc_fence_after();
+      }
+      // epilogue: lane n holds column n of T and of S
+      const int64_t sh = ((int64_t)x.it.slot * p.h_v + x.it.head) * 128 * 128 + n;
       bool bad = false;
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t r[32];
-        tc::tmem_ld32(trow(tm + TM_X, c0), r);
-        tc::tmem_wait_ld();
+      for (int h = 0; h < 2; h++) {
+        float *out = (h ? p.S_pool : p.T_pool) + sh;
 #pragma unroll
-        for (int j = 0; j < 32; j++) {
-          const float v = __uint_as_float(r[j]);
-          out[(int64_t)(c0 + j) * 128] = v;
-          bad |= !finite_f(v);
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t r[32];
+          tc::tmem_ld32(trow(tm + (h ? TM_XS : TM_XT), c0), r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; j++) {
+            const float v = __uint_as_float(r[j]);
+            out[(int64_t)(c0 + j) * 128] = v;
+            bad |= !finite_f(v);
+          }
         }
       }
       if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
