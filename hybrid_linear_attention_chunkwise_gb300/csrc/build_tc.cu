@@ -45,6 +45,8 @@
 // ticket.  Inputs come in by TMA (3-D maps over [token, head, channel],
 // 128-byte swizzle) through three buffers, two chunks ahead of their use.
 // All waits are bounded.
+#include <cstddef>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -118,9 +120,9 @@ struct __align__(1024) BuildTcSmem {
   float am[64][66];             // A = (I + M)^-1 (rows 8-byte aligned for pair loads)
   float lam[64], bg[64], bt[64];
   float ea[64], eb[64];         // b_t exp(lam_t - lam_0), exp(lam_0 - lam_i): M_ti = ea_t eb_i k_t.k_i
-  int fact;                     // the factored form is in range for this chunk
-  float dec[3][64];             // exp(lam_C - lam_t) of chunk c in [c % 3] (read by X)
+  float dec[3][64];             // exp(lam_C - lam_t) of chunk c in [c % 3] (read by X; pair loads)
   float gc[3];                  // G_C of chunk c in [c % 3] (read by X)
+  int fact;                     // the factored form is in range for this chunk
   uint64_t full[NBUF];
   uint64_t bar_g, bar_wu;       // P's MMA completions
   uint64_t bar_y1, bar_y2;      // X's chain 1 completions (S half, T half; P waits on the T half's)
@@ -131,6 +133,8 @@ struct __align__(1024) BuildTcSmem {
   int item;
   int abort;
 };
+
+static_assert(offsetof(BuildTcSmem, dec) % 8 == 0 && offsetof(BuildTcSmem, am) % 8 == 0, "pair loads");
 
 struct BuildTcArgs {
   BuildParams p;
@@ -149,13 +153,15 @@ __device__ __forceinline__ void wait_phase(BuildTcSmem &sm, const BuildParams &p
   if (!tc::mbar_wait(bar, ph & 1, aborted(sm) ? DRAIN_LIMIT : lim)) fail(sm, p);
 }
 
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi)
-__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
-  hi = __float2bfloat16_rn(x);
-  lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-}
-__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
-  return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi), for a pair, packed (x0
+// in the low half): one paired conversion for the high parts, one for the
+// exact residuals
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  const float r0 = x0 - __uint_as_float(hi << 16), r1 = x1 - __uint_as_float(hi & 0xFFFF0000u);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 // TMEM address of this thread's lane (warp w covers lanes 32 (w % 4) ..)
 __device__ __forceinline__ uint32_t trow(uint32_t base, int col) {
@@ -240,16 +246,9 @@ __device__ __forceinline__ void write_factors(BuildTcSmem &sm, int q) {
     uint32_t wh[4], wl[4], uh[4], ul[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) {
-      __nv_bfloat16 h0, l0, h1, l1;
-      const float a0 = sm.am[t][c0 + 2 * j], a1 = sm.am[t][c0 + 2 * j + 1];
-      split_bf16(a0 * sm.bg[c0 + 2 * j], h0, l0);
-      split_bf16(a1 * sm.bg[c0 + 2 * j + 1], h1, l1);
-      wh[j] = pack2(h0, h1);
-      wl[j] = pack2(l0, l1);
-      split_bf16(a0 * sm.bt[c0 + 2 * j], h0, l0);
-      split_bf16(a1 * sm.bt[c0 + 2 * j + 1], h1, l1);
-      uh[j] = pack2(h0, h1);
-      ul[j] = pack2(l0, l1);
+      const float2 a = *reinterpret_cast<const float2 *>(&sm.am[t][c0 + 2 * j]);
+      split_bf16x2(a.x * sm.bg[c0 + 2 * j], a.y * sm.bg[c0 + 2 * j + 1], wh[j], wl[j]);
+      split_bf16x2(a.x * sm.bt[c0 + 2 * j], a.y * sm.bt[c0 + 2 * j + 1], uh[j], ul[j]);
     }
     const uint32_t off = sw16(t, c0, 64);
     *reinterpret_cast<uint4 *>(sm.bwh + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
@@ -450,18 +449,24 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
 // (the accumulator chain 2 adds onto), in one pass over the half.
 __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC) {
 #pragma unroll
-  for (int c0 = 0; c0 < 128; c0 += 32) {
-    uint32_t r[32], xr[32];
-    tc::tmem_ld32(trow(tm + tx, c0), r);
+  for (int c0 = 0; c0 < 128; c0 += 64) {
+    uint32_t r[64];
+    tc::tmem_ld32(trow(tm + tx, c0), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tc::tmem_ld32(trow(tm + tx, c0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
     tc::tmem_wait_ld();
 #pragma unroll
-    for (int j = 0; j < 32; j++) {
-      const float v = __uint_as_float(r[j]);
-      xr[j] = tc::to_tf32(v);
-      r[j] = __float_as_uint(gC * v);
+    for (int h = 0; h < 2; h++) {
+      uint32_t xr[32];
+#pragma unroll
+      for (int j = 0; j < 32; j++) {
+        const float v = __uint_as_float(r[32 * h + j]);
+        xr[j] = tc::to_tf32(v);
+        r[32 * h + j] = __float_as_uint(gC * v);
+      }
+      tc::tmem_st32(trow(tm + TM_XR, c0 + 32 * h), xr);
     }
-    tc::tmem_st32(trow(tm + TM_XR, c0), xr);
-    tc::tmem_st32(trow(tm + tx, c0), r);
+    tc::tmem_st32(trow(tm + tx, c0), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tc::tmem_st32(trow(tm + tx, c0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
   }
   tc::tmem_wait_st();
 }
@@ -504,11 +509,8 @@ __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int
 #pragma unroll
       for (int j = 0; j < 4; j++) {
         const int jj = 8 * q8 + 2 * j, t = c0 + jj;
-        __nv_bfloat16 h0, l0, h1, l1;
-        split_bf16(-sm.dec[b3][t] * __uint_as_float(r[jj]), h0, l0);
-        split_bf16(-sm.dec[b3][t + 1] * __uint_as_float(r[jj + 1]), h1, l1);
-        hw[j] = pack2(h0, h1);
-        lw[j] = pack2(l0, l1);
+        const float2 dd = *reinterpret_cast<const float2 *>(&sm.dec[b3][t]);
+        split_bf16x2(-dd.x * __uint_as_float(r[jj]), -dd.y * __uint_as_float(r[jj + 1]), hw[j], lw[j]);
       }
       const uint32_t off = sw16(n, c0 + 8 * q8, 128);
       *reinterpret_cast<uint4 *>(sm.yh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
