@@ -244,6 +244,62 @@ def setup_compose(dev, hy, seed=0, n_layers=30):
 
 
 # ---------------------------------------------------------------- CPU oracle leg
+def _time_ms(fn, reps=5, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def measure_rows(dev, hy, peaks):
+    """The build rows outside the timed step, each against its own roofline:
+    the RetNet-style scalar-decay fast path (8 heads, d = 128, 16 x 512
+    tokens, bf16) and the cold uneven mix (256 segments of 256..8192
+    tokens, 16 key / 32 value heads, d = 128, w = 8, bf16) for GDN,
+    DeltaNet and the per-channel gate.  Which kernel ran is named."""
+    import torch
+    import synth_inputs as si
+    rows = {}
+
+    def one(name, W, bound_bytes_extra=0):
+        L = W.layers[0]
+        T = torch.empty(hy.pool_T_shape(W.variant, W.n_seg, W.h_v, W.d_k), device=dev)
+        S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
+        ms = _time_ms(lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=W.variant,
+                                               seam_w=W.seam_w, T_pool=T, S_pool=S))
+        bodies = np.maximum(np.diff(W.seg_offsets) - W.seam_w, 0)
+        in_b = 2 if W.dtype == torch.bfloat16 else 4
+        nbytes = (W.n_tokens * (W.h_k * W.d_k + W.h_v * W.d_v) * in_b + S.numel() * 4 + T.numel() * 4
+                  + (L.g.numel() * 4 if L.g is not None and L.g.dim() > 1 else 0)
+                  + (L.beta.numel() * 4 if L.beta is not None else 0))
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        r = {"ms": ms, "tokens_per_s": W.n_tokens / (ms * 1e-3), "algorithmic_bytes": nbytes,
+             "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"]}}
+        if W.variant in ("gdn", "deltanet", "channel"):
+            fl = build_flops(bodies, W.h_v, g=2 if W.variant != "channel" else 1)
+            tf = fl / (ms * 1e-3) / 1e12
+            r["tensor"] = {"achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": tf / peaks["bf16"]}
+        r["kernel"] = ("tensor-core chunkwise" if W.variant in ("gdn", "deltanet") and W.dtype == torch.bfloat16
+                       and W.d_k == 128 else "fp32 token recurrence")
+        rows[name] = r
+        del L, T, S
+
+    one("build: RetNet scalar decay, 8 heads, 16 x 512 tokens", si.workload(2, seed=0, device=dev))
+    for var in ("gdn", "deltanet", "channel"):
+        W = si.workload(5, seed=0, device=dev, variant=var)
+        one(f"build: uneven 256-segment mix ({W.n_tokens} tokens), {var}", W)
+        del W
+        torch.cuda.empty_cache()
+    return rows
+
+
 def run_profile_case(kind):
     """One small case of one kernel for an ncu capture: two warm-up launches,
     then the launch to capture.  Inputs are larger than L2 and a few GB at
@@ -349,6 +405,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements after the step")
     ap.add_argument("--profile", choices=["build", "compose"], default=None,
                     help="run one small case of one kernel (for an ncu capture) and exit")
     args = ap.parse_args()
@@ -474,6 +531,10 @@ def main():
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "what": "H2D of the layer's k/v/g/beta from pinned memory + build + D2H of all pairs"}
 
+    # the other build rows, each against its own roofline (after the timed
+    # region; not part of the step)
+    rows = measure_rows(dev, hy, peaks) if (rank == 0 and not args.no_rows) else None
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(W3, os.cpu_count() or 1)
@@ -490,6 +551,7 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
+            "rows": rows,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
