@@ -286,8 +286,10 @@ def measure_rows(dev, hy, peaks):
             fl = build_flops(bodies, W.h_v, g=2 if W.variant != "channel" else 1)
             tf = fl / (ms * 1e-3) / 1e12
             r["tensor"] = {"achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": tf / peaks["bf16"]}
-        r["kernel"] = ("tensor-core chunkwise" if W.variant in ("gdn", "deltanet") and W.dtype == torch.bfloat16
-                       and W.d_k == 128 else "fp32 token recurrence")
+        tc_shape = W.dtype == torch.bfloat16 and W.d_k == 128 and W.d_v == 128
+        r["kernel"] = ("tensor-core chunkwise" if tc_shape and W.variant in ("gdn", "deltanet")
+                       else "tensor-core fast path" if tc_shape and W.variant in ("scalar", "ungated", "diag")
+                       else "fp32 token recurrence")
         rows[name] = r
         del L, T, S
 

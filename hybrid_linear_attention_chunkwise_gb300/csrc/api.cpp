@@ -176,8 +176,10 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
   p.status = d->status;
   // bf16 scalar-gate delta rules with 128-wide heads run chunkwise on the
-  // tensor cores; every other case runs the fp32 token recurrence.  Both
-  // take one item per (segment, value head).
+  // tensor cores, bf16 transitions without an erase (scalar decay, ungated,
+  // diagonal gate) with 128-wide heads run the tensor-core fast path, and
+  // every other case runs the fp32 token recurrence.  All take one item per
+  // (segment, value head).
   const bool tc_path = build_tc_supported(p);
   const int parts = 1;
 
@@ -220,7 +222,9 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
   // may be released when it goes out of scope
   if (cudaMemcpyAsync(d->workspace, host.data(), need, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
   const cudaError_t e = tc_path ? launch_build_tc(p, d->n_tokens, (int)n_items, sm_count(), wait_limit(), s)
-                                : launch_build_token(p, (int)n_items, sm_count(), s);
+                        : build_fast_supported(p)
+                            ? launch_build_fast(p, d->n_tokens, (int)n_items, sm_count(), wait_limit(), s)
+                            : launch_build_token(p, (int)n_items, sm_count(), s);
   if (e != cudaSuccess) return HYPIC_ERR_CUDA;
   return HYPIC_OK;
 }

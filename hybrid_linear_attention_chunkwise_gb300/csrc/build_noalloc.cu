@@ -178,7 +178,9 @@ int hypic_segment_build_noalloc(const hypic_build_desc *d, hypic_stream_t stream
   // static buffer may be rewritten by the next call
   if (cudaMemcpyAsync(scratch, h_plan, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
   const cudaError_t e = tc_path ? launch_build_tc(p, d->n_tokens, (int)n_items, sm_count(), wait_limit(), s)
-                                : launch_build_token(p, (int)n_items, sm_count(), s);
+                        : build_fast_supported(p)
+                            ? launch_build_fast(p, d->n_tokens, (int)n_items, sm_count(), wait_limit(), s)
+                            : launch_build_token(p, (int)n_items, sm_count(), s);
   if (e != cudaSuccess) return HYPIC_ERR_CUDA;
   return HYPIC_OK;
 }

@@ -706,8 +706,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [n_tokens, heads, 128] bf16 as a 3-D map with 64-channel x 1-head x
-// 64-token boxes and 128-byte swizzle
+
+}  // namespace
+
 bool make_tmap_tokens(CUtensorMap *map, const void *base, int64_t n_tokens, int heads) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -719,8 +720,6 @@ bool make_tmap_tokens(CUtensorMap *map, const void *base, int64_t n_tokens, int 
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool build_tc_supported(const BuildParams &p) {
   auto a16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };

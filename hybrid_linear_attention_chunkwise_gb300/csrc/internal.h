@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "hypic.h"
@@ -67,6 +68,14 @@ cudaError_t launch_build_token(const BuildParams &p, int n_items, int n_sm, cuda
 bool build_tc_supported(const BuildParams &p);
 cudaError_t launch_build_tc(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, uint32_t wait_limit,
                             cudaStream_t s);
+// Tensor-core fast path (no erase: scalar decay, ungated, diagonal gate),
+// bf16 inputs, d_k = d_v = 128, 16-byte aligned k / v.
+bool build_fast_supported(const BuildParams &p);
+cudaError_t launch_build_fast(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, uint32_t wait_limit,
+                              cudaStream_t s);
+// [n_tokens, heads, 128] bf16 as a 3-D TMA map with 64-channel x 1-head x
+// 64-token boxes and 128-byte swizzle (false if the map cannot be encoded).
+bool make_tmap_tokens(CUtensorMap *map, const void *base, int64_t n_tokens, int heads);
 cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s);
 // The tensor-core compose covers dense transitions, bf16 seam tokens,

@@ -70,3 +70,17 @@ def test_build_tc_bounded_wait_reports_timeout():
     assert r.returncode == 0, r.stderr[-2000:]
     line = [ln for ln in r.stdout.splitlines() if ln.startswith("STATUS")][-1]
     assert line.split()[1] == "5" and line.split()[3] == "4.0", line
+
+
+@pytest.mark.parametrize("variant", ["scalar", "ungated", "diag"])
+def test_fast_path_long_segments(variant):
+    """The tensor-core fast path (no erase) over long bodies: the weighted
+    sum over thousands of tokens (RetNet decays close to one keep old tokens
+    alive) stays within the bf16 bar."""
+    W = si.workload(5, device=DEV, variant=variant, lengths=[4100, 2049, 77], h_k=2, h_v=2, seam_w=8)
+    if variant == "scalar":
+        W = si.workload(2, device=DEV, lengths=[4100, 2049, 77], h_k=2, h_v=2, seam_w=8)
+    T_pool, S_pool = gpu_build(W)
+    T, S = oracle_pairs(W)
+    eT, eS = compare_pairs(W, T_pool, S_pool, T, S, range(W.n_seg))
+    assert eT <= TOL_BF16 and eS <= TOL_BF16, (eT, eS)
