@@ -125,3 +125,21 @@ def build_chunked(variant, k, v, g, beta, start, end, h, h_k, h_v, *, chunk=C,
             corr = _mm(Kc.T, decay * Y, op, op, split_b=split_y)
         X = (Gc[:, None] if vec else Gc) * X - corr
     return X[:, :d_k], X[:, d_k:]
+
+
+def gram_subblocks(Kc, lam, sb=16):
+    """The decayed Gram of a chunk with a per-channel gate, strictly lower
+    part, M_ti = sum_c k_t[c] k_i[c] exp(lam_t[c] - lam_i[c]) (i < t), formed
+    the way the tensor-core kernel forms it: token rows in sub-blocks of
+    `sb`, each with the reference ref = lam just before the sub-block, as
+    the product of Q_t = k_t exp(lam_t - ref) and R_i = k_i exp(ref - lam_i).
+    Every exponent is bounded by the log-gate range of one sub-block."""
+    m = Kc.shape[0]
+    M = torch.zeros(m, m, dtype=Kc.dtype)
+    for b0 in range(0, m, sb):
+        b1 = min(m, b0 + sb)
+        ref = lam[b0 - 1] if b0 > 0 else torch.zeros_like(lam[0])
+        Q = Kc[b0:b1] * torch.exp(lam[b0:b1] - ref)
+        R = Kc[:b1] * torch.exp(ref - lam[:b1])
+        M[b0:b1, :b1] = Q @ R.T
+    return torch.tril(M, -1)

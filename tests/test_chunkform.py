@@ -20,3 +20,19 @@ def test_chunk_form_equals_token_form(variant, chunk):
             Tc, Sc = build_chunked(variant, k, v, g, beta, off[i], off[i + 1], h, h_k, h_v, chunk=chunk)
             assert np.abs(Tc.numpy() - T[i, h]).max() < 1e-12
             assert np.abs(Sc.numpy() - S[i, h]).max() < 1e-12 * max(1.0, np.abs(S[i, h]).max())
+
+
+@pytest.mark.parametrize("m,sb", [(32, 16), (29, 16), (64, 16)])
+def test_subblock_gram_equals_direct(m, sb):
+    """The per-channel decayed Gram as the kernel forms it (sub-block
+    references) equals the direct definition."""
+    import torch
+    from chunkform import gram_subblocks
+    gen = torch.Generator().manual_seed(7)
+    K = torch.randn(m, 8, generator=gen, dtype=torch.float64)
+    g = -torch.nn.functional.softplus(torch.randn(m, 8, generator=gen, dtype=torch.float64))
+    lam = torch.cumsum(g, 0)
+    E = torch.exp(lam[:, None, :] - lam[None, :, :])
+    direct = torch.tril(torch.einsum("tc,ic,tic->ti", K, K, E), -1)
+    got = gram_subblocks(K, lam, sb)
+    assert torch.allclose(got, direct, rtol=1e-12, atol=1e-14)
