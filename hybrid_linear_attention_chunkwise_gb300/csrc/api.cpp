@@ -69,6 +69,22 @@ bool debug_stall() {
 }
 }  // namespace hypic
 
+namespace hypic {
+
+// The build kernel for the call: bf16 inputs with 128-wide heads run
+// chunkwise on the tensor cores (scalar-gate delta rules, the per-channel
+// gated delta rule, and the fast path of the transitions without an erase:
+// scalar decay, ungated, diagonal gate); every other case runs the fp32 token
+// recurrence.
+cudaError_t launch_build(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, cudaStream_t s) {
+  if (build_tc_supported(p)) return launch_build_tc(p, n_tokens, n_items, n_sm, wait_limit(), s);
+  if (build_channel_supported(p)) return launch_build_channel(p, n_tokens, n_items, n_sm, wait_limit(), s);
+  if (build_fast_supported(p)) return launch_build_fast(p, n_tokens, n_items, n_sm, wait_limit(), s);
+  return launch_build_token(p, n_items, n_sm, s);
+}
+
+}  // namespace hypic
+
 extern "C" {
 
 int hypic_version(void) { return 100; }
@@ -175,12 +191,7 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
   p.plan = reinterpret_cast<PlanHeader *>(d->workspace);
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
   p.status = d->status;
-  // bf16 scalar-gate delta rules with 128-wide heads run chunkwise on the
-  // tensor cores, bf16 transitions without an erase (scalar decay, ungated,
-  // diagonal gate) with 128-wide heads run the tensor-core fast path, and
-  // every other case runs the fp32 token recurrence.  All take one item per
-  // (segment, value head).
-  const bool tc_path = build_tc_supported(p);
+  // one item per (segment, value head) on every kernel (see launch_build)
   const int parts = 1;
 
   const int64_t n_pairs = n_build_items(d);
@@ -221,11 +232,7 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
   // pageable source: the call returns once the bytes are staged, so `host`
   // may be released when it goes out of scope
   if (cudaMemcpyAsync(d->workspace, host.data(), need, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
-  const cudaError_t e = tc_path ? launch_build_tc(p, d->n_tokens, (int)n_items, sm_count(), wait_limit(), s)
-                        : build_fast_supported(p)
-                            ? launch_build_fast(p, d->n_tokens, (int)n_items, sm_count(), wait_limit(), s)
-                            : launch_build_token(p, (int)n_items, sm_count(), s);
-  if (e != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (launch_build(p, d->n_tokens, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
   return HYPIC_OK;
 }
 

@@ -136,8 +136,7 @@ int hypic_segment_build_noalloc(const hypic_build_desc *d, hypic_stream_t stream
   p.plan = reinterpret_cast<PlanHeader *>(scratch);
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
   p.status = d->status;
-  const bool tc_path = build_tc_supported(p);
-  const int parts = 1;  // one item per (segment, value head) on both paths
+  const int parts = 1;  // one item per (segment, value head) on every kernel
   const int64_t n_items = (int64_t)d->n_seg * d->h_v * parts;
 
   // Plan in the static host buffer: the ticket starts at zero, items go
@@ -177,11 +176,7 @@ int hypic_segment_build_noalloc(const hypic_build_desc *d, hypic_stream_t stream
   // pageable source: the call returns once the bytes are staged, so the
   // static buffer may be rewritten by the next call
   if (cudaMemcpyAsync(scratch, h_plan, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
-  const cudaError_t e = tc_path ? launch_build_tc(p, d->n_tokens, (int)n_items, sm_count(), wait_limit(), s)
-                        : build_fast_supported(p)
-                            ? launch_build_fast(p, d->n_tokens, (int)n_items, sm_count(), wait_limit(), s)
-                            : launch_build_token(p, (int)n_items, sm_count(), s);
-  if (e != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (launch_build(p, d->n_tokens, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
   return HYPIC_OK;
 }
 

@@ -709,16 +709,21 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-bool make_tmap_tokens(CUtensorMap *map, const void *base, int64_t n_tokens, int heads) {
+bool make_tmap_3d(CUtensorMap *map, CUtensorMapDataType dt, uint32_t esz, const void *base, int64_t n_tokens,
+                  int heads, uint32_t box_x, uint32_t box_t, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)n_tokens};
-  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)heads * 128 * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
+  cuuint64_t strides[2] = {128 * (cuuint64_t)esz, (cuuint64_t)heads * 128 * esz};
+  cuuint32_t box[3] = {box_x, 1, box_t};
   cuuint32_t es[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_tokens(CUtensorMap *map, const void *base, int64_t n_tokens, int heads, int rows) {
+  return make_tmap_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, n_tokens, heads, 64, (uint32_t)rows,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool build_tc_supported(const BuildParams &p) {

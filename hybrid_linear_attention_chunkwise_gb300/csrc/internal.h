@@ -62,6 +62,9 @@ __host__ __device__ inline bool is_dense_T(int v) { return is_delta(v); }
 __host__ __device__ inline bool is_vector_gate(int v) { return v == HYPIC_CHANNEL_DELTA || v == HYPIC_DIAG_GATE; }
 
 // Launchers (each returns a cudaError_t from the launch).
+// The build kernel for the parameters (tensor-core paths where they apply,
+// else the token recurrence), one item per (segment, value head).
+cudaError_t launch_build(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, cudaStream_t s);
 cudaError_t launch_build_token(const BuildParams &p, int n_items, int n_sm, cudaStream_t s);
 // Tensor-core chunkwise build: GDN / DeltaNet, bf16 inputs, d_k = d_v = 128,
 // 16-byte aligned k / v.  Items are (segment, head, half of [T | S]).
@@ -73,9 +76,19 @@ cudaError_t launch_build_tc(const BuildParams &p, int64_t n_tokens, int n_items,
 bool build_fast_supported(const BuildParams &p);
 cudaError_t launch_build_fast(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, uint32_t wait_limit,
                               cudaStream_t s);
-// [n_tokens, heads, 128] bf16 as a 3-D TMA map with 64-channel x 1-head x
-// 64-token boxes and 128-byte swizzle (false if the map cannot be encoded).
-bool make_tmap_tokens(CUtensorMap *map, const void *base, int64_t n_tokens, int heads);
+// [n_tokens, heads, 128] elements of `esz` bytes as a 3-D TMA map with
+// box_x-channel x 1-head x box_t-token boxes (false if the map cannot be
+// encoded).  Out-of-range tokens read as zero.
+bool make_tmap_3d(CUtensorMap *map, CUtensorMapDataType dt, uint32_t esz, const void *base, int64_t n_tokens,
+                  int heads, uint32_t box_x, uint32_t box_t, CUtensorMapSwizzle swz);
+// [n_tokens, heads, 128] bf16 with 64-channel x 1-head x `rows`-token boxes
+// and 128-byte swizzle.
+bool make_tmap_tokens(CUtensorMap *map, const void *base, int64_t n_tokens, int heads, int rows = 64);
+// Tensor-core chunkwise build for the per-channel gated delta rule, bf16
+// inputs, d_k = d_v = 128, 16-byte aligned k / v / g.
+bool build_channel_supported(const BuildParams &p);
+cudaError_t launch_build_channel(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, uint32_t wait_limit,
+                                 cudaStream_t s);
 cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s);
 // The tensor-core compose covers dense transitions, bf16 seam tokens,
