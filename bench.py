@@ -50,14 +50,16 @@ def _peaks():
 C = 64
 
 
-def build_flops(lengths, h_v, d_k=128, d_v=128, g=2):
+def build_flops(lengths, h_v, d_k=128, d_v=128, g=2, chunk=C):
     """Algorithmic FLOPs of the chunkwise build: per chunk of c tokens and
     value head, Gram 2c^2 d_k / g + W,U solves 2c^2 (d_k + d_v) + K^T Y
-    2c d_k (d_k + d_v) + W X (skipped on the first chunk) 2c d_k (d_k + d_v)."""
+    2c d_k (d_k + d_v) + W X (skipped on the first chunk) 2c d_k (d_k + d_v).
+    The chunk length is the kernel's (64 for the scalar gates, 32 for the
+    per-channel gate)."""
     tot = 0.0
     for L in lengths:
-        n_full, tail = divmod(int(L), C)
-        chunks = [C] * n_full + ([tail] if tail else [])
+        n_full, tail = divmod(int(L), chunk)
+        chunks = [chunk] * n_full + ([tail] if tail else [])
         for j, c in enumerate(chunks):
             f = 2 * c * c * d_k / g + 2 * c * c * (d_k + d_v) + 2 * c * d_k * (d_k + d_v)
             if j > 0:
@@ -92,8 +94,10 @@ def compose_flops(n_layers, n_seg, w, h_v, d_k=128, d_v=128):
 KERNEL_SOURCES = {
     "build": ("build_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
     "compose": ("compose_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
+    "channel": ("build_channel.cu", "tc.cuh", "common.cuh", "internal.h"),
 }
-PROFILE_FILES = {"build": "segment_build_tc__gdn_16x1024.md", "compose": "compose_seam_mma__gdn_4x32x100.md"}
+PROFILE_FILES = {"build": "segment_build_tc__gdn_16x1024.md", "compose": "compose_seam_mma__gdn_4x32x100.md",
+                 "channel": "segment_build_channel__16x1024.md"}
 
 
 def source_hash(kind):
@@ -283,11 +287,12 @@ def measure_rows(dev, hy, peaks):
         r = {"ms": ms, "tokens_per_s": W.n_tokens / (ms * 1e-3), "algorithmic_bytes": nbytes,
              "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"]}}
         if W.variant in ("gdn", "deltanet", "channel"):
-            fl = build_flops(bodies, W.h_v, g=2 if W.variant != "channel" else 1)
+            fl = (build_flops(bodies, W.h_v, g=1, chunk=32) if W.variant == "channel"
+                  else build_flops(bodies, W.h_v))
             tf = fl / (ms * 1e-3) / 1e12
             r["tensor"] = {"achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": tf / peaks["bf16"]}
         tc_shape = W.dtype == torch.bfloat16 and W.d_k == 128 and W.d_v == 128
-        r["kernel"] = ("tensor-core chunkwise" if tc_shape and W.variant in ("gdn", "deltanet")
+        r["kernel"] = ("tensor-core chunkwise" if tc_shape and W.variant in ("gdn", "deltanet", "channel")
                        else "tensor-core fast path" if tc_shape and W.variant in ("scalar", "ungated", "diag")
                        else "fp32 token recurrence")
         rows[name] = r
@@ -306,20 +311,22 @@ def run_profile_case(kind):
     """One small case of one kernel for an ncu capture: two warm-up launches,
     then the launch to capture.  Inputs are larger than L2 and a few GB at
     most.  build: GDN, 16 segments x 1024 tokens, h_k = 16, h_v = 32 (512
-    (segment, head) pairs); compose: 4 GDN layers x 32 heads x 100 segments, w = 8 (12800
-    pairs, 1.7 GB pool)."""
+    (segment, head) pairs); channel: the same shape with per-channel gates;
+    compose: 4 GDN layers x 32 heads x 100 segments, w = 8 (12800 pairs,
+    1.7 GB pool)."""
     import torch
     import hybrid_linear_attention_chunkwise_gb300 as hy
     import synth_inputs as si
     dev = torch.device("cuda", 0)
     hy.load()
-    if kind == "build":
-        W = si.workload(3, seed=0, device=dev, n_seg=16)
+    if kind in ("build", "channel"):
+        var = "gdn" if kind == "build" else "channel"
+        W = si.workload(3, seed=0, device=dev, n_seg=16, variant=var)
         L = W.layers[0]
         T = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_k), device=dev)
         S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
         ws = hy.alloc_workspace(hy.build_workspace_bytes(W.n_seg, W.h_k, W.h_v, W.d_k, W.d_v), dev)
-        run = lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=W.seam_w,
+        run = lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=var, seam_w=W.seam_w,
                                        T_pool=T, S_pool=S, workspace=ws)
         units = W.n_seg * W.h_v
     else:
@@ -408,7 +415,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements after the step")
-    ap.add_argument("--profile", choices=["build", "compose"], default=None,
+    ap.add_argument("--profile", choices=["build", "compose", "channel"], default=None,
                     help="run one small case of one kernel (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.impl == "reference":

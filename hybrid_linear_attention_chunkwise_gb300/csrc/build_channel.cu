@@ -237,51 +237,68 @@ __device__ __forceinline__ void tiles_pass(BuildChSmem &sm, int bk, int b2, int 
   }
 }
 
-// fragment pair (channels c, c + 1; c even) of k_t * exp(s (lam_t - ref)),
-// split hi + lo
-__device__ __forceinline__ void factor_pair(const unsigned char *kin, const float (*L)[128], int t, int c, float2 ref,
-                                            float s, uint32_t &hi, uint32_t &lo) {
-  const uint32_t kw = *reinterpret_cast<const uint32_t *>(kin + tile16(t, c & ~7) + (c & 7) * 2);
-  const float2 l = *reinterpret_cast<const float2 *>(&L[t][lsw(t, c)]);
-  split_bf16x2(bf_lo(kw) * __expf(s * (l.x - ref.x)), bf_hi(kw) * __expf(s * (l.y - ref.y)), hi, lo);
+// (k0 exp(e0), k1 exp(e1)) for the packed bf16 pair kw = (k0, k1), split
+// hi + lo
+__device__ __forceinline__ void factor_pair(uint32_t kw, float e0, float e1, uint32_t &hi, uint32_t &lo) {
+  split_bf16x2(bf_lo(kw) * __expf(e0), bf_hi(kw) * __expf(e1), hi, lo);
 }
 
 // Gram partials on the legacy warp MMA: warp wp takes channels 32 wp ..
 // 32 wp + 31.  Tiles (m16n8): 0, 1 = sub-block 0 (rows t 0..15) x columns
 // i 0..7, 8..15; 2..5 = sub-block 1 (rows 16..31) x columns 0..31 in
 // eighths.  Lane (g = lane / 4, u = lane % 4) ends with rows g, g + 8 and
-// columns 2u, 2u + 1 of each tile.
+// columns 2u, 2u + 1 of each tile.  The rows a lane's fragments touch are
+// g + 8 rr (rr = 0..3), all with t % 8 = g, so each is loaded once and every
+// factor it feeds is formed from it:
+//     rows of sub-block 0:  Q0 = k exp(lam),  R0 = k exp(-lam),  R1 = k exp(lam_15 - lam)
+//     rows of sub-block 1:  Q1 = k exp(lam - lam_15),  R1
+// (ref 0 for sub-block 0, lam_15 for sub-block 1).
 __device__ __forceinline__ void gram_pass(BuildChSmem &sm, int bk, int wp, int lane) {
-  const float(*L)[128] = sm.gin[bk];
+  const float *L = &sm.gin[bk][0][0];
   const unsigned char *kin = sm.kin[bk];
   const int g = lane >> 2, u = lane & 3;
   float acc[6][4];
 #pragma unroll
   for (int i = 0; i < 6; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  const float2 z = make_float2(0.f, 0.f);
 #pragma unroll 1
   for (int kk = 0; kk < 2; kk++) {
-    const int ca = 32 * wp + 16 * kk + 2 * u, cb = ca + 8;
-    const float2 ra = *reinterpret_cast<const float2 *>(&L[SB - 1][lsw(SB - 1, ca)]);
-    const float2 rb = *reinterpret_cast<const float2 *>(&L[SB - 1][lsw(SB - 1, cb)]);
+    const int c0 = 32 * wp + 16 * kk, c8 = (c0 & 63) >> 3;
+    // byte offsets (within a row) of the k pairs at channels c0 + 2u and
+    // c0 + 8 + 2u, and the lam columns of those pairs, for rows with t % 8 = g
+    const uint32_t ko[2] = {(uint32_t)((c0 >> 6) * 4096 + ((c8 ^ g) << 4) + 4 * u),
+                            (uint32_t)((c0 >> 6) * 4096 + (((c8 + 1) ^ g) << 4) + 4 * u)};
+    const int lc[2] = {(c0 + 2 * u) ^ (g << 3), (c0 + 8 + 2 * u) ^ (g << 3)};
+    uint32_t a0h[4], a0l[4], a1h[4], a1l[4], b0h[2][2], b0l[2][2], b1h[4][2], b1l[4][2];
 #pragma unroll
-    for (int b = 0; b < 2; b++) {
-      const float2 fa = b ? ra : z, fb = b ? rb : z;
-      uint32_t ah[4], al[4];
-      factor_pair(kin, L, SB * b + g, ca, fa, 1.f, ah[0], al[0]);
-      factor_pair(kin, L, SB * b + g + 8, ca, fa, 1.f, ah[1], al[1]);
-      factor_pair(kin, L, SB * b + g, cb, fb, 1.f, ah[2], al[2]);
-      factor_pair(kin, L, SB * b + g + 8, cb, fb, 1.f, ah[3], al[3]);
+    for (int h = 0; h < 2; h++) {
+      const float2 x = *reinterpret_cast<const float2 *>(&L[(SB - 1) * 128 + lsw(SB - 1, c0 + 8 * h + 2 * u)]);
 #pragma unroll
-      for (int n = 0; n < 2 + 2 * b; n++) {
-        uint32_t bh0, bl0, bh1, bl1;
-        factor_pair(kin, L, 8 * n + g, ca, fa, -1.f, bh0, bl0);
-        factor_pair(kin, L, 8 * n + g, cb, fb, -1.f, bh1, bl1);
-        float(&d)[4] = acc[2 * b + n];
-        mma_bf16_16816(d, ah[0], ah[1], ah[2], ah[3], bh0, bh1);
-        mma_bf16_16816(d, ah[0], ah[1], ah[2], ah[3], bl0, bl1);
-        mma_bf16_16816(d, al[0], al[1], al[2], al[3], bh0, bh1);
+      for (int rr = 0; rr < 4; rr++) {
+        const int row = g + 8 * rr;
+        const uint32_t kw = *reinterpret_cast<const uint32_t *>(kin + row * 128 + ko[h]);
+        const float2 l = *reinterpret_cast<const float2 *>(&L[row * 128 + lc[h]]);
+        if (rr < 2) {
+          factor_pair(kw, l.x, l.y, a0h[2 * h + rr], a0l[2 * h + rr]);
+          factor_pair(kw, -l.x, -l.y, b0h[rr][h], b0l[rr][h]);
+        } else {
+          factor_pair(kw, l.x - x.x, l.y - x.y, a1h[2 * h + rr - 2], a1l[2 * h + rr - 2]);
+        }
+        factor_pair(kw, x.x - l.x, x.y - l.y, b1h[rr][h], b1l[rr][h]);
       }
+    }
+#pragma unroll
+    for (int n = 0; n < 2; n++) {
+      float(&d)[4] = acc[n];
+      mma_bf16_16816(d, a0h[0], a0h[1], a0h[2], a0h[3], b0h[n][0], b0h[n][1]);
+      mma_bf16_16816(d, a0h[0], a0h[1], a0h[2], a0h[3], b0l[n][0], b0l[n][1]);
+      mma_bf16_16816(d, a0l[0], a0l[1], a0l[2], a0l[3], b0h[n][0], b0h[n][1]);
+    }
+#pragma unroll
+    for (int n = 0; n < 4; n++) {
+      float(&d)[4] = acc[2 + n];
+      mma_bf16_16816(d, a1h[0], a1h[1], a1h[2], a1h[3], b1h[n][0], b1h[n][1]);
+      mma_bf16_16816(d, a1h[0], a1h[1], a1h[2], a1h[3], b1l[n][0], b1l[n][1]);
+      mma_bf16_16816(d, a1l[0], a1l[1], a1l[2], a1l[3], b1h[n][0], b1h[n][1]);
     }
   }
 #pragma unroll

@@ -233,12 +233,12 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                : "memory");
 }
 
-// fp32 -> tf32 with round-to-nearest (ties away), low 13 bits zero
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
+// fp32 -> tf32 (low 13 bits zero) rounded to nearest, ties away from zero:
+// adding half a tf32 unit to the magnitude bits carries into the kept bits
+// (and into the exponent) exactly when the dropped part is at least half a
+// unit; two integer operations, full rate.  Infinities stay infinite; a NaN
+// stays non-finite.
+__device__ __forceinline__ uint32_t to_tf32(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
 
 }  // namespace tc
 }  // namespace hypic
