@@ -107,17 +107,12 @@ struct __align__(1024) BuildTcSmem {
   unsigned char wt[32768];      // W  [64 t x 128 d] tf32, K-major: B of chain 1
   unsigned char yh[16384];      // Ytilde hi [128 j x 64 t] bf16: A of chain 2
   unsigned char yl[16384];      // Ytilde lo
-  union {
-    struct {
-      unsigned char bwh[8192];  // A diag(bG) hi [64 t x 64 t'] bf16: B of the W MMA
-      unsigned char bwl[8192];  //   lo
-    };
-    float pm[3][16][18];        // block products of the inverse (done before the factors)
-  };
+  unsigned char bwh[8192];      // A diag(bG) hi [64 t x 64 t'] bf16: B of the W MMA
+  unsigned char bwl[8192];      //   lo
   unsigned char buh[8192];      // A diag(b) hi: B of the U MMA
   unsigned char bul[8192];      //   lo
   float nm[64][68];             // M (rows 16-byte aligned for vector stores)
-  float am[64][66];             // A = (I + M)^-1 (rows 8-byte aligned for pair loads)
+  float am[64][68];             // A = (I + M)^-1 (pitch 68: conflict-free fragment columns)
   float lam[64], bg[64], bt[64];
   float ea[64], eb[64];         // b_t exp(lam_t - lam_0), exp(lam_0 - lam_i): M_ti = ea_t eb_i k_t.k_i
   float dec[3][64];             // exp(lam_C - lam_t) of chunk c in [c % 3] (read by X; pair loads)
@@ -168,15 +163,94 @@ __device__ __forceinline__ uint32_t trow(uint32_t base, int col) {
   return base + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)col;
 }
 // ---------------------------------------------------------------- UT inverse
-// A = (I + N)^-1 for the strictly lower 64 x 64 N in sm.nm, into sm.am:
-// diagonal 16 x 16 blocks by forward substitution (one thread per column),
-// then the off-diagonal blocks level by level,
-//     A_ij = -A_ii * sum_{k=j}^{i-1} N_ik A_kj      (i > j).
-// Called by the 128 threads of the P group (q = index in the group); ends
-// with a group barrier.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Accumulator of one 16 x 16 block product on the warp MMA (two n-tiles),
+// kept as three independent partial sums (hi*hi, hi*lo, lo*hi) so that the
+// three products of a split operand pair do not wait on one another.
+struct Acc3 {
+  float d[3][2][4];
+};
+__device__ __forceinline__ void acc_zero(Acc3 &c) {
+#pragma unroll
+  for (int s = 0; s < 3; s++)
+#pragma unroll
+    for (int n = 0; n < 2; n++) c.d[s][n][0] = c.d[s][n][1] = c.d[s][n][2] = c.d[s][n][3] = 0.f;
+}
+// c += Z Y^T for the A operand Z (fragments split hi + lo in ah / al) and
+// Y a 16 x 16 block in shared memory (pitch yp): element (k, n) of the B
+// operand is Y[n][k]
+__device__ __forceinline__ void acc_mma(Acc3 &c, const uint32_t (&ah)[4], const uint32_t (&al)[4], const float *Y,
+                                        int yp, int g, int u) {
+#pragma unroll
+  for (int nt = 0; nt < 2; nt++) {
+    const float *Yr = Y + (8 * nt + g) * yp;
+    const float2 y0 = *reinterpret_cast<const float2 *>(&Yr[2 * u]);
+    const float2 y1 = *reinterpret_cast<const float2 *>(&Yr[2 * u + 8]);
+    uint32_t bh0, bl0, bh1, bl1;
+    split_bf16x2(y0.x, y0.y, bh0, bl0);
+    split_bf16x2(y1.x, y1.y, bh1, bl1);
+    mma16816(c.d[0][nt], ah, bh0, bh1);
+    mma16816(c.d[1][nt], ah, bl0, bl1);
+    mma16816(c.d[2][nt], al, bh0, bh1);
+  }
+}
+// A operand X^T for a 16 x 16 block X in shared memory (pitch xp): element
+// (m, k) = X[k][m], split hi + lo
+__device__ __forceinline__ void frag_t(const float *X, int xp, int g, int u, uint32_t (&ah)[4], uint32_t (&al)[4]) {
+  split_bf16x2(X[(2 * u) * xp + g], X[(2 * u + 1) * xp + g], ah[0], al[0]);
+  split_bf16x2(X[(2 * u) * xp + g + 8], X[(2 * u + 1) * xp + g + 8], ah[1], al[1]);
+  split_bf16x2(X[(2 * u + 8) * xp + g], X[(2 * u + 9) * xp + g], ah[2], al[2]);
+  split_bf16x2(X[(2 * u + 8) * xp + g + 8], X[(2 * u + 9) * xp + g + 8], ah[3], al[3]);
+}
+// A operand from an accumulator (its C fragments are A fragments), split
+__device__ __forceinline__ void frag_acc(const Acc3 &c, uint32_t (&ah)[4], uint32_t (&al)[4]) {
+  float v[2][4];
+#pragma unroll
+  for (int n = 0; n < 2; n++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) v[n][e] = c.d[0][n][e] + (c.d[1][n][e] + c.d[2][n][e]);
+  split_bf16x2(v[0][0], v[0][1], ah[0], al[0]);
+  split_bf16x2(v[0][2], v[0][3], ah[1], al[1]);
+  split_bf16x2(v[1][0], v[1][1], ah[2], al[2]);
+  split_bf16x2(v[1][2], v[1][3], ah[3], al[3]);
+}
+// c = (A_ij)^T accumulated with the opposite sign: write A_ij = -c^T
+__device__ __forceinline__ void store_neg_t(const Acc3 &c, float *Ao, int g, int u) {
+#pragma unroll
+  for (int nt = 0; nt < 2; nt++) {
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) v[e] = c.d[0][nt][e] + (c.d[1][nt][e] + c.d[2][nt][e]);
+    Ao[(8 * nt + 2 * u) * 68 + g] = -v[0];
+    Ao[(8 * nt + 2 * u + 1) * 68 + g] = -v[1];
+    Ao[(8 * nt + 2 * u) * 68 + g + 8] = -v[2];
+    Ao[(8 * nt + 2 * u + 1) * 68 + g + 8] = -v[3];
+  }
+}
+__device__ __forceinline__ const float *nblk(const BuildTcSmem &sm, int i, int j) { return &sm.nm[16 * i][16 * j]; }
+__device__ __forceinline__ float *ablk(BuildTcSmem &sm, int i, int j) { return &sm.am[16 * i][16 * j]; }
+
+// A = (I + N)^-1 for the strictly lower 64 x 64 N in sm.nm, into the lower
+// blocks of sm.am (blocks above the block diagonal are left unwritten), by
+// recursive doubling over 16 x 16 blocks (i > j:  A_ij = -sum A_ia N_ak A_kj
+// over j <= k < a <= i, from (I + N) A = I):
+//   1. the diagonal blocks by forward substitution (one thread per column);
+//   2. the lower-left block of each 32 x 32 half, A_10 and A_32:
+//        A_ij = -A_ii (N_ij A_jj);
+//   3. the lower-left 32 x 32 quarter, one warp per block (i, j), i in
+//      {2, 3}, j in {0, 1}:
+//        P_aj = sum_{k=j}^{1} N_ak A_kj,   A_ij = -sum_{a=2}^{i} A_ia P_aj.
+// Stages 2 and 3 run on the legacy warp MMA in transposed form (each
+// product's accumulator is the next one's A operand), operands split
+// hi + lo.  Called by the 128 threads of the P group; ends with a group
+// barrier.
 __device__ void ut_inverse(BuildTcSmem &sm, int q) {
-  for (int e = q; e < 64 * 64; e += NG) sm.am[e >> 6][e & 63] = 0.f;
-  tc::named_bar(BAR_P, NG);
   if (q < 64) {
     const int b = 16 * (q >> 4), l = q & 15;
     float a[16];
@@ -194,46 +268,37 @@ __device__ void ut_inverse(BuildTcSmem &sm, int q) {
     for (int r = 0; r < 16; r++) sm.am[b + r][b + l] = a[r];
   }
   tc::named_bar(BAR_P, NG);
-  // off-diagonal levels; each thread forms 2 x 2 output tiles (64 per block)
-  for (int d = 1; d < 4; d++) {
-    const int nb = 4 - d;  // blocks (i, i - d), i = d .. 3
-    for (int e = q; e < nb * 64; e += NG) {
-      const int bq = e >> 6, r = 2 * ((e >> 3) & 7), c = 2 * (e & 7);
-      const int i = d + bq, j = i - d;
-      float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
-      for (int k = j; k < i; k++) {
-#pragma unroll
-        for (int m = 0; m < 16; m++) {
-          const float n0 = sm.nm[16 * i + r][16 * k + m], n1 = sm.nm[16 * i + r + 1][16 * k + m];
-          const float2 a = *reinterpret_cast<const float2 *>(&sm.am[16 * k + m][16 * j + c]);
-          s00 = fmaf(n0, a.x, s00);
-          s01 = fmaf(n0, a.y, s01);
-          s10 = fmaf(n1, a.x, s10);
-          s11 = fmaf(n1, a.y, s11);
-        }
-      }
-      *reinterpret_cast<float2 *>(&sm.pm[bq][r][c]) = make_float2(s00, s01);
-      *reinterpret_cast<float2 *>(&sm.pm[bq][r + 1][c]) = make_float2(s10, s11);
-    }
-    tc::named_bar(BAR_P, NG);
-    for (int e = q; e < nb * 64; e += NG) {
-      const int bq = e >> 6, r = 2 * ((e >> 3) & 7), c = 2 * (e & 7);
-      const int i = d + bq, j = i - d;
-      float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; m++) {
-        const float a0 = sm.am[16 * i + r][16 * i + m], a1 = sm.am[16 * i + r + 1][16 * i + m];
-        const float2 pv = *reinterpret_cast<const float2 *>(&sm.pm[bq][m][c]);
-        s00 = fmaf(a0, pv.x, s00);
-        s01 = fmaf(a0, pv.y, s01);
-        s10 = fmaf(a1, pv.x, s10);
-        s11 = fmaf(a1, pv.y, s11);
-      }
-      *reinterpret_cast<float2 *>(&sm.am[16 * i + r][16 * j + c]) = make_float2(-s00, -s01);
-      *reinterpret_cast<float2 *>(&sm.am[16 * i + r + 1][16 * j + c]) = make_float2(-s10, -s11);
-    }
-    tc::named_bar(BAR_P, NG);
+  const int wp = q >> 5, lane = q & 31, g = lane >> 2, u = lane & 3;
+  uint32_t ah[4], al[4];
+  if (wp < 2) {  // A_10 (warp 0), A_32 (warp 1)
+    const int i = 2 * wp + 1, j = 2 * wp;
+    Acc3 pc, ac;
+    acc_zero(pc);
+    frag_t(ablk(sm, j, j), 68, g, u, ah, al);
+    acc_mma(pc, ah, al, nblk(sm, i, j), 68, g, u);  // (N_ij A_jj)^T
+    frag_acc(pc, ah, al);
+    acc_zero(ac);
+    acc_mma(ac, ah, al, ablk(sm, i, i), 68, g, u);  // (A_ii N_ij A_jj)^T
+    store_neg_t(ac, ablk(sm, i, j), g, u);
   }
+  tc::named_bar(BAR_P, NG);
+  {
+    const int i = 2 + (wp & 1), j = wp >> 1;
+    Acc3 ac;
+    acc_zero(ac);
+    for (int a = 2; a <= i; a++) {
+      Acc3 pc;  // P_aj^T = sum_k (N_ak A_kj)^T
+      acc_zero(pc);
+      for (int k = j; k < 2; k++) {
+        frag_t(ablk(sm, k, j), 68, g, u, ah, al);
+        acc_mma(pc, ah, al, nblk(sm, a, k), 68, g, u);
+      }
+      frag_acc(pc, ah, al);
+      acc_mma(ac, ah, al, ablk(sm, i, a), 68, g, u);  // += (A_ia P_aj)^T
+    }
+    store_neg_t(ac, ablk(sm, i, j), g, u);
+  }
+  tc::named_bar(BAR_P, NG);
 }
 
 // Split factor tiles A diag(bG) and A diag(b) (K-major bf16 [64 t x 64 t'],
@@ -246,9 +311,11 @@ __device__ __forceinline__ void write_factors(BuildTcSmem &sm, int q) {
     uint32_t wh[4], wl[4], uh[4], ul[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) {
-      const float2 a = *reinterpret_cast<const float2 *>(&sm.am[t][c0 + 2 * j]);
-      split_bf16x2(a.x * sm.bg[c0 + 2 * j], a.y * sm.bg[c0 + 2 * j + 1], wh[j], wl[j]);
-      split_bf16x2(a.x * sm.bt[c0 + 2 * j], a.y * sm.bt[c0 + 2 * j + 1], uh[j], ul[j]);
+      // blocks above the block diagonal of am are not written: mask t' > t
+      const float2 a2 = *reinterpret_cast<const float2 *>(&sm.am[t][c0 + 2 * j]);
+      const float ax = (c0 + 2 * j <= t) ? a2.x : 0.f, ay = (c0 + 2 * j + 1 <= t) ? a2.y : 0.f;
+      split_bf16x2(ax * sm.bg[c0 + 2 * j], ay * sm.bg[c0 + 2 * j + 1], wh[j], wl[j]);
+      split_bf16x2(ax * sm.bt[c0 + 2 * j], ay * sm.bt[c0 + 2 * j + 1], uh[j], ul[j]);
     }
     const uint32_t off = sw16(t, c0, 64);
     *reinterpret_cast<uint4 *>(sm.bwh + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
