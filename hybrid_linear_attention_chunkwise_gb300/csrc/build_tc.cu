@@ -97,6 +97,29 @@ __device__ __forceinline__ uint64_t mndesc16(uint32_t base, int t) {
   return tc::smem_desc(base + (uint32_t)(t * 128), 8192, 1024, tc::SW_128B);
 }
 
+// An item as the X group needs it (slot / head of the output, chunk count,
+// index of its first chunk in the CTA's chunk sequence); valid = 0 ends the
+// sequence.
+struct XItem {
+  int32_t slot, head, n_ch, valid;
+  uint32_t gch0;
+};
+// The copy issuer of the P group (its thread 0; kept in shared memory):
+// chunks are loaded in the CTA's chunk order, two ahead of the chunk being
+// prepared, from the current item and the next one (fetched one item ahead).
+struct Issuer {
+  BuildItem it[2];  // [0] the current item, [1] the next
+  int kh[2], nch[2];
+  bool ok[2];
+  int w, ch;        // cursor: chunk ch of it[w]
+  uint32_t g;       // the CTA's index of the chunk at the cursor
+};
+struct PItem {
+  BuildItem it;
+  int32_t kh, n_ch, valid;
+  uint32_t gch0;
+};
+
 struct __align__(1024) BuildTcSmem {
   // inputs as TMA tiles [64 t x 128] bf16 in two 64-channel slabs: K of
   // chunk c in kin[c % 3] (read by P's Gram and W and by X's chains 2 one
@@ -124,8 +147,11 @@ struct __align__(1024) BuildTcSmem {
   uint64_t bar_x1, bar_x2;      // X's chain 2 completions (S half, T half; P waits on the T half's)
   uint64_t wt_ready, ys_done;   // P -> X: W staged, -U in place; X -> P: chain-1 output consumed
   uint64_t never;
+  uint64_t item_full[2], item_free[2];  // P -> X item hand-off (two slots)
+  XItem xslot[2];
+  PItem pitem;                  // the P group's current item (broadcast by its thread 0)
+  Issuer iss;
   uint32_t tmem_base;
-  int item;
   int abort;
 };
 
@@ -325,11 +351,12 @@ __device__ __forceinline__ void write_factors(BuildTcSmem &sm, int q) {
   }
 }
 
-// K (and, for the S half, V) of chunk `ch` of item `it`
-__device__ __forceinline__ void issue_chunk(BuildTcSmem &sm, const BuildItem &it, int ch, int kh,
+// K and V of chunk `ch` of item `it`, the CTA's chunk g (buffers g % 3 and
+// g % 2)
+__device__ __forceinline__ void issue_chunk(BuildTcSmem &sm, const BuildItem &it, int ch, uint32_t g, int kh,
                                             const CUtensorMap *tk, const CUtensorMap *tv) {
   const int32_t t0 = (int32_t)(it.start + (int64_t)C * ch);
-  const int bk = ch % NBUF, bv = ch & 1;
+  const int bk = (int)(g % NBUF), bv = (int)(g & 1);
   tc::mbar_expect_tx(&sm.full[bk], 32768u);
   for (int s = 0; s < 2; s++) tc::tma_load_3d(sm.kin[bk] + s * 8192, tk, 64 * s, kh, t0, &sm.full[bk]);
   for (int s = 0; s < 2; s++) tc::tma_load_3d(sm.vin[bv] + s * 8192, tv, 64 * s, it.head, t0, &sm.full[bk]);
@@ -340,6 +367,33 @@ struct ItemCtx {
   int n_ch;
   uint32_t gch0;  // index of the item's first chunk in this CTA's chunk sequence
 };
+
+// the next chunk to issue exists (moves the cursor into the next item when
+// the current one is exhausted)
+__device__ __forceinline__ bool iss_pending(Issuer &s) {
+  if (s.w == 0 && s.ch >= s.nch[0] && s.ok[1]) {
+    s.w = 1;
+    s.ch = 0;
+  }
+  return s.ok[s.w] && s.ch < s.nch[s.w];
+}
+__device__ __forceinline__ void iss_issue(BuildTcSmem &sm, Issuer &s, const CUtensorMap *tk, const CUtensorMap *tv) {
+  issue_chunk(sm, s.it[s.w], s.ch, s.g, s.kh[s.w], tk, tv);
+  s.ch++;
+  s.g++;
+}
+__device__ __forceinline__ void fetch_item(BuildTcSmem &sm, const BuildParams &p, int n_items, BuildItem &it, int &kh,
+                                           int &nch, bool &ok) {
+  const int idx = aborted(sm) ? n_items : atomicAdd(&p.plan->ticket, 1);
+  ok = idx < n_items;
+  nch = 0;
+  kh = 0;
+  if (ok) {
+    it = p.items[idx];
+    kh = (int)(((int64_t)it.head * p.h_k) / p.h_v);
+    nch = (int)((it.end - it.start + C - 1) / C);
+  }
+}
 
 struct MmaIds {
   uint32_t gram, wu, wu_neg, c1, c2;
@@ -355,7 +409,7 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
   const BuildItem &it = x.it;
   const bool gdn = p.variant == HYPIC_GDN;
   const uint32_t g = x.gch0 + (uint32_t)ch;  // global chunk index
-  const int bk = ch % NBUF, bv = ch & 1, b3 = (int)(g % 3);
+  const int bk = (int)(g % NBUF), bv = (int)(g & 1), b3 = (int)(g % 3);
   const int64_t t0 = it.start + (int64_t)C * ch;
   const int nt = (it.end - t0) < C ? (int)(it.end - t0) : C;
   const int wp = q >> 5, lane = q & 31;
@@ -497,13 +551,13 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
   tc::tc_fence_before();
   tc::named_bar(BAR_P, NG);
   if (q == 0) {
-    // chunk ch + 2 goes to K buffer (ch + 2) % 3 = (ch - 1) % 3, free once X's
-    // last chain 2 of chunk ch - 1 (T half) is done (waited before
-    // wt_ready, so the phase waited on is the latest one), and to V buffer
-    // ch % 2, whose U MMA above is complete
-    if (ch + 2 < x.n_ch) {
-      if (ch >= 1) wait_phase(sm, p, &sm.bar_x2, g - 1, LIM);
-      if (!aborted(sm)) issue_chunk(sm, it, ch + 2, x.kh, tk, tv);
+    // the CTA's chunk g + 2 (of this item or the next) goes to K buffer
+    // (g + 2) % 3 = (g - 1) % 3, free once X's last chain 2 of chunk g - 1
+    // (T half) is done (waited before wt_ready, so the phase waited on is the
+    // latest one), and to V buffer g % 2, whose U MMA above is complete
+    if (iss_pending(sm.iss) && sm.iss.g == g + 2) {
+      if (g > 0) wait_phase(sm, p, &sm.bar_x2, g - 1, LIM);
+      iss_issue(sm, sm.iss, tk, tv);
     }
     tc::mbar_arrive(&sm.wt_ready);
   }
@@ -592,7 +646,7 @@ __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int
 __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx &x, int ch, int n, uint32_t tm,
                             const MmaIds &id, uint32_t LIM) {
   const uint32_t g = x.gch0 + (uint32_t)ch;
-  const int bk = ch % NBUF, b3 = (int)(g % 3);
+  const int bk = (int)(g % NBUF), b3 = (int)(g % 3);
   wait_phase(sm, p, &sm.wt_ready, g, LIM);
   tc::tc_fence_after();
   const float gC = sm.gc[b3];
@@ -655,6 +709,10 @@ __global__ void __launch_bounds__(NT, 1)
     tc::mbar_init(&sm.wt_ready, 1);
     tc::mbar_init(&sm.ys_done, 1);
     tc::mbar_init(&sm.never, 1);
+    for (int b = 0; b < 2; b++) {
+      tc::mbar_init(&sm.item_full[b], 1);
+      tc::mbar_init(&sm.item_free[b], 1);
+    }
     sm.abort = 0;
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmap_k);
@@ -677,24 +735,51 @@ __global__ void __launch_bounds__(NT, 1)
   id.c1 = tc::idesc(tc::FMT_TF32, 128, 64);
   id.c2 = tc::idesc(tc::FMT_BF16, 128, 128, false, false, false, /*b_mn=*/true);
   uint32_t ph_full[NBUF] = {0, 0, 0};
-  uint32_t gch = 0;  // chunks processed by this CTA so far
   const int n_items = p.plan->n_items;
 
-  for (;;) {
-    if (n == 0) sm.item = aborted(sm) ? n_items : atomicAdd(&p.plan->ticket, 1);
-    __syncthreads();
-    const int idx = sm.item;
-    __syncthreads();
-    if (idx >= n_items) break;
-    ItemCtx x;
-    x.it = p.items[idx];
-    x.kh = (int)(((int64_t)x.it.head * p.h_k) / p.h_v);
-    x.n_ch = (int)((x.it.end - x.it.start + C - 1) / C);
-    x.gch0 = gch;
-
+  Issuer &iss = sm.iss;
+  if (is_p) {
+    if (q == 0) {
+      iss.w = 0;
+      iss.ch = 0;
+      iss.g = 0;
+      fetch_item(sm, p, n_items, iss.it[0], iss.kh[0], iss.nch[0], iss.ok[0]);
+      iss.ok[1] = false;
+      iss.nch[1] = 0;
+      if (iss.ok[0]) fetch_item(sm, p, n_items, iss.it[1], iss.kh[1], iss.nch[1], iss.ok[1]);
+    }
+  }
+  uint32_t gch = 0;  // chunks prepared by this CTA so far (P group)
+  for (int k = 0;; k++) {
     if (is_p) {
-      if (q == 0)  // chunks 0 and 1; chunk c + 2 is issued at the end of prep(c)
-        for (int ch = 0; ch < 2 && ch < x.n_ch; ch++) issue_chunk(sm, x.it, ch, x.kh, &tmap_k, &tmap_v);
+      if (q == 0) {
+        // item k to slot k % 2 once X has taken item k - 2 from it
+        if (k >= 2) wait_phase(sm, p, &sm.item_free[k & 1], (uint32_t)(k - 2) >> 1, LIM);
+        XItem xi;
+        xi.slot = iss.it[0].slot;
+        xi.head = iss.it[0].head;
+        xi.n_ch = iss.nch[0];
+        xi.valid = iss.ok[0] ? 1 : 0;
+        xi.gch0 = gch;
+        sm.xslot[k & 1] = xi;
+        tc::mbar_arrive(&sm.item_full[k & 1]);
+        sm.pitem.it = iss.it[0];
+        sm.pitem.kh = iss.kh[0];
+        sm.pitem.n_ch = iss.nch[0];
+        sm.pitem.valid = iss.ok[0] ? 1 : 0;
+        sm.pitem.gch0 = gch;
+        // the item's first two chunks, if not yet issued
+        while (iss_pending(iss) && iss.g <= gch + 1) iss_issue(sm, iss, &tmap_k, &tmap_v);
+      }
+      tc::named_bar(BAR_P, NG);
+      ItemCtx x;
+      x.it = sm.pitem.it;
+      x.kh = sm.pitem.kh;
+      x.n_ch = sm.pitem.n_ch;
+      x.gch0 = sm.pitem.gch0;
+      const bool valid = sm.pitem.valid != 0;
+      tc::named_bar(BAR_P, NG);
+      if (!valid) break;
       float g_cur = 0.f, b_cur = 0.f;
       if (q < C && x.it.start + q < x.it.end) {
         if (p.variant == HYPIC_GDN) g_cur = p.g[(x.it.start + q) * p.h_v + x.it.head];
@@ -702,7 +787,33 @@ __global__ void __launch_bounds__(NT, 1)
       }
       for (int ch = 0; ch < x.n_ch; ch++)
         prep_chunk(sm, p, x, ch, q, tm, id, LIM, ph_full, g_cur, b_cur, &tmap_k, &tmap_v);
+      gch += (uint32_t)x.n_ch;
+      if (q == 0) {  // the next item becomes current; fetch the one after it
+        if (iss.w == 1) {
+          iss.w = 0;
+        } else {
+          iss.ch = 0;
+        }
+        iss.it[0] = iss.it[1];
+        iss.kh[0] = iss.kh[1];
+        iss.nch[0] = iss.nch[1];
+        iss.ok[0] = iss.ok[1];
+        iss.ok[1] = false;
+        iss.nch[1] = 0;
+        if (iss.ok[0]) fetch_item(sm, p, n_items, iss.it[1], iss.kh[1], iss.nch[1], iss.ok[1]);
+      }
     } else {
+      const bool got = tc::mbar_wait(&sm.item_full[k & 1], ((uint32_t)k >> 1) & 1, aborted(sm) ? DRAIN_LIMIT : LIM);
+      if (!got) fail(sm, p);
+      const XItem xi = sm.xslot[k & 1];
+      tc::named_bar(BAR_X, NG);
+      if (n == 0) tc::mbar_arrive(&sm.item_free[k & 1]);
+      if (!got || !xi.valid) break;
+      ItemCtx x;
+      x.it.slot = xi.slot;
+      x.it.head = xi.head;
+      x.n_ch = xi.n_ch;
+      x.gch0 = xi.gch0;
       // X^T := [I | 0]
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -720,7 +831,7 @@ __global__ void __launch_bounds__(NT, 1)
       tc::named_bar(BAR_X, NG);
       for (int ch = 0; ch < x.n_ch; ch++) chain_chunk(sm, p, x, ch, n, tm, id, LIM);
       if (x.n_ch > 0) {
-        wait_phase(sm, p, &sm.bar_x2, gch + (uint32_t)x.n_ch - 1, DRAIN_LIMIT);
+        wait_phase(sm, p, &sm.bar_x2, x.gch0 + (uint32_t)x.n_ch - 1, DRAIN_LIMIT);
         tc::tc_fence_after();
       }
       // epilogue: lane n holds column n of T and of S
@@ -743,10 +854,8 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
+      tc::tc_fence_before();
     }
-    gch += (uint32_t)x.n_ch;
-    tc::tc_fence_before();
-    __syncthreads();
   }
   // every copy issued for an item is consumed inside it: nothing in flight
   tc::tc_fence_before();
