@@ -538,7 +538,7 @@ __device__ void prep_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx 
 // XR <- RN(X_h) (chain 1 reads the start-of-chunk state), X_h <- X_h
 // Diag(exp(lam_C)) (TMEM column d = row d of X), in one pass over the half.
 __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, const float *gC) {
-#pragma unroll
+#pragma unroll 1
   for (int c0 = 0; c0 < 128; c0 += 64) {
     uint32_t r[64];
     tc::tmem_ld32(trow(tm + tx, c0), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
@@ -748,10 +748,10 @@ __global__ void __launch_bounds__(NT, 1)
       // epilogue: lane n holds column n of T and of S
       const int64_t sh = ((int64_t)x.it.slot * p.h_v + x.it.head) * 128 * 128 + n;
       bool bad = false;
-#pragma unroll
+#pragma unroll 1
       for (int h = 0; h < 2; h++) {
         float *out = (h ? p.S_pool : p.T_pool) + sh;
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t r[32];
           tc::tmem_ld32(trow(tm + (h ? TM_XS : TM_XT), c0), r);

@@ -331,7 +331,7 @@ __device__ void ut_inverse(BuildTcSmem &sm, int q) {
 // hi and lo): thread q writes 32 consecutive t' of row q / 2.
 __device__ __forceinline__ void write_factors(BuildTcSmem &sm, int q) {
   const int t = q >> 1, q0 = 32 * (q & 1);
-#pragma unroll
+#pragma unroll 1
   for (int h8 = 0; h8 < 4; h8++) {
     const int c0 = q0 + 8 * h8;
     uint32_t wh[4], wl[4], uh[4], ul[4];
@@ -486,7 +486,7 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
     const int t = q;
     const bool fact = sm.fact != 0;  // uniform over the chunk
     const float lt = sm.lam[t], btt = sm.bt[t], eat = sm.ea[t];
-#pragma unroll
+#pragma unroll 1
     for (int c0 = 0; c0 < 64; c0 += 32) {
       uint32_t r[32];
       float li[32];
@@ -538,7 +538,7 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
   // of the previous chunk (T half) is done with it (each warp writes whole
   // row segments)
   if (g > 0) wait_phase(sm, p, &sm.bar_y2, g - 1, LIM);
-#pragma unroll
+#pragma unroll 1
   for (int c0 = 0; c0 < 64; c0 += 32) {
     uint32_t r[32];
     tc::tmem_ld32(trow(tm + TM_WG, c0), r);
@@ -569,7 +569,7 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
 // XR <- RN(X_h) (chain 1 reads the start-of-chunk state), X_h <- G_C X_h
 // (the accumulator chain 2 adds onto), in one pass over the half.
 __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC) {
-#pragma unroll
+#pragma unroll 1
   for (int c0 = 0; c0 < 128; c0 += 64) {
     uint32_t r[64];
     tc::tmem_ld32(trow(tm + tx, c0), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
@@ -619,7 +619,7 @@ __device__ __forceinline__ void issue_chain2(BuildTcSmem &sm, uint32_t tm, uint3
 // Ytilde = -Y diag(exp(lam_C - lam_t)), split hi + lo, as the K-major A
 // tiles [128 j x 64 t] of chain 2 (the S half's Y already holds -U)
 __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int b3) {
-#pragma unroll
+#pragma unroll 1
   for (int c0 = 0; c0 < 64; c0 += 32) {
     uint32_t r[32];
     tc::tmem_ld32(trow(tm + TM_Y, c0), r);
@@ -837,10 +837,10 @@ __global__ void __launch_bounds__(NT, 1)
       // epilogue: lane n holds column n of T and of S
       const int64_t sh = ((int64_t)x.it.slot * p.h_v + x.it.head) * 128 * 128 + n;
       bool bad = false;
-#pragma unroll
+#pragma unroll 1
       for (int h = 0; h < 2; h++) {
         float *out = (h ? p.S_pool : p.T_pool) + sh;
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t r[32];
           tc::tmem_ld32(trow(tm + (h ? TM_XS : TM_XT), c0), r);
