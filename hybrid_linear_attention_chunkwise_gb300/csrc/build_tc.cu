@@ -26,12 +26,14 @@
 // Two warp groups run one chunk apart:
 //   P (warps 4-7) prepares chunk c+1 from its inputs alone
 //       Gram   K K^T                              kind::f16, exact inputs
-//       UT     A = (I + M)^-1                     SIMT, 16 x 16 blocks
+//       UT     A = (I + M)^-1                     recursive doubling: 16 x 16
+//                                                 diagonal blocks SIMT, the rest
+//                                                 on the legacy warp MMA
 //       W, U   W^T = K^T (A diag(bG))^T,  U^T = V^T (A diag(b))^T
 //                                                 kind::f16, factors split hi + lo
-//       and stages W (tf32, rounded) as the B operand of chain 1; U goes
-//       straight to the chain-1 accumulator as -U^T;
+//       (U goes straight to the chain-1 accumulator as -U^T);
 //   X (warps 0-3) advances both halves through chunk c, S half first
+//       W        staged from TMEM as chain 1's B operand (tf32, rounded)
 //       chain 1  Y^T = X^T W^T (- U^T)            kind::tf32, A from TMEM
 //       Ytilde   = -Y diag(exp(lam_C - lam)), split hi + lo
 //       chain 2  X^T = G_C X^T + Ytilde^T K       kind::f16 (B = K tile, MN-major)
@@ -43,7 +45,9 @@
 //
 // Items are (segment, value head) in LPT order, pulled by an atomic
 // ticket.  Inputs come in by TMA (3-D maps over [token, head, channel],
-// 128-byte swizzle) through three buffers, two chunks ahead of their use.
+// 128-byte swizzle) through three K and two V buffers; chunk c + 1 is
+// copied in while chunk c is prepared.  X stages W itself once P's W / U
+// MMAs are complete, so P hands a chunk over as soon as they are issued.
 // All waits are bounded.
 #include <cstddef>
 
@@ -105,7 +109,7 @@ struct XItem {
   uint32_t gch0;
 };
 // The copy issuer of the P group (its thread 0; kept in shared memory):
-// chunks are loaded in the CTA's chunk order, two ahead of the chunk being
+// chunks are loaded in the CTA's chunk order, one ahead of the chunk being
 // prepared, from the current item and the next one (fetched one item ahead).
 struct Issuer {
   BuildItem it[2];  // [0] the current item, [1] the next
@@ -145,7 +149,8 @@ struct __align__(1024) BuildTcSmem {
   uint64_t bar_g, bar_wu;       // P's MMA completions
   uint64_t bar_y1, bar_y2;      // X's chain 1 completions (S half, T half; P waits on the T half's)
   uint64_t bar_x1, bar_x2;      // X's chain 2 completions (S half, T half; P waits on the T half's)
-  uint64_t wt_ready, ys_done;   // P -> X: W staged, -U in place; X -> P: chain-1 output consumed
+  uint64_t wt_ready, ys_done;   // P -> X: W / U MMAs issued; X -> P: chain-1 output consumed
+  uint64_t wg_free;             // X -> P: W read out of TM_WG (the next Gram may overwrite it)
   uint64_t never;
   uint64_t item_full[2], item_free[2];  // P -> X item hand-off (two slots)
   XItem xslot[2];
@@ -470,8 +475,15 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
   tc::fence_proxy_async_smem();  // zeroed tail rows are MMA operands
   tc::tc_fence_before();
   tc::named_bar(BAR_P, NG);
-  // ---- Gram K K^T (K-major view; padded rows 64..127 are ignored)
+  // ---- Gram K K^T (K-major view; padded rows 64..127 are ignored) once X
+  // has read the previous chunk's W out of TM_WG.  That also means the U MMA
+  // of chunk g - 1 is complete (X waits for it first), so V buffer
+  // (g + 1) % 2 is free: the CTA's chunk g + 1 is copied in now (K buffer
+  // (g + 1) % 3, free since X's chain 2 of chunk g - 2 was waited for at
+  // the end of prep(g - 1)).
   if (q == 0) {
+    if (g > 0) wait_phase(sm, p, &sm.wg_free, g - 1, LIM);
+    if (iss_pending(sm.iss) && sm.iss.g == g + 1 && !aborted(sm)) iss_issue(sm, sm.iss, tk, tv);
     tc::tc_fence_after();
     const uint32_t kb = tc::smem_u32(kin);
 #pragma unroll
@@ -531,34 +543,10 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
       tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(ul, 16 * ks, 64), id.wu_neg, 1u);
     }
     tc::mma_commit(&sm.bar_wu);
-  }
-  wait_phase(sm, p, &sm.bar_wu, g, DRAIN_LIMIT);
-  tc::tc_fence_after();
-  // ---- stage W (tf32, rounded) as chain 1's B tile once the last chain 1
-  // of the previous chunk (T half) is done with it (each warp writes whole
-  // row segments)
-  if (g > 0) wait_phase(sm, p, &sm.bar_y2, g - 1, LIM);
-#pragma unroll 1
-  for (int c0 = 0; c0 < 64; c0 += 32) {
-    uint32_t r[32];
-    tc::tmem_ld32(trow(tm + TM_WG, c0), r);
-    tc::tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 32; j++)
-      *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, q, 64)) = tc::to_tf32(__uint_as_float(r[j]));
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  tc::named_bar(BAR_P, NG);
-  if (q == 0) {
-    // the CTA's chunk g + 2 (of this item or the next) goes to K buffer
-    // (g + 2) % 3 = (g - 1) % 3, free once X's last chain 2 of chunk g - 1
-    // (T half) is done (waited before wt_ready, so the phase waited on is the
-    // latest one), and to V buffer g % 2, whose U MMA above is complete
-    if (iss_pending(sm.iss) && sm.iss.g == g + 2) {
-      if (g > 0) wait_phase(sm, p, &sm.bar_x2, g - 1, LIM);
-      iss_issue(sm, sm.iss, tk, tv);
-    }
+    // hand chunk g to X.  X's chain 2 of chunk g - 1 must be complete before
+    // the copy of chunk g + 2 reuses its K buffer ((g + 2) % 3): waited here,
+    // before wt_ready, so the phase waited on is the latest one.
+    if (g > 0) wait_phase(sm, p, &sm.bar_x2, g - 1, LIM);
     tc::mbar_arrive(&sm.wt_ready);
   }
   g_cur = g_nxt;
@@ -648,14 +636,31 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   const uint32_t g = x.gch0 + (uint32_t)ch;
   const int bk = (int)(g % NBUF), b3 = (int)(g % 3);
   wait_phase(sm, p, &sm.wt_ready, g, LIM);
+  // ---- W (tf32, rounded) as chain 1's B tile, once P's W / U MMAs are
+  // complete (lane n holds row n of W^T; the previous chunk's chain 1 that
+  // read the tile was waited on before its Ytilde)
+  wait_phase(sm, p, &sm.bar_wu, g, DRAIN_LIMIT);
   tc::tc_fence_after();
+#pragma unroll 1
+  for (int c0 = 0; c0 < 64; c0 += 32) {
+    uint32_t r[32];
+    tc::tmem_ld32(trow(tm + TM_WG, c0), r);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; j++)
+      *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, n, 64)) = tc::to_tf32(__uint_as_float(r[j]));
+  }
+  tc::fence_proxy_async_smem();
   const float gC = sm.gc[b3];
   // ---- S half (its chain 2 of the previous chunk was waited on before the
   // T half's Ytilde)
   stage_half(tm, TM_XS, gC);
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
-  if (n == 0) issue_chain1(sm, tm, id, true, &sm.bar_y1);
+  if (n == 0) {
+    tc::mbar_arrive(&sm.wg_free);  // TM_WG is free for the next chunk's Gram
+    issue_chain1(sm, tm, id, true, &sm.bar_y1);
+  }
   wait_phase(sm, p, &sm.bar_y1, g, DRAIN_LIMIT);
   tc::tc_fence_after();
   split_y(sm, tm, n, b3);
@@ -708,6 +713,7 @@ __global__ void __launch_bounds__(NT, 1)
     tc::mbar_init(&sm.bar_x2, 1);
     tc::mbar_init(&sm.wt_ready, 1);
     tc::mbar_init(&sm.ys_done, 1);
+    tc::mbar_init(&sm.wg_free, 1);
     tc::mbar_init(&sm.never, 1);
     for (int b = 0; b < 2; b++) {
       tc::mbar_init(&sm.item_full[b], 1);
@@ -768,8 +774,10 @@ __global__ void __launch_bounds__(NT, 1)
         sm.pitem.n_ch = iss.nch[0];
         sm.pitem.valid = iss.ok[0] ? 1 : 0;
         sm.pitem.gch0 = gch;
-        // the item's first two chunks, if not yet issued
-        while (iss_pending(iss) && iss.g <= gch + 1) iss_issue(sm, iss, &tmap_k, &tmap_v);
+        // the item's first chunk, if not yet issued (its V buffer held chunk
+        // gch - 2, whose U MMA X has waited for; the second chunk is issued
+        // by prep(gch) once the U MMA of chunk gch - 1 is known complete)
+        while (iss_pending(iss) && iss.g <= gch) iss_issue(sm, iss, &tmap_k, &tmap_v);
       }
       tc::named_bar(BAR_P, NG);
       ItemCtx x;
