@@ -30,16 +30,17 @@
 //               hi + lo, one k-quarter per warp, partials summed in order)
 //       UT      A = (I + M)^-1 (SIMT, 16 x 16 blocks)
 //       W, U    W^T = (K exp(lam))^T F^T,  -U^T = -V^T F^T   kind::f16, split
-//       and stages W (tf32, rounded) as the B operand of chain 1;
+//               (-U^T straight into the chain-1 accumulator);
 //   X (warps 0-3) advances both halves through chunk c, S half first
+//       W        staged from TMEM as chain 1's B operand (tf32, rounded)
 //       chain 1  Y^T = X^T W^T (- U^T)                kind::tf32, A from TMEM
 //       Ytilde   = -Y, split hi + lo
 //       chain 2  X^T = X^T Diag(exp(lam_C)) + Ytilde^T Khat   kind::f16
 // handing off through mbarriers.  fp32 accumulation throughout.
 //
 // Items are (segment, value head) in LPT order, pulled by an atomic ticket.
-// K, V and the log-gates come in by TMA through two buffers, one chunk ahead
-// of their preparation.  All waits are bounded.
+// K, V and the log-gates come in by TMA through two buffers; chunk c + 1 is
+// copied in while chunk c is prepared.  All waits are bounded.
 #include <cstddef>
 
 #include <cuda.h>
@@ -124,7 +125,8 @@ struct __align__(1024) BuildChSmem {
   uint64_t bar_wu;              // P's MMA completion
   uint64_t bar_y1, bar_y2;      // X's chain 1 completions (S half, T half)
   uint64_t bar_x1, bar_x2;      // X's chain 2 completions (S half, T half)
-  uint64_t wt_ready, ys_done;   // P -> X: W staged, -U in place; X -> P: chain-1 output consumed
+  uint64_t wt_ready, ys_done;   // P -> X: W / U MMAs issued; X -> P: chain-1 output consumed
+  uint64_t wg_free;             // X -> P: W read out of TM_W (the next W MMA may overwrite it)
   uint64_t never;
   uint32_t tmem_base;
   int item;
@@ -476,6 +478,14 @@ __device__ void prep_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx 
   tc::named_bar(BAR_P, NG);
   const bool direct = (sm.fb[0] | sm.fb[1] | sm.fb[2] | sm.fb[3]) != 0;  // uniform over the group
   tiles_pass(sm, bk, b2, q);
+  if (q == 0 && ch >= 1 && ch + 1 < x.n_ch) {
+    // chunk ch + 1 goes to input buffer (ch + 1) % 2, which held chunk ch - 1:
+    // its U MMA (the last reader of its V tile) is complete once bar_wu of
+    // chunk g - 1 is (the phase waited on is the latest: the next one needs
+    // this chunk's W / U MMAs, issued below)
+    wait_phase(sm, p, &sm.bar_wu, g - 1, LIM);
+    if (!aborted(sm)) issue_chunk(sm, it, ch + 1, x.kh, tk, tv, tg);
+  }
   if (!direct) {
     gram_pass(sm, bk, wp, lane);
     tc::named_bar(BAR_P, NG);
@@ -491,7 +501,10 @@ __device__ void prep_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx 
   tc::named_bar(BAR_P, NG);
   // ---- W^T = (K exp(lam))^T F^T, and -U^T = -V^T F^T straight into the
   // chain-1 accumulator once X has consumed the previous chunk's chain-1 output
-  if (g > 0) wait_phase(sm, p, &sm.ys_done, g - 1, LIM);
+  if (g > 0) {
+    wait_phase(sm, p, &sm.ys_done, g - 1, LIM);
+    wait_phase(sm, p, &sm.wg_free, g - 1, LIM);  // X has read the previous W out of TM_W
+  }
   if (q == 0) {
     tc::tc_fence_after();
     const uint32_t gh = tc::smem_u32(sm.kgh), gl = tc::smem_u32(sm.kgl), vb = tc::smem_u32(sm.vin[bk]);
@@ -505,29 +518,9 @@ __device__ void prep_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx 
       tc::mma_ss_f16(tm + TM_Y, mndesc(vb, 16 * ks), kdesc16(fl, 16 * ks, C), id.wu_neg, 1u);
     }
     tc::mma_commit(&sm.bar_wu);
-  }
-  wait_phase(sm, p, &sm.bar_wu, g, DRAIN_LIMIT);
-  tc::tc_fence_after();
-  // ---- stage W (tf32, rounded) as chain 1's B tile once the last chain 1
-  // of the previous chunk (T half) is done with it
-  if (g > 0) wait_phase(sm, p, &sm.bar_y2, g - 1, LIM);
-  {
-    uint32_t r[32];
-    tc::tmem_ld32(trow(tm + TM_W, 0), r);
-    tc::tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 32; j++)
-      *reinterpret_cast<uint32_t *>(sm.wt + sw32(j, q, C)) = tc::to_tf32(__uint_as_float(r[j]));
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  tc::named_bar(BAR_P, NG);
-  if (q == 0) {
-    // input buffer bk is consumed (the U MMA that read V is complete): chunk
-    // ch + 2 goes there.  Chunk g is handed over once X has finished chunk
-    // g - 1 (waited before wt_ready, so the phase waited on is the latest);
-    // that also frees the Khat buffer that chunk g + 1 will use.
-    if (ch + 2 < x.n_ch && !aborted(sm)) issue_chunk(sm, it, ch + 2, x.kh, tk, tv, tg);
+    // hand chunk g to X once X has finished chunk g - 1 (waited before
+    // wt_ready, so the phase waited on is the latest); that also frees the
+    // Khat buffer and exp(lam_C) slot that chunk g + 1 will use
     if (g > 0) wait_phase(sm, p, &sm.bar_x2, g - 1, LIM);
     tc::mbar_arrive(&sm.wt_ready);
   }
@@ -621,14 +614,30 @@ __device__ void chain_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx
   const uint32_t g = x.gch0 + (uint32_t)ch;
   const int b2 = (int)(g & 1);
   wait_phase(sm, p, &sm.wt_ready, g, LIM);
+  // ---- W (tf32, rounded) as chain 1's B tile once P's W / U MMAs are
+  // complete (lane n holds row n of W^T; the previous chunk's chain 1 that
+  // read the tile was waited on before its Ytilde)
+  wait_phase(sm, p, &sm.bar_wu, g, DRAIN_LIMIT);
   tc::tc_fence_after();
+  {
+    uint32_t r[32];
+    tc::tmem_ld32(trow(tm + TM_W, 0), r);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; j++)
+      *reinterpret_cast<uint32_t *>(sm.wt + sw32(j, n, C)) = tc::to_tf32(__uint_as_float(r[j]));
+  }
+  tc::fence_proxy_async_smem();
   const float *gC = sm.gcv[b2];
   // ---- S half (its chain 2 of the previous chunk was waited on before the
   // T half's Ytilde)
   stage_half(tm, TM_XS, gC);
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
-  if (n == 0) issue_chain1(sm, tm, id, true, &sm.bar_y1);
+  if (n == 0) {
+    tc::mbar_arrive(&sm.wg_free);  // TM_W is free for the next chunk's W
+    issue_chain1(sm, tm, id, true, &sm.bar_y1);
+  }
   wait_phase(sm, p, &sm.bar_y1, g, DRAIN_LIMIT);
   tc::tc_fence_after();
   split_y(sm, tm, n);
@@ -679,6 +688,7 @@ __global__ void __launch_bounds__(NT, 1)
     tc::mbar_init(&sm.bar_x2, 1);
     tc::mbar_init(&sm.wt_ready, 1);
     tc::mbar_init(&sm.ys_done, 1);
+    tc::mbar_init(&sm.wg_free, 1);
     tc::mbar_init(&sm.never, 1);
     sm.abort = 0;
     tc::fence_mbar_init();
