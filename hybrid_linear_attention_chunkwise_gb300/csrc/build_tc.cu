@@ -148,7 +148,10 @@ struct __align__(1024) BuildTcSmem {
   uint64_t full[NBUF];
   uint64_t bar_g, bar_wu;       // P's MMA completions
   uint64_t bar_y1, bar_y2;      // X's chain 1 completions (S half, T half; P waits on the T half's)
-  uint64_t bar_x1, bar_x2;      // X's chain 2 completions (S half, T half; P waits on the T half's)
+  uint64_t bar_x1;              // X's chain 2 completion, S half
+  uint64_t bar_x2[2];           // X's chain 2 completion, T half, of chunks g with g % 2 = [i]
+                                // (phase g / 2): P can wait for chunk g - 2 while chunk g - 1
+                                // may already be complete
   uint64_t wt_ready, ys_done;   // P -> X: W / U MMAs issued; X -> P: chain-1 output consumed
   uint64_t wg_free;             // X -> P: W read out of TM_WG (the next Gram may overwrite it)
   uint64_t never;
@@ -478,12 +481,16 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
   // ---- Gram K K^T (K-major view; padded rows 64..127 are ignored) once X
   // has read the previous chunk's W out of TM_WG.  That also means the U MMA
   // of chunk g - 1 is complete (X waits for it first), so V buffer
-  // (g + 1) % 2 is free: the CTA's chunk g + 1 is copied in now (K buffer
-  // (g + 1) % 3, free since X's chain 2 of chunk g - 2 was waited for at
-  // the end of prep(g - 1)).
+  // (g + 1) % 2 is free: the CTA's chunk g + 1 is copied in now, into K
+  // buffer (g + 1) % 3 once X's chain 2 of chunk g - 2 (its last reader) is
+  // complete.  That barrier's next phase is chunk g's, which needs wt_ready
+  // of chunk g, arrived below: the phase waited on is its latest.
   if (q == 0) {
     if (g > 0) wait_phase(sm, p, &sm.wg_free, g - 1, LIM);
-    if (iss_pending(sm.iss) && sm.iss.g == g + 1 && !aborted(sm)) iss_issue(sm, sm.iss, tk, tv);
+    if (iss_pending(sm.iss) && sm.iss.g == g + 1 && !aborted(sm)) {
+      if (g >= 2) wait_phase(sm, p, &sm.bar_x2[(g - 2) & 1], (g - 2) >> 1, LIM);
+      iss_issue(sm, sm.iss, tk, tv);
+    }
     tc::tc_fence_after();
     const uint32_t kb = tc::smem_u32(kin);
 #pragma unroll
@@ -543,11 +550,7 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
       tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(ul, 16 * ks, 64), id.wu_neg, 1u);
     }
     tc::mma_commit(&sm.bar_wu);
-    // hand chunk g to X.  X's chain 2 of chunk g - 1 must be complete before
-    // the copy of chunk g + 2 reuses its K buffer ((g + 2) % 3): waited here,
-    // before wt_ready, so the phase waited on is the latest one.
-    if (g > 0) wait_phase(sm, p, &sm.bar_x2, g - 1, LIM);
-    tc::mbar_arrive(&sm.wt_ready);
+    tc::mbar_arrive(&sm.wt_ready);  // hand chunk g to X
   }
   g_cur = g_nxt;
   b_cur = b_nxt;
@@ -670,7 +673,7 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   if (n == 0) issue_chain2(sm, tm, TM_XS, bk, id, &sm.bar_x1);
   // ---- T half: XR is free (chain 1 of S is complete); the T half's chain 2
   // of the previous chunk must be
-  if (ch > 0) wait_phase(sm, p, &sm.bar_x2, g - 1, DRAIN_LIMIT);
+  if (ch > 0) wait_phase(sm, p, &sm.bar_x2[(g - 1) & 1], (g - 1) >> 1, DRAIN_LIMIT);
   tc::tc_fence_after();
   stage_half(tm, TM_XT, gC);
   tc::tc_fence_before();
@@ -686,7 +689,7 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   tc::named_bar(BAR_X, NG);
   if (n == 0) {
     tc::mbar_arrive(&sm.ys_done);  // TM_Y is free for the next chunk's -U
-    issue_chain2(sm, tm, TM_XT, bk, id, &sm.bar_x2);
+    issue_chain2(sm, tm, TM_XT, bk, id, &sm.bar_x2[g & 1]);
   }
 }
 
@@ -710,7 +713,8 @@ __global__ void __launch_bounds__(NT, 1)
     tc::mbar_init(&sm.bar_y1, 1);
     tc::mbar_init(&sm.bar_y2, 1);
     tc::mbar_init(&sm.bar_x1, 1);
-    tc::mbar_init(&sm.bar_x2, 1);
+    tc::mbar_init(&sm.bar_x2[0], 1);
+    tc::mbar_init(&sm.bar_x2[1], 1);
     tc::mbar_init(&sm.wt_ready, 1);
     tc::mbar_init(&sm.ys_done, 1);
     tc::mbar_init(&sm.wg_free, 1);
@@ -774,10 +778,15 @@ __global__ void __launch_bounds__(NT, 1)
         sm.pitem.n_ch = iss.nch[0];
         sm.pitem.valid = iss.ok[0] ? 1 : 0;
         sm.pitem.gch0 = gch;
-        // the item's first chunk, if not yet issued (its V buffer held chunk
-        // gch - 2, whose U MMA X has waited for; the second chunk is issued
-        // by prep(gch) once the U MMA of chunk gch - 1 is known complete)
-        while (iss_pending(iss) && iss.g <= gch) iss_issue(sm, iss, &tmap_k, &tmap_v);
+        // the item's first chunk, if not yet issued (only at the start, or
+        // after items with an empty body).  Its buffers last held chunks
+        // gch - 3 (K) and gch - 2 (V); once X has read W of chunk gch - 1,
+        // X has waited for chain 2 of chunk gch - 3 and for the W / U MMAs
+        // of chunk gch - 1.  The second chunk is issued by prep(gch).
+        if (iss_pending(iss) && iss.g <= gch) {
+          if (gch > 0) wait_phase(sm, p, &sm.wg_free, gch - 1, LIM);
+          while (iss_pending(iss) && iss.g <= gch) iss_issue(sm, iss, &tmap_k, &tmap_v);
+        }
       }
       tc::named_bar(BAR_P, NG);
       ItemCtx x;
@@ -839,7 +848,8 @@ __global__ void __launch_bounds__(NT, 1)
       tc::named_bar(BAR_X, NG);
       for (int ch = 0; ch < x.n_ch; ch++) chain_chunk(sm, p, x, ch, n, tm, id, LIM);
       if (x.n_ch > 0) {
-        wait_phase(sm, p, &sm.bar_x2, x.gch0 + (uint32_t)x.n_ch - 1, DRAIN_LIMIT);
+        const uint32_t gl = x.gch0 + (uint32_t)x.n_ch - 1;
+        wait_phase(sm, p, &sm.bar_x2[gl & 1], gl >> 1, DRAIN_LIMIT);
         tc::tc_fence_after();
       }
       // epilogue: lane n holds column n of T and of S
