@@ -124,7 +124,9 @@ struct __align__(1024) BuildChSmem {
   uint64_t full[2];
   uint64_t bar_wu;              // P's MMA completion
   uint64_t bar_y1, bar_y2;      // X's chain 1 completions (S half, T half)
-  uint64_t bar_x1, bar_x2;      // X's chain 2 completions (S half, T half)
+  uint64_t bar_x1;              // X's chain 2 completion, S half
+  uint64_t bar_x2[2];           // X's chain 2 completion, T half, of chunks g with g % 2 = [i]
+                                // (phase g / 2)
   uint64_t wt_ready, ys_done;   // P -> X: W / U MMAs issued; X -> P: chain-1 output consumed
   uint64_t wg_free;             // X -> P: W read out of TM_W (the next W MMA may overwrite it)
   uint64_t never;
@@ -474,6 +476,11 @@ __device__ void prep_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx 
     }
   }
   if (q < C) sm.bt[q] = b_cur;
+  // the Khat buffer and exp(lam_C) slot of this chunk held chunk g - 2: its
+  // chain 2 (the last reader) must be complete.  That barrier's next phase is
+  // chunk g's, which needs this chunk's wt_ready: the phase waited on is its
+  // latest.  (An item's first two chunks follow the item barrier.)
+  if (ch >= 2) wait_phase(sm, p, &sm.bar_x2[(g - 2) & 1], (g - 2) >> 1, LIM);
   lam_pass(sm, bk, b2, nt, q);
   tc::named_bar(BAR_P, NG);
   const bool direct = (sm.fb[0] | sm.fb[1] | sm.fb[2] | sm.fb[3]) != 0;  // uniform over the group
@@ -518,11 +525,7 @@ __device__ void prep_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx 
       tc::mma_ss_f16(tm + TM_Y, mndesc(vb, 16 * ks), kdesc16(fl, 16 * ks, C), id.wu_neg, 1u);
     }
     tc::mma_commit(&sm.bar_wu);
-    // hand chunk g to X once X has finished chunk g - 1 (waited before
-    // wt_ready, so the phase waited on is the latest); that also frees the
-    // Khat buffer and exp(lam_C) slot that chunk g + 1 will use
-    if (g > 0) wait_phase(sm, p, &sm.bar_x2, g - 1, LIM);
-    tc::mbar_arrive(&sm.wt_ready);
+    tc::mbar_arrive(&sm.wt_ready);  // hand chunk g to X
   }
   b_cur = b_nxt;
 }
@@ -647,7 +650,7 @@ __device__ void chain_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx
   if (n == 0) issue_chain2(sm, tm, TM_XS, b2, id, &sm.bar_x1);
   // ---- T half: XR is free (chain 1 of S is complete); the T half's chain 2
   // of the previous chunk must be
-  if (ch > 0) wait_phase(sm, p, &sm.bar_x2, g - 1, DRAIN_LIMIT);
+  if (ch > 0) wait_phase(sm, p, &sm.bar_x2[(g - 1) & 1], (g - 1) >> 1, DRAIN_LIMIT);
   tc::tc_fence_after();
   stage_half(tm, TM_XT, gC);
   tc::tc_fence_before();
@@ -663,7 +666,7 @@ __device__ void chain_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx
   tc::named_bar(BAR_X, NG);
   if (n == 0) {
     tc::mbar_arrive(&sm.ys_done);  // TM_Y is free for the next chunk's -U
-    issue_chain2(sm, tm, TM_XT, b2, id, &sm.bar_x2);
+    issue_chain2(sm, tm, TM_XT, b2, id, &sm.bar_x2[g & 1]);
   }
 }
 
@@ -685,7 +688,8 @@ __global__ void __launch_bounds__(NT, 1)
     tc::mbar_init(&sm.bar_y1, 1);
     tc::mbar_init(&sm.bar_y2, 1);
     tc::mbar_init(&sm.bar_x1, 1);
-    tc::mbar_init(&sm.bar_x2, 1);
+    tc::mbar_init(&sm.bar_x2[0], 1);
+    tc::mbar_init(&sm.bar_x2[1], 1);
     tc::mbar_init(&sm.wt_ready, 1);
     tc::mbar_init(&sm.ys_done, 1);
     tc::mbar_init(&sm.wg_free, 1);
@@ -752,7 +756,8 @@ __global__ void __launch_bounds__(NT, 1)
       tc::named_bar(BAR_X, NG);
       for (int ch = 0; ch < x.n_ch; ch++) chain_chunk(sm, p, x, ch, n, tm, id, LIM);
       if (x.n_ch > 0) {
-        wait_phase(sm, p, &sm.bar_x2, gch + (uint32_t)x.n_ch - 1, DRAIN_LIMIT);
+        const uint32_t gl = gch + (uint32_t)x.n_ch - 1;
+        wait_phase(sm, p, &sm.bar_x2[gl & 1], gl >> 1, DRAIN_LIMIT);
         tc::tc_fence_after();
       }
       // epilogue: lane n holds column n of T and of S
