@@ -59,8 +59,16 @@ class ComposeDesc(ctypes.Structure):
                 ("workspace", P), ("workspace_bytes", ctypes.c_size_t), ("status", P)]
 
 
+class MergeDesc(ctypes.Structure):
+    _fields_ = [("n_merge", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("variant", ctypes.c_int32),
+                ("later", P), ("earlier", P), ("out", P),
+                ("n_slots_in", ctypes.c_int64), ("n_slots_out", ctypes.c_int64),
+                ("T_in", P), ("S_in", P), ("T_out", P), ("S_out", P), ("status", P)]
+
+
 SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_workspace_bytes", "hypic_compose",
-           "hypic_compose_workspace_bytes", "hypic_plan_lpt", "hypic_status_from_word",
+           "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_plan_lpt", "hypic_status_from_word",
            "hypic_status_string", "hypic_version")
 
 
@@ -92,6 +100,8 @@ def load():
             lib.hypic_compose.restype = ctypes.c_int
             lib.hypic_compose_workspace_bytes.argtypes = [ctypes.POINTER(ComposeDesc)]
             lib.hypic_compose_workspace_bytes.restype = ctypes.c_size_t
+            lib.hypic_pair_merge.argtypes = [ctypes.POINTER(MergeDesc), P]
+            lib.hypic_pair_merge.restype = ctypes.c_int
             lib.hypic_plan_lpt.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P]
             lib.hypic_plan_lpt.restype = ctypes.c_int
             lib.hypic_status_from_word.argtypes = [ctypes.c_uint32]
@@ -268,6 +278,30 @@ def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, 
     rc = lib.hypic_compose(ctypes.byref(d), _stream(stream))
     if rc != OK:
         raise HypicError(rc, "hypic_compose")
+
+
+def pair_merge(later, earlier, out, T_in, S_in, T_out, S_out, *, variant: str, status=None, stream=None):
+    """hypic_pair_merge on torch tensors: for every merge m and head h,
+    T_out[out[m], h] = T_in[later[m], h] T_in[earlier[m], h] and
+    S_out[out[m], h] = T_in[later[m], h] S_in[earlier[m], h] + S_in[later[m], h].
+    later / earlier / out int32 [n_merge] (device); pools as written by
+    segment_build (T layout per variant, S [slots, h_v, d_k, d_v])."""
+    lib = load()
+    for name, t in (("later", later), ("earlier", earlier), ("out", out)):
+        _check(t, name, dtype=torch.int32, ndim=1)
+    _check(S_in, "S_in", dtype=torch.float32, ndim=4)
+    _check(S_out, "S_out", dtype=torch.float32, ndim=4)
+    d = MergeDesc()
+    d.n_merge = later.shape[0]
+    _, d.h_v, d.d_k, d.d_v = S_in.shape
+    d.variant = VARIANT[variant]
+    d.later, d.earlier, d.out = _ptr(later), _ptr(earlier), _ptr(out)
+    d.n_slots_in, d.n_slots_out = S_in.shape[0], S_out.shape[0]
+    d.T_in, d.S_in, d.T_out, d.S_out = _ptr(T_in), _ptr(S_in), _ptr(T_out), _ptr(S_out)
+    d.status = _ptr(status)
+    rc = lib.hypic_pair_merge(ctypes.byref(d), _stream(stream))
+    if rc != OK:
+        raise HypicError(rc, "hypic_pair_merge")
 
 
 def plan_lpt(costs, n_workers: int):

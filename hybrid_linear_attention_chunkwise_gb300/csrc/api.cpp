@@ -297,4 +297,37 @@ int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream) {
   return HYPIC_OK;
 }
 
+int hypic_pair_merge(const hypic_merge_desc *d, hypic_stream_t stream) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_merge < 0 || d->h_v < 1 || d->d_k < 1 || d->d_v < 1) return HYPIC_ERR_INVALID_ARG;
+  if (d->variant < HYPIC_GDN || d->variant > HYPIC_DIAG_GATE) return HYPIC_ERR_INVALID_ARG;
+  if (d->d_k > 128 || d->d_v > 128) return HYPIC_ERR_UNSUPPORTED;
+  if (d->n_slots_in < 0 || d->n_slots_out < 0) return HYPIC_ERR_INVALID_ARG;
+  if ((int64_t)d->n_merge * d->h_v > INT32_MAX) return HYPIC_ERR_UNSUPPORTED;
+  if (d->n_merge == 0) return HYPIC_OK;
+  if (!d->later || !d->earlier || !d->out || !aligned(d->later, 4) || !aligned(d->earlier, 4) || !aligned(d->out, 4))
+    return HYPIC_ERR_INVALID_ARG;
+  if (!d->T_in || !d->S_in || !d->T_out || !d->S_out) return HYPIC_ERR_INVALID_ARG;
+  if (!aligned(d->T_in, 4) || !aligned(d->S_in, 4) || !aligned(d->T_out, 4) || !aligned(d->S_out, 4))
+    return HYPIC_ERR_INVALID_ARG;
+  MergeParams p{};
+  p.n_merge = d->n_merge;
+  p.h_v = d->h_v;
+  p.d_k = d->d_k;
+  p.d_v = d->d_v;
+  p.variant = d->variant;
+  p.later = d->later;
+  p.earlier = d->earlier;
+  p.out = d->out;
+  p.n_slots_in = d->n_slots_in;
+  p.n_slots_out = d->n_slots_out;
+  p.T_in = d->T_in;
+  p.S_in = d->S_in;
+  p.T_out = d->T_out;
+  p.S_out = d->S_out;
+  p.status = d->status;
+  if (launch_merge(p, wait_limit(), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return HYPIC_ERR_CUDA;
+  return HYPIC_OK;
+}
+
 }  // extern "C"

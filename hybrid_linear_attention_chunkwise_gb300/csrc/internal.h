@@ -57,6 +57,15 @@ struct ComposeParams {
   uint32_t *status;
 };
 
+struct MergeParams {
+  int32_t n_merge, h_v, d_k, d_v, variant;
+  const int32_t *later, *earlier, *out;
+  int64_t n_slots_in, n_slots_out;
+  const float *T_in, *S_in;
+  float *T_out, *S_out;
+  uint32_t *status;
+};
+
 __host__ __device__ inline bool is_delta(int v) { return v == HYPIC_GDN || v == HYPIC_DELTANET || v == HYPIC_CHANNEL_DELTA; }
 __host__ __device__ inline bool is_dense_T(int v) { return is_delta(v); }
 __host__ __device__ inline bool is_vector_gate(int v) { return v == HYPIC_CHANNEL_DELTA || v == HYPIC_DIAG_GATE; }
@@ -89,6 +98,13 @@ bool make_tmap_tokens(CUtensorMap *map, const void *base, int64_t n_tokens, int 
 bool build_channel_supported(const BuildParams &p);
 cudaError_t launch_build_channel(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, uint32_t wait_limit,
                                  cudaStream_t s);
+// 2-D fp32 view [rows, 128] with 32-column x box_rows tiles and 128-byte
+// swizzle (one K-slab of a K-major tf32 MMA operand per tile).
+bool make_tmap_f32_rows(CUtensorMap *map, const float *base, uint64_t rows, uint32_t box_rows);
+// Pair merge: tensor cores for dense d_k = d_v = 128 with 16-byte aligned
+// pools, fp32 CUDA-core kernel otherwise.
+bool merge_tc_supported(const MergeParams &p);
+cudaError_t launch_merge(const MergeParams &p, uint32_t wait_limit, cudaStream_t s);
 cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s);
 // The tensor-core compose covers dense transitions, bf16 seam tokens,

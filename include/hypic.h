@@ -196,6 +196,45 @@ size_t hypic_compose_workspace_bytes(const hypic_compose_desc *d);
 int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream);
 
 /*
+ * hypic_pair_merge -- merge cached pairs of adjacent spans (pages §2.1: the
+ * composition rule applied to two segments, S(C1.C2) = T(C2) S(C1) + S(C2),
+ * with the transition of the joined span T(C1.C2) = T(C2) T(C1)):
+ *   for each merge m and value head h, with a = later[m], b = earlier[m],
+ *   o = out[m] (pool slots):
+ *     T_out[o, h] = T_in[a, h] T_in[b, h]
+ *     S_out[o, h] = T_in[a, h] S_in[b, h] + S_in[a, h]
+ * The merge is associative, so repeated merges build the pair of any run of
+ * consecutive segments (a tree of merges composes a chain in log depth).
+ * T layouts follow the variant as in hypic_segment_build: dense
+ * [slots, h_v, d_k, d_k] for GDN / DELTANET / CHANNEL_DELTA (matrix
+ * product), [slots, h_v] for SCALAR_DECAY / UNGATED (scalar product),
+ * [slots, h_v, d_k] for DIAG_GATE (elementwise product; S rows scaled).
+ * S pools are [slots, h_v, d_k, d_v].  All fp32.
+ * Slots index the input pools (n_slots_in) and the output pools
+ * (n_slots_out); a merge with a slot out of range is skipped and reported
+ * (HYPIC_STATUS_BAD_SLOT).  Output slots must be distinct, and when the
+ * output pools alias the input pools no output slot of a call may be an
+ * input slot of the same call (results are undefined otherwise).
+ * Dense d_k = d_v = 128 runs on the tensor cores with split tf32 operands
+ * (about fp32 accuracy); other shapes and the scalar / diagonal forms run on
+ * the CUDA cores in fp32.
+ */
+typedef struct {
+  int32_t n_merge;
+  int32_t h_v, d_k, d_v;
+  int32_t variant;
+  const int32_t *later;       /* [dev] [n_merge] slot of the later pair (T2, S2) */
+  const int32_t *earlier;     /* [dev] [n_merge] slot of the earlier pair (T1, S1) */
+  const int32_t *out;         /* [dev] [n_merge] output slot */
+  int64_t n_slots_in, n_slots_out;
+  const float *T_in, *S_in;   /* [dev] input pools */
+  float *T_out, *S_out;       /* [dev] output pools (may be the input pools, see above) */
+  uint32_t *status;           /* [dev] optional */
+} hypic_merge_desc;
+
+int hypic_pair_merge(const hypic_merge_desc *d, hypic_stream_t stream);
+
+/*
  * hypic_plan_lpt -- greedy longest-processing-time-first packing of items
  * over workers (pages §2.3: LPT balancing of segments over scatter workers).
  * Items are taken in order of decreasing cost (ties: lower index first) and
