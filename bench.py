@@ -95,9 +95,10 @@ KERNEL_SOURCES = {
     "build": ("build_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
     "compose": ("compose_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
     "channel": ("build_channel.cu", "tc.cuh", "common.cuh", "internal.h"),
+    "merge": ("merge.cu", "tc.cuh", "common.cuh", "internal.h"),
 }
 PROFILE_FILES = {"build": "segment_build_tc__gdn_16x1024.md", "compose": "compose_seam_mma__gdn_4x32x100.md",
-                 "channel": "segment_build_channel__16x1024.md"}
+                 "channel": "segment_build_channel__16x1024.md", "merge": "pair_merge_tc__4x32x50.md"}
 
 
 def source_hash(kind):
@@ -262,6 +263,31 @@ def _time_ms(fn, reps=5, warm=2):
     return e0.elapsed_time(e1) / reps
 
 
+def merge_row(dev, hy, peaks, comp):
+    """The pair merge on the warm-prompt pool: every layer's segments 2i+1
+    and 2i merged (1500 merges x 32 heads), into a fresh output pool.  Bytes
+    per (merge, head): four 64 KiB inputs read, two written."""
+    import torch
+    W = comp["W"]
+    n_l, n_seg = comp["n_layers"], W.n_seg
+    pairs = [(l * n_seg + 2 * i + 1, l * n_seg + 2 * i) for l in range(n_l) for i in range(n_seg // 2)]
+    later = torch.tensor([a for a, _ in pairs], dtype=torch.int32, device=dev)
+    earlier = torch.tensor([b for _, b in pairs], dtype=torch.int32, device=dev)
+    out = torch.arange(len(pairs), dtype=torch.int32, device=dev)
+    To = torch.empty((len(pairs), W.h_v, W.d_k, W.d_k), device=dev)
+    So = torch.empty((len(pairs), W.h_v, W.d_k, W.d_v), device=dev)
+    ms = _time_ms(lambda: hy.pair_merge(later, earlier, out, comp["T_pool"], comp["S_pool"], To, So,
+                                        variant="gdn"))
+    units = len(pairs) * W.h_v
+    nbytes = units * (4 + 2) * W.d_k * W.d_v * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del To, So
+    torch.cuda.empty_cache()
+    return {"ms": ms, "merges_per_s": units / (ms * 1e-3), "algorithmic_bytes": nbytes,
+            "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"]},
+            "kernel": "tensor-core pair merge (split tf32)"}
+
+
 def measure_rows(dev, hy, peaks):
     """The build rows outside the timed step, each against its own roofline:
     the RetNet-style scalar-decay fast path (8 heads, d = 128, 16 x 512
@@ -313,7 +339,8 @@ def run_profile_case(kind):
     most.  build: GDN, 16 segments x 1024 tokens, h_k = 16, h_v = 32 (512
     (segment, head) pairs); channel: the same shape with per-channel gates;
     compose: 4 GDN layers x 32 heads x 100 segments, w = 8 (12800 pairs,
-    1.7 GB pool)."""
+    1.7 GB pool); merge: that pool's adjacent segment pairs merged (4 x 50
+    merges x 32 heads)."""
     import torch
     import hybrid_linear_attention_chunkwise_gb300 as hy
     import synth_inputs as si
@@ -329,6 +356,17 @@ def run_profile_case(kind):
         run = lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=var, seam_w=W.seam_w,
                                        T_pool=T, S_pool=S, workspace=ws)
         units = W.n_seg * W.h_v
+    elif kind == "merge":
+        comp = setup_compose(dev, hy, n_layers=4)
+        W, n_seg = comp["W"], comp["W"].n_seg
+        pairs = [(l * n_seg + 2 * i + 1, l * n_seg + 2 * i) for l in range(4) for i in range(n_seg // 2)]
+        later = torch.tensor([a for a, _ in pairs], dtype=torch.int32, device=dev)
+        earlier = torch.tensor([b for _, b in pairs], dtype=torch.int32, device=dev)
+        outs = torch.arange(len(pairs), dtype=torch.int32, device=dev)
+        To = torch.empty((len(pairs), W.h_v, W.d_k, W.d_k), device=dev)
+        So = torch.empty_like(To)
+        run = lambda: hy.pair_merge(later, earlier, outs, comp["T_pool"], comp["S_pool"], To, So, variant="gdn")
+        units = len(pairs) * W.h_v
     else:
         comp = setup_compose(dev, hy, n_layers=4)
         sa = comp["sa"]
@@ -415,7 +453,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements after the step")
-    ap.add_argument("--profile", choices=["build", "compose", "channel"], default=None,
+    ap.add_argument("--profile", choices=["build", "compose", "channel", "merge"], default=None,
                     help="run one small case of one kernel (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -542,7 +580,11 @@ def main():
 
     # the other build rows, each against its own roofline (after the timed
     # region; not part of the step)
-    rows = measure_rows(dev, hy, peaks) if (rank == 0 and not args.no_rows) else None
+    rows = None
+    if rank == 0 and not args.no_rows:
+        rows = {f"merge: {comp['n_layers']} layers x {W4.h_v} heads x {W4.n_seg // 2} adjacent segment pairs":
+                merge_row(dev, hy, peaks, comp)}
+        rows.update(measure_rows(dev, hy, peaks))
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
