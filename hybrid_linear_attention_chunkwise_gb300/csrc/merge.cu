@@ -56,22 +56,30 @@ struct MergeArgs {
 
 __device__ __forceinline__ uint32_t trunc_tf32(float x) { return __float_as_uint(x) & 0xFFFFE000u; }
 
-// rows 64 hf .. 64 hf + 63 of column n of the [128 x 128] matrix M (row
-// pitch 128) -> A hi / lo in TMEM (this thread's lane, columns k)
-__device__ __forceinline__ void stage_a(const float *M, int n, int hf, uint32_t ah, uint32_t al) {
-#pragma unroll 1
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
+// rows 64 hf .. 64 hf + 63 of column n of a [128 x 128] matrix (row pitch
+// 128), held in x -> A hi / lo in TMEM (this thread's lane, columns k)
+__device__ __forceinline__ void stage_a(const float (&x)[64], uint32_t ah, uint32_t al) {
+#pragma unroll
   for (int b = 0; b < 4; b++) {
     uint32_t h[16], l[16];
 #pragma unroll
     for (int j = 0; j < 16; j++) {
-      const float x = M[(int64_t)(64 * hf + 16 * b + j) * 128 + n];
-      h[j] = tc::to_tf32(x);
-      l[j] = tc::to_tf32(x - __uint_as_float(h[j]));
+      h[j] = tc::to_tf32(x[16 * b + j]);
+      l[j] = tc::to_tf32(x[16 * b + j] - __uint_as_float(h[j]));
     }
     tc::tmem_st16(ah + 16 * b, h);
     tc::tmem_st16(al + 16 * b, l);
   }
   tc::tmem_wait_st();
+}
+__device__ __forceinline__ void load_col(const float *M, int n, int hf, float (&x)[64]) {
+#pragma unroll
+  for (int j = 0; j < 64; j++) x[j] = M[(int64_t)(64 * hf + j) * 128 + n];
 }
 
 // D (+)= A B with A from TMEM (columns a0.., 128 k) and B the four K-slabs
@@ -121,6 +129,8 @@ __global__ void __launch_bounds__(NT, 1)
     const int64_t pa = ((int64_t)a * p.h_v + h) * 128 * 128, pb = ((int64_t)b * p.h_v + h) * 128 * 128;
     const int64_t po = ((int64_t)o * p.h_v + h) * 128 * 128;
     if (tid == 0) {
+      // S2 (read in the epilogue) into L2 now, and T2 by TMA
+      prefetch_l2(p.S_in + pa, 65536u);
       tc::prefetch_tmap(&tmap_T);
       tc::mbar_expect_tx(&sm.full, 4u * SLAB);
       for (int sl = 0; sl < 4; sl++)
@@ -129,8 +139,15 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t ah = tm + lane_base + TM_AH + 64 * hf, al = tm + lane_base + TM_AL + 64 * hf;
     const uint32_t id = tc::idesc(tc::FMT_TF32, 128, 128);
-    // ---- A = T1^T (hi, lo); B lo from the landed slabs
-    stage_a(p.T_in + pb, n, hf, ah, al);
+    // ---- A = T1^T (hi, lo); S1's column loads in flight meanwhile; B lo
+    // from the landed slabs
+    float s1[64];
+    {
+      float x[64];
+      load_col(p.T_in + pb, n, hf, x);
+      load_col(p.S_in + pb, n, hf, s1);
+      stage_a(x, ah, al);
+    }
     bool ok = tc::mbar_wait(&sm.full, 0, LIM);
     if (!ok) report(p.status, HYPIC_STATUS_TIMEOUT);
     {
@@ -157,28 +174,13 @@ __global__ void __launch_bounds__(NT, 1)
       issue_product(tm + TM_DT, tm + TM_AL, sm.bh, id, true);
       tc::mma_commit(&sm.mma_t);
     }
-    // ---- S1 column into registers while the T product runs, then A = S1^T
-    float s1[64];
-#pragma unroll
-    for (int j = 0; j < 64; j++) s1[j] = p.S_in[pb + (int64_t)(64 * hf + j) * 128 + n];
+    // ---- A = S1^T once the T product has read A
     if (ok && !tc::mbar_wait(&sm.mma_t, 0, DRAIN_LIMIT)) {
       ok = false;
       report(p.status, HYPIC_STATUS_TIMEOUT);
     }
     tc::tc_fence_after();
-#pragma unroll
-    for (int b4 = 0; b4 < 4; b4++) {
-      uint32_t hh[16], ll[16];
-#pragma unroll
-      for (int j = 0; j < 16; j++) {
-        const float x = s1[16 * b4 + j];
-        hh[j] = tc::to_tf32(x);
-        ll[j] = tc::to_tf32(x - __uint_as_float(hh[j]));
-      }
-      tc::tmem_st16(ah + 16 * b4, hh);
-      tc::tmem_st16(al + 16 * b4, ll);
-    }
-    tc::tmem_wait_st();
+    stage_a(s1, ah, al);
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0 && ok) {
