@@ -63,8 +63,8 @@ class MergeDesc(ctypes.Structure):
     _fields_ = [("n_merge", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("variant", ctypes.c_int32),
                 ("later", P), ("earlier", P), ("out", P),
-                ("n_slots_in", ctypes.c_int64), ("n_slots_out", ctypes.c_int64),
-                ("T_in", P), ("S_in", P), ("T_out", P), ("S_out", P), ("status", P)]
+                ("n_slots_a", ctypes.c_int64), ("n_slots_b", ctypes.c_int64), ("n_slots_out", ctypes.c_int64),
+                ("T_a", P), ("S_a", P), ("T_b", P), ("S_b", P), ("T_out", P), ("S_out", P), ("status", P)]
 
 
 SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_workspace_bytes", "hypic_compose",
@@ -280,28 +280,156 @@ def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, 
         raise HypicError(rc, "hypic_compose")
 
 
-def pair_merge(later, earlier, out, T_in, S_in, T_out, S_out, *, variant: str, status=None, stream=None):
+def pair_merge(later, earlier, out, T_a, S_a, T_out, S_out, *, variant: str, T_b=None, S_b=None, status=None,
+               stream=None):
     """hypic_pair_merge on torch tensors: for every merge m and head h,
-    T_out[out[m], h] = T_in[later[m], h] T_in[earlier[m], h] and
-    S_out[out[m], h] = T_in[later[m], h] S_in[earlier[m], h] + S_in[later[m], h].
+    T_out[out[m], h] = T_a[later[m], h] T_b[earlier[m], h] and
+    S_out[out[m], h] = T_a[later[m], h] S_b[earlier[m], h] + S_a[later[m], h].
     later / earlier / out int32 [n_merge] (device); pools as written by
-    segment_build (T layout per variant, S [slots, h_v, d_k, d_v])."""
+    segment_build (T layout per variant, S [slots, h_v, d_k, d_v]); the pool
+    of the earlier pairs defaults to that of the later ones."""
     lib = load()
+    if T_b is None:
+        T_b, S_b = T_a, S_a
     for name, t in (("later", later), ("earlier", earlier), ("out", out)):
         _check(t, name, dtype=torch.int32, ndim=1)
-    _check(S_in, "S_in", dtype=torch.float32, ndim=4)
-    _check(S_out, "S_out", dtype=torch.float32, ndim=4)
+    for name, t in (("S_a", S_a), ("S_b", S_b), ("S_out", S_out)):
+        _check(t, name, dtype=torch.float32, ndim=4)
     d = MergeDesc()
     d.n_merge = later.shape[0]
-    _, d.h_v, d.d_k, d.d_v = S_in.shape
+    _, d.h_v, d.d_k, d.d_v = S_a.shape
     d.variant = VARIANT[variant]
     d.later, d.earlier, d.out = _ptr(later), _ptr(earlier), _ptr(out)
-    d.n_slots_in, d.n_slots_out = S_in.shape[0], S_out.shape[0]
-    d.T_in, d.S_in, d.T_out, d.S_out = _ptr(T_in), _ptr(S_in), _ptr(T_out), _ptr(S_out)
+    d.n_slots_a, d.n_slots_b, d.n_slots_out = S_a.shape[0], S_b.shape[0], S_out.shape[0]
+    d.T_a, d.S_a, d.T_b, d.S_b = _ptr(T_a), _ptr(S_a), _ptr(T_b), _ptr(S_b)
+    d.T_out, d.S_out = _ptr(T_out), _ptr(S_out)
     d.status = _ptr(status)
     rc = lib.hypic_pair_merge(ctypes.byref(d), _stream(stream))
     if rc != OK:
         raise HypicError(rc, "hypic_pair_merge")
+
+
+def compose_span_parallel(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str,
+                          S_out, seam_out=None, S_init=None, n_spans: int = 2):
+    """compose() of every (layer, head) chain split into n_spans contiguous
+    spans of segments, by associativity of the composition rule (the
+    segment parallelism of nav.aitube.vip §2.3 applied to one chain):
+
+      1. each segment's seam window is itself a short span: its pair is built
+         by segment_build over the seam tokens (seam_w = 0);
+      2. each span's pair is the merge, in prompt order, of its segments'
+         seam and cached pairs (pair_merge);
+      3. span s starts from S_s = T_{s-1} S_{s-1} + S(span s-1), S_0 = S_init
+         (an exclusive scan over the span pairs);
+      4. each span runs the ordinary compose from S_s, emitting its seam
+         outputs; the last span's final state is the chain's.
+
+    With one rank per span, steps 1, 2 and 4 need no exchange and step 3 is
+    an all-gather of one pair per (layer, head, span); here the spans run one
+    after another on this GPU.  Variants with per-token gates (all but
+    scalar decay, whose seam padding is not an identity token)."""
+    if variant == "scalar":
+        raise ValueError("compose_span_parallel: scalar decay is not supported")
+    L, n_seg = slot.shape
+    w = 0 if seam_k is None else seam_k.shape[2]
+    _, h_v, d_k, d_v = S_out.shape
+    h_k = seam_k.shape[3] if seam_k is not None else h_v
+    dev = S_out.device
+    n_spans = max(1, min(int(n_spans), n_seg))
+    bounds = np.linspace(0, n_seg, n_spans + 1).round().astype(np.int64)
+    slot_h = slot.detach().cpu().numpy()
+    i32 = lambda x: torch.as_tensor(np.asarray(x, dtype=np.int32), device=dev)
+    # 1. seam-window pairs, slot l * n_seg + i
+    T_sw = S_sw = None
+    if w > 0:
+        T_sw = torch.empty(pool_T_shape(variant, L * n_seg, h_v, d_k), device=dev)
+        S_sw = torch.empty((L * n_seg, h_v, d_k, d_v), device=dev)
+        offs = np.arange(0, n_seg * w + 1, w, dtype=np.int64)
+        for l in range(L):
+            kk = seam_k[l].reshape(n_seg * w, h_k, d_k)
+            vv = seam_v[l].reshape(n_seg * w, h_v, d_v)
+            gg = None if seam_g is None else seam_g[l].reshape((n_seg * w,) + tuple(seam_g.shape[3:]))
+            bb = None if seam_beta is None else seam_beta[l].reshape(n_seg * w, h_v)
+            segment_build(kk, vv, gg, bb, offs, variant=variant, seam_w=0, T_pool=T_sw, S_pool=S_sw,
+                          slot_of_seg=np.arange(n_seg, dtype=np.int32) + l * n_seg)
+    # 2. span pairs by sequential merges, batched over (layer, span); the
+    # accumulator ping-pongs between two pools, slot l * n_spans + s
+    n_acc = L * n_spans
+    acc_T = [torch.empty(pool_T_shape(variant, n_acc, h_v, d_k), device=dev) for _ in range(2)]
+    acc_S = [torch.empty((n_acc, h_v, d_k, d_v), device=dev) for _ in range(2)]
+    # elements of span s in order: (kind, segment) with kind 0 = seam, 1 = body
+    elems = [[(k, i) for i in range(bounds[s], bounds[s + 1]) for k in ((0, 1) if w > 0 else (1,))]
+             for s in range(n_spans)]
+    cur = 0
+    first = True
+    # a span of a single element: its pair is that element's
+    for l in range(L):
+        for s in range(n_spans):
+            if len(elems[s]) == 1:
+                k0, i0 = elems[s][0]
+                src_T, src_S = (T_sw, S_sw) if k0 == 0 else (T_pool, S_pool)
+                j = l * n_seg + i0 if k0 == 0 else int(slot_h[l, i0])
+                acc_T[cur][l * n_spans + s] = src_T[j]
+                acc_S[cur][l * n_spans + s] = src_S[j]
+    for step in range(max(len(e) for e in elems) - 1):
+        later, earlier, out, done = [], [], [], []
+        kinds = set()
+        for l in range(L):
+            for s in range(n_spans):
+                e = elems[s]
+                if step + 1 >= len(e):
+                    done.append(l * n_spans + s)  # finished: carried over below
+                    continue
+                kind, i = e[step + 1]
+                kinds.add(kind)
+                later.append(l * n_seg + i if kind == 0 else slot_h[l, i])
+                if first:
+                    k0, i0 = e[0]
+                    earlier.append(l * n_seg + i0 if k0 == 0 else slot_h[l, i0])
+                else:
+                    earlier.append(l * n_spans + s)
+                out.append(l * n_spans + s)
+        assert len(kinds) == 1  # every span steps through seam, body, seam, ... in lockstep
+        kind = kinds.pop()
+        Ta, Sa = (T_sw, S_sw) if kind == 0 else (T_pool, S_pool)
+        if first:
+            k0 = elems[0][0][0]
+            Tb, Sb = (T_sw, S_sw) if k0 == 0 else (T_pool, S_pool)
+        else:
+            Tb, Sb = acc_T[cur], acc_S[cur]
+        pair_merge(i32(later), i32(earlier), i32(out), Ta, Sa, acc_T[cur ^ 1], acc_S[cur ^ 1], variant=variant,
+                   T_b=Tb, S_b=Sb)
+        if done:  # spans that are complete keep their pair in the new buffer
+            idx = torch.as_tensor(done, device=dev)
+            acc_T[cur ^ 1][idx] = acc_T[cur][idx]
+            acc_S[cur ^ 1][idx] = acc_S[cur][idx]
+        cur ^= 1
+        first = False
+    span_T, span_S = acc_T[cur], acc_S[cur]
+    # 3. exclusive scan: S_s = T_{s-1} S_{s-1} + S(span s-1), as merges whose
+    # earlier operand is the state (its T half unused)
+    state = torch.zeros((L * n_spans, h_v, d_k, d_v), device=dev) if S_init is None else \
+        S_init.repeat_interleave(n_spans, dim=0).contiguous()
+    state_T = torch.zeros(pool_T_shape(variant, L * n_spans, h_v, d_k), device=dev)
+    scratch_T = torch.empty_like(state_T)
+    for s in range(1, n_spans):
+        later = [l * n_spans + s - 1 for l in range(L)]
+        earlier = later
+        out = [l * n_spans + s for l in range(L)]
+        pair_merge(i32(later), i32(earlier), i32(out), span_T, span_S, scratch_T, state, variant=variant,
+                   T_b=state_T, S_b=state)
+    # 4. each span's compose from its start state
+    for s in range(n_spans):
+        a, b = int(bounds[s]), int(bounds[s + 1])
+        sl = lambda x: None if x is None else x[:, a:b].contiguous()
+        so = None if seam_out is None else torch.empty_like(seam_out[:, a:b])
+        Si = state.reshape(L, n_spans, h_v, d_k, d_v)[:, s].contiguous()
+        Sf = S_out if s == n_spans - 1 else torch.empty_like(S_out)
+        sg = seam_g if (seam_g is not None and variant == "scalar") else sl(seam_g)
+        compose(slot[:, a:b].contiguous(), T_pool, S_pool, sl(seam_k), sl(seam_v), sl(seam_q), sg, sl(seam_beta),
+                variant=variant, S_out=Sf, seam_out=so, S_init=Si, h_k=h_k, d_k=d_k, d_v=d_v)
+        if so is not None:
+            seam_out[:, a:b] = so
 
 
 def plan_lpt(costs, n_workers: int):

@@ -302,14 +302,14 @@ int hypic_pair_merge(const hypic_merge_desc *d, hypic_stream_t stream) {
   if (d->n_merge < 0 || d->h_v < 1 || d->d_k < 1 || d->d_v < 1) return HYPIC_ERR_INVALID_ARG;
   if (d->variant < HYPIC_GDN || d->variant > HYPIC_DIAG_GATE) return HYPIC_ERR_INVALID_ARG;
   if (d->d_k > 128 || d->d_v > 128) return HYPIC_ERR_UNSUPPORTED;
-  if (d->n_slots_in < 0 || d->n_slots_out < 0) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_slots_a < 0 || d->n_slots_b < 0 || d->n_slots_out < 0) return HYPIC_ERR_INVALID_ARG;
   if ((int64_t)d->n_merge * d->h_v > INT32_MAX) return HYPIC_ERR_UNSUPPORTED;
   if (d->n_merge == 0) return HYPIC_OK;
   if (!d->later || !d->earlier || !d->out || !aligned(d->later, 4) || !aligned(d->earlier, 4) || !aligned(d->out, 4))
     return HYPIC_ERR_INVALID_ARG;
-  if (!d->T_in || !d->S_in || !d->T_out || !d->S_out) return HYPIC_ERR_INVALID_ARG;
-  if (!aligned(d->T_in, 4) || !aligned(d->S_in, 4) || !aligned(d->T_out, 4) || !aligned(d->S_out, 4))
-    return HYPIC_ERR_INVALID_ARG;
+  const float *pools[6] = {d->T_a, d->S_a, d->T_b, d->S_b, d->T_out, d->S_out};
+  for (const float *q : pools)
+    if (!q || !aligned(q, 4)) return HYPIC_ERR_INVALID_ARG;
   MergeParams p{};
   p.n_merge = d->n_merge;
   p.h_v = d->h_v;
@@ -319,10 +319,13 @@ int hypic_pair_merge(const hypic_merge_desc *d, hypic_stream_t stream) {
   p.later = d->later;
   p.earlier = d->earlier;
   p.out = d->out;
-  p.n_slots_in = d->n_slots_in;
+  p.n_slots_a = d->n_slots_a;
+  p.n_slots_b = d->n_slots_b;
   p.n_slots_out = d->n_slots_out;
-  p.T_in = d->T_in;
-  p.S_in = d->S_in;
+  p.T_a = d->T_a;
+  p.S_a = d->S_a;
+  p.T_b = d->T_b;
+  p.S_b = d->S_b;
   p.T_out = d->T_out;
   p.S_out = d->S_out;
   p.status = d->status;

@@ -60,8 +60,9 @@ struct ComposeParams {
 struct MergeParams {
   int32_t n_merge, h_v, d_k, d_v, variant;
   const int32_t *later, *earlier, *out;
-  int64_t n_slots_in, n_slots_out;
-  const float *T_in, *S_in;
+  int64_t n_slots_a, n_slots_b, n_slots_out;
+  const float *T_a, *S_a;  // later pairs
+  const float *T_b, *S_b;  // earlier pairs
   float *T_out, *S_out;
   uint32_t *status;
 };

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(NT, 1)
     tc::mbar_init(&sm.mma_t, 1);
     tc::mbar_init(&sm.mma_s, 1);
     const int a = p.later[m], b = p.earlier[m], o = p.out[m];
-    const bool bad = a < 0 || a >= p.n_slots_in || b < 0 || b >= p.n_slots_in || o < 0 || o >= p.n_slots_out;
+    const bool bad = a < 0 || a >= p.n_slots_a || b < 0 || b >= p.n_slots_b || o < 0 || o >= p.n_slots_out;
     sm.skip = bad ? 1 : 0;
     if (bad) report(p.status, HYPIC_STATUS_BAD_SLOT);
     tc::fence_mbar_init();
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int64_t po = ((int64_t)o * p.h_v + h) * 128 * 128;
     if (tid == 0) {
       // S2 (read in the epilogue) into L2 now, and T2 by TMA
-      prefetch_l2(p.S_in + pa, 65536u);
+      prefetch_l2(p.S_a + pa, 65536u);
       tc::prefetch_tmap(&tmap_T);
       tc::mbar_expect_tx(&sm.full, 4u * SLAB);
       for (int sl = 0; sl < 4; sl++)
@@ -144,8 +144,8 @@ __global__ void __launch_bounds__(NT, 1)
     float s1[64];
     {
       float x[64];
-      load_col(p.T_in + pb, n, hf, x);
-      load_col(p.S_in + pb, n, hf, s1);
+      load_col(p.T_b + pb, n, hf, x);
+      load_col(p.S_b + pb, n, hf, s1);
       stage_a(x, ah, al);
     }
     bool ok = tc::mbar_wait(&sm.full, 0, LIM);
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(NT, 1)
     // ---- T_out column n, rows 64 hf .. (lane n of D_T, columns = rows r)
     const uint32_t dt = tm + lane_base + TM_DT + 64 * hf, ds = tm + lane_base + TM_DS + 64 * hf;
     float *To = p.T_out + po + n, *So = p.S_out + po + n;
-    const float *S2 = p.S_in + pa + n;
+    const float *S2 = p.S_a + pa + n;
 #pragma unroll 1
     for (int b4 = 0; b4 < 4; b4++) {
       uint32_t r[16];
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(256) merge_simt_kernel(const MergeParams p) {
   __shared__ float t2[DMAX * DMAX / 2];  // dense T2 in two row halves (32 KiB)
   const int m = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
   const int a = p.later[m], b = p.earlier[m], o = p.out[m];
-  if (a < 0 || a >= p.n_slots_in || b < 0 || b >= p.n_slots_in || o < 0 || o >= p.n_slots_out) {
+  if (a < 0 || a >= p.n_slots_a || b < 0 || b >= p.n_slots_b || o < 0 || o >= p.n_slots_out) {
     if (threadIdx.x == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
     return;
   }
@@ -249,11 +249,11 @@ __global__ void __launch_bounds__(256) merge_simt_kernel(const MergeParams p) {
     float x[DMAX];
 #pragma unroll 1
     for (int k = 0; k < dk; k++)
-      x[k] = active ? (c < dk ? p.T_in[tb + (int64_t)k * dk + c] : p.S_in[sb + (int64_t)k * dv + (c - dk)]) : 0.f;
+      x[k] = active ? (c < dk ? p.T_b[tb + (int64_t)k * dk + c] : p.S_b[sb + (int64_t)k * dv + (c - dk)]) : 0.f;
     for (int half = 0; half < 2; half++) {
       const int r0 = half * ((dk + 1) / 2), r1 = half ? dk : (dk + 1) / 2;
       __syncthreads();
-      for (int e = threadIdx.x; e < (r1 - r0) * dk; e += blockDim.x) t2[e] = p.T_in[ta + (int64_t)r0 * dk + e];
+      for (int e = threadIdx.x; e < (r1 - r0) * dk; e += blockDim.x) t2[e] = p.T_a[ta + (int64_t)r0 * dk + e];
       __syncthreads();
       if (active) {
         for (int r = r0; r < r1; r++) {
@@ -261,21 +261,21 @@ __global__ void __launch_bounds__(256) merge_simt_kernel(const MergeParams p) {
           float acc = 0.f;
           for (int k = 0; k < dk; k++) acc = fmaf(row[k], x[k], acc);
           if (c < dk) p.T_out[to + (int64_t)r * dk + c] = acc;
-          else p.S_out[so + (int64_t)r * dv + (c - dk)] = acc + p.S_in[sa + (int64_t)r * dv + (c - dk)];
+          else p.S_out[so + (int64_t)r * dv + (c - dk)] = acc + p.S_a[sa + (int64_t)r * dv + (c - dk)];
         }
       }
     }
   } else if (is_vector_gate(p.variant)) {  // diagonal
     const int64_t ta = ((int64_t)a * p.h_v + h) * dk, tb = ((int64_t)b * p.h_v + h) * dk;
     const int64_t to = ((int64_t)o * p.h_v + h) * dk;
-    for (int r = threadIdx.x; r < dk; r += blockDim.x) p.T_out[to + r] = p.T_in[ta + r] * p.T_in[tb + r];
+    for (int r = threadIdx.x; r < dk; r += blockDim.x) p.T_out[to + r] = p.T_a[ta + r] * p.T_b[tb + r];
     for (int e = threadIdx.x; e < dk * dv; e += blockDim.x)
-      p.S_out[so + e] = fmaf(p.T_in[ta + e / dv], p.S_in[sb + e], p.S_in[sa + e]);
+      p.S_out[so + e] = fmaf(p.T_a[ta + e / dv], p.S_b[sb + e], p.S_a[sa + e]);
   } else {  // scalar
     const int64_t ta = (int64_t)a * p.h_v + h, tb = (int64_t)b * p.h_v + h, to = (int64_t)o * p.h_v + h;
-    const float t = p.T_in[ta];
-    if (threadIdx.x == 0) p.T_out[to] = t * p.T_in[tb];
-    for (int e = threadIdx.x; e < dk * dv; e += blockDim.x) p.S_out[so + e] = fmaf(t, p.S_in[sb + e], p.S_in[sa + e]);
+    const float t = p.T_a[ta];
+    if (threadIdx.x == 0) p.T_out[to] = t * p.T_b[tb];
+    for (int e = threadIdx.x; e < dk * dv; e += blockDim.x) p.S_out[so + e] = fmaf(t, p.S_b[sb + e], p.S_a[sa + e]);
   }
 }
 
@@ -283,7 +283,8 @@ __global__ void __launch_bounds__(256) merge_simt_kernel(const MergeParams p) {
 
 bool merge_tc_supported(const MergeParams &p) {
   auto a16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
-  return is_dense_T(p.variant) && p.d_k == 128 && p.d_v == 128 && a16(p.T_in) && a16(p.S_in);
+  return is_dense_T(p.variant) && p.d_k == 128 && p.d_v == 128 && a16(p.T_a) && a16(p.S_a) && a16(p.T_b) &&
+         a16(p.S_b);
 }
 
 cudaError_t launch_merge(const MergeParams &p, uint32_t wait_limit, cudaStream_t s) {
@@ -291,7 +292,7 @@ cudaError_t launch_merge(const MergeParams &p, uint32_t wait_limit, cudaStream_t
   if (grid < 1) return cudaSuccess;
   if (merge_tc_supported(p)) {
     CUtensorMap tmap;
-    if (!make_tmap_f32_rows(&tmap, p.T_in, (uint64_t)p.n_slots_in * p.h_v * 128, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_f32_rows(&tmap, p.T_a, (uint64_t)p.n_slots_a * p.h_v * 128, 128)) return cudaErrorInvalidValue;
     const size_t smem = sizeof(MergeSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(merge_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

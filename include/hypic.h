@@ -201,20 +201,21 @@ int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream);
  * with the transition of the joined span T(C1.C2) = T(C2) T(C1)):
  *   for each merge m and value head h, with a = later[m], b = earlier[m],
  *   o = out[m] (pool slots):
- *     T_out[o, h] = T_in[a, h] T_in[b, h]
- *     S_out[o, h] = T_in[a, h] S_in[b, h] + S_in[a, h]
- * The merge is associative, so repeated merges build the pair of any run of
- * consecutive segments (a tree of merges composes a chain in log depth).
+ *     T_out[o, h] = T_a[a, h] T_b[b, h]
+ *     S_out[o, h] = T_a[a, h] S_b[b, h] + S_a[a, h]
+ * The later pairs come from pool (T_a, S_a), the earlier ones from pool
+ * (T_b, S_b); the two may be the same pool.  The merge is associative, so
+ * repeated merges build the pair of any run of consecutive spans (a tree of
+ * merges composes a chain in log depth).
  * T layouts follow the variant as in hypic_segment_build: dense
  * [slots, h_v, d_k, d_k] for GDN / DELTANET / CHANNEL_DELTA (matrix
  * product), [slots, h_v] for SCALAR_DECAY / UNGATED (scalar product),
  * [slots, h_v, d_k] for DIAG_GATE (elementwise product; S rows scaled).
  * S pools are [slots, h_v, d_k, d_v].  All fp32.
- * Slots index the input pools (n_slots_in) and the output pools
- * (n_slots_out); a merge with a slot out of range is skipped and reported
- * (HYPIC_STATUS_BAD_SLOT).  Output slots must be distinct, and when the
- * output pools alias the input pools no output slot of a call may be an
- * input slot of the same call (results are undefined otherwise).
+ * A merge with a slot out of range of its pool (n_slots_a, n_slots_b,
+ * n_slots_out) is skipped and reported (HYPIC_STATUS_BAD_SLOT).  Output
+ * slots must be distinct, and no output slot of a call may alias an input
+ * slot of the same call (results are undefined otherwise).
  * Dense d_k = d_v = 128 runs on the tensor cores with split tf32 operands
  * (about fp32 accuracy); other shapes and the scalar / diagonal forms run on
  * the CUDA cores in fp32.
@@ -223,12 +224,13 @@ typedef struct {
   int32_t n_merge;
   int32_t h_v, d_k, d_v;
   int32_t variant;
-  const int32_t *later;       /* [dev] [n_merge] slot of the later pair (T2, S2) */
-  const int32_t *earlier;     /* [dev] [n_merge] slot of the earlier pair (T1, S1) */
+  const int32_t *later;       /* [dev] [n_merge] slot of the later pair (T2, S2) in pool a */
+  const int32_t *earlier;     /* [dev] [n_merge] slot of the earlier pair (T1, S1) in pool b */
   const int32_t *out;         /* [dev] [n_merge] output slot */
-  int64_t n_slots_in, n_slots_out;
-  const float *T_in, *S_in;   /* [dev] input pools */
-  float *T_out, *S_out;       /* [dev] output pools (may be the input pools, see above) */
+  int64_t n_slots_a, n_slots_b, n_slots_out;
+  const float *T_a, *S_a;     /* [dev] pool of the later pairs */
+  const float *T_b, *S_b;     /* [dev] pool of the earlier pairs */
+  float *T_out, *S_out;       /* [dev] output pool */
   uint32_t *status;           /* [dev] optional */
 } hypic_merge_desc;
 

@@ -144,3 +144,31 @@ def test_compose_tc_long_chain(variant):
                           np.transpose(seam, (0, 3, 1, 2, 4)).reshape(1, W.h_v, -1), inner=1).max()
     print(f"{variant} 100-segment chain: state {e1:.2e}, seam outputs {e2:.2e}")
     assert e1 <= TOL_BF16 and e2 <= TOL_BF16, (e1, e2)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "channel"])
+@pytest.mark.parametrize("w,n_spans", [(8, 2), (8, 3), (3, 5), (0, 4)])
+def test_compose_span_parallel(variant, w, n_spans):
+    """Segment parallelism on one chain: seam-window pairs built, each span's
+    pair merged, the span start states scanned, each span composed from its
+    start state.  Equals the oracle composition (final state and every seam
+    output) to the bf16 bar, like the one-pass compose."""
+    lens = [40, 130, 12, 64, 300, 25, 90]
+    W = si.workload(5, device=DEV, variant=variant, lengths=lens, h_k=2, h_v=4, seam_w=w, n_layers=2)
+    S_init = si.random_state((2, W.h_v, 128, 128), seed=1, cfg=5, device=DEV)
+    pools = [gpu_build(W, layer=l) for l in range(2)]
+    T_pool = torch.cat([p[0] for p in pools])
+    S_pool = torch.cat([p[1] for p in pools])
+    sa = seam_arrays(W, range(2))
+    slot = torch.arange(2 * W.n_seg, dtype=torch.int32, device=DEV).reshape(2, W.n_seg)
+    S_out = torch.empty((2, W.h_v, 128, 128), device=DEV)
+    seam_out = torch.zeros((2, W.n_seg, w, W.h_v, 128), device=DEV) if w else None
+    hy.compose_span_parallel(slot, T_pool, S_pool, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"],
+                             variant=variant, S_out=S_out, seam_out=seam_out, S_init=S_init, n_spans=n_spans)
+    torch.cuda.synchronize()
+    So, seam = _oracle_compose(W, T_pool, S_pool, sa, slot, S_init, 2)
+    assert per_head_rel_err(S_out, So).max() <= TOL_BF16
+    if w:
+        e = per_head_rel_err(seam_out.permute(0, 3, 1, 2, 4).reshape(2, W.h_v, -1),
+                             np.transpose(seam, (0, 3, 1, 2, 4)).reshape(2, W.h_v, -1), inner=1)
+        assert e.max() <= TOL_BF16, e.max()

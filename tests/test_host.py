@@ -175,19 +175,19 @@ def test_merge_rejects_bad_descriptors():
     def desc(**over):
         d = hy.MergeDesc()
         d.n_merge, d.h_v, d.d_k, d.d_v, d.variant = 2, 4, 128, 128, hy.GDN
-        d.later = d.earlier = d.out = d.T_in = d.S_in = d.T_out = d.S_out = fake
-        d.n_slots_in, d.n_slots_out = 4, 2
+        d.later = d.earlier = d.out = d.T_a = d.S_a = d.T_b = d.S_b = d.T_out = d.S_out = fake
+        d.n_slots_a, d.n_slots_b, d.n_slots_out = 4, 4, 2
         for k, v in over.items():
             setattr(d, k, v)
         return d
     for over, want in [(dict(n_merge=-1), 1), (dict(later=None), 1), (dict(out=None), 1),
-                       (dict(T_out=None), 1), (dict(S_in=None), 1), (dict(d_k=200), 2), (dict(variant=9), 1),
-                       (dict(h_v=0), 1), (dict(n_slots_in=-1), 1),
+                       (dict(T_out=None), 1), (dict(S_a=None), 1), (dict(T_b=None), 1), (dict(d_k=200), 2), (dict(variant=9), 1),
+                       (dict(h_v=0), 1), (dict(n_slots_a=-1), 1), (dict(n_slots_b=-1), 1),
                        (dict(earlier=ctypes.c_void_p((1 << 20) + 2)), 1),
                        (dict(S_out=ctypes.c_void_p((1 << 20) + 1)), 1)]:
         assert lib.hypic_pair_merge(ctypes.byref(desc(**over)), None) == want, over
     # nothing to do: accepted without touching any pointer
-    assert lib.hypic_pair_merge(ctypes.byref(desc(n_merge=0, later=None, T_in=None)), None) == 0
+    assert lib.hypic_pair_merge(ctypes.byref(desc(n_merge=0, later=None, T_a=None)), None) == 0
 
 
 def test_binding_refuses_host_tensors():
