@@ -89,3 +89,75 @@ def test_two_rank_sharded_build_equals_single_process(tmp_path):
     T, S = oracle.build_pairs("gdn", W.seg_offsets, W.seam_w, 1, 2, 16, 16, L.k, L.v, L.g, L.beta)
     assert np.array_equal(np.load(tmp_path / "T.npy"), np.asarray(T))
     assert np.array_equal(np.load(tmp_path / "S.npy"), np.asarray(S))
+
+
+def _span_rank_main(rank, world, port, lens, w, out_dir):
+    """Segment parallelism on one chain, one span per rank: each rank forms
+    its span's pair from its segments' seam-window and cached pairs, the
+    span pairs are exchanged by all-gather (the one collective), each rank
+    takes its start state from the exclusive scan and composes its span
+    (the fp64 oracle stands in for each rank's GPU)."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        W = si.workload(5, seed=3, device="cpu", variant="deltanet", lengths=lens, h_k=1, h_v=2, d=16,
+                        seam_w=w, dtype=torch.float32)
+        L = W.layers[0]
+        sa = si.seam_gather(W, L)
+        n_seg = W.n_seg
+        bounds = np.linspace(0, n_seg, world + 1).round().astype(int)
+        a, b = int(bounds[rank]), int(bounds[rank + 1])
+        # cached pairs of my segments' bodies
+        idx = np.concatenate([np.arange(W.seg_offsets[i], W.seg_offsets[i + 1]) for i in range(a, b)])
+        Tb, Sb = oracle.build_pairs("deltanet", si.offsets_from_lengths([lens[i] for i in range(a, b)]), w,
+                                    1, 2, 16, 16, L.k[idx], L.v[idx], None, L.beta[idx])
+        # pairs of my segments' seam windows (each window a body of w tokens)
+        n = b - a
+        Tw, Sw = oracle.build_pairs("deltanet", np.arange(0, n * w + 1, w), 0, 1, 2, 16, 16,
+                                    sa["k"][a:b].reshape(n * w, 1, 16), sa["v"][a:b].reshape(n * w, 2, 16), None,
+                                    sa["beta"][a:b].reshape(n * w, 2))
+        # my span's pair: seam, body, seam, body, ... merged in prompt order
+        accT, accS = np.asarray(Tw[0]), np.asarray(Sw[0])
+        for j in range(n):
+            if j > 0:
+                accT, accS = oracle.merge(Tw[j], Sw[j], accT, accS)
+            accT, accS = oracle.merge(Tb[j], Sb[j], accT, accS)
+        # exclusive scan over the ranks' span pairs
+        mine = torch.from_numpy(np.stack([accT, accS]))
+        allp = [torch.empty_like(mine) for _ in range(world)]
+        dist.all_gather(allp, mine)
+        S0 = si.random_state((1, 2, 16, 16), seed=0, cfg=5).double().numpy()[0]
+        state = S0
+        for r in range(rank):
+            Tr, Sr = allp[r][0].numpy(), allp[r][1].numpy()
+            state = np.einsum("hij,hjk->hik", Tr, state) + Sr
+        Sf, outs = oracle.compose("deltanet", Tb[None], Sb[None], sa["k"][None, a:b], sa["v"][None, a:b],
+                                  sa["q"][None, a:b], None, sa["beta"][None, a:b], 1, 2, S_init=state[None])
+        got = [None] * world
+        dist.all_gather_object(got, (np.asarray(Sf), np.asarray(outs)))
+        if rank == 0:
+            np.save(os.path.join(out_dir, "S_final.npy"), got[-1][0])
+            np.save(os.path.join(out_dir, "outs.npy"), np.concatenate([g[1] for g in got], axis=1))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_span_parallel_compose_equals_single_chain(tmp_path):
+    lens = [130, 64, 200, 9, 77, 300, 40]
+    w = 4
+    port = _free_port()
+    mp.start_processes(_span_rank_main, args=(2, port, lens, w, str(tmp_path)), nprocs=2, join=True,
+                       start_method="spawn")
+    W = si.workload(5, seed=3, device="cpu", variant="deltanet", lengths=lens, h_k=1, h_v=2, d=16, seam_w=w,
+                    dtype=torch.float32)
+    L = W.layers[0]
+    sa = si.seam_gather(W, L)
+    T, S = oracle.build_pairs("deltanet", W.seg_offsets, w, 1, 2, 16, 16, L.k, L.v, None, L.beta)
+    S0 = si.random_state((1, 2, 16, 16), seed=0, cfg=5).double().numpy()
+    Sf, outs = oracle.compose("deltanet", np.asarray(T)[None], np.asarray(S)[None], sa["k"][None], sa["v"][None],
+                              sa["q"][None], None, sa["beta"][None], 1, 2, S_init=S0)
+    got_S = np.load(tmp_path / "S_final.npy")
+    got_o = np.load(tmp_path / "outs.npy")
+    assert np.abs(got_S - np.asarray(Sf)).max() <= 1e-9 * max(1.0, np.abs(Sf).max())
+    valid = sa["valid"].numpy()
+    assert np.abs(got_o[0][valid] - np.asarray(outs)[0][valid]).max() <= 1e-9 * max(1.0, np.abs(outs).max())
