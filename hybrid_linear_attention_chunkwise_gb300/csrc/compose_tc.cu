@@ -2,28 +2,34 @@
 // variants (GDN, DeltaNet, per-channel delta) with bf16 seam tokens and
 // d_k = d_v = 128: the bandwidth-bound left-multiply-add S <- T_C S + S(C|0)
 // of the HYPIC news pages (nav.aitube.vip §2.1), with the seam-window advance
-// and per-token outputs of §2.2.
+// and per-token outputs of §2.2.  Two kernels share the pair streaming:
+//   compose_channel_kernel   per-channel gates: the seam tokens one by one on
+//                            the CUDA cores (below);
+//   compose_seam_mma_kernel  scalar gates: the seam tokens in groups of eight
+//                            on the tensor cores (further down).
 //
-// One CTA of 128 threads per (layer, value head) chain, two CTAs per SM.
-// Thread n owns column n of the running state S (128 fp32 registers).  Per
-// segment, in prompt order:
-//   seam  the seam tokens update S in place (local dot product k^T S[:,n],
-//         rank-1 update) and emit o_t[n] = q_t . S[:,n];
+// Per-channel kernel: one CTA of 256 threads per (layer, value head) chain,
+// two CTAs per SM.  Threads n and n + 128 own rows 0..63 and 64..127 of
+// column n of the running state S (64 fp32 registers each).  Per segment, in
+// prompt order:
+//   seam  each seam token scales S by its gates (S <- Diag(a) S), forms the
+//         half-column dot product k^T S[:,n], exchanges it with its partner
+//         through shared memory (one CTA barrier per token), applies the
+//         rank-1 update and emits o_t[n] = q_t . S[:,n] (partner sums are
+//         written out after the next barrier);
 //   MMA   S is rounded to tf32 and stored to TMEM as the A operand (lane n =
-//         S[:,n]^T); thread 0 issues D = S^T T_C^T (M = N = K = 128,
-//         kind::tf32) from TMEM A and a shared-memory B operand, so lane n of
-//         D is column n of T_C S;
-//   add   each thread adds column n of S(C|0), read from global memory.
+//         S[:,n]^T, columns 64 h .. 64 h + 63 from thread half h); thread 0
+//         issues D = S^T T_C^T (M = N = K = 128, kind::tf32) from TMEM A and
+//         a shared-memory B operand, so lane n of D is column n of T_C S;
+//   add   each thread adds its 64 rows of column n of S(C|0), loaded from
+//         global memory (warmed in L2 a segment ahead) while the MMA runs.
 // Data movement, all issued by thread 0 at the moment the consumer frees the
-// space (no producer warp: four warps per CTA leave each thread the full
-// register file it needs for its 128-value column):
+// space:
 //   T_C   four 16 KiB K-slabs per pair (TMA 2-D tiles, 128-byte swizzle = the
 //         K-major MMA operand layout) through a ring of NSLOT slots; the slots
 //         of a pair are refilled as soon as its MMAs complete;
-//   S(C|0) prefetched into L2 one segment ahead (bulk prefetch), then read
-//         with coalesced loads, 32 rows at a time, one chunk ahead;
-//   seam  k/q/v rows and the gate block of each group of SB tokens by bulk
-//         copies into one of two seam buffers.
+//   seam  k/q/v rows, gate rows and the beta block of each group of SB tokens
+//         by bulk copies into one of two seam buffers.
 // Each pool byte crosses HBM once: 128 KiB per (segment, head) pair.
 //
 // Every wait is bounded: one that runs out sets HYPIC_STATUS_TIMEOUT; the CTA
@@ -45,7 +51,7 @@ namespace {
 constexpr int NSLOT = 5;   // T_C K-slab ring (16 KiB each)
 constexpr int SLAB = 16384;
 constexpr int SB = 8;      // seam tokens per seam buffer
-constexpr int NT = 128;    // threads per CTA
+constexpr int NT = 256;    // threads per CTA (per-channel kernel): two per state column
 constexpr int MAX_HV = 128;
 constexpr uint32_t DRAIN_LIMIT = 1u << 22;
 
@@ -53,16 +59,15 @@ struct SeamBuf {
   __nv_bfloat16 k[SB][128];
   __nv_bfloat16 q[SB][128];
   __nv_bfloat16 v[SB][128];
-  union {
-    float gv[SB][128];       // per-channel log-gates of this head (channel variant)
-    float g[SB * MAX_HV];    // scalar log-gates of every head (GDN)
-  };
-  float b[SB * MAX_HV];      // beta of every head
+  float gv[SB][128];         // per-channel log-gates of this head, then a = e^g
+  float b[SB];               // beta of this head (plain loads, warmed in L2)
 };
 
 struct __align__(1024) ComposeTcSmem {
   unsigned char slot[NSLOT][SLAB];  // 1024-aligned: swizzled TMA tiles
   SeamBuf seam[2];
+  float xs[2][2][128];  // partial k^T S of the two halves, by token parity
+  float os[2][128];     // partial q^T S of the upper half, by token parity
   uint64_t full[NSLOT];
   uint64_t seam_full[2];
   uint64_t mma_done;
@@ -71,6 +76,8 @@ struct __align__(1024) ComposeTcSmem {
   int abort;
   int stop;
 };
+static_assert(sizeof(SeamBuf) % 16 == 0, "bulk-copy destinations must stay 16-byte aligned");
+static_assert(2 * (sizeof(ComposeTcSmem) + 2048) <= 228 * 1024, "two chains per SM");
 
 struct TcArgs {
   ComposeParams p;
@@ -125,9 +132,8 @@ __device__ __forceinline__ void issue_slab(SM &sm, const ComposeParams &p, const
   tc::tma_load_2d(sm.slot[si], tmap, 32 * j, (int32_t)(((int64_t)slot * p.h_v + c.h) * 128), &sm.full[si]);
 }
 
-// VEC: per-channel gate rows; GDN: scalar gate block; neither (DeltaNet): no
-// gates at all (seam_g is NULL then and must not be touched)
-template <bool VEC, bool GDN>
+// k / q / v rows and per-channel gate rows of seam group gq into seam buffer
+// gq % 2; its beta block (all heads, contiguous) is warmed in L2 (thread 0)
 __device__ __forceinline__ void issue_seam(ComposeTcSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
   if (gq >= c.n_seg * c.groups) return;
   const int seg = gq / c.groups, gi = gq % c.groups;
@@ -137,8 +143,7 @@ __device__ __forceinline__ void issue_seam(ComposeTcSmem &sm, const ComposeParam
   const int nt = min(SB, c.w - t0);
   const int64_t tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + t0;
   const uint32_t gbytes = (uint32_t)(nt * p.h_v * 4);
-  const uint32_t bytes = (uint32_t)nt * 3 * 256 + gbytes + (VEC ? (uint32_t)nt * 512 : 0) + (GDN ? gbytes : 0);
-  tc::mbar_expect_tx(&sm.seam_full[b], bytes);
+  tc::mbar_expect_tx(&sm.seam_full[b], (uint32_t)nt * (3 * 256 + 512));
   const __nv_bfloat16 *sk = static_cast<const __nv_bfloat16 *>(p.seam_k);
   const __nv_bfloat16 *sqp = static_cast<const __nv_bfloat16 *>(p.seam_q);
   const __nv_bfloat16 *sv = static_cast<const __nv_bfloat16 *>(p.seam_v);
@@ -146,10 +151,9 @@ __device__ __forceinline__ void issue_seam(ComposeTcSmem &sm, const ComposeParam
     tc::bulk_load(s.k[t], sk + ((tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.seam_full[b]);
     tc::bulk_load(s.q[t], sqp + ((tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.seam_full[b]);
     tc::bulk_load(s.v[t], sv + ((tok0 + t) * p.h_v + c.h) * 128, 256, &sm.seam_full[b]);
-    if (VEC) tc::bulk_load(s.gv[t], p.seam_g + ((tok0 + t) * p.h_v + c.h) * 128, 512, &sm.seam_full[b]);
+    tc::bulk_load(s.gv[t], p.seam_g + ((tok0 + t) * p.h_v + c.h) * 128, 512, &sm.seam_full[b]);
   }
-  tc::bulk_load(s.b, p.seam_beta + tok0 * p.h_v, gbytes, &sm.seam_full[b]);
-  if (GDN) tc::bulk_load(s.g, p.seam_g + tok0 * p.h_v, gbytes, &sm.seam_full[b]);
+  prefetch_l2(p.seam_beta + tok0 * p.h_v, gbytes);
 }
 
 __device__ __forceinline__ void prefetch_pair_S(const ComposeParams &p, const Chain &c, int seg) {
@@ -169,20 +173,19 @@ __device__ __forceinline__ void prefetch_pair(const ComposeParams &p, const Chai
   prefetch_l2(p.S_pool + off, 128 * 128 * 4);
 }
 
-// VAR: HYPIC_GDN, HYPIC_DELTANET or HYPIC_CHANNEL_DELTA
-template <int VAR>
 __global__ void __launch_bounds__(NT, 2)
-    compose_tc_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tmap_T) {
-  constexpr bool VEC = VAR == HYPIC_CHANNEL_DELTA;
-  constexpr bool GDN = VAR == HYPIC_GDN;
+    compose_channel_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tmap_T) {
   extern __shared__ unsigned char smem_raw[];
   // 1024-byte alignment by pointer arithmetic on the shared array, so the
   // compiler keeps every access in the shared address space
   ComposeTcSmem &sm = *reinterpret_cast<ComposeTcSmem *>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   const ComposeParams &p = args.p;
   const uint32_t LIM = args.wait_limit;
-  const int n = threadIdx.x;  // column of S owned by this thread
-  const int warp = n / 32;
+  const int tid = threadIdx.x;
+  const int n = tid & 127;   // column of S
+  const int hf = tid >> 7;   // rows 64*hf .. 64*hf+63 of that column
+  const int r0 = 64 * hf;
+  const int warp = tid / 32;
   Chain c;
   c.l = blockIdx.x / p.h_v;
   c.h = blockIdx.x % p.h_v;
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(NT, 2)
   const int total_groups = c.n_seg * c.groups;
   const uint32_t total_slabs = 4u * (uint32_t)c.n_seg;
 
-  if (n == 0) {
+  if (tid == 0) {
     for (int i = 0; i < NSLOT; i++) tc::mbar_init(&sm.full[i], 1);
     tc::mbar_init(&sm.seam_full[0], 1);
     tc::mbar_init(&sm.seam_full[1], 1);
@@ -209,16 +212,18 @@ __global__ void __launch_bounds__(NT, 2)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  // warps w and w + 4 share the TMEM lane quadrant w % 4 (lanes = columns)
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t tDh = sm.tmem_base + lane_base + r0, tAh = sm.tmem_base + 128 + lane_base + r0;
   const uint32_t tD = sm.tmem_base, tA = sm.tmem_base + 128;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 
   uint32_t issued = 0;  // T_C slabs issued (thread 0)
   int seam_issued = 0;  // seam groups issued (thread 0)
-  if (n == 0) {
+  if (tid == 0) {
     tc::prefetch_tmap(&tmap_T);
     for (; issued < (uint32_t)NSLOT && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued);
-    issue_seam<VEC, GDN>(sm, p, c, 0);
-    issue_seam<VEC, GDN>(sm, p, c, 1);
+    issue_seam(sm, p, c, 0);
+    issue_seam(sm, p, c, 1);
     seam_issued = min(2, total_groups);
     prefetch_pair_S(p, c, 0);
     prefetch_pair_S(p, c, 1);
@@ -226,16 +231,29 @@ __global__ void __launch_bounds__(NT, 2)
 
   if (args.debug_stall && !tc::mbar_wait(&sm.never, 0, LIM)) fail(sm, p);
 
-  const int64_t state = (int64_t)blockIdx.x * 128 * 128;
-  float S[128];
+  // this thread's rows of the state
+  const int64_t state = (int64_t)blockIdx.x * 128 * 128 + (int64_t)r0 * 128 + n;
+  float S[64];
 #pragma unroll
-  for (int i = 0; i < 128; i++) S[i] = p.S_init ? p.S_init[state + (int64_t)i * 128 + n] : 0.f;
+  for (int i = 0; i < 64; i++) S[i] = p.S_init ? p.S_init[state + (int64_t)i * 128] : 0.f;
   bool bad = false;
   const uint32_t id = tc::idesc(tc::FMT_TF32, 128, 128);
+  uint32_t u = 0;          // seam tokens processed (uniform): parity of the exchange buffers
+  int64_t pend = -1;       // lower half: token whose output waits for the upper half's partial
+  float opend = 0.f;
+  // lower half, after a CTA barrier: complete the pending output
+  auto flush = [&]() {
+    if (hf == 0 && pend >= 0) {
+      const float o = opend + sm.os[(u - 1) & 1][n];
+      p.seam_out[(pend * p.h_v + c.h) * 128 + n] = o;
+      bad |= !finite_f(o);
+    }
+    pend = -1;
+  };
 
   for (int seg = 0; seg < c.n_seg; seg++) {
     // uniform stop decision
-    if (n == 0) sm.stop = *(volatile int *)&sm.abort;
+    if (tid == 0) sm.stop = *(volatile int *)&sm.abort;
     __syncthreads();
     const bool stop = *(volatile int *)&sm.stop != 0;
     __syncthreads();
@@ -251,23 +269,30 @@ __global__ void __launch_bounds__(NT, 2)
       const int t0 = gi * SB;
       const int nt = ok ? min(SB, c.w - t0) : 0;
       const int64_t tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + t0;
-      if (VEC) {
-        // per-channel gates a = exp(g), once per buffer (thread n: channel n)
-        for (int t = 0; t < nt; t++) s.gv[t][n] = __expf(s.gv[t][n]);
-        __syncthreads();
-      }
+      // per-channel gates a = exp(g), once per buffer, and this head's betas
+      for (int e = tid; e < nt * 128; e += NT) (&s.gv[0][0])[e] = __expf((&s.gv[0][0])[e]);
+      if (tid < nt) s.b[tid] = p.seam_beta[(tok0 + tid) * p.h_v + c.h];
+      __syncthreads();
       for (int t = 0; t < nt; t++) {
-        const float vj = __bfloat162float(s.v[t][n]);
-        const float bt = s.b[t * p.h_v + c.h];
+        const float *ar = s.gv[t] + r0;
+        const __nv_bfloat16 *kr = s.k[t] + r0;
+        const __nv_bfloat16 *qr = s.q[t] + r0;
+        // S <- Diag(a) S and the half dot product k^T S
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 128; i += 8) {
+        for (int i = 0; i < 64; i += 8) {
           float kv[8];
-          unpack8(s.k[t] + i, kv);
-          if (VEC) {
-#pragma unroll
-            for (int j = 0; j < 8; j++) kv[j] *= s.gv[t][i + j];
-          }
+          unpack8(kr + i, kv);
+          const float4 a0 = *reinterpret_cast<const float4 *>(ar + i);
+          const float4 a1 = *reinterpret_cast<const float4 *>(ar + i + 4);
+          S[i] *= a0.x;
+          S[i + 1] *= a0.y;
+          S[i + 2] *= a0.z;
+          S[i + 3] *= a0.w;
+          S[i + 4] *= a1.x;
+          S[i + 5] *= a1.y;
+          S[i + 6] *= a1.z;
+          S[i + 7] *= a1.w;
           x0 = fmaf(kv[0], S[i], x0);
           x1 = fmaf(kv[1], S[i + 1], x1);
           x2 = fmaf(kv[2], S[i + 2], x2);
@@ -277,20 +302,22 @@ __global__ void __launch_bounds__(NT, 2)
           x2 = fmaf(kv[6], S[i + 6], x2);
           x3 = fmaf(kv[7], S[i + 7], x3);
         }
-        const float x = (x0 + x1) + (x2 + x3);
-        // S <- a (S - b k x) + b k v   (channel: Diag(a) S first, then the erase)
-        const float gs = GDN ? __expf(s.g[t * p.h_v + c.h]) : 1.f;
-        const float cc = VEC ? (bt * vj - bt * x) : (gs * (-bt * x) + bt * vj);
-#pragma unroll
-        for (int i = 0; i < 128; i++) {
-          const float a = VEC ? s.gv[t][i] : gs;
-          S[i] = fmaf(a, S[i], __bfloat162float(s.k[t][i]) * cc);
-        }
+        sm.xs[u & 1][hf][n] = (x0 + x1) + (x2 + x3);
+        __syncthreads();
+        flush();  // the previous token's output
+        // both halves sum in the same order: identical x
+        const float x = sm.xs[u & 1][0][n] + sm.xs[u & 1][1][n];
+        const float bt = s.b[t];
+        const float cc = bt * __bfloat162float(s.v[t][n]) - bt * x;
+        // S <- S + k c and the half output q^T S
         float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 128; i += 8) {
-          float qv[8];
-          unpack8(s.q[t] + i, qv);
+        for (int i = 0; i < 64; i += 8) {
+          float kv[8], qv[8];
+          unpack8(kr + i, kv);
+          unpack8(qr + i, qv);
+#pragma unroll
+          for (int j = 0; j < 8; j++) S[i + j] = fmaf(kv[j], cc, S[i + j]);
           o0 = fmaf(qv[0], S[i], o0);
           o1 = fmaf(qv[1], S[i + 1], o1);
           o2 = fmaf(qv[2], S[i + 2], o2);
@@ -301,29 +328,32 @@ __global__ void __launch_bounds__(NT, 2)
           o3 = fmaf(qv[7], S[i + 7], o3);
         }
         const float o = (o0 + o1) + (o2 + o3);
-        p.seam_out[((tok0 + t) * p.h_v + c.h) * 128 + n] = o;
-        bad |= !finite_f(o);
+        if (hf) sm.os[u & 1][n] = o;
+        opend = o;
+        pend = tok0 + t;
+        u++;
       }
       __syncthreads();  // every thread is done with this seam buffer
-      if (n == 0 && !aborted(sm) && gq + 2 < total_groups) {
-        issue_seam<VEC, GDN>(sm, p, c, gq + 2);
+      flush();
+      if (tid == 0 && !aborted(sm) && gq + 2 < total_groups) {
+        issue_seam(sm, p, c, gq + 2);
         seam_issued = gq + 3;
       }
     }
 
     // ---- S -> TMEM (A operand, tf32 round-to-nearest)
 #pragma unroll
-    for (int ch = 0; ch < 8; ch++) {
+    for (int ch = 0; ch < 4; ch++) {
       uint32_t r[16];
 #pragma unroll
       for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(S[16 * ch + j]);
-      tc::tmem_st16(tA + lane_base + 16 * ch, r);
+      tc::tmem_st16(tAh + 16 * ch, r);
     }
     tc::tmem_wait_st();
     tc::tc_fence_before();
     __syncthreads();
     const uint32_t q = 4u * (uint32_t)seg;
-    if (n == 0) {
+    if (tid == 0) {
       tc::tc_fence_after();
       bool ok = !aborted(sm);
       for (int sl = 0; sl < 4 && ok; sl++) {
@@ -343,41 +373,33 @@ __global__ void __launch_bounds__(NT, 2)
       }
       tc::mma_commit(&sm.mma_done);  // arrives once the MMAs above are complete
     }
+
+    // ---- S <- T_C S + S(C|0): S(C|0) loads in flight while the MMA runs (S
+    // itself is in TMEM A now; a skipped pair keeps S)
+    const int slot = pair_slot(p, c, seg);
+    if (slot < 0 && tid == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
+    const bool use = slot >= 0 && !aborted(sm);
+    if (use) {
+      const float *Sc = p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128 + (int64_t)r0 * 128 + n;
+#pragma unroll
+      for (int j = 0; j < 64; j++) S[j] = Sc[j * 128];
+    }
     if (!tc::mbar_wait(&sm.mma_done, seg & 1, DRAIN_LIMIT)) fail(sm, p);
     tc::tc_fence_after();
-    if (n == 0 && !aborted(sm)) {
+    if (tid == 0 && !aborted(sm)) {
       // this pair's four slots are free: refill them, and warm L2 with the
       // S(C|0) of the segment after next
       for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
       prefetch_pair_S(p, c, seg + 2);
     }
-
-    // ---- S <- T_C S + S(C|0)
-    const int slot = pair_slot(p, c, seg);
-    if (slot < 0 && n == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
-    const bool use = slot >= 0 && !aborted(sm);
-    const float *Sc = p.S_pool + ((int64_t)(slot < 0 ? 0 : slot) * p.h_v + c.h) * 128 * 128 + n;
-    float nxt[32];
+    if (use) {
 #pragma unroll
-    for (int j = 0; j < 32; j++) nxt[j] = use ? Sc[j * 128] : 0.f;
-#pragma unroll
-    for (int ch = 0; ch < 4; ch++) {
-      float cur[32];
-#pragma unroll
-      for (int j = 0; j < 32; j++) cur[j] = nxt[j];
-      if (ch < 3) {
-#pragma unroll
-        for (int j = 0; j < 32; j++) nxt[j] = use ? Sc[(32 * (ch + 1) + j) * 128] : 0.f;
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
+      for (int ch = 0; ch < 4; ch++) {
         uint32_t r[16];
-        tc::tmem_ld16(tD + lane_base + 32 * ch + 16 * hh, r);
+        tc::tmem_ld16(tDh + 16 * ch, r);
         tc::tmem_wait_ld();
-        if (use) {
 #pragma unroll
-          for (int j = 0; j < 16; j++) S[32 * ch + 16 * hh + j] = __uint_as_float(r[j]) + cur[16 * hh + j];
-        }
+        for (int j = 0; j < 16; j++) S[16 * ch + j] += __uint_as_float(r[j]);
       }
     }
     tc::tc_fence_before();  // TMEM reads done before the next MMA overwrites D
@@ -386,14 +408,14 @@ __global__ void __launch_bounds__(NT, 2)
   __syncthreads();
   if (!aborted(sm)) {
 #pragma unroll
-    for (int i = 0; i < 128; i++) {
-      p.S_out[state + (int64_t)i * 128 + n] = S[i];
+    for (int i = 0; i < 64; i++) {
+      p.S_out[state + (int64_t)i * 128] = S[i];
       bad |= !finite_f(S[i]);
     }
   }
   if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
   // drain: every copy thread 0 issued lands before the CTA releases its smem
-  if (n == 0) {
+  if (tid == 0) {
     const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
     for (uint32_t r = first; r < issued; r++) tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, DRAIN_LIMIT);
     for (int r = seam_issued > 2 ? seam_issued - 2 : 0; r < seam_issued; r++)
@@ -1110,7 +1132,7 @@ cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaS
   // token-by-token seam
   const bool vec = p.variant == HYPIC_CHANNEL_DELTA;
   const size_t smem = (vec ? sizeof(ComposeTcSmem) : sizeof(SeamMmaSmem)) + 1024;
-  auto kern = vec                       ? compose_tc_kernel<HYPIC_CHANNEL_DELTA>
+  auto kern = vec                       ? compose_channel_kernel
               : p.variant == HYPIC_GDN ? compose_seam_mma_kernel<true>
                                        : compose_seam_mma_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
