@@ -75,9 +75,11 @@ def build_bytes(n_tokens, n_pairs, h_k, h_v, d_k=128, d_v=128, in_bytes=2):
             + n_pairs * h_v * (d_k * d_k + d_k * d_v) * 4)
 
 
-def compose_bytes(n_layers, n_seg, w, h_k, h_v, d_k=128, d_v=128, in_bytes=2, with_init=False):
+def compose_bytes(n_layers, n_seg, w, h_k, h_v, d_k=128, d_v=128, in_bytes=2, with_init=False, gate_floats=1):
+    """gate_floats: fp32 gate values per (token, value head): 1 (scalar),
+    d_k (per-channel) or 0 (DeltaNet)."""
     pairs = n_layers * n_seg * h_v * (d_k * d_k + d_k * d_v) * 4
-    seam_in = n_layers * n_seg * w * (2 * h_k * d_k * in_bytes + h_v * d_v * in_bytes + 2 * h_v * 4)
+    seam_in = n_layers * n_seg * w * (2 * h_k * d_k * in_bytes + h_v * d_v * in_bytes + (1 + gate_floats) * h_v * 4)
     seam_out = n_layers * n_seg * w * h_v * d_v * 4
     states = n_layers * h_v * d_k * d_v * 4 * (2 if with_init else 1)
     slots = n_layers * n_seg * 4
@@ -218,12 +220,13 @@ def setup_build(dev, seed=0):
     return W
 
 
-def setup_compose(dev, hy, seed=0, n_layers=30):
-    """Cache pool of the warm RAG prompt: pairs of 30 GDN layers built on the
-    GPU from seeded token inputs (untimed set-up), plus the seam tokens."""
+def setup_compose(dev, hy, seed=0, n_layers=30, variant="gdn"):
+    """Cache pool of the warm RAG prompt: pairs of 30 GDN layers (or another
+    dense-transition variant) built on the GPU from seeded token inputs
+    (untimed set-up), plus the seam tokens."""
     import torch
     import synth_inputs as si
-    W = si.workload(4, seed=seed, device=dev, n_layers=1)
+    W = si.workload(4, seed=seed, device=dev, n_layers=1, variant=variant)
     n_seg = W.n_seg
     n_slots = n_layers * n_seg
     T_pool = torch.empty((n_slots, W.h_v, W.d_k, W.d_k), device=dev)
@@ -231,16 +234,17 @@ def setup_compose(dev, hy, seed=0, n_layers=30):
     seams = []
     for l in range(n_layers):
         lay = W.layers[0] if l == 0 else si.make_layer(seed=seed, cfg=4, layer=l, n_tokens=W.n_tokens, h_k=W.h_k,
-                                                        h_v=W.h_v, d_k=W.d_k, d_v=W.d_v, variant="gdn",
+                                                        h_v=W.h_v, d_k=W.d_k, d_v=W.d_v, variant=variant,
                                                         dtype=torch.bfloat16, device=dev)
         slots = np.arange(n_seg, dtype=np.int32) + l * n_seg
-        hy.segment_build(lay.k, lay.v, lay.g, lay.beta, W.seg_offsets, variant="gdn", seam_w=W.seam_w,
+        hy.segment_build(lay.k, lay.v, lay.g, lay.beta, W.seg_offsets, variant=variant, seam_w=W.seam_w,
                          T_pool=T_pool, S_pool=S_pool, slot_of_seg=slots)
         W.layers = [lay]
         seams.append(si.seam_gather(W, lay))
         del lay
     torch.cuda.synchronize()
-    sa = {k: torch.stack([s[k] for s in seams]).contiguous() for k in ("k", "v", "q", "g", "beta")}
+    sa = {k: (torch.stack([s[k] for s in seams]).contiguous() if seams[0][k] is not None else None)
+          for k in ("k", "v", "q", "g", "beta")}
     slot = torch.arange(n_slots, dtype=torch.int32, device=dev).reshape(n_layers, n_seg)
     S_out = torch.empty((n_layers, W.h_v, W.d_k, W.d_v), device=dev)
     seam_out = torch.empty((n_layers, n_seg, W.seam_w, W.h_v, W.d_v), device=dev)
@@ -286,6 +290,29 @@ def merge_row(dev, hy, peaks, comp):
     return {"ms": ms, "merges_per_s": units / (ms * 1e-3), "algorithmic_bytes": nbytes,
             "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"]},
             "kernel": "tensor-core pair merge (split tf32)"}
+
+
+def compose_variant_rows(dev, hy, peaks, n_layers=8):
+    """The compose of the other dense-transition variants on the warm-prompt
+    shape (8 layers x 32 heads x 100 segments, w = 8): DeltaNet (tensor-core
+    seam) and the per-channel gate (token-by-token seam)."""
+    import torch
+    rows = {}
+    for var, gate in (("deltanet", 0), ("channel", 128)):
+        comp = setup_compose(dev, hy, n_layers=n_layers, variant=var)
+        W, sa = comp["W"], comp["sa"]
+        ms = _time_ms(lambda: hy.compose(comp["slot"], comp["T_pool"], comp["S_pool"], sa["k"], sa["v"], sa["q"],
+                                         sa["g"], sa["beta"], variant=var, S_out=comp["S_out"],
+                                         seam_out=comp["seam_out"]))
+        nbytes = compose_bytes(n_layers, W.n_seg, W.seam_w, W.h_k, W.h_v, W.d_k, W.d_v, gate_floats=gate)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows[f"compose: {var}, {n_layers} layers x {W.h_v} heads x {W.n_seg} segments, w={W.seam_w}"] = {
+            "ms": ms, "algorithmic_bytes": nbytes,
+            "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"]},
+            "kernel": "tensor-core compose, " + ("tensor-core seam" if var == "deltanet" else "token seam")}
+        del comp, sa
+        torch.cuda.empty_cache()
+    return rows
 
 
 def measure_rows(dev, hy, peaks):
@@ -584,6 +611,7 @@ def main():
     if rank == 0 and not args.no_rows:
         rows = {f"merge: {comp['n_layers']} layers x {W4.h_v} heads x {W4.n_seg // 2} adjacent segment pairs":
                 merge_row(dev, hy, peaks, comp)}
+        rows.update(compose_variant_rows(dev, hy, peaks))
         rows.update(measure_rows(dev, hy, peaks))
 
     cpu = None

@@ -493,6 +493,9 @@ struct __align__(1024) SeamMmaSmem {
   uint64_t full[NSLOT];
   uint64_t raw_full[2];
   uint64_t mma_done;
+  uint64_t seam_done;  // fused group: the seam products are in D
+  uint64_t tk_done;    // fused group: T_C [K;Q]^T is in D
+  uint64_t d_read;     // fused group: every thread has read its seam columns of D
   uint64_t never;
   uint32_t tmem_base;
   int abort;
@@ -695,6 +698,9 @@ __global__ void __launch_bounds__(NT2, 2)
     tc::mbar_init(&sm.raw_full[0], 1);
     tc::mbar_init(&sm.raw_full[1], 1);
     tc::mbar_init(&sm.mma_done, 1);
+    tc::mbar_init(&sm.seam_done, 1);
+    tc::mbar_init(&sm.tk_done, 1);
+    tc::mbar_init(&sm.d_read, NT2);
     tc::mbar_init(&sm.never, 1);
     sm.abort = 0;
     tc::fence_mbar_init();
@@ -735,6 +741,7 @@ __global__ void __launch_bounds__(NT2, 2)
   const uint32_t id_T = tc::idesc(tc::FMT_TF32, 128, 128);
   const uint32_t id_s = tc::idesc(tc::FMT_TF32, 128, 16);
   uint32_t mcount = 0;  // commits to mma_done so far (uniform)
+  uint32_t nfused = 0;  // fused groups so far (uniform): phase of seam_done / tk_done / d_read
   const int ptid = tid - 32 * PREP_WARP0;
   float pb = 0.f, pg = 0.f;  // preparing threads ptid < GW: beta / log-gate of token ptid of the next group
 
@@ -770,13 +777,30 @@ __global__ void __launch_bounds__(NT2, 2)
     mcount++;
     tc::tc_fence_after();
   };
-  // D cols 0..15 = S^T [K;Q]^T (issuer)
+  // S^T [K;Q]^T (issuer) as four independent partial products, one per
+  // K-slab a of 32 channels, in D cols 32a .. 32a + 15 (short dependent
+  // accumulation chains; read_seam sums them)
   auto issue_seam_mma = [&]() {
     const uint32_t base = tc::smem_u32(&sm.bt[0][0][0]);
 #pragma unroll
-    for (int kk = 0; kk < 16; kk++) {
-      const uint64_t bd = tc::smem_desc(base + 2048 * (kk >> 2) + 32 * (kk & 3), 16, 1024, tc::SW_128B);
-      tc::mma_ts_tf32(tD, tA + 8 * kk, bd, id_s, kk != 0);
+    for (int k4 = 0; k4 < 4; k4++) {
+#pragma unroll
+      for (int a = 0; a < 4; a++) {
+        const uint64_t bd = tc::smem_desc(base + 2048 * a + 32 * k4, 16, 1024, tc::SW_128B);
+        tc::mma_ts_tf32(tD + 32 * a, tA + 32 * a + 8 * k4, bd, id_s, k4 != 0);
+      }
+    }
+  };
+  // k_t^T S0 (d[0..7]) and q_t^T S0 (d[8..15]) for column n (warp-collective)
+  auto read_seam = [&](uint32_t (&d)[16]) {
+    uint32_t e[16];
+    tc::tmem_ld16(tD + lane_base, d);
+#pragma unroll
+    for (int a = 1; a < 4; a++) {
+      tc::tmem_ld16(tD + lane_base + 32 * a, e);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; j++) d[j] = __float_as_uint(__uint_as_float(d[j]) + __uint_as_float(e[j]));
     }
   };
   // D = S^T T_C^T from TMEM A and the four K-slabs at ring position q (issuer)
@@ -886,7 +910,7 @@ __global__ void __launch_bounds__(NT2, 2)
       }
       wait_mma();
       uint32_t d[16];
-      tc::tmem_ld16(tD + lane_base, d);
+      read_seam(d);
       tc::tmem_wait_ld();
       if (!aborted(sm)) {
         float cc[GW];
@@ -941,33 +965,50 @@ __global__ void __launch_bounds__(NT2, 2)
       // the segment ends at e^{lam_last} D + S(C|0).
       const int gq = seg * c.groups + c.groups - 1;
       al = sm.gc[gq & 1].alast;
+      const uint32_t fph = nfused & 1;
+      nfused++;
       if (issuer) {
         tc::tc_fence_after();
-        if (!aborted(sm)) {
-          issue_seam_mma();
-          if (wait_slabs(q)) {
-            // D cols 16..31 = T_C [K;Q]^T: lane r holds (T_C k_i)[r]
-            const uint32_t bbase = tc::smem_u32(&sm.bt[0][0][0]);
+        if (!aborted(sm)) issue_seam_mma();
+        tc::mma_commit(&sm.seam_done);
+        if (!aborted(sm) && wait_slabs(q)) {
+          // T_C [K;Q]^T as four partial products, one per K-slab sl, in D
+          // cols 32 sl + 16 .. 32 sl + 31: lane r holds (T_C k_i)[r]
+          const uint32_t bbase = tc::smem_u32(&sm.bt[0][0][0]);
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++) {
             for (int sl = 0; sl < 4; sl++) {
               const uint32_t abase = tc::smem_u32(sm.slot[(q + sl) % NSLOT]);
-#pragma unroll
-              for (int kk = 0; kk < 4; kk++) {
-                const uint64_t ad = tc::smem_desc(abase + 32 * kk, 16, 1024, tc::SW_128B);
-                const uint64_t bd = tc::smem_desc(bbase + 2048 * sl + 32 * kk, 16, 1024, tc::SW_128B);
-                tc::mma_ss_tf32(tD + 16, ad, bd, id_s, (sl | kk) != 0);
-              }
+              const uint64_t ad = tc::smem_desc(abase + 32 * kk, 16, 1024, tc::SW_128B);
+              const uint64_t bd = tc::smem_desc(bbase + 2048 * sl + 32 * kk, 16, 1024, tc::SW_128B);
+              tc::mma_ss_tf32(tD + 32 * sl + 16, ad, bd, id_s, kk != 0);
             }
           }
         }
-        tc::mma_commit(&sm.mma_done);
+        tc::mma_commit(&sm.tk_done);
       }
-      wait_mma();
+      __syncwarp();
+      // warps 0..3 read the seam products as soon as they are in; warps 4..7
+      // the T_C k_i, into the seam term's B tile; the product may overwrite D
+      // once every thread has arrived at d_read
       uint32_t d[16];
       if (hf == 0) {
-        tc::tmem_ld16(tD + lane_base, d);  // k_t^T S0, q_t^T S0
+        if (!tc::mbar_wait(&sm.seam_done, fph, DRAIN_LIMIT)) fail(sm, p);
+        tc::tc_fence_after();
+        read_seam(d);
+        tc::tmem_wait_ld();
       } else {
-        uint32_t e[16];
-        tc::tmem_ld16(tD + lane_base + 16, e);  // (T_C k_i)[n]
+        if (!tc::mbar_wait(&sm.tk_done, fph, DRAIN_LIMIT)) fail(sm, p);
+        tc::tc_fence_after();
+        uint32_t e[8], f[8];
+        tc::tmem_ld8(tD + lane_base + 16, e);
+#pragma unroll
+        for (int a = 1; a < 4; a++) {
+          tc::tmem_ld8(tD + lane_base + 32 * a + 16, f);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 8; j++) e[j] = __float_as_uint(__uint_as_float(e[j]) + __uint_as_float(f[j]));
+        }
         tc::tmem_wait_ld();
         float tkr[GW];
 #pragma unroll
@@ -975,9 +1016,8 @@ __global__ void __launch_bounds__(NT2, 2)
         store_row_sw32(sm.tk, n, tkr);
         tc::fence_proxy_async_smem();
       }
-      tc::tmem_wait_ld();
       tc::tc_fence_before();
-      __syncthreads();
+      tc::mbar_arrive(&sm.d_read);
       if (hf == 0) {
         // warps 0..3, while the product runs: the group's recurrence and
         // outputs, and the seam term tile
@@ -996,6 +1036,7 @@ __global__ void __launch_bounds__(NT2, 2)
         tc::named_bar(BAR_CORR, 160);
       } else if (warp == ISSUER_WARP) {
         if (issuer) {
+          if (!tc::mbar_wait(&sm.d_read, fph, DRAIN_LIMIT)) fail(sm, p);
           tc::tc_fence_after();
           if (!aborted(sm)) issue_T_mma(q);
         }
