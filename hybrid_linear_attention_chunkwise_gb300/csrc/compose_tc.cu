@@ -493,8 +493,8 @@ struct __align__(1024) SeamMmaSmem {
   uint64_t full[NSLOT];
   uint64_t raw_full[2];
   uint64_t mma_done;
-  uint64_t seam_done;  // fused group: the seam products are in D
-  uint64_t tk_done;    // fused group: T_C [K;Q]^T is in D
+  uint64_t seam_done;  // fused group: the seam products are in D (four issuing threads)
+  uint64_t tk_done;    // fused group: T_C [K;Q]^T is in D (four issuing threads)
   uint64_t d_read;     // fused group: every thread has read its seam columns of D
   uint64_t never;
   uint32_t tmem_base;
@@ -698,8 +698,8 @@ __global__ void __launch_bounds__(NT2, 2)
     tc::mbar_init(&sm.raw_full[0], 1);
     tc::mbar_init(&sm.raw_full[1], 1);
     tc::mbar_init(&sm.mma_done, 1);
-    tc::mbar_init(&sm.seam_done, 1);
-    tc::mbar_init(&sm.tk_done, 1);
+    tc::mbar_init(&sm.seam_done, 4);
+    tc::mbar_init(&sm.tk_done, 4);
     tc::mbar_init(&sm.d_read, NT2);
     tc::mbar_init(&sm.never, 1);
     sm.abort = 0;
@@ -717,6 +717,7 @@ __global__ void __launch_bounds__(NT2, 2)
   const uint32_t tD = sm.tmem_base, tA = sm.tmem_base + 128;
   const uint32_t tDh = tD + lane_base + 64 * hf, tAh = tA + lane_base + 64 * hf;  // this thread's rows
   const bool issuer = tid == 32 * ISSUER_WARP;
+  const bool slab_issuer = warp >= ISSUER_WARP && (tid & 31) == 0;  // lane 0 of warps 4..7
 
   uint32_t issued = 0;  // T_C slabs issued (thread 0)
   int raw_issued = min(2, total_groups);  // seam groups issued (uniform)
@@ -967,21 +968,35 @@ __global__ void __launch_bounds__(NT2, 2)
       al = sm.gc[gq & 1].alast;
       const uint32_t fph = nfused & 1;
       nfused++;
-      if (issuer) {
+      if (slab_issuer) {
+        // lane 0 of warps 4..7, one K-slab a each (the issue of one MMA takes
+        // tens of cycles, so four threads issue the 32 small products in a
+        // quarter of the time): the seam partial product a, then, once T_C's
+        // K-slab a has landed, (T_C [K;Q]^T)'s partial product a
+        const int a = warp - ISSUER_WARP;
         tc::tc_fence_after();
-        if (!aborted(sm)) issue_seam_mma();
-        tc::mma_commit(&sm.seam_done);
-        if (!aborted(sm) && wait_slabs(q)) {
-          // T_C [K;Q]^T as four partial products, one per K-slab sl, in D
-          // cols 32 sl + 16 .. 32 sl + 31: lane r holds (T_C k_i)[r]
+        if (!aborted(sm)) {
           const uint32_t bbase = tc::smem_u32(&sm.bt[0][0][0]);
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) {
-            for (int sl = 0; sl < 4; sl++) {
-              const uint32_t abase = tc::smem_u32(sm.slot[(q + sl) % NSLOT]);
+          for (int k4 = 0; k4 < 4; k4++) {
+            const uint64_t bd = tc::smem_desc(bbase + 2048 * a + 32 * k4, 16, 1024, tc::SW_128B);
+            tc::mma_ts_tf32(tD + 32 * a, tA + 32 * a + 8 * k4, bd, id_s, k4 != 0);
+          }
+        }
+        tc::mma_commit(&sm.seam_done);
+        const uint32_t r = q + a;
+        if (!aborted(sm)) {
+          if (!tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, LIM)) {
+            fail(sm, p);
+          } else {
+            // D cols 32 a + 16 .. 32 a + 31: lane r holds partial (T_C k_i)[r]
+            const uint32_t abase = tc::smem_u32(sm.slot[r % NSLOT]);
+            const uint32_t bbase = tc::smem_u32(&sm.bt[0][0][0]) + 2048 * a;
+#pragma unroll
+            for (int kk = 0; kk < 4; kk++) {
               const uint64_t ad = tc::smem_desc(abase + 32 * kk, 16, 1024, tc::SW_128B);
-              const uint64_t bd = tc::smem_desc(bbase + 2048 * sl + 32 * kk, 16, 1024, tc::SW_128B);
-              tc::mma_ss_tf32(tD + 32 * sl + 16, ad, bd, id_s, kk != 0);
+              const uint64_t bd = tc::smem_desc(bbase + 32 * kk, 16, 1024, tc::SW_128B);
+              tc::mma_ss_tf32(tD + 32 * a + 16, ad, bd, id_s, kk != 0);
             }
           }
         }
@@ -1038,7 +1053,7 @@ __global__ void __launch_bounds__(NT2, 2)
         if (issuer) {
           if (!tc::mbar_wait(&sm.d_read, fph, DRAIN_LIMIT)) fail(sm, p);
           tc::tc_fence_after();
-          if (!aborted(sm)) issue_T_mma(q);
+          if (!aborted(sm) && wait_slabs(q)) issue_T_mma(q);
         }
         tc::named_bar(BAR_CORR, 160);
         if (issuer) {
