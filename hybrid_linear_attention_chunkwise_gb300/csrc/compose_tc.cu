@@ -493,6 +493,8 @@ struct __align__(1024) SeamMmaSmem {
   uint64_t full[NSLOT];
   uint64_t raw_full[2];
   uint64_t mma_done;
+  uint64_t t_done;     // the T_C S0 product of a pair is complete (its slabs are free)
+  uint64_t sc_full;    // the pair's S(C|0) has landed in its four slots
   uint64_t seam_done;  // fused group: the seam products are in D (four issuing threads)
   uint64_t tk_done;    // fused group: T_C [K;Q]^T is in D (four issuing threads)
   uint64_t d_read;     // fused group: every thread has read its seam columns of D
@@ -698,6 +700,8 @@ __global__ void __launch_bounds__(NT2, 2)
     tc::mbar_init(&sm.raw_full[0], 1);
     tc::mbar_init(&sm.raw_full[1], 1);
     tc::mbar_init(&sm.mma_done, 1);
+    tc::mbar_init(&sm.t_done, 1);
+    tc::mbar_init(&sm.sc_full, 1);
     tc::mbar_init(&sm.seam_done, 4);
     tc::mbar_init(&sm.tk_done, 4);
     tc::mbar_init(&sm.d_read, NT2);
@@ -743,6 +747,8 @@ __global__ void __launch_bounds__(NT2, 2)
   const uint32_t id_s = tc::idesc(tc::FMT_TF32, 128, 16);
   uint32_t mcount = 0;  // commits to mma_done so far (uniform)
   uint32_t nfused = 0;  // fused groups so far (uniform): phase of seam_done / tk_done / d_read
+  uint32_t npair = 0;   // pairs applied so far (uniform): phase of t_done / sc_full
+  bool refill_pending = false;  // thread 0: the last pair's slots await the next slabs
   const int ptid = tid - 32 * PREP_WARP0;
   float pb = 0.f, pg = 0.f;  // preparing threads ptid < GW: beta / log-gate of token ptid of the next group
 
@@ -815,6 +821,17 @@ __global__ void __launch_bounds__(NT2, 2)
       }
     }
   };
+  // issuer, once the T_C S0 product of the pair at ring position q (slot
+  // `slot` of the pool) is issued: when it completes, the pair's S(C|0)
+  // (64 KiB, contiguous) replaces T_C in the four slots, 16 KiB (32 rows)
+  // per slot
+  auto load_sc = [&](uint32_t q, int slot, uint32_t ph) {
+    tc::mma_commit(&sm.t_done);
+    if (!tc::mbar_wait(&sm.t_done, ph, DRAIN_LIMIT)) fail(sm, p);
+    tc::mbar_expect_tx(&sm.sc_full, 4 * SLAB);
+    const float *src = p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128;
+    for (int j = 0; j < 4; j++) tc::bulk_load(sm.slot[(q + j) % NSLOT], src + j * 32 * 128, SLAB, &sm.sc_full);
+  };
   // the four K-slabs at ring position q have landed (one thread)
   auto wait_slabs = [&](uint32_t q) {
     for (int sl = 0; sl < 4; sl++) {
@@ -883,6 +900,15 @@ __global__ void __launch_bounds__(NT2, 2)
     __syncthreads();
     if (*(volatile int *)&sm.stop != 0) break;
 
+    if (tid == 0 && refill_pending) {
+      // the last pair's slots (T_C, then S(C|0)) are free: refill them, and
+      // warm L2 with the pair of the segment after this one
+      refill_pending = false;
+      if (!aborted(sm)) {
+        for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
+        prefetch_pair(p, c, seg + 1);
+      }
+    }
     const int slot = slot_next;  // uniform
     const bool last = seg + 1 == c.n_seg;
     slot_next = last ? 0 : pair_slot(p, c, seg + 1);
@@ -1054,6 +1080,7 @@ __global__ void __launch_bounds__(NT2, 2)
           if (!tc::mbar_wait(&sm.d_read, fph, DRAIN_LIMIT)) fail(sm, p);
           tc::tc_fence_after();
           if (!aborted(sm) && wait_slabs(q)) issue_T_mma(q);
+          load_sc(q, slot, npair & 1);
         }
         tc::named_bar(BAR_CORR, 160);
         if (issuer) {
@@ -1075,38 +1102,39 @@ __global__ void __launch_bounds__(NT2, 2)
         tc::tc_fence_after();
         if (!aborted(sm) && wait_slabs(q)) issue_T_mma(q);
         tc::mma_commit(&sm.mma_done);
+        load_sc(q, slot, npair & 1);
       }
       if (preper && has_seam && !last) prepare(gq_next);
     }
 
-    // ---- S <- al D + S(C|0) for this thread's 64 rows (all loads issued
-    // before the wait); RN(S) back to TMEM A, the exact S to S_out where needed
-    const bool use = !aborted(sm);
-    const float *Sc = p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128 + (int64_t)(64 * hf) * 128 + n;
-    float sc[64];
-#pragma unroll
-    for (int j = 0; j < 64; j++) sc[j] = use ? Sc[j * 128] : 0.f;
+    // ---- S <- al D + S(C|0) for this thread's 64 rows, S(C|0) from the
+    // pair's slots (rows 32 j .. 32 j + 31 in slot q + j); RN(S) back to
+    // TMEM A, the exact S to S_out where needed
     // the next segment's first group is prepared (and visible) past here
     if (has_seam) __syncthreads();
     // the exact state is needed after this segment if it is the last one or
     // if the next one runs a register-path group
     const bool keep = last || slot_next < 0 || c.groups > 1 || (has_seam && sm.gc[gq_next & 1].alast < AL_MIN);
     wait_mma();
-    if (tid == 0 && !aborted(sm)) {
-      // this pair's four slots are free: refill them, and warm L2 with the
-      // pair of the segment after next
-      for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
-      prefetch_pair(p, c, seg + 2);
-    }
+    // (the copies are issued on every applied pair, aborted or not, and always land)
+    if (!tc::mbar_wait(&sm.sc_full, npair & 1, DRAIN_LIMIT)) fail(sm, p);
+    npair++;
+    if (tid == 0) refill_pending = true;  // at the top of the next segment, after every read of the slots
+    const bool use = !aborted(sm);
     if (use) {
+      const float *sc0 = reinterpret_cast<const float *>(sm.slot[(q + 2 * hf) % NSLOT]) + n;
+      const float *sc1 = reinterpret_cast<const float *>(sm.slot[(q + 2 * hf + 1) % NSLOT]) + n;
 #pragma unroll
       for (int b = 0; b < 4; b++) {
         uint32_t r[16];
         tc::tmem_ld16(tDh + 16 * b, r);
+        float sc[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) sc[j] = (b < 2 ? sc0 : sc1)[(16 * (b & 1) + j) * 128];
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; j++) {
-          const float x = fmaf(al, __uint_as_float(r[j]), sc[16 * b + j]);
+          const float x = fmaf(al, __uint_as_float(r[j]), sc[j]);
           if (keep) out[(int64_t)(16 * b + j) * 128] = x;
           if (last) bad |= !finite_f(x);
           r[j] = tc::to_tf32(x);
