@@ -163,14 +163,14 @@ __device__ __forceinline__ void prefetch_pair_S(const ComposeParams &p, const Ch
   prefetch_l2(p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128, 128 * 128 * 4);
 }
 
-// both halves of segment seg's pair (T_C and S(C|0), 64 KiB each) into L2
-__device__ __forceinline__ void prefetch_pair(const ComposeParams &p, const Chain &c, int seg) {
+// T_C of segment seg's pair (64 KiB) into L2.  Warming S(C|0) as well, or
+// warming further ahead, measured slower on the warm-prompt workload: the
+// extra L2 footprint of 300 chains evicts lines before they are used.
+__device__ __forceinline__ void prefetch_T(const ComposeParams &p, const Chain &c, int seg) {
   if (seg >= c.n_seg) return;
   const int slot = pair_slot(p, c, seg);
   if (slot < 0) return;
-  const int64_t off = ((int64_t)slot * p.h_v + c.h) * 128 * 128;
-  prefetch_l2(p.T_pool + off, 128 * 128 * 4);
-  prefetch_l2(p.S_pool + off, 128 * 128 * 4);
+  prefetch_l2(p.T_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128, 128 * 128 * 4);
 }
 
 __global__ void __launch_bounds__(NT, 2)
@@ -453,7 +453,17 @@ __global__ void __launch_bounds__(NT, 2)
 // skipped pair update the exact state (kept in S_out) instead.  Everything
 // that depends on the seam tokens only (the [K;Q] operand tile, the decayed
 // Grams, M) is prepared by warps 5..7 while warps 0..3 run the previous
-// group's recurrence; warp 4 issues the MMAs and the seam copies.
+// group's recurrence; warp 4 issues the T_C S0 product and the seam copies.
+//
+// Issue and data movement.  One tcgen05.mma takes tens of cycles to issue,
+// so the 32 small products of a fused group (S0^T [K;Q]^T and T_C [K;Q]^T,
+// K = 128 in steps of 8) are issued by lane 0 of warps 4..7, one K-slab each,
+// into separate partial accumulators that the readers sum.  Once the T_C S0
+// product is complete, the pair's S(C|0) (64 KiB, contiguous in the pool)
+// is bulk-copied into the four slots its T_C K-slabs have just freed and the
+// epilogue reads it from shared memory; the slots take the next pair's
+// K-slabs at the top of the next segment.  Only T_C is warmed in L2, one
+// segment ahead.
 // ---------------------------------------------------------------------------
 constexpr int GW = 8;             // seam tokens per group
 constexpr int NT2 = 256;          // threads per CTA: two per state column (rows 0..63, 64..127)
@@ -728,7 +738,7 @@ __global__ void __launch_bounds__(NT2, 2)
   if (tid == 0) {
     tc::prefetch_tmap(&tmap_T);
     for (; issued < (uint32_t)NSLOT && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued);
-    for (int s = 0; s < 2; s++) prefetch_pair(p, c, s);
+    for (int s = 0; s < 2; s++) prefetch_T(p, c, s);
   }
   if (warp == ISSUER_WARP) {
     for (int g = 0; g < raw_issued; g++) issue_raw_warp<GDN>(sm, p, c, g);
@@ -902,11 +912,12 @@ __global__ void __launch_bounds__(NT2, 2)
 
     if (tid == 0 && refill_pending) {
       // the last pair's slots (T_C, then S(C|0)) are free: refill them, and
-      // warm L2 with the pair of the segment after this one
+      // warm L2 with the next segment's T_C (S(C|0) streams from HBM by its
+      // bulk copies)
       refill_pending = false;
       if (!aborted(sm)) {
         for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
-        prefetch_pair(p, c, seg + 1);
+        prefetch_T(p, c, seg + 1);
       }
     }
     const int slot = slot_next;  // uniform
@@ -978,7 +989,7 @@ __global__ void __launch_bounds__(NT2, 2)
       // through the ring
       if (tid == 0 && !aborted(sm) && wait_slabs(q)) {
         for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
-        prefetch_pair(p, c, seg + 2);
+        prefetch_T(p, c, seg + 2);
       }
       if (preper && !last && has_seam) prepare(gq_next);
       tc::tc_fence_before();
