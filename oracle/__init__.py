@@ -167,6 +167,45 @@ def merge(*a, **kw):
     return default().merge(*a, **kw)
 
 
+def rerotation_matrix(d_k, delta, rot_dim, layout="interleaved", base=10000.0):
+    """R(delta) for the state re-rotation patch (HYPIC news pages §2.1, last
+    paragraph: variants with RoPE re-rotate the cached state; the pages give
+    no formula).  Reading used here: rotary position embedding rotates key
+    channel pairs by the angle (position x theta_i), theta_i =
+    base^(-2i / rot_dim), i < rot_dim / 2; moving a segment by delta positions
+    therefore multiplies every key by the block-diagonal R(delta) below.
+    Pairs are (2i, 2i + 1) ("interleaved") or (i, i + rot_dim / 2) ("half");
+    channels >= rot_dim are not rotated.  Each pair block is
+    [[cos phi, -sin phi], [sin phi, cos phi]], phi = delta theta_i."""
+    R = np.eye(d_k)
+    h = rot_dim // 2
+    for i in range(h):
+        phi = float(delta) * base ** (-2.0 * i / rot_dim)
+        c, s = np.cos(phi), np.sin(phi)
+        a, b = (2 * i, 2 * i + 1) if layout == "interleaved" else (i, i + h)
+        R[a, a], R[a, b], R[b, a], R[b, b] = c, -s, s, c
+    return R
+
+
+def rerotate(variant, T, S, deltas, rot_dim, layout="interleaved", base=10000.0):
+    """State re-rotation of cached pairs moved by deltas[m] positions: with
+    keys k' = R k every token transition of a scalar-gated variant becomes
+    R T_t R^T and every write R U_t, so the pair becomes
+    (R T_C R^T, R S(C|0)).  T: dense [n, h_v, d_k, d_k] (gdn, deltanet) or
+    scalar [n, h_v] (scalar, ungated; unchanged); S: [n, h_v, d_k, d_v]."""
+    T, S = _f64(T), _f64(S)
+    d_k = S.shape[-2]
+    To, So = T.copy(), np.empty_like(S)
+    for m, dl in enumerate(np.asarray(deltas).reshape(-1)):
+        R = rerotation_matrix(d_k, dl, rot_dim, layout, base)
+        So[m] = R @ S[m]
+        if variant in ("gdn", "deltanet"):
+            To[m] = R @ T[m] @ R.T
+        elif variant not in ("scalar", "ungated"):
+            raise ValueError(f"re-rotation is exact only for scalar gates, not {variant}")
+    return To, So
+
+
 def naive_sum(S_pairs):
     """The straw man the pages reject: sum of zero-initial final states over
     the segment axis (axis -4 of [.., n_seg, h_v, d_k, d_v])."""

@@ -25,6 +25,11 @@ the oracle with a planted mistake) and raises AssertionError on failure.
   prefix_free       a segment's pair does not depend on the tokens before it
   naive_wrong       (slow) with decay the naive sum is off by >= 10% of the
                     state norm on every head of the RetNet workload
+  rerotation_keys   re-rotating a pair by R(delta) equals building the pair
+                    from keys rotated by R(delta) (GDN, DeltaNet, RetNet,
+                    ungated; both channel pairings, partial rotary dim)
+  rerotation_group  R(0) = I, R orthogonal, re-rotation by d1 then d2 equals
+                    re-rotation by d1 + d2, norms and spectra preserved
 """
 from __future__ import annotations
 
@@ -266,5 +271,53 @@ def naive_wrong(orc, min_err=0.10):
     return errs
 
 
+def rerotation_keys(orc, rerotate=None):
+    """The pair of a segment whose keys are all multiplied by R(delta) is the
+    re-rotated pair: every token transition becomes R T_t R^T and every write
+    R U_t.  Checked against the oracle's token-by-token build, one delta per
+    segment (negative, zero, large), with the rotary dim below d_k."""
+    import oracle
+    rerotate = rerotate or oracle.rerotate
+    lens = [5, 7, 1, 7]
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    deltas = [3, -7, 0, 12345]
+    h_k, h_v, d_k, d_v = 2, 4, 6, 3
+    for vi, var in enumerate(("gdn", "deltanet", "scalar", "ungated")):
+        k, v, q, g, beta = tiny_inputs(var, int(off[-1]), h_k, h_v, d_k, d_v, 300 + vi)
+        T, S = orc.build_pairs(var, off, 0, h_k, h_v, d_k, d_v, k, v, g, beta)
+        for layout, rot in (("interleaved", 6), ("interleaved", 4), ("half", 4), ("half", 6)):
+            kr = k.copy()
+            for i, dl in enumerate(deltas):
+                R = oracle.rerotation_matrix(d_k, dl, rot, layout, base=50.0)
+                kr[off[i]:off[i + 1]] = np.einsum("ab,thb->tha", R, k[off[i]:off[i + 1]])
+            T2, S2 = orc.build_pairs(var, off, 0, h_k, h_v, d_k, d_v, kr, v, g, beta)
+            To, So = rerotate(var, T, S, deltas, rot, layout, base=50.0)
+            assert _rel(To, T2) < TIGHT, (var, layout, rot, "T")
+            assert _rel(So, S2) < TIGHT, (var, layout, rot, "S")
+
+
+def rerotation_group(orc, rerotate=None):
+    import oracle
+    rerotate = rerotate or oracle.rerotate
+    rng = np.random.default_rng(11)
+    d_k, d_v = 8, 5
+    T = rng.standard_normal((3, 2, d_k, d_k))
+    S = rng.standard_normal((3, 2, d_k, d_v))
+    for layout in ("interleaved", "half"):
+        R = oracle.rerotation_matrix(d_k, 777, d_k, layout)
+        assert np.abs(R @ R.T - np.eye(d_k)).max() < TIGHT
+        assert np.abs(oracle.rerotation_matrix(d_k, 0, d_k, layout) - np.eye(d_k)).max() == 0.0
+        d1, d2 = np.array([5, -40, 900]), np.array([-3, 41, 77])
+        Ta, Sa = rerotate("gdn", *rerotate("gdn", T, S, d1, d_k, layout), d2, d_k, layout)
+        Tb, Sb = rerotate("gdn", T, S, d1 + d2, d_k, layout)
+        assert _rel(Ta, Tb) < 1e-11 and _rel(Sa, Sb) < 1e-11, layout
+        To, So = rerotate("gdn", T, S, d1, d_k, layout)
+        assert abs(np.linalg.norm(So) - np.linalg.norm(S)) < TIGHT * np.linalg.norm(S)
+        ev0 = np.sort_complex(np.linalg.eigvals(T[1, 0]))
+        ev1 = np.sort_complex(np.linalg.eigvals(To[1, 0]))
+        assert np.abs(ev0 - ev1).max() < 1e-9, layout
+
+
 FAST_PINS = (dense_product, outputs, composition, composition_all, split_merge, ungated_sum,
-             retnet_closed, householder, contraction, cross_variant, prefix_free)
+             retnet_closed, householder, contraction, cross_variant, prefix_free, rerotation_keys,
+             rerotation_group)

@@ -73,3 +73,23 @@ def test_pins_catch_planted_mistakes(tmp_path):
             except AssertionError:
                 caught.append(pin.__name__)
         assert caught, f"planted mistake '{name}' passed every pin"
+
+
+def _rerotate_mutant(form):
+    """oracle.rerotate with one planted mistake in the transformation."""
+    def rr(variant, T, S, deltas, rot_dim, layout="interleaved", base=10000.0):
+        T, S = np.array(T, dtype=np.float64), np.array(S, dtype=np.float64)
+        To, So = T.copy(), np.empty_like(S)
+        for m, dl in enumerate(np.asarray(deltas).reshape(-1)):
+            R = oracle.rerotation_matrix(S.shape[-2], dl, rot_dim, layout, base)
+            So[m] = (R.T if form == "S by R^T" else R) @ S[m]
+            if variant in ("gdn", "deltanet"):
+                To[m] = {"T by R only": R @ T[m], "T by R^T T R": R.T @ T[m] @ R}.get(form, R @ T[m] @ R.T)
+        return To, So
+    return rr
+
+
+@pytest.mark.parametrize("form", ["T by R only", "T by R^T T R", "S by R^T"])
+def test_rerotation_pins_catch_planted_mistakes(orc, form):
+    with pytest.raises(AssertionError):
+        pins.rerotation_keys(orc, rerotate=_rerotate_mutant(form))
