@@ -292,6 +292,26 @@ def merge_row(dev, hy, peaks, comp):
             "kernel": "tensor-core pair merge (split tf32)"}
 
 
+def rerotate_row(dev, hy, peaks, comp):
+    """State re-rotation of the whole warm-prompt pool in place (every layer's
+    100 segments moved by a random shift, RoPE pairs (i, i + 64), all 128
+    channels): each pool byte read once and written once, 4 x 64 KiB per
+    (slot, head)."""
+    import torch
+    W = comp["W"]
+    n = comp["n_layers"] * W.n_seg
+    slots = torch.arange(n, dtype=torch.int32, device=dev)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    deltas = torch.randint(-100000, 100000, (n,), generator=gen, dtype=torch.int64).to(dev)
+    ms = _time_ms(lambda: hy.pair_rerotate(slots, slots, deltas, comp["T_pool"], comp["S_pool"], comp["T_pool"],
+                                           comp["S_pool"], variant="gdn", rot_dim=W.d_k, layout="half"))
+    nbytes = n * W.h_v * 4 * W.d_k * W.d_v * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": ms, "algorithmic_bytes": nbytes,
+            "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"]},
+            "kernel": "pair re-rotation (fp32, in place)"}
+
+
 def compose_variant_rows(dev, hy, peaks, n_layers=8):
     """The compose of the other dense-transition variants on the warm-prompt
     shape (8 layers x 32 heads x 100 segments, w = 8): DeltaNet (tensor-core
@@ -611,6 +631,8 @@ def main():
     if rank == 0 and not args.no_rows:
         rows = {f"merge: {comp['n_layers']} layers x {W4.h_v} heads x {W4.n_seg // 2} adjacent segment pairs":
                 merge_row(dev, hy, peaks, comp)}
+        rows[f"re-rotation: {comp['n_layers']} layers x {W4.n_seg} segments x {W4.h_v} heads, in place"] = \
+            rerotate_row(dev, hy, peaks, comp)
         rows.update(compose_variant_rows(dev, hy, peaks))
         rows.update(measure_rows(dev, hy, peaks))
 

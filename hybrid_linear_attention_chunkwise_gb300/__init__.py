@@ -67,9 +67,20 @@ class MergeDesc(ctypes.Structure):
                 ("T_a", P), ("S_a", P), ("T_b", P), ("S_b", P), ("T_out", P), ("S_out", P), ("status", P)]
 
 
+class RerotateDesc(ctypes.Structure):
+    _fields_ = [("n_items", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("variant", ctypes.c_int32), ("rot_dim", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("base", ctypes.c_double),
+                ("slot_in", P), ("slot_out", P), ("delta", P),
+                ("n_slots_in", ctypes.c_int64), ("n_slots_out", ctypes.c_int64),
+                ("T_in", P), ("S_in", P), ("T_out", P), ("S_out", P), ("status", P)]
+
+
+ROPE_LAYOUT = {"interleaved": 0, "half": 1}
+
 SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_workspace_bytes", "hypic_compose",
-           "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_plan_lpt", "hypic_status_from_word",
-           "hypic_status_string", "hypic_version")
+           "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_pair_rerotate", "hypic_plan_lpt",
+           "hypic_status_from_word", "hypic_status_string", "hypic_version")
 
 
 class HypicError(RuntimeError):
@@ -102,6 +113,8 @@ def load():
             lib.hypic_compose_workspace_bytes.restype = ctypes.c_size_t
             lib.hypic_pair_merge.argtypes = [ctypes.POINTER(MergeDesc), P]
             lib.hypic_pair_merge.restype = ctypes.c_int
+            lib.hypic_pair_rerotate.argtypes = [ctypes.POINTER(RerotateDesc), P]
+            lib.hypic_pair_rerotate.restype = ctypes.c_int
             lib.hypic_plan_lpt.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P]
             lib.hypic_plan_lpt.restype = ctypes.c_int
             lib.hypic_status_from_word.argtypes = [ctypes.c_uint32]
@@ -307,6 +320,37 @@ def pair_merge(later, earlier, out, T_a, S_a, T_out, S_out, *, variant: str, T_b
     rc = lib.hypic_pair_merge(ctypes.byref(d), _stream(stream))
     if rc != OK:
         raise HypicError(rc, "hypic_pair_merge")
+
+
+def pair_rerotate(slot_in, slot_out, delta, T_in, S_in, T_out, S_out, *, variant: str, rot_dim: int,
+                  layout: str = "interleaved", base: float = 10000.0, status=None, stream=None):
+    """hypic_pair_rerotate on torch tensors: the pair in slot_in[m] of a
+    segment moved by delta[m] positions, re-rotated into slot_out[m]:
+    T_out = R T_in R^T, S_out = R S_in with R = R(delta[m]) the rotary
+    rotation of the key channels (pairs per `layout`, the first rot_dim
+    channels, theta_i = base^(-2i / rot_dim)).  slot_in / slot_out int32
+    [n_items], delta int64 [n_items] (device); the output pool may be the
+    input pool (in place)."""
+    lib = load()
+    for name, t in (("slot_in", slot_in), ("slot_out", slot_out)):
+        _check(t, name, dtype=torch.int32, ndim=1)
+    _check(delta, "delta", dtype=torch.int64, ndim=1)
+    for name, t in (("S_in", S_in), ("S_out", S_out)):
+        _check(t, name, dtype=torch.float32, ndim=4)
+    d = RerotateDesc()
+    d.n_items = slot_in.shape[0]
+    _, d.h_v, d.d_k, d.d_v = S_in.shape
+    d.variant = VARIANT[variant]
+    d.rot_dim = int(rot_dim)
+    d.layout = ROPE_LAYOUT[layout]
+    d.base = float(base)
+    d.slot_in, d.slot_out, d.delta = _ptr(slot_in), _ptr(slot_out), _ptr(delta)
+    d.n_slots_in, d.n_slots_out = S_in.shape[0], S_out.shape[0]
+    d.T_in, d.S_in, d.T_out, d.S_out = _ptr(T_in), _ptr(S_in), _ptr(T_out), _ptr(S_out)
+    d.status = _ptr(status)
+    rc = lib.hypic_pair_rerotate(ctypes.byref(d), _stream(stream))
+    if rc != OK:
+        raise HypicError(rc, "hypic_pair_rerotate")
 
 
 def compose_span_parallel(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str,

@@ -333,4 +333,47 @@ int hypic_pair_merge(const hypic_merge_desc *d, hypic_stream_t stream) {
   return HYPIC_OK;
 }
 
+int hypic_pair_rerotate(const hypic_rerotate_desc *d, hypic_stream_t stream) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_items < 0 || d->h_v < 1 || d->d_k < 1 || d->d_v < 1) return HYPIC_ERR_INVALID_ARG;
+  if (d->variant < HYPIC_GDN || d->variant > HYPIC_DIAG_GATE) return HYPIC_ERR_INVALID_ARG;
+  if (d->layout != HYPIC_ROPE_INTERLEAVED && d->layout != HYPIC_ROPE_HALF) return HYPIC_ERR_INVALID_ARG;
+  if (d->rot_dim < 2 || (d->rot_dim & 1) || d->rot_dim > d->d_k) return HYPIC_ERR_INVALID_ARG;
+  if (d->layout == HYPIC_ROPE_HALF && (d->rot_dim % 8) != 0) return HYPIC_ERR_INVALID_ARG;
+  if (!(d->base > 0.0)) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_slots_in < 0 || d->n_slots_out < 0) return HYPIC_ERR_INVALID_ARG;
+  // per-channel and diagonal gates do not commute with the rotation
+  if (d->variant == HYPIC_CHANNEL_DELTA || d->variant == HYPIC_DIAG_GATE) return HYPIC_ERR_UNSUPPORTED;
+  if (d->d_k > 128 || d->d_v > 128 || (d->d_k % 4) != 0 || (d->d_v % 4) != 0) return HYPIC_ERR_UNSUPPORTED;
+  if ((int64_t)d->n_items * ((d->h_v + 3) / 4) > INT32_MAX) return HYPIC_ERR_UNSUPPORTED;
+  if (d->n_items == 0) return HYPIC_OK;
+  if (!d->slot_in || !d->slot_out || !d->delta || !aligned(d->slot_in, 4) || !aligned(d->slot_out, 4) ||
+      !aligned(d->delta, 8))
+    return HYPIC_ERR_INVALID_ARG;
+  const float *pools[4] = {d->T_in, d->S_in, d->T_out, d->S_out};
+  for (const float *q : pools)
+    if (!q || !aligned(q, 16)) return HYPIC_ERR_INVALID_ARG;
+  RerotateParams p{};
+  p.n_items = d->n_items;
+  p.h_v = d->h_v;
+  p.d_k = d->d_k;
+  p.d_v = d->d_v;
+  p.variant = d->variant;
+  p.rot_dim = d->rot_dim;
+  p.layout = d->layout;
+  p.base = d->base;
+  p.slot_in = d->slot_in;
+  p.slot_out = d->slot_out;
+  p.delta = d->delta;
+  p.n_slots_in = d->n_slots_in;
+  p.n_slots_out = d->n_slots_out;
+  p.T_in = d->T_in;
+  p.S_in = d->S_in;
+  p.T_out = d->T_out;
+  p.S_out = d->S_out;
+  p.status = d->status;
+  if (launch_rerotate(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return HYPIC_ERR_CUDA;
+  return HYPIC_OK;
+}
+
 }  // extern "C"

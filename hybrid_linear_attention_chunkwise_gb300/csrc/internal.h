@@ -57,6 +57,17 @@ struct ComposeParams {
   uint32_t *status;
 };
 
+struct RerotateParams {
+  int32_t n_items, h_v, d_k, d_v, variant, rot_dim, layout;
+  double base;
+  const int32_t *slot_in, *slot_out;
+  const int64_t *delta;
+  int64_t n_slots_in, n_slots_out;
+  const float *T_in, *S_in;
+  float *T_out, *S_out;
+  uint32_t *status;
+};
+
 struct MergeParams {
   int32_t n_merge, h_v, d_k, d_v, variant;
   const int32_t *later, *earlier, *out;
@@ -106,6 +117,7 @@ bool make_tmap_f32_rows(CUtensorMap *map, const float *base, uint64_t rows, uint
 // pools, fp32 CUDA-core kernel otherwise.
 bool merge_tc_supported(const MergeParams &p);
 cudaError_t launch_merge(const MergeParams &p, uint32_t wait_limit, cudaStream_t s);
+cudaError_t launch_rerotate(const RerotateParams &p, cudaStream_t s);
 cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s);
 // The tensor-core compose covers dense transitions, bf16 seam tokens,

@@ -237,6 +237,53 @@ typedef struct {
 int hypic_pair_merge(const hypic_merge_desc *d, hypic_stream_t stream);
 
 /*
+ * hypic_pair_rerotate -- state re-rotation of cached pairs for segments that
+ * are reused at a shifted position (pages §2.1, last paragraph: for variants
+ * with RoPE the cached state is re-rotated; the pages give no formula).
+ * Reading used: rotary position embedding multiplies every key by block-
+ * diagonal 2 x 2 rotations, pair i turning by (position x theta_i) with
+ * theta_i = base^(-2i / rot_dim), i < rot_dim / 2.  A segment moved by delta
+ * positions therefore has all its keys multiplied by R(delta); every token
+ * transition of a scalar-gated variant becomes R T_t R^T and every write
+ * R U_t, so for item m (i = slot_in[m], o = slot_out[m], R = R(delta[m])):
+ *   T_out[o, h] = R T_in[i, h] R^T,   S_out[o, h] = R S_in[i, h]
+ * for every value head h.  Channel pairs are (2i, 2i + 1) for
+ * HYPIC_ROPE_INTERLEAVED and (i, i + rot_dim / 2) for HYPIC_ROPE_HALF;
+ * channels >= rot_dim are not rotated.  rot_dim is even, 2 <= rot_dim <= d_k
+ * (HYPIC_ROPE_HALF: a multiple of 8).
+ * Variants: GDN and DELTANET (dense T [slots, h_v, d_k, d_k]); SCALAR_DECAY
+ * and UNGATED (scalar T [slots, h_v], copied unchanged).  Per-channel and
+ * diagonal gates do not commute with R, so the patch is not exact for them:
+ * HYPIC_ERR_UNSUPPORTED.  S pools are [slots, h_v, d_k, d_v]; all fp32;
+ * d_k and d_v are multiples of 4, at most 128.
+ * The angles are formed in fp64 (exact for |delta| < 2^53), the rotation in
+ * fp32.  slot_out[m] may equal slot_in[m] in the same pool (in place): each
+ * (slot, head) block is read whole before it is written.  Items must not
+ * share an output slot, nor read a slot that another item of the call
+ * writes (results are undefined otherwise).  An item with a slot out of
+ * range is skipped and reported (HYPIC_STATUS_BAD_SLOT).
+ */
+typedef enum { HYPIC_ROPE_INTERLEAVED = 0, HYPIC_ROPE_HALF = 1 } hypic_rope_layout;
+
+typedef struct {
+  int32_t n_items;
+  int32_t h_v, d_k, d_v;
+  int32_t variant;
+  int32_t rot_dim;
+  int32_t layout;             /* hypic_rope_layout */
+  double base;                /* > 0 (10000 in the common RoPE setting) */
+  const int32_t *slot_in;     /* [dev] [n_items] pair to re-rotate */
+  const int32_t *slot_out;    /* [dev] [n_items] where the result goes */
+  const int64_t *delta;       /* [dev] [n_items] position shift (new start - cached start) */
+  int64_t n_slots_in, n_slots_out;
+  const float *T_in, *S_in;   /* [dev] input pool */
+  float *T_out, *S_out;       /* [dev] output pool (may be the input pool) */
+  uint32_t *status;           /* [dev] optional */
+} hypic_rerotate_desc;
+
+int hypic_pair_rerotate(const hypic_rerotate_desc *d, hypic_stream_t stream);
+
+/*
  * hypic_plan_lpt -- greedy longest-processing-time-first packing of items
  * over workers (pages §2.3: LPT balancing of segments over scatter workers).
  * Items are taken in order of decreasing cost (ties: lower index first) and

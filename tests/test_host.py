@@ -190,6 +190,31 @@ def test_merge_rejects_bad_descriptors():
     assert lib.hypic_pair_merge(ctypes.byref(desc(n_merge=0, later=None, T_a=None)), None) == 0
 
 
+def test_rerotate_rejects_bad_descriptors():
+    lib = hy.load()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def desc(**over):
+        d = hy.RerotateDesc()
+        d.n_items, d.h_v, d.d_k, d.d_v, d.variant = 2, 4, 128, 128, hy.GDN
+        d.rot_dim, d.layout, d.base = 128, 0, 10000.0
+        d.slot_in = d.slot_out = d.delta = d.T_in = d.S_in = d.T_out = d.S_out = fake
+        d.n_slots_in, d.n_slots_out = 4, 4
+        for k, v in over.items():
+            setattr(d, k, v)
+        return d
+    for over, want in [(dict(n_items=-1), 1), (dict(slot_in=None), 1), (dict(delta=None), 1),
+                       (dict(T_out=None), 1), (dict(S_in=None), 1), (dict(variant=9), 1), (dict(h_v=0), 1),
+                       (dict(rot_dim=0), 1), (dict(rot_dim=7), 1), (dict(rot_dim=130), 1), (dict(layout=2), 1),
+                       (dict(layout=1, rot_dim=12), 1), (dict(base=0.0), 1), (dict(base=float("nan")), 1),
+                       (dict(n_slots_in=-1), 1), (dict(d_k=200, rot_dim=128), 2), (dict(d_v=126), 2),
+                       (dict(variant=hy.VARIANT["channel"]), 2), (dict(variant=hy.VARIANT["diag"]), 2),
+                       (dict(delta=ctypes.c_void_p((1 << 20) + 4)), 1),
+                       (dict(S_out=ctypes.c_void_p((1 << 20) + 4)), 1)]:
+        assert lib.hypic_pair_rerotate(ctypes.byref(desc(**over)), None) == want, over
+    assert lib.hypic_pair_rerotate(ctypes.byref(desc(n_items=0, slot_in=None, T_in=None)), None) == 0
+
+
 def test_binding_refuses_host_tensors():
     with pytest.raises(ValueError):
         hy._ptr(torch.zeros(4))
