@@ -372,7 +372,7 @@ int hypic_pair_rerotate(const hypic_rerotate_desc *d, hypic_stream_t stream) {
   p.T_out = d->T_out;
   p.S_out = d->S_out;
   p.status = d->status;
-  if (launch_rerotate(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (launch_rerotate(p, wait_limit(), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return HYPIC_ERR_CUDA;
   return HYPIC_OK;
 }
 

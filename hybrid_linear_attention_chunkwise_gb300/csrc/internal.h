@@ -117,7 +117,7 @@ bool make_tmap_f32_rows(CUtensorMap *map, const float *base, uint64_t rows, uint
 // pools, fp32 CUDA-core kernel otherwise.
 bool merge_tc_supported(const MergeParams &p);
 cudaError_t launch_merge(const MergeParams &p, uint32_t wait_limit, cudaStream_t s);
-cudaError_t launch_rerotate(const RerotateParams &p, cudaStream_t s);
+cudaError_t launch_rerotate(const RerotateParams &p, uint32_t wait_limit, cudaStream_t s);
 cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s);
 // The tensor-core compose covers dense transitions, bf16 seam tokens,

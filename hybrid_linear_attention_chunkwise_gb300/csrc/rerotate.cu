@@ -15,50 +15,72 @@
 // channel pairs, so each (slot, head) block is staged whole in shared memory
 // and then written: the operation may run in place.
 //
-// One CTA per (item, group of HPC value heads): the angle table is formed
-// once per CTA in fp64 (pow and sincos of the library; the shift is exact up
-// to 2^53) and rounded to fp32; the data is moved with 16-byte loads and
-// stores.  This is a bandwidth-bound kernel: each pool byte is read once and
-// written once.
+// One CTA per (item, group of HPC value heads), one CTA per SM: the angle
+// table is formed once per CTA in fp64 (pow and sincos of the library; the
+// shift is exact up to 2^53) and rounded to fp32, while the first blocks are
+// already in flight.  The CTA's blocks (T then S of each head) stream through
+// a ring of NBUF shared-memory buffers by 1-D bulk copies, two blocks ahead
+// of the one being rotated; results leave by 16-byte stores.  This is a
+// bandwidth-bound kernel: each pool byte is read once and written once.
+// Every wait is bounded (HYPIC_STATUS_TIMEOUT; copies in flight are drained
+// before the CTA exits).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace hypic {
 
 namespace {
 
-constexpr int NT = 256;  // threads per CTA
-constexpr int HPC = 4;   // value heads per CTA
+constexpr int NT = 256;    // threads per CTA
+constexpr int HPC = 8;     // value heads per CTA
+constexpr int NBUF = 3;    // block buffers (two blocks in flight ahead)
+constexpr uint32_t DRAIN_LIMIT = 1u << 22;
 
-struct RerotSmem {
-  float buf[128 * 128];  // one (slot, head) block of T or S
+struct __align__(128) RerotSmem {
+  float buf[NBUF][128 * 128];  // (slot, head) blocks of T or S
   float C[128], G[128];
   int P[128];
+  uint64_t full[NBUF];
 };
 
-// stage rows x cols (cols a multiple of 4) of src into buf, 16 bytes a time
-__device__ __forceinline__ void stage(float *buf, const float *src, int n4) {
-  const float4 *s4 = reinterpret_cast<const float4 *>(src);
-  float4 *b4 = reinterpret_cast<float4 *>(buf);
-  for (int i = threadIdx.x; i < n4; i += NT) b4[i] = s4[i];
-}
-
-__global__ void __launch_bounds__(NT) rerotate_kernel(const RerotateParams p) {
+__global__ void __launch_bounds__(NT, 1) rerotate_kernel(const RerotateParams p, uint32_t lim) {
   extern __shared__ unsigned char smem_raw[];
-  RerotSmem &sm = *reinterpret_cast<RerotSmem *>(smem_raw);
+  RerotSmem &sm = *reinterpret_cast<RerotSmem *>(smem_raw + ((128u - (tc::smem_u32(smem_raw) & 127u)) & 127u));
+  const int tid = threadIdx.x;
   const int hgroups = (p.h_v + HPC - 1) / HPC;
   const int m = blockIdx.x / hgroups;
   const int h0 = (blockIdx.x % hgroups) * HPC;
   const int si = p.slot_in[m], so = p.slot_out[m];
   if (si < 0 || si >= p.n_slots_in || so < 0 || so >= p.n_slots_out) {
-    if (threadIdx.x == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
+    if (tid == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
     return;
   }
   const int dk = p.d_k, dv = p.d_v;
-  // the channel table of R(delta)
-  if (threadIdx.x < dk) {
-    const int a = threadIdx.x;
+  const bool dense = p.variant == HYPIC_GDN || p.variant == HYPIC_DELTANET;
+  const int per_head = dense ? 2 : 1;  // blocks per head: T and S, or S
+  const int nj = min(HPC, p.h_v - h0) * per_head;
+  auto is_T = [&](int j) { return dense && (j % per_head) == 0; };
+  auto head = [&](int j) { return h0 + j / per_head; };
+  // block j of this CTA into buffer j % NBUF (thread 0)
+  auto issue = [&](int j) {
+    if (j >= nj) return;
+    const int h = head(j);
+    const float *src = is_T(j) ? p.T_in + ((int64_t)si * p.h_v + h) * dk * dk
+                               : p.S_in + ((int64_t)si * p.h_v + h) * dk * dv;
+    const uint32_t bytes = (uint32_t)(is_T(j) ? dk * dk : dk * dv) * 4u;
+    tc::mbar_expect_tx(&sm.full[j % NBUF], bytes);
+    tc::bulk_load(sm.buf[j % NBUF], src, bytes, &sm.full[j % NBUF]);
+  };
+  if (tid == 0) {
+    for (int b = 0; b < NBUF; b++) tc::mbar_init(&sm.full[b], 1);
+    tc::fence_mbar_init();
+    for (int j = 0; j < NBUF - 1; j++) issue(j);
+  }
+  // the channel table of R(delta), while the first blocks land
+  if (tid < dk) {
+    const int a = tid;
     const int h = p.rot_dim / 2;
     float c = 1.f, g = 0.f;
     int partner = a;
@@ -83,60 +105,73 @@ __global__ void __launch_bounds__(NT) rerotate_kernel(const RerotateParams p) {
     sm.G[a] = g;
     sm.P[a] = partner;
   }
-  const bool dense = p.variant == HYPIC_GDN || p.variant == HYPIC_DELTANET;
-  for (int hh = 0; hh < HPC; hh++) {
-    const int h = h0 + hh;
-    if (h >= p.h_v) break;
-    if (dense) {
-      __syncthreads();  // table written / previous block consumed
-      stage(sm.buf, p.T_in + ((int64_t)si * p.h_v + h) * dk * dk, dk * dk / 4);
-      __syncthreads();
+  if (!dense && tid < min(HPC, p.h_v - h0))  // gamma^L I commutes with R
+    p.T_out[(int64_t)so * p.h_v + h0 + tid] = p.T_in[(int64_t)si * p.h_v + h0 + tid];
+  __syncthreads();  // table and barrier init visible
+
+  bool ok = true;
+  int first_fail = nj;  // thread 0: the first block whose wait ran out
+  for (int j = 0; j < nj; j++) {
+    // buffer (j + NBUF - 1) % NBUF was last read in iteration j - 1; after a
+    // wait has run out no further copy is issued
+    if (tid == 0 && ok) issue(j + NBUF - 1);
+    ok = ok && tc::mbar_wait(&sm.full[j % NBUF], (j / NBUF) & 1, lim);
+    if (!ok && tid == 0 && first_fail == nj) {
+      first_fail = j;
+      report(p.status, HYPIC_STATUS_TIMEOUT);
+    }
+    const float *blk = sm.buf[j % NBUF];
+    const int h = head(j);
+    if (ok && is_T(j)) {
       const int q4 = dk / 4;
-      for (int idx = threadIdx.x; idx < dk * q4; idx += NT) {
+      float *dst = p.T_out + ((int64_t)so * p.h_v + h) * dk * dk;
+      for (int idx = tid; idx < dk * q4; idx += NT) {
         const int a = idx / q4, b0 = 4 * (idx % q4);
         const float ca = sm.C[a], ga = sm.G[a];
-        const float *ra = sm.buf + a * dk, *rp = sm.buf + sm.P[a] * dk;
+        const float *ra = blk + a * dk, *rp = blk + sm.P[a] * dk;
         float o[4];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-          const int b = b0 + j, pb = sm.P[b];
+        for (int jj = 0; jj < 4; jj++) {
+          const int b = b0 + jj, pb = sm.P[b];
           const float cb = sm.C[b], gb = sm.G[b];
           // R[a][a] T[a][.] R[b][.] + R[a][P a] T[P a][.] R[b][.]
           const float top = fmaf(cb, ra[b], gb * ra[pb]);
           const float bot = fmaf(cb, rp[b], gb * rp[pb]);
-          o[j] = fmaf(ca, top, ga * bot);
+          o[jj] = fmaf(ca, top, ga * bot);
         }
-        *reinterpret_cast<float4 *>(p.T_out + ((int64_t)so * p.h_v + h) * dk * dk + a * dk + b0) =
-            make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4 *>(dst + a * dk + b0) = make_float4(o[0], o[1], o[2], o[3]);
       }
-    } else if (threadIdx.x == 0) {
-      p.T_out[(int64_t)so * p.h_v + h] = p.T_in[(int64_t)si * p.h_v + h];  // gamma^L I commutes with R
+    } else if (ok) {
+      const int v4 = dv / 4;
+      float *dst = p.S_out + ((int64_t)so * p.h_v + h) * dk * dv;
+      for (int idx = tid; idx < dk * v4; idx += NT) {
+        const int a = idx / v4, j0 = 4 * (idx % v4);
+        const float ca = sm.C[a], ga = sm.G[a];
+        const float4 x = *reinterpret_cast<const float4 *>(blk + a * dv + j0);
+        const float4 y = *reinterpret_cast<const float4 *>(blk + sm.P[a] * dv + j0);
+        *reinterpret_cast<float4 *>(dst + a * dv + j0) =
+            make_float4(fmaf(ca, x.x, ga * y.x), fmaf(ca, x.y, ga * y.y), fmaf(ca, x.z, ga * y.z),
+                        fmaf(ca, x.w, ga * y.w));
+      }
     }
-    __syncthreads();
-    stage(sm.buf, p.S_in + ((int64_t)si * p.h_v + h) * dk * dv, dk * dv / 4);
-    __syncthreads();
-    const int v4 = dv / 4;
-    for (int idx = threadIdx.x; idx < dk * v4; idx += NT) {
-      const int a = idx / v4, j0 = 4 * (idx % v4);
-      const float ca = sm.C[a], ga = sm.G[a];
-      const float4 x = *reinterpret_cast<const float4 *>(sm.buf + a * dv + j0);
-      const float4 y = *reinterpret_cast<const float4 *>(sm.buf + sm.P[a] * dv + j0);
-      *reinterpret_cast<float4 *>(p.S_out + ((int64_t)so * p.h_v + h) * dk * dv + a * dv + j0) =
-          make_float4(fmaf(ca, x.x, ga * y.x), fmaf(ca, x.y, ga * y.y), fmaf(ca, x.z, ga * y.z),
-                      fmaf(ca, x.w, ga * y.w));
-    }
+    __syncthreads();  // this buffer is free for block j + NBUF
   }
+  // drain: copies issued but not yet seen complete (only after a timeout:
+  // blocks first_fail .. first_fail + NBUF - 1) land before the CTA exits
+  if (tid == 0)
+    for (int j = first_fail; j < nj && j < first_fail + NBUF; j++)
+      tc::mbar_wait(&sm.full[j % NBUF], (j / NBUF) & 1, DRAIN_LIMIT);
 }
 
 }  // namespace
 
-cudaError_t launch_rerotate(const RerotateParams &p, cudaStream_t s) {
+cudaError_t launch_rerotate(const RerotateParams &p, uint32_t wait_limit, cudaStream_t s) {
   const int64_t grid = (int64_t)p.n_items * ((p.h_v + HPC - 1) / HPC);
   if (grid < 1) return cudaSuccess;
-  const int smem = (int)sizeof(RerotSmem);
+  const int smem = (int)sizeof(RerotSmem) + 128;
   cudaError_t e = cudaFuncSetAttribute(rerotate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  rerotate_kernel<<<(unsigned)grid, NT, smem, s>>>(p);
+  rerotate_kernel<<<(unsigned)grid, NT, smem, s>>>(p, wait_limit);
   return cudaGetLastError();
 }
 
