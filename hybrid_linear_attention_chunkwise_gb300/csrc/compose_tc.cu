@@ -958,24 +958,30 @@ __global__ void __launch_bounds__(NT2, 2)
         for (int i = 0; i < GW; i++) cc[i] *= G.eb[i];
         const float al = G.alast;
         const float *bt = &sm.bt[0][0][0] + 1024 * hf;  // K-slabs 2*hf, 2*hf+1 hold this thread's rows
+        // 16 rows at a time: their exact values are loaded together, and
+        // RN(S) of the block goes straight to TMEM A
 #pragma unroll 1
-        for (int rr = 0; rr < 64; rr++) {
-          float x = al * (exact ? exact[(int64_t)rr * 128] : 0.f);
-          const float *row = bt + (rr >> 5) * 512 + (rr & 3);
-          const int chunk = (rr & 31) >> 2;
+        for (int r0 = 0; r0 < 64; r0 += 16) {
+          float ex[16];
 #pragma unroll
-          for (int i = 0; i < GW; i++) x = fmaf(row[i * 32 + ((chunk ^ i) << 2)], cc[i], x);
-          out[(int64_t)rr * 128] = x;
+          for (int j = 0; j < 16; j++) ex[j] = exact ? exact[(int64_t)(r0 + j) * 128] : 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; j++) {
+            const int rr = r0 + j;
+            float x = al * ex[j];
+            const float *row = bt + (rr >> 5) * 512 + (rr & 3);
+            const int chunk = (rr & 31) >> 2;
+#pragma unroll
+            for (int i = 0; i < GW; i++) x = fmaf(row[i * 32 + ((chunk ^ i) << 2)], cc[i], x);
+            out[(int64_t)rr * 128] = x;
+            ex[j] = x;
+          }
+          uint32_t rn[16];
+#pragma unroll
+          for (int j = 0; j < 16; j++) rn[j] = tc::to_tf32(ex[j]);
+          tc::tmem_st16(tAh + r0, rn);
         }
         exact = out;
-        tc::tc_fence_before();  // the D reads above precede the stores to A
-#pragma unroll
-        for (int b = 0; b < 4; b++) {
-          uint32_t r[16];
-#pragma unroll
-          for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(out[(int64_t)(16 * b + j) * 128]);
-          tc::tmem_st16(tAh + 16 * b, r);
-        }
       }
       tc::tmem_wait_st();
       tc::tc_fence_before();
