@@ -14,7 +14,8 @@
 // prompt order:
 //   seam  each seam token scales S by its gates (S <- Diag(a) S), forms the
 //         half-column dot product k^T S[:,n], exchanges it with its partner
-//         through shared memory (one CTA barrier per token), applies the
+//         through shared memory (one 64-thread barrier per token and warp
+//         pair), applies the
 //         rank-1 update and emits o_t[n] = q_t . S[:,n] (partner sums are
 //         written out after the next barrier);
 //   MMA   S is rounded to tf32 and stored to TMEM as the A operand (lane n =
@@ -133,9 +134,11 @@ __device__ __forceinline__ void issue_slab(SM &sm, const ComposeParams &p, const
 }
 
 // k / q / v rows and per-channel gate rows of seam group gq into seam buffer
-// gq % 2; its beta block (all heads, contiguous) is warmed in L2 (thread 0)
-__device__ __forceinline__ void issue_seam(ComposeTcSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
+// gq % 2, one bulk copy per lane of the calling warp (all 32 lanes call:
+// 4 nt <= 32 copies); its beta block (all heads, contiguous) is warmed in L2
+__device__ __forceinline__ void issue_seam_warp(ComposeTcSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
   if (gq >= c.n_seg * c.groups) return;
+  const int lane = threadIdx.x & 31;
   const int seg = gq / c.groups, gi = gq % c.groups;
   const int b = gq & 1;
   SeamBuf &s = sm.seam[b];
@@ -143,17 +146,24 @@ __device__ __forceinline__ void issue_seam(ComposeTcSmem &sm, const ComposeParam
   const int nt = min(SB, c.w - t0);
   const int64_t tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + t0;
   const uint32_t gbytes = (uint32_t)(nt * p.h_v * 4);
-  tc::mbar_expect_tx(&sm.seam_full[b], (uint32_t)nt * (3 * 256 + 512));
-  const __nv_bfloat16 *sk = static_cast<const __nv_bfloat16 *>(p.seam_k);
-  const __nv_bfloat16 *sqp = static_cast<const __nv_bfloat16 *>(p.seam_q);
-  const __nv_bfloat16 *sv = static_cast<const __nv_bfloat16 *>(p.seam_v);
-  for (int t = 0; t < nt; t++) {
-    tc::bulk_load(s.k[t], sk + ((tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.seam_full[b]);
-    tc::bulk_load(s.q[t], sqp + ((tok0 + t) * p.h_k + c.kh) * 128, 256, &sm.seam_full[b]);
-    tc::bulk_load(s.v[t], sv + ((tok0 + t) * p.h_v + c.h) * 128, 256, &sm.seam_full[b]);
-    tc::bulk_load(s.gv[t], p.seam_g + ((tok0 + t) * p.h_v + c.h) * 128, 512, &sm.seam_full[b]);
+  if (lane == 0) tc::mbar_expect_tx(&sm.seam_full[b], (uint32_t)nt * (3 * 256 + 512));
+  __syncwarp();
+  if (lane < 4 * nt) {
+    const int t = lane >> 2, kind = lane & 3;
+    const int64_t tok = tok0 + t;
+    if (kind == 0)
+      tc::bulk_load(s.k[t], static_cast<const __nv_bfloat16 *>(p.seam_k) + (tok * p.h_k + c.kh) * 128, 256,
+                    &sm.seam_full[b]);
+    else if (kind == 1)
+      tc::bulk_load(s.q[t], static_cast<const __nv_bfloat16 *>(p.seam_q) + (tok * p.h_k + c.kh) * 128, 256,
+                    &sm.seam_full[b]);
+    else if (kind == 2)
+      tc::bulk_load(s.v[t], static_cast<const __nv_bfloat16 *>(p.seam_v) + (tok * p.h_v + c.h) * 128, 256,
+                    &sm.seam_full[b]);
+    else
+      tc::bulk_load(s.gv[t], p.seam_g + (tok * p.h_v + c.h) * 128, 512, &sm.seam_full[b]);
   }
-  prefetch_l2(p.seam_beta + tok0 * p.h_v, gbytes);
+  if (lane == 31) prefetch_l2(p.seam_beta + tok0 * p.h_v, gbytes);
 }
 
 __device__ __forceinline__ void prefetch_pair_S(const ComposeParams &p, const Chain &c, int seg) {
@@ -218,15 +228,17 @@ __global__ void __launch_bounds__(NT, 2)
   const uint32_t tD = sm.tmem_base, tA = sm.tmem_base + 128;
 
   uint32_t issued = 0;  // T_C slabs issued (thread 0)
-  int seam_issued = 0;  // seam groups issued (thread 0)
+  constexpr int SEAM_WARP = 7;  // issues the seam copies, one per lane
+  int seam_issued = min(2, total_groups);  // seam groups issued (the seam warp)
   if (tid == 0) {
     tc::prefetch_tmap(&tmap_T);
     for (; issued < (uint32_t)NSLOT && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued);
-    issue_seam(sm, p, c, 0);
-    issue_seam(sm, p, c, 1);
-    seam_issued = min(2, total_groups);
     prefetch_pair_S(p, c, 0);
     prefetch_pair_S(p, c, 1);
+  }
+  if (warp == SEAM_WARP) {
+    issue_seam_warp(sm, p, c, 0);
+    issue_seam_warp(sm, p, c, 1);
   }
 
   if (args.debug_stall && !tc::mbar_wait(&sm.never, 0, LIM)) fail(sm, p);
@@ -303,7 +315,9 @@ __global__ void __launch_bounds__(NT, 2)
           x3 = fmaf(kv[7], S[i + 7], x3);
         }
         sm.xs[u & 1][hf][n] = (x0 + x1) + (x2 + x3);
-        __syncthreads();
+        // threads n and n + 128 (warps w and w + 4) exchange through a
+        // 64-thread named barrier of their own
+        tc::named_bar(1 + (warp & 3), 64);
         flush();  // the previous token's output
         // both halves sum in the same order: identical x
         const float x = sm.xs[u & 1][0][n] + sm.xs[u & 1][1][n];
@@ -335,8 +349,8 @@ __global__ void __launch_bounds__(NT, 2)
       }
       __syncthreads();  // every thread is done with this seam buffer
       flush();
-      if (tid == 0 && !aborted(sm) && gq + 2 < total_groups) {
-        issue_seam(sm, p, c, gq + 2);
+      if (gq + 2 < total_groups && warp == SEAM_WARP && !__shfl_sync(0xffffffffu, aborted(sm), 0)) {
+        issue_seam_warp(sm, p, c, gq + 2);
         seam_issued = gq + 3;
       }
     }
@@ -414,10 +428,12 @@ __global__ void __launch_bounds__(NT, 2)
     }
   }
   if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
-  // drain: every copy thread 0 issued lands before the CTA releases its smem
+  // drain: every copy issued lands before the CTA releases its smem
   if (tid == 0) {
     const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
     for (uint32_t r = first; r < issued; r++) tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, DRAIN_LIMIT);
+  }
+  if (tid == 32 * SEAM_WARP) {
     for (int r = seam_issued > 2 ? seam_issued - 2 : 0; r < seam_issued; r++)
       tc::mbar_wait(&sm.seam_full[r & 1], (r >> 1) & 1, DRAIN_LIMIT);
   }
