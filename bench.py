@@ -335,6 +335,34 @@ def compose_variant_rows(dev, hy, peaks, n_layers=8):
     return rows
 
 
+def forward_row(dev, hy):
+    """hypic_segment_forward on the config-3 GDN layer: the pairs and the
+    output of every token (zero-initial body state) by the fp32 token
+    recurrence.  ALU-bound: per token and value head, 2 d_k (d_k + d_v)
+    FMAs for the erase and update of [T | S] and d_k d_v for the output;
+    the peak is the fp32 FMA rate of the CUDA cores, 152 SMs x 128 lanes x 2
+    FLOP x the SM clock (2070 MHz)."""
+    import torch
+    import synth_inputs as si
+    W = si.workload(3, seed=0, device=dev)
+    L = W.layers[0]
+    T = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_k), device=dev)
+    S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
+    o = torch.empty((W.n_tokens, W.h_v, W.d_v), device=dev)
+    ms = _time_ms(lambda: hy.segment_forward(L.k, L.v, L.q, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=0,
+                                             T_pool=T, S_pool=S, o_out=o), reps=3, warm=1)
+    fma = W.n_tokens * W.h_v * (2 * W.d_k * (W.d_k + W.d_v) + W.d_k * W.d_v)
+    tf = 2 * fma / (ms * 1e-3) / 1e12
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = n_sm * 128 * 2 * 2.070e9 / 1e12
+    del T, S, o
+    torch.cuda.empty_cache()
+    return {"ms": ms, "tokens_per_s": W.n_tokens / (ms * 1e-3),
+            "alu": {"achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                    "peak_source": "fp32 FMA lanes x SM clock (derived)"},
+            "kernel": "fp32 token recurrence with outputs (CUDA cores)"}
+
+
 def measure_rows(dev, hy, peaks):
     """The build rows outside the timed step, each against its own roofline:
     the RetNet-style scalar-decay fast path (8 heads, d = 128, 16 x 512
@@ -372,6 +400,7 @@ def measure_rows(dev, hy, peaks):
         del L, T, S
 
     one("build: RetNet scalar decay, 8 heads, 16 x 512 tokens", si.workload(2, seed=0, device=dev))
+    rows["forward: GDN layer 64 x 1024 tokens, pairs + body outputs (fp32 token recurrence)"] = forward_row(dev, hy)
     for var in ("gdn", "deltanet", "channel"):
         W = si.workload(5, seed=0, device=dev, variant=var)
         one(f"build: uneven 256-segment mix ({W.n_tokens} tokens), {var}", W)

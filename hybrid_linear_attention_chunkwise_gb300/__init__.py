@@ -67,6 +67,10 @@ class MergeDesc(ctypes.Structure):
                 ("T_a", P), ("S_a", P), ("T_b", P), ("S_b", P), ("T_out", P), ("S_out", P), ("status", P)]
 
 
+class ForwardDesc(ctypes.Structure):
+    _fields_ = [("build", BuildDesc), ("q", P), ("o_out", P)]
+
+
 class RerotateDesc(ctypes.Structure):
     _fields_ = [("n_items", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("variant", ctypes.c_int32), ("rot_dim", ctypes.c_int32),
@@ -79,7 +83,8 @@ class RerotateDesc(ctypes.Structure):
 ROPE_LAYOUT = {"interleaved": 0, "half": 1}
 
 SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_workspace_bytes", "hypic_compose",
-           "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_pair_rerotate", "hypic_plan_lpt",
+           "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_pair_rerotate", "hypic_segment_forward",
+           "hypic_plan_lpt",
            "hypic_status_from_word", "hypic_status_string", "hypic_version")
 
 
@@ -113,6 +118,8 @@ def load():
             lib.hypic_compose_workspace_bytes.restype = ctypes.c_size_t
             lib.hypic_pair_merge.argtypes = [ctypes.POINTER(MergeDesc), P]
             lib.hypic_pair_merge.restype = ctypes.c_int
+            lib.hypic_segment_forward.argtypes = [ctypes.POINTER(ForwardDesc), P]
+            lib.hypic_segment_forward.restype = ctypes.c_int
             lib.hypic_pair_rerotate.argtypes = [ctypes.POINTER(RerotateDesc), P]
             lib.hypic_pair_rerotate.restype = ctypes.c_int
             lib.hypic_plan_lpt.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P]
@@ -236,6 +243,32 @@ def segment_build(k, v, g, beta, seg_offsets, *, variant: str, seam_w: int, T_po
     del keep
     if rc != OK:
         raise HypicError(rc, "hypic_segment_build")
+    return workspace
+
+
+def segment_forward(k, v, q, g, beta, seg_offsets, *, variant: str, seam_w: int, T_pool, S_pool, o_out,
+                    slot_of_seg=None, workspace=None, status=None, flags: int = 0, stream=None):
+    """hypic_segment_forward on torch tensors: segment_build's pairs plus
+    o_out [N, h_v, d_v] fp32, the output of every body token from the
+    zero-initial body state (seam-token rows are not written).  q [N, h_k,
+    d_k] in k's dtype."""
+    lib = load()
+    _check(q, "q", dtype=k.dtype, ndim=3)
+    _check(o_out, "o_out", dtype=torch.float32, ndim=3)
+    d = ForwardDesc()
+    b, keep = _build_desc(k, v, g, beta, seg_offsets, variant, seam_w, T_pool, S_pool, slot_of_seg,
+                          workspace, status, flags)
+    if workspace is None:
+        nb = int(lib.hypic_build_workspace_bytes(ctypes.byref(b)))
+        workspace = alloc_workspace(nb, k.device)
+        b.workspace = _ptr(workspace)
+        b.workspace_bytes = workspace.numel()
+    d.build = b
+    d.q, d.o_out = _ptr(q), _ptr(o_out)
+    rc = lib.hypic_segment_forward(ctypes.byref(d), _stream(stream))
+    del keep
+    if rc != OK:
+        raise HypicError(rc, "hypic_segment_forward")
     return workspace
 
 

@@ -142,7 +142,12 @@ size_t hypic_build_workspace_bytes(const hypic_build_desc *d) {
   return plan_bytes(2 * n_build_items(d));  // room for up to two items per pair
 }
 
-int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// the build (q == NULL) or the prefill forward (q, o_out): validation, LPT
+// plan, launch
+int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_stream_t stream) {
   if (!d) return HYPIC_ERR_INVALID_ARG;
   int st = check_common_shapes(d->h_k, d->h_v, d->d_k, d->d_v, d->seam_w, d->variant, d->in_dtype);
   if (st) return st;
@@ -188,6 +193,8 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
   p.beta = d->beta;
   p.T_pool = d->T_pool;
   p.S_pool = d->S_pool;
+  p.q = q;
+  p.o_out = o_out;
   p.plan = reinterpret_cast<PlanHeader *>(d->workspace);
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
   p.status = d->status;
@@ -232,8 +239,29 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
   // pageable source: the call returns once the bytes are staged, so `host`
   // may be released when it goes out of scope
   if (cudaMemcpyAsync(d->workspace, host.data(), need, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
-  if (launch_build(p, d->n_tokens, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
+  // the forward runs on the fp32 token kernel (its outputs are a local dot
+  // product per state column)
+  const cudaError_t e = o_out ? launch_build_token(p, (int)n_items, sm_count(), s)
+                              : launch_build(p, d->n_tokens, (int)n_items, sm_count(), s);
+  if (e != cudaSuccess) return HYPIC_ERR_CUDA;
   return HYPIC_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
+  return build_impl(d, nullptr, nullptr, stream);
+}
+
+int hypic_segment_forward(const hypic_forward_desc *d, hypic_stream_t stream) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  const hypic_build_desc &b = d->build;
+  if (b.n_tokens > 0 && b.n_seg > 0) {
+    const size_t esz = b.in_dtype == HYPIC_IN_BF16 ? 2 : 4;
+    if (!d->q || !aligned(d->q, esz) || !d->o_out || !aligned(d->o_out, 4)) return HYPIC_ERR_INVALID_ARG;
+  }
+  return build_impl(&b, d->q, d->o_out ? d->o_out : nullptr, stream);
 }
 
 size_t hypic_compose_workspace_bytes(const hypic_compose_desc *d) {

@@ -18,6 +18,10 @@
 // Items are pulled from the LPT-ordered plan by an atomic ticket (dynamic
 // list scheduling in LPT order); an item's result does not depend on which
 // block computes it.
+//
+// With an output array (the prefill forward, hypic_segment_forward) every
+// body token also emits o_t = S_t^T q_t from the zero-initial body state:
+// one more local dot product per S column and token.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -35,6 +39,7 @@ struct TokSmem {
   float a[TB][DK];    // vector gates: a = exp(g); else unused
   float lg[TB][DK];   // vector gates: g (for the log-sum of diagonal T)
   float v[TB][128];
+  float q[TB][DK];    // forward: q (zero beyond d_k / past the end)
   float gs[TB];       // scalar gate a_t (GDN) / 1
   float b[TB];        // beta_t (0 on padding tokens)
   int item;
@@ -85,6 +90,7 @@ __global__ void __launch_bounds__(256) build_token_kernel(BuildParams p) {
           }
         }
         sm.k[t][i] = kv;
+        if (p.o_out) sm.q[t][i] = (t < nt && i < d_k) ? load_in(p.q, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype) : 0.f;
         if (vec) {
           sm.a[t][i] = a;
           sm.kd[t][i] = kv * a;
@@ -145,6 +151,19 @@ __global__ void __launch_bounds__(256) build_token_kernel(BuildParams p) {
 #pragma unroll
               for (int i = 0; i < DK; i++) X[i] = fmaf(gs, X[i], kk[i] * vj);
             }
+          }
+          if (p.o_out && !is_T) {
+            // o_t[col] = q_t . S_t[:, col] (post-update state)
+            const float *qq = sm.q[t];
+            float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+            for (int i = 0; i < DK; i += 4) {
+              o0 = fmaf(qq[i + 0], X[i + 0], o0);
+              o1 = fmaf(qq[i + 1], X[i + 1], o1);
+              o2 = fmaf(qq[i + 2], X[i + 2], o2);
+              o3 = fmaf(qq[i + 3], X[i + 3], o3);
+            }
+            p.o_out[((t0 + t) * p.h_v + h) * (int64_t)d_v + col] = (o0 + o1) + (o2 + o3);
           }
         }
       }

@@ -38,6 +38,8 @@ struct BuildParams {
   const void *k, *v;
   const float *g, *beta;
   float *T_pool, *S_pool;
+  const void *q;            // forward: [n_tokens, h_k, d_k] (NULL: pairs only)
+  float *o_out;             // forward: [n_tokens, h_v, d_v] body-token outputs
   PlanHeader *plan;         // device copy of the plan
   const BuildItem *items;   // = (BuildItem*)(plan + 1)
   uint32_t *status;

@@ -135,6 +135,27 @@ size_t hypic_build_workspace_bytes(const hypic_build_desc *d);
 int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream);
 
 /*
+ * hypic_segment_forward -- the prefill forward of the cached segments: the
+ * build above (the same pairs, into the same pools) and, for every body
+ * token t (the seam window excluded) of every segment and value head h, the
+ * output of the zero-initial body state (pages §2.1: a segment's first
+ * prefill is position independent, its state starting from zero),
+ *   o_out[t, h] = S_t^T q_t,   S_t = T_t S_{t-1} + U_t,   S = 0 before the body,
+ * with the post-update state, as for the seam outputs of hypic_compose.
+ * q is [n_tokens, h_k, d_k] in the build's in_dtype (grouped heads as for k);
+ * o_out is [n_tokens, h_v, d_v] fp32, its seam-token rows are not written.
+ * Runs the fp32 token recurrence (CUDA cores) for every variant and head
+ * size; workspace and validation as for hypic_segment_build.
+ */
+typedef struct {
+  hypic_build_desc build;
+  const void *q;   /* [dev] [n_tokens, h_k, d_k] */
+  float *o_out;    /* [dev] [n_tokens, h_v, d_v] */
+} hypic_forward_desc;
+
+int hypic_segment_forward(const hypic_forward_desc *d, hypic_stream_t stream);
+
+/*
  * hypic_segment_build_noalloc -- hypic_segment_build for callers that cannot
  * allocate device memory.  The pages have no counterpart: this is a
  * deployment variant of the same build, with the same results bit for bit.

@@ -148,6 +148,21 @@ def test_build_rejects_bad_descriptors():
     assert lib.hypic_segment_build(ctypes.byref(d), None) == 1
 
 
+def test_forward_rejects_bad_descriptors():
+    lib = hy.load()
+    off = np.asarray([0, 3, 8], dtype=np.int64)
+    po = off.ctypes.data_as(ctypes.c_void_p)
+    fake = ctypes.c_void_p(1 << 20)
+    for over, want in [(dict(q=None), 1), (dict(o_out=None), 1), (dict(o_out=ctypes.c_void_p((1 << 20) + 2)), 1),
+                       (dict(build=dict(d_k=129)), 2), (dict(build=dict(k=None)), 1),
+                       (dict(build=dict(workspace=None)), 3)]:
+        d = hy.ForwardDesc()
+        d.build = _fake_build_desc(seg_offsets=po, **over.get("build", {}))
+        d.q = over.get("q", fake)
+        d.o_out = over.get("o_out", fake)
+        assert lib.hypic_segment_forward(ctypes.byref(d), None) == want, over
+
+
 def test_compose_rejects_bad_descriptors():
     lib = hy.load()
     fake = ctypes.c_void_p(1 << 20)
