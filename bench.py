@@ -336,12 +336,13 @@ def compose_variant_rows(dev, hy, peaks, n_layers=8):
 
 
 def forward_row(dev, hy):
-    """hypic_segment_forward on the config-3 GDN layer: the pairs and the
-    output of every token (zero-initial body state) by the fp32 token
-    recurrence.  ALU-bound: per token and value head, 2 d_k (d_k + d_v)
-    FMAs for the erase and update of [T | S] and d_k d_v for the output;
-    the peak is the fp32 FMA rate of the CUDA cores, 152 SMs x 128 lanes x 2
-    FLOP x the SM clock (2070 MHz)."""
+    """hypic_segment_forward on the config-3 GDN layer: the pairs (the
+    tensor-core build) and the output of every token (zero-initial body
+    state) by the fp32 token recurrence over the state columns.  The output
+    pass is ALU-bound: per token and value head 3 d_k d_v FMAs (erase dot
+    product, update, output); the fraction below divides them by the whole
+    call's time (build included), against the fp32 FMA rate of the CUDA
+    cores, SMs x 128 lanes x 2 FLOP x the SM clock (2070 MHz)."""
     import torch
     import synth_inputs as si
     W = si.workload(3, seed=0, device=dev)
@@ -351,7 +352,7 @@ def forward_row(dev, hy):
     o = torch.empty((W.n_tokens, W.h_v, W.d_v), device=dev)
     ms = _time_ms(lambda: hy.segment_forward(L.k, L.v, L.q, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=0,
                                              T_pool=T, S_pool=S, o_out=o), reps=3, warm=1)
-    fma = W.n_tokens * W.h_v * (2 * W.d_k * (W.d_k + W.d_v) + W.d_k * W.d_v)
+    fma = W.n_tokens * W.h_v * 3 * W.d_k * W.d_v
     tf = 2 * fma / (ms * 1e-3) / 1e12
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     peak = n_sm * 128 * 2 * 2.070e9 / 1e12
@@ -360,7 +361,7 @@ def forward_row(dev, hy):
     return {"ms": ms, "tokens_per_s": W.n_tokens / (ms * 1e-3),
             "alu": {"achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                     "peak_source": "fp32 FMA lanes x SM clock (derived)"},
-            "kernel": "fp32 token recurrence with outputs (CUDA cores)"}
+            "kernel": "tensor-core build, then the fp32 token recurrence over the state columns"}
 
 
 def measure_rows(dev, hy, peaks):
@@ -400,7 +401,7 @@ def measure_rows(dev, hy, peaks):
         del L, T, S
 
     one("build: RetNet scalar decay, 8 heads, 16 x 512 tokens", si.workload(2, seed=0, device=dev))
-    rows["forward: GDN layer 64 x 1024 tokens, pairs + body outputs (fp32 token recurrence)"] = forward_row(dev, hy)
+    rows["forward: GDN layer 64 x 1024 tokens, pairs + body outputs"] = forward_row(dev, hy)
     for var in ("gdn", "deltanet", "channel"):
         W = si.workload(5, seed=0, device=dev, variant=var)
         one(f"build: uneven 256-segment mix ({W.n_tokens} tokens), {var}", W)

@@ -239,11 +239,18 @@ int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_str
   // pageable source: the call returns once the bytes are staged, so `host`
   // may be released when it goes out of scope
   if (cudaMemcpyAsync(d->workspace, host.data(), need, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
-  // the forward runs on the fp32 token kernel (its outputs are a local dot
-  // product per state column)
-  const cudaError_t e = o_out ? launch_build_token(p, (int)n_items, sm_count(), s)
-                              : launch_build(p, d->n_tokens, (int)n_items, sm_count(), s);
-  if (e != cudaSuccess) return HYPIC_ERR_CUDA;
+  BuildParams pb = p;
+  pb.q = nullptr;
+  pb.o_out = nullptr;
+  if (launch_build(pb, d->n_tokens, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (o_out) {
+    // the forward: the pairs above, then the outputs by the fp32 token
+    // recurrence over the S columns alone (a local dot product per column
+    // and token), from a fresh ticket over the same plan
+    p.out_only = 1;
+    if (cudaMemsetAsync(d->workspace, 0, sizeof(int32_t), s) != cudaSuccess) return HYPIC_ERR_CUDA;
+    if (launch_build_token(p, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
+  }
   return HYPIC_OK;
 }
 }  // namespace

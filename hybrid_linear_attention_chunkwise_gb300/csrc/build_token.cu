@@ -21,7 +21,9 @@
 //
 // With an output array (the prefill forward, hypic_segment_forward) every
 // body token also emits o_t = S_t^T q_t from the zero-initial body state:
-// one more local dot product per S column and token.
+// one more local dot product per S column and token.  The forward runs it
+// outputs-only (out_only: S columns alone, nothing written to the pools)
+// after the pairs have come from the fastest build kernel.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -53,7 +55,7 @@ __global__ void __launch_bounds__(256) build_token_kernel(BuildParams p) {
   const bool delta = is_delta(p.variant);
   const bool vec = is_vector_gate(p.variant);
   const int d_k = p.d_k, d_v = p.d_v;
-  const int n_t_thr = delta ? DK : 0;              // threads [0, DK) own T columns
+  const int n_t_thr = (delta && !p.out_only) ? DK : 0;  // threads [0, DK) own T columns
   const bool is_T = tid < n_t_thr;
   const int col = is_T ? tid : tid - n_t_thr;      // column within T or S
   const bool active = is_T ? (col < d_k) : (col < d_v);
@@ -171,6 +173,7 @@ __global__ void __launch_bounds__(256) build_token_kernel(BuildParams p) {
     }
 
     // epilogue: write the pair into the pool slot
+    if (p.out_only) continue;
     const int64_t sh = (int64_t)it.slot * p.h_v + h;
     bool bad = false;
     if (active) {
@@ -214,7 +217,7 @@ template <int DK>
 cudaError_t launch_dk(const BuildParams &p, int n_items, int n_sm, cudaStream_t s) {
   const bool delta = is_delta(p.variant);
   const int dvp = ((p.d_v + 31) / 32) * 32;
-  int threads = (delta ? DK : 0) + dvp;
+  int threads = (delta && !p.out_only ? DK : 0) + dvp;
   const int dkp = ((p.d_k + 31) / 32) * 32;
   if (threads < dkp) threads = dkp;  // diagonal gates: one thread per channel for the log-sum
   threads = ((threads + 31) / 32) * 32;

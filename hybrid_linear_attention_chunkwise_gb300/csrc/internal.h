@@ -40,6 +40,7 @@ struct BuildParams {
   float *T_pool, *S_pool;
   const void *q;            // forward: [n_tokens, h_k, d_k] (NULL: pairs only)
   float *o_out;             // forward: [n_tokens, h_v, d_v] body-token outputs
+  int32_t out_only;         // token kernel: outputs only (S columns, no pair written)
   PlanHeader *plan;         // device copy of the plan
   const BuildItem *items;   // = (BuildItem*)(plan + 1)
   uint32_t *status;

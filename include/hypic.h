@@ -144,8 +144,9 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream);
  * with the post-update state, as for the seam outputs of hypic_compose.
  * q is [n_tokens, h_k, d_k] in the build's in_dtype (grouped heads as for k);
  * o_out is [n_tokens, h_v, d_v] fp32, its seam-token rows are not written.
- * Runs the fp32 token recurrence (CUDA cores) for every variant and head
- * size; workspace and validation as for hypic_segment_build.
+ * The pairs come from the build's own kernels; the outputs from the fp32
+ * token recurrence over the state columns (CUDA cores), for every variant
+ * and head size.  Workspace and validation as for hypic_segment_build.
  */
 typedef struct {
   hypic_build_desc build;
