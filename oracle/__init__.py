@@ -12,6 +12,9 @@ xix.ai linear-layer and seam paragraphs):
               then S <- T_C S + S(C|0);
   full     -- the plain recurrence over a whole prompt (the full recompute);
   merge    -- (T2,S2) o (T1,S1) = (T2 T1, T2 S1 + S2);
+  rerotate -- the state re-rotation patch for RoPE-shifted reuse
+              (R T_C R^T, R S(C|0)), numpy fp64 (reading of the pages' one
+              sentence on it: rotary angles position x base^(-2i/rot_dim));
   naive    -- the straw man: sum of zero-initial states.
 The arithmetic is the C file ``hypic_oracle.c`` (fp64, token by token);
 ``dense_twin`` restates the definition with explicit dense matrices for tiny
