@@ -245,11 +245,10 @@ int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_str
   if (launch_build(pb, d->n_tokens, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
   if (o_out) {
     // the forward: the pairs above, then the outputs by the fp32 token
-    // recurrence over the S columns alone (a local dot product per column
-    // and token), from a fresh ticket over the same plan
-    p.out_only = 1;
+    // recurrence over the S columns alone, from a fresh ticket over the same
+    // plan
     if (cudaMemsetAsync(d->workspace, 0, sizeof(int32_t), s) != cudaSuccess) return HYPIC_ERR_CUDA;
-    if (launch_build_token(p, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
+    if (launch_forward_out(p, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
   }
   return HYPIC_OK;
 }

@@ -18,12 +18,6 @@
 // Items are pulled from the LPT-ordered plan by an atomic ticket (dynamic
 // list scheduling in LPT order); an item's result does not depend on which
 // block computes it.
-//
-// With an output array (the prefill forward, hypic_segment_forward) every
-// body token also emits o_t = S_t^T q_t from the zero-initial body state:
-// one more local dot product per S column and token.  The forward runs it
-// outputs-only (out_only: S columns alone, nothing written to the pools)
-// after the pairs have come from the fastest build kernel.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -31,6 +25,8 @@
 namespace hypic {
 
 namespace {
+
+__device__ __forceinline__ void tc_named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 constexpr int TB = 16;  // tokens per shared-memory tile
 
@@ -41,7 +37,6 @@ struct TokSmem {
   float a[TB][DK];    // vector gates: a = exp(g); else unused
   float lg[TB][DK];   // vector gates: g (for the log-sum of diagonal T)
   float v[TB][128];
-  float q[TB][DK];    // forward: q (zero beyond d_k / past the end)
   float gs[TB];       // scalar gate a_t (GDN) / 1
   float b[TB];        // beta_t (0 on padding tokens)
   int item;
@@ -55,7 +50,7 @@ __global__ void __launch_bounds__(256) build_token_kernel(BuildParams p) {
   const bool delta = is_delta(p.variant);
   const bool vec = is_vector_gate(p.variant);
   const int d_k = p.d_k, d_v = p.d_v;
-  const int n_t_thr = (delta && !p.out_only) ? DK : 0;  // threads [0, DK) own T columns
+  const int n_t_thr = delta ? DK : 0;              // threads [0, DK) own T columns
   const bool is_T = tid < n_t_thr;
   const int col = is_T ? tid : tid - n_t_thr;      // column within T or S
   const bool active = is_T ? (col < d_k) : (col < d_v);
@@ -92,7 +87,6 @@ __global__ void __launch_bounds__(256) build_token_kernel(BuildParams p) {
           }
         }
         sm.k[t][i] = kv;
-        if (p.o_out) sm.q[t][i] = (t < nt && i < d_k) ? load_in(p.q, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype) : 0.f;
         if (vec) {
           sm.a[t][i] = a;
           sm.kd[t][i] = kv * a;
@@ -154,26 +148,12 @@ __global__ void __launch_bounds__(256) build_token_kernel(BuildParams p) {
               for (int i = 0; i < DK; i++) X[i] = fmaf(gs, X[i], kk[i] * vj);
             }
           }
-          if (p.o_out && !is_T) {
-            // o_t[col] = q_t . S_t[:, col] (post-update state)
-            const float *qq = sm.q[t];
-            float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll
-            for (int i = 0; i < DK; i += 4) {
-              o0 = fmaf(qq[i + 0], X[i + 0], o0);
-              o1 = fmaf(qq[i + 1], X[i + 1], o1);
-              o2 = fmaf(qq[i + 2], X[i + 2], o2);
-              o3 = fmaf(qq[i + 3], X[i + 3], o3);
-            }
-            p.o_out[((t0 + t) * p.h_v + h) * (int64_t)d_v + col] = (o0 + o1) + (o2 + o3);
-          }
         }
       }
       __syncthreads();
     }
 
     // epilogue: write the pair into the pool slot
-    if (p.out_only) continue;
     const int64_t sh = (int64_t)it.slot * p.h_v + h;
     bool bad = false;
     if (active) {
@@ -217,7 +197,7 @@ template <int DK>
 cudaError_t launch_dk(const BuildParams &p, int n_items, int n_sm, cudaStream_t s) {
   const bool delta = is_delta(p.variant);
   const int dvp = ((p.d_v + 31) / 32) * 32;
-  int threads = (delta && !p.out_only ? DK : 0) + dvp;
+  int threads = (delta ? DK : 0) + dvp;
   const int dkp = ((p.d_k + 31) / 32) * 32;
   if (threads < dkp) threads = dkp;  // diagonal gates: one thread per channel for the log-sum
   threads = ((threads + 31) / 32) * 32;
@@ -235,7 +215,185 @@ cudaError_t launch_dk(const BuildParams &p, int n_items, int n_sm, cudaStream_t 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// The outputs of the prefill forward (hypic_segment_forward): for every body
+// token of every item, o_t = S_t^T q_t from the zero-initial body state, by
+// the same token recurrence over the S columns only (the pairs come from the
+// build kernels).  Each column is split over two threads, rows 0..DK/2-1 and
+// DK/2..DK-1 (threads col and col + DVP, in warps w and w + DVP/32), so a
+// column holds DK/2 registers per thread and twice as many warps fit an SM;
+// the halves exchange their partial dot products through shared memory
+// under a 64-thread barrier of their own (one per token), the lower half
+// writing the output of a token after the next barrier.
+// ---------------------------------------------------------------------------
+template <int DK>
+struct FwdSmem {
+  TokSmem<DK> t;
+  float q[TB][DK];
+  float xs[2][2][128];  // partial k^T S of the two halves, by token parity
+  float os[2][128];     // partial q^T S of the upper half, by token parity
+};
+
+template <int DK>
+__global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  FwdSmem<DK> &fs = *reinterpret_cast<FwdSmem<DK> *>(smem_raw);
+  TokSmem<DK> &sm = fs.t;
+  constexpr int HALF = DK / 2;
+  const int tid = threadIdx.x;
+  const bool delta = is_delta(p.variant);
+  const bool vec = is_vector_gate(p.variant);
+  const int d_k = p.d_k, d_v = p.d_v;
+  const int hf = tid / dvp, col = tid % dvp, r0 = hf * HALF;
+  const bool active = col < d_v;
+  const int bar = 1 + col / 32;  // the pair of warps holding this column
+  const int n_items = p.plan->n_items;
+
+  for (;;) {
+    if (tid == 0) sm.item = atomicAdd(&p.plan->ticket, 1);
+    __syncthreads();
+    const int idx = sm.item;
+    __syncthreads();
+    if (idx >= n_items) break;
+    const BuildItem it = p.items[idx];
+    const int h = it.head;
+    const int kh = (int)(((int64_t)h * p.h_k) / p.h_v);
+    float X[HALF];
+#pragma unroll
+    for (int i = 0; i < HALF; i++) X[i] = 0.f;
+    float gconst = 1.f;
+    if (p.variant == HYPIC_SCALAR_DECAY) gconst = expf(p.g[h]);
+    uint32_t u = 0;       // tokens so far: parity of the exchange buffers
+    int64_t pend = -1;    // lower half: token whose output waits for the upper half's partial
+    float opend = 0.f;
+    auto flush = [&]() {
+      if (hf == 0 && pend >= 0 && active)
+        p.o_out[(pend * p.h_v + h) * (int64_t)d_v + col] = opend + fs.os[(u - 1) & 1][col];
+      pend = -1;
+    };
+
+    for (int64_t t0 = it.start; t0 < it.end; t0 += TB) {
+      const int nt = (int)((it.end - t0) < TB ? (it.end - t0) : TB);
+      for (int e = tid; e < TB * DK; e += blockDim.x) {
+        const int t = e / DK, i = e % DK;
+        float kv = 0.f, qv = 0.f, a = 1.f;
+        if (t < nt && i < d_k) {
+          kv = load_in(p.k, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype);
+          qv = load_in(p.q, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype);
+          if (vec) a = expf(p.g[((t0 + t) * p.h_v + h) * (int64_t)d_k + i]);
+        }
+        sm.k[t][i] = kv;
+        fs.q[t][i] = qv;
+        if (vec) {
+          sm.a[t][i] = a;
+          sm.kd[t][i] = kv * a;
+        }
+      }
+      for (int e = tid; e < TB * 128; e += blockDim.x) {
+        const int t = e / 128, j = e % 128;
+        sm.v[t][j] = (t < nt && j < d_v) ? load_in(p.v, ((t0 + t) * p.h_v + h) * (int64_t)d_v + j, p.in_dtype) : 0.f;
+      }
+      for (int t = tid; t < TB; t += blockDim.x) {
+        float gs = 1.f, b = 0.f;
+        if (t < nt) {
+          if (p.variant == HYPIC_GDN) gs = expf(p.g[(t0 + t) * p.h_v + h]);
+          else if (p.variant == HYPIC_SCALAR_DECAY) gs = gconst;
+          if (delta) b = p.beta[(t0 + t) * p.h_v + h];
+        }
+        sm.gs[t] = gs;
+        sm.b[t] = b;
+      }
+      __syncthreads();
+      flush();  // the last token of the previous tile
+      for (int t = 0; t < nt; t++) {
+        const float b = sm.b[t], gs = sm.gs[t];
+        const float vj = sm.v[t][col < 128 ? col : 0];
+        const float *kk = sm.k[t] + r0;
+        if (delta) {
+          const float *kd = (vec ? sm.kd[t] : sm.k[t]) + r0;
+          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+          for (int i = 0; i < HALF; i += 4) {
+            x0 = fmaf(kd[i + 0], X[i + 0], x0);
+            x1 = fmaf(kd[i + 1], X[i + 1], x1);
+            x2 = fmaf(kd[i + 2], X[i + 2], x2);
+            x3 = fmaf(kd[i + 3], X[i + 3], x3);
+          }
+          fs.xs[u & 1][hf][col] = (x0 + x1) + (x2 + x3);
+          tc_named_bar(bar, 64);
+          flush();
+          // both halves sum in the same order: identical x
+          const float x = fs.xs[u & 1][0][col] + fs.xs[u & 1][1][col];
+          const float c = vec ? (b * vj - b * x) : (gs * (-b * x) + b * vj);
+          if (vec) {
+            const float *aa = sm.a[t] + r0;
+#pragma unroll
+            for (int i = 0; i < HALF; i++) X[i] = fmaf(aa[i], X[i], kk[i] * c);
+          } else {
+#pragma unroll
+            for (int i = 0; i < HALF; i++) X[i] = fmaf(gs, X[i], kk[i] * c);
+          }
+        } else {
+          if (vec) {
+            const float *aa = sm.a[t] + r0;
+#pragma unroll
+            for (int i = 0; i < HALF; i++) X[i] = fmaf(aa[i], X[i], kk[i] * vj);
+          } else {
+#pragma unroll
+            for (int i = 0; i < HALF; i++) X[i] = fmaf(gs, X[i], kk[i] * vj);
+          }
+        }
+        // the half output q^T S
+        const float *qq = fs.q[t] + r0;
+        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < HALF; i += 4) {
+          o0 = fmaf(qq[i + 0], X[i + 0], o0);
+          o1 = fmaf(qq[i + 1], X[i + 1], o1);
+          o2 = fmaf(qq[i + 2], X[i + 2], o2);
+          o3 = fmaf(qq[i + 3], X[i + 3], o3);
+        }
+        const float o = (o0 + o1) + (o2 + o3);
+        if (hf) fs.os[u & 1][col] = o;
+        opend = o;
+        pend = t0 + t;
+        u++;
+        if (!delta) {
+          // no erase barrier in these variants: the output exchange needs one
+          tc_named_bar(bar, 64);
+          flush();
+        }
+      }
+      __syncthreads();  // the tile buffers are free
+    }
+    flush();
+  }
+}
+
 }  // namespace
+
+// the output pass of the prefill forward (pairs written elsewhere)
+cudaError_t launch_forward_out(const BuildParams &p, int n_items, int n_sm, cudaStream_t s) {
+  const int dvp = ((p.d_v + 31) / 32) * 32;
+  const int threads = 2 * dvp;
+  auto go = [&](auto kern, size_t smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int grid = n_sm * per_sm;
+    if (grid > n_items) grid = n_items;
+    if (grid < 1) return cudaSuccess;
+    kern<<<grid, threads, smem, s>>>(p, dvp);
+    return cudaGetLastError();
+  };
+  if (p.d_k <= 16) return go(forward_out_kernel<16>, sizeof(FwdSmem<16>));
+  if (p.d_k <= 32) return go(forward_out_kernel<32>, sizeof(FwdSmem<32>));
+  if (p.d_k <= 64) return go(forward_out_kernel<64>, sizeof(FwdSmem<64>));
+  return go(forward_out_kernel<128>, sizeof(FwdSmem<128>));
+}
 
 cudaError_t launch_build_token(const BuildParams &p, int n_items, int n_sm, cudaStream_t s) {
   if (p.d_k <= 16) return launch_dk<16>(p, n_items, n_sm, s);

@@ -40,7 +40,6 @@ struct BuildParams {
   float *T_pool, *S_pool;
   const void *q;            // forward: [n_tokens, h_k, d_k] (NULL: pairs only)
   float *o_out;             // forward: [n_tokens, h_v, d_v] body-token outputs
-  int32_t out_only;         // token kernel: outputs only (S columns, no pair written)
   PlanHeader *plan;         // device copy of the plan
   const BuildItem *items;   // = (BuildItem*)(plan + 1)
   uint32_t *status;
@@ -90,6 +89,7 @@ __host__ __device__ inline bool is_vector_gate(int v) { return v == HYPIC_CHANNE
 // else the token recurrence), one item per (segment, value head).
 cudaError_t launch_build(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, cudaStream_t s);
 cudaError_t launch_build_token(const BuildParams &p, int n_items, int n_sm, cudaStream_t s);
+cudaError_t launch_forward_out(const BuildParams &p, int n_items, int n_sm, cudaStream_t s);
 // Tensor-core chunkwise build: GDN / DeltaNet, bf16 inputs, d_k = d_v = 128,
 // 16-byte aligned k / v.  Items are (segment, head, half of [T | S]).
 bool build_tc_supported(const BuildParams &p);
