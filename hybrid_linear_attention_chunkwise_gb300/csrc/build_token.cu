@@ -18,6 +18,8 @@
 // Items are pulled from the LPT-ordered plan by an atomic ticket (dynamic
 // list scheduling in LPT order); an item's result does not depend on which
 // block computes it.
+#include <cstddef>
+
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -229,10 +231,20 @@ cudaError_t launch_dk(const BuildParams &p, int n_items, int n_sm, cudaStream_t 
 template <int DK>
 struct FwdSmem {
   TokSmem<DK> t;
-  float q[TB][DK];
+  alignas(16) float q[TB][DK];  // rows read 16 bytes a time
   float xs[2][2][128];  // partial k^T S of the two halves, by token parity
   float os[2][128];     // partial q^T S of the upper half, by token parity
 };
+// every row read by 16-byte loads starts on a 16-byte boundary (and so does
+// each half row: DK / 2 floats is a multiple of 4)
+template <int DK>
+constexpr bool fwd_rows_aligned() {
+  return offsetof(FwdSmem<DK>, q) % 16 == 0 && offsetof(TokSmem<DK>, k) % 16 == 0 &&
+         offsetof(TokSmem<DK>, kd) % 16 == 0 && offsetof(TokSmem<DK>, a) % 16 == 0 && (DK * 4) % 16 == 0 &&
+         (DK / 2) % 4 == 0;
+}
+static_assert(fwd_rows_aligned<16>() && fwd_rows_aligned<32>() && fwd_rows_aligned<64>() && fwd_rows_aligned<128>(),
+              "16-byte shared-memory rows");
 
 template <int DK>
 __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp) {
@@ -266,6 +278,32 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
     uint32_t u = 0;       // tokens so far: parity of the exchange buffers
     int64_t pend = -1;    // lower half: token whose output waits for the upper half's partial
     float opend = 0.f;
+    // X <- Diag(a) X + k c (per-channel gate) or gs X + k c, 16 bytes a time
+    auto update = [&](int t, float c) {
+      const float *kk = sm.k[t] + r0;
+      if (vec) {
+        const float *aa = sm.a[t] + r0;
+#pragma unroll
+        for (int i = 0; i < HALF; i += 4) {
+          const float4 kv = *reinterpret_cast<const float4 *>(kk + i);
+          const float4 av = *reinterpret_cast<const float4 *>(aa + i);
+          X[i + 0] = fmaf(av.x, X[i + 0], kv.x * c);
+          X[i + 1] = fmaf(av.y, X[i + 1], kv.y * c);
+          X[i + 2] = fmaf(av.z, X[i + 2], kv.z * c);
+          X[i + 3] = fmaf(av.w, X[i + 3], kv.w * c);
+        }
+      } else {
+        const float gs = sm.gs[t];
+#pragma unroll
+        for (int i = 0; i < HALF; i += 4) {
+          const float4 kv = *reinterpret_cast<const float4 *>(kk + i);
+          X[i + 0] = fmaf(gs, X[i + 0], kv.x * c);
+          X[i + 1] = fmaf(gs, X[i + 1], kv.y * c);
+          X[i + 2] = fmaf(gs, X[i + 2], kv.z * c);
+          X[i + 3] = fmaf(gs, X[i + 3], kv.w * c);
+        }
+      }
+    };
     auto flush = [&]() {
       if (hf == 0 && pend >= 0 && active)
         p.o_out[(pend * p.h_v + h) * (int64_t)d_v + col] = opend + fs.os[(u - 1) & 1][col];
@@ -308,16 +346,16 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
       for (int t = 0; t < nt; t++) {
         const float b = sm.b[t], gs = sm.gs[t];
         const float vj = sm.v[t][col < 128 ? col : 0];
-        const float *kk = sm.k[t] + r0;
         if (delta) {
           const float *kd = (vec ? sm.kd[t] : sm.k[t]) + r0;
           float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
 #pragma unroll
           for (int i = 0; i < HALF; i += 4) {
-            x0 = fmaf(kd[i + 0], X[i + 0], x0);
-            x1 = fmaf(kd[i + 1], X[i + 1], x1);
-            x2 = fmaf(kd[i + 2], X[i + 2], x2);
-            x3 = fmaf(kd[i + 3], X[i + 3], x3);
+            const float4 w = *reinterpret_cast<const float4 *>(kd + i);  // 16-byte aligned rows
+            x0 = fmaf(w.x, X[i + 0], x0);
+            x1 = fmaf(w.y, X[i + 1], x1);
+            x2 = fmaf(w.z, X[i + 2], x2);
+            x3 = fmaf(w.w, X[i + 3], x3);
           }
           fs.xs[u & 1][hf][col] = (x0 + x1) + (x2 + x3);
           tc_named_bar(bar, 64);
@@ -325,33 +363,20 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
           // both halves sum in the same order: identical x
           const float x = fs.xs[u & 1][0][col] + fs.xs[u & 1][1][col];
           const float c = vec ? (b * vj - b * x) : (gs * (-b * x) + b * vj);
-          if (vec) {
-            const float *aa = sm.a[t] + r0;
-#pragma unroll
-            for (int i = 0; i < HALF; i++) X[i] = fmaf(aa[i], X[i], kk[i] * c);
-          } else {
-#pragma unroll
-            for (int i = 0; i < HALF; i++) X[i] = fmaf(gs, X[i], kk[i] * c);
-          }
+          update(t, c);
         } else {
-          if (vec) {
-            const float *aa = sm.a[t] + r0;
-#pragma unroll
-            for (int i = 0; i < HALF; i++) X[i] = fmaf(aa[i], X[i], kk[i] * vj);
-          } else {
-#pragma unroll
-            for (int i = 0; i < HALF; i++) X[i] = fmaf(gs, X[i], kk[i] * vj);
-          }
+          update(t, vj);
         }
         // the half output q^T S
         const float *qq = fs.q[t] + r0;
         float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
         for (int i = 0; i < HALF; i += 4) {
-          o0 = fmaf(qq[i + 0], X[i + 0], o0);
-          o1 = fmaf(qq[i + 1], X[i + 1], o1);
-          o2 = fmaf(qq[i + 2], X[i + 2], o2);
-          o3 = fmaf(qq[i + 3], X[i + 3], o3);
+          const float4 w = *reinterpret_cast<const float4 *>(qq + i);
+          o0 = fmaf(w.x, X[i + 0], o0);
+          o1 = fmaf(w.y, X[i + 1], o1);
+          o2 = fmaf(w.z, X[i + 2], o2);
+          o3 = fmaf(w.w, X[i + 3], o3);
         }
         const float o = (o0 + o1) + (o2 + o3);
         if (hf) fs.os[u & 1][col] = o;
