@@ -98,9 +98,12 @@ KERNEL_SOURCES = {
     "compose": ("compose_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
     "channel": ("build_channel.cu", "tc.cuh", "common.cuh", "internal.h"),
     "merge": ("merge.cu", "tc.cuh", "common.cuh", "internal.h"),
+    "rerotate": ("rerotate.cu", "tc.cuh", "common.cuh", "internal.h"),
+    "forward": ("build_token.cu", "common.cuh", "internal.h"),
 }
 PROFILE_FILES = {"build": "segment_build_tc__gdn_16x1024.md", "compose": "compose_seam_mma__gdn_4x32x100.md",
-                 "channel": "segment_build_channel__16x1024.md", "merge": "pair_merge_tc__4x32x50.md"}
+                 "channel": "segment_build_channel__16x1024.md", "merge": "pair_merge_tc__4x32x50.md",
+                 "rerotate": "pair_rerotate__4x100x32.md", "forward": "forward_out__gdn_16x1024.md"}
 
 
 def source_hash(kind):
@@ -417,7 +420,8 @@ def run_profile_case(kind):
     (segment, head) pairs); channel: the same shape with per-channel gates;
     compose: 4 GDN layers x 32 heads x 100 segments, w = 8 (12800 pairs,
     1.7 GB pool); merge: that pool's adjacent segment pairs merged (4 x 50
-    merges x 32 heads)."""
+    merges x 32 heads); rerotate: that pool re-rotated in place (400 slots x
+    32 heads); forward: the build case's forward (its output kernel)."""
     import torch
     import hybrid_linear_attention_chunkwise_gb300 as hy
     import synth_inputs as si
@@ -444,6 +448,24 @@ def run_profile_case(kind):
         So = torch.empty_like(To)
         run = lambda: hy.pair_merge(later, earlier, outs, comp["T_pool"], comp["S_pool"], To, So, variant="gdn")
         units = len(pairs) * W.h_v
+    elif kind == "rerotate":
+        comp = setup_compose(dev, hy, n_layers=4)
+        W = comp["W"]
+        n = comp["n_layers"] * W.n_seg
+        slots = torch.arange(n, dtype=torch.int32, device=dev)
+        deltas = torch.arange(n, dtype=torch.int64, device=dev) * 997 - 50000
+        run = lambda: hy.pair_rerotate(slots, slots, deltas, comp["T_pool"], comp["S_pool"], comp["T_pool"],
+                                       comp["S_pool"], variant="gdn", rot_dim=W.d_k, layout="half")
+        units = n * W.h_v
+    elif kind == "forward":
+        W = si.workload(3, seed=0, device=dev, n_seg=16)
+        L = W.layers[0]
+        T = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_k), device=dev)
+        S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
+        o = torch.empty((W.n_tokens, W.h_v, W.d_v), device=dev)
+        run = lambda: hy.segment_forward(L.k, L.v, L.q, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=0,
+                                         T_pool=T, S_pool=S, o_out=o)
+        units = W.n_tokens * W.h_v
     else:
         comp = setup_compose(dev, hy, n_layers=4)
         sa = comp["sa"]
@@ -530,7 +552,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements after the step")
-    ap.add_argument("--profile", choices=["build", "compose", "channel", "merge"], default=None,
+    ap.add_argument("--profile", choices=["build", "compose", "channel", "merge", "rerotate", "forward"], default=None,
                     help="run one small case of one kernel (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.impl == "reference":
