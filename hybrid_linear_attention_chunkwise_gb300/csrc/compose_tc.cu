@@ -2,35 +2,17 @@
 // variants (GDN, DeltaNet, per-channel delta) with bf16 seam tokens and
 // d_k = d_v = 128: the bandwidth-bound left-multiply-add S <- T_C S + S(C|0)
 // of the HYPIC news pages (nav.aitube.vip §2.1), with the seam-window advance
-// and per-token outputs of §2.2.  Two kernels share the pair streaming:
-//   compose_channel_kernel   per-channel gates: the seam tokens one by one on
-//                            the CUDA cores (below);
-//   compose_seam_mma_kernel  scalar gates: the seam tokens in groups of eight
-//                            on the tensor cores (further down).
+// and per-token outputs of §2.2, in one kernel (compose_seam_mma_kernel,
+// below): one CTA of 256 threads per (layer, value head) chain, two CTAs per
+// SM, the seam tokens in groups of eight on the tensor cores, the last group
+// of a segment fused with the pair's T_C S product.
 //
-// Per-channel kernel: one CTA of 256 threads per (layer, value head) chain,
-// two CTAs per SM.  Threads n and n + 128 own rows 0..63 and 64..127 of
-// column n of the running state S (64 fp32 registers each).  Per segment, in
-// prompt order:
-//   seam  each seam token scales S by its gates (S <- Diag(a) S), forms the
-//         half-column dot product k^T S[:,n], exchanges it with its partner
-//         through shared memory (one 64-thread barrier per token and warp
-//         pair), applies the
-//         rank-1 update and emits o_t[n] = q_t . S[:,n] (partner sums are
-//         written out after the next barrier);
-//   MMA   S is rounded to tf32 and stored to TMEM as the A operand (lane n =
-//         S[:,n]^T, columns 64 h .. 64 h + 63 from thread half h); thread 0
-//         issues D = S^T T_C^T (M = N = K = 128, kind::tf32) from TMEM A and
-//         a shared-memory B operand, so lane n of D is column n of T_C S;
-//   add   each thread adds its 64 rows of column n of S(C|0), loaded from
-//         global memory (warmed in L2 a segment ahead) while the MMA runs.
-// Data movement, all issued by thread 0 at the moment the consumer frees the
-// space:
+// Data movement:
 //   T_C   four 16 KiB K-slabs per pair (TMA 2-D tiles, 128-byte swizzle = the
-//         K-major MMA operand layout) through a ring of NSLOT slots; the slots
-//         of a pair are refilled as soon as its MMAs complete;
-//   seam  k/q/v rows, gate rows and the beta block of each group of SB tokens
-//         by bulk copies into one of two seam buffers.
+//         K-major MMA operand layout) through a ring of shared-memory slots;
+//   S(C|0) bulk-copied into the slots T_C has just freed;
+//   seam  k/q/v rows by bulk copies, gates and betas by plain loads, one or
+//         two groups ahead.
 // Each pool byte crosses HBM once: 128 KiB per (segment, head) pair.
 //
 // Every wait is bounded: one that runs out sets HYPIC_STATUS_TIMEOUT; the CTA
@@ -51,34 +33,8 @@ namespace {
 
 constexpr int NSLOT = 5;   // T_C K-slab ring (16 KiB each)
 constexpr int SLAB = 16384;
-constexpr int SB = 8;      // seam tokens per seam buffer
-constexpr int NT = 256;    // threads per CTA (per-channel kernel): two per state column
 constexpr int MAX_HV = 128;
 constexpr uint32_t DRAIN_LIMIT = 1u << 22;
-
-struct SeamBuf {
-  __nv_bfloat16 k[SB][128];
-  __nv_bfloat16 q[SB][128];
-  __nv_bfloat16 v[SB][128];
-  float gv[SB][128];         // per-channel log-gates of this head, then a = e^g
-  float b[SB];               // beta of this head (plain loads, warmed in L2)
-};
-
-struct __align__(1024) ComposeTcSmem {
-  unsigned char slot[NSLOT][SLAB];  // 1024-aligned: swizzled TMA tiles
-  SeamBuf seam[2];
-  float xs[2][2][128];  // partial k^T S of the two halves, by token parity
-  float os[2][128];     // partial q^T S of the upper half, by token parity
-  uint64_t full[NSLOT];
-  uint64_t seam_full[2];
-  uint64_t mma_done;
-  uint64_t never;  // no thread ever arrives here (debug stall)
-  uint32_t tmem_base;
-  int abort;
-  int stop;
-};
-static_assert(sizeof(SeamBuf) % 16 == 0, "bulk-copy destinations must stay 16-byte aligned");
-static_assert(2 * (sizeof(ComposeTcSmem) + 2048) <= 228 * 1024, "two chains per SM");
 
 struct TcArgs {
   ComposeParams p;
@@ -123,54 +79,14 @@ __device__ __forceinline__ int pair_slot(const ComposeParams &p, const Chain &c,
 // T_C K-slab r (pair r/4, columns 32*(r%4) .. +32) into ring slot r % NSLOT
 template <class SM>
 __device__ __forceinline__ void issue_slab(SM &sm, const ComposeParams &p, const Chain &c, const CUtensorMap *tmap,
-                                           uint32_t r) {
+                                           uint32_t r, int ring = NSLOT) {
   if (r >= 4u * (uint32_t)c.n_seg) return;
   const int seg = (int)(r / 4), j = (int)(r % 4);
   int slot = pair_slot(p, c, seg);
   if (slot < 0) slot = 0;  // keep the ring in step; the pair is skipped at use
-  const int si = r % NSLOT;
+  const int si = r % ring;
   tc::mbar_expect_tx(&sm.full[si], SLAB);
   tc::tma_load_2d(sm.slot[si], tmap, 32 * j, (int32_t)(((int64_t)slot * p.h_v + c.h) * 128), &sm.full[si]);
-}
-
-// k / q / v rows and per-channel gate rows of seam group gq into seam buffer
-// gq % 2, one bulk copy per lane of the calling warp (all 32 lanes call:
-// 4 nt <= 32 copies); its beta block (all heads, contiguous) is warmed in L2
-__device__ __forceinline__ void issue_seam_warp(ComposeTcSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
-  if (gq >= c.n_seg * c.groups) return;
-  const int lane = threadIdx.x & 31;
-  const int seg = gq / c.groups, gi = gq % c.groups;
-  const int b = gq & 1;
-  SeamBuf &s = sm.seam[b];
-  const int t0 = gi * SB;
-  const int nt = min(SB, c.w - t0);
-  const int64_t tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + t0;
-  const uint32_t gbytes = (uint32_t)(nt * p.h_v * 4);
-  if (lane == 0) tc::mbar_expect_tx(&sm.seam_full[b], (uint32_t)nt * (3 * 256 + 512));
-  __syncwarp();
-  if (lane < 4 * nt) {
-    const int t = lane >> 2, kind = lane & 3;
-    const int64_t tok = tok0 + t;
-    if (kind == 0)
-      tc::bulk_load(s.k[t], static_cast<const __nv_bfloat16 *>(p.seam_k) + (tok * p.h_k + c.kh) * 128, 256,
-                    &sm.seam_full[b]);
-    else if (kind == 1)
-      tc::bulk_load(s.q[t], static_cast<const __nv_bfloat16 *>(p.seam_q) + (tok * p.h_k + c.kh) * 128, 256,
-                    &sm.seam_full[b]);
-    else if (kind == 2)
-      tc::bulk_load(s.v[t], static_cast<const __nv_bfloat16 *>(p.seam_v) + (tok * p.h_v + c.h) * 128, 256,
-                    &sm.seam_full[b]);
-    else
-      tc::bulk_load(s.gv[t], p.seam_g + (tok * p.h_v + c.h) * 128, 512, &sm.seam_full[b]);
-  }
-  if (lane == 31) prefetch_l2(p.seam_beta + tok0 * p.h_v, gbytes);
-}
-
-__device__ __forceinline__ void prefetch_pair_S(const ComposeParams &p, const Chain &c, int seg) {
-  if (seg >= c.n_seg) return;
-  const int slot = pair_slot(p, c, seg);
-  if (slot < 0) return;
-  prefetch_l2(p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128, 128 * 128 * 4);
 }
 
 // T_C of segment seg's pair (64 KiB) into L2.  Warming S(C|0) as well, or
@@ -183,270 +99,9 @@ __device__ __forceinline__ void prefetch_T(const ComposeParams &p, const Chain &
   prefetch_l2(p.T_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128, 128 * 128 * 4);
 }
 
-__global__ void __launch_bounds__(NT, 2)
-    compose_channel_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tmap_T) {
-  extern __shared__ unsigned char smem_raw[];
-  // 1024-byte alignment by pointer arithmetic on the shared array, so the
-  // compiler keeps every access in the shared address space
-  ComposeTcSmem &sm = *reinterpret_cast<ComposeTcSmem *>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
-  const ComposeParams &p = args.p;
-  const uint32_t LIM = args.wait_limit;
-  const int tid = threadIdx.x;
-  const int n = tid & 127;   // column of S
-  const int hf = tid >> 7;   // rows 64*hf .. 64*hf+63 of that column
-  const int r0 = 64 * hf;
-  const int warp = tid / 32;
-  Chain c;
-  c.l = blockIdx.x / p.h_v;
-  c.h = blockIdx.x % p.h_v;
-  c.kh = (int)(((int64_t)c.h * p.h_k) / p.h_v);
-  c.n_seg = p.n_seg;
-  c.w = p.seam_w;
-  c.groups = (c.w + SB - 1) / SB;
-  const int total_groups = c.n_seg * c.groups;
-  const uint32_t total_slabs = 4u * (uint32_t)c.n_seg;
-
-  if (tid == 0) {
-    for (int i = 0; i < NSLOT; i++) tc::mbar_init(&sm.full[i], 1);
-    tc::mbar_init(&sm.seam_full[0], 1);
-    tc::mbar_init(&sm.seam_full[1], 1);
-    tc::mbar_init(&sm.mma_done, 1);
-    tc::mbar_init(&sm.never, 1);
-    sm.abort = 0;
-    tc::fence_mbar_init();
-  }
-  if (warp == 0) {
-    tc::tmem_alloc(&sm.tmem_base, 256);
-    tc::tmem_relinquish();
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  // warps w and w + 4 share the TMEM lane quadrant w % 4 (lanes = columns)
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t tDh = sm.tmem_base + lane_base + r0, tAh = sm.tmem_base + 128 + lane_base + r0;
-  const uint32_t tD = sm.tmem_base, tA = sm.tmem_base + 128;
-
-  uint32_t issued = 0;  // T_C slabs issued (thread 0)
-  constexpr int SEAM_WARP = 7;  // issues the seam copies, one per lane
-  int seam_issued = min(2, total_groups);  // seam groups issued (the seam warp)
-  if (tid == 0) {
-    tc::prefetch_tmap(&tmap_T);
-    for (; issued < (uint32_t)NSLOT && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued);
-    prefetch_pair_S(p, c, 0);
-    prefetch_pair_S(p, c, 1);
-  }
-  if (warp == SEAM_WARP) {
-    issue_seam_warp(sm, p, c, 0);
-    issue_seam_warp(sm, p, c, 1);
-  }
-
-  if (args.debug_stall && !tc::mbar_wait(&sm.never, 0, LIM)) fail(sm, p);
-
-  // this thread's rows of the state
-  const int64_t state = (int64_t)blockIdx.x * 128 * 128 + (int64_t)r0 * 128 + n;
-  float S[64];
-#pragma unroll
-  for (int i = 0; i < 64; i++) S[i] = p.S_init ? p.S_init[state + (int64_t)i * 128] : 0.f;
-  bool bad = false;
-  const uint32_t id = tc::idesc(tc::FMT_TF32, 128, 128);
-  uint32_t u = 0;          // seam tokens processed (uniform): parity of the exchange buffers
-  int64_t pend = -1;       // lower half: token whose output waits for the upper half's partial
-  float opend = 0.f;
-  // lower half, after a CTA barrier: complete the pending output
-  auto flush = [&]() {
-    if (hf == 0 && pend >= 0) {
-      const float o = opend + sm.os[(u - 1) & 1][n];
-      p.seam_out[(pend * p.h_v + c.h) * 128 + n] = o;
-      bad |= !finite_f(o);
-    }
-    pend = -1;
-  };
-
-  for (int seg = 0; seg < c.n_seg; seg++) {
-    // uniform stop decision
-    if (tid == 0) sm.stop = *(volatile int *)&sm.abort;
-    __syncthreads();
-    const bool stop = *(volatile int *)&sm.stop != 0;
-    __syncthreads();
-    if (stop) break;
-
-    // ---- seam tokens
-    for (int gi = 0; gi < c.groups; gi++) {
-      const int gq = seg * c.groups + gi;
-      const int b = gq & 1;
-      const bool ok = !aborted(sm) && tc::mbar_wait(&sm.seam_full[b], (gq >> 1) & 1, LIM);
-      if (!ok) fail(sm, p);
-      SeamBuf &s = sm.seam[b];
-      const int t0 = gi * SB;
-      const int nt = ok ? min(SB, c.w - t0) : 0;
-      const int64_t tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + t0;
-      // per-channel gates a = exp(g), once per buffer, and this head's betas
-      for (int e = tid; e < nt * 128; e += NT) (&s.gv[0][0])[e] = __expf((&s.gv[0][0])[e]);
-      if (tid < nt) s.b[tid] = p.seam_beta[(tok0 + tid) * p.h_v + c.h];
-      __syncthreads();
-      for (int t = 0; t < nt; t++) {
-        const float *ar = s.gv[t] + r0;
-        const __nv_bfloat16 *kr = s.k[t] + r0;
-        const __nv_bfloat16 *qr = s.q[t] + r0;
-        // S <- Diag(a) S and the half dot product k^T S
-        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 64; i += 8) {
-          float kv[8];
-          unpack8(kr + i, kv);
-          const float4 a0 = *reinterpret_cast<const float4 *>(ar + i);
-          const float4 a1 = *reinterpret_cast<const float4 *>(ar + i + 4);
-          S[i] *= a0.x;
-          S[i + 1] *= a0.y;
-          S[i + 2] *= a0.z;
-          S[i + 3] *= a0.w;
-          S[i + 4] *= a1.x;
-          S[i + 5] *= a1.y;
-          S[i + 6] *= a1.z;
-          S[i + 7] *= a1.w;
-          x0 = fmaf(kv[0], S[i], x0);
-          x1 = fmaf(kv[1], S[i + 1], x1);
-          x2 = fmaf(kv[2], S[i + 2], x2);
-          x3 = fmaf(kv[3], S[i + 3], x3);
-          x0 = fmaf(kv[4], S[i + 4], x0);
-          x1 = fmaf(kv[5], S[i + 5], x1);
-          x2 = fmaf(kv[6], S[i + 6], x2);
-          x3 = fmaf(kv[7], S[i + 7], x3);
-        }
-        sm.xs[u & 1][hf][n] = (x0 + x1) + (x2 + x3);
-        // threads n and n + 128 (warps w and w + 4) exchange through a
-        // 64-thread named barrier of their own
-        tc::named_bar(1 + (warp & 3), 64);
-        flush();  // the previous token's output
-        // both halves sum in the same order: identical x
-        const float x = sm.xs[u & 1][0][n] + sm.xs[u & 1][1][n];
-        const float bt = s.b[t];
-        const float cc = bt * __bfloat162float(s.v[t][n]) - bt * x;
-        // S <- S + k c and the half output q^T S
-        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 64; i += 8) {
-          float kv[8], qv[8];
-          unpack8(kr + i, kv);
-          unpack8(qr + i, qv);
-#pragma unroll
-          for (int j = 0; j < 8; j++) S[i + j] = fmaf(kv[j], cc, S[i + j]);
-          o0 = fmaf(qv[0], S[i], o0);
-          o1 = fmaf(qv[1], S[i + 1], o1);
-          o2 = fmaf(qv[2], S[i + 2], o2);
-          o3 = fmaf(qv[3], S[i + 3], o3);
-          o0 = fmaf(qv[4], S[i + 4], o0);
-          o1 = fmaf(qv[5], S[i + 5], o1);
-          o2 = fmaf(qv[6], S[i + 6], o2);
-          o3 = fmaf(qv[7], S[i + 7], o3);
-        }
-        const float o = (o0 + o1) + (o2 + o3);
-        if (hf) sm.os[u & 1][n] = o;
-        opend = o;
-        pend = tok0 + t;
-        u++;
-      }
-      __syncthreads();  // every thread is done with this seam buffer
-      flush();
-      if (gq + 2 < total_groups && warp == SEAM_WARP && !__shfl_sync(0xffffffffu, aborted(sm), 0)) {
-        issue_seam_warp(sm, p, c, gq + 2);
-        seam_issued = gq + 3;
-      }
-    }
-
-    // ---- S -> TMEM (A operand, tf32 round-to-nearest)
-#pragma unroll
-    for (int ch = 0; ch < 4; ch++) {
-      uint32_t r[16];
-#pragma unroll
-      for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(S[16 * ch + j]);
-      tc::tmem_st16(tAh + 16 * ch, r);
-    }
-    tc::tmem_wait_st();
-    tc::tc_fence_before();
-    __syncthreads();
-    const uint32_t q = 4u * (uint32_t)seg;
-    if (tid == 0) {
-      tc::tc_fence_after();
-      bool ok = !aborted(sm);
-      for (int sl = 0; sl < 4 && ok; sl++) {
-        const uint32_t r = q + sl;
-        const int si = r % NSLOT;
-        if (!tc::mbar_wait(&sm.full[si], (r / NSLOT) & 1, LIM)) {
-          fail(sm, p);
-          ok = false;
-          break;
-        }
-        const uint32_t base = tc::smem_u32(sm.slot[si]);
-#pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
-          const uint64_t bd = tc::smem_desc(base + 32 * kk, 16, 1024, tc::SW_128B);
-          tc::mma_ts_tf32(tD, tA + 32 * sl + 8 * kk, bd, id, (sl | kk) != 0);
-        }
-      }
-      tc::mma_commit(&sm.mma_done);  // arrives once the MMAs above are complete
-    }
-
-    // ---- S <- T_C S + S(C|0): S(C|0) loads in flight while the MMA runs (S
-    // itself is in TMEM A now; a skipped pair keeps S)
-    const int slot = pair_slot(p, c, seg);
-    if (slot < 0 && tid == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
-    const bool use = slot >= 0 && !aborted(sm);
-    if (use) {
-      const float *Sc = p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128 + (int64_t)r0 * 128 + n;
-#pragma unroll
-      for (int j = 0; j < 64; j++) S[j] = Sc[j * 128];
-    }
-    if (!tc::mbar_wait(&sm.mma_done, seg & 1, DRAIN_LIMIT)) fail(sm, p);
-    tc::tc_fence_after();
-    if (tid == 0 && !aborted(sm)) {
-      // this pair's four slots are free: refill them, and warm L2 with the
-      // S(C|0) of the segment after next
-      for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
-      prefetch_pair_S(p, c, seg + 2);
-    }
-    if (use) {
-#pragma unroll
-      for (int ch = 0; ch < 4; ch++) {
-        uint32_t r[16];
-        tc::tmem_ld16(tDh + 16 * ch, r);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; j++) S[16 * ch + j] += __uint_as_float(r[j]);
-      }
-    }
-    tc::tc_fence_before();  // TMEM reads done before the next MMA overwrites D
-  }
-
-  __syncthreads();
-  if (!aborted(sm)) {
-#pragma unroll
-    for (int i = 0; i < 64; i++) {
-      p.S_out[state + (int64_t)i * 128] = S[i];
-      bad |= !finite_f(S[i]);
-    }
-  }
-  if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
-  // drain: every copy issued lands before the CTA releases its smem
-  if (tid == 0) {
-    const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
-    for (uint32_t r = first; r < issued; r++) tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, DRAIN_LIMIT);
-  }
-  if (tid == 32 * SEAM_WARP) {
-    for (int r = seam_issued > 2 ? seam_issued - 2 : 0; r < seam_issued; r++)
-      tc::mbar_wait(&sm.seam_full[r & 1], (r >> 1) & 1, DRAIN_LIMIT);
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc::tc_fence_after();
-    tc::tmem_dealloc(sm.tmem_base, 256);
-  }
-}
-
 // ---------------------------------------------------------------------------
-// Scalar-gate variants (GDN, DeltaNet): the seam tokens on the tensor cores.
+// The seam tokens on the tensor cores (GDN and DeltaNet; the per-channel gate
+// through prep_group_channel above, with the changes described there).
 //
 // For a group of nt <= 8 seam tokens entered with state S0, cumulative
 // log-gates lam_t = g_0 + ... + g_t (DeltaNet: 0) and c_t = b_t (v_t - xh_t),
@@ -671,11 +326,159 @@ __device__ __forceinline__ void prep_group(SeamMmaSmem &sm, const ComposeParams 
   tc::fence_proxy_async_smem();  // the operand tile is read by the tensor cores
 }
 
+// Per-channel gate tiles in the fifth slot (the ring of this variant has
+// four): the T_C k-hat operand (16 rows, K-major, 128-byte swizzle; rows
+// 8..15 zero), k-hat [128][GW] and E_last [128] fp32 for the register path,
+// and reduction scratch.
+struct ChTiles {
+  float *ktile;   // 8 KiB
+  float *khat;    // [128][GW]
+  float *elast;   // [128]
+  float *red;     // [3 warps][64] Gram partials, then [3] minima
+};
+__device__ __forceinline__ ChTiles ch_tiles(SeamMmaSmem &sm) {
+  float *base = reinterpret_cast<float *>(sm.slot[NSLOT - 1]);
+  return ChTiles{base, base + 2048, base + 2048 + 128 * GW, base + 2048 + 128 * GW + 128};
+}
+
+// Per-channel gate: the group constants of gq, by the NPREP preparing
+// threads (beta of token ptid passed in by threads ptid < GW).  With lam_t
+// the per-channel cumulative log-gate over the group and E_t = e^{lam_t},
+// the per-token update S_t = Diag(a_t) S_{t-1} + k_t c_t^T (c_t = b_t (v_t -
+// x_t), x_t = (a_t . k_t)^T S_{t-1}) unrolls to
+//   x_t = (E_t . k_t)^T S0 + sum_{i<t} [sum_ch k_t k_i e^{lam_t - lam_i}] c_i
+//   o_t = (E_t . q_t)^T S0 + sum_{i<=t} [sum_ch q_t k_i e^{lam_t - lam_i}] c_i
+//   S_n = E_last . S0 + sum_i (e^{lam_last - lam_i} . k_i) c_i^T  (rows scaled)
+// A group is fused with the pair when e^{lam_last} >= e^{-80} on every
+// channel (and the seam window is one group): TMEM A then holds RN(E_last .
+// S0) (the epilogue before scales it), so the operand rows are
+// e^{lam_t - lam_last} . k_t and . q_t (<= e^{80}), and
+//   T_C S_n = T_C (E_last . S0) + sum_i (T_C k-hat_i) c_i^T,
+// k-hat_i = e^{lam_last - lam_i} . k_i, one more operand tile.  Otherwise the
+// rows are E_t . k_t and E_t . q_t and the register path updates the exact
+// state with k-hat and E_last.  The Grams take a per-channel weight, summed
+// over the channels directly (2 channels per thread, then a warp tree and the
+// three warps, in a fixed order).  Flags for the kernel: alast = 1 (fused) or
+// 0, ea = 1, eb = 1.
+__device__ __forceinline__ void prep_group_channel(SeamMmaSmem &sm, const ComposeParams &p, const Chain &c, int gq,
+                                                   float b_n) {
+  const int ptid = threadIdx.x - 32 * PREP_WARP0;
+  const SeamGroup sg = seam_group(p, c, gq);
+  const int nt = sg.nt;
+  const SeamRaw &r = sm.raw[gq & 1];
+  GroupConst &G = sm.gc[gq & 1];
+  const ChTiles T = ch_tiles(sm);
+  const int wp = ptid >> 5, lane = ptid & 31;
+  if (ptid < GW) {
+    G.beta[ptid] = b_n;
+    G.ea[ptid] = ptid < nt ? 1.f : 0.f;  // the decay is inside the operand rows
+    G.eb[ptid] = ptid < nt ? 1.f : 0.f;
+  }
+  // pass 1: this thread's channels (ptid and, for ptid < 32, ptid + 96)
+  float lam[2][GW], kt[2][GW], qt[2][GW];
+  float mn = 0.f;
+#pragma unroll
+  for (int u = 0; u < 2; u++) {
+    const int ch = ptid + NPREP * u;
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t < GW; t++) {
+      const bool in = ch < 128 && t < nt;
+      acc += in ? p.seam_g[((sg.tok0 + t) * p.h_v + c.h) * 128 + ch] : 0.f;
+      lam[u][t] = acc;
+      kt[u][t] = in ? __bfloat162float(r.k[t][ch]) : 0.f;
+      qt[u][t] = in ? __bfloat162float(r.q[t][ch]) : 0.f;
+    }
+    if (ch < 128) mn = fminf(mn, pick(lam[u], nt - 1));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  if (lane == 0) T.red[192 + wp] = mn;
+  tc::named_bar(BAR_PREP, NPREP);
+  // fused: a one-group seam window, a valid pair (a skipped pair runs the
+  // register path), and no channel decaying below e^{-80} over the group
+  const bool fuse = c.groups == 1 && pair_slot(p, c, gq / c.groups) >= 0 &&
+                    fminf(fminf(T.red[192], T.red[193]), T.red[194]) >= -80.f;
+  if (ptid == 0) G.alast = fuse ? 1.f : 0.f;
+  // pass 2: tiles and Gram partials
+  float part[64];
+#pragma unroll
+  for (int j = 0; j < 64; j++) part[j] = 0.f;
+#pragma unroll
+  for (int u = 0; u < 2; u++) {
+    const int ch = ptid + NPREP * u;
+    if (ch >= 128) break;
+    const float ll = pick(lam[u], nt - 1);
+    const float sh = fuse ? ll : 0.f;  // operand rows e^{lam_t - sh}
+    unsigned char *slab = reinterpret_cast<unsigned char *>(&sm.bt[ch >> 5][0][0]);
+    unsigned char *kslab = reinterpret_cast<unsigned char *>(T.ktile) + 2048 * (ch >> 5);
+    const int chunk = (ch & 31) >> 2, within = (ch & 3) * 4;
+#pragma unroll
+    for (int t = 0; t < GW; t++) {
+      const float e = __expf(lam[u][t] - sh);
+      *reinterpret_cast<uint32_t *>(slab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(e * kt[u][t]);
+      *reinterpret_cast<uint32_t *>(slab + (GW + t) * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(e * qt[u][t]);
+      const float kh = __expf(ll - lam[u][t]) * kt[u][t];
+      *reinterpret_cast<uint32_t *>(kslab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(kh);
+      T.khat[ch * GW + t] = kh;
+    }
+    T.elast[ch] = __expf(ll);
+#pragma unroll
+    for (int t = 0; t < GW; t++) {
+#pragma unroll
+      for (int i = 0; i <= t; i++) {
+        const float w = __expf(lam[u][t] - lam[u][i]);
+        if (i < t) part[t * (t - 1) / 2 + i] = fmaf(kt[u][t] * kt[u][i], w, part[t * (t - 1) / 2 + i]);
+        part[28 + t * (t + 1) / 2 + i] = fmaf(qt[u][t] * kt[u][i], w, part[28 + t * (t + 1) / 2 + i]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 64; j++) {
+    float v = part[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) T.red[wp * 64 + j] = v;
+  }
+  tc::named_bar(BAR_PREP, NPREP);
+  if (ptid < 64) {
+    const float v = (T.red[ptid] + T.red[64 + ptid]) + T.red[128 + ptid];
+    if (ptid < 28) {
+      const int j = ptid;
+      int t = 1;
+      while (t * (t + 1) / 2 <= j) t++;  // t(t-1)/2 <= j < t(t+1)/2
+      G.gk[t][j - t * (t - 1) / 2] = v;
+    } else {
+      const int j = ptid - 28;
+      int t = 0;
+      while ((t + 1) * (t + 2) / 2 <= j) t++;  // t(t+1)/2 <= j < (t+1)(t+2)/2
+      G.gq[t][j - t * (t + 1) / 2] = v;
+    }
+  }
+  tc::named_bar(BAR_PREP, NPREP);
+  // M: thread j < 8 solves column j by forward substitution
+  if (ptid < GW) {
+    const int j = ptid;
+    float m[GW];
+#pragma unroll
+    for (int t = 0; t < GW; t++) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < t; i++) s = fmaf(G.gk[t][i], (i >= j) ? m[i] : 0.f, s);
+      m[t] = t < j ? 0.f : (t == j ? G.beta[t] : -G.beta[t] * s);
+      G.mm[t][j] = m[t];
+    }
+  }
+  tc::fence_proxy_async_smem();  // the operand tiles are read by the tensor cores
+}
+
 // bulk copies of group gq's k / q / v rows, one per lane of the calling warp
-// (all 32 lanes call); its beta and gate rows (all heads, contiguous) are
-// warmed in L2 for the plain loads one group ahead
-template <bool GDN>
+// (all 32 lanes call); its beta and scalar gate rows (all heads, contiguous)
+// and, for the per-channel gate, this head's gate rows are warmed in L2 for
+// the plain loads of the preparing warps
+template <int VAR>
 __device__ __forceinline__ void issue_raw_warp(SeamMmaSmem &sm, const ComposeParams &p, const Chain &c, int gq) {
+  constexpr bool GDN = VAR == HYPIC_GDN;
   const int lane = threadIdx.x & 31;
   const SeamGroup sg = seam_group(p, c, gq);
   const int b = gq & 1;
@@ -696,11 +499,22 @@ __device__ __forceinline__ void issue_raw_warp(SeamMmaSmem &sm, const ComposePar
     prefetch_l2(p.seam_beta + sg.tok0 * p.h_v, gbytes);
     if (GDN) prefetch_l2(p.seam_g + sg.tok0 * p.h_v, gbytes);
   }
+  // lanes 24 .. 24 + nt - 1 (never copy lanes: 3 nt <= 24): one token's
+  // 512-byte gate row each
+  if (VAR == HYPIC_CHANNEL_DELTA && lane >= 24 && lane - 24 < sg.nt)
+    prefetch_l2(p.seam_g + ((sg.tok0 + (lane - 24)) * p.h_v + c.h) * 128, 512);
 }
 
-template <bool GDN>
+// VAR: HYPIC_GDN, HYPIC_DELTANET or HYPIC_CHANNEL_DELTA
+template <int VAR>
 __global__ void __launch_bounds__(NT2, 2)
     compose_seam_mma_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tmap_T) {
+  constexpr bool GDN = VAR == HYPIC_GDN;
+  constexpr bool CH = VAR == HYPIC_CHANNEL_DELTA;
+  // the per-channel gate streams T_C through four slots; the fifth holds its
+  // group tiles (the T_C k-hat operand, k-hat and E_last for the register
+  // path, reduction scratch)
+  constexpr int RING = CH ? 4 : NSLOT;
   extern __shared__ unsigned char smem_raw[];
   SeamMmaSmem &sm = *reinterpret_cast<SeamMmaSmem *>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   const ComposeParams &p = args.p;
@@ -753,11 +567,11 @@ __global__ void __launch_bounds__(NT2, 2)
   int raw_issued = min(2, total_groups);  // seam groups issued (uniform)
   if (tid == 0) {
     tc::prefetch_tmap(&tmap_T);
-    for (; issued < (uint32_t)NSLOT && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued);
+    for (; issued < (uint32_t)RING && issued < total_slabs; issued++) issue_slab(sm, p, c, &tmap_T, issued, RING);
     for (int s = 0; s < 2; s++) prefetch_T(p, c, s);
   }
   if (warp == ISSUER_WARP) {
-    for (int g = 0; g < raw_issued; g++) issue_raw_warp<GDN>(sm, p, c, g);
+    for (int g = 0; g < raw_issued; g++) issue_raw_warp<VAR>(sm, p, c, g);
   }
 
   if (args.debug_stall && !tc::mbar_wait(&sm.never, 0, LIM)) fail(sm, p);
@@ -794,14 +608,17 @@ __global__ void __launch_bounds__(NT2, 2)
   auto prepare = [&](int gq) {
     const bool ok = !aborted(sm) && tc::mbar_wait(&sm.raw_full[gq & 1], (gq >> 1) & 1, LIM);
     if (!ok) fail(sm, p);
-    prep_group(sm, p, c, gq, pb, pg);
+    if (CH)
+      prep_group_channel(sm, p, c, gq, pb);
+    else
+      prep_group(sm, p, c, gq, pb, pg);
     load_bg(gq + 1);
   };
   // after a barrier that follows group gq's recurrence: its raw buffer is
   // free, refill it with group gq + 2 (uniform call; the issuer warp copies)
   auto release_raw = [&](int gq) {
     if (gq + 2 < total_groups) {
-      if (warp == ISSUER_WARP && !aborted(sm)) issue_raw_warp<GDN>(sm, p, c, gq + 2);
+      if (warp == ISSUER_WARP && !aborted(sm)) issue_raw_warp<VAR>(sm, p, c, gq + 2);
       raw_issued = gq + 3;
     }
   };
@@ -839,7 +656,7 @@ __global__ void __launch_bounds__(NT2, 2)
   // D = S^T T_C^T from TMEM A and the four K-slabs at ring position q (issuer)
   auto issue_T_mma = [&](uint32_t q) {
     for (int sl = 0; sl < 4; sl++) {
-      const uint32_t base = tc::smem_u32(sm.slot[(q + sl) % NSLOT]);
+      const uint32_t base = tc::smem_u32(sm.slot[(q + sl) % RING]);
 #pragma unroll
       for (int kk = 0; kk < 4; kk++) {
         const uint64_t bd = tc::smem_desc(base + 32 * kk, 16, 1024, tc::SW_128B);
@@ -856,13 +673,13 @@ __global__ void __launch_bounds__(NT2, 2)
     if (!tc::mbar_wait(&sm.t_done, ph, DRAIN_LIMIT)) fail(sm, p);
     tc::mbar_expect_tx(&sm.sc_full, 4 * SLAB);
     const float *src = p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128;
-    for (int j = 0; j < 4; j++) tc::bulk_load(sm.slot[(q + j) % NSLOT], src + j * 32 * 128, SLAB, &sm.sc_full);
+    for (int j = 0; j < 4; j++) tc::bulk_load(sm.slot[(q + j) % RING], src + j * 32 * 128, SLAB, &sm.sc_full);
   };
   // the four K-slabs at ring position q have landed (one thread)
   auto wait_slabs = [&](uint32_t q) {
     for (int sl = 0; sl < 4; sl++) {
       const uint32_t r = q + sl;
-      if (!tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, LIM)) {
+      if (!tc::mbar_wait(&sm.full[r % RING], (r / RING) & 1, LIM)) {
         fail(sm, p);
         return false;
       }
@@ -900,16 +717,30 @@ __global__ void __launch_bounds__(NT2, 2)
     }
   };
 
+  if (CH) {
+    // rows 8..15 of the T_C k-hat operand stay zero
+    float *kt = ch_tiles(sm).ktile;
+    for (int e = tid; e < 4 * 256; e += NT2) kt[(e >> 8) * 512 + 256 + (e & 255)] = 0.f;
+  }
   if (preper) {
     load_bg(0);
     if (has_seam) prepare(0);
   }
-  // RN(S_init) -> TMEM A
+  // RN(S_init) -> TMEM A (per-channel gate, first group fused: RN(E_last .
+  // S_init))
+  bool scale0 = false;
+  if (CH) {
+    __syncthreads();  // the first group's constants and tiles
+    scale0 = has_seam && c.n_seg > 0 && pair_slot(p, c, 0) >= 0 && sm.gc[0].alast >= AL_MIN;
+  }
 #pragma unroll
   for (int b = 0; b < 4; b++) {
     uint32_t r[16];
 #pragma unroll
-    for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(exact ? exact[(int64_t)(16 * b + j) * 128] : 0.f);
+    for (int j = 0; j < 16; j++) {
+      const float x = exact ? exact[(int64_t)(16 * b + j) * 128] : 0.f;
+      r[j] = tc::to_tf32(CH && scale0 ? x * ch_tiles(sm).elast[64 * hf + 16 * b + j] : x);
+    }
     tc::tmem_st16(tAh + 16 * b, r);
   }
   tc::tmem_wait_st();
@@ -932,7 +763,7 @@ __global__ void __launch_bounds__(NT2, 2)
       // bulk copies)
       refill_pending = false;
       if (!aborted(sm)) {
-        for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
+        for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued, RING);
         prefetch_T(p, c, seg + 1);
       }
     }
@@ -970,34 +801,66 @@ __global__ void __launch_bounds__(NT2, 2)
         float cc[GW];
         seam_recurrence(d, gq, cc);
         const GroupConst &G = sm.gc[gq & 1];
-#pragma unroll
-        for (int i = 0; i < GW; i++) cc[i] *= G.eb[i];
-        const float al = G.alast;
-        const float *bt = &sm.bt[0][0][0] + 1024 * hf;  // K-slabs 2*hf, 2*hf+1 hold this thread's rows
-        // 16 rows at a time: their exact values are loaded together, and
-        // RN(S) of the block goes straight to TMEM A
+        if (CH) {
+          // row r: S <- E_last[r] S + sum_i k-hat_i[r] c_i (k-hat and E_last
+          // from the tk / cp tiles)
+          const float *kh = ch_tiles(sm).khat + 64 * hf * GW;
+          const float *el = ch_tiles(sm).elast + 64 * hf;
 #pragma unroll 1
-        for (int r0 = 0; r0 < 64; r0 += 16) {
-          float ex[16];
+          for (int r0 = 0; r0 < 64; r0 += 16) {
+            float ex[16];  // 16 independent loads in flight
 #pragma unroll
-          for (int j = 0; j < 16; j++) ex[j] = exact ? exact[(int64_t)(r0 + j) * 128] : 0.f;
+            for (int j = 0; j < 16; j++) ex[j] = exact ? exact[(int64_t)(r0 + j) * 128] : 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; j++) {
-            const int rr = r0 + j;
-            float x = al * ex[j];
-            const float *row = bt + (rr >> 5) * 512 + (rr & 3);
-            const int chunk = (rr & 31) >> 2;
+            for (int j = 0; j < 16; j++) {
+              const int rr = r0 + j;
+              const float4 k0 = *reinterpret_cast<const float4 *>(kh + rr * GW);
+              const float4 k1 = *reinterpret_cast<const float4 *>(kh + rr * GW + 4);
+              float x = el[rr] * ex[j];
+              x = fmaf(k0.x, cc[0], x);
+              x = fmaf(k0.y, cc[1], x);
+              x = fmaf(k0.z, cc[2], x);
+              x = fmaf(k0.w, cc[3], x);
+              x = fmaf(k1.x, cc[4], x);
+              x = fmaf(k1.y, cc[5], x);
+              x = fmaf(k1.z, cc[6], x);
+              x = fmaf(k1.w, cc[7], x);
+              out[(int64_t)rr * 128] = x;
+              ex[j] = x;
+            }
+            uint32_t rn[16];
 #pragma unroll
-            for (int i = 0; i < GW; i++) x = fmaf(row[i * 32 + ((chunk ^ i) << 2)], cc[i], x);
-            out[(int64_t)rr * 128] = x;
-            ex[j] = x;
+            for (int j = 0; j < 16; j++) rn[j] = tc::to_tf32(ex[j]);
+            tc::tmem_st16(tAh + r0, rn);
           }
-          uint32_t rn[16];
+        } else {
 #pragma unroll
-          for (int j = 0; j < 16; j++) rn[j] = tc::to_tf32(ex[j]);
-          tc::tmem_st16(tAh + r0, rn);
+          for (int i = 0; i < GW; i++) cc[i] *= G.eb[i];
+          const float al = G.alast;
+          const float *bt = &sm.bt[0][0][0] + 1024 * hf;  // K-slabs 2*hf, 2*hf+1 hold this thread's rows
+#pragma unroll 1
+          for (int r0 = 0; r0 < 64; r0 += 16) {
+            float ex[16];  // 16 independent loads in flight
+#pragma unroll
+            for (int j = 0; j < 16; j++) ex[j] = exact ? exact[(int64_t)(r0 + j) * 128] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+              const int rr = r0 + j;
+              float x = al * ex[j];
+              const float *row = bt + (rr >> 5) * 512 + (rr & 3);
+              const int chunk = (rr & 31) >> 2;
+#pragma unroll
+              for (int i = 0; i < GW; i++) x = fmaf(row[i * 32 + ((chunk ^ i) << 2)], cc[i], x);
+              out[(int64_t)rr * 128] = x;
+              ex[j] = x;
+            }
+            uint32_t rn[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) rn[j] = tc::to_tf32(ex[j]);
+            tc::tmem_st16(tAh + r0, rn);
+          }
         }
-        exact = out;
+        exact = out;  // RN(S) went to TMEM A row block by row block above
       }
       tc::tmem_wait_st();
       tc::tc_fence_before();
@@ -1010,10 +873,27 @@ __global__ void __launch_bounds__(NT2, 2)
       // a bad slot skips the pair; its slabs (loaded from slot 0) still pass
       // through the ring
       if (tid == 0 && !aborted(sm) && wait_slabs(q)) {
-        for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued);
+        for (int sl = 0; sl < 4 && issued < total_slabs; sl++, issued++) issue_slab(sm, p, c, &tmap_T, issued, RING);
         prefetch_T(p, c, seg + 2);
       }
       if (preper && !last && has_seam) prepare(gq_next);
+      if (CH && !last && has_seam) {
+        // the epilogue that scales TMEM A is skipped: if the next group is
+        // fused, A <- RN(E_last . S) from the exact state the register path
+        // left in S_out
+        __syncthreads();
+        if (sm.gc[gq_next & 1].alast >= AL_MIN && !aborted(sm)) {
+          const float *el = ch_tiles(sm).elast + 64 * hf;
+#pragma unroll
+          for (int b = 0; b < 4; b++) {
+            uint32_t r[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) r[j] = tc::to_tf32(out[(int64_t)(16 * b + j) * 128] * el[16 * b + j]);
+            tc::tmem_st16(tAh + 16 * b, r);
+          }
+          tc::tmem_wait_st();
+        }
+      }
       tc::tc_fence_before();
       continue;
     }
@@ -1045,12 +925,12 @@ __global__ void __launch_bounds__(NT2, 2)
         tc::mma_commit(&sm.seam_done);
         const uint32_t r = q + a;
         if (!aborted(sm)) {
-          if (!tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, LIM)) {
+          if (!tc::mbar_wait(&sm.full[r % RING], (r / RING) & 1, LIM)) {
             fail(sm, p);
           } else {
             // D cols 32 a + 16 .. 32 a + 31: lane r holds partial (T_C k_i)[r]
-            const uint32_t abase = tc::smem_u32(sm.slot[r % NSLOT]);
-            const uint32_t bbase = tc::smem_u32(&sm.bt[0][0][0]) + 2048 * a;
+            const uint32_t abase = tc::smem_u32(sm.slot[r % RING]);
+            const uint32_t bbase = (CH ? tc::smem_u32(ch_tiles(sm).ktile) : tc::smem_u32(&sm.bt[0][0][0])) + 2048 * a;
 #pragma unroll
             for (int kk = 0; kk < 4; kk++) {
               const uint64_t ad = tc::smem_desc(abase + 32 * kk, 16, 1024, tc::SW_128B);
@@ -1148,6 +1028,8 @@ __global__ void __launch_bounds__(NT2, 2)
     // the exact state is needed after this segment if it is the last one or
     // if the next one runs a register-path group
     const bool keep = last || slot_next < 0 || c.groups > 1 || (has_seam && sm.gc[gq_next & 1].alast < AL_MIN);
+    const bool scale_next = CH && !keep && has_seam;  // the next segment's group is fused
+    const float *el_next = CH ? ch_tiles(sm).elast + 64 * hf : nullptr;
     wait_mma();
     // (the copies are issued on every applied pair, aborted or not, and always land)
     if (!tc::mbar_wait(&sm.sc_full, npair & 1, DRAIN_LIMIT)) fail(sm, p);
@@ -1155,8 +1037,8 @@ __global__ void __launch_bounds__(NT2, 2)
     if (tid == 0) refill_pending = true;  // at the top of the next segment, after every read of the slots
     const bool use = !aborted(sm);
     if (use) {
-      const float *sc0 = reinterpret_cast<const float *>(sm.slot[(q + 2 * hf) % NSLOT]) + n;
-      const float *sc1 = reinterpret_cast<const float *>(sm.slot[(q + 2 * hf + 1) % NSLOT]) + n;
+      const float *sc0 = reinterpret_cast<const float *>(sm.slot[(q + 2 * hf) % RING]) + n;
+      const float *sc1 = reinterpret_cast<const float *>(sm.slot[(q + 2 * hf + 1) % RING]) + n;
 #pragma unroll
       for (int b = 0; b < 4; b++) {
         uint32_t r[16];
@@ -1170,7 +1052,8 @@ __global__ void __launch_bounds__(NT2, 2)
           const float x = fmaf(al, __uint_as_float(r[j]), sc[j]);
           if (keep) out[(int64_t)(16 * b + j) * 128] = x;
           if (last) bad |= !finite_f(x);
-          r[j] = tc::to_tf32(x);
+          // per-channel gate, next group fused: TMEM A holds RN(E_last . S)
+          r[j] = tc::to_tf32(CH && scale_next ? x * el_next[16 * b + j] : x);
         }
         tc::tmem_st16(tAh + 16 * b, r);
       }
@@ -1188,8 +1071,8 @@ __global__ void __launch_bounds__(NT2, 2)
   if ((p.flags & HYPIC_FLAG_CHECK_FINITE) && bad) report(p.status, HYPIC_STATUS_NONFINITE);
   // drain: every copy issued lands before the CTA releases its smem
   if (tid == 0) {
-    const uint32_t first = issued > (uint32_t)NSLOT ? issued - NSLOT : 0;
-    for (uint32_t r = first; r < issued; r++) tc::mbar_wait(&sm.full[r % NSLOT], (r / NSLOT) & 1, DRAIN_LIMIT);
+    const uint32_t first = issued > (uint32_t)RING ? issued - RING : 0;
+    for (uint32_t r = first; r < issued; r++) tc::mbar_wait(&sm.full[r % RING], (r / RING) & 1, DRAIN_LIMIT);
     for (int r = raw_issued > 2 ? raw_issued - 2 : 0; r < raw_issued; r++)
       tc::mbar_wait(&sm.raw_full[r & 1], (r >> 1) & 1, DRAIN_LIMIT);
   }
@@ -1245,13 +1128,11 @@ bool compose_tc_supported(const ComposeParams &p) {
 cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s) {
   CUtensorMap tmap;
   if (!make_tmap_f32_rows(&tmap, p.T_pool, (uint64_t)p.n_slots * p.h_v * 128, 128)) return cudaErrorInvalidValue;
-  // scalar gates: seam tokens on the tensor cores; per-channel gates: the
-  // token-by-token seam
-  const bool vec = p.variant == HYPIC_CHANNEL_DELTA;
-  const size_t smem = (vec ? sizeof(ComposeTcSmem) : sizeof(SeamMmaSmem)) + 1024;
-  auto kern = vec                       ? compose_channel_kernel
-              : p.variant == HYPIC_GDN ? compose_seam_mma_kernel<true>
-                                       : compose_seam_mma_kernel<false>;
+  // seam tokens on the tensor cores for every dense variant
+  const size_t smem = sizeof(SeamMmaSmem) + 1024;
+  auto kern = p.variant == HYPIC_GDN        ? compose_seam_mma_kernel<HYPIC_GDN>
+              : p.variant == HYPIC_DELTANET ? compose_seam_mma_kernel<HYPIC_DELTANET>
+                                            : compose_seam_mma_kernel<HYPIC_CHANNEL_DELTA>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.n_layers * p.h_v;
@@ -1260,7 +1141,7 @@ cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaS
   a.p = p;
   a.wait_limit = wait_limit;
   a.debug_stall = debug_stall() ? 1 : 0;
-  kern<<<grid, vec ? NT : NT2, smem, s>>>(a, tmap);
+  kern<<<grid, NT2, smem, s>>>(a, tmap);
   return cudaGetLastError();
 }
 

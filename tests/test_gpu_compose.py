@@ -74,10 +74,11 @@ def test_compose_tc_parity(variant, w):
         assert e.max() <= TOL_BF16, e.max()
 
 
-def test_compose_tc_bad_slot_reported_and_skipped():
-    W = si.workload(5, device=DEV, variant="deltanet", lengths=[30, 40, 50], h_k=1, h_v=4, seam_w=8)
+@pytest.mark.parametrize("variant", ["deltanet", "channel"])
+def test_compose_tc_bad_slot_reported_and_skipped(variant):
+    W = si.workload(5, device=DEV, variant=variant, lengths=[30, 40, 50, 60], h_k=1, h_v=4, seam_w=8)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    slot = torch.tensor([[0, 99, 2]], dtype=torch.int32, device=DEV)
+    slot = torch.tensor([[0, 99, 2, 3]], dtype=torch.int32, device=DEV)
     T_pool, S_pool, sa, _, S_out, seam_out = _run(W, 1, status=status, slot=slot)
     assert hy.status_from_word(int(status.item())) == 7   # HYPIC_ERR_BAD_SLOT
     # the chain skipped the bad pair: same as composing with (I, 0) there
@@ -85,9 +86,9 @@ def test_compose_tc_bad_slot_reported_and_skipped():
     S2 = S_pool.clone()
     T2[1] = torch.eye(128, device=DEV)
     S2[1] = 0
-    ok_slot = torch.tensor([[0, 1, 2]], dtype=torch.int32, device=DEV)
+    ok_slot = torch.tensor([[0, 1, 2, 3]], dtype=torch.int32, device=DEV)
     ref = torch.empty_like(S_out)
-    hy.compose(ok_slot, T2, S2, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"], variant="deltanet", S_out=ref,
+    hy.compose(ok_slot, T2, S2, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"], variant=variant, S_out=ref,
                seam_out=torch.empty_like(seam_out))
     torch.cuda.synchronize()
     assert per_head_rel_err(S_out, ref).max() <= TOL_BF16
@@ -172,3 +173,29 @@ def test_compose_span_parallel(variant, w, n_spans):
         e = per_head_rel_err(seam_out.permute(0, 3, 1, 2, 4).reshape(2, W.h_v, -1),
                              np.transpose(seam, (0, 3, 1, 2, 4)).reshape(2, W.h_v, -1), inner=1)
         assert e.max() <= TOL_BF16, e.max()
+
+
+def test_compose_channel_steep_gates():
+    """Per-channel gates: a few channels decay below e^-80 over a seam group
+    (those groups take the exact-state path), the rest stay mild (fused with
+    the pair); both against the oracle composing the same fp32 pairs."""
+    lens = [40, 130, 64, 300, 25, 90]
+    W = si.workload(5, device=DEV, variant="channel", lengths=lens, h_k=2, h_v=4, seam_w=8)
+    pools = [gpu_build(W)]
+    T_pool, S_pool = pools[0]
+    sa = seam_arrays(W, [0])
+    g = sa["g"].clone()
+    g[0, 1::2, :, :, 5::17] *= 40.0  # odd segments: a few channels decay steeply
+    S_init = si.random_state((1, W.h_v, 128, 128), seed=2, cfg=5, device=DEV)
+    slot = torch.arange(W.n_seg, dtype=torch.int32, device=DEV).reshape(1, W.n_seg)
+    S_out = torch.empty((1, W.h_v, 128, 128), device=DEV)
+    seam_out = torch.zeros((1, W.n_seg, W.seam_w, W.h_v, 128), device=DEV)
+    hy.compose(slot, T_pool, S_pool, sa["k"], sa["v"], sa["q"], g, sa["beta"], variant="channel", S_out=S_out,
+               seam_out=seam_out, S_init=S_init)
+    torch.cuda.synchronize()
+    So, seam = oracle.compose("channel", T_pool.cpu()[None], S_pool.cpu()[None], sa["k"].cpu(), sa["v"].cpu(),
+                              sa["q"].cpu(), g.cpu(), sa["beta"].cpu(), W.h_k, W.h_v, S_init=S_init.cpu())
+    assert per_head_rel_err(S_out, So).max() <= TOL_BF16
+    e = per_head_rel_err(seam_out.permute(0, 3, 1, 2, 4).reshape(1, W.h_v, -1),
+                         np.transpose(seam, (0, 3, 1, 2, 4)).reshape(1, W.h_v, -1), inner=1)
+    assert e.max() <= TOL_BF16, e.max()
