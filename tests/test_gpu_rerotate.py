@@ -52,7 +52,7 @@ CASES = [("gdn", "interleaved", 128, 128, 128), ("gdn", "half", 128, 128, 128), 
 
 @pytest.mark.parametrize("variant,layout,rot,d_k,d_v", CASES)
 def test_rerotate_vs_oracle(variant, layout, rot, d_k, d_v):
-    h_v = 6  # not a multiple of the four heads a CTA takes
+    h_v = 6  # not a multiple of the eight heads a CTA takes
     T, S = _pools(variant, 5, h_v, d_k, d_v, seed=rot + d_k)
     deltas = [0, 1, -37, 1000003, -999983]
     slot_in, slot_out = [4, 0, 2, 1, 3], [0, 1, 2, 3, 4]
