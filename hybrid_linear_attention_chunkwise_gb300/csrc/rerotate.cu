@@ -42,6 +42,8 @@ struct __align__(128) RerotSmem {
   float buf[NBUF][128 * 128];  // (slot, head) blocks of T or S
   float C[128], G[128];
   int P[128];
+  int PQ[32], SW[32];  // per channel quad: the quad holding its partners, and
+                       // whether partners sit swapped within it (interleaved)
   uint64_t full[NBUF];
 };
 
@@ -105,6 +107,17 @@ __global__ void __launch_bounds__(NT, 1) rerotate_kernel(const RerotateParams p,
     sm.G[a] = g;
     sm.P[a] = partner;
   }
+  __syncthreads();  // channel table visible
+  // Quad q's partners, channel by channel, are the quad P[4q] / 4: for the
+  // interleaved pairing that is q itself with neighbours swapped (a channel
+  // of the quad left unrotated has G = 0, so its swapped partner adds a
+  // zero); for the half pairing (rot_dim a multiple of 8) a quad lies wholly
+  // in one half or wholly unrotated, so its partners form one aligned quad.
+  if (tid < dk / 4) {
+    const int pa = sm.P[4 * tid];
+    sm.PQ[tid] = pa / 4;
+    sm.SW[tid] = pa == 4 * tid + 1;
+  }
   if (!dense && tid < min(HPC, p.h_v - h0))  // gamma^L I commutes with R
     p.T_out[(int64_t)so * p.h_v + h0 + tid] = p.T_in[(int64_t)si * p.h_v + h0 + tid];
   __syncthreads();  // table and barrier init visible
@@ -123,23 +136,51 @@ __global__ void __launch_bounds__(NT, 1) rerotate_kernel(const RerotateParams p,
     const float *blk = sm.buf[j % NBUF];
     const int h = head(j);
     if (ok && is_T(j)) {
+      // four outputs (a, b0 .. b0 + 3) per step from 16-byte loads: the
+      // quad of b0 and its partner quad (swapped in place when the pairs
+      // are interleaved), in rows a and P[a]
       const int q4 = dk / 4;
       float *dst = p.T_out + ((int64_t)so * p.h_v + h) * dk * dk;
-      for (int idx = tid; idx < dk * q4; idx += NT) {
-        const int a = idx / q4, b0 = 4 * (idx % q4);
+      auto rot4 = [&](int a, int bq, const float4 cb, const float4 gb, int pq, bool sw) {
         const float ca = sm.C[a], ga = sm.G[a];
         const float *ra = blk + a * dk, *rp = blk + sm.P[a] * dk;
-        float o[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; jj++) {
-          const int b = b0 + jj, pb = sm.P[b];
-          const float cb = sm.C[b], gb = sm.G[b];
-          // R[a][a] T[a][.] R[b][.] + R[a][P a] T[P a][.] R[b][.]
-          const float top = fmaf(cb, ra[b], gb * ra[pb]);
-          const float bot = fmaf(cb, rp[b], gb * rp[pb]);
-          o[jj] = fmaf(ca, top, ga * bot);
+        const float4 xa = *reinterpret_cast<const float4 *>(ra + 4 * bq);
+        const float4 xp = *reinterpret_cast<const float4 *>(rp + 4 * bq);
+        float4 ya = *reinterpret_cast<const float4 *>(ra + 4 * pq);
+        float4 yp = *reinterpret_cast<const float4 *>(rp + 4 * pq);
+        if (sw) {
+          ya = make_float4(ya.y, ya.x, ya.w, ya.z);
+          yp = make_float4(yp.y, yp.x, yp.w, yp.z);
         }
-        *reinterpret_cast<float4 *>(dst + a * dk + b0) = make_float4(o[0], o[1], o[2], o[3]);
+        // R[a][a] T[a][.] R[b][.] + R[a][P a] T[P a][.] R[b][.]
+        auto one = [&](float cbj, float gbj, float xaj, float yaj, float xpj, float ypj) {
+          return fmaf(ca, fmaf(cbj, xaj, gbj * yaj), ga * fmaf(cbj, xpj, gbj * ypj));
+        };
+        *reinterpret_cast<float4 *>(dst + a * dk + 4 * bq) =
+            make_float4(one(cb.x, gb.x, xa.x, ya.x, xp.x, yp.x), one(cb.y, gb.y, xa.y, ya.y, xp.y, yp.y),
+                        one(cb.z, gb.z, xa.z, ya.z, xp.z, yp.z), one(cb.w, gb.w, xa.w, ya.w, xp.w, yp.w));
+      };
+      auto quad = [&](int bq, float4 &cb, float4 &gb, int &pq, bool &sw) {
+        cb = *reinterpret_cast<const float4 *>(sm.C + 4 * bq);
+        gb = *reinterpret_cast<const float4 *>(sm.G + 4 * bq);
+        pq = sm.PQ[bq];
+        sw = sm.SW[bq] != 0;
+      };
+      if (NT % q4 == 0) {  // each thread keeps one column quad
+        const int bq = tid % q4;
+        float4 cb, gb;
+        int pq;
+        bool sw;
+        quad(bq, cb, gb, pq, sw);
+        for (int a = tid / q4; a < dk; a += NT / q4) rot4(a, bq, cb, gb, pq, sw);
+      } else {
+        for (int idx = tid; idx < dk * q4; idx += NT) {
+          float4 cb, gb;
+          int pq;
+          bool sw;
+          quad(idx % q4, cb, gb, pq, sw);
+          rot4(idx / q4, idx % q4, cb, gb, pq, sw);
+        }
       }
     } else if (ok) {
       const int v4 = dv / 4;
