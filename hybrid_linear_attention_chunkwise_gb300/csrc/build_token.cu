@@ -19,6 +19,7 @@
 // list scheduling in LPT order); an item's result does not depend on which
 // block computes it.
 #include <cstddef>
+#include <cstdint>
 
 #include <cuda_runtime.h>
 
@@ -31,6 +32,19 @@ namespace {
 __device__ __forceinline__ void tc_named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 constexpr int TB = 16;  // tokens per shared-memory tile
+
+// Ampere-style asynchronous copies into shared memory (16 bytes bypassing
+// L1, or 4 bytes), completed per thread by a group wait
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 template <int DK>
 struct TokSmem {
@@ -246,8 +260,30 @@ constexpr bool fwd_rows_aligned() {
 static_assert(fwd_rows_aligned<16>() && fwd_rows_aligned<32>() && fwd_rows_aligned<64>() && fwd_rows_aligned<128>(),
               "16-byte shared-memory rows");
 
+// One stage of raw (input-dtype) token inputs for a tile, copied ahead by
+// cp.async: k and q rows (DK elements apart), v rows (128 apart), the gate
+// (a row of d_k floats per token for vector gates, else one float) and beta.
+// Every part starts on a 16-byte boundary.
+struct FwdRaw {
+  int k, q, v, g, b, bytes;
+};
+__host__ __device__ inline FwdRaw fwd_raw_layout(int DK, int es, bool vec) {
+  FwdRaw r;
+  r.k = 0;
+  r.q = TB * DK * es;
+  r.v = 2 * TB * DK * es;
+  r.g = r.v + TB * 128 * es;
+  r.b = r.g + (vec ? TB * DK * 4 : TB * 4);
+  r.bytes = r.b + TB * 4;
+  return r;
+}
 template <int DK>
-__global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp) {
+__host__ __device__ constexpr size_t fwd_raw_offset() {
+  return (sizeof(FwdSmem<DK>) + 15) / 16 * 16;
+}
+
+template <int DK>
+__global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp, int async_tiles) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   FwdSmem<DK> &fs = *reinterpret_cast<FwdSmem<DK> *>(smem_raw);
   TokSmem<DK> &sm = fs.t;
@@ -260,6 +296,9 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
   const bool active = col < d_v;
   const int bar = 1 + col / 32;  // the pair of warps holding this column
   const int n_items = p.plan->n_items;
+  const int es = p.in_dtype == HYPIC_IN_BF16 ? 2 : 4;
+  const FwdRaw lay = fwd_raw_layout(DK, es, vec);
+  unsigned char *raw = smem_raw + fwd_raw_offset<DK>();  // two stages when async_tiles
 
   for (;;) {
     if (tid == 0) sm.item = atomicAdd(&p.plan->ticket, 1);
@@ -310,36 +349,115 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
       pend = -1;
     };
 
-    for (int64_t t0 = it.start; t0 < it.end; t0 += TB) {
+    // raw inputs of the tile at t0 (nt tokens) into stage st, by cp.async
+    auto issue_tile = [&](int64_t t0, int nt, int st) {
+      unsigned char *base = raw + st * lay.bytes;
+      const int ck = d_k * es / 16, cv = d_v * es / 16;
+      const char *kb = static_cast<const char *>(p.k), *qb = static_cast<const char *>(p.q);
+      const char *vb = static_cast<const char *>(p.v);
+      for (int e = tid; e < nt * ck; e += blockDim.x) {
+        const int t = e / ck, c = e % ck;
+        const int64_t src = ((t0 + t) * p.h_k + kh) * (int64_t)d_k * es + 16 * c;
+        cp_async16(base + lay.k + t * DK * es + 16 * c, kb + src);
+        cp_async16(base + lay.q + t * DK * es + 16 * c, qb + src);
+      }
+      for (int e = tid; e < nt * cv; e += blockDim.x) {
+        const int t = e / cv, c = e % cv;
+        cp_async16(base + lay.v + t * 128 * es + 16 * c, vb + ((t0 + t) * p.h_v + h) * (int64_t)d_v * es + 16 * c);
+      }
+      if (vec) {
+        const int cg = d_k / 4;
+        for (int e = tid; e < nt * cg; e += blockDim.x) {
+          const int t = e / cg, c = e % cg;
+          cp_async16(base + lay.g + (t * DK + 4 * c) * 4, p.g + ((t0 + t) * p.h_v + h) * (int64_t)d_k + 4 * c);
+        }
+      } else if (p.variant == HYPIC_GDN) {
+        for (int t = tid; t < nt; t += blockDim.x) cp_async4(base + lay.g + 4 * t, p.g + (t0 + t) * p.h_v + h);
+      }
+      if (delta)
+        for (int t = tid; t < nt; t += blockDim.x) cp_async4(base + lay.b + 4 * t, p.beta + (t0 + t) * p.h_v + h);
+      cp_async_commit();
+    };
+    auto raw_in = [&](const unsigned char *b, int i) -> float {
+      return es == 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(b)[i])
+                     : reinterpret_cast<const float *>(b)[i];
+    };
+    const int64_t first_nt = (it.end - it.start) < TB ? (it.end - it.start) : TB;
+    if (async_tiles && first_nt > 0) issue_tile(it.start, (int)first_nt, 0);
+
+    int ti = 0;
+    for (int64_t t0 = it.start; t0 < it.end; t0 += TB, ti++) {
       const int nt = (int)((it.end - t0) < TB ? (it.end - t0) : TB);
-      for (int e = tid; e < TB * DK; e += blockDim.x) {
-        const int t = e / DK, i = e % DK;
-        float kv = 0.f, qv = 0.f, a = 1.f;
-        if (t < nt && i < d_k) {
-          kv = load_in(p.k, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype);
-          qv = load_in(p.q, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype);
-          if (vec) a = expf(p.g[((t0 + t) * p.h_v + h) * (int64_t)d_k + i]);
+      if (async_tiles) {
+        cp_async_wait_all();
+        __syncthreads();  // this tile's raw inputs visible to all threads
+        const unsigned char *base = raw + (ti & 1) * lay.bytes;
+        for (int e = tid; e < TB * DK; e += blockDim.x) {
+          const int t = e / DK, i = e % DK;
+          float kv = 0.f, qv = 0.f, a = 1.f;
+          if (t < nt && i < d_k) {
+            kv = raw_in(base + lay.k, t * DK + i);
+            qv = raw_in(base + lay.q, t * DK + i);
+            if (vec) a = expf(reinterpret_cast<const float *>(base + lay.g)[t * DK + i]);
+          }
+          sm.k[t][i] = kv;
+          fs.q[t][i] = qv;
+          if (vec) {
+            sm.a[t][i] = a;
+            sm.kd[t][i] = kv * a;
+          }
         }
-        sm.k[t][i] = kv;
-        fs.q[t][i] = qv;
-        if (vec) {
-          sm.a[t][i] = a;
-          sm.kd[t][i] = kv * a;
+        for (int e = tid; e < TB * 128; e += blockDim.x) {
+          const int t = e / 128, j = e % 128;
+          sm.v[t][j] = (t < nt && j < d_v) ? raw_in(base + lay.v, t * 128 + j) : 0.f;
         }
-      }
-      for (int e = tid; e < TB * 128; e += blockDim.x) {
-        const int t = e / 128, j = e % 128;
-        sm.v[t][j] = (t < nt && j < d_v) ? load_in(p.v, ((t0 + t) * p.h_v + h) * (int64_t)d_v + j, p.in_dtype) : 0.f;
-      }
-      for (int t = tid; t < TB; t += blockDim.x) {
-        float gs = 1.f, b = 0.f;
-        if (t < nt) {
-          if (p.variant == HYPIC_GDN) gs = expf(p.g[(t0 + t) * p.h_v + h]);
-          else if (p.variant == HYPIC_SCALAR_DECAY) gs = gconst;
-          if (delta) b = p.beta[(t0 + t) * p.h_v + h];
+        for (int t = tid; t < TB; t += blockDim.x) {
+          float gs = 1.f, b = 0.f;
+          if (t < nt) {
+            if (p.variant == HYPIC_GDN) gs = expf(reinterpret_cast<const float *>(base + lay.g)[t]);
+            else if (p.variant == HYPIC_SCALAR_DECAY) gs = gconst;
+            if (delta) b = reinterpret_cast<const float *>(base + lay.b)[t];
+          }
+          sm.gs[t] = gs;
+          sm.b[t] = b;
         }
-        sm.gs[t] = gs;
-        sm.b[t] = b;
+        // the next tile's copies run under this tile's recurrence; its stage
+        // was last read by the conversion of the previous tile, which every
+        // thread finished before the barrier above
+        if (t0 + TB < it.end) {
+          const int64_t rest = it.end - (t0 + TB);
+          issue_tile(t0 + TB, (int)(rest < TB ? rest : TB), (ti + 1) & 1);
+        }
+      } else {
+        for (int e = tid; e < TB * DK; e += blockDim.x) {
+          const int t = e / DK, i = e % DK;
+          float kv = 0.f, qv = 0.f, a = 1.f;
+          if (t < nt && i < d_k) {
+            kv = load_in(p.k, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype);
+            qv = load_in(p.q, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype);
+            if (vec) a = expf(p.g[((t0 + t) * p.h_v + h) * (int64_t)d_k + i]);
+          }
+          sm.k[t][i] = kv;
+          fs.q[t][i] = qv;
+          if (vec) {
+            sm.a[t][i] = a;
+            sm.kd[t][i] = kv * a;
+          }
+        }
+        for (int e = tid; e < TB * 128; e += blockDim.x) {
+          const int t = e / 128, j = e % 128;
+          sm.v[t][j] = (t < nt && j < d_v) ? load_in(p.v, ((t0 + t) * p.h_v + h) * (int64_t)d_v + j, p.in_dtype) : 0.f;
+        }
+        for (int t = tid; t < TB; t += blockDim.x) {
+          float gs = 1.f, b = 0.f;
+          if (t < nt) {
+            if (p.variant == HYPIC_GDN) gs = expf(p.g[(t0 + t) * p.h_v + h]);
+            else if (p.variant == HYPIC_SCALAR_DECAY) gs = gconst;
+            if (delta) b = p.beta[(t0 + t) * p.h_v + h];
+          }
+          sm.gs[t] = gs;
+          sm.b[t] = b;
+        }
       }
       __syncthreads();
       flush();  // the last token of the previous tile
@@ -397,11 +515,19 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
 
 }  // namespace
 
-// the output pass of the prefill forward (pairs written elsewhere)
+// the output pass of the prefill forward (pairs written elsewhere); the
+// token inputs are copied a tile ahead by cp.async when every row they are
+// read in starts on a 16-byte boundary, else staged by plain loads
 cudaError_t launch_forward_out(const BuildParams &p, int n_items, int n_sm, cudaStream_t s) {
   const int dvp = ((p.d_v + 31) / 32) * 32;
   const int threads = 2 * dvp;
-  auto go = [&](auto kern, size_t smem) -> cudaError_t {
+  const int es = p.in_dtype == HYPIC_IN_BF16 ? 2 : 4;
+  const bool vec = is_vector_gate(p.variant);
+  auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+  const bool async_ok = (p.d_k * es) % 16 == 0 && (p.d_v * es) % 16 == 0 && al16(p.k) && al16(p.q) && al16(p.v) &&
+                        (!vec || ((p.d_k % 4) == 0 && al16(p.g)));
+  auto go = [&](auto kern, size_t base, int DK) -> cudaError_t {
+    const size_t smem = base + (async_ok ? 2 * (size_t)fwd_raw_layout(DK, es, vec).bytes : 0);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -411,13 +537,13 @@ cudaError_t launch_forward_out(const BuildParams &p, int n_items, int n_sm, cuda
     int grid = n_sm * per_sm;
     if (grid > n_items) grid = n_items;
     if (grid < 1) return cudaSuccess;
-    kern<<<grid, threads, smem, s>>>(p, dvp);
+    kern<<<grid, threads, smem, s>>>(p, dvp, async_ok ? 1 : 0);
     return cudaGetLastError();
   };
-  if (p.d_k <= 16) return go(forward_out_kernel<16>, sizeof(FwdSmem<16>));
-  if (p.d_k <= 32) return go(forward_out_kernel<32>, sizeof(FwdSmem<32>));
-  if (p.d_k <= 64) return go(forward_out_kernel<64>, sizeof(FwdSmem<64>));
-  return go(forward_out_kernel<128>, sizeof(FwdSmem<128>));
+  if (p.d_k <= 16) return go(forward_out_kernel<16>, fwd_raw_offset<16>(), 16);
+  if (p.d_k <= 32) return go(forward_out_kernel<32>, fwd_raw_offset<32>(), 32);
+  if (p.d_k <= 64) return go(forward_out_kernel<64>, fwd_raw_offset<64>(), 64);
+  return go(forward_out_kernel<128>, fwd_raw_offset<128>(), 128);
 }
 
 cudaError_t launch_build_token(const BuildParams &p, int n_items, int n_sm, cudaStream_t s) {
