@@ -71,6 +71,11 @@ class ForwardDesc(ctypes.Structure):
     _fields_ = [("build", BuildDesc), ("q", P), ("o_out", P)]
 
 
+class HostBuildDesc(ctypes.Structure):
+    _fields_ = [("build", BuildDesc), ("host_k", P), ("host_v", P), ("host_g", P), ("host_beta", P),
+                ("host_T", P), ("host_S", P), ("n_chunks", ctypes.c_int32)]
+
+
 class RerotateDesc(ctypes.Structure):
     _fields_ = [("n_items", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("variant", ctypes.c_int32), ("rot_dim", ctypes.c_int32),
@@ -84,6 +89,7 @@ ROPE_LAYOUT = {"interleaved": 0, "half": 1}
 
 SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_workspace_bytes", "hypic_compose",
            "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_pair_rerotate", "hypic_segment_forward",
+           "hypic_segment_build_host",
            "hypic_plan_lpt",
            "hypic_status_from_word", "hypic_status_string", "hypic_version")
 
@@ -120,6 +126,8 @@ def load():
             lib.hypic_pair_merge.restype = ctypes.c_int
             lib.hypic_segment_forward.argtypes = [ctypes.POINTER(ForwardDesc), P]
             lib.hypic_segment_forward.restype = ctypes.c_int
+            lib.hypic_segment_build_host.argtypes = [ctypes.POINTER(HostBuildDesc), P]
+            lib.hypic_segment_build_host.restype = ctypes.c_int
             lib.hypic_pair_rerotate.argtypes = [ctypes.POINTER(RerotateDesc), P]
             lib.hypic_pair_rerotate.restype = ctypes.c_int
             lib.hypic_plan_lpt.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P]
@@ -269,6 +277,49 @@ def segment_forward(k, v, q, g, beta, seg_offsets, *, variant: str, seam_w: int,
     del keep
     if rc != OK:
         raise HypicError(rc, "hypic_segment_forward")
+    return workspace
+
+
+def _host_ptr(t, like, name):
+    """Address of a host tensor shaped and typed like its device twin."""
+    if t is None:
+        if like is not None:
+            raise ValueError(f"{name}: host array missing")
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: contiguous host tensor expected")
+    if like is None or t.dtype != like.dtype or t.shape != like.shape:
+        raise ValueError(f"{name}: must match its device buffer in shape and dtype")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def segment_build_host(k_host, v_host, g_host, beta_host, seg_offsets, *, variant: str, seam_w: int, k, v, g, beta,
+                       T_pool, S_pool, T_host, S_host, n_chunks: int = 8, slot_of_seg=None, workspace=None,
+                       status=None, flags: int = 0, stream=None):
+    """hypic_segment_build_host on torch tensors: the build from host inputs
+    (k_host, v_host, g_host, beta_host, page-locked for overlap) to host
+    pools (T_host, S_host), with k, v, g, beta, T_pool, S_pool the device
+    buffers of the same shapes used as staging.  Segments go in n_chunks
+    groups whose input copies, builds and output copies overlap.  The host
+    pools are complete once `stream` is synchronised."""
+    lib = load()
+    b, keep = _build_desc(k, v, g, beta, seg_offsets, variant, seam_w, T_pool, S_pool, slot_of_seg,
+                          workspace, status, flags)
+    if workspace is None:
+        nb = int(lib.hypic_build_workspace_bytes(ctypes.byref(b)))
+        workspace = alloc_workspace(nb, k.device)
+        b.workspace = _ptr(workspace)
+        b.workspace_bytes = workspace.numel()
+    d = HostBuildDesc()
+    d.build = b
+    d.host_k, d.host_v = _host_ptr(k_host, k, "k_host"), _host_ptr(v_host, v, "v_host")
+    d.host_g, d.host_beta = _host_ptr(g_host, g, "g_host"), _host_ptr(beta_host, beta, "beta_host")
+    d.host_T, d.host_S = _host_ptr(T_host, T_pool, "T_host"), _host_ptr(S_host, S_pool, "S_host")
+    d.n_chunks = int(n_chunks)
+    rc = lib.hypic_segment_build_host(ctypes.byref(d), _stream(stream))
+    del keep
+    if rc != OK:
+        raise HypicError(rc, "hypic_segment_build_host")
     return workspace
 
 

@@ -1,6 +1,7 @@
 // api.cpp -- host side of libhypic: descriptor validation, the LPT work plan,
 // workspace sizing and kernel launches behind the C ABI of hypic.h.
 #include <algorithm>
+#include <mutex>
 #include <cstdlib>
 #include <cstring>
 #include <numeric>
@@ -77,6 +78,10 @@ namespace hypic {
 // scalar decay, ungated, diagonal gate); every other case runs the fp32 token
 // recurrence.
 cudaError_t launch_build(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, cudaStream_t s) {
+  // no tokens at all: every pair is (I, 0) (or the empty gate product), which
+  // the token kernel writes without reading an input; the tensor-core
+  // kernels cannot describe an empty token tensor
+  if (n_tokens == 0) return launch_build_token(p, n_items, n_sm, s);
   if (build_tc_supported(p)) return launch_build_tc(p, n_tokens, n_items, n_sm, wait_limit(), s);
   if (build_channel_supported(p)) return launch_build_channel(p, n_tokens, n_items, n_sm, wait_limit(), s);
   if (build_fast_supported(p)) return launch_build_fast(p, n_tokens, n_items, n_sm, wait_limit(), s);
@@ -147,7 +152,9 @@ size_t hypic_build_workspace_bytes(const hypic_build_desc *d) {
 namespace {
 // the build (q == NULL) or the prefill forward (q, o_out): validation, LPT
 // plan, launch
-int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_stream_t stream) {
+// the argument checks of a build (everything but the workspace); fills the
+// slot of every segment
+int check_build(const hypic_build_desc *d, std::vector<int32_t> &slots) {
   if (!d) return HYPIC_ERR_INVALID_ARG;
   int st = check_common_shapes(d->h_k, d->h_v, d->d_k, d->d_v, d->seam_w, d->variant, d->in_dtype);
   if (st) return st;
@@ -164,20 +171,28 @@ int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_str
   const bool delta = is_delta(d->variant);
   const bool needs_g = d->variant == HYPIC_GDN || d->variant == HYPIC_CHANNEL_DELTA ||
                        d->variant == HYPIC_DIAG_GATE || d->variant == HYPIC_SCALAR_DECAY;
-  if (needs_g && (!d->g || !aligned(d->g, 4))) return HYPIC_ERR_INVALID_ARG;
+  // per-token log-gates are read only when there are tokens; the per-head
+  // decay always
+  const bool reads_g = needs_g && (d->n_tokens > 0 || d->variant == HYPIC_SCALAR_DECAY);
+  if (reads_g && (!d->g || !aligned(d->g, 4))) return HYPIC_ERR_INVALID_ARG;
   if (delta && d->n_tokens > 0 && (!d->beta || !aligned(d->beta, 4))) return HYPIC_ERR_INVALID_ARG;
   if (!d->T_pool || !d->S_pool || !aligned(d->T_pool, 4) || !aligned(d->S_pool, 4)) return HYPIC_ERR_INVALID_ARG;
   // slots: in range and distinct (two items writing one slot would race)
-  std::vector<int32_t> slots(d->n_seg);
+  slots.assign(d->n_seg, 0);
   for (int i = 0; i < d->n_seg; i++) slots[i] = d->slot_of_seg ? d->slot_of_seg[i] : i;
-  {
-    std::vector<int32_t> s2(slots);
-    std::sort(s2.begin(), s2.end());
-    for (int i = 0; i < d->n_seg; i++) {
-      if (s2[i] < 0 || s2[i] >= d->n_slots) return HYPIC_ERR_INVALID_ARG;
-      if (i && s2[i] == s2[i - 1]) return HYPIC_ERR_INVALID_ARG;
-    }
+  std::vector<int32_t> s2(slots);
+  std::sort(s2.begin(), s2.end());
+  for (int i = 0; i < d->n_seg; i++) {
+    if (s2[i] < 0 || s2[i] >= d->n_slots) return HYPIC_ERR_INVALID_ARG;
+    if (i && s2[i] == s2[i - 1]) return HYPIC_ERR_INVALID_ARG;
   }
+  return HYPIC_OK;
+}
+
+int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_stream_t stream) {
+  std::vector<int32_t> slots;
+  int st = check_build(d, slots);
+  if (st || d->n_seg == 0) return st;
   BuildParams p{};
   p.h_k = d->h_k;
   p.h_v = d->h_v;
@@ -254,11 +269,145 @@ int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_str
 }
 }  // namespace
 
+
+// ---- the host-buffer build: copy streams and events per device, created on
+// first use and kept for the life of the process.  An event may be recorded
+// again while earlier waits on it are pending: a wait takes the record that
+// precedes it.
+namespace {
+constexpr int kMaxHostChunks = 64;
+constexpr int kMaxDevices = 64;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, fin = nullptr;
+  cudaEvent_t in_done[kMaxHostChunks] = {}, built[kMaxHostChunks] = {};
+};
+std::mutex g_host_mu;
+HostPipe g_pipes[kMaxDevices];
+
+int host_pipe(HostPipe *&hp) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HYPIC_ERR_CUDA;
+  hp = &g_pipes[dev];
+  if (hp->ready) return HYPIC_OK;
+  auto ev = [](cudaEvent_t *e) { return *e || cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+  if (!hp->in && cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking) != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (!hp->out && cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking) != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (!ev(&hp->start) || !ev(&hp->fin)) return HYPIC_ERR_CUDA;
+  for (int i = 0; i < kMaxHostChunks; i++)
+    if (!ev(&hp->in_done[i]) || !ev(&hp->built[i])) return HYPIC_ERR_CUDA;
+  hp->ready = true;
+  return HYPIC_OK;
+}
+
+int64_t T_slot_floats(const hypic_build_desc &b) {
+  if (is_dense_T(b.variant)) return (int64_t)b.h_v * b.d_k * b.d_k;
+  if (b.variant == HYPIC_DIAG_GATE) return (int64_t)b.h_v * b.d_k;
+  return b.h_v;
+}
+}  // namespace
+
 extern "C" {
 
 int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream) {
   return build_impl(d, nullptr, nullptr, stream);
 }
+
+int hypic_segment_build_host(const hypic_host_build_desc *d, hypic_stream_t stream) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  const hypic_build_desc &b = d->build;
+  std::vector<int32_t> slots;
+  int st = check_build(&b, slots);
+  if (st) return st;
+  if (d->n_chunks < 1 || !d->host_T || !d->host_S) return HYPIC_ERR_INVALID_ARG;
+  if (b.n_tokens > 0 && (!d->host_k || !d->host_v)) return HYPIC_ERR_INVALID_ARG;
+  if ((b.g == nullptr) != (d->host_g == nullptr) || (b.beta == nullptr) != (d->host_beta == nullptr))
+    return HYPIC_ERR_INVALID_ARG;
+  if (b.n_seg == 0) return HYPIC_OK;
+  if (!b.workspace || b.workspace_bytes < hypic_build_workspace_bytes(&b) || !aligned(b.workspace, kAlign))
+    return HYPIC_ERR_WORKSPACE;
+
+  const int n_seg = b.n_seg;
+  const int n_ch = std::min(std::min(d->n_chunks, n_seg), kMaxHostChunks);
+  // group boundaries: about equal token counts, at least one segment each
+  std::vector<int> bnd(n_ch + 1);
+  bnd[0] = 0;
+  bnd[n_ch] = n_seg;
+  for (int c = 1; c < n_ch; c++) {
+    const int64_t target = (int64_t)((double)b.n_tokens * c / n_ch);
+    int j = (int)(std::lower_bound(b.seg_offsets, b.seg_offsets + n_seg + 1, target) - b.seg_offsets);
+    j = std::max(j, bnd[c - 1] + 1);
+    j = std::min(j, n_seg - (n_ch - c));
+    bnd[c] = j;
+  }
+  const size_t es = (size_t)in_size(b.in_dtype);
+  const bool vec = is_vector_gate(b.variant);
+  const bool tok_g = b.variant == HYPIC_GDN || vec;  // g per token (else per head, or none)
+  const size_t k_tok = (size_t)b.h_k * b.d_k * es, v_tok = (size_t)b.h_v * b.d_v * es;
+  const size_t g_tok = (size_t)b.h_v * (vec ? b.d_k : 1) * 4, beta_tok = (size_t)b.h_v * 4;
+  const size_t T_slot = (size_t)T_slot_floats(b) * 4, S_slot = (size_t)b.h_v * b.d_k * b.d_v * 4;
+
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  HostPipe *hp = nullptr;
+  if ((st = host_pipe(hp))) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  auto h2d = [&](const void *dst, const void *src, size_t n) {
+    return n == 0 || ok(cudaMemcpyAsync(const_cast<void *>(dst), src, n, cudaMemcpyHostToDevice, hp->in));
+  };
+  if (!ok(cudaEventRecord(hp->start, s)) || !ok(cudaStreamWaitEvent(hp->in, hp->start, 0)) ||
+      !ok(cudaStreamWaitEvent(hp->out, hp->start, 0)))
+    return HYPIC_ERR_CUDA;
+  const bool has_beta = is_delta(b.variant) && b.beta;
+  if (b.variant == HYPIC_SCALAR_DECAY && !h2d(b.g, d->host_g, (size_t)b.h_v * 4)) return HYPIC_ERR_CUDA;  // per head
+  std::vector<int64_t> off;
+  for (int c = 0; c < n_ch; c++) {
+    const int a = bnd[c], e = bnd[c + 1];
+    const int64_t t0 = b.seg_offsets[a], nt = b.seg_offsets[e] - t0;
+    auto at = [](const void *base, size_t bytes) { return static_cast<const char *>(base) + bytes; };
+    if (nt > 0) {
+      if (!h2d(at(b.k, t0 * k_tok), at(d->host_k, t0 * k_tok), nt * k_tok) ||
+          !h2d(at(b.v, t0 * v_tok), at(d->host_v, t0 * v_tok), nt * v_tok))
+        return HYPIC_ERR_CUDA;
+      if (tok_g && !h2d(at(b.g, t0 * g_tok), at(d->host_g, t0 * g_tok), nt * g_tok)) return HYPIC_ERR_CUDA;
+      if (has_beta && !h2d(at(b.beta, t0 * beta_tok), at(d->host_beta, t0 * beta_tok), nt * beta_tok))
+        return HYPIC_ERR_CUDA;
+    }
+    if (!ok(cudaEventRecord(hp->in_done[c], hp->in)) || !ok(cudaStreamWaitEvent(s, hp->in_done[c], 0)))
+      return HYPIC_ERR_CUDA;
+    // the group's build: the same descriptor over its segments, rebased
+    off.assign(e - a + 1, 0);
+    for (int i = a; i <= e; i++) off[i - a] = b.seg_offsets[i] - t0;
+    hypic_build_desc cb = b;
+    cb.n_tokens = (int32_t)nt;
+    cb.n_seg = e - a;
+    cb.seg_offsets = off.data();
+    cb.slot_of_seg = slots.data() + a;
+    cb.k = at(b.k, t0 * k_tok);
+    cb.v = at(b.v, t0 * v_tok);
+    if (tok_g) cb.g = reinterpret_cast<const float *>(at(b.g, t0 * g_tok));
+    if (has_beta) cb.beta = reinterpret_cast<const float *>(at(b.beta, t0 * beta_tok));
+    if ((st = build_impl(&cb, nullptr, nullptr, stream))) return st;
+    if (!ok(cudaEventRecord(hp->built[c], s)) || !ok(cudaStreamWaitEvent(hp->out, hp->built[c], 0)))
+      return HYPIC_ERR_CUDA;
+    // its slots out, runs of consecutive slots as one copy
+    for (int i = a; i < e;) {
+      int j = i + 1;
+      while (j < e && slots[j] == slots[j - 1] + 1) j++;
+      const size_t s0 = (size_t)slots[i], n = (size_t)(j - i);
+      if (!ok(cudaMemcpyAsync(reinterpret_cast<char *>(d->host_T) + s0 * T_slot, at(b.T_pool, s0 * T_slot),
+                              n * T_slot, cudaMemcpyDeviceToHost, hp->out)) ||
+          !ok(cudaMemcpyAsync(reinterpret_cast<char *>(d->host_S) + s0 * S_slot, at(b.S_pool, s0 * S_slot),
+                              n * S_slot, cudaMemcpyDeviceToHost, hp->out)))
+        return HYPIC_ERR_CUDA;
+      i = j;
+    }
+  }
+  if (!ok(cudaEventRecord(hp->fin, hp->out)) || !ok(cudaStreamWaitEvent(s, hp->fin, 0))) return HYPIC_ERR_CUDA;
+  return HYPIC_OK;
+}
+
 
 int hypic_segment_forward(const hypic_forward_desc *d, hypic_stream_t stream) {
   if (!d) return HYPIC_ERR_INVALID_ARG;

@@ -157,6 +157,50 @@ typedef struct {
 int hypic_segment_forward(const hypic_forward_desc *d, hypic_stream_t stream);
 
 /*
+ * hypic_segment_build_host -- hypic_segment_build from inputs in host memory
+ * to pairs in host memory, with the copies overlapped with the build.  The
+ * pages have no counterpart: this is the deployment form of the same build
+ * (pages §2.1: the pair is cached at a segment's first prefill), with the
+ * same pool contents bit for bit.
+ *
+ * d->build is a full hypic_segment_build descriptor whose [dev] buffers
+ * (k, v, g, beta, T_pool, S_pool, workspace) the call fills and reads as
+ * staging: k, v, g, beta are overwritten with the host inputs, the pool
+ * slots of the segments are written by the build.  The host_* arrays have the
+ * same shapes as their device counterparts; host_T / host_S mirror the whole
+ * pools, and only the slots of the segments are written.  host_g / host_beta
+ * are NULL exactly when build.g / build.beta are.
+ *
+ * The segments are split into min(n_chunks, n_seg, 64) groups of
+ * consecutive segments with about equal token counts.  Per group, the token
+ * range of k, v, g, beta is copied in on a copy stream of the library, the
+ * build of the group runs on `stream` once those copies are done, and the
+ * group's pool slots are copied out on a second copy stream once its build
+ * is done; so group c's build overlaps group c+1's inputs and group c-1's
+ * outputs.  All of it is ordered after the work already on `stream`, and
+ * `stream` waits for the last copy out: the host arrays are complete once
+ * `stream` is synchronised.  Overlap needs page-locked host arrays; pageable
+ * ones give the same results with the copies serialised.
+ *
+ * Returns a hypic_status.  Every argument is checked before anything is
+ * enqueued; a CUDA error while enqueuing returns HYPIC_ERR_CUDA with the
+ * outputs undefined.  Host calls are serialised by a lock (the copy streams
+ * and their events are shared per device).
+ */
+typedef struct {
+  hypic_build_desc build;
+  const void *host_k;     /* [host] as build.k */
+  const void *host_v;     /* [host] as build.v */
+  const float *host_g;    /* [host] as build.g */
+  const float *host_beta; /* [host] as build.beta */
+  float *host_T;          /* [host] as build.T_pool */
+  float *host_S;          /* [host] as build.S_pool */
+  int32_t n_chunks;       /* >= 1 */
+} hypic_host_build_desc;
+
+int hypic_segment_build_host(const hypic_host_build_desc *d, hypic_stream_t stream);
+
+/*
  * hypic_segment_build_noalloc -- hypic_segment_build for callers that cannot
  * allocate device memory.  The pages have no counterpart: this is a
  * deployment variant of the same build, with the same results bit for bit.

@@ -163,6 +163,32 @@ def test_forward_rejects_bad_descriptors():
         assert lib.hypic_segment_forward(ctypes.byref(d), None) == want, over
 
 
+def test_build_host_rejects_bad_descriptors():
+    """hypic_segment_build_host checks everything before the first CUDA call:
+    the build's own checks, the chunk count, the host arrays (present exactly
+    where their device twins are), then the workspace."""
+    lib = hy.load()
+    off = np.asarray([0, 3, 8], dtype=np.int64)
+    po = off.ctypes.data_as(ctypes.c_void_p)
+    host = ctypes.c_void_p(1 << 21)
+    for over, want in [(dict(n_chunks=0), 1), (dict(host_T=None), 1), (dict(host_S=None), 1),
+                       (dict(host_k=None), 1), (dict(host_v=None), 1), (dict(host_g=None), 1),
+                       (dict(host_beta=None), 1), (dict(build=dict(beta=None)), 1),
+                       (dict(build=dict(d_k=129)), 2), (dict(build=dict(workspace=None)), 3),
+                       (dict(build=dict(workspace_bytes=16)), 3)]:
+        d = hy.HostBuildDesc()
+        d.build = _fake_build_desc(seg_offsets=po, **over.get("build", {}))
+        for name in ("host_k", "host_v", "host_g", "host_beta", "host_T", "host_S"):
+            setattr(d, name, over.get(name, host))
+        d.n_chunks = over.get("n_chunks", 4)
+        assert lib.hypic_segment_build_host(ctypes.byref(d), None) == want, over
+    d = hy.HostBuildDesc()  # a gate-free variant given a host gate array
+    d.build = _fake_build_desc(seg_offsets=po, variant=hy.UNGATED, g=None, beta=None)
+    d.host_k = d.host_v = d.host_T = d.host_S = d.host_g = host
+    d.n_chunks = 2
+    assert lib.hypic_segment_build_host(ctypes.byref(d), None) == 1
+
+
 def test_compose_rejects_bad_descriptors():
     lib = hy.load()
     fake = ctypes.c_void_p(1 << 20)
