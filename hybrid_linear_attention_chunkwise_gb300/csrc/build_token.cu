@@ -29,7 +29,6 @@ namespace hypic {
 
 namespace {
 
-__device__ __forceinline__ void tc_named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 constexpr int TB = 16;  // tokens per shared-memory tile
 
@@ -235,27 +234,41 @@ cudaError_t launch_dk(const BuildParams &p, int n_items, int n_sm, cudaStream_t 
 // The outputs of the prefill forward (hypic_segment_forward): for every body
 // token of every item, o_t = S_t^T q_t from the zero-initial body state, by
 // the same token recurrence over the S columns only (the pairs come from the
-// build kernels).  Each column is split over two threads, rows 0..DK/2-1 and
-// DK/2..DK-1 (threads col and col + DVP, in warps w and w + DVP/32), so a
-// column holds DK/2 registers per thread and twice as many warps fit an SM;
-// the halves exchange their partial dot products through shared memory
-// under a 64-thread barrier of their own (one per token), the lower half
-// writing the output of a token after the next barrier.
+// build kernels).
+//
+// A warp holds 16 state columns.  Lane 8*qr + pr keeps columns 2*pr and
+// 2*pr + 1 of them over key rows [qr*DK/4, (qr+1)*DK/4), so the four
+// quarters of a column pair sit in one warp: their partial dot products
+// (k^T S for the erase, q^T S for the output) are summed by two xor
+// shuffles, a butterfly that gives all four lanes the same bits, with no
+// shared-memory exchange and no barrier per token.  Each 16-byte load of a
+// k or q row feeds both columns.  In shared memory the rows are padded by
+// 16 bytes per quarter, so the four quarters' broadcast loads fall in
+// different banks.
 // ---------------------------------------------------------------------------
 template <int DK>
 struct FwdSmem {
-  TokSmem<DK> t;
-  alignas(16) float q[TB][DK];  // rows read 16 bytes a time
-  float xs[2][2][128];  // partial k^T S of the two halves, by token parity
-  float os[2][128];     // partial q^T S of the upper half, by token parity
+  static constexpr int QR = DK / 4;    // key rows per quarter
+  static constexpr int RP = DK + 16;   // padded row: quarter q starts at q * (QR + 4)
+  alignas(16) float k[TB][RP];
+  alignas(16) float kd[TB][RP];  // vector gates: k * a (the erase acts after Diag(a)); else unused
+  alignas(16) float a[TB][RP];   // vector gates: a = exp(g); else unused
+  alignas(16) float q[TB][RP];
+  float v[TB][128];
+  float gs[TB];  // scalar gate a_t (GDN) / gamma (scalar decay) / 1
+  float b[TB];   // beta_t (0 on padding tokens)
+  int item;
 };
-// every row read by 16-byte loads starts on a 16-byte boundary (and so does
-// each half row: DK / 2 floats is a multiple of 4)
+template <int DK>
+__host__ __device__ constexpr int fwd_pad(int i) {
+  return i + 4 * (i / (DK / 4));
+}
+// every row, and every quarter of one, starts on a 16-byte boundary
 template <int DK>
 constexpr bool fwd_rows_aligned() {
-  return offsetof(FwdSmem<DK>, q) % 16 == 0 && offsetof(TokSmem<DK>, k) % 16 == 0 &&
-         offsetof(TokSmem<DK>, kd) % 16 == 0 && offsetof(TokSmem<DK>, a) % 16 == 0 && (DK * 4) % 16 == 0 &&
-         (DK / 2) % 4 == 0;
+  return offsetof(FwdSmem<DK>, k) % 16 == 0 && offsetof(FwdSmem<DK>, kd) % 16 == 0 &&
+         offsetof(FwdSmem<DK>, a) % 16 == 0 && offsetof(FwdSmem<DK>, q) % 16 == 0 &&
+         (FwdSmem<DK>::RP * 4) % 16 == 0 && (DK / 4) % 4 == 0;
 }
 static_assert(fwd_rows_aligned<16>() && fwd_rows_aligned<32>() && fwd_rows_aligned<64>() && fwd_rows_aligned<128>(),
               "16-byte shared-memory rows");
@@ -282,19 +295,24 @@ __host__ __device__ constexpr size_t fwd_raw_offset() {
   return (sizeof(FwdSmem<DK>) + 15) / 16 * 16;
 }
 
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 8);
+  return x + __shfl_xor_sync(0xffffffffu, x, 16);
+}
+
 template <int DK>
-__global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp, int async_tiles) {
+__global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int async_tiles) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  FwdSmem<DK> &fs = *reinterpret_cast<FwdSmem<DK> *>(smem_raw);
-  TokSmem<DK> &sm = fs.t;
-  constexpr int HALF = DK / 2;
-  const int tid = threadIdx.x;
+  FwdSmem<DK> &sm = *reinterpret_cast<FwdSmem<DK> *>(smem_raw);
+  constexpr int QR = DK / 4;
+  const int tid = threadIdx.x, lane = tid & 31;
   const bool delta = is_delta(p.variant);
   const bool vec = is_vector_gate(p.variant);
   const int d_k = p.d_k, d_v = p.d_v;
-  const int hf = tid / dvp, col = tid % dvp, r0 = hf * HALF;
-  const bool active = col < d_v;
-  const int bar = 1 + col / 32;  // the pair of warps holding this column
+  const int qr = lane >> 3;
+  const int c0 = (tid >> 5) * 16 + 2 * (lane & 7);  // the thread's first column
+  const int ro = fwd_pad<DK>(qr * QR);              // its quarter in a padded row
+  const int v0c = c0 < 128 ? c0 : 0, v1c = c0 + 1 < 128 ? c0 + 1 : 0;
   const int n_items = p.plan->n_items;
   const int es = p.in_dtype == HYPIC_IN_BF16 ? 2 : 4;
   const FwdRaw lay = fwd_raw_layout(DK, es, vec);
@@ -309,45 +327,11 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
     const BuildItem it = p.items[idx];
     const int h = it.head;
     const int kh = (int)(((int64_t)h * p.h_k) / p.h_v);
-    float X[HALF];
+    float X0[QR], X1[QR];
 #pragma unroll
-    for (int i = 0; i < HALF; i++) X[i] = 0.f;
+    for (int i = 0; i < QR; i++) X0[i] = X1[i] = 0.f;
     float gconst = 1.f;
     if (p.variant == HYPIC_SCALAR_DECAY) gconst = expf(p.g[h]);
-    uint32_t u = 0;       // tokens so far: parity of the exchange buffers
-    int64_t pend = -1;    // lower half: token whose output waits for the upper half's partial
-    float opend = 0.f;
-    // X <- Diag(a) X + k c (per-channel gate) or gs X + k c, 16 bytes a time
-    auto update = [&](int t, float c) {
-      const float *kk = sm.k[t] + r0;
-      if (vec) {
-        const float *aa = sm.a[t] + r0;
-#pragma unroll
-        for (int i = 0; i < HALF; i += 4) {
-          const float4 kv = *reinterpret_cast<const float4 *>(kk + i);
-          const float4 av = *reinterpret_cast<const float4 *>(aa + i);
-          X[i + 0] = fmaf(av.x, X[i + 0], kv.x * c);
-          X[i + 1] = fmaf(av.y, X[i + 1], kv.y * c);
-          X[i + 2] = fmaf(av.z, X[i + 2], kv.z * c);
-          X[i + 3] = fmaf(av.w, X[i + 3], kv.w * c);
-        }
-      } else {
-        const float gs = sm.gs[t];
-#pragma unroll
-        for (int i = 0; i < HALF; i += 4) {
-          const float4 kv = *reinterpret_cast<const float4 *>(kk + i);
-          X[i + 0] = fmaf(gs, X[i + 0], kv.x * c);
-          X[i + 1] = fmaf(gs, X[i + 1], kv.y * c);
-          X[i + 2] = fmaf(gs, X[i + 2], kv.z * c);
-          X[i + 3] = fmaf(gs, X[i + 3], kv.w * c);
-        }
-      }
-    };
-    auto flush = [&]() {
-      if (hf == 0 && pend >= 0 && active)
-        p.o_out[(pend * p.h_v + h) * (int64_t)d_v + col] = opend + fs.os[(u - 1) & 1][col];
-      pend = -1;
-    };
 
     // raw inputs of the tile at t0 (nt tokens) into stage st, by cp.async
     auto issue_tile = [&](int64_t t0, int nt, int st) {
@@ -382,6 +366,16 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
       return es == 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(b)[i])
                      : reinterpret_cast<const float *>(b)[i];
     };
+    // the fp32 tile from either source: k, q, a, k*a into padded rows
+    auto put_row = [&](int t, int i, float kv, float qv, float a) {
+      const int j = fwd_pad<DK>(i);
+      sm.k[t][j] = kv;
+      sm.q[t][j] = qv;
+      if (vec) {
+        sm.a[t][j] = a;
+        sm.kd[t][j] = kv * a;
+      }
+    };
     const int64_t first_nt = (it.end - it.start) < TB ? (it.end - it.start) : TB;
     if (async_tiles && first_nt > 0) issue_tile(it.start, (int)first_nt, 0);
 
@@ -400,12 +394,7 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
             qv = raw_in(base + lay.q, t * DK + i);
             if (vec) a = expf(reinterpret_cast<const float *>(base + lay.g)[t * DK + i]);
           }
-          sm.k[t][i] = kv;
-          fs.q[t][i] = qv;
-          if (vec) {
-            sm.a[t][i] = a;
-            sm.kd[t][i] = kv * a;
-          }
+          put_row(t, i, kv, qv, a);
         }
         for (int e = tid; e < TB * 128; e += blockDim.x) {
           const int t = e / 128, j = e % 128;
@@ -437,12 +426,7 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
             qv = load_in(p.q, ((t0 + t) * p.h_k + kh) * (int64_t)d_k + i, p.in_dtype);
             if (vec) a = expf(p.g[((t0 + t) * p.h_v + h) * (int64_t)d_k + i]);
           }
-          sm.k[t][i] = kv;
-          fs.q[t][i] = qv;
-          if (vec) {
-            sm.a[t][i] = a;
-            sm.kd[t][i] = kv * a;
-          }
+          put_row(t, i, kv, qv, a);
         }
         for (int e = tid; e < TB * 128; e += blockDim.x) {
           const int t = e / 128, j = e % 128;
@@ -460,56 +444,83 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
         }
       }
       __syncthreads();
-      flush();  // the last token of the previous tile
       for (int t = 0; t < nt; t++) {
         const float b = sm.b[t], gs = sm.gs[t];
-        const float vj = sm.v[t][col < 128 ? col : 0];
+        const float v0 = sm.v[t][v0c], v1 = sm.v[t][v1c];
+        float c0v = v0, c1v = v1;  // X <- G X + k c^T (the column coefficients)
         if (delta) {
-          const float *kd = (vec ? sm.kd[t] : sm.k[t]) + r0;
-          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+          const float *kd = (vec ? sm.kd[t] : sm.k[t]) + ro;
+          float xa = 0.f, xb = 0.f, ya = 0.f, yb = 0.f;
 #pragma unroll
-          for (int i = 0; i < HALF; i += 4) {
-            const float4 w = *reinterpret_cast<const float4 *>(kd + i);  // 16-byte aligned rows
-            x0 = fmaf(w.x, X[i + 0], x0);
-            x1 = fmaf(w.y, X[i + 1], x1);
-            x2 = fmaf(w.z, X[i + 2], x2);
-            x3 = fmaf(w.w, X[i + 3], x3);
+          for (int i = 0; i < QR; i += 4) {
+            const float4 w = *reinterpret_cast<const float4 *>(kd + i);
+            xa = fmaf(w.x, X0[i + 0], xa);
+            xb = fmaf(w.y, X0[i + 1], xb);
+            ya = fmaf(w.x, X1[i + 0], ya);
+            yb = fmaf(w.y, X1[i + 1], yb);
+            xa = fmaf(w.z, X0[i + 2], xa);
+            xb = fmaf(w.w, X0[i + 3], xb);
+            ya = fmaf(w.z, X1[i + 2], ya);
+            yb = fmaf(w.w, X1[i + 3], yb);
           }
-          fs.xs[u & 1][hf][col] = (x0 + x1) + (x2 + x3);
-          tc_named_bar(bar, 64);
-          flush();
-          // both halves sum in the same order: identical x
-          const float x = fs.xs[u & 1][0][col] + fs.xs[u & 1][1][col];
-          const float c = vec ? (b * vj - b * x) : (gs * (-b * x) + b * vj);
-          update(t, c);
-        } else {
-          update(t, vj);
+          const float x0 = quad_sum(xa + xb), x1 = quad_sum(ya + yb);
+          c0v = vec ? (b * v0 - b * x0) : (gs * (-b * x0) + b * v0);
+          c1v = vec ? (b * v1 - b * x1) : (gs * (-b * x1) + b * v1);
         }
-        // the half output q^T S
-        const float *qq = fs.q[t] + r0;
-        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+        const float *kk = sm.k[t] + ro;
+        if (vec) {
+          const float *aa = sm.a[t] + ro;
 #pragma unroll
-        for (int i = 0; i < HALF; i += 4) {
-          const float4 w = *reinterpret_cast<const float4 *>(qq + i);
-          o0 = fmaf(w.x, X[i + 0], o0);
-          o1 = fmaf(w.y, X[i + 1], o1);
-          o2 = fmaf(w.z, X[i + 2], o2);
-          o3 = fmaf(w.w, X[i + 3], o3);
+          for (int i = 0; i < QR; i += 4) {
+            const float4 kv = *reinterpret_cast<const float4 *>(kk + i);
+            const float4 av = *reinterpret_cast<const float4 *>(aa + i);
+            X0[i + 0] = fmaf(av.x, X0[i + 0], kv.x * c0v);
+            X0[i + 1] = fmaf(av.y, X0[i + 1], kv.y * c0v);
+            X0[i + 2] = fmaf(av.z, X0[i + 2], kv.z * c0v);
+            X0[i + 3] = fmaf(av.w, X0[i + 3], kv.w * c0v);
+            X1[i + 0] = fmaf(av.x, X1[i + 0], kv.x * c1v);
+            X1[i + 1] = fmaf(av.y, X1[i + 1], kv.y * c1v);
+            X1[i + 2] = fmaf(av.z, X1[i + 2], kv.z * c1v);
+            X1[i + 3] = fmaf(av.w, X1[i + 3], kv.w * c1v);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < QR; i += 4) {
+            const float4 kv = *reinterpret_cast<const float4 *>(kk + i);
+            X0[i + 0] = fmaf(gs, X0[i + 0], kv.x * c0v);
+            X0[i + 1] = fmaf(gs, X0[i + 1], kv.y * c0v);
+            X0[i + 2] = fmaf(gs, X0[i + 2], kv.z * c0v);
+            X0[i + 3] = fmaf(gs, X0[i + 3], kv.w * c0v);
+            X1[i + 0] = fmaf(gs, X1[i + 0], kv.x * c1v);
+            X1[i + 1] = fmaf(gs, X1[i + 1], kv.y * c1v);
+            X1[i + 2] = fmaf(gs, X1[i + 2], kv.z * c1v);
+            X1[i + 3] = fmaf(gs, X1[i + 3], kv.w * c1v);
+          }
         }
-        const float o = (o0 + o1) + (o2 + o3);
-        if (hf) fs.os[u & 1][col] = o;
-        opend = o;
-        pend = t0 + t;
-        u++;
-        if (!delta) {
-          // no erase barrier in these variants: the output exchange needs one
-          tc_named_bar(bar, 64);
-          flush();
+        // the output q^T S of both columns
+        const float *qq = sm.q[t] + ro;
+        float oa = 0.f, ob = 0.f, pa = 0.f, pb = 0.f;
+#pragma unroll
+        for (int i = 0; i < QR; i += 4) {
+          const float4 w = *reinterpret_cast<const float4 *>(qq + i);
+          oa = fmaf(w.x, X0[i + 0], oa);
+          ob = fmaf(w.y, X0[i + 1], ob);
+          pa = fmaf(w.x, X1[i + 0], pa);
+          pb = fmaf(w.y, X1[i + 1], pb);
+          oa = fmaf(w.z, X0[i + 2], oa);
+          ob = fmaf(w.w, X0[i + 3], ob);
+          pa = fmaf(w.z, X1[i + 2], pa);
+          pb = fmaf(w.w, X1[i + 3], pb);
+        }
+        const float o0 = quad_sum(oa + ob), o1 = quad_sum(pa + pb);
+        if (qr == 0) {
+          float *dst = p.o_out + ((t0 + t) * p.h_v + h) * (int64_t)d_v;
+          if (c0 < d_v) dst[c0] = o0;
+          if (c0 + 1 < d_v) dst[c0 + 1] = o1;
         }
       }
       __syncthreads();  // the tile buffers are free
     }
-    flush();
   }
 }
 
@@ -519,8 +530,7 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int dvp
 // token inputs are copied a tile ahead by cp.async when every row they are
 // read in starts on a 16-byte boundary, else staged by plain loads
 cudaError_t launch_forward_out(const BuildParams &p, int n_items, int n_sm, cudaStream_t s) {
-  const int dvp = ((p.d_v + 31) / 32) * 32;
-  const int threads = 2 * dvp;
+  const int threads = 32 * ((p.d_v + 15) / 16);  // a warp per 16 state columns
   const int es = p.in_dtype == HYPIC_IN_BF16 ? 2 : 4;
   const bool vec = is_vector_gate(p.variant);
   auto al16 = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
@@ -537,7 +547,7 @@ cudaError_t launch_forward_out(const BuildParams &p, int n_items, int n_sm, cuda
     int grid = n_sm * per_sm;
     if (grid > n_items) grid = n_items;
     if (grid < 1) return cudaSuccess;
-    kern<<<grid, threads, smem, s>>>(p, dvp, async_ok ? 1 : 0);
+    kern<<<grid, threads, smem, s>>>(p, async_ok ? 1 : 0);
     return cudaGetLastError();
   };
   if (p.d_k <= 16) return go(forward_out_kernel<16>, fwd_raw_offset<16>(), 16);
