@@ -327,9 +327,13 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int asy
     const BuildItem it = p.items[idx];
     const int h = it.head;
     const int kh = (int)(((int64_t)h * p.h_k) / p.h_v);
+    // scalar gates: the state is A * X (A uniform over the block), so that
+    // the gated update X <- g X + k c^T costs one FMA per element; vector
+    // gates: the state is X
     float X0[QR], X1[QR];
 #pragma unroll
     for (int i = 0; i < QR; i++) X0[i] = X1[i] = 0.f;
+    float A = 1.f;
     float gconst = 1.f;
     if (p.variant == HYPIC_SCALAR_DECAY) gconst = expf(p.g[h]);
 
@@ -463,7 +467,11 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int asy
             ya = fmaf(w.z, X1[i + 2], ya);
             yb = fmaf(w.w, X1[i + 3], yb);
           }
-          const float x0 = quad_sum(xa + xb), x1 = quad_sum(ya + yb);
+          float x0 = quad_sum(xa + xb), x1 = quad_sum(ya + yb);
+          if (!vec) {
+            x0 *= A;
+            x1 *= A;
+          }
           c0v = vec ? (b * v0 - b * x0) : (gs * (-b * x0) + b * v0);
           c1v = vec ? (b * v1 - b * x1) : (gs * (-b * x1) + b * v1);
         }
@@ -484,18 +492,32 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int asy
             X1[i + 3] = fmaf(av.w, X1[i + 3], kv.w * c1v);
           }
         } else {
+          // A g X + k c^T = A' (X + k (c / A')^T) with A' = A g; before A'
+          // gets small enough for c / A' to overflow, it is folded into X
+          float An = A * gs;
+          if (An < 0x1p-64f) {
+#pragma unroll
+            for (int i = 0; i < QR; i++) {
+              X0[i] *= An;
+              X1[i] *= An;
+            }
+            An = 1.f;
+          }
+          const float inv = 1.f / An;
+          const float d0 = c0v * inv, d1 = c1v * inv;
 #pragma unroll
           for (int i = 0; i < QR; i += 4) {
             const float4 kv = *reinterpret_cast<const float4 *>(kk + i);
-            X0[i + 0] = fmaf(gs, X0[i + 0], kv.x * c0v);
-            X0[i + 1] = fmaf(gs, X0[i + 1], kv.y * c0v);
-            X0[i + 2] = fmaf(gs, X0[i + 2], kv.z * c0v);
-            X0[i + 3] = fmaf(gs, X0[i + 3], kv.w * c0v);
-            X1[i + 0] = fmaf(gs, X1[i + 0], kv.x * c1v);
-            X1[i + 1] = fmaf(gs, X1[i + 1], kv.y * c1v);
-            X1[i + 2] = fmaf(gs, X1[i + 2], kv.z * c1v);
-            X1[i + 3] = fmaf(gs, X1[i + 3], kv.w * c1v);
+            X0[i + 0] = fmaf(kv.x, d0, X0[i + 0]);
+            X0[i + 1] = fmaf(kv.y, d0, X0[i + 1]);
+            X0[i + 2] = fmaf(kv.z, d0, X0[i + 2]);
+            X0[i + 3] = fmaf(kv.w, d0, X0[i + 3]);
+            X1[i + 0] = fmaf(kv.x, d1, X1[i + 0]);
+            X1[i + 1] = fmaf(kv.y, d1, X1[i + 1]);
+            X1[i + 2] = fmaf(kv.z, d1, X1[i + 2]);
+            X1[i + 3] = fmaf(kv.w, d1, X1[i + 3]);
           }
+          A = An;
         }
         // the output q^T S of both columns
         const float *qq = sm.q[t] + ro;
@@ -512,7 +534,8 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int asy
           pa = fmaf(w.z, X1[i + 2], pa);
           pb = fmaf(w.w, X1[i + 3], pb);
         }
-        const float o0 = quad_sum(oa + ob), o1 = quad_sum(pa + pb);
+        const float sc = vec ? 1.f : A;
+        const float o0 = sc * quad_sum(oa + ob), o1 = sc * quad_sum(pa + pb);
         if (qr == 0) {
           float *dst = p.o_out + ((t0 + t) * p.h_v + h) * (int64_t)d_v;
           if (c0 < d_v) dst[c0] = o0;
