@@ -379,12 +379,19 @@ def measure_rows(dev, hy, peaks):
     import synth_inputs as si
     rows = {}
 
-    def one(name, W, bound_bytes_extra=0):
+    def one(name, W, round_robin=False):
         L = W.layers[0]
         T = torch.empty(hy.pool_T_shape(W.variant, W.n_seg, W.h_v, W.d_k), device=dev)
         S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
         ms = _time_ms(lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=W.variant,
                                                seam_w=W.seam_w, T_pool=T, S_pool=S))
+        if round_robin:
+            # the same kernel and items, handed to the SMs round-robin in
+            # segment order instead of longest-first (pages §2.3: LPT against
+            # round-robin balancing of uneven segments)
+            ms_rr = _time_ms(lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=W.variant,
+                                                      seam_w=W.seam_w, T_pool=T, S_pool=S,
+                                                      flags=hy.FLAG_ROUND_ROBIN))
         bodies = np.maximum(np.diff(W.seg_offsets) - W.seam_w, 0)
         in_b = 2 if W.dtype == torch.bfloat16 else 4
         nbytes = (W.n_tokens * (W.h_k * W.d_k + W.h_v * W.d_v) * in_b + S.numel() * 4 + T.numel() * 4
@@ -394,14 +401,15 @@ def measure_rows(dev, hy, peaks):
         r = {"ms": ms, "tokens_per_s": W.n_tokens / (ms * 1e-3), "algorithmic_bytes": nbytes,
              "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"]}}
         if W.variant in ("gdn", "deltanet", "channel"):
-            fl = (build_flops(bodies, W.h_v, g=1, chunk=32) if W.variant == "channel"
-                  else build_flops(bodies, W.h_v))
+            # the 64-token chunk formula for every variant (the per-channel
+            # kernel's own chunk length does not change the algorithmic work)
+            fl = build_flops(bodies, W.h_v, g=1 if W.variant == "channel" else 2)
             tf = fl / (ms * 1e-3) / 1e12
             r["tensor"] = {"achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": tf / peaks["bf16"]}
-        tc_shape = W.dtype == torch.bfloat16 and W.d_k == 128 and W.d_v == 128
-        r["kernel"] = ("tensor-core chunkwise" if tc_shape and W.variant in ("gdn", "deltanet", "channel")
-                       else "tensor-core fast path" if tc_shape and W.variant in ("scalar", "ungated", "diag")
-                       else "fp32 token recurrence")
+        r["kernel"] = hy.build_path(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=W.variant, seam_w=W.seam_w,
+                                    T_pool=T, S_pool=S)
+        if round_robin:
+            r["lpt_vs_round_robin"] = {"lpt_ms": ms, "round_robin_ms": ms_rr, "speedup": ms_rr / ms}
         rows[name] = r
         del L, T, S
 
@@ -409,7 +417,7 @@ def measure_rows(dev, hy, peaks):
     rows["forward: GDN layer 64 x 1024 tokens, pairs + body outputs"] = forward_row(dev, hy)
     for var in ("gdn", "deltanet", "channel"):
         W = si.workload(5, seed=0, device=dev, variant=var)
-        one(f"build: uneven 256-segment mix ({W.n_tokens} tokens), {var}", W)
+        one(f"build: uneven 256-segment mix ({W.n_tokens} tokens), {var}", W, round_robin=var == "gdn")
         del W
         torch.cuda.empty_cache()
     return rows

@@ -31,6 +31,10 @@ VARIANT = {"gdn": GDN, "deltanet": DELTANET, "channel": CHANNEL_DELTA, "scalar":
            "ungated": UNGATED, "diag": DIAG_GATE}
 IN_BF16, IN_F32 = 0, 1
 FLAG_CHECK_FINITE = 1
+FLAG_ROUND_ROBIN = 2            # build: static round-robin schedule (measurement)
+FLAG_REQUIRE_TENSOR_CORES = 4   # refuse calls that would run an fp32 CUDA-core kernel
+PATHS = ("none", "tc_chunkwise", "tc_channel", "tc_fast", "f32_token", "tc_compose", "f32_compose", "tc_merge",
+         "f32_merge")
 STATUS_TIMEOUT, STATUS_NONFINITE, STATUS_BAD_SLOT = 1, 2, 4
 OK = 0
 
@@ -90,6 +94,7 @@ ROPE_LAYOUT = {"interleaved": 0, "half": 1}
 SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_workspace_bytes", "hypic_compose",
            "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_pair_rerotate", "hypic_segment_forward",
            "hypic_segment_build_host",
+           "hypic_build_path", "hypic_forward_path", "hypic_compose_path", "hypic_merge_path",
            "hypic_plan_lpt",
            "hypic_status_from_word", "hypic_status_string", "hypic_version")
 
@@ -130,6 +135,10 @@ def load():
             lib.hypic_segment_build_host.restype = ctypes.c_int
             lib.hypic_pair_rerotate.argtypes = [ctypes.POINTER(RerotateDesc), P]
             lib.hypic_pair_rerotate.restype = ctypes.c_int
+            for name, desc in (("hypic_build_path", BuildDesc), ("hypic_forward_path", ForwardDesc),
+                               ("hypic_compose_path", ComposeDesc), ("hypic_merge_path", MergeDesc)):
+                getattr(lib, name).argtypes = [ctypes.POINTER(desc)]
+                getattr(lib, name).restype = ctypes.c_int
             lib.hypic_plan_lpt.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P]
             lib.hypic_plan_lpt.restype = ctypes.c_int
             lib.hypic_status_from_word.argtypes = [ctypes.c_uint32]
@@ -323,7 +332,7 @@ def segment_build_host(k_host, v_host, g_host, beta_host, seg_offsets, *, varian
     return workspace
 
 
-NOALLOC_MAX_PAIRS = 16383  # HYPIC_NOALLOC_MAX_PAIRS
+NOALLOC_MAX_PAIRS = 32766  # HYPIC_NOALLOC_MAX_PAIRS
 
 
 def segment_build_noalloc(k, v, g, beta, seg_offsets, *, variant: str, seam_w: int, T_pool, S_pool,
@@ -341,12 +350,8 @@ def segment_build_noalloc(k, v, g, beta, seg_offsets, *, variant: str, seam_w: i
         raise HypicError(rc, "hypic_segment_build_noalloc")
 
 
-def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str,
-            S_out, seam_out=None, S_init=None, h_k=None, d_k=None, d_v=None, status=None,
-            flags: int = 0, stream=None):
-    """hypic_compose on torch tensors.  slot int32 [L, n_seg] (device);
-    seam arrays [L, n_seg, w, heads, d]; S_out [L, h_v, d_k, d_v]."""
-    lib = load()
+def _compose_desc(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, variant, S_out, seam_out,
+                  S_init, h_k, status, flags):
     _check(slot, "slot", dtype=torch.int32, ndim=2)
     _check(S_out, "S_out", dtype=torch.float32, ndim=4)
     for name, t in (("seam_k", seam_k), ("seam_v", seam_v), ("seam_q", seam_q)):
@@ -358,8 +363,7 @@ def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, 
     d.seam_w = w
     d.h_k = seam_k.shape[3] if seam_k is not None else (h_k if h_k is not None else d.h_v)
     d.variant = VARIANT[variant]
-    ref = seam_k if seam_k is not None else None
-    d.in_dtype = _in_dtype(ref) if ref is not None else IN_BF16
+    d.in_dtype = _in_dtype(seam_k) if seam_k is not None else IN_BF16
     d.flags = int(flags)
     d.slot = _ptr(slot)
     d.n_slots = S_pool.shape[0]
@@ -367,25 +371,64 @@ def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, 
     d.seam_k, d.seam_v, d.seam_q = _ptr(seam_k), _ptr(seam_v), _ptr(seam_q)
     d.seam_g, d.seam_beta = _ptr(seam_g), _ptr(seam_beta)
     d.S_init, d.S_out, d.seam_out = _ptr(S_init), _ptr(S_out), _ptr(seam_out)
+    d.status = _ptr(status)
+    return d
+
+
+def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str,
+            S_out, seam_out=None, S_init=None, h_k=None, d_k=None, d_v=None, status=None,
+            flags: int = 0, stream=None):
+    """hypic_compose on torch tensors.  slot int32 [L, n_seg] (device);
+    seam arrays [L, n_seg, w, heads, d]; S_out [L, h_v, d_k, d_v]."""
+    lib = load()
+    d = _compose_desc(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, variant, S_out, seam_out,
+                      S_init, h_k, status, flags)
     nb = int(lib.hypic_compose_workspace_bytes(ctypes.byref(d)))
     ws = alloc_workspace(nb, S_out.device) if nb else None
     d.workspace = _ptr(ws)
     d.workspace_bytes = 0 if ws is None else ws.numel()
-    d.status = _ptr(status)
     rc = lib.hypic_compose(ctypes.byref(d), _stream(stream))
     if rc != OK:
         raise HypicError(rc, "hypic_compose")
 
 
-def pair_merge(later, earlier, out, T_a, S_a, T_out, S_out, *, variant: str, T_b=None, S_b=None, status=None,
-               stream=None):
-    """hypic_pair_merge on torch tensors: for every merge m and head h,
-    T_out[out[m], h] = T_a[later[m], h] T_b[earlier[m], h] and
-    S_out[out[m], h] = T_a[later[m], h] S_b[earlier[m], h] + S_a[later[m], h].
-    later / earlier / out int32 [n_merge] (device); pools as written by
-    segment_build (T layout per variant, S [slots, h_v, d_k, d_v]); the pool
-    of the earlier pairs defaults to that of the later ones."""
-    lib = load()
+def compose_path(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str, S_out,
+                 seam_out=None, S_init=None, h_k=None, flags: int = 0) -> str:
+    """hypic_compose_path: the kernel compose() runs for these arguments."""
+    d = _compose_desc(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, variant, S_out, seam_out,
+                      S_init, h_k, None, flags)
+    return _path_name(load().hypic_compose_path(ctypes.byref(d)), "hypic_compose_path")
+
+
+def _path_name(rc, where):
+    if rc < 0:
+        raise HypicError(-rc, where)
+    return PATHS[rc]
+
+
+def build_path(k, v, g, beta, seg_offsets, *, variant: str, seam_w: int, T_pool, S_pool, slot_of_seg=None,
+               flags: int = 0) -> str:
+    """hypic_build_path: the kernel segment_build() runs for these arguments."""
+    d, keep = _build_desc(k, v, g, beta, seg_offsets, variant, seam_w, T_pool, S_pool, slot_of_seg, None, None,
+                          flags)
+    rc = load().hypic_build_path(ctypes.byref(d))
+    del keep
+    return _path_name(rc, "hypic_build_path")
+
+
+def forward_path(k, v, q, g, beta, seg_offsets, *, variant: str, seam_w: int, T_pool, S_pool, o_out,
+                 flags: int = 0) -> str:
+    """hypic_forward_path: the kernel of segment_forward()'s per-token outputs."""
+    d = ForwardDesc()
+    b, keep = _build_desc(k, v, g, beta, seg_offsets, variant, seam_w, T_pool, S_pool, None, None, None, flags)
+    d.build = b
+    d.q, d.o_out = _ptr(q), _ptr(o_out)
+    rc = load().hypic_forward_path(ctypes.byref(d))
+    del keep
+    return _path_name(rc, "hypic_forward_path")
+
+
+def _merge_desc(later, earlier, out, T_a, S_a, T_out, S_out, variant, T_b, S_b, status):
     if T_b is None:
         T_b, S_b = T_a, S_a
     for name, t in (("later", later), ("earlier", earlier), ("out", out)):
@@ -401,9 +444,27 @@ def pair_merge(later, earlier, out, T_a, S_a, T_out, S_out, *, variant: str, T_b
     d.T_a, d.S_a, d.T_b, d.S_b = _ptr(T_a), _ptr(S_a), _ptr(T_b), _ptr(S_b)
     d.T_out, d.S_out = _ptr(T_out), _ptr(S_out)
     d.status = _ptr(status)
-    rc = lib.hypic_pair_merge(ctypes.byref(d), _stream(stream))
+    return d
+
+
+def pair_merge(later, earlier, out, T_a, S_a, T_out, S_out, *, variant: str, T_b=None, S_b=None, status=None,
+               stream=None):
+    """hypic_pair_merge on torch tensors: for every merge m and head h,
+    T_out[out[m], h] = T_a[later[m], h] T_b[earlier[m], h] and
+    S_out[out[m], h] = T_a[later[m], h] S_b[earlier[m], h] + S_a[later[m], h].
+    later / earlier / out int32 [n_merge] (device); pools as written by
+    segment_build (T layout per variant, S [slots, h_v, d_k, d_v]); the pool
+    of the earlier pairs defaults to that of the later ones."""
+    d = _merge_desc(later, earlier, out, T_a, S_a, T_out, S_out, variant, T_b, S_b, status)
+    rc = load().hypic_pair_merge(ctypes.byref(d), _stream(stream))
     if rc != OK:
         raise HypicError(rc, "hypic_pair_merge")
+
+
+def merge_path(later, earlier, out, T_a, S_a, T_out, S_out, *, variant: str, T_b=None, S_b=None) -> str:
+    """hypic_merge_path: the kernel pair_merge() runs for these arguments."""
+    d = _merge_desc(later, earlier, out, T_a, S_a, T_out, S_out, variant, T_b, S_b, None)
+    return _path_name(load().hypic_merge_path(ctypes.byref(d)), "hypic_merge_path")
 
 
 def pair_rerotate(slot_in, slot_out, delta, T_in, S_in, T_out, S_out, *, variant: str, rot_dim: int,

@@ -42,7 +42,6 @@ int check_common_shapes(int h_k, int h_v, int d_k, int d_v, int seam_w, int vari
 
 int64_t n_build_items(const hypic_build_desc *d) { return (int64_t)d->n_seg * d->h_v; }
 
-size_t plan_bytes(int64_t n_items) { return round_up(sizeof(PlanHeader) + n_items * sizeof(BuildItem), kAlign); }
 
 }  // namespace
 
@@ -77,15 +76,122 @@ namespace hypic {
 // gated delta rule, and the fast path of the transitions without an erase:
 // scalar decay, ungated, diagonal gate); every other case runs the fp32 token
 // recurrence.
-cudaError_t launch_build(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, cudaStream_t s) {
+int build_path(const BuildParams &p, int64_t n_tokens) {
   // no tokens at all: every pair is (I, 0) (or the empty gate product), which
   // the token kernel writes without reading an input; the tensor-core
   // kernels cannot describe an empty token tensor
-  if (n_tokens == 0) return launch_build_token(p, n_items, n_sm, s);
-  if (build_tc_supported(p)) return launch_build_tc(p, n_tokens, n_items, n_sm, wait_limit(), s);
-  if (build_channel_supported(p)) return launch_build_channel(p, n_tokens, n_items, n_sm, wait_limit(), s);
-  if (build_fast_supported(p)) return launch_build_fast(p, n_tokens, n_items, n_sm, wait_limit(), s);
-  return launch_build_token(p, n_items, n_sm, s);
+  if (n_tokens == 0) return HYPIC_PATH_F32_TOKEN;
+  if (build_tc_supported(p)) return HYPIC_PATH_TC_CHUNKWISE;
+  if (build_channel_supported(p)) return HYPIC_PATH_TC_CHANNEL;
+  if (build_fast_supported(p)) return HYPIC_PATH_TC_FAST;
+  return HYPIC_PATH_F32_TOKEN;
+}
+
+cudaError_t launch_build(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, cudaStream_t s) {
+  switch (build_path(p, n_tokens)) {
+    case HYPIC_PATH_TC_CHUNKWISE: return launch_build_tc(p, n_tokens, n_items, n_sm, wait_limit(), s);
+    case HYPIC_PATH_TC_CHANNEL: return launch_build_channel(p, n_tokens, n_items, n_sm, wait_limit(), s);
+    case HYPIC_PATH_TC_FAST: return launch_build_fast(p, n_tokens, n_items, n_sm, wait_limit(), s);
+    default: return launch_build_token(p, n_items, n_sm, s);
+  }
+}
+
+// ---- build descriptors: the checks and the plan every build entry point
+// shares (no heap use, so that the allocation-free entry point runs them too)
+int check_build_shapes(const hypic_build_desc *d) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  int st = check_common_shapes(d->h_k, d->h_v, d->d_k, d->d_v, d->seam_w, d->variant, d->in_dtype);
+  if (st) return st;
+  if (d->n_tokens < 0 || d->n_seg < 0 || d->n_slots < 0) return HYPIC_ERR_INVALID_ARG;
+  if (!d->seg_offsets) return HYPIC_ERR_INVALID_ARG;
+  if (d->seg_offsets[0] != 0 || d->seg_offsets[d->n_seg] != d->n_tokens) return HYPIC_ERR_INVALID_ARG;
+  for (int i = 0; i < d->n_seg; i++)
+    if (d->seg_offsets[i + 1] < d->seg_offsets[i]) return HYPIC_ERR_INVALID_ARG;
+  if (d->flags & ~(HYPIC_FLAG_CHECK_FINITE | HYPIC_FLAG_ROUND_ROBIN | HYPIC_FLAG_REQUIRE_TENSOR_CORES))
+    return HYPIC_ERR_INVALID_ARG;
+  if (n_build_items(d) > INT32_MAX / 2) return HYPIC_ERR_UNSUPPORTED;
+  return HYPIC_OK;
+}
+
+int check_build_pointers(const hypic_build_desc *d) {
+  const int esz = in_size(d->in_dtype);
+  if (d->n_tokens > 0) {
+    if (!d->k || !d->v || !aligned(d->k, esz) || !aligned(d->v, esz)) return HYPIC_ERR_INVALID_ARG;
+  }
+  const bool delta = is_delta(d->variant);
+  const bool needs_g = d->variant == HYPIC_GDN || d->variant == HYPIC_CHANNEL_DELTA ||
+                       d->variant == HYPIC_DIAG_GATE || d->variant == HYPIC_SCALAR_DECAY;
+  // per-token log-gates are read only when there are tokens; the per-head
+  // decay always
+  const bool reads_g = needs_g && (d->n_tokens > 0 || d->variant == HYPIC_SCALAR_DECAY);
+  if (reads_g && (!d->g || !aligned(d->g, 4))) return HYPIC_ERR_INVALID_ARG;
+  if (delta && d->n_tokens > 0 && (!d->beta || !aligned(d->beta, 4))) return HYPIC_ERR_INVALID_ARG;
+  if (!d->T_pool || !d->S_pool || !aligned(d->T_pool, 4) || !aligned(d->S_pool, 4)) return HYPIC_ERR_INVALID_ARG;
+  return HYPIC_OK;
+}
+
+int check_build_slots(const hypic_build_desc *d, int32_t *sorted) {
+  for (int i = 0; i < d->n_seg; i++) sorted[i] = d->slot_of_seg ? d->slot_of_seg[i] : i;
+  std::sort(sorted, sorted + d->n_seg);
+  for (int i = 0; i < d->n_seg; i++) {
+    if (sorted[i] < 0 || sorted[i] >= d->n_slots) return HYPIC_ERR_INVALID_ARG;
+    if (i && sorted[i] == sorted[i - 1]) return HYPIC_ERR_INVALID_ARG;  // two items writing one slot would race
+  }
+  return HYPIC_OK;
+}
+
+size_t build_plan_size(int64_t n_items) { return sizeof(PlanHeader) + (size_t)n_items * sizeof(BuildItem); }
+
+void fill_build_plan(const hypic_build_desc *d, void *plan) {
+  const int64_t n_items = n_build_items(d);
+  PlanHeader *hdr = static_cast<PlanHeader *>(plan);
+  std::memset(hdr, 0, sizeof(PlanHeader));
+  hdr->n_items = (int32_t)n_items;
+  const bool rr = (d->flags & HYPIC_FLAG_ROUND_ROBIN) != 0;
+  hdr->mode = rr ? PLAN_ROUND_ROBIN : PLAN_LPT;
+  BuildItem *items = reinterpret_cast<BuildItem *>(hdr + 1);
+  int64_t r = 0;
+  for (int i = 0; i < d->n_seg; i++) {
+    BuildItem b;
+    b.seg = i;
+    b.slot = d->slot_of_seg ? d->slot_of_seg[i] : i;
+    b.part = 0;
+    b.start = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
+    b.end = d->seg_offsets[i + 1];
+    for (int h = 0; h < d->h_v; h++) {
+      b.head = h;
+      items[r++] = b;
+    }
+  }
+  if (rr) return;  // index order: segment-major, head-minor
+  // LPT: longest body first; ties in index order (a total order, so the
+  // in-place sort is deterministic)
+  std::sort(items, items + n_items, [](const BuildItem &a, const BuildItem &b) {
+    const int64_t ca = a.end - a.start, cb = b.end - b.start;
+    if (ca != cb) return ca > cb;
+    if (a.seg != b.seg) return a.seg < b.seg;
+    return a.head < b.head;
+  });
+}
+
+BuildParams build_params(const hypic_build_desc *d) {
+  BuildParams p{};
+  p.h_k = d->h_k;
+  p.h_v = d->h_v;
+  p.d_k = d->d_k;
+  p.d_v = d->d_v;
+  p.variant = d->variant;
+  p.in_dtype = d->in_dtype;
+  p.flags = d->flags;
+  p.n_slots = d->n_slots;
+  p.k = d->k;
+  p.v = d->v;
+  p.g = d->g;
+  p.beta = d->beta;
+  p.T_pool = d->T_pool;
+  p.S_pool = d->S_pool;
+  p.status = d->status;
+  return p;
 }
 
 }  // namespace hypic
@@ -144,112 +250,53 @@ int hypic_plan_lpt(const int64_t *costs, int32_t n_items, int32_t n_workers, int
 
 size_t hypic_build_workspace_bytes(const hypic_build_desc *d) {
   if (!d || d->n_seg < 0 || d->h_v < 1) return 0;
-  return plan_bytes(2 * n_build_items(d));  // room for up to two items per pair
+  return round_up(build_plan_size(n_build_items(d)), kAlign);  // one item per (segment, value head)
 }
 
 }  // extern "C"
 
 namespace {
-// the build (q == NULL) or the prefill forward (q, o_out): validation, LPT
-// plan, launch
 // the argument checks of a build (everything but the workspace); fills the
 // slot of every segment
 int check_build(const hypic_build_desc *d, std::vector<int32_t> &slots) {
-  if (!d) return HYPIC_ERR_INVALID_ARG;
-  int st = check_common_shapes(d->h_k, d->h_v, d->d_k, d->d_v, d->seam_w, d->variant, d->in_dtype);
-  if (st) return st;
-  if (d->n_tokens < 0 || d->n_seg < 0 || d->n_slots < 0) return HYPIC_ERR_INVALID_ARG;
-  if (!d->seg_offsets) return HYPIC_ERR_INVALID_ARG;
-  if (d->seg_offsets[0] != 0 || d->seg_offsets[d->n_seg] != d->n_tokens) return HYPIC_ERR_INVALID_ARG;
-  for (int i = 0; i < d->n_seg; i++)
-    if (d->seg_offsets[i + 1] < d->seg_offsets[i]) return HYPIC_ERR_INVALID_ARG;
-  if (d->n_seg == 0) return HYPIC_OK;
-  const int esz = in_size(d->in_dtype);
-  if (d->n_tokens > 0) {
-    if (!d->k || !d->v || !aligned(d->k, esz) || !aligned(d->v, esz)) return HYPIC_ERR_INVALID_ARG;
-  }
-  const bool delta = is_delta(d->variant);
-  const bool needs_g = d->variant == HYPIC_GDN || d->variant == HYPIC_CHANNEL_DELTA ||
-                       d->variant == HYPIC_DIAG_GATE || d->variant == HYPIC_SCALAR_DECAY;
-  // per-token log-gates are read only when there are tokens; the per-head
-  // decay always
-  const bool reads_g = needs_g && (d->n_tokens > 0 || d->variant == HYPIC_SCALAR_DECAY);
-  if (reads_g && (!d->g || !aligned(d->g, 4))) return HYPIC_ERR_INVALID_ARG;
-  if (delta && d->n_tokens > 0 && (!d->beta || !aligned(d->beta, 4))) return HYPIC_ERR_INVALID_ARG;
-  if (!d->T_pool || !d->S_pool || !aligned(d->T_pool, 4) || !aligned(d->S_pool, 4)) return HYPIC_ERR_INVALID_ARG;
-  // slots: in range and distinct (two items writing one slot would race)
+  int st = check_build_shapes(d);
+  if (st || d->n_seg == 0) return st;
+  if ((st = check_build_pointers(d))) return st;
+  std::vector<int32_t> sorted(d->n_seg);
+  if ((st = check_build_slots(d, sorted.data()))) return st;
   slots.assign(d->n_seg, 0);
   for (int i = 0; i < d->n_seg; i++) slots[i] = d->slot_of_seg ? d->slot_of_seg[i] : i;
-  std::vector<int32_t> s2(slots);
-  std::sort(s2.begin(), s2.end());
-  for (int i = 0; i < d->n_seg; i++) {
-    if (s2[i] < 0 || s2[i] >= d->n_slots) return HYPIC_ERR_INVALID_ARG;
-    if (i && s2[i] == s2[i - 1]) return HYPIC_ERR_INVALID_ARG;
-  }
   return HYPIC_OK;
 }
 
+// HYPIC_FLAG_REQUIRE_TENSOR_CORES: refuse a call that would run an fp32
+// CUDA-core kernel (a call with no tokens has nothing to compute and passes)
+bool refused_fallback(uint32_t flags, int path, int64_t n_tokens) {
+  return (flags & HYPIC_FLAG_REQUIRE_TENSOR_CORES) && n_tokens > 0 &&
+         (path == HYPIC_PATH_F32_TOKEN || path == HYPIC_PATH_F32_COMPOSE);
+}
+
+// the build (q == NULL) or the prefill forward (q, o_out): validation, LPT
+// plan, launch
 int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_stream_t stream) {
   std::vector<int32_t> slots;
   int st = check_build(d, slots);
   if (st || d->n_seg == 0) return st;
-  BuildParams p{};
-  p.h_k = d->h_k;
-  p.h_v = d->h_v;
-  p.d_k = d->d_k;
-  p.d_v = d->d_v;
-  p.variant = d->variant;
-  p.in_dtype = d->in_dtype;
-  p.flags = d->flags;
-  p.n_slots = d->n_slots;
-  p.k = d->k;
-  p.v = d->v;
-  p.g = d->g;
-  p.beta = d->beta;
-  p.T_pool = d->T_pool;
-  p.S_pool = d->S_pool;
+  BuildParams p = build_params(d);
+  if (refused_fallback(d->flags, build_path(p, d->n_tokens), d->n_tokens)) return HYPIC_ERR_UNSUPPORTED;
+  // the forward's outputs run on the CUDA cores
+  if (o_out && refused_fallback(d->flags, HYPIC_PATH_F32_TOKEN, d->n_tokens)) return HYPIC_ERR_UNSUPPORTED;
   p.q = q;
   p.o_out = o_out;
   p.plan = reinterpret_cast<PlanHeader *>(d->workspace);
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
-  p.status = d->status;
+
   // one item per (segment, value head) on every kernel (see launch_build)
-  const int parts = 1;
-
-  const int64_t n_pairs = n_build_items(d);
-  const int64_t n_items = n_pairs * parts;
-  if (n_items > INT32_MAX / 2) return HYPIC_ERR_UNSUPPORTED;
-  const size_t need = plan_bytes(n_items);
+  const int64_t n_items = n_build_items(d);
+  const size_t need = round_up(build_plan_size(n_items), kAlign);
   if (!d->workspace || d->workspace_bytes < need || !aligned(d->workspace, kAlign)) return HYPIC_ERR_WORKSPACE;
-
-  // ---- LPT plan over the items; cost = body length ----
-  std::vector<int64_t> cost(n_items);
-  for (int64_t it = 0; it < n_items; it++) {
-    const int i = (int)((it / parts) / d->h_v);
-    const int64_t s0 = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
-    cost[it] = d->seg_offsets[i + 1] - s0;
-  }
-  std::vector<int32_t> order(n_items);
-  st = hypic_plan_lpt(cost.data(), (int32_t)n_items, sm_count(), order.data(), nullptr, nullptr);
-  if (st) return st;
   std::vector<unsigned char> host(need, 0);
-  PlanHeader *hdr = reinterpret_cast<PlanHeader *>(host.data());
-  hdr->ticket = 0;
-  hdr->n_items = (int32_t)n_items;
-  BuildItem *items = reinterpret_cast<BuildItem *>(hdr + 1);
-  for (int64_t r = 0; r < n_items; r++) {
-    const int64_t it = order[r];
-    const int64_t pr = it / parts;
-    const int i = (int)(pr / d->h_v);
-    BuildItem b;
-    b.seg = i;
-    b.head = (int32_t)(pr % d->h_v);
-    b.slot = slots[i];
-    b.part = (int32_t)(it % parts);
-    b.start = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
-    b.end = d->seg_offsets[i + 1];
-    items[r] = b;
-  }
+  fill_build_plan(d, host.data());
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // pageable source: the call returns once the bytes are staged, so `host`
   // may be released when it goes out of scope
@@ -269,6 +316,101 @@ int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_str
 }
 }  // namespace
 
+
+namespace {
+int check_compose(const hypic_compose_desc *d) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  int st = check_common_shapes(d->h_k, d->h_v, d->d_k, d->d_v, d->seam_w, d->variant, d->in_dtype);
+  if (st) return st;
+  if (d->n_layers < 0 || d->n_seg < 0 || d->n_slots < 0) return HYPIC_ERR_INVALID_ARG;
+  if (d->flags & ~(HYPIC_FLAG_CHECK_FINITE | HYPIC_FLAG_REQUIRE_TENSOR_CORES)) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_layers == 0) return HYPIC_OK;
+  if (!d->S_out || !aligned(d->S_out, 4)) return HYPIC_ERR_INVALID_ARG;
+  if (d->S_init && !aligned(d->S_init, 4)) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_seg > 0) {
+    if (!d->slot || !aligned(d->slot, 4) || !d->T_pool || !d->S_pool) return HYPIC_ERR_INVALID_ARG;
+    if (!aligned(d->T_pool, 4) || !aligned(d->S_pool, 4)) return HYPIC_ERR_INVALID_ARG;
+  }
+  const bool delta = is_delta(d->variant);
+  const int esz = in_size(d->in_dtype);
+  if (d->seam_w > 0 && d->n_seg > 0) {
+    if (!d->seam_k || !d->seam_v || !d->seam_q || !d->seam_out) return HYPIC_ERR_INVALID_ARG;
+    if (!aligned(d->seam_k, esz) || !aligned(d->seam_v, esz) || !aligned(d->seam_q, esz)) return HYPIC_ERR_INVALID_ARG;
+    if (!aligned(d->seam_out, 4)) return HYPIC_ERR_INVALID_ARG;
+    if (delta && !d->seam_beta) return HYPIC_ERR_INVALID_ARG;
+    if ((d->variant == HYPIC_GDN || is_vector_gate(d->variant)) && !d->seam_g) return HYPIC_ERR_INVALID_ARG;
+  }
+  if (d->variant == HYPIC_SCALAR_DECAY && !d->seam_g) return HYPIC_ERR_INVALID_ARG;
+  return HYPIC_OK;
+}
+
+ComposeParams compose_params(const hypic_compose_desc *d) {
+  ComposeParams p{};
+  p.n_layers = d->n_layers;
+  p.n_seg = d->n_seg;
+  p.h_k = d->h_k;
+  p.h_v = d->h_v;
+  p.d_k = d->d_k;
+  p.d_v = d->d_v;
+  p.seam_w = d->seam_w;
+  p.variant = d->variant;
+  p.in_dtype = d->in_dtype;
+  p.flags = d->flags;
+  p.slot = d->slot;
+  p.n_slots = d->n_slots;
+  p.T_pool = d->T_pool;
+  p.S_pool = d->S_pool;
+  p.seam_k = d->seam_k;
+  p.seam_v = d->seam_v;
+  p.seam_q = d->seam_q;
+  p.seam_g = d->seam_g;
+  p.seam_beta = d->seam_beta;
+  p.S_init = d->S_init;
+  p.S_out = d->S_out;
+  p.seam_out = d->seam_out;
+  p.status = d->status;
+  return p;
+}
+
+int check_merge(const hypic_merge_desc *d) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_merge < 0 || d->h_v < 1 || d->d_k < 1 || d->d_v < 1) return HYPIC_ERR_INVALID_ARG;
+  if (d->variant < HYPIC_GDN || d->variant > HYPIC_DIAG_GATE) return HYPIC_ERR_INVALID_ARG;
+  if (d->d_k > 128 || d->d_v > 128) return HYPIC_ERR_UNSUPPORTED;
+  if (d->n_slots_a < 0 || d->n_slots_b < 0 || d->n_slots_out < 0) return HYPIC_ERR_INVALID_ARG;
+  if ((int64_t)d->n_merge * d->h_v > INT32_MAX) return HYPIC_ERR_UNSUPPORTED;
+  if (d->n_merge == 0) return HYPIC_OK;
+  if (!d->later || !d->earlier || !d->out || !aligned(d->later, 4) || !aligned(d->earlier, 4) || !aligned(d->out, 4))
+    return HYPIC_ERR_INVALID_ARG;
+  const float *pools[6] = {d->T_a, d->S_a, d->T_b, d->S_b, d->T_out, d->S_out};
+  for (const float *q : pools)
+    if (!q || !aligned(q, 4)) return HYPIC_ERR_INVALID_ARG;
+  return HYPIC_OK;
+}
+
+MergeParams merge_params(const hypic_merge_desc *d) {
+  MergeParams p{};
+  p.n_merge = d->n_merge;
+  p.h_v = d->h_v;
+  p.d_k = d->d_k;
+  p.d_v = d->d_v;
+  p.variant = d->variant;
+  p.later = d->later;
+  p.earlier = d->earlier;
+  p.out = d->out;
+  p.n_slots_a = d->n_slots_a;
+  p.n_slots_b = d->n_slots_b;
+  p.n_slots_out = d->n_slots_out;
+  p.T_a = d->T_a;
+  p.S_a = d->S_a;
+  p.T_b = d->T_b;
+  p.S_b = d->S_b;
+  p.T_out = d->T_out;
+  p.S_out = d->S_out;
+  p.status = d->status;
+  return p;
+}
+}  // namespace
 
 // ---- the host-buffer build: copy streams and events per device, created on
 // first use and kept for the life of the process.  An event may be recorded
@@ -425,95 +567,56 @@ size_t hypic_compose_workspace_bytes(const hypic_compose_desc *d) {
 }
 
 int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream) {
-  if (!d) return HYPIC_ERR_INVALID_ARG;
-  int st = check_common_shapes(d->h_k, d->h_v, d->d_k, d->d_v, d->seam_w, d->variant, d->in_dtype);
-  if (st) return st;
-  if (d->n_layers < 0 || d->n_seg < 0 || d->n_slots < 0) return HYPIC_ERR_INVALID_ARG;
-  if (d->n_layers == 0) return HYPIC_OK;
-  if (!d->S_out || !aligned(d->S_out, 4)) return HYPIC_ERR_INVALID_ARG;
-  if (d->S_init && !aligned(d->S_init, 4)) return HYPIC_ERR_INVALID_ARG;
-  if (d->n_seg > 0) {
-    if (!d->slot || !aligned(d->slot, 4) || !d->T_pool || !d->S_pool) return HYPIC_ERR_INVALID_ARG;
-    if (!aligned(d->T_pool, 4) || !aligned(d->S_pool, 4)) return HYPIC_ERR_INVALID_ARG;
-  }
-  const bool delta = is_delta(d->variant);
-  const int esz = in_size(d->in_dtype);
-  if (d->seam_w > 0 && d->n_seg > 0) {
-    if (!d->seam_k || !d->seam_v || !d->seam_q || !d->seam_out) return HYPIC_ERR_INVALID_ARG;
-    if (!aligned(d->seam_k, esz) || !aligned(d->seam_v, esz) || !aligned(d->seam_q, esz)) return HYPIC_ERR_INVALID_ARG;
-    if (!aligned(d->seam_out, 4)) return HYPIC_ERR_INVALID_ARG;
-    if (delta && !d->seam_beta) return HYPIC_ERR_INVALID_ARG;
-    if ((d->variant == HYPIC_GDN || is_vector_gate(d->variant)) && !d->seam_g) return HYPIC_ERR_INVALID_ARG;
-  }
-  if (d->variant == HYPIC_SCALAR_DECAY && !d->seam_g) return HYPIC_ERR_INVALID_ARG;
-
-  ComposeParams p{};
-  p.n_layers = d->n_layers;
-  p.n_seg = d->n_seg;
-  p.h_k = d->h_k;
-  p.h_v = d->h_v;
-  p.d_k = d->d_k;
-  p.d_v = d->d_v;
-  p.seam_w = d->seam_w;
-  p.variant = d->variant;
-  p.in_dtype = d->in_dtype;
-  p.flags = d->flags;
-  p.slot = d->slot;
-  p.n_slots = d->n_slots;
-  p.T_pool = d->T_pool;
-  p.S_pool = d->S_pool;
-  p.seam_k = d->seam_k;
-  p.seam_v = d->seam_v;
-  p.seam_q = d->seam_q;
-  p.seam_g = d->seam_g;
-  p.seam_beta = d->seam_beta;
-  p.S_init = d->S_init;
-  p.S_out = d->S_out;
-  p.seam_out = d->seam_out;
-  p.status = d->status;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int st = check_compose(d);
+  if (st || d->n_layers == 0) return st;
+  const ComposeParams p = compose_params(d);
   // Dense transitions with bf16 seam tokens and 128-wide heads stream the
   // pool through the tensor cores; fp32 inputs (1e-5 bar), smaller heads and
   // scalar/diagonal transitions run the fp32 kernel.
-  cudaError_t e = compose_tc_supported(p) ? launch_compose_tc(p, wait_limit(), s) : launch_compose_simt(p, s);
+  const int path = compose_tc_supported(p) ? HYPIC_PATH_TC_COMPOSE : HYPIC_PATH_F32_COMPOSE;
+  if (refused_fallback(d->flags, path, d->n_seg)) return HYPIC_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = path == HYPIC_PATH_TC_COMPOSE ? launch_compose_tc(p, wait_limit(), s) : launch_compose_simt(p, s);
   if (e != cudaSuccess) return HYPIC_ERR_CUDA;
   return HYPIC_OK;
 }
 
 int hypic_pair_merge(const hypic_merge_desc *d, hypic_stream_t stream) {
-  if (!d) return HYPIC_ERR_INVALID_ARG;
-  if (d->n_merge < 0 || d->h_v < 1 || d->d_k < 1 || d->d_v < 1) return HYPIC_ERR_INVALID_ARG;
-  if (d->variant < HYPIC_GDN || d->variant > HYPIC_DIAG_GATE) return HYPIC_ERR_INVALID_ARG;
-  if (d->d_k > 128 || d->d_v > 128) return HYPIC_ERR_UNSUPPORTED;
-  if (d->n_slots_a < 0 || d->n_slots_b < 0 || d->n_slots_out < 0) return HYPIC_ERR_INVALID_ARG;
-  if ((int64_t)d->n_merge * d->h_v > INT32_MAX) return HYPIC_ERR_UNSUPPORTED;
-  if (d->n_merge == 0) return HYPIC_OK;
-  if (!d->later || !d->earlier || !d->out || !aligned(d->later, 4) || !aligned(d->earlier, 4) || !aligned(d->out, 4))
-    return HYPIC_ERR_INVALID_ARG;
-  const float *pools[6] = {d->T_a, d->S_a, d->T_b, d->S_b, d->T_out, d->S_out};
-  for (const float *q : pools)
-    if (!q || !aligned(q, 4)) return HYPIC_ERR_INVALID_ARG;
-  MergeParams p{};
-  p.n_merge = d->n_merge;
-  p.h_v = d->h_v;
-  p.d_k = d->d_k;
-  p.d_v = d->d_v;
-  p.variant = d->variant;
-  p.later = d->later;
-  p.earlier = d->earlier;
-  p.out = d->out;
-  p.n_slots_a = d->n_slots_a;
-  p.n_slots_b = d->n_slots_b;
-  p.n_slots_out = d->n_slots_out;
-  p.T_a = d->T_a;
-  p.S_a = d->S_a;
-  p.T_b = d->T_b;
-  p.S_b = d->S_b;
-  p.T_out = d->T_out;
-  p.S_out = d->S_out;
-  p.status = d->status;
-  if (launch_merge(p, wait_limit(), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return HYPIC_ERR_CUDA;
+  int st = check_merge(d);
+  if (st || d->n_merge == 0) return st;
+  if (launch_merge(merge_params(d), wait_limit(), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return HYPIC_ERR_CUDA;
   return HYPIC_OK;
+}
+
+// ---- which kernel a call runs (the same predicates as the dispatch above)
+int hypic_build_path(const hypic_build_desc *d) {
+  const int st = check_build_shapes(d);
+  if (st) return -st;
+  if (d->n_seg == 0) return HYPIC_PATH_NONE;
+  return build_path(build_params(d), d->n_tokens);
+}
+
+int hypic_forward_path(const hypic_forward_desc *d) {
+  if (!d) return -HYPIC_ERR_INVALID_ARG;
+  const int st = check_build_shapes(&d->build);
+  if (st) return -st;
+  if (d->build.n_seg == 0) return HYPIC_PATH_NONE;
+  return HYPIC_PATH_F32_TOKEN;  // the outputs: fp32 token recurrence over the state columns
+}
+
+int hypic_compose_path(const hypic_compose_desc *d) {
+  const int st = check_compose(d);
+  if (st) return -st;
+  if (d->n_layers == 0) return HYPIC_PATH_NONE;
+  return compose_tc_supported(compose_params(d)) ? HYPIC_PATH_TC_COMPOSE : HYPIC_PATH_F32_COMPOSE;
+}
+
+int hypic_merge_path(const hypic_merge_desc *d) {
+  const int st = check_merge(d);
+  if (st) return -st;
+  if (d->n_merge == 0) return HYPIC_PATH_NONE;
+  return merge_tc_supported(merge_params(d)) ? HYPIC_PATH_TC_MERGE : HYPIC_PATH_F32_MERGE;
 }
 
 int hypic_pair_rerotate(const hypic_rerotate_desc *d, hypic_stream_t stream) {

@@ -718,9 +718,10 @@ __global__ void __launch_bounds__(NT, 1)
   uint32_t ph_full[2] = {0, 0};
   uint32_t gch = 0;  // chunks processed by this CTA so far
   const int n_items = p.plan->n_items;
+  int taken = 0;  // items fetched by this CTA (thread n == 0)
 
   for (;;) {
-    if (n == 0) sm.item = aborted(sm) ? n_items : atomicAdd(&p.plan->ticket, 1);
+    if (n == 0) sm.item = aborted(sm) ? n_items : take_item(p.plan, taken);
     __syncthreads();
     const int idx = sm.item;
     __syncthreads();

@@ -109,9 +109,10 @@ __global__ void __launch_bounds__(NT, 2)
   uint32_t ph_full[2] = {0, 0};
   uint32_t mcount = 0;  // commits to mma_done so far (uniform)
   const int n_items = p.plan->n_items;
+  int taken = 0;  // items fetched by this CTA (thread 0)
 
   for (;;) {
-    if (tid == 0) sm.item = aborted(sm) ? n_items : atomicAdd(&p.plan->ticket, 1);
+    if (tid == 0) sm.item = aborted(sm) ? n_items : take_item(p.plan, taken);
     __syncthreads();
     const int idx = sm.item;
     __syncthreads();

@@ -117,6 +117,7 @@ struct Issuer {
   bool ok[2];
   int w, ch;        // cursor: chunk ch of it[w]
   uint32_t g;       // the CTA's index of the chunk at the cursor
+  int taken;        // items fetched by this CTA so far
 };
 struct PItem {
   BuildItem it;
@@ -392,7 +393,7 @@ __device__ __forceinline__ void iss_issue(BuildTcSmem &sm, Issuer &s, const CUte
 }
 __device__ __forceinline__ void fetch_item(BuildTcSmem &sm, const BuildParams &p, int n_items, BuildItem &it, int &kh,
                                            int &nch, bool &ok) {
-  const int idx = aborted(sm) ? n_items : atomicAdd(&p.plan->ticket, 1);
+  const int idx = aborted(sm) ? n_items : take_item(p.plan, sm.iss.taken);
   ok = idx < n_items;
   nch = 0;
   kh = 0;
@@ -753,6 +754,7 @@ __global__ void __launch_bounds__(NT, 1)
       iss.w = 0;
       iss.ch = 0;
       iss.g = 0;
+      iss.taken = 0;
       fetch_item(sm, p, n_items, iss.it[0], iss.kh[0], iss.nch[0], iss.ok[0]);
       iss.ok[1] = false;
       iss.nch[1] = 0;

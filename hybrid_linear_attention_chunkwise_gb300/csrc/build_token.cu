@@ -70,9 +70,10 @@ __global__ void __launch_bounds__(256) build_token_kernel(BuildParams p) {
   const int col = is_T ? tid : tid - n_t_thr;      // column within T or S
   const bool active = is_T ? (col < d_k) : (col < d_v);
   const int n_items = p.plan->n_items;
+  int taken = 0;  // items fetched by this CTA (thread 0)
 
   for (;;) {
-    if (tid == 0) sm.item = atomicAdd(&p.plan->ticket, 1);
+    if (tid == 0) sm.item = take_item(p.plan, taken);
     __syncthreads();
     const int idx = sm.item;
     __syncthreads();
@@ -317,9 +318,10 @@ __global__ void __launch_bounds__(256) forward_out_kernel(BuildParams p, int asy
   const int es = p.in_dtype == HYPIC_IN_BF16 ? 2 : 4;
   const FwdRaw lay = fwd_raw_layout(DK, es, vec);
   unsigned char *raw = smem_raw + fwd_raw_offset<DK>();  // two stages when async_tiles
+  int taken = 0;  // items fetched by this CTA (thread 0)
 
   for (;;) {
-    if (tid == 0) sm.item = atomicAdd(&p.plan->ticket, 1);
+    if (tid == 0) sm.item = take_item(p.plan, taken);
     __syncthreads();
     const int idx = sm.item;
     __syncthreads();

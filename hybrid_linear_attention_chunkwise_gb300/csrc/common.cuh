@@ -18,4 +18,12 @@ __device__ __forceinline__ void report(uint32_t *status, uint32_t bits) {
 
 __device__ __forceinline__ bool finite_f(float x) { return isfinite(x); }
 
+// The next plan item for this CTA (called by the one thread that fetches the
+// CTA's items; `taken` counts its fetches): the shared ticket for an LPT
+// plan, the static round-robin sequence blockIdx.x + k * gridDim.x otherwise.
+__device__ __forceinline__ int take_item(PlanHeader *plan, int &taken) {
+  if (plan->mode == PLAN_ROUND_ROBIN) return (int)blockIdx.x + (int)gridDim.x * taken++;
+  return atomicAdd(&plan->ticket, 1);
+}
+
 }  // namespace hypic

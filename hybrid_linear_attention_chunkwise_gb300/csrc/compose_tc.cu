@@ -826,6 +826,7 @@ __global__ void __launch_bounds__(NT2, 2)
               x = fmaf(k1.z, cc[6], x);
               x = fmaf(k1.w, cc[7], x);
               out[(int64_t)rr * 128] = x;
+              bad |= !finite_f(x);
               ex[j] = x;
             }
             uint32_t rn[16];
@@ -852,6 +853,7 @@ __global__ void __launch_bounds__(NT2, 2)
 #pragma unroll
               for (int i = 0; i < GW; i++) x = fmaf(row[i * 32 + ((chunk ^ i) << 2)], cc[i], x);
               out[(int64_t)rr * 128] = x;
+              bad |= !finite_f(x);
               ex[j] = x;
             }
             uint32_t rn[16];
@@ -1051,7 +1053,7 @@ __global__ void __launch_bounds__(NT2, 2)
         for (int j = 0; j < 16; j++) {
           const float x = fmaf(al, __uint_as_float(r[j]), sc[j]);
           if (keep) out[(int64_t)(16 * b + j) * 128] = x;
-          if (last) bad |= !finite_f(x);
+          bad |= !finite_f(x);  // every segment: a non-finite state is reported where it appears
           // per-channel gate, next group fused: TMEM A holds RN(E_last . S)
           r[j] = tc::to_tf32(CH && scale_next ? x * el_next[16 * b + j] : x);
         }

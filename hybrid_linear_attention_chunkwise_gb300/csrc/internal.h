@@ -21,12 +21,22 @@ struct BuildItem {
   int64_t end;    // one past the last token
 };
 
-// Device-visible build plan header, followed by n_items BuildItem records in
-// LPT order.  `ticket` is the dynamic work counter (zeroed by the host copy).
+// Device-visible build plan header, followed by n_items BuildItem records.
+// `ticket` is the dynamic work counter (zeroed by the host copy).  `mode`
+// says how the persistent build kernels take items:
+//   PLAN_LPT          items in LPT order (longest body first, ties by index),
+//                     each CTA takes the next one from the shared ticket when
+//                     it is free: greedy LPT list scheduling over the SMs;
+//   PLAN_ROUND_ROBIN  items in index order (segment-major), CTA b takes items
+//                     b, b + grid, b + 2 grid, ...: a static round-robin
+//                     assignment, kept for measuring what LPT gains.
+constexpr int32_t PLAN_LPT = 0;
+constexpr int32_t PLAN_ROUND_ROBIN = 1;
 struct PlanHeader {
   int32_t ticket;
   int32_t n_items;
-  int32_t pad[14];  // keeps the item array 64-byte aligned
+  int32_t mode;
+  int32_t pad[13];  // keeps the item array 64-byte aligned
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header size");
 
@@ -83,6 +93,25 @@ struct MergeParams {
 __host__ __device__ inline bool is_delta(int v) { return v == HYPIC_GDN || v == HYPIC_DELTANET || v == HYPIC_CHANNEL_DELTA; }
 __host__ __device__ inline bool is_dense_T(int v) { return is_delta(v); }
 __host__ __device__ inline bool is_vector_gate(int v) { return v == HYPIC_CHANNEL_DELTA || v == HYPIC_DIAG_GATE; }
+
+// ---- build descriptors (host, no heap use; shared by every build entry
+// point so that they accept and plan exactly the same calls)
+// Shapes, segment offsets and the size limits of the descriptor.
+int check_build_shapes(const hypic_build_desc *d);
+// Input, gate and pool pointers (only those the call reads or writes).
+int check_build_pointers(const hypic_build_desc *d);
+// Slots in range and distinct; `sorted` is caller scratch of n_seg entries.
+int check_build_slots(const hypic_build_desc *d, int32_t *sorted);
+// Bytes of a plan of n_items items (header + items, not rounded).
+size_t build_plan_size(int64_t n_items);
+// Writes the plan of every (segment, value head) item of d into `plan`
+// (build_plan_size(n_seg * h_v) bytes): LPT order and mode, or index order
+// and PLAN_ROUND_ROBIN under HYPIC_FLAG_ROUND_ROBIN.  In-place sort, no heap.
+void fill_build_plan(const hypic_build_desc *d, void *plan);
+// Kernel parameters of a build descriptor; the plan pointer is left NULL.
+BuildParams build_params(const hypic_build_desc *d);
+// The kernel a build with these parameters runs (a hypic_path value).
+int build_path(const BuildParams &p, int64_t n_tokens);
 
 // Launchers (each returns a cudaError_t from the launch).
 // The build kernel for the parameters (tensor-core paths where they apply,

@@ -242,9 +242,16 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 // fp32 -> tf32 (low 13 bits zero) rounded to nearest, ties away from zero:
 // adding half a tf32 unit to the magnitude bits carries into the kept bits
 // (and into the exponent) exactly when the dropped part is at least half a
-// unit; two integer operations, full rate.  Infinities stay infinite; a NaN
-// stays non-finite.
-__device__ __forceinline__ uint32_t to_tf32(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
+// unit.  A finite value that rounds past the largest tf32 becomes an
+// infinity, and an infinity stays one.  A NaN must not take part in that
+// addition: its carry can run through the exponent into the sign bit (the
+// all-ones NaN 0x7FFFFFFF would become -0.0), so every NaN maps to the quiet
+// NaN 0x7FC00000, which tf32 holds exactly.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t r = (u + 0x1000u) & 0xFFFFE000u;
+  return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : r;
+}
 
 }  // namespace tc
 }  // namespace hypic

@@ -29,7 +29,11 @@
  * Conventions for every entry point:
  *   - Pointers marked [dev] are caller-owned device memory, [host] are host
  *     memory read during the call only.  The library allocates no device
- *     memory and keeps no global mutable state; calls are thread-safe.
+ *     memory.  Two entry points keep process-wide state and serialise their
+ *     host calls with a lock: hypic_segment_build_host (copy streams and
+ *     events per device, created on first use) and
+ *     hypic_segment_build_noalloc (a fixed device array); see each.  Every
+ *     other entry point keeps no global mutable state and is thread-safe.
  *   - Work is enqueued asynchronously on the caller's stream.  Host-side
  *     validation runs first: an invalid descriptor returns an error code and
  *     launches nothing.  A failed launch returns HYPIC_ERR_CUDA.
@@ -81,6 +85,32 @@ typedef enum {
 
 /* flags */
 #define HYPIC_FLAG_CHECK_FINITE 1u /* scan outputs for NaN/Inf and report through the status word */
+/* Build only, for measurement: hand the (segment, value head) items to the
+ * SMs round-robin in segment order (CTA b takes items b, b + grid, ...)
+ * instead of longest-first through the dynamic ticket.  The results are the
+ * same bit for bit; only the schedule, and so the makespan, changes (pages
+ * §2.3 compare LPT with round-robin). */
+#define HYPIC_FLAG_ROUND_ROBIN 2u
+/* Build, forward and compose: refuse (HYPIC_ERR_UNSUPPORTED, nothing
+ * launched) a call whose inputs would send it to an fp32 CUDA-core kernel
+ * instead of a tensor-core one, e.g. a 128-wide bf16 build whose k or v is
+ * not 16-byte aligned, or a compose with h_v not a multiple of 4.  A call
+ * with no tokens (build) or no segments (compose) has nothing to compute and
+ * is not refused.  The hypic_*_path queries below tell the path up front. */
+#define HYPIC_FLAG_REQUIRE_TENSOR_CORES 4u
+
+/* The kernel family a call runs, as returned by the hypic_*_path queries. */
+typedef enum {
+  HYPIC_PATH_NONE = 0,         /* nothing to launch (no segment, layer or merge) */
+  HYPIC_PATH_TC_CHUNKWISE = 1, /* build: tensor-core chunkwise, GDN / DeltaNet */
+  HYPIC_PATH_TC_CHANNEL = 2,   /* build: tensor-core chunkwise, per-channel gate */
+  HYPIC_PATH_TC_FAST = 3,      /* build: tensor-core fast path (scalar decay, ungated, diagonal) */
+  HYPIC_PATH_F32_TOKEN = 4,    /* build / forward outputs: fp32 token recurrence, CUDA cores */
+  HYPIC_PATH_TC_COMPOSE = 5,   /* compose: tensor cores (dense T, bf16 seam, d = 128) */
+  HYPIC_PATH_F32_COMPOSE = 6,  /* compose: fp32, CUDA cores */
+  HYPIC_PATH_TC_MERGE = 7,     /* merge: tensor cores, split tf32 */
+  HYPIC_PATH_F32_MERGE = 8     /* merge: fp32, CUDA cores */
+} hypic_path;
 
 /* Device status word bits (OR-ed by kernels; cleared by the caller). */
 #define HYPIC_STATUS_TIMEOUT   1u
@@ -205,13 +235,16 @@ int hypic_segment_build_host(const hypic_host_build_desc *d, hypic_stream_t stre
  * allocate device memory.  The pages have no counterpart: this is a
  * deployment variant of the same build, with the same results bit for bit.
  *
- * d->workspace and d->workspace_bytes are ignored.  The work plan goes to a
- * fixed device array of HYPIC_NOALLOC_SCRATCH_BYTES (1 MiB) inside the
- * library; its address is looked up once per device.  The call allocates no
- * device or heap memory (no cudaMalloc / cudaFree).
+ * d->workspace and d->workspace_bytes are ignored.  The work plan (a 64-byte
+ * header, then 32 bytes per (segment, value head) pair) goes to a fixed
+ * device array of HYPIC_NOALLOC_SCRATCH_BYTES (1 MiB) inside the library; its
+ * address is looked up once per device, by the first call on that device.
+ * The call allocates no device or heap memory (no cudaMalloc / cudaFree).
+ * It runs the same checks and the same plan as hypic_segment_build.
  *
- * Limit: n_seg * h_v <= HYPIC_NOALLOC_MAX_PAIRS; a larger problem returns
- * HYPIC_ERR_WORKSPACE before any CUDA call and launches nothing.
+ * Limit: n_seg * h_v <= HYPIC_NOALLOC_MAX_PAIRS (the plan then fills the
+ * array exactly); a larger problem returns HYPIC_ERR_WORKSPACE before any
+ * CUDA call and launches nothing.
  *
  * Every call in the process shares the one array.  Calls ordered on the GPU
  * (one stream, or ordered by events) are safe; calls that overlap on the GPU
@@ -220,7 +253,7 @@ int hypic_segment_build_host(const hypic_host_build_desc *d, hypic_stream_t stre
  * opens each call.
  */
 #define HYPIC_NOALLOC_SCRATCH_BYTES 1048576
-#define HYPIC_NOALLOC_MAX_PAIRS 16383
+#define HYPIC_NOALLOC_MAX_PAIRS 32766
 int hypic_segment_build_noalloc(const hypic_build_desc *d, hypic_stream_t stream);
 
 /*
@@ -360,6 +393,19 @@ int hypic_pair_rerotate(const hypic_rerotate_desc *d, hypic_stream_t stream);
  */
 int hypic_plan_lpt(const int64_t *costs, int32_t n_items, int32_t n_workers, int32_t *order_out,
                    int32_t *worker_out, int64_t *makespan_out);
+
+/*
+ * Path queries: the hypic_path the matching call would run for this
+ * descriptor (the same predicates the dispatch uses: variant, dtype, head
+ * sizes, h_v, pointer alignment), or minus a hypic_status when the shapes are
+ * invalid.  Host-only; nothing is read from device memory and nothing is
+ * launched.  hypic_forward_path reports the kernel of the per-token outputs
+ * (its pairs come from the hypic_build_path kernel).
+ */
+int hypic_build_path(const hypic_build_desc *d);
+int hypic_forward_path(const hypic_forward_desc *d);
+int hypic_compose_path(const hypic_compose_desc *d);
+int hypic_merge_path(const hypic_merge_desc *d);
 
 /* Decode a device status word into the first hypic_status it reports. */
 int hypic_status_from_word(uint32_t word);

@@ -90,3 +90,43 @@ def test_forward_gdn_layer_sampled():
         assert err <= tol_for(torch.bfloat16), (i, err)
     eT, eS = compare_pairs(W, T, S, *oracle_pairs(W, segs=[5]), [5])
     assert eT <= tol_for(torch.bfloat16) and eS <= tol_for(torch.bfloat16)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "scalar"])
+@pytest.mark.parametrize("gate", ["steep", "underflow"])
+def test_forward_steep_gates_token_by_token(variant, gate):
+    """Scalar gates keep the state as A * X with the scale folded into X
+    before A drops below 2^-64.  Log-gates around -20 per token fold at
+    nearly every token; a gate of -200 underflows e^g to 0 in fp32 and must
+    clear the state.  Every body token's output is checked on its own,
+    relative to the larger of its own norm and the head's RMS output norm, so
+    a slip at one token (e.g. just after a fold) fails.  DeltaNet has no gate
+    and must be unaffected."""
+    lens = [70, 200, 33, 129]
+    W = si.workload(2 if variant == "scalar" else 5, device=DEV, variant=variant, lengths=lens, h_k=2, h_v=4,
+                    seam_w=4)
+    L = W.layers[0]
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    if variant == "gdn":
+        g = -15.0 - 10.0 * torch.rand(L.g.shape, generator=gen)
+        if gate == "underflow":
+            g[50:60] = -200.0   # inside the first body, and a run of them
+            g[300:301] = -200.0
+        L.g.copy_(g.to(L.g.device))
+    elif variant == "scalar":
+        L.g.fill_(-200.0 if gate == "underflow" else -20.0)
+    T, S, o = _forward(W)
+    oc = o.cpu().double().numpy()
+    tol = tol_for(torch.bfloat16)
+    for i in range(W.n_seg):
+        s0, e, ref = _body_outputs_ref(W, i)
+        if ref is None:
+            continue
+        got = oc[s0:e]                                   # [tokens, h_v, d_v]
+        dn = np.linalg.norm(got - ref, axis=-1)           # [tokens, h_v]
+        rn = np.linalg.norm(ref, axis=-1)
+        rms = np.sqrt((rn ** 2).mean(axis=0, keepdims=True))
+        worst = (dn / np.maximum(rn, rms)).max()
+        assert np.isfinite(got).all() and worst <= tol, (i, worst)
+    eT, eS = compare_pairs(W, T, S, *oracle_pairs(W), range(W.n_seg))
+    assert eT <= tol and eS <= tol, (eT, eS)

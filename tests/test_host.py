@@ -259,3 +259,134 @@ def test_rerotate_rejects_bad_descriptors():
 def test_binding_refuses_host_tensors():
     with pytest.raises(ValueError):
         hy._ptr(torch.zeros(4))
+
+
+# ---- which kernel a call runs, and refusing the CUDA-core fallbacks
+
+def test_build_path_query_follows_dtype_shape_and_alignment():
+    """hypic_build_path names the kernel the build dispatch picks: the
+    tensor-core kernels for bf16 128-wide heads with 16-byte aligned inputs,
+    the fp32 token recurrence otherwise (and for a call with no tokens)."""
+    lib = hy.load()
+    off = np.asarray([0, 3, 8], dtype=np.int64)
+    po = off.ctypes.data_as(ctypes.c_void_p)
+    tc = dict(in_dtype=hy.IN_BF16, d_k=128, d_v=128)
+    cases = [
+        (dict(variant=hy.GDN, **tc), "tc_chunkwise"),
+        (dict(variant=hy.DELTANET, **tc), "tc_chunkwise"),
+        (dict(variant=hy.CHANNEL_DELTA, **tc), "tc_channel"),
+        (dict(variant=hy.SCALAR_DECAY, **tc), "tc_fast"),
+        (dict(variant=hy.UNGATED, **tc), "tc_fast"),
+        (dict(variant=hy.DIAG_GATE, **tc), "tc_fast"),
+        (dict(variant=hy.GDN, k=ctypes.c_void_p((1 << 20) + 2), **tc), "f32_token"),   # k not 16-byte aligned
+        (dict(variant=hy.GDN, v=ctypes.c_void_p((1 << 20) + 8), **tc), "f32_token"),
+        (dict(variant=hy.GDN, in_dtype=hy.IN_F32, d_k=128, d_v=128), "f32_token"),
+        (dict(variant=hy.GDN, in_dtype=hy.IN_BF16, d_k=64, d_v=128), "f32_token"),
+        (dict(variant=hy.GDN, n_tokens=0, seg_offsets=np.zeros(3, np.int64).ctypes.data_as(ctypes.c_void_p),
+              **tc), "f32_token"),
+        (dict(variant=hy.GDN, n_seg=0, **tc), "none"),
+    ]
+    for over, want in cases:
+        over.setdefault("seg_offsets", po)
+        if over.get("n_seg") == 0:
+            over["seg_offsets"] = np.zeros(1, np.int64).ctypes.data_as(ctypes.c_void_p)
+            over["n_tokens"] = 0
+        d = _fake_build_desc(**over)
+        assert hy.PATHS[lib.hypic_build_path(ctypes.byref(d))] == want, over
+    assert lib.hypic_build_path(ctypes.byref(_fake_build_desc(seg_offsets=po, d_k=129))) == -2
+    assert lib.hypic_build_path(ctypes.byref(_fake_build_desc(seg_offsets=po, h_v=3, h_k=2))) == -1
+
+
+def test_compose_and_merge_path_queries():
+    lib = hy.load()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def cdesc(**over):
+        d = hy.ComposeDesc()
+        d.n_layers, d.n_seg, d.h_k, d.h_v, d.d_k, d.d_v, d.seam_w = 1, 2, 2, 4, 128, 128, 8
+        d.variant, d.in_dtype = hy.GDN, hy.IN_BF16
+        d.slot = d.T_pool = d.S_pool = d.seam_k = d.seam_v = d.seam_q = d.seam_g = d.seam_beta = fake
+        d.S_out = d.seam_out = fake
+        d.n_slots = 2
+        for k, v in over.items():
+            setattr(d, k, v)
+        return d
+    assert hy.PATHS[lib.hypic_compose_path(ctypes.byref(cdesc()))] == "tc_compose"
+    assert hy.PATHS[lib.hypic_compose_path(ctypes.byref(cdesc(variant=hy.CHANNEL_DELTA)))] == "tc_compose"
+    for over in (dict(h_v=2, h_k=2), dict(in_dtype=hy.IN_F32), dict(d_k=64),
+                 dict(seam_k=ctypes.c_void_p((1 << 20) + 8)), dict(variant=hy.SCALAR_DECAY, seam_beta=None)):
+        assert hy.PATHS[lib.hypic_compose_path(ctypes.byref(cdesc(**over)))] == "f32_compose", over
+    assert hy.PATHS[lib.hypic_compose_path(ctypes.byref(cdesc(n_layers=0)))] == "none"
+    assert lib.hypic_compose_path(ctypes.byref(cdesc(S_out=None))) == -1
+
+    def mdesc(**over):
+        d = hy.MergeDesc()
+        d.n_merge, d.h_v, d.d_k, d.d_v, d.variant = 2, 4, 128, 128, hy.GDN
+        d.later = d.earlier = d.out = d.T_a = d.S_a = d.T_b = d.S_b = d.T_out = d.S_out = fake
+        d.n_slots_a, d.n_slots_b, d.n_slots_out = 4, 4, 2
+        for k, v in over.items():
+            setattr(d, k, v)
+        return d
+    assert hy.PATHS[lib.hypic_merge_path(ctypes.byref(mdesc()))] == "tc_merge"
+    assert hy.PATHS[lib.hypic_merge_path(ctypes.byref(mdesc(d_k=64)))] == "f32_merge"
+    assert hy.PATHS[lib.hypic_merge_path(ctypes.byref(mdesc(variant=hy.SCALAR_DECAY)))] == "f32_merge"
+    assert hy.PATHS[lib.hypic_merge_path(ctypes.byref(mdesc(T_a=ctypes.c_void_p((1 << 20) + 4))))] == "f32_merge"
+    assert hy.PATHS[lib.hypic_merge_path(ctypes.byref(mdesc(n_merge=0)))] == "none"
+
+
+def test_require_tensor_cores_refuses_fallbacks_before_any_cuda_call():
+    """With HYPIC_FLAG_REQUIRE_TENSOR_CORES a call that would fall back to an
+    fp32 CUDA-core kernel returns HYPIC_ERR_UNSUPPORTED and launches nothing
+    (so these fake pointers are never touched, with or without a GPU)."""
+    lib = hy.load()
+    off = np.asarray([0, 3, 8], dtype=np.int64)
+    po = off.ctypes.data_as(ctypes.c_void_p)
+    req = hy.FLAG_REQUIRE_TENSOR_CORES
+    for over in (dict(in_dtype=hy.IN_BF16, d_k=128, d_v=128, k=ctypes.c_void_p((1 << 20) + 2)),
+                 dict(in_dtype=hy.IN_F32, d_k=128, d_v=128), dict(in_dtype=hy.IN_BF16, d_k=32, d_v=32)):
+        d = _fake_build_desc(seg_offsets=po, flags=req, **over)
+        assert lib.hypic_segment_build(ctypes.byref(d), None) == 2, over
+        assert lib.hypic_segment_build_noalloc(ctypes.byref(d), None) == 2, over
+    # the forward's outputs run on the CUDA cores: refused under the flag
+    d = hy.ForwardDesc()
+    d.build = _fake_build_desc(seg_offsets=po, flags=req, in_dtype=hy.IN_BF16, d_k=128, d_v=128)
+    d.q = d.o_out = ctypes.c_void_p(1 << 20)
+    assert lib.hypic_segment_forward(ctypes.byref(d), None) == 2
+    fake = ctypes.c_void_p(1 << 20)
+    c = hy.ComposeDesc()
+    c.n_layers, c.n_seg, c.h_k, c.h_v, c.d_k, c.d_v, c.seam_w = 1, 2, 2, 2, 128, 128, 8
+    c.variant, c.in_dtype, c.flags = hy.GDN, hy.IN_BF16, req
+    c.slot = c.T_pool = c.S_pool = c.seam_k = c.seam_v = c.seam_q = c.seam_g = c.seam_beta = fake
+    c.S_out = c.seam_out = fake
+    c.n_slots = 2
+    assert lib.hypic_compose(ctypes.byref(c), None) == 2  # h_v = 2: not a multiple of 4
+    # unknown flag bits are refused
+    d = _fake_build_desc(seg_offsets=po, flags=64)
+    assert lib.hypic_segment_build(ctypes.byref(d), None) == 1
+    c.flags = hy.FLAG_ROUND_ROBIN   # a build-only flag
+    assert lib.hypic_compose(ctypes.byref(c), None) == 1
+
+
+def test_build_workspace_is_one_item_per_pair():
+    """64-byte plan header plus 32 bytes per (segment, value head), rounded
+    up to 256 bytes; the allocation-free entry point's limit fills its 1 MiB
+    array exactly."""
+    for n_seg, h_v in ((1, 1), (64, 32), (7, 3)):
+        nb = hy.build_workspace_bytes(n_seg, 1, h_v, 128, 128)
+        assert nb == (64 + 32 * n_seg * h_v + 255) // 256 * 256
+    assert 64 + 32 * hy.NOALLOC_MAX_PAIRS == 1 << 20
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake device pointers: only where no GPU can be reached")
+def test_noalloc_and_workspace_build_agree_on_a_no_token_call():
+    """A GDN descriptor with no tokens and no log-gate array is valid for
+    hypic_segment_build (the gates are never read); the allocation-free entry
+    point runs the same checks, so it must not refuse it either.  Without a
+    GPU both get as far as their first CUDA call and fail there alike."""
+    lib = hy.load()
+    off = np.zeros(3, np.int64)
+    d = _fake_build_desc(n_tokens=0, seg_offsets=off.ctypes.data_as(ctypes.c_void_p), g=None, beta=None, k=None,
+                         v=None)
+    a = lib.hypic_segment_build(ctypes.byref(d), None)
+    b = lib.hypic_segment_build_noalloc(ctypes.byref(d), None)
+    assert a == b == 4, (a, b)  # HYPIC_ERR_CUDA: validation passed on both

@@ -1,9 +1,11 @@
 """hypic_segment_build_noalloc: the build with its work plan in the library's
-fixed device scratch.  Two calls in a row through the C ABI, on different
-inputs, must each equal the workspace entry point's result bit for bit (the
-second call only can if the first left no stale plan or ticket behind); the
-tensor-core path at exactly the pair limit fills the scratch to its last
-byte; a larger problem is refused before any CUDA call.
+fixed device scratch, for callers that cannot allocate device memory.  Two
+calls in a row through the C ABI, on different inputs, must each equal the
+workspace entry point's result bit for bit (the second call only can if the
+first left no stale plan or ticket behind); at exactly the pair limit the
+plan (64-byte header, 32 bytes per (segment, value head)) fills the 1 MiB
+scratch to its last byte; a larger problem is refused before any CUDA call;
+a call that the workspace entry point accepts is accepted too.
 
 Collected last on purpose (file name), so it also runs after every other
 test in the same process."""
@@ -46,10 +48,10 @@ def _both(W, slots, n_slots):
 
 
 CASES = [
-    # tensor-core chunkwise path (two items per pair)
+    # tensor-core chunkwise path
     dict(cfg=5, variant="gdn", lengths=[1, 64, 65, 300, 129, 8, 9, 700], h_k=2, h_v=4, seam_w=8),
     dict(cfg=5, variant="deltanet", lengths=[200, 63, 1000, 16], h_k=1, h_v=2, seam_w=8),
-    # fp32 token path (one item per pair)
+    # fp32 token path
     dict(cfg=1, variant="channel", lengths=[50, 3, 90, 17, 64], h_k=1, h_v=2, seam_w=4, d=32),
 ]
 
@@ -93,6 +95,7 @@ def test_noalloc_at_the_pair_limit(_built):
     """n_seg * h_v == HYPIC_NOALLOC_MAX_PAIRS on the tensor-core path: the
     plan fills the whole fixed scratch; every slot must match the workspace
     build.  Short segments (0..70 body tokens) keep it quick."""
+    assert 64 + 32 * hy.NOALLOC_MAX_PAIRS == 1 << 20
     n = hy.NOALLOC_MAX_PAIRS
     lens = np.random.default_rng(5).integers(1, 79, size=n).tolist()
     W = si.workload(5, seed=3, device=DEV, variant="gdn", lengths=lens, h_k=1, h_v=1, seam_w=8)
@@ -102,7 +105,7 @@ def test_noalloc_at_the_pair_limit(_built):
     assert torch.equal(Tg, Tr) and torch.equal(Sg, Sr)
 
 
-@pytest.mark.parametrize("n_seg,h_v", [(hy.NOALLOC_MAX_PAIRS + 1, 1), (8192, 2)])
+@pytest.mark.parametrize("n_seg,h_v", [(hy.NOALLOC_MAX_PAIRS + 1, 1), (16384, 2)])
 def test_noalloc_refuses_problems_beyond_the_limit(_lib, n_seg, h_v):
     """Refused with HYPIC_ERR_WORKSPACE before any CUDA call (runs without a
     GPU too: no device pointer is read)."""
@@ -115,3 +118,18 @@ def test_noalloc_refuses_problems_beyond_the_limit(_lib, n_seg, h_v):
     d.n_slots = n_seg
     rc = lib.hypic_segment_build_noalloc(ctypes.byref(d), None)
     assert rc == 3, hy.status_string(rc)      # HYPIC_ERR_WORKSPACE
+
+
+@pytest.mark.gpu
+def test_noalloc_accepts_a_no_token_call_like_the_workspace_build(_built):
+    """GDN with no tokens and no log-gate array (never read): both entry
+    points accept it and write (I, 0) into every segment's slot."""
+    k = torch.zeros((0, 1, 128), dtype=torch.bfloat16, device=DEV)
+    v = torch.zeros((0, 2, 128), dtype=torch.bfloat16, device=DEV)
+    off = np.zeros(4, np.int64)
+    eye = torch.eye(128, device=DEV)
+    for fn in (hy.segment_build, hy.segment_build_noalloc):
+        T, S = new_pools("gdn", 3, 2, 128, 128, DEV)
+        fn(k, v, None, None, off, variant="gdn", seam_w=8, T_pool=T, S_pool=S)
+        torch.cuda.synchronize()
+        assert torch.equal(T, eye.expand_as(T)) and torch.equal(S, torch.zeros_like(S))
