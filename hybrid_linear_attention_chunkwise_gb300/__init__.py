@@ -33,6 +33,8 @@ IN_BF16, IN_F32 = 0, 1
 FLAG_CHECK_FINITE = 1
 FLAG_ROUND_ROBIN = 2            # build: static round-robin schedule (measurement)
 FLAG_REQUIRE_TENSOR_CORES = 4   # refuse calls that would run an fp32 CUDA-core kernel
+FLAG_TRANSITION_ONLY = 8        # compose: the product of the transitions alone
+SLOT_SKIP = -1                  # build: leave this segment out
 PATHS = ("none", "tc_chunkwise", "tc_channel", "tc_fast", "f32_token", "tc_compose", "f32_compose", "tc_merge",
          "f32_merge")
 STATUS_TIMEOUT, STATUS_NONFINITE, STATUS_BAD_SLOT = 1, 2, 4
@@ -60,6 +62,14 @@ class ComposeDesc(ctypes.Structure):
                 ("slot", P), ("n_slots", ctypes.c_int64), ("T_pool", P), ("S_pool", P),
                 ("seam_k", P), ("seam_v", P), ("seam_q", P), ("seam_g", P), ("seam_beta", P),
                 ("S_init", P), ("S_out", P), ("seam_out", P),
+                ("workspace", P), ("workspace_bytes", ctypes.c_size_t), ("status", P),
+                ("seg_stride", ctypes.c_int32)]
+
+
+class SpanScanDesc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_spans", ctypes.c_int32), ("h_v", ctypes.c_int32),
+                ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
+                ("T_span", P), ("S_span", P), ("S_init", P), ("S_start", P),
                 ("workspace", P), ("workspace_bytes", ctypes.c_size_t), ("status", P)]
 
 
@@ -95,6 +105,8 @@ SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_wo
            "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_pair_rerotate", "hypic_segment_forward",
            "hypic_segment_build_host",
            "hypic_build_path", "hypic_forward_path", "hypic_compose_path", "hypic_merge_path",
+           "hypic_span_scan", "hypic_span_scan_workspace_bytes", "hypic_compose_spans",
+           "hypic_compose_spans_workspace_bytes",
            "hypic_plan_lpt",
            "hypic_status_from_word", "hypic_status_string", "hypic_version")
 
@@ -139,6 +151,14 @@ def load():
                                ("hypic_compose_path", ComposeDesc), ("hypic_merge_path", MergeDesc)):
                 getattr(lib, name).argtypes = [ctypes.POINTER(desc)]
                 getattr(lib, name).restype = ctypes.c_int
+            lib.hypic_span_scan.argtypes = [ctypes.POINTER(SpanScanDesc), P]
+            lib.hypic_span_scan.restype = ctypes.c_int
+            lib.hypic_span_scan_workspace_bytes.argtypes = [ctypes.POINTER(SpanScanDesc)]
+            lib.hypic_span_scan_workspace_bytes.restype = ctypes.c_size_t
+            lib.hypic_compose_spans.argtypes = [ctypes.POINTER(ComposeDesc), ctypes.c_int32, P, P]
+            lib.hypic_compose_spans.restype = ctypes.c_int
+            lib.hypic_compose_spans_workspace_bytes.argtypes = [ctypes.POINTER(ComposeDesc), ctypes.c_int32]
+            lib.hypic_compose_spans_workspace_bytes.restype = ctypes.c_size_t
             lib.hypic_plan_lpt.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, P]
             lib.hypic_plan_lpt.restype = ctypes.c_int
             lib.hypic_status_from_word.argtypes = [ctypes.c_uint32]
@@ -351,7 +371,7 @@ def segment_build_noalloc(k, v, g, beta, seg_offsets, *, variant: str, seam_w: i
 
 
 def _compose_desc(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, variant, S_out, seam_out,
-                  S_init, h_k, status, flags):
+                  S_init, h_k, status, flags, span=None):
     _check(slot, "slot", dtype=torch.int32, ndim=2)
     _check(S_out, "S_out", dtype=torch.float32, ndim=4)
     for name, t in (("seam_k", seam_k), ("seam_v", seam_v), ("seam_q", seam_q)):
@@ -365,24 +385,42 @@ def _compose_desc(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_bet
     d.variant = VARIANT[variant]
     d.in_dtype = _in_dtype(seam_k) if seam_k is not None else IN_BF16
     d.flags = int(flags)
-    d.slot = _ptr(slot)
-    d.n_slots = S_pool.shape[0]
+    at = lambda t: _ptr(t)  # whole arrays
+    if span is not None:
+        # segments [a, b) of the per-layer arrays, composed in place: the
+        # pointers advance by a segments, the layer stride stays n_seg
+        a, b = int(span[0]), int(span[1])
+        if not 0 <= a <= b <= d.n_seg:
+            raise ValueError(f"span {span} outside 0..{d.n_seg}")
+        d.seg_stride, d.n_seg = d.n_seg, b - a
+
+        def at(t):
+            if t is None or t.dim() < 2 or t.shape[1] == 0 or a == t.shape[1]:
+                return _ptr(t)
+            return ctypes.c_void_p(t[:, a].data_ptr())
+    d.slot = at(slot)
+    d.n_slots = T_pool.shape[0]
     d.T_pool, d.S_pool = _ptr(T_pool), _ptr(S_pool)
-    d.seam_k, d.seam_v, d.seam_q = _ptr(seam_k), _ptr(seam_v), _ptr(seam_q)
-    d.seam_g, d.seam_beta = _ptr(seam_g), _ptr(seam_beta)
-    d.S_init, d.S_out, d.seam_out = _ptr(S_init), _ptr(S_out), _ptr(seam_out)
+    d.seam_k, d.seam_v, d.seam_q = at(seam_k), at(seam_v), at(seam_q)
+    d.seam_g = _ptr(seam_g) if (seam_g is not None and seam_g.dim() == 2) else at(seam_g)  # scalar decay: per layer
+    d.seam_beta = at(seam_beta)
+    d.S_init, d.S_out, d.seam_out = _ptr(S_init), _ptr(S_out), at(seam_out)
     d.status = _ptr(status)
     return d
 
 
 def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str,
             S_out, seam_out=None, S_init=None, h_k=None, d_k=None, d_v=None, status=None,
-            flags: int = 0, stream=None):
+            flags: int = 0, stream=None, span=None):
     """hypic_compose on torch tensors.  slot int32 [L, n_seg] (device);
-    seam arrays [L, n_seg, w, heads, d]; S_out [L, h_v, d_k, d_v]."""
+    seam arrays [L, n_seg, w, heads, d]; S_out [L, h_v, d_k, d_v].
+    span=(a, b) composes segments a .. b-1 of those arrays only, in place
+    (seam outputs of the other segments untouched).  With
+    flags=FLAG_TRANSITION_ONLY, S_pool may be None and S_init None stands
+    for the identity."""
     lib = load()
     d = _compose_desc(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, variant, S_out, seam_out,
-                      S_init, h_k, status, flags)
+                      S_init, h_k, status, flags, span)
     nb = int(lib.hypic_compose_workspace_bytes(ctypes.byref(d)))
     ws = alloc_workspace(nb, S_out.device) if nb else None
     d.workspace = _ptr(ws)
@@ -498,127 +536,51 @@ def pair_rerotate(slot_in, slot_out, delta, T_in, S_in, T_out, S_out, *, variant
         raise HypicError(rc, "hypic_pair_rerotate")
 
 
-def compose_span_parallel(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str,
-                          S_out, seam_out=None, S_init=None, n_spans: int = 2):
-    """compose() of every (layer, head) chain split into n_spans contiguous
-    spans of segments, by associativity of the composition rule (the
-    segment parallelism of nav.aitube.vip §2.3 applied to one chain):
+def span_scan(T_span, S_span, S_start, *, S_init=None, status=None, stream=None):
+    """hypic_span_scan on torch tensors: the start state of every span,
+    S_start[0] = S_init (or 0), S_start[s] = T_span[s-1] S_start[s-1] +
+    S_span[s-1].  T_span [n_spans, L, h_v, d_k, d_k], S_span / S_start
+    [n_spans, L, h_v, d_k, d_v], S_init [L, h_v, d_k, d_v] (device, fp32)."""
+    lib = load()
+    _check(S_start, "S_start", dtype=torch.float32, ndim=5)
+    d = SpanScanDesc()
+    d.n_spans, d.n_layers, d.h_v, d.d_k, d.d_v = S_start.shape
+    for name, t in (("T_span", T_span), ("S_span", S_span)):
+        _check(t, name, dtype=torch.float32, ndim=5)
+    d.T_span, d.S_span, d.S_init, d.S_start = _ptr(T_span), _ptr(S_span), _ptr(S_init), _ptr(S_start)
+    ws = alloc_workspace(int(lib.hypic_span_scan_workspace_bytes(ctypes.byref(d))), S_start.device)
+    d.workspace, d.workspace_bytes = _ptr(ws), ws.numel()
+    d.status = _ptr(status)
+    rc = lib.hypic_span_scan(ctypes.byref(d), _stream(stream))
+    if rc != OK:
+        raise HypicError(rc, "hypic_span_scan")
 
-      1. each segment's seam window is itself a short span: its pair is built
-         by segment_build over the seam tokens (seam_w = 0);
-      2. each span's pair is the merge, in prompt order, of its segments'
-         seam and cached pairs (pair_merge);
-      3. span s starts from S_s = T_{s-1} S_{s-1} + S(span s-1), S_0 = S_init
-         (an exclusive scan over the span pairs);
-      4. each span runs the ordinary compose from S_s, emitting its seam
-         outputs; the last span's final state is the chain's.
 
-    With one rank per span, steps 1, 2 and 4 need no exchange and step 3 is
-    an all-gather of one pair per (layer, head, span); here the spans run one
-    after another on this GPU.  Variants with per-token gates (all but
-    scalar decay, whose seam padding is not an identity token)."""
-    if variant == "scalar":
-        raise ValueError("compose_span_parallel: scalar decay is not supported")
-    L, n_seg = slot.shape
-    w = 0 if seam_k is None else seam_k.shape[2]
-    _, h_v, d_k, d_v = S_out.shape
-    h_k = seam_k.shape[3] if seam_k is not None else h_v
-    dev = S_out.device
-    n_spans = max(1, min(int(n_spans), n_seg))
-    bounds = np.linspace(0, n_seg, n_spans + 1).round().astype(np.int64)
-    slot_h = slot.detach().cpu().numpy()
-    i32 = lambda x: torch.as_tensor(np.asarray(x, dtype=np.int32), device=dev)
-    # 1. seam-window pairs, slot l * n_seg + i
-    T_sw = S_sw = None
-    if w > 0:
-        T_sw = torch.empty(pool_T_shape(variant, L * n_seg, h_v, d_k), device=dev)
-        S_sw = torch.empty((L * n_seg, h_v, d_k, d_v), device=dev)
-        offs = np.arange(0, n_seg * w + 1, w, dtype=np.int64)
-        for l in range(L):
-            kk = seam_k[l].reshape(n_seg * w, h_k, d_k)
-            vv = seam_v[l].reshape(n_seg * w, h_v, d_v)
-            gg = None if seam_g is None else seam_g[l].reshape((n_seg * w,) + tuple(seam_g.shape[3:]))
-            bb = None if seam_beta is None else seam_beta[l].reshape(n_seg * w, h_v)
-            segment_build(kk, vv, gg, bb, offs, variant=variant, seam_w=0, T_pool=T_sw, S_pool=S_sw,
-                          slot_of_seg=np.arange(n_seg, dtype=np.int32) + l * n_seg)
-    # 2. span pairs by sequential merges, batched over (layer, span); the
-    # accumulator ping-pongs between two pools, slot l * n_spans + s
-    n_acc = L * n_spans
-    acc_T = [torch.empty(pool_T_shape(variant, n_acc, h_v, d_k), device=dev) for _ in range(2)]
-    acc_S = [torch.empty((n_acc, h_v, d_k, d_v), device=dev) for _ in range(2)]
-    # elements of span s in order: (kind, segment) with kind 0 = seam, 1 = body
-    elems = [[(k, i) for i in range(bounds[s], bounds[s + 1]) for k in ((0, 1) if w > 0 else (1,))]
-             for s in range(n_spans)]
-    cur = 0
-    first = True
-    # a span of a single element: its pair is that element's
-    for l in range(L):
-        for s in range(n_spans):
-            if len(elems[s]) == 1:
-                k0, i0 = elems[s][0]
-                src_T, src_S = (T_sw, S_sw) if k0 == 0 else (T_pool, S_pool)
-                j = l * n_seg + i0 if k0 == 0 else int(slot_h[l, i0])
-                acc_T[cur][l * n_spans + s] = src_T[j]
-                acc_S[cur][l * n_spans + s] = src_S[j]
-    for step in range(max(len(e) for e in elems) - 1):
-        later, earlier, out, done = [], [], [], []
-        kinds = set()
-        for l in range(L):
-            for s in range(n_spans):
-                e = elems[s]
-                if step + 1 >= len(e):
-                    done.append(l * n_spans + s)  # finished: carried over below
-                    continue
-                kind, i = e[step + 1]
-                kinds.add(kind)
-                later.append(l * n_seg + i if kind == 0 else slot_h[l, i])
-                if first:
-                    k0, i0 = e[0]
-                    earlier.append(l * n_seg + i0 if k0 == 0 else slot_h[l, i0])
-                else:
-                    earlier.append(l * n_spans + s)
-                out.append(l * n_spans + s)
-        assert len(kinds) == 1  # every span steps through seam, body, seam, ... in lockstep
-        kind = kinds.pop()
-        Ta, Sa = (T_sw, S_sw) if kind == 0 else (T_pool, S_pool)
-        if first:
-            k0 = elems[0][0][0]
-            Tb, Sb = (T_sw, S_sw) if k0 == 0 else (T_pool, S_pool)
-        else:
-            Tb, Sb = acc_T[cur], acc_S[cur]
-        pair_merge(i32(later), i32(earlier), i32(out), Ta, Sa, acc_T[cur ^ 1], acc_S[cur ^ 1], variant=variant,
-                   T_b=Tb, S_b=Sb)
-        if done:  # spans that are complete keep their pair in the new buffer
-            idx = torch.as_tensor(done, device=dev)
-            acc_T[cur ^ 1][idx] = acc_T[cur][idx]
-            acc_S[cur ^ 1][idx] = acc_S[cur][idx]
-        cur ^= 1
-        first = False
-    span_T, span_S = acc_T[cur], acc_S[cur]
-    # 3. exclusive scan: S_s = T_{s-1} S_{s-1} + S(span s-1), as merges whose
-    # earlier operand is the state (its T half unused)
-    state = torch.zeros((L * n_spans, h_v, d_k, d_v), device=dev) if S_init is None else \
-        S_init.repeat_interleave(n_spans, dim=0).contiguous()
-    state_T = torch.zeros(pool_T_shape(variant, L * n_spans, h_v, d_k), device=dev)
-    scratch_T = torch.empty_like(state_T)
-    for s in range(1, n_spans):
-        later = [l * n_spans + s - 1 for l in range(L)]
-        earlier = later
-        out = [l * n_spans + s for l in range(L)]
-        pair_merge(i32(later), i32(earlier), i32(out), span_T, span_S, scratch_T, state, variant=variant,
-                   T_b=state_T, S_b=state)
-    # 4. each span's compose from its start state
-    for s in range(n_spans):
-        a, b = int(bounds[s]), int(bounds[s + 1])
-        sl = lambda x: None if x is None else x[:, a:b].contiguous()
-        so = None if seam_out is None else torch.empty_like(seam_out[:, a:b])
-        Si = state.reshape(L, n_spans, h_v, d_k, d_v)[:, s].contiguous()
-        Sf = S_out if s == n_spans - 1 else torch.empty_like(S_out)
-        sg = seam_g if (seam_g is not None and variant == "scalar") else sl(seam_g)
-        compose(slot[:, a:b].contiguous(), T_pool, S_pool, sl(seam_k), sl(seam_v), sl(seam_q), sg, sl(seam_beta),
-                variant=variant, S_out=Sf, seam_out=so, S_init=Si, h_k=h_k, d_k=d_k, d_v=d_v)
-        if so is not None:
-            seam_out[:, a:b] = so
+def span_bounds(n_seg: int, n_spans: int):
+    """Segment boundaries of n_spans consecutive spans of about equal segment
+    counts (every segment costs its seam window plus one pair)."""
+    n_spans = max(1, min(int(n_spans), max(int(n_seg), 1)))
+    return np.linspace(0, n_seg, n_spans + 1).round().astype(np.int32)
+
+
+def compose_spans(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str, S_out,
+                  seam_out=None, S_init=None, n_spans: int = 2, bounds=None, h_k=None, status=None, flags: int = 0,
+                  stream=None):
+    """hypic_compose_spans on torch tensors: compose() computed by segment
+    parallelism (nav.aitube.vip §2.3) with the chains split into n_spans
+    consecutive spans of segments (or at `bounds`): the span pairs, their
+    exclusive scan, then every span from its start state.  Same arguments
+    and results as compose()."""
+    lib = load()
+    d = _compose_desc(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, variant, S_out, seam_out,
+                      S_init, h_k, status, flags)
+    b = span_bounds(d.n_seg, n_spans) if bounds is None else np.ascontiguousarray(np.asarray(bounds, np.int32))
+    ns = len(b) - 1
+    ws = alloc_workspace(int(lib.hypic_compose_spans_workspace_bytes(ctypes.byref(d), ns)), S_out.device)
+    d.workspace, d.workspace_bytes = _ptr(ws), ws.numel()
+    rc = lib.hypic_compose_spans(ctypes.byref(d), ns, b.ctypes.data_as(P), _stream(stream))
+    if rc != OK:
+        raise HypicError(rc, "hypic_compose_spans")
 
 
 def plan_lpt(costs, n_workers: int):

@@ -134,6 +134,7 @@ int check_build_slots(const hypic_build_desc *d, int32_t *sorted) {
   for (int i = 0; i < d->n_seg; i++) sorted[i] = d->slot_of_seg ? d->slot_of_seg[i] : i;
   std::sort(sorted, sorted + d->n_seg);
   for (int i = 0; i < d->n_seg; i++) {
+    if (sorted[i] == HYPIC_SLOT_SKIP) continue;  // segment not built
     if (sorted[i] < 0 || sorted[i] >= d->n_slots) return HYPIC_ERR_INVALID_ARG;
     if (i && sorted[i] == sorted[i - 1]) return HYPIC_ERR_INVALID_ARG;  // two items writing one slot would race
   }
@@ -142,11 +143,9 @@ int check_build_slots(const hypic_build_desc *d, int32_t *sorted) {
 
 size_t build_plan_size(int64_t n_items) { return sizeof(PlanHeader) + (size_t)n_items * sizeof(BuildItem); }
 
-void fill_build_plan(const hypic_build_desc *d, void *plan) {
-  const int64_t n_items = n_build_items(d);
+int64_t fill_build_plan(const hypic_build_desc *d, void *plan) {
   PlanHeader *hdr = static_cast<PlanHeader *>(plan);
   std::memset(hdr, 0, sizeof(PlanHeader));
-  hdr->n_items = (int32_t)n_items;
   const bool rr = (d->flags & HYPIC_FLAG_ROUND_ROBIN) != 0;
   hdr->mode = rr ? PLAN_ROUND_ROBIN : PLAN_LPT;
   BuildItem *items = reinterpret_cast<BuildItem *>(hdr + 1);
@@ -155,6 +154,7 @@ void fill_build_plan(const hypic_build_desc *d, void *plan) {
     BuildItem b;
     b.seg = i;
     b.slot = d->slot_of_seg ? d->slot_of_seg[i] : i;
+    if (b.slot == HYPIC_SLOT_SKIP) continue;
     b.part = 0;
     b.start = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
     b.end = d->seg_offsets[i + 1];
@@ -163,7 +163,9 @@ void fill_build_plan(const hypic_build_desc *d, void *plan) {
       items[r++] = b;
     }
   }
-  if (rr) return;  // index order: segment-major, head-minor
+  const int64_t n_items = r;
+  hdr->n_items = (int32_t)n_items;
+  if (rr) return n_items;  // index order: segment-major, head-minor
   // LPT: longest body first; ties in index order (a total order, so the
   // in-place sort is deterministic)
   std::sort(items, items + n_items, [](const BuildItem &a, const BuildItem &b) {
@@ -172,6 +174,7 @@ void fill_build_plan(const hypic_build_desc *d, void *plan) {
     if (a.seg != b.seg) return a.seg < b.seg;
     return a.head < b.head;
   });
+  return n_items;
 }
 
 BuildParams build_params(const hypic_build_desc *d) {
@@ -291,12 +294,13 @@ int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_str
   p.plan = reinterpret_cast<PlanHeader *>(d->workspace);
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
 
-  // one item per (segment, value head) on every kernel (see launch_build)
-  const int64_t n_items = n_build_items(d);
-  const size_t need = round_up(build_plan_size(n_items), kAlign);
+  // one item per (segment, value head) on every kernel (see launch_build);
+  // skipped segments have none
+  const size_t need = round_up(build_plan_size(n_build_items(d)), kAlign);
   if (!d->workspace || d->workspace_bytes < need || !aligned(d->workspace, kAlign)) return HYPIC_ERR_WORKSPACE;
   std::vector<unsigned char> host(need, 0);
-  fill_build_plan(d, host.data());
+  const int64_t n_items = fill_build_plan(d, host.data());
+  if (n_items == 0) return HYPIC_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // pageable source: the call returns once the bytes are staged, so `host`
   // may be released when it goes out of scope
@@ -323,18 +327,22 @@ int check_compose(const hypic_compose_desc *d) {
   int st = check_common_shapes(d->h_k, d->h_v, d->d_k, d->d_v, d->seam_w, d->variant, d->in_dtype);
   if (st) return st;
   if (d->n_layers < 0 || d->n_seg < 0 || d->n_slots < 0) return HYPIC_ERR_INVALID_ARG;
-  if (d->flags & ~(HYPIC_FLAG_CHECK_FINITE | HYPIC_FLAG_REQUIRE_TENSOR_CORES)) return HYPIC_ERR_INVALID_ARG;
+  if (d->seg_stride != 0 && d->seg_stride < d->n_seg) return HYPIC_ERR_INVALID_ARG;
+  if (d->flags & ~(HYPIC_FLAG_CHECK_FINITE | HYPIC_FLAG_REQUIRE_TENSOR_CORES | HYPIC_FLAG_TRANSITION_ONLY))
+    return HYPIC_ERR_INVALID_ARG;
+  const bool trans = (d->flags & HYPIC_FLAG_TRANSITION_ONLY) != 0;
+  if (trans && d->d_v != d->d_k) return HYPIC_ERR_INVALID_ARG;  // the state is a transition
   if (d->n_layers == 0) return HYPIC_OK;
   if (!d->S_out || !aligned(d->S_out, 4)) return HYPIC_ERR_INVALID_ARG;
   if (d->S_init && !aligned(d->S_init, 4)) return HYPIC_ERR_INVALID_ARG;
   if (d->n_seg > 0) {
-    if (!d->slot || !aligned(d->slot, 4) || !d->T_pool || !d->S_pool) return HYPIC_ERR_INVALID_ARG;
+    if (!d->slot || !aligned(d->slot, 4) || !d->T_pool || (!d->S_pool && !trans)) return HYPIC_ERR_INVALID_ARG;
     if (!aligned(d->T_pool, 4) || !aligned(d->S_pool, 4)) return HYPIC_ERR_INVALID_ARG;
   }
   const bool delta = is_delta(d->variant);
   const int esz = in_size(d->in_dtype);
   if (d->seam_w > 0 && d->n_seg > 0) {
-    if (!d->seam_k || !d->seam_v || !d->seam_q || !d->seam_out) return HYPIC_ERR_INVALID_ARG;
+    if (!d->seam_k || !d->seam_v || !d->seam_q || (!d->seam_out && !trans)) return HYPIC_ERR_INVALID_ARG;
     if (!aligned(d->seam_k, esz) || !aligned(d->seam_v, esz) || !aligned(d->seam_q, esz)) return HYPIC_ERR_INVALID_ARG;
     if (!aligned(d->seam_out, 4)) return HYPIC_ERR_INVALID_ARG;
     if (delta && !d->seam_beta) return HYPIC_ERR_INVALID_ARG;
@@ -353,6 +361,7 @@ ComposeParams compose_params(const hypic_compose_desc *d) {
   p.d_k = d->d_k;
   p.d_v = d->d_v;
   p.seam_w = d->seam_w;
+  p.seg_stride = d->seg_stride ? d->seg_stride : d->n_seg;
   p.variant = d->variant;
   p.in_dtype = d->in_dtype;
   p.flags = d->flags;
@@ -385,6 +394,64 @@ int check_merge(const hypic_merge_desc *d) {
   const float *pools[6] = {d->T_a, d->S_a, d->T_b, d->S_b, d->T_out, d->S_out};
   for (const float *q : pools)
     if (!q || !aligned(q, 4)) return HYPIC_ERR_INVALID_ARG;
+  return HYPIC_OK;
+}
+
+// One compose launch: tensor cores where they apply, else the fp32 kernel.
+// Transition-only with no S_init starts from the identity, written into
+// S_out first (the kernels allow S_out to alias S_init).
+int compose_launch(ComposeParams p, hypic_stream_t stream) {
+  const int path = compose_tc_supported(p) ? HYPIC_PATH_TC_COMPOSE : HYPIC_PATH_F32_COMPOSE;
+  if (refused_fallback(p.flags, path, p.n_seg)) return HYPIC_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((p.flags & HYPIC_FLAG_TRANSITION_ONLY) && !p.S_init) {
+    if (launch_fill_identity(p.S_out, (int64_t)p.n_layers * p.h_v, p.d_k, s) != cudaSuccess) return HYPIC_ERR_CUDA;
+    p.S_init = p.S_out;
+  }
+  const cudaError_t e = path == HYPIC_PATH_TC_COMPOSE ? launch_compose_tc(p, wait_limit(), s) : launch_compose_simt(p, s);
+  return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
+}
+
+// S_start[0] = S_init (or 0); S_start[s] = T_span[s-1] S_start[s-1] +
+// S_span[s-1], one single-pair compose per step (no seam tokens).  `slots`
+// is device scratch of n_layers int32.
+int span_scan_impl(int L, int n_spans, int H, int dk, int dv, const float *T_span, const float *S_span,
+                   const float *S_init, float *S_start, int32_t *slots, uint32_t *status, hypic_stream_t stream) {
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t T_per = (size_t)L * H * dk * dk, S_per = (size_t)L * H * dk * dv;
+  if (S_init) {
+    if (cudaMemcpyAsync(S_start, S_init, S_per * 4, cudaMemcpyDeviceToDevice, cs) != cudaSuccess) return HYPIC_ERR_CUDA;
+  } else if (cudaMemsetAsync(S_start, 0, S_per * 4, cs) != cudaSuccess) {
+    return HYPIC_ERR_CUDA;
+  }
+  if (n_spans < 2) return HYPIC_OK;
+  std::vector<int32_t> idx(L);
+  std::iota(idx.begin(), idx.end(), 0);
+  // pageable source: the copy is staged before the call returns
+  if (cudaMemcpyAsync(slots, idx.data(), (size_t)L * 4, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return HYPIC_ERR_CUDA;
+  for (int s = 1; s < n_spans; s++) {
+    ComposeParams p{};
+    p.n_layers = L;
+    p.n_seg = 1;
+    p.seg_stride = 1;
+    p.h_k = H;
+    p.h_v = H;
+    p.d_k = dk;
+    p.d_v = dv;
+    p.seam_w = 0;
+    p.variant = HYPIC_DELTANET;  // a dense transition, no seam token
+    p.in_dtype = HYPIC_IN_BF16;
+    p.slot = slots;
+    p.n_slots = L;
+    p.T_pool = T_span + (s - 1) * T_per;
+    p.S_pool = S_span + (s - 1) * S_per;
+    p.S_init = S_start + (s - 1) * S_per;
+    p.S_out = S_start + s * S_per;
+    p.status = status;
+    const int st = compose_launch(p, stream);
+    if (st) return st;
+  }
   return HYPIC_OK;
 }
 
@@ -535,6 +602,10 @@ int hypic_segment_build_host(const hypic_host_build_desc *d, hypic_stream_t stre
       return HYPIC_ERR_CUDA;
     // its slots out, runs of consecutive slots as one copy
     for (int i = a; i < e;) {
+      if (slots[i] == HYPIC_SLOT_SKIP) {
+        i++;
+        continue;
+      }
       int j = i + 1;
       while (j < e && slots[j] == slots[j - 1] + 1) j++;
       const size_t s0 = (size_t)slots[i], n = (size_t)(j - i);
@@ -569,15 +640,108 @@ size_t hypic_compose_workspace_bytes(const hypic_compose_desc *d) {
 int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream) {
   int st = check_compose(d);
   if (st || d->n_layers == 0) return st;
-  const ComposeParams p = compose_params(d);
-  // Dense transitions with bf16 seam tokens and 128-wide heads stream the
-  // pool through the tensor cores; fp32 inputs (1e-5 bar), smaller heads and
-  // scalar/diagonal transitions run the fp32 kernel.
-  const int path = compose_tc_supported(p) ? HYPIC_PATH_TC_COMPOSE : HYPIC_PATH_F32_COMPOSE;
-  if (refused_fallback(d->flags, path, d->n_seg)) return HYPIC_ERR_UNSUPPORTED;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = path == HYPIC_PATH_TC_COMPOSE ? launch_compose_tc(p, wait_limit(), s) : launch_compose_simt(p, s);
-  if (e != cudaSuccess) return HYPIC_ERR_CUDA;
+  return compose_launch(compose_params(d), stream);
+}
+
+size_t hypic_span_scan_workspace_bytes(const hypic_span_scan_desc *d) {
+  if (!d) return 0;
+  if (d->n_layers < 1 || d->n_spans < 1) return 0;
+  return round_up((size_t)d->n_layers * 4, kAlign);
+}
+
+int hypic_span_scan(const hypic_span_scan_desc *d, hypic_stream_t stream) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_layers < 0 || d->n_spans < 0 || d->h_v < 1 || d->d_k < 1 || d->d_v < 1) return HYPIC_ERR_INVALID_ARG;
+  if (d->d_k > 128 || d->d_v > 128) return HYPIC_ERR_UNSUPPORTED;
+  if (d->n_layers == 0 || d->n_spans == 0) return HYPIC_OK;
+  if (!d->S_start || !aligned(d->S_start, 4) || (d->S_init && !aligned(d->S_init, 4))) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_spans > 1 && (!d->T_span || !d->S_span || !aligned(d->T_span, 4) || !aligned(d->S_span, 4)))
+    return HYPIC_ERR_INVALID_ARG;
+  const size_t need = hypic_span_scan_workspace_bytes(d);
+  if (!d->workspace || d->workspace_bytes < need || !aligned(d->workspace, kAlign)) return HYPIC_ERR_WORKSPACE;
+  return span_scan_impl(d->n_layers, d->n_spans, d->h_v, d->d_k, d->d_v, d->T_span, d->S_span, d->S_init, d->S_start,
+                        static_cast<int32_t *>(d->workspace), d->status, stream);
+}
+
+size_t hypic_compose_spans_workspace_bytes(const hypic_compose_desc *d, int32_t n_spans) {
+  if (!d || d->n_layers < 1 || n_spans < 1 || d->h_v < 1 || d->d_k < 1 || d->d_v < 1) return 0;
+  const size_t mat = (size_t)n_spans * d->n_layers * d->h_v;
+  return round_up(mat * d->d_k * d->d_k * 4, kAlign) + 2 * round_up(mat * d->d_k * d->d_v * 4, kAlign) +
+         round_up((size_t)d->n_layers * 4, kAlign);
+}
+
+int hypic_compose_spans(const hypic_compose_desc *d, int32_t n_spans, const int32_t *span_bounds,
+                        hypic_stream_t stream) {
+  int st = check_compose(d);
+  if (st) return st;
+  if (d->flags & HYPIC_FLAG_TRANSITION_ONLY) return HYPIC_ERR_INVALID_ARG;
+  if (n_spans < 1 || !span_bounds || span_bounds[0] != 0 || span_bounds[n_spans] != d->n_seg)
+    return HYPIC_ERR_INVALID_ARG;
+  for (int s = 0; s < n_spans; s++)
+    if (span_bounds[s + 1] < span_bounds[s]) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_layers == 0) return HYPIC_OK;
+  const size_t need = hypic_compose_spans_workspace_bytes(d, n_spans);
+  if (!d->workspace || d->workspace_bytes < need || !aligned(d->workspace, kAlign)) return HYPIC_ERR_WORKSPACE;
+  const int L = d->n_layers, H = d->h_v, dk = d->d_k, dv = d->d_v;
+  const size_t mat = (size_t)n_spans * L * H;
+  char *ws = static_cast<char *>(d->workspace);
+  float *T_span = reinterpret_cast<float *>(ws);
+  ws += round_up(mat * dk * dk * 4, kAlign);
+  float *S_span = reinterpret_cast<float *>(ws);
+  ws += round_up(mat * dk * dv * 4, kAlign);
+  float *S_start = reinterpret_cast<float *>(ws);
+  ws += round_up(mat * dk * dv * 4, kAlign);
+  int32_t *scan_slots = reinterpret_cast<int32_t *>(ws);
+  const size_t T_per = (size_t)L * H * dk * dk, S_per = (size_t)L * H * dk * dv;  // one span, every layer
+  const ComposeParams base = compose_params(d);
+  const int esz = in_size(d->in_dtype);
+  const bool vec = is_vector_gate(d->variant);
+  const size_t w = (size_t)d->seam_w;
+  // span s of every chain: the arrays advanced by a segments, n_seg = b - a,
+  // the layer stride kept
+  auto span_params = [&](int s) {
+    ComposeParams p = base;
+    const size_t a = (size_t)span_bounds[s];
+    p.n_seg = span_bounds[s + 1] - span_bounds[s];
+    p.slot = d->slot ? d->slot + a : nullptr;
+    auto adv = [&](const void *x, size_t per_seg) {
+      return x ? static_cast<const void *>(static_cast<const char *>(x) + a * per_seg) : nullptr;
+    };
+    p.seam_k = adv(d->seam_k, w * d->h_k * d->d_k * esz);
+    p.seam_v = adv(d->seam_v, w * d->h_v * d->d_v * esz);
+    p.seam_q = adv(d->seam_q, w * d->h_k * d->d_k * esz);
+    if (d->variant != HYPIC_SCALAR_DECAY)  // per-token gates (a scalar decay is per layer)
+      p.seam_g = static_cast<const float *>(adv(d->seam_g, w * d->h_v * (vec ? d->d_k : 1) * 4));
+    p.seam_beta = static_cast<const float *>(adv(d->seam_beta, w * d->h_v * 4));
+    p.seam_out = d->seam_out ? d->seam_out + a * w * d->h_v * d->d_v : nullptr;
+    return p;
+  };
+  // 1. the pair of every span but the last (nothing follows it): S from
+  // zero (its seam outputs are overwritten in step 3), T from the identity
+  for (int s = 0; s + 1 < n_spans; s++) {
+    ComposeParams p = span_params(s);
+    p.S_init = nullptr;
+    p.S_out = S_span + s * S_per;
+    if ((st = compose_launch(p, stream))) return st;
+    ComposeParams t = span_params(s);
+    t.flags |= HYPIC_FLAG_TRANSITION_ONLY;
+    t.d_v = dk;
+    t.S_init = nullptr;  // the identity
+    t.S_out = T_span + s * T_per;
+    t.seam_out = nullptr;
+    if ((st = compose_launch(t, stream))) return st;
+  }
+  // 2. the exclusive scan over the spans
+  if ((st = span_scan_impl(L, n_spans, H, dk, dv, T_span, S_span, d->S_init, S_start, scan_slots, d->status, stream)))
+    return st;
+  // 3. every span from its start state, with its seam outputs; the last
+  // span's final state is the chain's
+  for (int s = 0; s < n_spans; s++) {
+    ComposeParams p = span_params(s);
+    p.S_init = S_start + s * S_per;
+    p.S_out = s + 1 == n_spans ? d->S_out : S_span + s * S_per;  // earlier spans' final states: scratch
+    if ((st = compose_launch(p, stream))) return st;
+  }
   return HYPIC_OK;
 }
 

@@ -84,9 +84,10 @@ int hypic_segment_build_noalloc(const hypic_build_desc *d, hypic_stream_t stream
   if ((st = scratch_ptr(&scratch))) return st;
   p.plan = reinterpret_cast<PlanHeader *>(scratch);
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
-  const int64_t n_items = (int64_t)d->n_seg * d->h_v;  // one item per (segment, value head)
+  // one item per (segment, value head); the ticket starts at zero
+  const int64_t n_items = fill_build_plan(d, h_plan);
+  if (n_items == 0) return HYPIC_OK;
   const size_t bytes = build_plan_size(n_items);
-  fill_build_plan(d, h_plan);  // the ticket starts at zero
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // pageable source: the call returns once the bytes are staged, so the

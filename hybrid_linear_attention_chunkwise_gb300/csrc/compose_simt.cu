@@ -13,6 +13,8 @@
 //         and diagonal T_C scale S in place.
 // Every product is an fp32 FMA chain (no tensor cores): this path exists for
 // fp32 inputs, where the 1e-5 bar leaves no room for tf32/bf16 operands.
+#include <algorithm>
+
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -44,6 +46,7 @@ __global__ void __launch_bounds__(128) compose_simt_kernel(ComposeParams p) {
   const bool act = n < d_v;
   const bool delta = is_delta(p.variant), vec = is_vector_gate(p.variant);
   const int64_t state = (int64_t)chain * d_k * d_v;
+  const bool trans = (p.flags & HYPIC_FLAG_TRANSITION_ONLY) != 0;  // U_t and S(C|0) count as zero
 
   float S[DK];
 #pragma unroll
@@ -51,7 +54,7 @@ __global__ void __launch_bounds__(128) compose_simt_kernel(ComposeParams p) {
 
   bool bad = false;
   for (int seg = 0; seg < p.n_seg; seg++) {
-    const int64_t tok0 = ((int64_t)l * p.n_seg + seg) * w;
+    const int64_t tok0 = ((int64_t)l * p.seg_stride + seg) * w;
     // ---- seam tokens ----
     for (int s0 = 0; s0 < w; s0 += SB) {
       const int nt = min(SB, w - s0);
@@ -72,7 +75,10 @@ __global__ void __launch_bounds__(128) compose_simt_kernel(ComposeParams p) {
       }
       for (int e = n; e < SB * 128; e += blockDim.x) {
         const int t = e / 128, j = e % 128;
-        sm.v[t][j] = (t < nt && j < d_v) ? load_in(p.seam_v, ((tok0 + s0 + t) * p.h_v + h) * (int64_t)d_v + j, p.in_dtype) : 0.f;
+        // transition-only: v is not read (d_v is then d_k, not the v rows' width)
+        sm.v[t][j] = (t < nt && j < d_v && !trans)
+                         ? load_in(p.seam_v, ((tok0 + s0 + t) * p.h_v + h) * (int64_t)d_v + j, p.in_dtype)
+                         : 0.f;
       }
       for (int t = n; t < SB; t += blockDim.x) {
         float gs = 1.f, b = 0.f;
@@ -87,7 +93,7 @@ __global__ void __launch_bounds__(128) compose_simt_kernel(ComposeParams p) {
       }
       __syncthreads();
       for (int t = 0; t < nt; t++) {
-        const float vj = act ? sm.v[t][n] : 0.f;
+        const float vj = act && !trans ? sm.v[t][n] : 0.f;  // transition-only: no write
         const float gs = sm.gs[t], b = sm.b[t];
         if (delta) {
           const float *kd = vec ? sm.kd[t] : sm.k[t];
@@ -123,7 +129,7 @@ __global__ void __launch_bounds__(128) compose_simt_kernel(ComposeParams p) {
           o2 = fmaf(sm.q[t][i + 2], S[i + 2], o2);
           o3 = fmaf(sm.q[t][i + 3], S[i + 3], o3);
         }
-        if (act) {
+        if (act && !trans) {
           const float o = (o0 + o1) + (o2 + o3);
           p.seam_out[((tok0 + s0 + t) * p.h_v + h) * (int64_t)d_v + n] = o;
           bad |= !finite_f(o);
@@ -131,13 +137,13 @@ __global__ void __launch_bounds__(128) compose_simt_kernel(ComposeParams p) {
       }
     }
     // ---- cached pair ----
-    const int slot = p.slot[(int64_t)l * p.n_seg + seg];
+    const int slot = p.slot[(int64_t)l * p.seg_stride + seg];
     if (slot < 0 || slot >= p.n_slots) {
       if (n == 0) report(p.status, HYPIC_STATUS_BAD_SLOT);
       continue;  // uniform across the block: the chain skips this pair
     }
     const int64_t sh = (int64_t)slot * p.h_v + h;
-    const float *Sc = p.S_pool + sh * d_k * d_v;
+    const float *Sc = trans ? nullptr : p.S_pool + sh * d_k * d_v;
     if (delta) {
       __syncthreads();
       const float *Tc = p.T_pool + sh * d_k * d_k;
@@ -169,19 +175,19 @@ __global__ void __launch_bounds__(128) compose_simt_kernel(ComposeParams p) {
       }
 #pragma unroll
       for (int r = 0; r < DK; r++) {
-        const float sc = (act && r < d_k) ? Sc[(int64_t)r * d_v + n] : 0.f;
+        const float sc = (act && r < d_k && !trans) ? Sc[(int64_t)r * d_v + n] : 0.f;
         S[r] = sm.S[r][n] + sc;
       }
     } else if (vec) {
       const float *Tc = p.T_pool + sh * d_k;
 #pragma unroll
       for (int i = 0; i < DK; i++)
-        if (i < d_k && act) S[i] = fmaf(Tc[i], S[i], Sc[(int64_t)i * d_v + n]);
+        if (i < d_k && act) S[i] = fmaf(Tc[i], S[i], trans ? 0.f : Sc[(int64_t)i * d_v + n]);
     } else {
       const float tc = p.T_pool[sh];
 #pragma unroll
       for (int i = 0; i < DK; i++)
-        if (i < d_k && act) S[i] = fmaf(tc, S[i], Sc[(int64_t)i * d_v + n]);
+        if (i < d_k && act) S[i] = fmaf(tc, S[i], trans ? 0.f : Sc[(int64_t)i * d_v + n]);
     }
   }
   if (act) {
@@ -206,7 +212,23 @@ cudaError_t launch_dk(const ComposeParams &p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+__global__ void fill_identity_kernel(float *out, int64_t n_mats, int d) {
+  const int64_t total = n_mats * d * d;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = (e / d) % d, c = e % d;
+    out[e] = r == c ? 1.f : 0.f;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fill_identity(float *out, int64_t n_mats, int d, cudaStream_t s) {
+  if (n_mats < 1) return cudaSuccess;
+  const int64_t total = n_mats * d * d;
+  const int grid = (int)std::min<int64_t>((total + 255) / 256, 4096);
+  fill_identity_kernel<<<grid, 256, 0, s>>>(out, n_mats, d);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s) {
   if (p.d_k <= 16) return launch_dk<16>(p, s);

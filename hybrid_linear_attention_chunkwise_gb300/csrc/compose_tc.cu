@@ -72,7 +72,7 @@ struct Chain {
 };
 
 __device__ __forceinline__ int pair_slot(const ComposeParams &p, const Chain &c, int seg) {
-  const int s = p.slot[(int64_t)c.l * p.n_seg + seg];
+  const int s = p.slot[(int64_t)c.l * p.seg_stride + seg];
   return (s < 0 || s >= p.n_slots) ? -1 : s;
 }
 
@@ -207,7 +207,7 @@ struct SeamGroup {
 __device__ __forceinline__ SeamGroup seam_group(const ComposeParams &p, const Chain &c, int gq) {
   const int seg = gq / c.groups, gi = gq % c.groups;
   SeamGroup g;
-  g.tok0 = ((int64_t)c.l * p.n_seg + seg) * c.w + gi * GW;
+  g.tok0 = ((int64_t)c.l * p.seg_stride + seg) * c.w + gi * GW;
   g.nt = min(GW, c.w - gi * GW);
   return g;
 }
@@ -519,6 +519,7 @@ __global__ void __launch_bounds__(NT2, 2)
   SeamMmaSmem &sm = *reinterpret_cast<SeamMmaSmem *>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   const ComposeParams &p = args.p;
   const uint32_t LIM = args.wait_limit;
+  const bool trans = (p.flags & HYPIC_FLAG_TRANSITION_ONLY) != 0;  // U_t and S(C|0) count as zero
   const int tid = threadIdx.x;
   const int n = tid & 127;   // column of S
   const int hf = tid >> 7;   // rows 64*hf .. 64*hf+63 of that column
@@ -672,7 +673,9 @@ __global__ void __launch_bounds__(NT2, 2)
     tc::mma_commit(&sm.t_done);
     if (!tc::mbar_wait(&sm.t_done, ph, DRAIN_LIMIT)) fail(sm, p);
     tc::mbar_expect_tx(&sm.sc_full, 4 * SLAB);
-    const float *src = p.S_pool + ((int64_t)slot * p.h_v + c.h) * 128 * 128;
+    // transition-only: S(C|0) counts as zero; the copy (kept so the pipeline
+    // is unchanged) reads the pair's T_C instead of S_pool, which may be NULL
+    const float *src = (trans ? p.T_pool : p.S_pool) + ((int64_t)slot * p.h_v + c.h) * 128 * 128;
     for (int j = 0; j < 4; j++) tc::bulk_load(sm.slot[(q + j) % RING], src + j * 32 * 128, SLAB, &sm.sc_full);
   };
   // the four K-slabs at ring position q have landed (one thread)
@@ -695,7 +698,7 @@ __global__ void __launch_bounds__(NT2, 2)
     float u[GW];
 #pragma unroll
     for (int t = 0; t < GW; t++)
-      u[t] = t < sg.nt ? __bfloat162float(raw.v[t][n]) - G.ea[t] * __uint_as_float(d[t]) : 0.f;
+      u[t] = t < sg.nt ? (trans ? 0.f : __bfloat162float(raw.v[t][n])) - G.ea[t] * __uint_as_float(d[t]) : 0.f;
 #pragma unroll
     for (int t = 0; t < GW; t++) {
       float x = 0.f;
@@ -710,7 +713,7 @@ __global__ void __launch_bounds__(NT2, 2)
           float o = G.ea[t] * __uint_as_float(d[8 + t]);
 #pragma unroll
           for (int i = 0; i <= t; i++) o = fmaf(G.gq[t][i], cc[i], o);
-          p.seam_out[((sg.tok0 + t) * p.h_v + c.h) * 128 + n] = o;
+          if (!trans) p.seam_out[((sg.tok0 + t) * p.h_v + c.h) * 128 + n] = o;
           bad |= !finite_f(o);
         }
       }
@@ -1051,7 +1054,7 @@ __global__ void __launch_bounds__(NT2, 2)
         tc::tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; j++) {
-          const float x = fmaf(al, __uint_as_float(r[j]), sc[j]);
+          const float x = fmaf(al, __uint_as_float(r[j]), trans ? 0.f : sc[j]);
           if (keep) out[(int64_t)(16 * b + j) * 128] = x;
           bad |= !finite_f(x);  // every segment: a non-finite state is reported where it appears
           // per-channel gate, next group fused: TMEM A holds RN(E_last . S)

@@ -57,6 +57,7 @@ struct BuildParams {
 
 struct ComposeParams {
   int32_t n_layers, n_seg, h_k, h_v, d_k, d_v, seam_w;
+  int32_t seg_stride;  // segments per layer in slot, seam_* and seam_out (>= n_seg)
   int32_t variant, in_dtype;
   uint32_t flags;
   const int32_t *slot;
@@ -105,9 +106,11 @@ int check_build_slots(const hypic_build_desc *d, int32_t *sorted);
 // Bytes of a plan of n_items items (header + items, not rounded).
 size_t build_plan_size(int64_t n_items);
 // Writes the plan of every (segment, value head) item of d into `plan`
-// (build_plan_size(n_seg * h_v) bytes): LPT order and mode, or index order
-// and PLAN_ROUND_ROBIN under HYPIC_FLAG_ROUND_ROBIN.  In-place sort, no heap.
-void fill_build_plan(const hypic_build_desc *d, void *plan);
+// (at most build_plan_size(n_seg * h_v) bytes; segments whose slot is
+// HYPIC_SLOT_SKIP have no items) and returns the item count: LPT order and
+// mode, or index order and PLAN_ROUND_ROBIN under HYPIC_FLAG_ROUND_ROBIN.
+// In-place sort, no heap.
+int64_t fill_build_plan(const hypic_build_desc *d, void *plan);
 // Kernel parameters of a build descriptor; the plan pointer is left NULL.
 BuildParams build_params(const hypic_build_desc *d);
 // The kernel a build with these parameters runs (a hypic_path value).
@@ -151,6 +154,8 @@ bool merge_tc_supported(const MergeParams &p);
 cudaError_t launch_merge(const MergeParams &p, uint32_t wait_limit, cudaStream_t s);
 cudaError_t launch_rerotate(const RerotateParams &p, uint32_t wait_limit, cudaStream_t s);
 cudaError_t launch_compose_simt(const ComposeParams &p, cudaStream_t s);
+// out[m] = I (d x d) for m < n_mats
+cudaError_t launch_fill_identity(float *out, int64_t n_mats, int d, cudaStream_t s);
 cudaError_t launch_compose_tc(const ComposeParams &p, uint32_t wait_limit, cudaStream_t s);
 // The tensor-core compose covers dense transitions, bf16 seam tokens,
 // d_k = d_v = 128, h_v % 4 == 0 and 16-byte aligned tensors.

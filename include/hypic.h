@@ -112,6 +112,19 @@ typedef enum {
   HYPIC_PATH_F32_MERGE = 8     /* merge: fp32, CUDA cores */
 } hypic_path;
 
+/* Compose only: compose the transitions alone.  Every seam write U_t and
+ * every cached S(C|0) counts as zero (S_pool is not read and may be NULL;
+ * seam_v is read but its values do not matter; seam_out is not written and
+ * may be NULL), so the chain's final state is  T_{C_n} T_n,w .. T_n,1 ...
+ * T_{C_1} T_1,w .. T_1,1 S_init: from the identity, the transition of the
+ * whole run of segments (the T of a span, pages §2.1 composition rule and
+ * §2.3 segment parallelism).  d_v must equal d_k; S_init NULL stands for the
+ * identity in this mode (not for zero). */
+#define HYPIC_FLAG_TRANSITION_ONLY 8u
+
+/* Slot value that leaves a segment out of a build (see hypic_segment_build). */
+#define HYPIC_SLOT_SKIP (-1)
+
 /* Device status word bits (OR-ed by kernels; cleared by the caller). */
 #define HYPIC_STATUS_TIMEOUT   1u
 #define HYPIC_STATUS_NONFINITE 2u
@@ -131,7 +144,10 @@ typedef enum {
  * tokens form the seam window and are left out of the pair (§2.2), so the
  * pair covers the body [seg_offsets[i] + seam_w, seg_offsets[i+1]).  A body
  * that is empty gives (I, 0).  The pair of segment i goes to pool slot
- * slot_of_seg[i] (or slot i when slot_of_seg is NULL).
+ * slot_of_seg[i] (or slot i when slot_of_seg is NULL); a segment whose slot
+ * is HYPIC_SLOT_SKIP is not built (a worker that builds its own share of
+ * the segments of one prompt, pages §2.3, passes the whole prompt and skips
+ * the others' segments).
  *
  * Work is split into (segment, value head) items packed over the SMs
  * longest-first (LPT), the single-GPU analogue of the pages' greedy LPT
@@ -150,7 +166,7 @@ typedef struct {
                                  [n_tokens,h_v,d_k]; SCALAR_DECAY [h_v]; NULL otherwise */
   const float *beta;          /* [dev] [n_tokens, h_v] for the delta variants, NULL otherwise */
   const int64_t *seg_offsets; /* [host] [n_seg+1], non-decreasing, from 0 to n_tokens */
-  const int32_t *slot_of_seg; /* [host] [n_seg] distinct slots in [0, n_slots), or NULL */
+  const int32_t *slot_of_seg; /* [host] [n_seg] distinct slots in [0, n_slots) or HYPIC_SLOT_SKIP, or NULL */
   int64_t n_slots;
   float *T_pool;              /* [dev] see the shape note above */
   float *S_pool;              /* [dev] [n_slots, h_v, d_k, d_v] */
@@ -289,10 +305,66 @@ typedef struct {
   void *workspace;            /* [dev] >= hypic_compose_workspace_bytes() */
   size_t workspace_bytes;
   uint32_t *status;           /* [dev] optional */
+  int32_t seg_stride;         /* segments per layer in slot, seam_* and seam_out (0: n_seg); with
+                                 pointers advanced by a segments, n_seg = b - a composes the span
+                                 [a, b) of longer per-layer arrays in place */
 } hypic_compose_desc;
 
 size_t hypic_compose_workspace_bytes(const hypic_compose_desc *d);
 int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream);
+
+/*
+ * hypic_span_scan -- the start state of every span of compose chains split
+ * into n_spans consecutive spans of segments (pages §2.3 segment
+ * parallelism, combined by the §2.1 composition rule): with the pair
+ * (T_s, S_s) of span s of layer l (T_s from hypic_compose with
+ * HYPIC_FLAG_TRANSITION_ONLY, S_s from hypic_compose from a zero state),
+ *   S_start[0, l] = S_init[l] (or 0),
+ *   S_start[s, l] = T_{s-1} S_start[s-1, l] + S_{s-1}      (s = 1 .. n_spans-1)
+ * for every value head, an exclusive scan over the spans.  Span-major
+ * layouts: T_span [n_spans, n_layers, h_v, d_k, d_k], S_span and S_start
+ * [n_spans, n_layers, h_v, d_k, d_v], S_init [n_layers, h_v, d_k, d_v], all
+ * fp32 device memory; S_start must not overlap the inputs.  Each step is one
+ * hypic_compose launch of one pair per chain (tensor cores where
+ * hypic_compose takes them), so n_spans - 1 launches.  The workspace holds
+ * the slot indices (hypic_span_scan_workspace_bytes).  Returns a
+ * hypic_status; device conditions go to the status word as for compose.
+ */
+typedef struct {
+  int32_t n_layers, n_spans;
+  int32_t h_v, d_k, d_v;
+  const float *T_span;   /* [dev] */
+  const float *S_span;   /* [dev] */
+  const float *S_init;   /* [dev] or NULL (= 0) */
+  float *S_start;        /* [dev] */
+  void *workspace;       /* [dev] >= hypic_span_scan_workspace_bytes(), 256-byte aligned */
+  size_t workspace_bytes;
+  uint32_t *status;      /* [dev] optional */
+} hypic_span_scan_desc;
+
+size_t hypic_span_scan_workspace_bytes(const hypic_span_scan_desc *d);
+int hypic_span_scan(const hypic_span_scan_desc *d, hypic_stream_t stream);
+
+/*
+ * hypic_compose_spans -- hypic_compose computed by segment parallelism on
+ * one GPU (pages §2.3): the n_seg segments of every chain are split into
+ * n_spans consecutive spans at span_bounds (host, [n_spans + 1], from 0 to
+ * n_seg, non-decreasing); each span's pair comes from two composes of its
+ * segments alone (its S from zero, its T with HYPIC_FLAG_TRANSITION_ONLY),
+ * hypic_span_scan gives every span its start state, and each span is then
+ * composed from that state, writing its seam outputs; the last span's final
+ * state is S_out.  The results equal hypic_compose's within its accuracy.
+ * On several GPUs each worker runs one span and only the span pairs are
+ * exchanged (one (T, S) per layer, head and span); this entry point runs the
+ * spans one after another and serves as the single-GPU form and reference.
+ * `d` is an ordinary compose descriptor (d_v = d_k, no transition-only
+ * flag); the workspace (hypic_compose_spans_workspace_bytes) holds the span
+ * pairs, start states and slot indices, about
+ * 3 * n_spans * n_layers * h_v * d_k * d_k * 4 bytes.
+ */
+size_t hypic_compose_spans_workspace_bytes(const hypic_compose_desc *d, int32_t n_spans);
+int hypic_compose_spans(const hypic_compose_desc *d, int32_t n_spans, const int32_t *span_bounds,
+                        hypic_stream_t stream);
 
 /*
  * hypic_pair_merge -- merge cached pairs of adjacent spans (pages §2.1: the

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synth_inputs as si
-from gpu_common import gpu_build, seam_arrays
+from gpu_common import dense_T, gpu_build, seam_arrays
 from tolerance import TOL_BF16, per_head_rel_err
 import hybrid_linear_attention_chunkwise_gb300 as hy
 
@@ -46,7 +46,7 @@ def _run(W, n_layers, S_init=None, status=None, slot=None):
 
 def _oracle_compose(W, T_pool, S_pool, sa, slot, S_init, n_layers):
     sl = slot.long().cpu()
-    Tp = T_pool.cpu()[sl]          # [L, n_seg, h_v, 128, 128]
+    Tp = dense_T(W.variant, T_pool, 128)[sl.numpy()]   # [L, n_seg, h_v, 128, 128]
     Sp = S_pool.cpu()[sl]
     outs = []
     for l in range(n_layers):
@@ -99,7 +99,7 @@ import sys, torch
 sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + '/tests')
 import synth_inputs as si
 import hybrid_linear_attention_chunkwise_gb300 as hy
-from gpu_common import gpu_build, seam_arrays
+from gpu_common import dense_T, gpu_build, seam_arrays
 W = si.workload(5, device='cuda', variant='gdn', lengths=[40, 70, 33], h_k=1, h_v=4, seam_w=8)
 T, S = gpu_build(W)
 torch.cuda.synchronize()
@@ -147,25 +147,33 @@ def test_compose_tc_long_chain(variant):
     assert e1 <= TOL_BF16 and e2 <= TOL_BF16, (e1, e2)
 
 
-@pytest.mark.parametrize("variant", ["gdn", "deltanet", "channel"])
-@pytest.mark.parametrize("w,n_spans", [(8, 2), (8, 3), (3, 5), (0, 4)])
-def test_compose_span_parallel(variant, w, n_spans):
-    """Segment parallelism on one chain: seam-window pairs built, each span's
-    pair merged, the span start states scanned, each span composed from its
-    start state.  Equals the oracle composition (final state and every seam
-    output) to the bf16 bar, like the one-pass compose."""
-    lens = [40, 130, 12, 64, 300, 25, 90]
-    W = si.workload(5, device=DEV, variant=variant, lengths=lens, h_k=2, h_v=4, seam_w=w, n_layers=2)
-    S_init = si.random_state((2, W.h_v, 128, 128), seed=1, cfg=5, device=DEV)
-    pools = [gpu_build(W, layer=l) for l in range(2)]
+def _chains(variant, w, n_layers=2, lens=(40, 130, 12, 64, 300, 25, 90)):
+    cfg = 2 if variant == "scalar" else 5
+    W = si.workload(cfg, device=DEV, variant=variant, lengths=list(lens), h_k=2, h_v=4, seam_w=w, n_layers=n_layers)
+    pools = [gpu_build(W, layer=l) for l in range(n_layers)]
     T_pool = torch.cat([p[0] for p in pools])
     S_pool = torch.cat([p[1] for p in pools])
-    sa = seam_arrays(W, range(2))
-    slot = torch.arange(2 * W.n_seg, dtype=torch.int32, device=DEV).reshape(2, W.n_seg)
+    sa = seam_arrays(W, range(n_layers))
+    slot = torch.arange(n_layers * W.n_seg, dtype=torch.int32, device=DEV).reshape(n_layers, W.n_seg)
+    return W, T_pool, S_pool, sa, slot
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "channel", "scalar", "diag"])
+@pytest.mark.parametrize("w,bounds", [(8, [0, 4, 7]), (8, [0, 2, 5, 7]), (3, [0, 1, 2, 3, 5, 7]), (0, [0, 2, 4, 6, 7]),
+                                      (8, [0, 3, 3, 7]), (8, [0, 7])])
+def test_compose_spans_vs_oracle(variant, w, bounds):
+    """Segment parallelism through the C ABI (hypic_compose_spans): each
+    span's pair from two composes of its own segments (S from zero, T by
+    the transition-only compose from the identity), the span start states by
+    the exclusive scan, each span composed from its start state.  Equals the
+    oracle composition (final state and every seam output) to the bf16 bar,
+    like the one-pass compose; an empty span and a single span included."""
+    W, T_pool, S_pool, sa, slot = _chains(variant, w)
+    S_init = si.random_state((2, W.h_v, 128, 128), seed=1, cfg=5, device=DEV)
     S_out = torch.empty((2, W.h_v, 128, 128), device=DEV)
     seam_out = torch.zeros((2, W.n_seg, w, W.h_v, 128), device=DEV) if w else None
-    hy.compose_span_parallel(slot, T_pool, S_pool, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"],
-                             variant=variant, S_out=S_out, seam_out=seam_out, S_init=S_init, n_spans=n_spans)
+    hy.compose_spans(slot, T_pool, S_pool, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"], variant=variant,
+                     S_out=S_out, seam_out=seam_out, S_init=S_init, bounds=bounds, h_k=W.h_k)
     torch.cuda.synchronize()
     So, seam = _oracle_compose(W, T_pool, S_pool, sa, slot, S_init, 2)
     assert per_head_rel_err(S_out, So).max() <= TOL_BF16
@@ -173,6 +181,41 @@ def test_compose_span_parallel(variant, w, n_spans):
         e = per_head_rel_err(seam_out.permute(0, 3, 1, 2, 4).reshape(2, W.h_v, -1),
                              np.transpose(seam, (0, 3, 1, 2, 4)).reshape(2, W.h_v, -1), inner=1)
         assert e.max() <= TOL_BF16, e.max()
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet", "channel", "scalar", "diag"])
+def test_transition_only_compose_is_the_product_of_transitions(variant):
+    """HYPIC_FLAG_TRANSITION_ONLY from the identity gives the transition of
+    the whole chain: the oracle composition of the same pairs and seam tokens
+    with every write (v, S(C|0)) set to zero, from S_init = I."""
+    W, T_pool, S_pool, sa, slot = _chains(variant, 8)
+    T_out = torch.empty((2, W.h_v, 128, 128), device=DEV)
+    hy.compose(slot, T_pool, None, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"], variant=variant, S_out=T_out,
+               seam_out=None, flags=hy.FLAG_TRANSITION_ONLY, h_k=W.h_k)
+    torch.cuda.synchronize()
+    eye = torch.eye(128).expand(2, W.h_v, 128, 128).contiguous()
+    zero_v = {**sa, "v": torch.zeros_like(sa["v"])}
+    So, _ = _oracle_compose(W, T_pool, torch.zeros_like(S_pool), zero_v, slot, eye, 2)
+    assert per_head_rel_err(T_out, So).max() <= TOL_BF16
+
+
+def test_span_scan_vs_oracle_merges():
+    """hypic_span_scan: S_start[s] = T_{s-1} S_start[s-1] + S_{s-1}, against
+    the oracle merge of the same fp32 pairs, 5 spans x 3 layers x 4 heads."""
+    gen = torch.Generator(device="cpu").manual_seed(9)
+    n_sp, L, H = 5, 3, 4
+    T = (torch.randn(n_sp, L, H, 128, 128, generator=gen, dtype=torch.float64) / np.sqrt(128)).float()
+    S = torch.randn(n_sp, L, H, 128, 128, generator=gen, dtype=torch.float64).float()
+    S0 = torch.randn(L, H, 128, 128, generator=gen, dtype=torch.float64).float()
+    out = torch.empty((n_sp, L, H, 128, 128), device=DEV)
+    hy.span_scan(T.to(DEV), S.to(DEV), out, S_init=S0.to(DEV))
+    torch.cuda.synchronize()
+    ref = [S0.numpy().astype(np.float64)]
+    for s in range(1, n_sp):
+        _, nxt = oracle.merge(T[s - 1].numpy(), S[s - 1].numpy(), T[s - 1].numpy(), ref[-1])
+        ref.append(nxt)
+    for s in range(n_sp):
+        assert per_head_rel_err(out[s].cpu(), ref[s]).max() <= TOL_BF16, s
 
 
 def test_compose_channel_steep_gates():

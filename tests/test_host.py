@@ -390,3 +390,61 @@ def test_noalloc_and_workspace_build_agree_on_a_no_token_call():
     a = lib.hypic_segment_build(ctypes.byref(d), None)
     b = lib.hypic_segment_build_noalloc(ctypes.byref(d), None)
     assert a == b == 4, (a, b)  # HYPIC_ERR_CUDA: validation passed on both
+
+
+def test_span_entry_points_reject_bad_descriptors():
+    """Transition-only compose, compose over spans and the span scan check
+    their arguments before any CUDA call."""
+    lib = hy.load()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def cdesc(**over):
+        d = hy.ComposeDesc()
+        d.n_layers, d.n_seg, d.h_k, d.h_v, d.d_k, d.d_v, d.seam_w = 1, 4, 1, 1, 16, 16, 2
+        d.variant, d.in_dtype = hy.GDN, hy.IN_F32
+        d.slot = d.T_pool = d.S_pool = d.seam_k = d.seam_v = d.seam_q = d.seam_g = d.seam_beta = fake
+        d.S_out = d.seam_out = fake
+        d.n_slots = 4
+        for k, v in over.items():
+            setattr(d, k, v)
+        return d
+    T = hy.FLAG_TRANSITION_ONLY
+    for over, want in [(dict(flags=T, d_v=8), 1),             # the state of a transition is d_k x d_k
+                       (dict(seg_stride=3), 1),                # a stride below n_seg
+                       (dict(flags=16), 1)]:                   # unknown flag
+        assert lib.hypic_compose(ctypes.byref(cdesc(**over)), None) == want, over
+    bnd = lambda *b: np.asarray(b, dtype=np.int32)
+    for b, want in [(bnd(0, 2, 3), 1), (bnd(1, 2, 4), 1), (bnd(0, 3, 2, 4), 1)]:
+        d = cdesc()
+        d.workspace, d.workspace_bytes = ctypes.c_void_p(1 << 24), 1 << 30
+        assert lib.hypic_compose_spans(ctypes.byref(d), len(b) - 1, b.ctypes.data_as(ctypes.c_void_p), None) == want
+    d = cdesc(flags=T)
+    b = bnd(0, 2, 4)
+    assert lib.hypic_compose_spans(ctypes.byref(d), 2, b.ctypes.data_as(ctypes.c_void_p), None) == 1
+    d = cdesc()
+    d.workspace, d.workspace_bytes = ctypes.c_void_p(1 << 24), 16
+    assert lib.hypic_compose_spans(ctypes.byref(d), 2, b.ctypes.data_as(ctypes.c_void_p), None) == 3
+    s = hy.SpanScanDesc()
+    s.n_layers, s.n_spans, s.h_v, s.d_k, s.d_v = 2, 3, 4, 128, 128
+    s.T_span = s.S_span = s.S_start = fake
+    assert lib.hypic_span_scan(ctypes.byref(s), None) == 3          # no workspace
+    s.workspace, s.workspace_bytes = ctypes.c_void_p(1 << 24), 1 << 20
+    s.S_start = None
+    assert lib.hypic_span_scan(ctypes.byref(s), None) == 1
+    s.S_start, s.d_k = fake, 200
+    assert lib.hypic_span_scan(ctypes.byref(s), None) == 2
+    assert lib.hypic_span_scan_workspace_bytes(ctypes.byref(s)) == 256
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake device pointers: only where no GPU can be reached")
+def test_build_accepts_skipped_segments_and_rejects_duplicates():
+    """HYPIC_SLOT_SKIP leaves a segment out; the other slots must stay
+    distinct and in range (checked before any CUDA call)."""
+    lib = hy.load()
+    off = np.asarray([0, 3, 8], dtype=np.int64)
+    po = off.ctypes.data_as(ctypes.c_void_p)
+    for slots, want_invalid in (([-1, 1], False), ([-1, -1], False), ([1, 1], True), ([-2, 0], True), ([0, 2], True)):
+        sl = np.asarray(slots, dtype=np.int32)
+        d = _fake_build_desc(seg_offsets=po, slot_of_seg=sl.ctypes.data_as(ctypes.c_void_p))
+        rc = lib.hypic_segment_build(ctypes.byref(d), None)
+        assert (rc == 1) == want_invalid, (slots, rc)
