@@ -550,7 +550,7 @@ __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, const float
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const float v = __uint_as_float(r[32 * h + j + e]);
-          xr[j + e] = tc::to_tf32(v);
+          xr[j + e] = tc::to_tf32_fast(v);  // X itself keeps any NaN (it is the accumulator)
           r[32 * h + j + e] = __float_as_uint(sc[e] * v);
         }
       }
@@ -628,7 +628,9 @@ __device__ void chain_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx
     tc::tmem_wait_ld();
 #pragma unroll
     for (int j = 0; j < 32; j++)
-      *reinterpret_cast<uint32_t *>(sm.wt + sw32(j, n, C)) = tc::to_tf32(__uint_as_float(r[j]));
+      // a NaN in W comes from an input that reaches X through K, U or the
+      // gates as well
+      *reinterpret_cast<uint32_t *>(sm.wt + sw32(j, n, C)) = tc::to_tf32_fast(__uint_as_float(r[j]));
   }
   tc::fence_proxy_async_smem();
   const float *gC = sm.gcv[b2];

@@ -573,7 +573,7 @@ __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC) {
 #pragma unroll
       for (int j = 0; j < 32; j++) {
         const float v = __uint_as_float(r[32 * h + j]);
-        xr[j] = tc::to_tf32(v);
+        xr[j] = tc::to_tf32_fast(v);  // X itself keeps any NaN (it is the accumulator)
         r[32 * h + j] = __float_as_uint(gC * v);
       }
       tc::tmem_st32(trow(tm + TM_XR, c0 + 32 * h), xr);
@@ -652,7 +652,9 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
     tc::tmem_wait_ld();
 #pragma unroll
     for (int j = 0; j < 32; j++)
-      *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, n, 64)) = tc::to_tf32(__uint_as_float(r[j]));
+      // a NaN in W comes from an input that reaches X through K, U or the
+      // gates as well
+      *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, n, 64)) = tc::to_tf32_fast(__uint_as_float(r[j]));
   }
   tc::fence_proxy_async_smem();
   const float gC = sm.gc[b3];

@@ -1052,13 +1052,28 @@ __global__ void __launch_bounds__(NT2, 2)
 #pragma unroll
         for (int j = 0; j < 16; j++) sc[j] = (b < 2 ? sc0 : sc1)[(16 * (b & 1) + j) * 128];
         tc::tmem_wait_ld();
+        // nf turns NaN once any x of the block is not finite (x * 0 is NaN
+        // exactly then): the fast rounding below may lose a NaN, so such a
+        // block (rare) is formed again with the guarded rounding, and
+        // reported (every segment, where the non-finite value appears)
+        float nf = 0.f;
 #pragma unroll
         for (int j = 0; j < 16; j++) {
           const float x = fmaf(al, __uint_as_float(r[j]), trans ? 0.f : sc[j]);
           if (keep) out[(int64_t)(16 * b + j) * 128] = x;
-          bad |= !finite_f(x);  // every segment: a non-finite state is reported where it appears
+          nf = fmaf(x, 0.f, nf);
           // per-channel gate, next group fused: TMEM A holds RN(E_last . S)
-          r[j] = tc::to_tf32(CH && scale_next ? x * el_next[16 * b + j] : x);
+          r[j] = tc::to_tf32_fast(CH && scale_next ? x * el_next[16 * b + j] : x);
+        }
+        if (__any_sync(0xffffffffu, nf != nf)) {  // warp-uniform: the TMEM load below is .sync.aligned
+          bad |= nf != nf;
+          tc::tmem_ld16(tDh + 16 * b, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; j++) {
+            const float x = fmaf(al, __uint_as_float(r[j]), trans ? 0.f : sc[j]);
+            r[j] = tc::to_tf32(CH && scale_next ? x * el_next[16 * b + j] : x);
+          }
         }
         tc::tmem_st16(tAh + 16 * b, r);
       }

@@ -253,5 +253,15 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
   return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : r;
 }
 
+// The same rounding without the NaN guard (two integer operations): a NaN
+// may come out as a zero or an infinity.  Only for an operand copy whose
+// exact fp32 value stays in an accumulator of its own that the copy's
+// products are added to (so a NaN lives on there and reaches the output),
+// or whose NaN reaches the output through another operand as well; the
+// build's state copy and its W tile are such copies.  A state whose only
+// copy is the rounded one must use to_tf32 (or detect non-finite values
+// itself).
+__device__ __forceinline__ uint32_t to_tf32_fast(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
+
 }  // namespace tc
 }  // namespace hypic
