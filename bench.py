@@ -340,14 +340,27 @@ def compose_variant_rows(dev, hy, peaks, n_layers=8):
     return rows
 
 
-def forward_row(dev, hy):
-    """hypic_segment_forward on the config-3 GDN layer: the pairs (the
-    tensor-core build) and the output of every token (zero-initial body
-    state) by the fp32 token recurrence over the state columns.  The output
-    pass is ALU-bound: per token and value head 3 d_k d_v FMAs (erase dot
-    product, update, output); the fraction below divides them by the whole
-    call's time (build included), against the fp32 FMA rate of the CUDA
-    cores, SMs x 128 lanes x 2 FLOP x the SM clock (2070 MHz)."""
+def forward_flops(lengths, h_v, d_k=128, d_v=128, g=2, chunk=C):
+    """Algorithmic FLOPs of the prefill forward's per-token outputs on top of
+    the build's: per chunk of c tokens and value head, Q S_0 2 c d_k d_v, the
+    causal (Q K^T) part c (c + 1) d_k / g (its Gram shared by the g value
+    heads of a key head) and its product with Delta c (c + 1) d_v."""
+    tot = 0.0
+    for L in lengths:
+        n_full, tail = divmod(int(L), chunk)
+        for c in [chunk] * n_full + ([tail] if tail else []):
+            tot += 2 * c * d_k * d_v + c * (c + 1) * d_k / g + c * (c + 1) * d_v
+    return tot * h_v
+
+
+def forward_row(dev, hy, peaks):
+    """hypic_segment_forward on the config-3 GDN layer (64 x 1024 tokens,
+    16 key / 32 value heads, d = 128, bf16): the pairs and the output of
+    every body token from the zero-initial body state.  On the tensor-core
+    path the build records every chunk's start state and Delta and a second
+    kernel forms the outputs chunk by chunk; the row reports the whole
+    call's algorithmic FLOPs (build plus outputs) against the bf16 tensor
+    peak, and names the output kernel that ran."""
     import torch
     import synth_inputs as si
     W = si.workload(3, seed=0, device=dev)
@@ -355,18 +368,23 @@ def forward_row(dev, hy):
     T = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_k), device=dev)
     S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
     o = torch.empty((W.n_tokens, W.h_v, W.d_v), device=dev)
-    ms = _time_ms(lambda: hy.segment_forward(L.k, L.v, L.q, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=0,
-                                             T_pool=T, S_pool=S, o_out=o), reps=3, warm=1)
-    fma = W.n_tokens * W.h_v * 3 * W.d_k * W.d_v
-    tf = 2 * fma / (ms * 1e-3) / 1e12
-    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    peak = n_sm * 128 * 2 * 2.070e9 / 1e12
-    del T, S, o
+    ws = [None]
+
+    def run():
+        ws[0] = hy.segment_forward(L.k, L.v, L.q, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=0, T_pool=T,
+                                   S_pool=S, o_out=o, workspace=ws[0])
+    ms = _time_ms(run, reps=5, warm=2)
+    path = hy.forward_path(L.k, L.v, L.q, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=0, T_pool=T, S_pool=S,
+                           o_out=o)
+    bodies = np.diff(W.seg_offsets) - W.seam_w
+    fl = build_flops(bodies, W.h_v) + forward_flops(bodies, W.h_v)
+    tf = fl / (ms * 1e-3) / 1e12
+    del T, S, o, ws
     torch.cuda.empty_cache()
-    return {"ms": ms, "tokens_per_s": W.n_tokens / (ms * 1e-3),
-            "alu": {"achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
-                    "peak_source": "fp32 FMA lanes x SM clock (derived)"},
-            "kernel": "tensor-core build, then the fp32 token recurrence over the state columns"}
+    return {"ms": ms, "tokens_per_s": W.n_tokens / (ms * 1e-3), "algorithmic_flops": fl,
+            "tensor": {"achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": tf / peaks["bf16"],
+                       "peak_source": peaks["src"] + " bf16 dense (burst)"},
+            "kernel": "outputs: " + path}
 
 
 def measure_rows(dev, hy, peaks):
@@ -414,13 +432,82 @@ def measure_rows(dev, hy, peaks):
         del L, T, S
 
     one("build: RetNet scalar decay, 8 heads, 16 x 512 tokens", si.workload(2, seed=0, device=dev))
-    rows["forward: GDN layer 64 x 1024 tokens, pairs + body outputs"] = forward_row(dev, hy)
+    rows["forward: GDN layer 64 x 1024 tokens, pairs + body outputs"] = forward_row(dev, hy, peaks)
     for var in ("gdn", "deltanet", "channel"):
         W = si.workload(5, seed=0, device=dev, variant=var)
         one(f"build: uneven 256-segment mix ({W.n_tokens} tokens), {var}", W, round_robin=var == "gdn")
         del W
         torch.cuda.empty_cache()
     return rows
+
+
+def segment_parallel_rows(dev, hy, comp, compose_ms_one, ws, rank):
+    """N > 1: the pages' segment parallelism (nav.aitube.vip §2.3) across the
+    ranks, each timed as the max over ranks of CUDA-event times after two
+    warm-up runs:
+      cold build: the uneven 256-segment GDN prompt, segments LPT-scattered
+        over the ranks, each rank's pairs sent to rank 0's pool while its
+        next group builds; against rank 0 building all of it alone;
+      compose: the warm-prompt chains split into one span per rank (span
+        pairs all-gathered, scanned, spans composed), against one GPU's
+        compose of the whole chains (the timed step's compose)."""
+    import torch
+    import torch.distributed as dist
+    import synth_inputs as si
+    from hybrid_linear_attention_chunkwise_gb300 import segment_parallel as sp
+
+    def timed(fn, reps=3):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        t = torch.tensor([a.elapsed_time(b) / reps], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    W = si.workload(5, seed=0, device=dev, variant="gdn")
+    L = W.layers[0]
+    T = S = None
+    if rank == 0:
+        T = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_k), device=dev)
+        S = torch.empty_like(T)
+    scatter_ms = timed(lambda: sp.cold_build_scatter(L.k, L.v, L.g, L.beta, W.seg_offsets, variant="gdn",
+                                                     seam_w=W.seam_w, T_pool=T, S_pool=S, n_groups=4))
+    one_ms = None
+    if rank == 0:
+        for _ in range(2):
+            hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=W.seam_w, T_pool=T,
+                             S_pool=S)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(3):
+            hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant="gdn", seam_w=W.seam_w, T_pool=T,
+                             S_pool=S)
+        b.record()
+        torch.cuda.synchronize()
+        one_ms = a.elapsed_time(b) / 3
+    dist.barrier()
+    del W, L, T, S
+    torch.cuda.empty_cache()
+    sa = comp["sa"]
+    seam = {k: sa[k] for k in ("k", "v", "q", "g", "beta")}
+    S_out = torch.empty_like(comp["S_out"])
+    shard_ms = timed(lambda: sp.compose_sharded(comp["slot"], comp["T_pool"], comp["S_pool"], seam, variant="gdn",
+                                                S_out=S_out, seam_out=comp["seam_out"]))
+    out = {"cold_build_scatter": {"ms": scatter_ms, "one_gpu_ms": one_ms, "ranks": ws,
+                                  "speedup": (one_ms / scatter_ms) if one_ms else None,
+                                  "what": "uneven 256-segment GDN prompt, LPT scatter, pairs to rank 0 by NCCL p2p"},
+           "compose_sharded": {"ms": shard_ms, "one_gpu_ms": compose_ms_one, "ranks": ws,
+                               "speedup": compose_ms_one / shard_ms,
+                               "what": "warm-prompt chains, one span per rank, span pairs all-gathered"}}
+    return out
 
 
 def run_profile_case(kind):
@@ -699,6 +786,11 @@ def main():
         rows.update(compose_variant_rows(dev, hy, peaks))
         rows.update(measure_rows(dev, hy, peaks))
 
+    # segment parallelism across the ranks (N > 1 only; every rank takes part)
+    seg_par = None
+    if ws > 1 and not args.no_rows:
+        seg_par = segment_parallel_rows(dev, hy, comp, c_ms, ws, rank)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(W3, os.cpu_count() or 1)
@@ -716,6 +808,7 @@ def main():
             "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
             "rows": rows,
+            "segment_parallel": seg_par,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

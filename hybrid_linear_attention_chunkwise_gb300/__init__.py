@@ -36,7 +36,7 @@ FLAG_REQUIRE_TENSOR_CORES = 4   # refuse calls that would run an fp32 CUDA-core 
 FLAG_TRANSITION_ONLY = 8        # compose: the product of the transitions alone
 SLOT_SKIP = -1                  # build: leave this segment out
 PATHS = ("none", "tc_chunkwise", "tc_channel", "tc_fast", "f32_token", "tc_compose", "f32_compose", "tc_merge",
-         "f32_merge")
+         "f32_merge", "tc_forward")
 STATUS_TIMEOUT, STATUS_NONFINITE, STATUS_BAD_SLOT = 1, 2, 4
 OK = 0
 
@@ -105,7 +105,7 @@ SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_wo
            "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_pair_rerotate", "hypic_segment_forward",
            "hypic_segment_build_host",
            "hypic_build_path", "hypic_forward_path", "hypic_compose_path", "hypic_merge_path",
-           "hypic_span_scan", "hypic_span_scan_workspace_bytes", "hypic_compose_spans",
+           "hypic_span_scan", "hypic_span_scan_workspace_bytes", "hypic_compose_spans", "hypic_forward_workspace_bytes",
            "hypic_compose_spans_workspace_bytes",
            "hypic_plan_lpt",
            "hypic_status_from_word", "hypic_status_string", "hypic_version")
@@ -151,6 +151,8 @@ def load():
                                ("hypic_compose_path", ComposeDesc), ("hypic_merge_path", MergeDesc)):
                 getattr(lib, name).argtypes = [ctypes.POINTER(desc)]
                 getattr(lib, name).restype = ctypes.c_int
+            lib.hypic_forward_workspace_bytes.argtypes = [ctypes.POINTER(ForwardDesc)]
+            lib.hypic_forward_workspace_bytes.restype = ctypes.c_size_t
             lib.hypic_span_scan.argtypes = [ctypes.POINTER(SpanScanDesc), P]
             lib.hypic_span_scan.restype = ctypes.c_int
             lib.hypic_span_scan_workspace_bytes.argtypes = [ctypes.POINTER(SpanScanDesc)]
@@ -288,20 +290,22 @@ def segment_forward(k, v, q, g, beta, seg_offsets, *, variant: str, seam_w: int,
     """hypic_segment_forward on torch tensors: segment_build's pairs plus
     o_out [N, h_v, d_v] fp32, the output of every body token from the
     zero-initial body state (seam-token rows are not written).  q [N, h_k,
-    d_k] in k's dtype."""
+    d_k] in k's dtype.  The workspace (allocated here when None) is
+    hypic_forward_workspace_bytes: about 96 KiB per 64-token chunk and value
+    head on the tensor-core path."""
     lib = load()
     _check(q, "q", dtype=k.dtype, ndim=3)
     _check(o_out, "o_out", dtype=torch.float32, ndim=3)
     d = ForwardDesc()
     b, keep = _build_desc(k, v, g, beta, seg_offsets, variant, seam_w, T_pool, S_pool, slot_of_seg,
                           workspace, status, flags)
-    if workspace is None:
-        nb = int(lib.hypic_build_workspace_bytes(ctypes.byref(b)))
-        workspace = alloc_workspace(nb, k.device)
-        b.workspace = _ptr(workspace)
-        b.workspace_bytes = workspace.numel()
     d.build = b
     d.q, d.o_out = _ptr(q), _ptr(o_out)
+    if workspace is None:
+        nb = int(lib.hypic_forward_workspace_bytes(ctypes.byref(d)))
+        workspace = alloc_workspace(nb, k.device)
+        d.build.workspace = _ptr(workspace)
+        d.build.workspace_bytes = workspace.numel()
     rc = lib.hypic_segment_forward(ctypes.byref(d), _stream(stream))
     del keep
     if rc != OK:

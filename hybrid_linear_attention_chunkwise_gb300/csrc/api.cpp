@@ -279,6 +279,32 @@ bool refused_fallback(uint32_t flags, int path, int64_t n_tokens) {
          (path == HYPIC_PATH_F32_TOKEN || path == HYPIC_PATH_F32_COMPOSE);
 }
 
+// The tensor-core forward's workspace after the plan: per chunk record
+// (64-token chunk of a built segment's body) and value head, the chunk's
+// start state (64 KiB) and Delta (32 KiB), then one output item each.
+// `chunk_base` (optional) receives every segment's first record index.
+struct FwdLayout {
+  int64_t n_rec = 0;  // chunk records (per value head)
+  size_t plan = 0, rec_S = 0, rec_D = 0, items = 0, total = 0;
+};
+FwdLayout forward_layout(const hypic_build_desc *d, std::vector<int32_t> *chunk_base) {
+  FwdLayout f;
+  if (chunk_base) chunk_base->assign(d->n_seg, 0);
+  for (int i = 0; i < d->n_seg; i++) {
+    if (chunk_base) (*chunk_base)[i] = (int32_t)f.n_rec;
+    if (d->slot_of_seg && d->slot_of_seg[i] == HYPIC_SLOT_SKIP) continue;
+    const int64_t body = d->seg_offsets[i + 1] - std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
+    f.n_rec += (body + 63) / 64;
+  }
+  const size_t n = (size_t)f.n_rec * d->h_v;
+  f.plan = round_up(build_plan_size(n_build_items(d)), kAlign);
+  f.rec_S = f.plan;
+  f.rec_D = f.rec_S + round_up(n * 128 * 128 * 4, kAlign);
+  f.items = f.rec_D + round_up(n * 64 * 128 * 4, kAlign);
+  f.total = f.items + round_up(n * forward_item_bytes(), kAlign);
+  return f;
+}
+
 // the build (q == NULL) or the prefill forward (q, o_out): validation, LPT
 // plan, launch
 int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_stream_t stream) {
@@ -287,29 +313,68 @@ int build_impl(const hypic_build_desc *d, const void *q, float *o_out, hypic_str
   if (st || d->n_seg == 0) return st;
   BuildParams p = build_params(d);
   if (refused_fallback(d->flags, build_path(p, d->n_tokens), d->n_tokens)) return HYPIC_ERR_UNSUPPORTED;
-  // the forward's outputs run on the CUDA cores
-  if (o_out && refused_fallback(d->flags, HYPIC_PATH_F32_TOKEN, d->n_tokens)) return HYPIC_ERR_UNSUPPORTED;
   p.q = q;
   p.o_out = o_out;
+  // the forward's outputs: tensor cores from the recording build's chunk
+  // records where they apply, else the fp32 token recurrence (CUDA cores)
+  const bool tc_fwd = o_out && d->n_tokens > 0 && forward_tc_supported(p);
+  if (o_out && !tc_fwd && refused_fallback(d->flags, HYPIC_PATH_F32_TOKEN, d->n_tokens)) return HYPIC_ERR_UNSUPPORTED;
   p.plan = reinterpret_cast<PlanHeader *>(d->workspace);
   p.items = reinterpret_cast<const BuildItem *>(p.plan + 1);
 
   // one item per (segment, value head) on every kernel (see launch_build);
   // skipped segments have none
-  const size_t need = round_up(build_plan_size(n_build_items(d)), kAlign);
+  const size_t need_plan = round_up(build_plan_size(n_build_items(d)), kAlign);
+  std::vector<int32_t> chunk_base;
+  const FwdLayout fl = tc_fwd ? forward_layout(d, &chunk_base) : FwdLayout{};
+  const size_t need = tc_fwd ? fl.total : need_plan;
   if (!d->workspace || d->workspace_bytes < need || !aligned(d->workspace, kAlign)) return HYPIC_ERR_WORKSPACE;
-  std::vector<unsigned char> host(need, 0);
+  std::vector<unsigned char> host(need_plan, 0);
   const int64_t n_items = fill_build_plan(d, host.data());
   if (n_items == 0) return HYPIC_OK;
+  if (tc_fwd) {
+    // every item's first chunk record (BuildItem.part)
+    BuildItem *it = reinterpret_cast<BuildItem *>(reinterpret_cast<PlanHeader *>(host.data()) + 1);
+    for (int64_t r = 0; r < n_items; r++) it[r].part = chunk_base[it[r].seg];
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // pageable source: the call returns once the bytes are staged, so `host`
   // may be released when it goes out of scope
-  if (cudaMemcpyAsync(d->workspace, host.data(), need, cudaMemcpyHostToDevice, s) != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (cudaMemcpyAsync(d->workspace, host.data(), need_plan, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return HYPIC_ERR_CUDA;
   BuildParams pb = p;
   pb.q = nullptr;
   pb.o_out = nullptr;
+  if (tc_fwd) {
+    char *ws = static_cast<char *>(d->workspace);
+    pb.rec_S = reinterpret_cast<float *>(ws + fl.rec_S);
+    pb.rec_D = reinterpret_cast<float *>(ws + fl.rec_D);
+  }
   if (launch_build(pb, d->n_tokens, (int)n_items, sm_count(), s) != cudaSuccess) return HYPIC_ERR_CUDA;
-  if (o_out) {
+  if (tc_fwd) {
+    // the outputs: one item per (chunk record, value head)
+    const int64_t n_out = fl.n_rec * d->h_v;
+    if (n_out > INT32_MAX) return HYPIC_ERR_UNSUPPORTED;
+    std::vector<unsigned char> fitems((size_t)n_out * forward_item_bytes());
+    int64_t r = 0;
+    for (int i = 0; i < d->n_seg; i++) {
+      if (d->slot_of_seg && d->slot_of_seg[i] == HYPIC_SLOT_SKIP) continue;
+      const int64_t start = std::min(d->seg_offsets[i] + d->seam_w, d->seg_offsets[i + 1]);
+      const int64_t end = d->seg_offsets[i + 1];
+      for (int64_t t0 = start, c = 0; t0 < end; t0 += 64, c++)
+        for (int h = 0; h < d->h_v; h++)
+          forward_fill_item(fitems.data(), r++, chunk_base[i] + (int32_t)c, h, (int32_t)std::min<int64_t>(64, end - t0),
+                            t0);
+    }
+    char *ws = static_cast<char *>(d->workspace);
+    if (cudaMemcpyAsync(ws + fl.items, fitems.data(), fitems.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return HYPIC_ERR_CUDA;
+    BuildParams pf = p;
+    pf.rec_S = pb.rec_S;
+    pf.rec_D = pb.rec_D;
+    if (launch_forward_tc(pf, ws + fl.items, (int)n_out, d->n_tokens, wait_limit(), s) != cudaSuccess)
+      return HYPIC_ERR_CUDA;
+  } else if (o_out) {
     // the forward: the pairs above, then the outputs by the fp32 token
     // recurrence over the S columns alone, from a fresh ticket over the same
     // plan
@@ -766,7 +831,20 @@ int hypic_forward_path(const hypic_forward_desc *d) {
   const int st = check_build_shapes(&d->build);
   if (st) return -st;
   if (d->build.n_seg == 0) return HYPIC_PATH_NONE;
-  return HYPIC_PATH_F32_TOKEN;  // the outputs: fp32 token recurrence over the state columns
+  BuildParams p = build_params(&d->build);
+  p.q = d->q;
+  p.o_out = d->o_out;
+  return d->build.n_tokens > 0 && forward_tc_supported(p) ? HYPIC_PATH_TC_FORWARD : HYPIC_PATH_F32_TOKEN;
+}
+
+size_t hypic_forward_workspace_bytes(const hypic_forward_desc *d) {
+  if (!d || check_build_shapes(&d->build) != HYPIC_OK) return 0;
+  BuildParams p = build_params(&d->build);
+  p.q = d->q;
+  p.o_out = d->o_out;
+  if (d->build.n_tokens > 0 && d->build.n_seg > 0 && forward_tc_supported(p))
+    return forward_layout(&d->build, nullptr).total;
+  return hypic_build_workspace_bytes(&d->build);
 }
 
 int hypic_compose_path(const hypic_compose_desc *d) {

@@ -107,6 +107,7 @@ __device__ __forceinline__ uint64_t mndesc16(uint32_t base, int t) {
 struct XItem {
   int32_t slot, head, n_ch, valid;
   uint32_t gch0;
+  int32_t cbase;  // recording build: index of the item's first chunk record
 };
 // The copy issuer of the P group (its thread 0; kept in shared memory):
 // chunks are loaded in the CTA's chunk order, one ahead of the chunk being
@@ -558,9 +559,23 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
 }
 
 // ---------------------------------------------------------------- X group
-// XR <- RN(X_h) (chain 1 reads the start-of-chunk state), X_h <- G_C X_h
-// (the accumulator chain 2 adds onto), in one pass over the half.
-__device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC) {
+// The X group keeps the state scaled: the true block is a * X_h, with one
+// scale a per item shared by both halves.  A chunk's decay G_C then needs no
+// pass over the block: a <- a G_C, chain 1 takes W scaled by the old a
+// (Y = W (a X) - U) and chain 2 adds Ytilde / a_new (X_new = X + K^T Ytilde
+// / a_new), both folded into passes that run anyway.  When a G_C drops below
+// SCALE_MIN the scale is folded into the block in the staging pass
+// (X <- a G_C X, a <- 1), so 1 / a stays below 2^60 and a decay that
+// underflows to zero clears the state.
+constexpr float SCALE_MIN = 8.6736174e-19f;  // 2^-60
+
+// XR <- RN(X_h) (chain 1 reads the start-of-chunk state) in one pass over the
+// half; when folding, also X_h <- s X_h (the accumulator chain 2 adds onto).
+// Recording build: `rec` (non-NULL for the S half) receives the true
+// start-of-chunk state ra * X, column n of S (this thread's lane) at
+// rec[d * 128].
+template <bool REC>
+__device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, bool fold, float s, float *rec, float ra) {
 #pragma unroll 1
   for (int c0 = 0; c0 < 128; c0 += 64) {
     uint32_t r[64];
@@ -573,13 +588,16 @@ __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC) {
 #pragma unroll
       for (int j = 0; j < 32; j++) {
         const float v = __uint_as_float(r[32 * h + j]);
+        if (REC && rec) rec[(int64_t)(c0 + 32 * h + j) * 128] = ra * v;
         xr[j] = tc::to_tf32_fast(v);  // X itself keeps any NaN (it is the accumulator)
-        r[32 * h + j] = __float_as_uint(gC * v);
+        r[32 * h + j] = __float_as_uint(s * v);
       }
       tc::tmem_st32(trow(tm + TM_XR, c0 + 32 * h), xr);
     }
-    tc::tmem_st32(trow(tm + tx, c0), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-    tc::tmem_st32(trow(tm + tx, c0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+    if (fold) {
+      tc::tmem_st32(trow(tm + tx, c0), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+      tc::tmem_st32(trow(tm + tx, c0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+    }
   }
   tc::tmem_wait_st();
 }
@@ -610,12 +628,19 @@ __device__ __forceinline__ void issue_chain2(BuildTcSmem &sm, uint32_t tm, uint3
 
 // Ytilde = -Y diag(exp(lam_C - lam_t)), split hi + lo, as the K-major A
 // tiles [128 j x 64 t] of chain 2 (the S half's Y already holds -U)
-__device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int b3) {
+// Recording build: `rec` (non-NULL for the S half) receives
+// Delta = U - W S_0 = -Y of the chunk, column n, at rec[t * 128].
+template <bool REC>
+__device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int b3, float inv, float *rec) {
 #pragma unroll 1
   for (int c0 = 0; c0 < 64; c0 += 32) {
     uint32_t r[32];
     tc::tmem_ld32(trow(tm + TM_Y, c0), r);
     tc::tmem_wait_ld();
+    if (REC && rec) {
+#pragma unroll
+      for (int j = 0; j < 32; j++) rec[(int64_t)(c0 + j) * 128] = -__uint_as_float(r[j]);
+    }
 #pragma unroll
     for (int q8 = 0; q8 < 4; q8++) {
       uint32_t hw[4], lw[4];
@@ -623,7 +648,8 @@ __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int
       for (int j = 0; j < 4; j++) {
         const int jj = 8 * q8 + 2 * j, t = c0 + jj;
         const float2 dd = *reinterpret_cast<const float2 *>(&sm.dec[b3][t]);
-        split_bf16x2(-dd.x * __uint_as_float(r[jj]), -dd.y * __uint_as_float(r[jj + 1]), hw[j], lw[j]);
+        split_bf16x2((-inv * dd.x) * __uint_as_float(r[jj]), (-inv * dd.y) * __uint_as_float(r[jj + 1]), hw[j],
+                     lw[j]);
       }
       const uint32_t off = sw16(n, c0 + 8 * q8, 128);
       *reinterpret_cast<uint4 *>(sm.yh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -635,10 +661,18 @@ __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int
 // Advances both halves of the state through chunk ch (n = thread = TMEM
 // lane), the S half first: its chain 1 accumulates onto the -U^T that P put
 // in TM_Y.
+template <bool REC>
 __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx &x, int ch, int n, uint32_t tm,
-                            const MmaIds &id, uint32_t LIM) {
+                            const MmaIds &id, uint32_t LIM, float &a) {
   const uint32_t g = x.gch0 + (uint32_t)ch;
   const int bk = (int)(g % NBUF), b3 = (int)(g % 3);
+  // recording build: this chunk's records (S half only)
+  float *rec_s = nullptr, *rec_d = nullptr;
+  if (REC) {
+    const int64_t rc = (int64_t)(x.it.part + ch) * p.h_v + x.it.head;
+    rec_s = p.rec_S + rc * 128 * 128 + n;
+    rec_d = p.rec_D + rc * 64 * 128 + n;
+  }
   wait_phase(sm, p, &sm.wt_ready, g, LIM);
   // ---- W (tf32, rounded) as chain 1's B tile, once P's W / U MMAs are
   // complete (lane n holds row n of W^T; the previous chunk's chain 1 that
@@ -654,13 +688,16 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
     for (int j = 0; j < 32; j++)
       // a NaN in W comes from an input that reaches X through K, U or the
       // gates as well
-      *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, n, 64)) = tc::to_tf32_fast(__uint_as_float(r[j]));
+      *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, n, 64)) = tc::to_tf32_fast(a * __uint_as_float(r[j]));
   }
   tc::fence_proxy_async_smem();
-  const float gC = sm.gc[b3];
+  // the scale after this chunk (uniform over the group)
+  const float an = a * sm.gc[b3];
+  const bool fold = !(an >= SCALE_MIN) && an == an;  // a NaN scale stays (and reaches the output)
+  const float inv = fold ? 1.f : 1.f / an;           // chain 2 adds Ytilde / a_new
   // ---- S half (its chain 2 of the previous chunk was waited on before the
   // T half's Ytilde)
-  stage_half(tm, TM_XS, gC);
+  stage_half<REC>(tm, TM_XS, fold, an, rec_s, a);
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
   if (n == 0) {
@@ -669,7 +706,7 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   }
   wait_phase(sm, p, &sm.bar_y1, g, DRAIN_LIMIT);
   tc::tc_fence_after();
-  split_y(sm, tm, n, b3);
+  split_y<REC>(sm, tm, n, b3, inv, rec_d);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
@@ -678,7 +715,7 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   // of the previous chunk must be
   if (ch > 0) wait_phase(sm, p, &sm.bar_x2[(g - 1) & 1], (g - 1) >> 1, DRAIN_LIMIT);
   tc::tc_fence_after();
-  stage_half(tm, TM_XT, gC);
+  stage_half<REC>(tm, TM_XT, fold, an, nullptr, a);
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
   if (n == 0) issue_chain1(sm, tm, id, false, &sm.bar_y2);
@@ -686,7 +723,7 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   // the Ytilde tiles are free once the S half's chain 2 has read them
   wait_phase(sm, p, &sm.bar_x1, g, DRAIN_LIMIT);
   tc::tc_fence_after();
-  split_y(sm, tm, n, b3);
+  split_y<REC>(sm, tm, n, b3, inv, nullptr);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
@@ -694,8 +731,10 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
     tc::mbar_arrive(&sm.ys_done);  // TM_Y is free for the next chunk's -U
     issue_chain2(sm, tm, TM_XT, bk, id, &sm.bar_x2[g & 1]);
   }
+  a = fold ? 1.f : an;
 }
 
+template <bool REC>
 __global__ void __launch_bounds__(NT, 1)
     build_tc_kernel(const __grid_constant__ BuildTcArgs args, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v) {
@@ -775,6 +814,7 @@ __global__ void __launch_bounds__(NT, 1)
         xi.n_ch = iss.nch[0];
         xi.valid = iss.ok[0] ? 1 : 0;
         xi.gch0 = gch;
+        xi.cbase = iss.it[0].part;
         sm.xslot[k & 1] = xi;
         tc::mbar_arrive(&sm.item_full[k & 1]);
         sm.pitem.it = iss.it[0];
@@ -832,6 +872,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (!got || !xi.valid) break;
       ItemCtx x;
       x.it.slot = xi.slot;
+      x.it.part = xi.cbase;
       x.it.head = xi.head;
       x.n_ch = xi.n_ch;
       x.gch0 = xi.gch0;
@@ -850,7 +891,8 @@ __global__ void __launch_bounds__(NT, 1)
       tc::tmem_wait_st();
       tc::tc_fence_before();
       tc::named_bar(BAR_X, NG);
-      for (int ch = 0; ch < x.n_ch; ch++) chain_chunk(sm, p, x, ch, n, tm, id, LIM);
+      float a = 1.f;  // the block is a * X
+      for (int ch = 0; ch < x.n_ch; ch++) chain_chunk<REC>(sm, p, x, ch, n, tm, id, LIM, a);
       if (x.n_ch > 0) {
         const uint32_t gl = x.gch0 + (uint32_t)x.n_ch - 1;
         wait_phase(sm, p, &sm.bar_x2[gl & 1], gl >> 1, DRAIN_LIMIT);
@@ -869,7 +911,7 @@ __global__ void __launch_bounds__(NT, 1)
           tc::tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; j++) {
-            const float v = __uint_as_float(r[j]);
+            const float v = a * __uint_as_float(r[j]);
             out[(int64_t)(c0 + j) * 128] = v;
             bad |= !finite_f(v);
           }
@@ -936,7 +978,10 @@ cudaError_t launch_build_tc(const BuildParams &p, int64_t n_tokens, int n_items,
   if (!make_tmap_tokens(&tk, p.k, n_tokens, p.h_k) || !make_tmap_tokens(&tv, p.v, n_tokens, p.h_v))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(BuildTcSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(build_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the recording build (the prefill forward's first pass) also writes every
+  // chunk's start state and Delta
+  auto kern = p.rec_S ? build_tc_kernel<true> : build_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = n_sm < n_items ? n_sm : n_items;
   if (grid < 1) return cudaSuccess;
@@ -944,7 +989,7 @@ cudaError_t launch_build_tc(const BuildParams &p, int64_t n_tokens, int n_items,
   a.p = p;
   a.wait_limit = wait_limit;
   a.debug_stall = debug_stall() ? 1 : 0;
-  build_tc_kernel<<<grid, NT, smem, s>>>(a, tk, tv);
+  kern<<<grid, NT, smem, s>>>(a, tk, tv);
   return cudaGetLastError();
 }
 

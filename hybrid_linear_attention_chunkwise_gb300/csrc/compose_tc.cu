@@ -1044,6 +1044,11 @@ __global__ void __launch_bounds__(NT2, 2)
     if (use) {
       const float *sc0 = reinterpret_cast<const float *>(sm.slot[(q + 2 * hf) % RING]) + n;
       const float *sc1 = reinterpret_cast<const float *>(sm.slot[(q + 2 * hf + 1) % RING]) + n;
+      // nf turns NaN once any x is not finite (x * 0 is NaN exactly then):
+      // the fast rounding may lose a NaN, so a warp that holds one (rare)
+      // forms its rows again with the guarded rounding; reported on every
+      // segment, where the non-finite value appears
+      float nf = 0.f;
 #pragma unroll
       for (int b = 0; b < 4; b++) {
         uint32_t r[16];
@@ -1052,11 +1057,6 @@ __global__ void __launch_bounds__(NT2, 2)
 #pragma unroll
         for (int j = 0; j < 16; j++) sc[j] = (b < 2 ? sc0 : sc1)[(16 * (b & 1) + j) * 128];
         tc::tmem_wait_ld();
-        // nf turns NaN once any x of the block is not finite (x * 0 is NaN
-        // exactly then): the fast rounding below may lose a NaN, so such a
-        // block (rare) is formed again with the guarded rounding, and
-        // reported (every segment, where the non-finite value appears)
-        float nf = 0.f;
 #pragma unroll
         for (int j = 0; j < 16; j++) {
           const float x = fmaf(al, __uint_as_float(r[j]), trans ? 0.f : sc[j]);
@@ -1065,17 +1065,24 @@ __global__ void __launch_bounds__(NT2, 2)
           // per-channel gate, next group fused: TMEM A holds RN(E_last . S)
           r[j] = tc::to_tf32_fast(CH && scale_next ? x * el_next[16 * b + j] : x);
         }
-        if (__any_sync(0xffffffffu, nf != nf)) {  // warp-uniform: the TMEM load below is .sync.aligned
-          bad |= nf != nf;
+        tc::tmem_st16(tAh + 16 * b, r);
+      }
+      if (__any_sync(0xffffffffu, nf != nf)) {  // warp-uniform: the TMEM accesses are .sync.aligned
+        bad |= nf != nf;
+        tc::tmem_wait_st();
+#pragma unroll 1
+        for (int b = 0; b < 4; b++) {
+          uint32_t r[16];
           tc::tmem_ld16(tDh + 16 * b, r);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; j++) {
-            const float x = fmaf(al, __uint_as_float(r[j]), trans ? 0.f : sc[j]);
+            const float sc = (b < 2 ? sc0 : sc1)[(16 * (b & 1) + j) * 128];
+            const float x = fmaf(al, __uint_as_float(r[j]), trans ? 0.f : sc);
             r[j] = tc::to_tf32(CH && scale_next ? x * el_next[16 * b + j] : x);
           }
+          tc::tmem_st16(tAh + 16 * b, r);
         }
-        tc::tmem_st16(tAh + 16 * b, r);
       }
       if (keep) exact = out;
     }

@@ -50,6 +50,9 @@ struct BuildParams {
   float *T_pool, *S_pool;
   const void *q;            // forward: [n_tokens, h_k, d_k] (NULL: pairs only)
   float *o_out;             // forward: [n_tokens, h_v, d_v] body-token outputs
+  float *rec_S;             // recording build (tensor-core forward): per (chunk, head) the chunk's
+  float *rec_D;             //   start state [128 d][128 j] and Delta = U - W S_0 [64 t][128 j];
+                            //   the item's first chunk record is BuildItem.part (NULL: no records)
   PlanHeader *plan;         // device copy of the plan
   const BuildItem *items;   // = (BuildItem*)(plan + 1)
   uint32_t *status;
@@ -127,6 +130,15 @@ cudaError_t launch_forward_out(const BuildParams &p, int n_items, int n_sm, cuda
 bool build_tc_supported(const BuildParams &p);
 cudaError_t launch_build_tc(const BuildParams &p, int64_t n_tokens, int n_items, int n_sm, uint32_t wait_limit,
                             cudaStream_t s);
+// Tensor-core per-token outputs of the prefill forward (GDN / DeltaNet, bf16,
+// d = 128, 16-byte aligned q and o_out) from the recording build's chunk
+// records: one item per (chunk record, value head); `items` holds
+// forward_item_bytes() per item, written by forward_fill_item.
+bool forward_tc_supported(const BuildParams &p);
+cudaError_t launch_forward_tc(const BuildParams &p, const void *items, int n_items, int64_t n_tokens,
+                              uint32_t wait_limit, cudaStream_t s);
+size_t forward_item_bytes();
+void forward_fill_item(void *items, int64_t idx, int32_t rec, int32_t head, int32_t nt, int64_t tok0);
 // Tensor-core fast path (no erase: scalar decay, ungated, diagonal gate),
 // bf16 inputs, d_k = d_v = 128, 16-byte aligned k / v.
 bool build_fast_supported(const BuildParams &p);

@@ -109,7 +109,8 @@ typedef enum {
   HYPIC_PATH_TC_COMPOSE = 5,   /* compose: tensor cores (dense T, bf16 seam, d = 128) */
   HYPIC_PATH_F32_COMPOSE = 6,  /* compose: fp32, CUDA cores */
   HYPIC_PATH_TC_MERGE = 7,     /* merge: tensor cores, split tf32 */
-  HYPIC_PATH_F32_MERGE = 8     /* merge: fp32, CUDA cores */
+  HYPIC_PATH_F32_MERGE = 8,    /* merge: fp32, CUDA cores */
+  HYPIC_PATH_TC_FORWARD = 9    /* forward outputs: tensor cores, from the build's chunk records */
 } hypic_path;
 
 /* Compose only: compose the transitions alone.  Every seam write U_t and
@@ -190,9 +191,17 @@ int hypic_segment_build(const hypic_build_desc *d, hypic_stream_t stream);
  * with the post-update state, as for the seam outputs of hypic_compose.
  * q is [n_tokens, h_k, d_k] in the build's in_dtype (grouped heads as for k);
  * o_out is [n_tokens, h_v, d_v] fp32, its seam-token rows are not written.
- * The pairs come from the build's own kernels; the outputs from the fp32
- * token recurrence over the state columns (CUDA cores), for every variant
- * and head size.  Workspace and validation as for hypic_segment_build.
+ * The pairs come from the build's own kernels.  For GDN and DeltaNet with
+ * bf16 inputs, d_k = d_v = 128 and 16-byte aligned k, v, q and o_out, the
+ * outputs run on the tensor cores: the build also records every 64-token
+ * chunk's start state S_0 and its Delta = U - W S_0 in the workspace, and a
+ * second kernel forms each chunk's outputs from them,
+ *   o_t = G_t S_0^T q_t + sum_{i<=t} e^(lam_t - lam_i) (q_t . k_i) Delta_i,
+ * independently for every (chunk, value head).  Every other case runs the
+ * fp32 token recurrence over the state columns (CUDA cores).  The workspace
+ * is hypic_forward_workspace_bytes() (about 96 KiB per chunk and value head
+ * on the tensor-core path; the build's plan otherwise); validation as for
+ * hypic_segment_build.
  */
 typedef struct {
   hypic_build_desc build;
@@ -200,6 +209,7 @@ typedef struct {
   float *o_out;    /* [dev] [n_tokens, h_v, d_v] */
 } hypic_forward_desc;
 
+size_t hypic_forward_workspace_bytes(const hypic_forward_desc *d);
 int hypic_segment_forward(const hypic_forward_desc *d, hypic_stream_t stream);
 
 /*

@@ -130,3 +130,43 @@ def test_forward_steep_gates_token_by_token(variant, gate):
         assert np.isfinite(got).all() and worst <= tol, (i, worst)
     eT, eS = compare_pairs(W, T, S, *oracle_pairs(W), range(W.n_seg))
     assert eT <= tol and eS <= tol, (eT, eS)
+
+
+def test_forward_path_query_names_the_tensor_core_outputs():
+    """bf16 GDN / DeltaNet with 128-wide heads take the tensor-core output
+    kernel (chunk records of the build); fp32 inputs, narrower heads and the
+    other variants the fp32 token recurrence."""
+    lens = [70, 130]
+    for variant, d, dtype, want in (("gdn", 128, torch.bfloat16, "tc_forward"),
+                                    ("deltanet", 128, torch.bfloat16, "tc_forward"),
+                                    ("gdn", 128, torch.float32, "f32_token"),
+                                    ("gdn", 32, torch.bfloat16, "f32_token"),
+                                    ("channel", 128, torch.bfloat16, "f32_token")):
+        W = si.workload(5, device=DEV, variant=variant, lengths=lens, h_k=2, h_v=4, d=d, seam_w=8, dtype=dtype)
+        L = W.layers[0]
+        T, S = new_pools(variant, W.n_seg, W.h_v, W.d_k, W.d_v, DEV)
+        o = torch.empty((W.n_tokens, W.h_v, W.d_v), device=DEV)
+        got = hy.forward_path(L.k, L.v, L.q, L.g, L.beta, W.seg_offsets, variant=variant, seam_w=8, T_pool=T,
+                              S_pool=S, o_out=o)
+        assert got == want, (variant, d, dtype, got)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "deltanet"])
+def test_forward_tc_long_bodies_every_token(variant):
+    """Bodies of 1 .. 1100 tokens (chunk tails of every length class, one
+    body of a single token) on the tensor-core output path: every output
+    token against the oracle recurrence, the pairs against the oracle's."""
+    lens = [9, 72, 1100, 200, 65, 127, 64, 8]
+    W = si.workload(5, device=DEV, variant=variant, lengths=lens, h_k=2, h_v=4, seam_w=8)
+    T, S, o = _forward(W)
+    oc = o.cpu().double().numpy()
+    tol = tol_for(torch.bfloat16)
+    for i in range(W.n_seg):
+        s0, e, ref = _body_outputs_ref(W, i)
+        assert np.isnan(oc[int(W.seg_offsets[i]):s0]).all()
+        if ref is None:
+            continue
+        err = per_head_rel_err(np.transpose(oc[s0:e], (1, 0, 2)), np.transpose(ref, (1, 0, 2))).max()
+        assert err <= tol, (i, err)
+    eT, eS = compare_pairs(W, T, S, *oracle_pairs(W), range(W.n_seg))
+    assert eT <= tol and eS <= tol, (eT, eS)

@@ -347,11 +347,16 @@ def test_require_tensor_cores_refuses_fallbacks_before_any_cuda_call():
         d = _fake_build_desc(seg_offsets=po, flags=req, **over)
         assert lib.hypic_segment_build(ctypes.byref(d), None) == 2, over
         assert lib.hypic_segment_build_noalloc(ctypes.byref(d), None) == 2, over
-    # the forward's outputs run on the CUDA cores: refused under the flag
+    # a q off the 16-byte grid sends the forward's outputs to the CUDA
+    # cores: refused under the flag
     d = hy.ForwardDesc()
     d.build = _fake_build_desc(seg_offsets=po, flags=req, in_dtype=hy.IN_BF16, d_k=128, d_v=128)
-    d.q = d.o_out = ctypes.c_void_p(1 << 20)
+    d.q = ctypes.c_void_p((1 << 20) + 2)
+    d.o_out = ctypes.c_void_p(1 << 20)
+    assert hy.PATHS[lib.hypic_forward_path(ctypes.byref(d))] == "f32_token"
     assert lib.hypic_segment_forward(ctypes.byref(d), None) == 2
+    d.q = ctypes.c_void_p(1 << 20)
+    assert hy.PATHS[lib.hypic_forward_path(ctypes.byref(d))] == "tc_forward"
     fake = ctypes.c_void_p(1 << 20)
     c = hy.ComposeDesc()
     c.n_layers, c.n_seg, c.h_k, c.h_v, c.d_k, c.d_v, c.seam_w = 1, 2, 2, 2, 128, 128, 8
