@@ -749,16 +749,31 @@ def main():
         dk = {n: torch.empty_like(getattr(L3, n)) for n in ("k", "v", "g", "beta")}
         hT = torch.empty(T3.shape, dtype=torch.float32).pin_memory()
         hS = torch.empty(S3.shape, dtype=torch.float32).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in pin.values())
-        d2h = hT.numel() * 4 + hS.numel() * 4
+        # the compose leg: seam tokens from host memory, states and seam
+        # outputs back to host memory, the pool resident on the device
+        sa4 = comp["sa"]
+        keys = ("k", "v", "q", "g", "beta")
+        pin4 = {n: sa4[n].cpu().pin_memory() for n in keys}
+        st4 = {n: torch.empty_like(sa4[n]) for n in keys}
+        hS4 = torch.empty(comp["S_out"].shape, dtype=torch.float32).pin_memory()
+        ho4 = torch.empty(comp["seam_out"].shape, dtype=torch.float32).pin_memory()
+        h2d = (sum(x.numel() * x.element_size() for x in pin.values())
+               + sum(x.numel() * x.element_size() for x in pin4.values()))
+        d2h = hT.numel() * 4 + hS.numel() * 4 + hS4.numel() * 4 + ho4.numel() * 4
 
         def e2e_step():
-            # one C-ABI call: host inputs in, host pairs out, the copies of
-            # one group of segments overlapping the build of the next
+            # two C-ABI calls: host inputs in, host pairs out, the copies of
+            # one group of segments overlapping the build of the next; then
+            # host seam tokens in, host states and seam outputs out, the
+            # copies of one group of layers overlapping the next's compose
             hy.segment_build_host(pin["k"], pin["v"], pin["g"], pin["beta"], W3.seg_offsets, variant="gdn",
                                   seam_w=W3.seam_w, k=dk["k"], v=dk["v"], g=dk["g"], beta=dk["beta"],
                                   T_pool=T3, S_pool=S3, T_host=hT, S_host=hS, n_chunks=E2E_CHUNKS,
                                   workspace=ws3)
+            hy.compose_host(*(pin4[n] for n in keys), comp["slot"], comp["T_pool"], comp["S_pool"], variant="gdn",
+                            seam_k=st4["k"], seam_v=st4["v"], seam_q=st4["q"], seam_g=st4["g"], seam_beta=st4["beta"],
+                            S_out=comp["S_out"], S_out_host=hS4, seam_out=comp["seam_out"], seam_out_host=ho4,
+                            n_chunks=E2E_CHUNKS)
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
@@ -772,8 +787,11 @@ def main():
         e_ms = e0.elapsed_time(e1) / args.steps
         e2e = {"value": ws * W3.n_tokens / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-               "what": "hypic_segment_build_host: H2D of the layer's k/v/g/beta from pinned memory, build, D2H of "
-                       f"all pairs, in {E2E_CHUNKS} overlapped groups of segments"}
+               "what": "the whole step from host buffers: hypic_segment_build_host (H2D of the layer's "
+                       f"k/v/g/beta from pinned memory, build, D2H of all pairs, {E2E_CHUNKS} overlapped groups of "
+                       "segments), then hypic_compose_host (H2D of the warm prompt's seam tokens, compose against "
+                       f"the resident pool, D2H of the final states and seam outputs, {E2E_CHUNKS} overlapped "
+                       "groups of layers)"}
 
     # the other build rows, each against its own roofline (after the timed
     # region; not part of the step)

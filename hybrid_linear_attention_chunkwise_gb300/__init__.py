@@ -66,6 +66,12 @@ class ComposeDesc(ctypes.Structure):
                 ("seg_stride", ctypes.c_int32)]
 
 
+class HostComposeDesc(ctypes.Structure):
+    _fields_ = [("compose", ComposeDesc), ("host_seam_k", P), ("host_seam_v", P), ("host_seam_q", P),
+                ("host_seam_g", P), ("host_seam_beta", P), ("host_S_init", P), ("host_S_out", P),
+                ("host_seam_out", P), ("n_chunks", ctypes.c_int32)]
+
+
 class SpanScanDesc(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_spans", ctypes.c_int32), ("h_v", ctypes.c_int32),
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
@@ -103,7 +109,7 @@ ROPE_LAYOUT = {"interleaved": 0, "half": 1}
 
 SYMBOLS = ("hypic_segment_build", "hypic_segment_build_noalloc", "hypic_build_workspace_bytes", "hypic_compose",
            "hypic_compose_workspace_bytes", "hypic_pair_merge", "hypic_pair_rerotate", "hypic_segment_forward",
-           "hypic_segment_build_host",
+           "hypic_segment_build_host", "hypic_compose_host",
            "hypic_build_path", "hypic_forward_path", "hypic_compose_path", "hypic_merge_path",
            "hypic_span_scan", "hypic_span_scan_workspace_bytes", "hypic_compose_spans", "hypic_forward_workspace_bytes",
            "hypic_compose_spans_workspace_bytes",
@@ -151,6 +157,8 @@ def load():
                                ("hypic_compose_path", ComposeDesc), ("hypic_merge_path", MergeDesc)):
                 getattr(lib, name).argtypes = [ctypes.POINTER(desc)]
                 getattr(lib, name).restype = ctypes.c_int
+            lib.hypic_compose_host.argtypes = [ctypes.POINTER(HostComposeDesc), P]
+            lib.hypic_compose_host.restype = ctypes.c_int
             lib.hypic_forward_workspace_bytes.argtypes = [ctypes.POINTER(ForwardDesc)]
             lib.hypic_forward_workspace_bytes.restype = ctypes.c_size_t
             lib.hypic_span_scan.argtypes = [ctypes.POINTER(SpanScanDesc), P]
@@ -432,6 +440,33 @@ def compose(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, 
     rc = lib.hypic_compose(ctypes.byref(d), _stream(stream))
     if rc != OK:
         raise HypicError(rc, "hypic_compose")
+
+
+def compose_host(seam_k_host, seam_v_host, seam_q_host, seam_g_host, seam_beta_host, slot, T_pool, S_pool, *,
+                 variant: str, seam_k, seam_v, seam_q, seam_g, seam_beta, S_out, S_out_host, seam_out=None,
+                 seam_out_host=None, S_init=None, S_init_host=None, n_chunks: int = 8, h_k=None, status=None,
+                 flags: int = 0, stream=None):
+    """hypic_compose_host on torch tensors: compose() from host seam tokens
+    (page-locked for overlap) to host states and seam outputs, with the
+    device seam arrays, S_init, S_out and seam_out used as staging; the
+    layers go in n_chunks groups whose copies overlap the compose.  The host
+    arrays are complete once `stream` is synchronised."""
+    lib = load()
+    d = HostComposeDesc()
+    d.compose = _compose_desc(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, variant, S_out,
+                              seam_out, S_init, h_k, status, flags)
+    d.host_seam_k = _host_ptr(seam_k_host, seam_k, "seam_k_host")
+    d.host_seam_v = _host_ptr(seam_v_host, seam_v, "seam_v_host")
+    d.host_seam_q = _host_ptr(seam_q_host, seam_q, "seam_q_host")
+    d.host_seam_g = _host_ptr(seam_g_host, seam_g, "seam_g_host")
+    d.host_seam_beta = _host_ptr(seam_beta_host, seam_beta, "seam_beta_host")
+    d.host_S_init = _host_ptr(S_init_host, S_init, "S_init_host") if S_init_host is not None else None
+    d.host_S_out = _host_ptr(S_out_host, S_out, "S_out_host")
+    d.host_seam_out = _host_ptr(seam_out_host, seam_out, "seam_out_host")
+    d.n_chunks = int(n_chunks)
+    rc = lib.hypic_compose_host(ctypes.byref(d), _stream(stream))
+    if rc != OK:
+        raise HypicError(rc, "hypic_compose_host")
 
 
 def compose_path(slot, T_pool, S_pool, seam_k, seam_v, seam_q, seam_g, seam_beta, *, variant: str, S_out,

@@ -687,6 +687,84 @@ int hypic_segment_build_host(const hypic_host_build_desc *d, hypic_stream_t stre
 }
 
 
+int hypic_compose_host(const hypic_host_compose_desc *d, hypic_stream_t stream) {
+  if (!d) return HYPIC_ERR_INVALID_ARG;
+  const hypic_compose_desc &c = d->compose;
+  int st = check_compose(&c);
+  if (st) return st;
+  if (c.flags & HYPIC_FLAG_TRANSITION_ONLY) return HYPIC_ERR_INVALID_ARG;
+  if (d->n_chunks < 1 || !d->host_S_out) return HYPIC_ERR_INVALID_ARG;
+  const bool seam = c.seam_w > 0 && c.n_seg > 0;
+  auto pair_ok = [](const void *dev, const void *host) { return (dev == nullptr) == (host == nullptr); };
+  if (seam && (!d->host_seam_k || !d->host_seam_v || !d->host_seam_q || !d->host_seam_out)) return HYPIC_ERR_INVALID_ARG;
+  if (!pair_ok(c.seam_g, d->host_seam_g) || !pair_ok(c.seam_beta, d->host_seam_beta)) return HYPIC_ERR_INVALID_ARG;
+  if (d->host_S_init && !c.S_init) return HYPIC_ERR_INVALID_ARG;
+  if (c.n_layers == 0) return HYPIC_OK;
+  const ComposeParams base = compose_params(&c);
+  const int L = c.n_layers;
+  const int n_ch = std::min(std::min(d->n_chunks, L), kMaxHostChunks);
+  const size_t es = (size_t)in_size(c.in_dtype), w = (size_t)c.seam_w;
+  const size_t seg_stride = (size_t)base.seg_stride;
+  const bool vec = is_vector_gate(c.variant);
+  // bytes per layer of each array
+  const size_t k_l = seg_stride * w * c.h_k * c.d_k * es, v_l = seg_stride * w * c.h_v * c.d_v * es;
+  const size_t g_l = c.variant == HYPIC_SCALAR_DECAY ? (size_t)c.h_v * 4 : seg_stride * w * c.h_v * (vec ? c.d_k : 1) * 4;
+  const size_t b_l = seg_stride * w * c.h_v * 4, o_l = seg_stride * w * c.h_v * c.d_v * 4;
+  const size_t s_l = (size_t)c.h_v * c.d_k * c.d_v * 4;
+
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  HostPipe *hp = nullptr;
+  if ((st = host_pipe(hp))) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  auto at = [](const void *base_, size_t bytes) { return static_cast<const char *>(base_) + bytes; };
+  auto h2d = [&](const void *dst, const void *src, size_t n) {
+    return n == 0 || !dst || ok(cudaMemcpyAsync(const_cast<void *>(dst), src, n, cudaMemcpyHostToDevice, hp->in));
+  };
+  auto d2h = [&](void *dst, const void *src, size_t n) {
+    return n == 0 || !dst || ok(cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, hp->out));
+  };
+  if (!ok(cudaEventRecord(hp->start, s)) || !ok(cudaStreamWaitEvent(hp->in, hp->start, 0)) ||
+      !ok(cudaStreamWaitEvent(hp->out, hp->start, 0)))
+    return HYPIC_ERR_CUDA;
+  for (int g = 0; g < n_ch; g++) {
+    const int l0 = (int)((int64_t)L * g / n_ch), l1 = (int)((int64_t)L * (g + 1) / n_ch), nl = l1 - l0;
+    if (seam) {
+      if (!h2d(at(c.seam_k, l0 * k_l), at(d->host_seam_k, l0 * k_l), nl * k_l) ||
+          !h2d(at(c.seam_v, l0 * v_l), at(d->host_seam_v, l0 * v_l), nl * v_l) ||
+          !h2d(at(c.seam_q, l0 * k_l), at(d->host_seam_q, l0 * k_l), nl * k_l) ||
+          !h2d(c.seam_beta ? at(c.seam_beta, l0 * b_l) : nullptr, at(d->host_seam_beta, l0 * b_l), nl * b_l))
+        return HYPIC_ERR_CUDA;
+    }
+    if ((seam || c.variant == HYPIC_SCALAR_DECAY) &&
+        !h2d(c.seam_g ? at(c.seam_g, l0 * g_l) : nullptr, at(d->host_seam_g, l0 * g_l), nl * g_l))
+      return HYPIC_ERR_CUDA;
+    if (d->host_S_init && !h2d(at(c.S_init, l0 * s_l), at(d->host_S_init, l0 * s_l), nl * s_l)) return HYPIC_ERR_CUDA;
+    if (!ok(cudaEventRecord(hp->in_done[g], hp->in)) || !ok(cudaStreamWaitEvent(s, hp->in_done[g], 0)))
+      return HYPIC_ERR_CUDA;
+    // the group's compose: the same call over its layers
+    ComposeParams p = base;
+    p.n_layers = nl;
+    p.slot = c.slot ? c.slot + (size_t)l0 * seg_stride : nullptr;
+    p.seam_k = c.seam_k ? at(c.seam_k, l0 * k_l) : nullptr;
+    p.seam_v = c.seam_v ? at(c.seam_v, l0 * v_l) : nullptr;
+    p.seam_q = c.seam_q ? at(c.seam_q, l0 * k_l) : nullptr;
+    p.seam_g = c.seam_g ? reinterpret_cast<const float *>(at(c.seam_g, l0 * g_l)) : nullptr;
+    p.seam_beta = c.seam_beta ? reinterpret_cast<const float *>(at(c.seam_beta, l0 * b_l)) : nullptr;
+    p.S_init = c.S_init ? reinterpret_cast<const float *>(at(c.S_init, l0 * s_l)) : nullptr;
+    p.S_out = c.S_out + (size_t)l0 * s_l / 4;
+    p.seam_out = c.seam_out ? c.seam_out + (size_t)l0 * o_l / 4 : nullptr;
+    if ((st = compose_launch(p, stream))) return st;
+    if (!ok(cudaEventRecord(hp->built[g], s)) || !ok(cudaStreamWaitEvent(hp->out, hp->built[g], 0)))
+      return HYPIC_ERR_CUDA;
+    if (!d2h(reinterpret_cast<char *>(d->host_S_out) + l0 * s_l, p.S_out, nl * s_l) ||
+        (seam && !d2h(reinterpret_cast<char *>(d->host_seam_out) + l0 * o_l, p.seam_out, nl * o_l)))
+      return HYPIC_ERR_CUDA;
+  }
+  if (!ok(cudaEventRecord(hp->fin, hp->out)) || !ok(cudaStreamWaitEvent(s, hp->fin, 0))) return HYPIC_ERR_CUDA;
+  return HYPIC_OK;
+}
+
 int hypic_segment_forward(const hypic_forward_desc *d, hypic_stream_t stream) {
   if (!d) return HYPIC_ERR_INVALID_ARG;
   const hypic_build_desc &b = d->build;

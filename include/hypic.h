@@ -30,8 +30,9 @@
  *   - Pointers marked [dev] are caller-owned device memory, [host] are host
  *     memory read during the call only.  The library allocates no device
  *     memory.  Two entry points keep process-wide state and serialise their
- *     host calls with a lock: hypic_segment_build_host (copy streams and
- *     events per device, created on first use) and
+ *     host calls with a lock: hypic_segment_build_host and
+ *     hypic_compose_host (copy streams and events per device, created on
+ *     first use) and
  *     hypic_segment_build_noalloc (a fixed device array); see each.  Every
  *     other entry point keeps no global mutable state and is thread-safe.
  *   - Work is enqueued asynchronously on the caller's stream.  Host-side
@@ -322,6 +323,44 @@ typedef struct {
 
 size_t hypic_compose_workspace_bytes(const hypic_compose_desc *d);
 int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream);
+
+/*
+ * hypic_compose_host -- hypic_compose from seam tokens in host memory to
+ * states and seam outputs in host memory, the cached pairs resident on the
+ * device, with the copies overlapped with the compose.  The pages have no
+ * counterpart: this is the deployment form of the same compose (pages §2.1
+ * composition rule, §2.2 seam window), with the same results bit for bit.
+ *
+ * d->compose is a full hypic_compose descriptor whose [dev] seam arrays
+ * (seam_k, seam_v, seam_q, seam_g, seam_beta), S_init, S_out and seam_out the
+ * call uses as staging: the seam arrays (and S_init, when host_S_init is
+ * given) are overwritten with the host inputs.  The host_* arrays have the
+ * shapes of their device counterparts and are NULL exactly when those are;
+ * host_S_out and host_seam_out (NULL when seam_w = 0) receive the results.
+ *
+ * The layers are split into min(n_chunks, n_layers, 64) groups of
+ * consecutive layers.  Per group, the group's seam tokens (and initial
+ * states) are copied in on a copy stream of the library, its compose runs
+ * on `stream` once they are in, and its states and seam outputs are copied
+ * out on a second copy stream once it is done; so group c's compose
+ * overlaps group c+1's inputs and group c-1's outputs.  Everything is ordered
+ * after the work already on `stream`, and `stream` waits for the last copy
+ * out: the host arrays are complete once `stream` is synchronised.  Overlap
+ * needs page-locked host arrays.  Returns a hypic_status; every argument is
+ * checked first.  Host calls are serialised by a lock (the copy streams and
+ * events are shared per device with hypic_segment_build_host).
+ */
+typedef struct {
+  hypic_compose_desc compose;
+  const void *host_seam_k, *host_seam_v, *host_seam_q; /* [host] as compose.seam_* */
+  const float *host_seam_g, *host_seam_beta;           /* [host] */
+  const float *host_S_init;                             /* [host] or NULL (then compose.S_init is read as is) */
+  float *host_S_out;                                    /* [host] [n_layers, h_v, d_k, d_v] */
+  float *host_seam_out;                                 /* [host] [n_layers, n_seg, seam_w, h_v, d_v] */
+  int32_t n_chunks;                                     /* >= 1 */
+} hypic_host_compose_desc;
+
+int hypic_compose_host(const hypic_host_compose_desc *d, hypic_stream_t stream);
 
 /*
  * hypic_span_scan -- the start state of every span of compose chains split

@@ -453,3 +453,37 @@ def test_build_accepts_skipped_segments_and_rejects_duplicates():
         d = _fake_build_desc(seg_offsets=po, slot_of_seg=sl.ctypes.data_as(ctypes.c_void_p))
         rc = lib.hypic_segment_build(ctypes.byref(d), None)
         assert (rc == 1) == want_invalid, (slots, rc)
+
+
+def test_compose_host_rejects_bad_descriptors():
+    """hypic_compose_host checks the compose descriptor, the chunk count and
+    the host arrays (present exactly where their device twins are) before
+    its first CUDA call."""
+    lib = hy.load()
+    fake = ctypes.c_void_p(1 << 20)
+    host = ctypes.c_void_p(1 << 21)
+
+    def desc(**over):
+        d = hy.HostComposeDesc()
+        c = d.compose
+        c.n_layers, c.n_seg, c.h_k, c.h_v, c.d_k, c.d_v, c.seam_w = 2, 3, 1, 1, 16, 16, 2
+        c.variant, c.in_dtype = hy.GDN, hy.IN_F32
+        c.slot = c.T_pool = c.S_pool = c.seam_k = c.seam_v = c.seam_q = c.seam_g = c.seam_beta = fake
+        c.S_out = c.seam_out = fake
+        c.n_slots = 6
+        for n in ("host_seam_k", "host_seam_v", "host_seam_q", "host_seam_g", "host_seam_beta", "host_S_out",
+                  "host_seam_out"):
+            setattr(d, n, host)
+        d.n_chunks = 2
+        for k, v in over.items():
+            if k.startswith("c_"):
+                setattr(d.compose, k[2:], v)
+            else:
+                setattr(d, k, v)
+        return d
+    for over, want in [(dict(n_chunks=0), 1), (dict(host_S_out=None), 1), (dict(host_seam_q=None), 1),
+                       (dict(host_seam_out=None), 1), (dict(host_seam_g=None), 1), (dict(host_seam_beta=None), 1),
+                       (dict(host_S_init=host), 1),            # a host S_init needs its device staging
+                       (dict(c_S_out=None), 1), (dict(c_d_v=200), 2),
+                       (dict(c_flags=hy.FLAG_TRANSITION_ONLY), 1)]:
+        assert lib.hypic_compose_host(ctypes.byref(desc(**over)), None) == want, over
