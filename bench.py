@@ -101,11 +101,11 @@ KERNEL_SOURCES = {
     "channel": ("build_channel.cu", "tc.cuh", "common.cuh", "internal.h"),
     "merge": ("merge.cu", "tc.cuh", "common.cuh", "internal.h"),
     "rerotate": ("rerotate.cu", "tc.cuh", "common.cuh", "internal.h"),
-    "forward": ("build_token.cu", "common.cuh", "internal.h"),
+    "forward": ("forward_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
 }
 PROFILE_FILES = {"build": "segment_build_tc__gdn_16x1024.md", "compose": "compose_seam_mma__gdn_4x32x100.md",
                  "channel": "segment_build_channel__16x1024.md", "merge": "pair_merge_tc__4x32x50.md",
-                 "rerotate": "pair_rerotate__4x100x32.md", "forward": "forward_out__gdn_16x1024.md"}
+                 "rerotate": "pair_rerotate__4x100x32.md", "forward": "forward_tc__gdn_16x1024.md"}
 
 
 def source_hash(kind):

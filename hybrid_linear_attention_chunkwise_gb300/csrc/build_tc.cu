@@ -559,23 +559,12 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
 }
 
 // ---------------------------------------------------------------- X group
-// The X group keeps the state scaled: the true block is a * X_h, with one
-// scale a per item shared by both halves.  A chunk's decay G_C then needs no
-// pass over the block: a <- a G_C, chain 1 takes W scaled by the old a
-// (Y = W (a X) - U) and chain 2 adds Ytilde / a_new (X_new = X + K^T Ytilde
-// / a_new), both folded into passes that run anyway.  When a G_C drops below
-// SCALE_MIN the scale is folded into the block in the staging pass
-// (X <- a G_C X, a <- 1), so 1 / a stays below 2^60 and a decay that
-// underflows to zero clears the state.
-constexpr float SCALE_MIN = 8.6736174e-19f;  // 2^-60
-
-// XR <- RN(X_h) (chain 1 reads the start-of-chunk state) in one pass over the
-// half; when folding, also X_h <- s X_h (the accumulator chain 2 adds onto).
-// Recording build: `rec` (non-NULL for the S half) receives the true
-// start-of-chunk state ra * X, column n of S (this thread's lane) at
-// rec[d * 128].
+// XR <- RN(X_h) (chain 1 reads the start-of-chunk state), X_h <- G_C X_h
+// (the accumulator chain 2 adds onto), in one pass over the half.
+// Recording build: `rec` (non-NULL for the S half) receives the
+// start-of-chunk state, column n of S (this thread's lane) at rec[d * 128].
 template <bool REC>
-__device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, bool fold, float s, float *rec, float ra) {
+__device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC, float *rec) {
 #pragma unroll 1
   for (int c0 = 0; c0 < 128; c0 += 64) {
     uint32_t r[64];
@@ -588,16 +577,14 @@ __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, bool fold, 
 #pragma unroll
       for (int j = 0; j < 32; j++) {
         const float v = __uint_as_float(r[32 * h + j]);
-        if (REC && rec) rec[(int64_t)(c0 + 32 * h + j) * 128] = ra * v;
+        if (REC && rec) rec[(int64_t)(c0 + 32 * h + j) * 128] = v;
         xr[j] = tc::to_tf32_fast(v);  // X itself keeps any NaN (it is the accumulator)
-        r[32 * h + j] = __float_as_uint(s * v);
+        r[32 * h + j] = __float_as_uint(gC * v);
       }
       tc::tmem_st32(trow(tm + TM_XR, c0 + 32 * h), xr);
     }
-    if (fold) {
-      tc::tmem_st32(trow(tm + tx, c0), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-      tc::tmem_st32(trow(tm + tx, c0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-    }
+    tc::tmem_st32(trow(tm + tx, c0), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tc::tmem_st32(trow(tm + tx, c0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
   }
   tc::tmem_wait_st();
 }
@@ -631,7 +618,7 @@ __device__ __forceinline__ void issue_chain2(BuildTcSmem &sm, uint32_t tm, uint3
 // Recording build: `rec` (non-NULL for the S half) receives
 // Delta = U - W S_0 = -Y of the chunk, column n, at rec[t * 128].
 template <bool REC>
-__device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int b3, float inv, float *rec) {
+__device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int b3, float *rec) {
 #pragma unroll 1
   for (int c0 = 0; c0 < 64; c0 += 32) {
     uint32_t r[32];
@@ -648,8 +635,7 @@ __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int
       for (int j = 0; j < 4; j++) {
         const int jj = 8 * q8 + 2 * j, t = c0 + jj;
         const float2 dd = *reinterpret_cast<const float2 *>(&sm.dec[b3][t]);
-        split_bf16x2((-inv * dd.x) * __uint_as_float(r[jj]), (-inv * dd.y) * __uint_as_float(r[jj + 1]), hw[j],
-                     lw[j]);
+        split_bf16x2(-dd.x * __uint_as_float(r[jj]), -dd.y * __uint_as_float(r[jj + 1]), hw[j], lw[j]);
       }
       const uint32_t off = sw16(n, c0 + 8 * q8, 128);
       *reinterpret_cast<uint4 *>(sm.yh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -663,7 +649,7 @@ __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int
 // in TM_Y.
 template <bool REC>
 __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx &x, int ch, int n, uint32_t tm,
-                            const MmaIds &id, uint32_t LIM, float &a) {
+                            const MmaIds &id, uint32_t LIM) {
   const uint32_t g = x.gch0 + (uint32_t)ch;
   const int bk = (int)(g % NBUF), b3 = (int)(g % 3);
   // recording build: this chunk's records (S half only)
@@ -688,16 +674,13 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
     for (int j = 0; j < 32; j++)
       // a NaN in W comes from an input that reaches X through K, U or the
       // gates as well
-      *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, n, 64)) = tc::to_tf32_fast(a * __uint_as_float(r[j]));
+      *reinterpret_cast<uint32_t *>(sm.wt + sw32(c0 + j, n, 64)) = tc::to_tf32_fast(__uint_as_float(r[j]));
   }
   tc::fence_proxy_async_smem();
-  // the scale after this chunk (uniform over the group)
-  const float an = a * sm.gc[b3];
-  const bool fold = !(an >= SCALE_MIN) && an == an;  // a NaN scale stays (and reaches the output)
-  const float inv = fold ? 1.f : 1.f / an;           // chain 2 adds Ytilde / a_new
+  const float gC = sm.gc[b3];
   // ---- S half (its chain 2 of the previous chunk was waited on before the
   // T half's Ytilde)
-  stage_half<REC>(tm, TM_XS, fold, an, rec_s, a);
+  stage_half<REC>(tm, TM_XS, gC, rec_s);
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
   if (n == 0) {
@@ -706,7 +689,7 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   }
   wait_phase(sm, p, &sm.bar_y1, g, DRAIN_LIMIT);
   tc::tc_fence_after();
-  split_y<REC>(sm, tm, n, b3, inv, rec_d);
+  split_y<REC>(sm, tm, n, b3, rec_d);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
@@ -715,7 +698,7 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   // of the previous chunk must be
   if (ch > 0) wait_phase(sm, p, &sm.bar_x2[(g - 1) & 1], (g - 1) >> 1, DRAIN_LIMIT);
   tc::tc_fence_after();
-  stage_half<REC>(tm, TM_XT, fold, an, nullptr, a);
+  stage_half<REC>(tm, TM_XT, gC, nullptr);
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
   if (n == 0) issue_chain1(sm, tm, id, false, &sm.bar_y2);
@@ -723,7 +706,7 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   // the Ytilde tiles are free once the S half's chain 2 has read them
   wait_phase(sm, p, &sm.bar_x1, g, DRAIN_LIMIT);
   tc::tc_fence_after();
-  split_y<REC>(sm, tm, n, b3, inv, nullptr);
+  split_y<REC>(sm, tm, n, b3, nullptr);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   tc::named_bar(BAR_X, NG);
@@ -731,7 +714,6 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
     tc::mbar_arrive(&sm.ys_done);  // TM_Y is free for the next chunk's -U
     issue_chain2(sm, tm, TM_XT, bk, id, &sm.bar_x2[g & 1]);
   }
-  a = fold ? 1.f : an;
 }
 
 template <bool REC>
@@ -891,8 +873,7 @@ __global__ void __launch_bounds__(NT, 1)
       tc::tmem_wait_st();
       tc::tc_fence_before();
       tc::named_bar(BAR_X, NG);
-      float a = 1.f;  // the block is a * X
-      for (int ch = 0; ch < x.n_ch; ch++) chain_chunk<REC>(sm, p, x, ch, n, tm, id, LIM, a);
+      for (int ch = 0; ch < x.n_ch; ch++) chain_chunk<REC>(sm, p, x, ch, n, tm, id, LIM);
       if (x.n_ch > 0) {
         const uint32_t gl = x.gch0 + (uint32_t)x.n_ch - 1;
         wait_phase(sm, p, &sm.bar_x2[gl & 1], gl >> 1, DRAIN_LIMIT);
@@ -911,7 +892,7 @@ __global__ void __launch_bounds__(NT, 1)
           tc::tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; j++) {
-            const float v = a * __uint_as_float(r[j]);
+            const float v = __uint_as_float(r[j]);
             out[(int64_t)(c0 + j) * 128] = v;
             bad |= !finite_f(v);
           }

@@ -409,27 +409,70 @@ __device__ __forceinline__ void prep_group_channel(SeamMmaSmem &sm, const Compos
     const int ch = ptid + NPREP * u;
     if (ch >= 128) break;
     const float ll = pick(lam[u], nt - 1);
-    const float sh = fuse ? ll : 0.f;  // operand rows e^{lam_t - sh}
     unsigned char *slab = reinterpret_cast<unsigned char *>(&sm.bt[ch >> 5][0][0]);
     unsigned char *kslab = reinterpret_cast<unsigned char *>(T.ktile) + 2048 * (ch >> 5);
     const int chunk = (ch & 31) >> 2, within = (ch & 3) * 4;
+    if (fuse) {
+      // every channel decays by at least e^{-80} over the group, so the
+      // decay factors split as e^{lam_t - lam_i} = E_t R_i with
+      // E_t = e^{lam_t} <= 1 and R_i = e^{-lam_i} <= e^80: 16 exponentials
+      // per channel instead of one per (t, i) pair, and the Gram partials
+      // become plain products of the scaled rows
+      float E[GW], R[GW];
 #pragma unroll
-    for (int t = 0; t < GW; t++) {
-      const float e = __expf(lam[u][t] - sh);
-      *reinterpret_cast<uint32_t *>(slab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(e * kt[u][t]);
-      *reinterpret_cast<uint32_t *>(slab + (GW + t) * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(e * qt[u][t]);
-      const float kh = __expf(ll - lam[u][t]) * kt[u][t];
-      *reinterpret_cast<uint32_t *>(kslab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(kh);
-      T.khat[ch * GW + t] = kh;
-    }
-    T.elast[ch] = __expf(ll);
+      for (int t = 0; t < GW; t++) {
+        E[t] = __expf(lam[u][t]);
+        R[t] = __expf(-lam[u][t]);
+      }
+      const float El = __expf(ll), Rl = __expf(-ll);
 #pragma unroll
-    for (int t = 0; t < GW; t++) {
+      for (int t = 0; t < GW; t++) {
+        const float e = E[t] * Rl;  // operand rows e^{lam_t - lam_last}
+        *reinterpret_cast<uint32_t *>(slab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(e * kt[u][t]);
+        *reinterpret_cast<uint32_t *>(slab + (GW + t) * 128 + ((chunk ^ t) << 4) + within) =
+            tc::to_tf32(e * qt[u][t]);
+        const float kh = (El * R[t]) * kt[u][t];
+        *reinterpret_cast<uint32_t *>(kslab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(kh);
+        T.khat[ch * GW + t] = kh;
+      }
+      T.elast[ch] = El;
+      // in place: R <- k R, k <- k E, q <- q E
 #pragma unroll
-      for (int i = 0; i <= t; i++) {
-        const float w = __expf(lam[u][t] - lam[u][i]);
-        if (i < t) part[t * (t - 1) / 2 + i] = fmaf(kt[u][t] * kt[u][i], w, part[t * (t - 1) / 2 + i]);
-        part[28 + t * (t + 1) / 2 + i] = fmaf(qt[u][t] * kt[u][i], w, part[28 + t * (t + 1) / 2 + i]);
+      for (int t = 0; t < GW; t++) {
+        R[t] *= kt[u][t];
+        kt[u][t] *= E[t];
+        qt[u][t] *= E[t];
+      }
+#pragma unroll
+      for (int t = 0; t < GW; t++) {
+#pragma unroll
+        for (int i = 0; i <= t; i++) {
+          if (i < t) part[t * (t - 1) / 2 + i] = fmaf(kt[u][t], R[i], part[t * (t - 1) / 2 + i]);
+          part[28 + t * (t + 1) / 2 + i] = fmaf(qt[u][t], R[i], part[28 + t * (t + 1) / 2 + i]);
+        }
+      }
+    } else {
+      // a channel decays below e^{-80} over the group: every factor
+      // formed directly (bounded by 1)
+#pragma unroll
+      for (int t = 0; t < GW; t++) {
+        const float e = __expf(lam[u][t]);
+        *reinterpret_cast<uint32_t *>(slab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(e * kt[u][t]);
+        *reinterpret_cast<uint32_t *>(slab + (GW + t) * 128 + ((chunk ^ t) << 4) + within) =
+            tc::to_tf32(e * qt[u][t]);
+        const float kh = __expf(ll - lam[u][t]) * kt[u][t];
+        *reinterpret_cast<uint32_t *>(kslab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(kh);
+        T.khat[ch * GW + t] = kh;
+      }
+      T.elast[ch] = __expf(ll);
+#pragma unroll
+      for (int t = 0; t < GW; t++) {
+#pragma unroll
+        for (int i = 0; i <= t; i++) {
+          const float w = __expf(lam[u][t] - lam[u][i]);
+          if (i < t) part[t * (t - 1) / 2 + i] = fmaf(kt[u][t] * kt[u][i], w, part[t * (t - 1) / 2 + i]);
+          part[28 + t * (t + 1) / 2 + i] = fmaf(qt[u][t] * kt[u][i], w, part[28 + t * (t + 1) / 2 + i]);
+        }
       }
     }
   }
@@ -534,7 +577,7 @@ __global__ void __launch_bounds__(NT2, 2)
   c.groups = (c.w + GW - 1) / GW;
   const int total_groups = c.n_seg * c.groups;
   const uint32_t total_slabs = 4u * (uint32_t)c.n_seg;
-  const bool has_seam = c.groups > 0;
+  const bool has_seam = c.groups > 0 && c.n_seg > 0;  // no segment: no seam group to wait for
 
   if (tid == 0) {
     for (int i = 0; i < NSLOT; i++) tc::mbar_init(&sm.full[i], 1);
@@ -1048,7 +1091,9 @@ __global__ void __launch_bounds__(NT2, 2)
       // the fast rounding may lose a NaN, so a warp that holds one (rare)
       // forms its rows again with the guarded rounding; reported on every
       // segment, where the non-finite value appears
-      float nf = 0.f;
+      float nfa[8];  // eight short chains (none on the critical path)
+#pragma unroll
+      for (int i = 0; i < 8; i++) nfa[i] = 0.f;
 #pragma unroll
       for (int b = 0; b < 4; b++) {
         uint32_t r[16];
@@ -1061,12 +1106,13 @@ __global__ void __launch_bounds__(NT2, 2)
         for (int j = 0; j < 16; j++) {
           const float x = fmaf(al, __uint_as_float(r[j]), trans ? 0.f : sc[j]);
           if (keep) out[(int64_t)(16 * b + j) * 128] = x;
-          nf = fmaf(x, 0.f, nf);
+          nfa[j & 7] = fmaf(x, 0.f, nfa[j & 7]);
           // per-channel gate, next group fused: TMEM A holds RN(E_last . S)
           r[j] = tc::to_tf32_fast(CH && scale_next ? x * el_next[16 * b + j] : x);
         }
         tc::tmem_st16(tAh + 16 * b, r);
       }
+      const float nf = ((nfa[0] + nfa[1]) + (nfa[2] + nfa[3])) + ((nfa[4] + nfa[5]) + (nfa[6] + nfa[7]));
       if (__any_sync(0xffffffffu, nf != nf)) {  // warp-uniform: the TMEM accesses are .sync.aligned
         bad |= nf != nf;
         tc::tmem_wait_st();

@@ -172,9 +172,11 @@ def test_compose_spans_vs_oracle(variant, w, bounds):
     S_init = si.random_state((2, W.h_v, 128, 128), seed=1, cfg=5, device=DEV)
     S_out = torch.empty((2, W.h_v, 128, 128), device=DEV)
     seam_out = torch.zeros((2, W.n_seg, w, W.h_v, 128), device=DEV) if w else None
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
     hy.compose_spans(slot, T_pool, S_pool, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"], variant=variant,
-                     S_out=S_out, seam_out=seam_out, S_init=S_init, bounds=bounds, h_k=W.h_k)
+                     S_out=S_out, seam_out=seam_out, S_init=S_init, bounds=bounds, h_k=W.h_k, status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0, hy.status_from_word(int(status.item()))
     So, seam = _oracle_compose(W, T_pool, S_pool, sa, slot, S_init, 2)
     assert per_head_rel_err(S_out, So).max() <= TOL_BF16
     if w:
@@ -242,3 +244,20 @@ def test_compose_channel_steep_gates():
     e = per_head_rel_err(seam_out.permute(0, 3, 1, 2, 4).reshape(1, W.h_v, -1),
                          np.transpose(seam, (0, 3, 1, 2, 4)).reshape(1, W.h_v, -1), inner=1)
     assert e.max() <= TOL_BF16, e.max()
+
+
+@pytest.mark.parametrize("variant", ["gdn", "channel", "scalar"])
+def test_compose_of_no_segment_passes_the_state_through(variant):
+    """A chain with no segment (an empty span of a longer prompt) returns
+    S_init unchanged, writes no seam output and reports nothing, seam window
+    or not."""
+    W, T_pool, S_pool, sa, slot = _chains(variant, 8)
+    S_init = si.random_state((2, W.h_v, 128, 128), seed=3, cfg=5, device=DEV)
+    S_out = torch.empty_like(S_init)
+    seam_out = torch.full((2, W.n_seg, 8, W.h_v, 128), 7.0, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hy.compose(slot, T_pool, S_pool, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"], variant=variant, S_out=S_out,
+               seam_out=seam_out, S_init=S_init, h_k=W.h_k, status=status, span=(3, 3))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, hy.status_from_word(int(status.item()))
+    assert torch.equal(S_out, S_init) and torch.all(seam_out == 7.0)
