@@ -562,7 +562,8 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
 // XR <- RN(X_h) (chain 1 reads the start-of-chunk state), X_h <- G_C X_h
 // (the accumulator chain 2 adds onto), in one pass over the half.
 // Recording build: `rec` (non-NULL for the S half) receives the
-// start-of-chunk state, column n of S (this thread's lane) at rec[d * 128].
+// start-of-chunk state, column n of S (this thread's lane), as row n of S^T:
+// rec[d] for d = 0..127, in 16-byte stores.
 template <bool REC>
 __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC, float *rec) {
 #pragma unroll 1
@@ -571,13 +572,17 @@ __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC, f
     tc::tmem_ld32(trow(tm + tx, c0), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
     tc::tmem_ld32(trow(tm + tx, c0 + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
     tc::tmem_wait_ld();
+    if (REC && rec) {
+#pragma unroll
+      for (int e = 0; e < 64; e += 4)
+        *reinterpret_cast<uint4 *>(rec + c0 + e) = make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
+    }
 #pragma unroll
     for (int h = 0; h < 2; h++) {
       uint32_t xr[32];
 #pragma unroll
       for (int j = 0; j < 32; j++) {
         const float v = __uint_as_float(r[32 * h + j]);
-        if (REC && rec) rec[(int64_t)(c0 + 32 * h + j) * 128] = v;
         xr[j] = tc::to_tf32_fast(v);  // X itself keeps any NaN (it is the accumulator)
         r[32 * h + j] = __float_as_uint(gC * v);
       }
@@ -616,7 +621,8 @@ __device__ __forceinline__ void issue_chain2(BuildTcSmem &sm, uint32_t tm, uint3
 // Ytilde = -Y diag(exp(lam_C - lam_t)), split hi + lo, as the K-major A
 // tiles [128 j x 64 t] of chain 2 (the S half's Y already holds -U)
 // Recording build: `rec` (non-NULL for the S half) receives
-// Delta = U - W S_0 = -Y of the chunk, column n, at rec[t * 128].
+// Delta = U - W S_0 = -Y of the chunk, column n, as row n of Delta^T:
+// rec[t] for t = 0..63, in 16-byte stores.
 template <bool REC>
 __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int b3, float *rec) {
 #pragma unroll 1
@@ -626,7 +632,9 @@ __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int
     tc::tmem_wait_ld();
     if (REC && rec) {
 #pragma unroll
-      for (int j = 0; j < 32; j++) rec[(int64_t)(c0 + j) * 128] = -__uint_as_float(r[j]);
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4 *>(rec + c0 + j) = make_float4(-__uint_as_float(r[j]), -__uint_as_float(r[j + 1]),
+                                                                -__uint_as_float(r[j + 2]), -__uint_as_float(r[j + 3]));
     }
 #pragma unroll
     for (int q8 = 0; q8 < 4; q8++) {
@@ -656,8 +664,8 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   float *rec_s = nullptr, *rec_d = nullptr;
   if (REC) {
     const int64_t rc = (int64_t)(x.it.part + ch) * p.h_v + x.it.head;
-    rec_s = p.rec_S + rc * 128 * 128 + n;
-    rec_d = p.rec_D + rc * 64 * 128 + n;
+    rec_s = p.rec_S + rc * 128 * 128 + (int64_t)n * 128;  // S_0^T row n
+    rec_d = p.rec_D + rc * 64 * 128 + (int64_t)n * 64;    // Delta^T row n
   }
   wait_phase(sm, p, &sm.wt_ready, g, LIM);
   // ---- W (tf32, rounded) as chain 1's B tile, once P's W / U MMAs are

@@ -7,7 +7,9 @@
 // and every body token t emits o_t = S_t^T q_t with the post-update state.
 // The recording build (build_tc.cu) leaves, for every 64-token chunk of every
 // (segment, value head), the chunk's start state S_0 and
-// Delta = U - W S_0, the chunk's WY-form state increments.  Inside the
+// Delta = U - W S_0, the chunk's WY-form state increments, both transposed
+// (S_0^T [128 j][128 d], Delta^T [128 j][64 t]) so that every thread moves
+// its own row with 16-byte accesses.  Inside the
 // chunk, with lam_t = sum_{j<=t} g_j from the chunk start and G_t = e^lam_t,
 //     S_t = G_t S_0 + sum_{i<=t} (G_t / G_i) k_i Delta_i^T,
 // so the outputs of the chunk are
@@ -160,28 +162,36 @@ __global__ void __launch_bounds__(NT, 2)
   // thread (j, hf) converts tokens 32 hf .. 32 hf + 31 of column j
   const int64_t rc = (int64_t)it.rec * p.h_v + it.head;
   {
-    const float *S0 = p.rec_S + rc * 128 * 128 + j;
-#pragma unroll 1
-    for (int b = 0; b < 2; b++) {  // 32 rows at a time
-      float x[32];
+    // every load of the thread in flight at once: row j of S_0^T, elements
+    // 64 hf .. 64 hf + 63, and row j of Delta^T, elements 32 hf .. 32 hf + 31
+    const float4 *S0 = reinterpret_cast<const float4 *>(p.rec_S + rc * 128 * 128 + (int64_t)j * 128 + 64 * hf);
+    const float4 *D = reinterpret_cast<const float4 *>(p.rec_D + rc * 64 * 128 + (int64_t)j * 64 + 32 * hf);
+    float4 xs[16], xd[8];
 #pragma unroll
-      for (int e = 0; e < 32; e++) x[e] = S0[(int64_t)(64 * hf + 32 * b + e) * 128];
+    for (int e = 0; e < 16; e++) xs[e] = S0[e];
+#pragma unroll
+    for (int e = 0; e < 8; e++) xd[e] = D[e];
+#pragma unroll
+    for (int b = 0; b < 2; b++) {  // 32 rows d at a time
       uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int e = 0; e < 16; e++) split_bf16x2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+      for (int e = 0; e < 8; e++) {
+        const float4 v = xs[8 * b + e];
+        split_bf16x2(v.x, v.y, hi[2 * e], lo[2 * e]);
+        split_bf16x2(v.z, v.w, hi[2 * e + 1], lo[2 * e + 1]);
+      }
       // column c of the packed operand holds rows 2c, 2c + 1
       tc::tmem_st16(tm + lane_base + TM_S + 32 * hf + 16 * b, hi);
       tc::tmem_st16(tm + lane_base + TM_S + 64 + 32 * hf + 16 * b, lo);
     }
-    const float *D = p.rec_D + rc * 64 * 128 + j;
-    float x[32];
-#pragma unroll
-    for (int e = 0; e < 32; e++) x[e] = D[(int64_t)(32 * hf + e) * 128];
 #pragma unroll
     for (int q8 = 0; q8 < 4; q8++) {
       uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int e = 0; e < 4; e++) split_bf16x2(x[8 * q8 + 2 * e], x[8 * q8 + 2 * e + 1], hw[e], lw[e]);
+      const float4 a = xd[2 * q8], b = xd[2 * q8 + 1];
+      split_bf16x2(a.x, a.y, hw[0], lw[0]);
+      split_bf16x2(a.z, a.w, hw[1], lw[1]);
+      split_bf16x2(b.x, b.y, hw[2], lw[2]);
+      split_bf16x2(b.z, b.w, hw[3], lw[3]);
       const uint32_t off = sw16(j, 32 * hf + 8 * q8, 128);
       *reinterpret_cast<uint4 *>(sm.dth + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *reinterpret_cast<uint4 *>(sm.dtl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
