@@ -445,8 +445,30 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
     sm.bt[q] = b_cur;
     sm.lam[q] = g_cur;
   }
+  tc::fence_proxy_async_smem();  // zeroed tail rows are MMA operands
+  tc::tc_fence_before();
   tc::named_bar(BAR_P, NG);
-  if (wp == 0) {  // lam_t = sum_{j<=t} g_j (two tokens per lane)
+  if (q == 0) {
+    // ---- Gram K K^T (K-major view; padded rows 64..127 are ignored) once X
+    // has read the previous chunk's W out of TM_WG.  That also means the U
+    // MMA of chunk g - 1 is complete (X waits for it first), so V buffer
+    // (g + 1) % 2 is free: the CTA's chunk g + 1 is copied in now, into K
+    // buffer (g + 1) % 3 once X's chain 2 of chunk g - 2 (its last reader) is
+    // complete.  That barrier's next phase is chunk g's, which needs wt_ready
+    // of chunk g, arrived below: the phase waited on is its latest.  The
+    // gate scan below runs on another warp meanwhile.
+    if (g > 0) wait_phase(sm, p, &sm.wg_free, g - 1, LIM);
+    if (iss_pending(sm.iss) && sm.iss.g == g + 1 && !aborted(sm)) {
+      if (g >= 2) wait_phase(sm, p, &sm.bar_x2[(g - 2) & 1], (g - 2) >> 1, LIM);
+      iss_issue(sm, sm.iss, tk, tv);
+    }
+    tc::tc_fence_after();
+    const uint32_t kb = tc::smem_u32(kin);
+#pragma unroll
+    for (int ks = 0; ks < 8; ks++)
+      tc::mma_ss_f16(tm + TM_WG, kdesc16(kb, 16 * ks, 64), kdesc16(kb, 16 * ks, 64), id.gram, ks > 0);
+    tc::mma_commit(&sm.bar_g);
+  } else if (wp == 1) {  // lam_t = sum_{j<=t} g_j (two tokens per lane)
     float x0 = sm.lam[lane], x1 = sm.lam[lane + 32];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -477,29 +499,7 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
       sm.fact = (l0 - lc) <= 80.f;
     }
   }
-  tc::fence_proxy_async_smem();  // zeroed tail rows are MMA operands
-  tc::tc_fence_before();
-  tc::named_bar(BAR_P, NG);
-  // ---- Gram K K^T (K-major view; padded rows 64..127 are ignored) once X
-  // has read the previous chunk's W out of TM_WG.  That also means the U MMA
-  // of chunk g - 1 is complete (X waits for it first), so V buffer
-  // (g + 1) % 2 is free: the CTA's chunk g + 1 is copied in now, into K
-  // buffer (g + 1) % 3 once X's chain 2 of chunk g - 2 (its last reader) is
-  // complete.  That barrier's next phase is chunk g's, which needs wt_ready
-  // of chunk g, arrived below: the phase waited on is its latest.
-  if (q == 0) {
-    if (g > 0) wait_phase(sm, p, &sm.wg_free, g - 1, LIM);
-    if (iss_pending(sm.iss) && sm.iss.g == g + 1 && !aborted(sm)) {
-      if (g >= 2) wait_phase(sm, p, &sm.bar_x2[(g - 2) & 1], (g - 2) >> 1, LIM);
-      iss_issue(sm, sm.iss, tk, tv);
-    }
-    tc::tc_fence_after();
-    const uint32_t kb = tc::smem_u32(kin);
-#pragma unroll
-    for (int ks = 0; ks < 8; ks++)
-      tc::mma_ss_f16(tm + TM_WG, kdesc16(kb, 16 * ks, 64), kdesc16(kb, 16 * ks, 64), id.gram, ks > 0);
-    tc::mma_commit(&sm.bar_g);
-  }
+  tc::named_bar(BAR_P, NG);  // the scan's results
   wait_phase(sm, p, &sm.bar_g, g, DRAIN_LIMIT);
   tc::tc_fence_after();
   // ---- M_ti = b_t exp(lam_t - lam_i) k_t.k_i (i < t): warps holding lanes 0..63
@@ -562,8 +562,8 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
 // XR <- RN(X_h) (chain 1 reads the start-of-chunk state), X_h <- G_C X_h
 // (the accumulator chain 2 adds onto), in one pass over the half.
 // Recording build: `rec` (non-NULL for the S half) receives the
-// start-of-chunk state, column n of S (this thread's lane), as row n of S^T:
-// rec[d] for d = 0..127, in 16-byte stores.
+// start-of-chunk state, column n of S (this thread's lane) at rec[d * 128]
+// (a warp's stores fill whole 128-byte lines).
 template <bool REC>
 __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC, float *rec) {
 #pragma unroll 1
@@ -574,8 +574,7 @@ __device__ __forceinline__ void stage_half(uint32_t tm, uint32_t tx, float gC, f
     tc::tmem_wait_ld();
     if (REC && rec) {
 #pragma unroll
-      for (int e = 0; e < 64; e += 4)
-        *reinterpret_cast<uint4 *>(rec + c0 + e) = make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
+      for (int e = 0; e < 64; e++) rec[(int64_t)(c0 + e) * 128] = __uint_as_float(r[e]);
     }
 #pragma unroll
     for (int h = 0; h < 2; h++) {
@@ -621,8 +620,7 @@ __device__ __forceinline__ void issue_chain2(BuildTcSmem &sm, uint32_t tm, uint3
 // Ytilde = -Y diag(exp(lam_C - lam_t)), split hi + lo, as the K-major A
 // tiles [128 j x 64 t] of chain 2 (the S half's Y already holds -U)
 // Recording build: `rec` (non-NULL for the S half) receives
-// Delta = U - W S_0 = -Y of the chunk, column n, as row n of Delta^T:
-// rec[t] for t = 0..63, in 16-byte stores.
+// Delta = U - W S_0 = -Y of the chunk, column n, at rec[t * 128].
 template <bool REC>
 __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int b3, float *rec) {
 #pragma unroll 1
@@ -632,9 +630,7 @@ __device__ __forceinline__ void split_y(BuildTcSmem &sm, uint32_t tm, int n, int
     tc::tmem_wait_ld();
     if (REC && rec) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4 *>(rec + c0 + j) = make_float4(-__uint_as_float(r[j]), -__uint_as_float(r[j + 1]),
-                                                                -__uint_as_float(r[j + 2]), -__uint_as_float(r[j + 3]));
+      for (int j = 0; j < 32; j++) rec[(int64_t)(c0 + j) * 128] = -__uint_as_float(r[j]);
     }
 #pragma unroll
     for (int q8 = 0; q8 < 4; q8++) {
@@ -664,8 +660,8 @@ __device__ void chain_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx
   float *rec_s = nullptr, *rec_d = nullptr;
   if (REC) {
     const int64_t rc = (int64_t)(x.it.part + ch) * p.h_v + x.it.head;
-    rec_s = p.rec_S + rc * 128 * 128 + (int64_t)n * 128;  // S_0^T row n
-    rec_d = p.rec_D + rc * 64 * 128 + (int64_t)n * 64;    // Delta^T row n
+    rec_s = p.rec_S + rc * 128 * 128 + n;  // S_0 [128 d][128 j], column n
+    rec_d = p.rec_D + rc * 64 * 128 + n;   // Delta [64 t][128 j], column n
   }
   wait_phase(sm, p, &sm.wt_ready, g, LIM);
   // ---- W (tf32, rounded) as chain 1's B tile, once P's W / U MMAs are
