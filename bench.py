@@ -98,12 +98,14 @@ E2E_CHUNKS = 8  # segment groups of the end-to-end build (copies overlap the bui
 KERNEL_SOURCES = {
     "build": ("build_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
     "compose": ("compose_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
+    "compose_channel": ("compose_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
     "channel": ("build_channel.cu", "tc.cuh", "common.cuh", "internal.h"),
     "merge": ("merge.cu", "tc.cuh", "common.cuh", "internal.h"),
     "rerotate": ("rerotate.cu", "tc.cuh", "common.cuh", "internal.h"),
     "forward": ("forward_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
 }
 PROFILE_FILES = {"build": "segment_build_tc__gdn_16x1024.md", "compose": "compose_seam_mma__gdn_4x32x100.md",
+                 "compose_channel": "compose_seam_mma__channel_4x32x100.md",
                  "channel": "segment_build_channel__16x1024.md", "merge": "pair_merge_tc__4x32x50.md",
                  "rerotate": "pair_rerotate__4x100x32.md", "forward": "forward_tc__gdn_16x1024.md"}
 
@@ -516,7 +518,7 @@ def run_profile_case(kind):
     most.  build: GDN, 16 segments x 1024 tokens, h_k = 16, h_v = 32 (512
     (segment, head) pairs); channel: the same shape with per-channel gates;
     compose: 4 GDN layers x 32 heads x 100 segments, w = 8 (12800 pairs,
-    1.7 GB pool); merge: that pool's adjacent segment pairs merged (4 x 50
+    1.7 GB pool); compose_channel: the same with per-channel gates; merge: that pool's adjacent segment pairs merged (4 x 50
     merges x 32 heads); rerotate: that pool re-rotated in place (400 slots x
     32 heads); forward: the build case's forward (its output kernel)."""
     import torch
@@ -564,10 +566,11 @@ def run_profile_case(kind):
                                          T_pool=T, S_pool=S, o_out=o)
         units = W.n_tokens * W.h_v
     else:
-        comp = setup_compose(dev, hy, n_layers=4)
+        var = "channel" if kind == "compose_channel" else "gdn"
+        comp = setup_compose(dev, hy, n_layers=4, variant=var)
         sa = comp["sa"]
         run = lambda: hy.compose(comp["slot"], comp["T_pool"], comp["S_pool"], sa["k"], sa["v"], sa["q"], sa["g"],
-                                 sa["beta"], variant="gdn", S_out=comp["S_out"], seam_out=comp["seam_out"])
+                                 sa["beta"], variant=var, S_out=comp["S_out"], seam_out=comp["seam_out"])
         units = comp["n_layers"] * comp["W"].n_seg * comp["W"].h_v
     for _ in range(3):
         run()
@@ -649,7 +652,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements after the step")
-    ap.add_argument("--profile", choices=["build", "compose", "channel", "merge", "rerotate", "forward"], default=None,
+    ap.add_argument("--profile", choices=["build", "compose", "compose_channel", "channel", "merge", "rerotate", "forward"],
+                    default=None,
                     help="run one small case of one kernel (for an ncu capture) and exit")
     args = ap.parse_args()
     if args.impl == "reference":

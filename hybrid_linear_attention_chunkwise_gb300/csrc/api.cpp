@@ -702,7 +702,12 @@ int hypic_compose_host(const hypic_host_compose_desc *d, hypic_stream_t stream) 
   if (c.n_layers == 0) return HYPIC_OK;
   const ComposeParams base = compose_params(&c);
   const int L = c.n_layers;
-  const int n_ch = std::min(std::min(d->n_chunks, L), kMaxHostChunks);
+  // groups of whole waves: a launch of fewer chains than the GPU holds at
+  // once (two per SM on the tensor-core path) takes as long as a full wave,
+  // so the layers are never split finer than the waves the chains need
+  const int64_t slots = 2 * (int64_t)sm_count();
+  const int waves = (int)std::max<int64_t>(1, ((int64_t)L * c.h_v + slots - 1) / slots);
+  const int n_ch = std::min(std::min(std::min(d->n_chunks, L), waves), kMaxHostChunks);
   const size_t es = (size_t)in_size(c.in_dtype), w = (size_t)c.seam_w;
   const size_t seg_stride = (size_t)base.seg_stride;
   const bool vec = is_vector_gate(c.variant);

@@ -666,6 +666,16 @@ __global__ void __launch_bounds__(NT2, 2)
     else
       prep_group(sm, p, c, gq, pb, pg);
     load_bg(gq + 1);
+    if (CH && gq + 1 < total_groups) {
+      // the next group's per-channel gates (8 tokens x 512 bytes) into L1
+      // now, so that its preparation does not wait on DRAM for them
+      const int ptid = tid - 32 * PREP_WARP0;
+      const SeamGroup sg = seam_group(p, c, gq + 1);
+      if (ptid < 4 * GW && (ptid >> 2) < sg.nt) {
+        const float *a = p.seam_g + ((sg.tok0 + (ptid >> 2)) * p.h_v + c.h) * 128 + 32 * (ptid & 3);
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+      }
+    }
   };
   // after a barrier that follows group gq's recurrence: its raw buffer is
   // free, refill it with group gq + 2 (uniform call; the issuer warp copies)

@@ -338,8 +338,10 @@ int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream);
  * shapes of their device counterparts and are NULL exactly when those are;
  * host_S_out and host_seam_out (NULL when seam_w = 0) receive the results.
  *
- * The layers are split into min(n_chunks, n_layers, 64) groups of
- * consecutive layers.  Per group, the group's seam tokens (and initial
+ * The layers are split into min(n_chunks, n_layers, 64, W) groups of
+ * consecutive layers, W the number of waves the n_layers x h_v chains take
+ * on the device (two chains per SM), so that no group's launch runs a
+ * partial wave for nothing.  Per group, the group's seam tokens (and initial
  * states) are copied in on a copy stream of the library, its compose runs
  * on `stream` once they are in, and its states and seam outputs are copied
  * out on a second copy stream once it is done; so group c's compose

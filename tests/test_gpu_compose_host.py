@@ -30,9 +30,9 @@ def _pinned(t):
     return None if t is None else t.detach().cpu().contiguous().pin_memory()
 
 
-def _prompt(variant, n_layers, w=8):
+def _prompt(variant, n_layers, w=8, h_k=2, h_v=4):
     cfg = 2 if variant == "scalar" else 5
-    W = si.workload(cfg, device=DEV, variant=variant, lengths=[60, 200, 33, 128, 90], h_k=2, h_v=4, seam_w=w,
+    W = si.workload(cfg, device=DEV, variant=variant, lengths=[60, 200, 33, 128, 90], h_k=h_k, h_v=h_v, seam_w=w,
                     n_layers=n_layers)
     pools = [gpu_build(W, layer=l) for l in range(n_layers)]
     T_pool = torch.cat([p[0] for p in pools])
@@ -43,10 +43,12 @@ def _prompt(variant, n_layers, w=8):
 
 
 @pytest.mark.parametrize("variant", ["gdn", "channel", "scalar"])
-@pytest.mark.parametrize("n_chunks,with_init", [(1, False), (3, True), (9, True)])
-def test_compose_host_equals_device_compose(variant, n_chunks, with_init):
-    L = 5
-    W, T_pool, S_pool, sa, slot = _prompt(variant, L)
+@pytest.mark.parametrize("n_chunks,with_init,L,h_v", [(1, False, 5, 4), (3, True, 5, 4), (9, True, 12, 32),
+                                                     (2, False, 12, 32)])
+def test_compose_host_equals_device_compose(variant, n_chunks, with_init, L, h_v):
+    """12 layers x 32 heads (384 chains) take two waves on the device, so the
+    call runs two groups of layers; 5 x 4 chains run as one."""
+    W, T_pool, S_pool, sa, slot = _prompt(variant, L, h_k=h_v // 2, h_v=h_v)
     S_init = si.random_state((L, W.h_v, 128, 128), seed=4, cfg=5, device=DEV) if with_init else None
     keys = ("k", "v", "q", "g", "beta")
     # the device compose
