@@ -242,6 +242,20 @@ __device__ __forceinline__ void gram_mma(const SeamRaw &r, float (&dd)[4]) {
   }
 }
 
+// M = (I + diag(beta) Gk)^{-1} diag(beta), column j, by forward substitution
+// (Gk strictly lower triangular: the decayed key Gram of the group)
+__device__ __forceinline__ void solve_m(GroupConst &G, int j) {
+  float m[GW];
+#pragma unroll
+  for (int t = 0; t < GW; t++) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < t; i++) s = fmaf(G.gk[t][i], (i >= j) ? m[i] : 0.f, s);
+    m[t] = t < j ? 0.f : (t == j ? G.beta[t] : -G.beta[t] * s);
+    G.mm[t][j] = m[t];
+  }
+}
+
 // State-independent preparation of group gq by the NPREP threads of warps
 // PREP_WARP0.. (its raw buffer has landed).  Threads ptid < GW pass beta and
 // the log-gate of the group's token ptid (loaded one group ahead; zero past
@@ -310,19 +324,7 @@ __device__ __forceinline__ void prep_group(SeamMmaSmem &sm, const ComposeParams 
     G.alast = __expf(lam_last);
   }
   tc::named_bar(BAR_PREP, NPREP);
-  // M: thread j < 8 solves column j by forward substitution
-  if (ptid < GW) {
-    const int j = ptid;
-    float m[GW];
-#pragma unroll
-    for (int t = 0; t < GW; t++) {
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < t; i++) s = fmaf(G.gk[t][i], (i >= j) ? m[i] : 0.f, s);
-      m[t] = t < j ? 0.f : (t == j ? G.beta[t] : -G.beta[t] * s);
-      G.mm[t][j] = m[t];
-    }
-  }
+  if (ptid < GW) solve_m(G, ptid);
   tc::fence_proxy_async_smem();  // the operand tile is read by the tensor cores
 }
 
@@ -356,12 +358,61 @@ __device__ __forceinline__ ChTiles ch_tiles(SeamMmaSmem &sm) {
 //   T_C S_n = T_C (E_last . S0) + sum_i (T_C k-hat_i) c_i^T,
 // k-hat_i = e^{lam_last - lam_i} . k_i, one more operand tile.  Otherwise the
 // rows are E_t . k_t and E_t . q_t and the register path updates the exact
-// state with k-hat and E_last.  The Grams take a per-channel weight, summed
-// over the channels directly (2 channels per thread, then a warp tree and the
-// three warps, in a fixed order).  Flags for the kernel: alast = 1 (fused) or
-// 0, ea = 1, eb = 1.
+// state with k-hat and E_last.  The Grams take a per-channel weight: for a
+// fused group the two operand tiles already carry it (one warp multiplies
+// them, gram_tiles_tf32), otherwise it is formed per (t, i) pair and summed
+// over the channels on the CUDA cores.  The gates gl are loaded by the caller
+// (load_gates_channel).  Flags for the kernel: alast = 1 (fused) or 0, ea =
+// 1, eb = 1.
+// per-channel log-gates of group gq for the channels of preparing thread
+// ptid (ptid and ptid + NPREP), zero past the group and past the prompt;
+// issued ahead of prep_group_channel so that their latency overlaps other work
+__device__ __forceinline__ void load_gates_channel(const ComposeParams &p, const Chain &c, int gq, int total_groups,
+                                                   float (&gl)[2][GW]) {
+  const int ptid = threadIdx.x - 32 * PREP_WARP0;
+  const bool any = gq < total_groups;
+  const SeamGroup sg = seam_group(p, c, any ? gq : 0);
+#pragma unroll
+  for (int u = 0; u < 2; u++) {
+    const int ch = ptid + NPREP * u;
+#pragma unroll
+    for (int t = 0; t < GW; t++)
+      gl[u][t] = any && ch < 128 && t < sg.nt ? p.seam_g[((sg.tok0 + t) * p.h_v + c.h) * 128 + ch] : 0.f;
+  }
+}
+
+// Decayed Grams of a fused group from its two operand tiles, on the legacy
+// warp MMA (one warp, 16 x m16n8k8 tf32): row t of the [K;Q] tile holds
+// e^{lam_t - lam_last} . k_t (rows 8..15: . q_t) and row i of the T_C k-hat
+// tile e^{lam_last - lam_i} . k_i, so their channel sums are the decayed
+// products of the unrolled recurrence, at the tf32 precision of the other
+// operands of the group.  Lane (g = lane/4, u = lane%4) receives D[g][2u],
+// D[g][2u+1], D[g+8][2u], D[g+8][2u+1].
+__device__ __forceinline__ void gram_tiles_tf32(const float *bt, const float *kt, float (&dd)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, u = lane & 3;
+  const uint32_t *A = reinterpret_cast<const uint32_t *>(bt);
+  const uint32_t *B = reinterpret_cast<const uint32_t *>(kt);
+  dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
+#pragma unroll
+  for (int s = 0; s < 16; s++) {
+    // channels 8s + u and 8s + u + 4: slab s/4, 16-byte chunks 2(s%4) and
+    // 2(s%4) + 1 (swizzled by the row), word u
+    const int slab = (s >> 2) * 512, c0 = 2 * (s & 3);
+    const int w0 = ((c0 ^ g) << 2) + u, w1 = (((c0 + 1) ^ g) << 2) + u;
+    const uint32_t a0 = A[slab + g * 32 + w0], a1 = A[slab + (g + 8) * 32 + w0];
+    const uint32_t a2 = A[slab + g * 32 + w1], a3 = A[slab + (g + 8) * 32 + w1];
+    const uint32_t b0 = B[slab + g * 32 + w0], b1 = B[slab + g * 32 + w1];
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(dd[0]), "+f"(dd[1]), "+f"(dd[2]), "+f"(dd[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
 __device__ __forceinline__ void prep_group_channel(SeamMmaSmem &sm, const ComposeParams &p, const Chain &c, int gq,
-                                                   float b_n) {
+                                                   float b_n, const float (&gl)[2][GW]) {
   const int ptid = threadIdx.x - 32 * PREP_WARP0;
   const SeamGroup sg = seam_group(p, c, gq);
   const int nt = sg.nt;
@@ -384,7 +435,7 @@ __device__ __forceinline__ void prep_group_channel(SeamMmaSmem &sm, const Compos
 #pragma unroll
     for (int t = 0; t < GW; t++) {
       const bool in = ch < 128 && t < nt;
-      acc += in ? p.seam_g[((sg.tok0 + t) * p.h_v + c.h) * 128 + ch] : 0.f;
+      acc += gl[u][t];  // zero past nt
       lam[u][t] = acc;
       kt[u][t] = in ? __bfloat162float(r.k[t][ch]) : 0.f;
       qt[u][t] = in ? __bfloat162float(r.q[t][ch]) : 0.f;
@@ -400,60 +451,59 @@ __device__ __forceinline__ void prep_group_channel(SeamMmaSmem &sm, const Compos
   const bool fuse = c.groups == 1 && pair_slot(p, c, gq / c.groups) >= 0 &&
                     fminf(fminf(T.red[192], T.red[193]), T.red[194]) >= -80.f;
   if (ptid == 0) G.alast = fuse ? 1.f : 0.f;
-  // pass 2: tiles and Gram partials
-  float part[64];
+  if (fuse) {
+    // pass 2, fused: every channel decays by at least e^{-80} over the
+    // group, so the decay factors split as e^{lam_t - lam_i} = E_t R_i with
+    // E_t = e^{lam_t} <= 1 and R_i = e^{-lam_i} <= e^80: 16 exponentials
+    // per channel, and the two operand tiles carry every decay the Grams need
 #pragma unroll
-  for (int j = 0; j < 64; j++) part[j] = 0.f;
-#pragma unroll
-  for (int u = 0; u < 2; u++) {
-    const int ch = ptid + NPREP * u;
-    if (ch >= 128) break;
-    const float ll = pick(lam[u], nt - 1);
-    unsigned char *slab = reinterpret_cast<unsigned char *>(&sm.bt[ch >> 5][0][0]);
-    unsigned char *kslab = reinterpret_cast<unsigned char *>(T.ktile) + 2048 * (ch >> 5);
-    const int chunk = (ch & 31) >> 2, within = (ch & 3) * 4;
-    if (fuse) {
-      // every channel decays by at least e^{-80} over the group, so the
-      // decay factors split as e^{lam_t - lam_i} = E_t R_i with
-      // E_t = e^{lam_t} <= 1 and R_i = e^{-lam_i} <= e^80: 16 exponentials
-      // per channel instead of one per (t, i) pair, and the Gram partials
-      // become plain products of the scaled rows
-      float E[GW], R[GW];
-#pragma unroll
-      for (int t = 0; t < GW; t++) {
-        E[t] = __expf(lam[u][t]);
-        R[t] = __expf(-lam[u][t]);
-      }
+    for (int u = 0; u < 2; u++) {
+      const int ch = ptid + NPREP * u;
+      if (ch >= 128) break;
+      const float ll = pick(lam[u], nt - 1);
+      unsigned char *slab = reinterpret_cast<unsigned char *>(&sm.bt[ch >> 5][0][0]);
+      unsigned char *kslab = reinterpret_cast<unsigned char *>(T.ktile) + 2048 * (ch >> 5);
+      const int chunk = (ch & 31) >> 2, within = (ch & 3) * 4;
       const float El = __expf(ll), Rl = __expf(-ll);
 #pragma unroll
       for (int t = 0; t < GW; t++) {
-        const float e = E[t] * Rl;  // operand rows e^{lam_t - lam_last}
+        const float e = __expf(lam[u][t]) * Rl;  // operand rows e^{lam_t - lam_last}
         *reinterpret_cast<uint32_t *>(slab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(e * kt[u][t]);
         *reinterpret_cast<uint32_t *>(slab + (GW + t) * 128 + ((chunk ^ t) << 4) + within) =
             tc::to_tf32(e * qt[u][t]);
-        const float kh = (El * R[t]) * kt[u][t];
+        const float kh = (El * __expf(-lam[u][t])) * kt[u][t];  // k-hat_t
         *reinterpret_cast<uint32_t *>(kslab + t * 128 + ((chunk ^ t) << 4) + within) = tc::to_tf32(kh);
-        T.khat[ch * GW + t] = kh;
       }
       T.elast[ch] = El;
-      // in place: R <- k R, k <- k E, q <- q E
+    }
+    tc::named_bar(BAR_PREP, NPREP);  // both tiles are complete
+    if (wp == 0) {
+      float dd[4];
+      gram_tiles_tf32(&sm.bt[0][0][0], T.ktile, dd);
+      const int t = lane >> 2;
 #pragma unroll
-      for (int t = 0; t < GW; t++) {
-        R[t] *= kt[u][t];
-        kt[u][t] *= E[t];
-        qt[u][t] *= E[t];
+      for (int j = 0; j < 2; j++) {
+        const int i = 2 * (lane & 3) + j;
+        const bool in = t < nt && i < nt;
+        G.gk[t][i] = (in && i < t) ? dd[j] : 0.f;
+        G.gq[t][i] = (in && i <= t) ? dd[2 + j] : 0.f;
       }
+      __syncwarp();
+      if (lane < GW) solve_m(G, lane);
+    }
+  } else {
+    // pass 2, a channel decays below e^{-80} over the group: every factor
+    // formed directly (bounded by 1), k-hat kept for the register path, and
+    // the Grams summed over the channels on the CUDA cores (2 channels per
+    // thread, then a warp tree and the three warps, in a fixed order)
 #pragma unroll
-      for (int t = 0; t < GW; t++) {
-#pragma unroll
-        for (int i = 0; i <= t; i++) {
-          if (i < t) part[t * (t - 1) / 2 + i] = fmaf(kt[u][t], R[i], part[t * (t - 1) / 2 + i]);
-          part[28 + t * (t + 1) / 2 + i] = fmaf(qt[u][t], R[i], part[28 + t * (t + 1) / 2 + i]);
-        }
-      }
-    } else {
-      // a channel decays below e^{-80} over the group: every factor
-      // formed directly (bounded by 1)
+    for (int u = 0; u < 2; u++) {
+      const int ch = ptid + NPREP * u;
+      if (ch >= 128) break;
+      const float ll = pick(lam[u], nt - 1);
+      unsigned char *slab = reinterpret_cast<unsigned char *>(&sm.bt[ch >> 5][0][0]);
+      unsigned char *kslab = reinterpret_cast<unsigned char *>(T.ktile) + 2048 * (ch >> 5);
+      const int chunk = (ch & 31) >> 2, within = (ch & 3) * 4;
 #pragma unroll
       for (int t = 0; t < GW; t++) {
         const float e = __expf(lam[u][t]);
@@ -465,61 +515,64 @@ __device__ __forceinline__ void prep_group_channel(SeamMmaSmem &sm, const Compos
         T.khat[ch * GW + t] = kh;
       }
       T.elast[ch] = __expf(ll);
+    }
+    // the 64 Gram partials (gk: t(t-1)/2 + i, i < t; gq: 28 + t(t+1)/2 + i,
+    // i <= t) in four rounds of 16, each summed over the warp by a
+    // reduce-scatter: at the level with lane offset o a lane keeps the half
+    // of its values selected by (lane & o) and adds its partner's copy of
+    // that half; after the levels 16, 8, 4, 2 and a last exchange with lane
+    // offset 1, lane l holds the warp sum of partial (l / 2) % 16 of the round
 #pragma unroll
-      for (int t = 0; t < GW; t++) {
+    for (int rd = 0; rd < 4; rd++) {
+      float part[16];
 #pragma unroll
-        for (int i = 0; i <= t; i++) {
-          const float w = __expf(lam[u][t] - lam[u][i]);
-          if (i < t) part[t * (t - 1) / 2 + i] = fmaf(kt[u][t] * kt[u][i], w, part[t * (t - 1) / 2 + i]);
-          part[28 + t * (t + 1) / 2 + i] = fmaf(qt[u][t] * kt[u][i], w, part[28 + t * (t + 1) / 2 + i]);
+      for (int j = 0; j < 16; j++) part[j] = 0.f;
+#pragma unroll
+      for (int u = 0; u < 2; u++) {
+        if (ptid + NPREP * u >= 128) break;
+#pragma unroll
+        for (int t = 0; t < GW; t++) {
+#pragma unroll
+          for (int i = 0; i <= t; i++) {
+            const int jk = t * (t - 1) / 2 + i - 16 * rd, jq = 28 + t * (t + 1) / 2 + i - 16 * rd;
+            const bool ink = i < t && jk >= 0 && jk < 16, inq = jq >= 0 && jq < 16;
+            if (!ink && !inq) continue;
+            const float w = __expf(lam[u][t] - lam[u][i]);
+            if (ink) part[jk] = fmaf(kt[u][t] * kt[u][i], w, part[jk]);
+            if (inq) part[jq] = fmaf(qt[u][t] * kt[u][i], w, part[jq]);
+          }
         }
       }
-    }
-  }
-  // warp sum of the 64 partials as a reduce-scatter: at the level with lane
-  // offset o each lane keeps the half of its values selected by (lane & o)
-  // and adds its partner's copy of that half, so five levels leave lane l
-  // the sums of partials 2l and 2l + 1 (62 shuffles instead of 320)
 #pragma unroll
-  for (int o = 16, n = 32; o > 0; o >>= 1, n >>= 1) {
-    const bool up = (lane & o) != 0;
+      for (int o = 16, n = 8; o > 1; o >>= 1, n >>= 1) {
+        const bool up = (lane & o) != 0;
 #pragma unroll
-    for (int j = 0; j < n; j++) {
-      const float keep = up ? part[n + j] : part[j];
-      const float send = up ? part[j] : part[n + j];
-      part[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        for (int j = 0; j < n; j++) {
+          const float keep = up ? part[n + j] : part[j];
+          const float send = up ? part[j] : part[n + j];
+          part[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      part[0] += __shfl_xor_sync(0xffffffffu, part[0], 1);
+      if ((lane & 1) == 0) T.red[wp * 64 + 16 * rd + ((lane >> 1) & 15)] = part[0];
     }
-  }
-  T.red[wp * 64 + 2 * lane] = part[0];
-  T.red[wp * 64 + 2 * lane + 1] = part[1];
-  tc::named_bar(BAR_PREP, NPREP);
-  if (ptid < 64) {
-    const float v = (T.red[ptid] + T.red[64 + ptid]) + T.red[128 + ptid];
-    if (ptid < 28) {
-      const int j = ptid;
-      int t = 1;
-      while (t * (t + 1) / 2 <= j) t++;  // t(t-1)/2 <= j < t(t+1)/2
-      G.gk[t][j - t * (t - 1) / 2] = v;
-    } else {
-      const int j = ptid - 28;
-      int t = 0;
-      while ((t + 1) * (t + 2) / 2 <= j) t++;  // t(t+1)/2 <= j < (t+1)(t+2)/2
-      G.gq[t][j - t * (t + 1) / 2] = v;
+    tc::named_bar(BAR_PREP, NPREP);
+    if (ptid < 64) {
+      const float v = (T.red[ptid] + T.red[64 + ptid]) + T.red[128 + ptid];
+      if (ptid < 28) {
+        const int j = ptid;
+        int t = 1;
+        while (t * (t + 1) / 2 <= j) t++;  // t(t-1)/2 <= j < t(t+1)/2
+        G.gk[t][j - t * (t - 1) / 2] = v;
+      } else {
+        const int j = ptid - 28;
+        int t = 0;
+        while ((t + 1) * (t + 2) / 2 <= j) t++;  // t(t+1)/2 <= j < (t+1)(t+2)/2
+        G.gq[t][j - t * (t + 1) / 2] = v;
+      }
     }
-  }
-  tc::named_bar(BAR_PREP, NPREP);
-  // M: thread j < 8 solves column j by forward substitution
-  if (ptid < GW) {
-    const int j = ptid;
-    float m[GW];
-#pragma unroll
-    for (int t = 0; t < GW; t++) {
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < t; i++) s = fmaf(G.gk[t][i], (i >= j) ? m[i] : 0.f, s);
-      m[t] = t < j ? 0.f : (t == j ? G.beta[t] : -G.beta[t] * s);
-      G.mm[t][j] = m[t];
-    }
+    tc::named_bar(BAR_PREP, NPREP);
+    if (ptid < GW) solve_m(G, ptid);
   }
   tc::fence_proxy_async_smem();  // the operand tiles are read by the tensor cores
 }
@@ -644,6 +697,8 @@ __global__ void __launch_bounds__(NT2, 2)
   bool refill_pending = false;  // thread 0: the last pair's slots await the next slabs
   const int ptid = tid - 32 * PREP_WARP0;
   float pb = 0.f, pg = 0.f;  // preparing threads ptid < GW: beta / log-gate of token ptid of the next group
+  float gl[2][GW];           // per-channel gate: the preparing thread's gates of group gl_for
+  int gl_for = -1;
 
   auto load_bg = [&](int gq) {
     pb = 0.f;
@@ -661,21 +716,12 @@ __global__ void __launch_bounds__(NT2, 2)
   auto prepare = [&](int gq) {
     const bool ok = !aborted(sm) && tc::mbar_wait(&sm.raw_full[gq & 1], (gq >> 1) & 1, LIM);
     if (!ok) fail(sm, p);
-    if (CH)
-      prep_group_channel(sm, p, c, gq, pb);
-    else
+    if (CH) {
+      if (gl_for != gq) load_gates_channel(p, c, gq, total_groups, gl);
+      prep_group_channel(sm, p, c, gq, pb, gl);
+    } else
       prep_group(sm, p, c, gq, pb, pg);
     load_bg(gq + 1);
-    if (CH && gq + 1 < total_groups) {
-      // the next group's per-channel gates (8 tokens x 512 bytes) into L1
-      // now, so that its preparation does not wait on DRAM for them
-      const int ptid = tid - 32 * PREP_WARP0;
-      const SeamGroup sg = seam_group(p, c, gq + 1);
-      if (ptid < 4 * GW && (ptid >> 2) < sg.nt) {
-        const float *a = p.seam_g + ((sg.tok0 + (ptid >> 2)) * p.h_v + c.h) * 128 + 32 * (ptid & 3);
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
-      }
-    }
   };
   // after a barrier that follows group gq's recurrence: its raw buffer is
   // free, refill it with group gq + 2 (uniform call; the issuer warp copies)
@@ -974,6 +1020,12 @@ __global__ void __launch_bounds__(NT2, 2)
       al = sm.gc[gq & 1].alast;
       const uint32_t fph = nfused & 1;
       nfused++;
+      if (CH && preper && !last) {
+        // the gates of the group that opens the next segment, in flight
+        // while these warps issue and read the products below
+        load_gates_channel(p, c, gq_next, total_groups, gl);
+        gl_for = gq_next;
+      }
       if (slab_issuer) {
         // lane 0 of warps 4..7, one K-slab a each (the issue of one MMA takes
         // tens of cycles, so four threads issue the 32 small products in a
@@ -1046,8 +1098,9 @@ __global__ void __launch_bounds__(NT2, 2)
         if (!aborted(sm)) {
           seam_recurrence(d, gq, cc);
           const GroupConst &G = sm.gc[gq & 1];
+          const float inv_al = 1.f / al;  // one division, not one per token
 #pragma unroll
-          for (int i = 0; i < GW; i++) cc[i] *= G.eb[i] / al;  // e^{-lam_i} c_i
+          for (int i = 0; i < GW; i++) cc[i] *= G.eb[i] * inv_al;  // e^{-lam_i} c_i
         } else {
 #pragma unroll
           for (int i = 0; i < GW; i++) cc[i] = 0.f;
