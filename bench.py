@@ -322,21 +322,22 @@ def rerotate_row(dev, hy, peaks, comp):
 def compose_variant_rows(dev, hy, peaks, n_layers=8):
     """The compose of the other dense-transition variants on the warm-prompt
     shape (8 layers x 32 heads x 100 segments, w = 8): DeltaNet (tensor-core
-    seam) and the per-channel gate (token-by-token seam)."""
+    seam) and the per-channel gate (tensor-core seam with per-channel
+    operand tiles); the kernel named is the one the path query reports."""
     import torch
     rows = {}
     for var, gate in (("deltanet", 0), ("channel", 128)):
         comp = setup_compose(dev, hy, n_layers=n_layers, variant=var)
         W, sa = comp["W"], comp["sa"]
-        ms = _time_ms(lambda: hy.compose(comp["slot"], comp["T_pool"], comp["S_pool"], sa["k"], sa["v"], sa["q"],
-                                         sa["g"], sa["beta"], variant=var, S_out=comp["S_out"],
-                                         seam_out=comp["seam_out"]))
+        args = (comp["slot"], comp["T_pool"], comp["S_pool"], sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"])
+        ms = _time_ms(lambda: hy.compose(*args, variant=var, S_out=comp["S_out"], seam_out=comp["seam_out"]))
+        path = hy.compose_path(*args, variant=var, S_out=comp["S_out"], seam_out=comp["seam_out"])
         nbytes = compose_bytes(n_layers, W.n_seg, W.seam_w, W.h_k, W.h_v, W.d_k, W.d_v, gate_floats=gate)
         gbs = nbytes / (ms * 1e-3) / 1e9
         rows[f"compose: {var}, {n_layers} layers x {W.h_v} heads x {W.n_seg} segments, w={W.seam_w}"] = {
             "ms": ms, "algorithmic_bytes": nbytes,
             "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"]},
-            "kernel": "tensor-core compose, " + ("tensor-core seam" if var == "deltanet" else "token seam")}
+            "kernel": path}
         del comp, sa
         torch.cuda.empty_cache()
     return rows
