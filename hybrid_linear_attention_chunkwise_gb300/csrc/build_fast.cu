@@ -9,8 +9,9 @@
 //     S(C|0) = sum_t (w_t . k_t) v_t^T,   w_t = prod_{j > t} a_j
 // (gamma^(L-1-t) for the scalar decay, 1 when ungated) -- one GEMM over the
 // body's tokens.  The body is walked backwards in chunks of 64 tokens, so
-// each weight is a running suffix product of the gates (no overflow: every
-// weight is <= 1), and D = S^T accumulates in TMEM:
+// each per-channel weight is a running suffix product of the gates (no
+// overflow: every weight is <= 1; the scalar decay's weight is formed in
+// closed form, once per token), and D = S^T accumulates in TMEM:
 //     D[j][c] += sum_t V[t][j] (w_t[c] k_t[c])     (kind::f16, A = the V
 // tile, B = the weighted K tile, both MN-major views of [token x channel]
 // tiles; the weighted keys are split hi + lo in bf16, ~2^-17; ungated
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(NT, 2)
     if (tid == 0 && !aborted(sm))
       for (int r = 0; r < 2 && r < n_ch; r++) issue(r);
 
-    float s_log = 0.f;  // log of the weight of the token just before the chunk walked so far (channel tid)
+    float s_log = 0.f;  // per-channel gate: log of the weight of the token just before the chunk walked so far (channel tid)
     for (int r = 0; r < n_ch; r++) {
       const int ch = n_ch - 1 - r;
       const int64_t t0 = it.start + (int64_t)C * ch;
@@ -157,20 +158,55 @@ __global__ void __launch_bounds__(NT, 2)
         tc::tc_fence_after();
         if (tid == 0 && r + 1 < n_ch && !aborted(sm)) issue(r + 1);
       }
-      if (weighted) {
-        // w_t = exp(sum of the gates after t), walking the chunk backwards
+      if (scalar) {
+        // w_t = gamma^(end - 1 - t) in closed form (one exponential per
+        // token, shared by its channels): thread tid forms 8 vectors of 8
+        // channels, tokens t = v / 16, with 16-byte loads and stores
+#pragma unroll 2
+        for (int m = 0; m < 8; m++) {
+          const int v = tid + NT * m, t = v >> 4, c8 = (v & 15) << 3;
+          const uint32_t off = tile_off(t, c8);
+          const float w = t < nt ? __expf((float)(it.end - 1 - (t0 + t)) * g_scalar) : 0.f;
+          const uint4 kw = *reinterpret_cast<const uint4 *>(sm.kin[b] + off);
+          const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            const float k0 = __uint_as_float(kk[j] << 16) * w, k1 = __uint_as_float(kk[j] & 0xFFFF0000u) * w;
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(k0, k1);
+            hi[j] = *reinterpret_cast<const uint32_t *>(&h2);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(k0 - __uint_as_float(hi[j] << 16),
+                                                            k1 - __uint_as_float(hi[j] & 0xFFFF0000u));
+            lo[j] = *reinterpret_cast<const uint32_t *>(&l2);
+          }
+          *reinterpret_cast<uint4 *>(sm.kh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4 *>(sm.kl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      } else if (diag) {
+        // w_t = exp(sum of the gates after t) per channel, walking the chunk
+        // backwards in blocks of 16 tokens: the block's keys are loaded
+        // before any of its weighted keys is stored (the loads do not wait
+        // behind the stores)
         const unsigned char *kt = sm.kin[b];
 #pragma unroll
-        for (int t = C - 1; t >= 0; t--) {
-          float k = 0.f;
-          if (t < nt) {
-            k = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kt + tile_off(t, tid))) * __expf(s_log);
-            s_log += diag ? gl[t] : g_scalar;
+        for (int t1 = C; t1 > 0; t1 -= 16) {
+          float kv[16];
+#pragma unroll
+          for (int j = 0; j < 16; j++)
+            kv[j] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(kt + tile_off(t1 - 1 - j, tid)));
+#pragma unroll
+          for (int j = 0; j < 16; j++) {
+            const int t = t1 - 1 - j;
+            float k = 0.f;
+            if (t < nt) {
+              k = kv[j] * __expf(s_log);
+              s_log += gl[t];
+            }
+            const __nv_bfloat16 hi = __float2bfloat16_rn(k);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(k - __bfloat162float(hi));
+            *reinterpret_cast<__nv_bfloat16 *>(sm.kh + tile_off(t, tid)) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(sm.kl + tile_off(t, tid)) = lo;
           }
-          const __nv_bfloat16 hi = __float2bfloat16_rn(k);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(k - __bfloat162float(hi));
-          *reinterpret_cast<__nv_bfloat16 *>(sm.kh + tile_off(t, tid)) = hi;
-          *reinterpret_cast<__nv_bfloat16 *>(sm.kl + tile_off(t, tid)) = lo;
         }
       } else if (nt < C) {
         // ragged chunk, ungated: zero the key rows past the body
