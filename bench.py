@@ -766,19 +766,25 @@ def main():
                + sum(x.numel() * x.element_size() for x in pin4.values()))
         d2h = hT.numel() * 4 + hS.numel() * 4 + hS4.numel() * 4 + ho4.numel() * 4
 
+        side = torch.cuda.Stream()
+
         def e2e_step():
-            # two C-ABI calls: host inputs in, host pairs out, the copies of
-            # one group of segments overlapping the build of the next; then
-            # host seam tokens in, host states and seam outputs out, the
-            # copies of one group of layers overlapping the next's compose
+            # two C-ABI calls, on two streams (the cold prompt's build and the
+            # warm prompt's compose are independent): host inputs in, host
+            # pairs out, the copies of one group of segments overlapping the
+            # build of the next; and host seam tokens in, host states and
+            # seam outputs out, the copies of one group of layers overlapping
+            # the next's compose.  The step ends when both have.
+            side.wait_stream(stream)
             hy.segment_build_host(pin["k"], pin["v"], pin["g"], pin["beta"], W3.seg_offsets, variant="gdn",
                                   seam_w=W3.seam_w, k=dk["k"], v=dk["v"], g=dk["g"], beta=dk["beta"],
                                   T_pool=T3, S_pool=S3, T_host=hT, S_host=hS, n_chunks=E2E_CHUNKS,
-                                  workspace=ws3)
+                                  workspace=ws3, stream=stream)
             hy.compose_host(*(pin4[n] for n in keys), comp["slot"], comp["T_pool"], comp["S_pool"], variant="gdn",
                             seam_k=st4["k"], seam_v=st4["v"], seam_q=st4["q"], seam_g=st4["g"], seam_beta=st4["beta"],
                             S_out=comp["S_out"], S_out_host=hS4, seam_out=comp["seam_out"], seam_out_host=ho4,
-                            n_chunks=E2E_CHUNKS)
+                            n_chunks=E2E_CHUNKS, stream=side)
+            stream.wait_stream(side)
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
@@ -792,11 +798,13 @@ def main():
         e_ms = e0.elapsed_time(e1) / args.steps
         e2e = {"value": ws * W3.n_tokens / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-               "what": "the whole step from host buffers: hypic_segment_build_host (H2D of the layer's "
+               "what": "the whole step from host buffers, two C-ABI calls on two streams: "
+                       "hypic_segment_build_host (H2D of the layer's "
                        f"k/v/g/beta from pinned memory, build, D2H of all pairs, {E2E_CHUNKS} overlapped groups of "
-                       "segments), then hypic_compose_host (H2D of the warm prompt's seam tokens, compose against "
-                       f"the resident pool, D2H of the final states and seam outputs, {E2E_CHUNKS} overlapped "
-                       "groups of layers)"}
+                       "segments) and hypic_compose_host (H2D of the warm prompt's seam tokens, compose against "
+                       "the resident pool, D2H of the final states and seam outputs, overlapped groups of "
+                       "layers); the host link moves about 210 GB/s one way and 300 GB/s both ways on this "
+                       "GB300, so the step's copies alone take about 6.6 ms"}
 
     # the other build rows, each against its own roofline (after the timed
     # region; not part of the step)

@@ -544,26 +544,44 @@ MergeParams merge_params(const hypic_merge_desc *d) {
 }
 }  // namespace
 
-// ---- the host-buffer build: copy streams and events per device, created on
-// first use and kept for the life of the process.  An event may be recorded
-// again while earlier waits on it are pending: a wait takes the record that
-// precedes it.
+// ---- the host-buffer calls: copy streams and events per (device, caller
+// stream), created on first use and kept for the life of the process, so
+// that host-buffer calls on different streams overlap their copies.  Past
+// kPipesPerDevice caller streams, the first pipe is shared (still correct,
+// without the overlap).  An event may be recorded again while earlier waits
+// on it are pending: a wait takes the record that precedes it.
 namespace {
 constexpr int kMaxHostChunks = 64;
 constexpr int kMaxDevices = 64;
+constexpr int kPipesPerDevice = 8;
 struct HostPipe {
   bool ready = false;
+  bool used = false;
+  cudaStream_t owner = nullptr;  // the caller stream this pipe serves
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t start = nullptr, fin = nullptr;
   cudaEvent_t in_done[kMaxHostChunks] = {}, built[kMaxHostChunks] = {};
 };
 std::mutex g_host_mu;
-HostPipe g_pipes[kMaxDevices];
+HostPipe g_pipes[kMaxDevices][kPipesPerDevice];
 
-int host_pipe(HostPipe *&hp) {
+int host_pipe(HostPipe *&hp, cudaStream_t owner) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HYPIC_ERR_CUDA;
-  hp = &g_pipes[dev];
+  hp = &g_pipes[dev][0];
+  for (int i = 0; i < kPipesPerDevice; i++) {
+    HostPipe &c = g_pipes[dev][i];
+    if (c.used && c.owner == owner) {
+      hp = &c;
+      break;
+    }
+    if (!c.used) {
+      c.used = true;
+      c.owner = owner;
+      hp = &c;
+      break;
+    }
+  }
   if (hp->ready) return HYPIC_OK;
   auto ev = [](cudaEvent_t *e) { return *e || cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
   if (!hp->in && cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking) != cudaSuccess) return HYPIC_ERR_CUDA;
@@ -623,9 +641,9 @@ int hypic_segment_build_host(const hypic_host_build_desc *d, hypic_stream_t stre
   const size_t T_slot = (size_t)T_slot_floats(b) * 4, S_slot = (size_t)b.h_v * b.d_k * b.d_v * 4;
 
   std::lock_guard<std::mutex> lock(g_host_mu);
-  HostPipe *hp = nullptr;
-  if ((st = host_pipe(hp))) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  HostPipe *hp = nullptr;
+  if ((st = host_pipe(hp, s))) return st;
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
   auto h2d = [&](const void *dst, const void *src, size_t n) {
     return n == 0 || ok(cudaMemcpyAsync(const_cast<void *>(dst), src, n, cudaMemcpyHostToDevice, hp->in));
@@ -718,9 +736,9 @@ int hypic_compose_host(const hypic_host_compose_desc *d, hypic_stream_t stream) 
   const size_t s_l = (size_t)c.h_v * c.d_k * c.d_v * 4;
 
   std::lock_guard<std::mutex> lock(g_host_mu);
-  HostPipe *hp = nullptr;
-  if ((st = host_pipe(hp))) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  HostPipe *hp = nullptr;
+  if ((st = host_pipe(hp, s))) return st;
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
   auto at = [](const void *base_, size_t bytes) { return static_cast<const char *>(base_) + bytes; };
   auto h2d = [&](const void *dst, const void *src, size_t n) {

@@ -31,8 +31,8 @@
  *     memory read during the call only.  The library allocates no device
  *     memory.  Two entry points keep process-wide state and serialise their
  *     host calls with a lock: hypic_segment_build_host and
- *     hypic_compose_host (copy streams and events per device, created on
- *     first use) and
+ *     hypic_compose_host (copy streams and events per device and caller
+ *     stream, created on first use) and
  *     hypic_segment_build_noalloc (a fixed device array); see each.  Every
  *     other entry point keeps no global mutable state and is thread-safe.
  *   - Work is enqueued asynchronously on the caller's stream.  Host-side
@@ -241,8 +241,10 @@ int hypic_segment_forward(const hypic_forward_desc *d, hypic_stream_t stream);
  *
  * Returns a hypic_status.  Every argument is checked before anything is
  * enqueued; a CUDA error while enqueuing returns HYPIC_ERR_CUDA with the
- * outputs undefined.  Host calls are serialised by a lock (the copy streams
- * and their events are shared per device).
+ * outputs undefined.  Host calls are serialised by a lock.  The copy streams
+ * and their events belong to the caller's stream (up to eight caller streams
+ * per device; beyond that they are shared), so host-buffer calls on
+ * different streams overlap their copies and kernels.
  */
 typedef struct {
   hypic_build_desc build;
@@ -349,8 +351,9 @@ int hypic_compose(const hypic_compose_desc *d, hypic_stream_t stream);
  * after the work already on `stream`, and `stream` waits for the last copy
  * out: the host arrays are complete once `stream` is synchronised.  Overlap
  * needs page-locked host arrays.  Returns a hypic_status; every argument is
- * checked first.  Host calls are serialised by a lock (the copy streams and
- * events are shared per device with hypic_segment_build_host).
+ * checked first.  Host calls are serialised by a lock; the copy streams and
+ * events belong to the caller's stream, as for hypic_segment_build_host (a
+ * build and a compose from host buffers on two streams overlap).
  */
 typedef struct {
   hypic_compose_desc compose;

@@ -115,3 +115,50 @@ def test_build_with_no_tokens(variant):
                           n_chunks=3)
     torch.cuda.synchronize()
     assert torch.equal(hT, want_T) and torch.equal(hS, torch.zeros(S.shape))
+
+
+def test_host_build_and_host_compose_on_two_streams():
+    """A host-buffer build and a host-buffer compose enqueued on two streams
+    (each caller stream gets its own copy streams, so they overlap) give the
+    device calls' results bit for bit; repeated, the pipes are reused."""
+    lens = [40, 130, 12, 64, 300, 5, 77, 200]
+    W = si.workload(5, device=DEV, variant="gdn", lengths=lens, h_k=2, h_v=4, seam_w=8, n_layers=3)
+    L = W.layers[0]
+    hk, hv, hg, hb = (_pinned(getattr(L, n)) for n in ("k", "v", "g", "beta"))
+    T_ref, S_ref = gpu_build(W)
+    # a compose over the three layers' pools
+    from gpu_common import seam_arrays
+    pools = [gpu_build(W, layer=l) for l in range(3)]
+    T_pool = torch.cat([p[0] for p in pools])
+    S_pool = torch.cat([p[1] for p in pools])
+    sa = seam_arrays(W, range(3))
+    keys = ("k", "v", "q", "g", "beta")
+    slot = torch.arange(3 * W.n_seg, dtype=torch.int32, device=DEV).reshape(3, W.n_seg)
+    So_ref = torch.empty((3, W.h_v, 128, 128), device=DEV)
+    oo_ref = torch.empty((3, W.n_seg, W.seam_w, W.h_v, 128), device=DEV)
+    hy.compose(slot, T_pool, S_pool, *(sa[k] for k in keys), variant="gdn", S_out=So_ref, seam_out=oo_ref, h_k=W.h_k)
+    torch.cuda.synchronize()
+    host4 = {k: _pinned(sa[k]) for k in keys}
+    sA, sB = torch.cuda.Stream(), torch.cuda.Stream()
+    for rep in range(2):
+        T, S = new_pools("gdn", W.n_seg, W.h_v, 128, 128, DEV)
+        hT = torch.full(T.shape, 7.0).pin_memory()
+        hS = torch.full(S.shape, 7.0).pin_memory()
+        st = {k: torch.zeros_like(sa[k]) for k in keys}
+        So = torch.empty_like(So_ref)
+        oo = torch.empty_like(oo_ref)
+        hSo = torch.full(So.shape, float("nan")).pin_memory()
+        hoo = torch.full(oo.shape, float("nan")).pin_memory()
+        stage = [torch.zeros_like(x) for x in (L.k, L.v, L.g, L.beta)]
+        sA.wait_stream(torch.cuda.current_stream())  # the buffers above are filled on the current stream
+        sB.wait_stream(torch.cuda.current_stream())
+        hy.segment_build_host(hk, hv, hg, hb, W.seg_offsets, variant="gdn", seam_w=W.seam_w, k=stage[0], v=stage[1],
+                              g=stage[2], beta=stage[3], T_pool=T, S_pool=S, T_host=hT, S_host=hS, n_chunks=3,
+                              stream=sA)
+        hy.compose_host(*(host4[k] for k in keys), slot, T_pool, S_pool, variant="gdn", seam_k=st["k"],
+                        seam_v=st["v"], seam_q=st["q"], seam_g=st["g"], seam_beta=st["beta"], S_out=So,
+                        S_out_host=hSo, seam_out=oo, seam_out_host=hoo, n_chunks=3, h_k=W.h_k, stream=sB)
+        sA.synchronize()
+        sB.synchronize()
+        assert torch.equal(hT, T_ref.cpu()) and torch.equal(hS, S_ref.cpu()), rep
+        assert torch.equal(hSo, So_ref.cpu()) and torch.equal(hoo, oo_ref.cpu()), rep
