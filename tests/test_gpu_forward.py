@@ -92,7 +92,7 @@ def test_forward_gdn_layer_sampled():
     assert eT <= tol_for(torch.bfloat16) and eS <= tol_for(torch.bfloat16)
 
 
-@pytest.mark.parametrize("variant", ["gdn", "deltanet", "scalar"])
+@pytest.mark.parametrize("variant", ["gdn", "gdn_f32", "deltanet", "scalar"])
 @pytest.mark.parametrize("gate", ["steep", "underflow"])
 def test_forward_steep_gates_token_by_token(variant, gate):
     """Scalar gates keep the state as A * X with the scale folded into X
@@ -101,10 +101,14 @@ def test_forward_steep_gates_token_by_token(variant, gate):
     clear the state.  Every body token's output is checked on its own,
     relative to the larger of its own norm and the head's RMS output norm, so
     a slip at one token (e.g. just after a fold) fails.  DeltaNet has no gate
-    and must be unaffected."""
+    and must be unaffected.  bf16 GDN runs the tensor-core outputs, fp32 GDN
+    and the scalar decay the fp32 token recurrence whose state folds the
+    scale."""
     lens = [70, 200, 33, 129]
+    dtype = torch.float32 if variant == "gdn_f32" else torch.bfloat16
+    variant = "gdn" if variant == "gdn_f32" else variant
     W = si.workload(2 if variant == "scalar" else 5, device=DEV, variant=variant, lengths=lens, h_k=2, h_v=4,
-                    seam_w=4)
+                    seam_w=4, dtype=dtype)
     L = W.layers[0]
     gen = torch.Generator(device="cpu").manual_seed(7)
     if variant == "gdn":
@@ -117,7 +121,7 @@ def test_forward_steep_gates_token_by_token(variant, gate):
         L.g.fill_(-200.0 if gate == "underflow" else -20.0)
     T, S, o = _forward(W)
     oc = o.cpu().double().numpy()
-    tol = tol_for(torch.bfloat16)
+    tol = tol_for(dtype)
     for i in range(W.n_seg):
         s0, e, ref = _body_outputs_ref(W, i)
         if ref is None:
