@@ -103,11 +103,13 @@ KERNEL_SOURCES = {
     "merge": ("merge.cu", "tc.cuh", "common.cuh", "internal.h"),
     "rerotate": ("rerotate.cu", "tc.cuh", "common.cuh", "internal.h"),
     "forward": ("forward_tc.cu", "tc.cuh", "common.cuh", "internal.h"),
+    "fast": ("build_fast.cu", "tc.cuh", "common.cuh", "internal.h"),
 }
 PROFILE_FILES = {"build": "segment_build_tc__gdn_16x1024.md", "compose": "compose_seam_mma__gdn_4x32x100.md",
                  "compose_channel": "compose_seam_mma__channel_4x32x100.md",
                  "channel": "segment_build_channel__16x1024.md", "merge": "pair_merge_tc__4x32x50.md",
-                 "rerotate": "pair_rerotate__4x100x32.md", "forward": "forward_tc__gdn_16x1024.md"}
+                 "rerotate": "pair_rerotate__4x100x32.md", "forward": "forward_tc__gdn_16x1024.md",
+                 "fast": "build_fast__retnet_8x16x8192.md"}
 
 
 def source_hash(kind):
@@ -521,7 +523,9 @@ def run_profile_case(kind):
     compose: 4 GDN layers x 32 heads x 100 segments, w = 8 (12800 pairs,
     1.7 GB pool); compose_channel: the same with per-channel gates; merge: that pool's adjacent segment pairs merged (4 x 50
     merges x 32 heads); rerotate: that pool re-rotated in place (400 slots x
-    32 heads); forward: the build case's forward (its output kernel)."""
+    32 heads); forward: the build case's forward (its output kernel); fast:
+    the RetNet fast path, 8 heads x 16 segments x 8192 tokens (128 items,
+    0.5 GB of keys and values)."""
     import torch
     import hybrid_linear_attention_chunkwise_gb300 as hy
     import synth_inputs as si
@@ -535,6 +539,15 @@ def run_profile_case(kind):
         S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
         ws = hy.alloc_workspace(hy.build_workspace_bytes(W.n_seg, W.h_k, W.h_v, W.d_k, W.d_v), dev)
         run = lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=var, seam_w=W.seam_w,
+                                       T_pool=T, S_pool=S, workspace=ws)
+        units = W.n_seg * W.h_v
+    elif kind == "fast":
+        W = si.workload(2, seed=0, device=dev, seg_len=8192)
+        L = W.layers[0]
+        T = torch.empty(hy.pool_T_shape(W.variant, W.n_seg, W.h_v, W.d_k), device=dev)
+        S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
+        ws = hy.alloc_workspace(hy.build_workspace_bytes(W.n_seg, W.h_k, W.h_v, W.d_k, W.d_v), dev)
+        run = lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=W.variant, seam_w=W.seam_w,
                                        T_pool=T, S_pool=S, workspace=ws)
         units = W.n_seg * W.h_v
     elif kind == "merge":
@@ -653,7 +666,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements after the step")
-    ap.add_argument("--profile", choices=["build", "compose", "compose_channel", "channel", "merge", "rerotate", "forward"],
+    ap.add_argument("--profile", choices=["build", "compose", "compose_channel", "channel", "merge", "rerotate", "forward",
+                                          "fast"],
                     default=None,
                     help="run one small case of one kernel (for an ncu capture) and exit")
     args = ap.parse_args()
