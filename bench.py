@@ -406,14 +406,18 @@ def measure_rows(dev, hy, peaks):
         L = W.layers[0]
         T = torch.empty(hy.pool_T_shape(W.variant, W.n_seg, W.h_v, W.d_k), device=dev)
         S = torch.empty((W.n_seg, W.h_v, W.d_k, W.d_v), device=dev)
+        # the workspace once, as the timed step does (a small build is
+        # otherwise timed partly on the host's per-call allocation)
+        ws = hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=W.variant, seam_w=W.seam_w,
+                              T_pool=T, S_pool=S)
         ms = _time_ms(lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=W.variant,
-                                               seam_w=W.seam_w, T_pool=T, S_pool=S))
+                                               seam_w=W.seam_w, T_pool=T, S_pool=S, workspace=ws))
         if round_robin:
             # the same kernel and items, handed to the SMs round-robin in
             # segment order instead of longest-first (pages §2.3: LPT against
             # round-robin balancing of uneven segments)
             ms_rr = _time_ms(lambda: hy.segment_build(L.k, L.v, L.g, L.beta, W.seg_offsets, variant=W.variant,
-                                                      seam_w=W.seam_w, T_pool=T, S_pool=S,
+                                                      seam_w=W.seam_w, T_pool=T, S_pool=S, workspace=ws,
                                                       flags=hy.FLAG_ROUND_ROBIN))
         bodies = np.maximum(np.diff(W.seg_offsets) - W.seam_w, 0)
         in_b = 2 if W.dtype == torch.bfloat16 else 4
@@ -434,7 +438,7 @@ def measure_rows(dev, hy, peaks):
         if round_robin:
             r["lpt_vs_round_robin"] = {"lpt_ms": ms, "round_robin_ms": ms_rr, "speedup": ms_rr / ms}
         rows[name] = r
-        del L, T, S
+        del L, T, S, ws
 
     one("build: RetNet scalar decay, 8 heads, 16 x 512 tokens", si.workload(2, seed=0, device=dev))
     rows["forward: GDN layer 64 x 1024 tokens, pairs + body outputs"] = forward_row(dev, hy, peaks)
