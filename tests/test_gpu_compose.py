@@ -261,3 +261,27 @@ def test_compose_of_no_segment_passes_the_state_through(variant):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, hy.status_from_word(int(status.item()))
     assert torch.equal(S_out, S_init) and torch.all(seam_out == 7.0)
+
+
+def test_compose_widest_heads_on_the_tensor_cores():
+    """128 value heads (the widest the tensor-core compose takes) against the
+    oracle; 132 heads run the fp32 kernel, as the path query says."""
+    for h_v, want in ((128, "tc_compose"), (132, "f32_compose")):
+        W = si.workload(5, device=DEV, variant="gdn", lengths=[40, 90, 30], h_k=h_v // 4, h_v=h_v, seam_w=8,
+                        n_layers=1)
+        S_init = si.random_state((1, W.h_v, 128, 128), seed=2, cfg=5, device=DEV)
+        pools = [gpu_build(W, layer=0)]
+        T_pool, S_pool = pools[0]
+        sa = seam_arrays(W, range(1))
+        slot = torch.arange(W.n_seg, dtype=torch.int32, device=DEV).reshape(1, W.n_seg)
+        args = (slot, T_pool, S_pool, sa["k"], sa["v"], sa["q"], sa["g"], sa["beta"])
+        S_out = torch.empty((1, W.h_v, 128, 128), device=DEV)
+        seam_out = torch.zeros((1, W.n_seg, 8, W.h_v, 128), device=DEV)
+        assert hy.compose_path(*args, variant="gdn", S_out=S_out, seam_out=seam_out, S_init=S_init) == want
+        hy.compose(*args, variant="gdn", S_out=S_out, seam_out=seam_out, S_init=S_init)
+        torch.cuda.synchronize()
+        So, seam = _oracle_compose(W, T_pool, S_pool, sa, slot, S_init, 1)
+        assert per_head_rel_err(S_out, So).max() <= TOL_BF16, h_v
+        e = per_head_rel_err(seam_out.permute(0, 3, 1, 2, 4).reshape(1, W.h_v, -1),
+                             np.transpose(seam, (0, 3, 1, 2, 4)).reshape(1, W.h_v, -1), inner=1)
+        assert e.max() <= TOL_BF16, (h_v, e.max())
