@@ -512,17 +512,26 @@ __device__ void prep_chunk(BuildChSmem &sm, const BuildParams &p, const ItemCtx 
     wait_phase(sm, p, &sm.ys_done, g - 1, LIM);
     wait_phase(sm, p, &sm.wg_free, g - 1, LIM);  // X has read the previous W out of TM_W
   }
-  if (q == 0) {
+  if (q == 0 || q == 32) {
+    // two issuers (lane 0 of the first two warps), one accumulator each: W
+    // into TM_W, -U into TM_Y; X waits for both commits and both arrivals
     tc::tc_fence_after();
-    const uint32_t gh = tc::smem_u32(sm.kgh), gl = tc::smem_u32(sm.kgl), vb = tc::smem_u32(sm.vin[bk]);
     const uint32_t fh = tc::smem_u32(sm.fh), fl = tc::smem_u32(sm.fl);
+    if (q == 0) {
+      const uint32_t gh = tc::smem_u32(sm.kgh), gl = tc::smem_u32(sm.kgl);
 #pragma unroll
-    for (int ks = 0; ks < 2; ks++) {
-      tc::mma_ss_f16(tm + TM_W, mndesc(gh, 16 * ks), kdesc16(fh, 16 * ks, C), id.wu, ks > 0);
-      tc::mma_ss_f16(tm + TM_W, mndesc(gh, 16 * ks), kdesc16(fl, 16 * ks, C), id.wu, 1u);
-      tc::mma_ss_f16(tm + TM_W, mndesc(gl, 16 * ks), kdesc16(fh, 16 * ks, C), id.wu, 1u);
-      tc::mma_ss_f16(tm + TM_Y, mndesc(vb, 16 * ks), kdesc16(fh, 16 * ks, C), id.wu_neg, ks > 0);
-      tc::mma_ss_f16(tm + TM_Y, mndesc(vb, 16 * ks), kdesc16(fl, 16 * ks, C), id.wu_neg, 1u);
+      for (int ks = 0; ks < 2; ks++) {
+        tc::mma_ss_f16(tm + TM_W, mndesc(gh, 16 * ks), kdesc16(fh, 16 * ks, C), id.wu, ks > 0);
+        tc::mma_ss_f16(tm + TM_W, mndesc(gh, 16 * ks), kdesc16(fl, 16 * ks, C), id.wu, 1u);
+        tc::mma_ss_f16(tm + TM_W, mndesc(gl, 16 * ks), kdesc16(fh, 16 * ks, C), id.wu, 1u);
+      }
+    } else {
+      const uint32_t vb = tc::smem_u32(sm.vin[bk]);
+#pragma unroll
+      for (int ks = 0; ks < 2; ks++) {
+        tc::mma_ss_f16(tm + TM_Y, mndesc(vb, 16 * ks), kdesc16(fh, 16 * ks, C), id.wu_neg, ks > 0);
+        tc::mma_ss_f16(tm + TM_Y, mndesc(vb, 16 * ks), kdesc16(fl, 16 * ks, C), id.wu_neg, 1u);
+      }
     }
     tc::mma_commit(&sm.bar_wu);
     tc::mbar_arrive(&sm.wt_ready);  // hand chunk g to X
@@ -686,13 +695,13 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (n == 0) {
     for (int b = 0; b < 2; b++) tc::mbar_init(&sm.full[b], 1);
-    tc::mbar_init(&sm.bar_wu, 1);
+    tc::mbar_init(&sm.bar_wu, 2);
     tc::mbar_init(&sm.bar_y1, 1);
     tc::mbar_init(&sm.bar_y2, 1);
     tc::mbar_init(&sm.bar_x1, 1);
     tc::mbar_init(&sm.bar_x2[0], 1);
     tc::mbar_init(&sm.bar_x2[1], 1);
-    tc::mbar_init(&sm.wt_ready, 1);
+    tc::mbar_init(&sm.wt_ready, 2);
     tc::mbar_init(&sm.ys_done, 1);
     tc::mbar_init(&sm.wg_free, 1);
     tc::mbar_init(&sm.never, 1);

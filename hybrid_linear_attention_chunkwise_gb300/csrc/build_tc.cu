@@ -539,17 +539,26 @@ __device__ void prep_chunk(BuildTcSmem &sm, const BuildParams &p, const ItemCtx 
   // into the chain-1 accumulator once X has consumed the previous chunk's
   // chain-1 output
   if (g > 0) wait_phase(sm, p, &sm.ys_done, g - 1, LIM);
-  if (q == 0) {
+  if (q == 0 || q == 32) {
+    // two issuers (lane 0 of the first two warps), one accumulator each: W
+    // into TM_WG, -U into TM_Y; X waits for both commits and both arrivals
     tc::tc_fence_after();
-    const uint32_t kb = tc::smem_u32(kin), vb = tc::smem_u32(vin);
-    const uint32_t wh = tc::smem_u32(sm.bwh), wl = tc::smem_u32(sm.bwl);
-    const uint32_t uh = tc::smem_u32(sm.buh), ul = tc::smem_u32(sm.bul);
+    if (q == 0) {
+      const uint32_t kb = tc::smem_u32(kin);
+      const uint32_t wh = tc::smem_u32(sm.bwh), wl = tc::smem_u32(sm.bwl);
 #pragma unroll
-    for (int ks = 0; ks < 4; ks++) {
-      tc::mma_ss_f16(tm + TM_WG, mndesc16(kb, 16 * ks), kdesc16(wh, 16 * ks, 64), id.wu, ks > 0);
-      tc::mma_ss_f16(tm + TM_WG, mndesc16(kb, 16 * ks), kdesc16(wl, 16 * ks, 64), id.wu, 1u);
-      tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(uh, 16 * ks, 64), id.wu_neg, ks > 0);
-      tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(ul, 16 * ks, 64), id.wu_neg, 1u);
+      for (int ks = 0; ks < 4; ks++) {
+        tc::mma_ss_f16(tm + TM_WG, mndesc16(kb, 16 * ks), kdesc16(wh, 16 * ks, 64), id.wu, ks > 0);
+        tc::mma_ss_f16(tm + TM_WG, mndesc16(kb, 16 * ks), kdesc16(wl, 16 * ks, 64), id.wu, 1u);
+      }
+    } else {
+      const uint32_t vb = tc::smem_u32(vin);
+      const uint32_t uh = tc::smem_u32(sm.buh), ul = tc::smem_u32(sm.bul);
+#pragma unroll
+      for (int ks = 0; ks < 4; ks++) {
+        tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(uh, 16 * ks, 64), id.wu_neg, ks > 0);
+        tc::mma_ss_f16(tm + TM_Y, mndesc16(vb, 16 * ks), kdesc16(ul, 16 * ks, 64), id.wu_neg, 1u);
+      }
     }
     tc::mma_commit(&sm.bar_wu);
     tc::mbar_arrive(&sm.wt_ready);  // hand chunk g to X
@@ -737,13 +746,13 @@ __global__ void __launch_bounds__(NT, 1)
   if (n == 0) {
     for (int b = 0; b < NBUF; b++) tc::mbar_init(&sm.full[b], 1);
     tc::mbar_init(&sm.bar_g, 1);
-    tc::mbar_init(&sm.bar_wu, 1);
+    tc::mbar_init(&sm.bar_wu, 2);
     tc::mbar_init(&sm.bar_y1, 1);
     tc::mbar_init(&sm.bar_y2, 1);
     tc::mbar_init(&sm.bar_x1, 1);
     tc::mbar_init(&sm.bar_x2[0], 1);
     tc::mbar_init(&sm.bar_x2[1], 1);
-    tc::mbar_init(&sm.wt_ready, 1);
+    tc::mbar_init(&sm.wt_ready, 2);
     tc::mbar_init(&sm.ys_done, 1);
     tc::mbar_init(&sm.wg_free, 1);
     tc::mbar_init(&sm.never, 1);
