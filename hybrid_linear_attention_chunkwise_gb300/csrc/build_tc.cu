@@ -269,6 +269,19 @@ __device__ __forceinline__ void store_neg_t(const Acc3 &c, float *Ao, int g, int
     Ao[(8 * nt + 2 * u + 1) * 68 + g + 8] = -v[3];
   }
 }
+// c = X^T: write X (the same sums frag_acc would split)
+__device__ __forceinline__ void store_t(const Acc3 &c, float *Ao, int g, int u) {
+#pragma unroll
+  for (int nt = 0; nt < 2; nt++) {
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) v[e] = c.d[0][nt][e] + (c.d[1][nt][e] + c.d[2][nt][e]);
+    Ao[(8 * nt + 2 * u) * 68 + g] = v[0];
+    Ao[(8 * nt + 2 * u + 1) * 68 + g] = v[1];
+    Ao[(8 * nt + 2 * u) * 68 + g + 8] = v[2];
+    Ao[(8 * nt + 2 * u + 1) * 68 + g + 8] = v[3];
+  }
+}
 __device__ __forceinline__ const float *nblk(const BuildTcSmem &sm, int i, int j) { return &sm.nm[16 * i][16 * j]; }
 __device__ __forceinline__ float *ablk(BuildTcSmem &sm, int i, int j) { return &sm.am[16 * i][16 * j]; }
 
@@ -279,11 +292,14 @@ __device__ __forceinline__ float *ablk(BuildTcSmem &sm, int i, int j) { return &
 //   1. the diagonal blocks by forward substitution (one thread per column);
 //   2. the lower-left block of each 32 x 32 half, A_10 and A_32:
 //        A_ij = -A_ii (N_ij A_jj);
-//   3. the lower-left 32 x 32 quarter, one warp per block (i, j), i in
-//      {2, 3}, j in {0, 1}:
-//        P_aj = sum_{k=j}^{1} N_ak A_kj,   A_ij = -sum_{a=2}^{i} A_ia P_aj.
-// Stages 2 and 3 run on the legacy warp MMA in transposed form (each
-// product's accumulator is the next one's A operand), operands split
+//   3. the lower-left 32 x 32 quarter in two steps of one warp per block
+//      (a or i in {2, 3}, j in {0, 1}):
+//        P_aj = sum_{k=j}^{1} N_ak A_kj   (into the unused block (j, a) of nm),
+//        A_ij = -sum_{a=2}^{i} A_ia P_aj.
+//      Each warp's chain is two block products per step instead of six
+//      when every warp formed the P blocks it needs itself.
+// Stages 2 and 3 run on the legacy warp MMA in transposed form (in stage 2
+// each product's accumulator is the next one's A operand), operands split
 // hi + lo.  Called by the 128 threads of the P group; ends with a group
 // barrier.
 __device__ void ut_inverse(BuildTcSmem &sm, int q) {
@@ -318,18 +334,23 @@ __device__ void ut_inverse(BuildTcSmem &sm, int q) {
     store_neg_t(ac, ablk(sm, i, j), g, u);
   }
   tc::named_bar(BAR_P, NG);
+  {  // P_aj = sum_{k=j}^{1} N_ak A_kj into the unused block (j, a) of nm
+    const int a = 2 + (wp & 1), j = wp >> 1;
+    Acc3 pc;
+    acc_zero(pc);
+    for (int k = j; k < 2; k++) {
+      frag_t(ablk(sm, k, j), 68, g, u, ah, al);
+      acc_mma(pc, ah, al, nblk(sm, a, k), 68, g, u);
+    }
+    store_t(pc, &sm.nm[16 * j][16 * a], g, u);
+  }
+  tc::named_bar(BAR_P, NG);
   {
     const int i = 2 + (wp & 1), j = wp >> 1;
     Acc3 ac;
     acc_zero(ac);
     for (int a = 2; a <= i; a++) {
-      Acc3 pc;  // P_aj^T = sum_k (N_ak A_kj)^T
-      acc_zero(pc);
-      for (int k = j; k < 2; k++) {
-        frag_t(ablk(sm, k, j), 68, g, u, ah, al);
-        acc_mma(pc, ah, al, nblk(sm, a, k), 68, g, u);
-      }
-      frag_acc(pc, ah, al);
+      frag_t(&sm.nm[16 * j][16 * a], 68, g, u, ah, al);
       acc_mma(ac, ah, al, ablk(sm, i, a), 68, g, u);  // += (A_ia P_aj)^T
     }
     store_neg_t(ac, ablk(sm, i, j), g, u);
