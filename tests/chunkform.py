@@ -143,3 +143,37 @@ def gram_subblocks(Kc, lam, sb=16):
         R = Kc[:b1] * torch.exp(ref - lam[:b1])
         M[b0:b1, :b1] = Q @ R.T
     return torch.tril(M, -1)
+
+
+def block_inverse(N, b=16):
+    """A = (I + N)^{-1} for a strictly lower N, by the block schedule of the
+    tensor-core build's preparation group (blocks of `b`, four of them for a
+    64-token chunk, two for a 32-token one):
+      1. the diagonal blocks by forward substitution;
+      2. A_10 = -A_11 N_10 A_00 and A_32 = -A_33 N_32 A_22;
+      3. with the leading half done, P_aj = sum_{k=j}^{1} N_ak A_kj for
+         a in {2, 3}, j in {0, 1}, then A_ij = -sum_{a=2}^{i} A_ia P_aj.
+    Blocks above the block diagonal are never read (they start as NaN here,
+    so a read of one shows in the result)."""
+    m = N.shape[0]
+    nb = m // b
+    assert nb * b == m and nb in (2, 4)
+    A = torch.full((m, m), float("nan"), dtype=N.dtype)
+    blk = lambda X, i, j: X[b * i:b * (i + 1), b * j:b * (j + 1)]
+    for d in range(nb):  # stage 1: column by column, row by row
+        Nd = blk(N, d, d)
+        Ad = torch.zeros(b, b, dtype=N.dtype)
+        for col in range(b):
+            Ad[col, col] = 1.0
+            for r in range(col + 1, b):
+                Ad[r, col] = -(Nd[r, :r] * Ad[:r, col]).sum()
+        blk(A, d, d)[:] = Ad
+    for h in range(nb // 2):  # stage 2
+        i, j = 2 * h + 1, 2 * h
+        blk(A, i, j)[:] = -blk(A, i, i) @ (blk(N, i, j) @ blk(A, j, j))
+    if nb == 4:  # stage 3
+        P = {(a, j): sum(blk(N, a, k) @ blk(A, k, j) for k in range(j, 2)) for a in (2, 3) for j in (0, 1)}
+        for i in (2, 3):
+            for j in (0, 1):
+                blk(A, i, j)[:] = -sum(blk(A, i, a) @ P[(a, j)] for a in range(2, i + 1))
+    return torch.tril(A)

@@ -36,3 +36,22 @@ def test_subblock_gram_equals_direct(m, sb):
     direct = torch.tril(torch.einsum("tc,ic,tic->ti", K, K, E), -1)
     got = gram_subblocks(K, lam, sb)
     assert torch.allclose(got, direct, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("m", [32, 64])
+def test_block_inverse_schedule(m):
+    """The preparation group's block schedule for A = (I + N)^{-1} (the
+    diagonal blocks, then A_10 and A_32, then the P blocks and the lower-left
+    quarter) equals the inverse, and reads no block above the diagonal."""
+    import torch
+    from chunkform import block_inverse
+    gen = torch.Generator().manual_seed(11)
+    K = torch.nn.functional.normalize(torch.randn(m, 128, generator=gen, dtype=torch.float64), dim=1)
+    beta = torch.sigmoid(torch.randn(m, generator=gen, dtype=torch.float64))
+    lam = torch.cumsum(-torch.rand(m, generator=gen, dtype=torch.float64) * 0.1, 0)
+    N = torch.tril(beta[:, None] * torch.exp(lam[:, None] - lam[None, :]) * (K @ K.T), -1)
+    A = block_inverse(N)
+    assert not torch.isnan(A).any()
+    eye = torch.eye(m, dtype=torch.float64)
+    assert torch.allclose(A, torch.linalg.inv(eye + N), rtol=1e-12, atol=1e-12)
+    assert torch.allclose((eye + N) @ A, eye, atol=1e-12)
