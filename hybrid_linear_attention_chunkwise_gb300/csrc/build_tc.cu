@@ -30,8 +30,7 @@
 //                                                 diagonal blocks SIMT, the rest
 //                                                 on the legacy warp MMA
 //       W, U   W^T = K^T (A diag(bG))^T,  U^T = V^T (A diag(b))^T
-//                                                 kind::f16, factors split hi + lo,
-//                                                 W and U issued by two threads
+//                                                 kind::f16, factors split hi + lo
 //       (U goes straight to the chain-1 accumulator as -U^T);
 //   X (warps 0-3) advances both halves through chunk c, S half first
 //       W        staged from TMEM as chain 1's B operand (tf32, rounded)
